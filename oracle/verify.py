@@ -223,6 +223,10 @@ def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
     # Exact chain rejection sampling [AReno Phase 2]: accept x_j with
     # probability min(1, p_j(x_j) / q_j(x_j)), written without a division as
     # u_j * q_j(x_j) < p_j(x_j) with u_j uniform in (0, 1).
+    # READING: every draft token is validated, reached or not; an
+    # out-of-range draft is rejected when the chain reaches it.
+    if any(not (0 <= int(x) < V) for x in drafts_r[:k]):
+        flags |= F_BAD_TOKEN
     a = k
     accept, margin_accept = [], []
     for j in range(k):
@@ -230,7 +234,6 @@ def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
         if 0 <= x < V:
             px, qx = targets[j].p[x], q_r[j][x]
         else:
-            flags |= F_BAD_TOKEN   # READING: an out-of-range draft is rejected
             px, qx = 0.0, 0.0
         u = philox.accept_uniform(seed, row, j)
         acc = bool(u * qx < px)

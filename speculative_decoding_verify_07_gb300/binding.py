@@ -1,0 +1,231 @@
+"""ctypes binding of libspecverify.so (argument marshalling only).
+
+Every function here checks tensor devices, dtypes and shapes, then calls the C
+ABI declared in include/spec_verify.h with raw device pointers and the current
+CUDA stream.  All computation happens in the library's CUDA kernels; there is
+no CPU or PyTorch fallback.  Importing this module raises if the library has
+not been built (see ``speculative_decoding_verify_07_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libspecverify.so")
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+
+SPEC_OK = 0
+SPEC_E_NULL = -1
+SPEC_E_DIM = -2
+SPEC_E_DTYPE = -3
+SPEC_E_ALIGN = -4
+SPEC_E_WORKSPACE = -5
+SPEC_E_CUDA = -6
+SPEC_E_ARCH = -7
+
+F_MARGIN_ACCEPT = 1
+F_MARGIN_DRAW = 2
+F_MARGIN_TOPP = 4
+F_NAN = 8
+F_BAD_TOKEN = 16
+F_BAD_PARAM = 32
+F_RESIDUAL_EMPTY = 64
+F_BAD_IDX = 128
+
+SPEC_MAX_V = 524288
+SPEC_MAX_K = 16
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing; build it with "
+            "`python -m speculative_decoding_verify_07_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    lib.spec_verify_workspace_size.argtypes = [i32, i32, i32]
+    lib.spec_verify_workspace_size.restype = sz
+    lib.spec_verify.argtypes = [vp, i32, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_verify.restype = i32
+    lib.spec_commit.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
+    lib.spec_commit.restype = i32
+    lib.spec_philox4x32_10.argtypes = [vp, u64, vp, ctypes.c_int64, vp]
+    lib.spec_philox4x32_10.restype = i32
+    lib.spec_status_string.argtypes = [i32]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    lib.spec_version.argtypes = []
+    lib.spec_version.restype = i32
+    return lib
+
+
+LIB = _load()
+LIB_PATH = _LIB_PATH
+
+
+def status_string(code: int) -> str:
+    return LIB.spec_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(LIB.spec_version())
+
+
+def workspace_size(B: int, k: int, V: int) -> int:
+    return int(LIB.spec_verify_workspace_size(int(B), int(k), int(V)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_params(temperature, top_k, top_p, device) -> torch.Tensor:
+    """Pack per-row (temperature, top_k, top_p) into the [B, 4] int32 layout of spec_params_t."""
+    T = torch.as_tensor(temperature, dtype=torch.float32).reshape(-1)
+    K = torch.as_tensor(top_k, dtype=torch.int32).reshape(-1)
+    P = torch.as_tensor(top_p, dtype=torch.float32).reshape(-1)
+    z = torch.zeros_like(K)
+    packed = torch.stack([T.view(torch.int32), K, P.view(torch.int32), z], dim=1).contiguous()
+    return packed.to(device)
+
+
+class VerifyOutputs:
+    def __init__(self, B: int, k: int, device):
+        self.tokens = torch.empty((B, k + 1), dtype=torch.int32, device=device)
+        self.accept_len = torch.empty((B,), dtype=torch.int32, device=device)
+        self.logprobs = torch.empty((B, k + 1), dtype=torch.float32, device=device)
+        self.alpha = torch.empty((B, max(k, 0)), dtype=torch.float32, device=device)
+        self.flags = torch.empty((B,), dtype=torch.int32, device=device)   # uint32 bit pattern
+
+
+def new_workspace(B: int, k: int, V: int, device) -> torch.Tensor:
+    """A zero-filled workspace (the library leaves it zero-filled after each call)."""
+    n = workspace_size(B, k, V)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def spec_verify(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.Tensor, seed: int,
+                out: VerifyOutputs | None = None, workspace: torch.Tensor | None = None,
+                stream=None) -> VerifyOutputs:
+    """Run the verify step; inputs and outputs are CUDA tensors (see spec_verify.h).
+
+    logits [B, k+1, V] float32 or bfloat16; draft_probs [B, k, V] float32;
+    draft_tokens [B, k] int32; params [B, 4] int32 from make_params().
+    """
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, k+1, V]")
+    B, k1, V = logits.shape
+    k = k1 - 1
+    dev = logits.device
+    if logits.dtype == torch.float32:
+        dt = SPEC_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    if k > 0:
+        _check(draft_probs, "draft_probs", torch.float32, (B, k, V), dev)
+        _check(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _check(params, "params", torch.int32, (B, 4), dev)
+    if out is None:
+        out = VerifyOutputs(B, k, dev)
+    if workspace is None:
+        workspace = new_workspace(B, k, V, dev)
+    rc = LIB.spec_verify(_ptr(logits), dt, _ptr(draft_probs) if k > 0 else None,
+                         _ptr(draft_tokens) if k > 0 else None, _ptr(params),
+                         ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), B, k, V,
+                         _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.logprobs),
+                         _ptr(out.alpha) if k > 0 else None, _ptr(out.flags),
+                         _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_verify")
+    return out
+
+
+def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cache_conv,
+                flags=None, stream=None):
+    """Commit accepted states (see spec_commit in spec_verify.h).
+
+    verify_rec [L, B, S, H, Dk, Dv] float32 or None; verify_conv [L, B, S, W, C]
+    16-bit (bfloat16/int16) or None; accept_len [B] int32; cache_slot [B] int32
+    or None; cache_rec [L, slots, H, Dk, Dv]; cache_conv [L, slots, W, C].
+    """
+    if verify_rec is not None:
+        L, B, S, H, Dk, Dv = verify_rec.shape
+        slots = cache_rec.shape[1]
+        if verify_rec.dtype != torch.float32 or cache_rec.dtype != torch.float32:
+            raise TypeError("recurrent state must be float32")
+        if tuple(cache_rec.shape) != (L, slots, H, Dk, Dv):
+            raise ValueError("cache_rec shape mismatch")
+    else:
+        H = Dk = Dv = 1
+    if verify_conv is not None:
+        Lc, Bc, Sc, W, C = verify_conv.shape
+        if verify_rec is None:
+            L, B, S = Lc, Bc, Sc
+            slots = cache_conv.shape[1]
+        elif (Lc, Bc, Sc) != (L, B, S):
+            raise ValueError("verify_conv and verify_rec disagree on [L, B, S]")
+        if verify_conv.element_size() != 2 or cache_conv.element_size() != 2:
+            raise TypeError("conv state must be a 16-bit type")
+        if tuple(cache_conv.shape) != (L, slots, W, C):
+            raise ValueError("cache_conv shape mismatch")
+    else:
+        W = C = 1
+    if verify_rec is None and verify_conv is None:
+        raise ValueError("nothing to commit")
+    for t, nm in ((verify_rec, "verify_rec"), (verify_conv, "verify_conv"), (cache_rec, "cache_rec"),
+                  (cache_conv, "cache_conv")):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    dev = accept_len.device
+    _check(accept_len, "accept_len", torch.int32, (B,), dev)
+    if cache_slot is not None:
+        _check(cache_slot, "cache_slot", torch.int32, (B,), dev)
+    rc = LIB.spec_commit(_ptr(verify_rec), _ptr(verify_conv), _ptr(accept_len), _ptr(cache_slot),
+                         _ptr(cache_rec), _ptr(cache_conv), L, B, S, H, Dk, Dv, W, C, slots,
+                         _ptr(flags), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_commit")
+
+
+def philox4x32_10(ctr: torch.Tensor, seed: int, stream=None) -> torch.Tensor:
+    """Device Philox4x32-10 of a [n, 4] int32 (bit pattern) counter tensor."""
+    if ctr.dim() != 2 or ctr.shape[1] != 4 or ctr.dtype != torch.int32 or not ctr.is_contiguous():
+        raise ValueError("ctr must be a contiguous [n, 4] int32 tensor")
+    out = torch.empty_like(ctr)
+    rc = LIB.spec_philox4x32_10(_ptr(ctr), ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), _ptr(out),
+                                ctr.shape[0], _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_philox4x32_10")
+    return out

@@ -1,0 +1,206 @@
+// Device helpers shared by the verify and commit kernels (sm_103a).
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMargin = 1e-6f;
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10, written from J. K. Salmon et al., "Parallel random numbers:
+// as easy as 1, 2, 3" (SC'11), section 3: each round multiplies counter words
+// 0 and 2 by the two Philox-4x32 multipliers, permutes
+// (X0,X1,X2,X3) -> (hi(M1 X2)^X1^K0, lo(M1 X2), hi(M0 X0)^X3^K1, lo(M0 X0)),
+// and bumps the key by the Weyl constants; ten rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
+  return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+}
+
+// U = ((w >> 9) + 1/2) * 2^-23 and 1 - U, both exact: 1 + m*2^-23 is built
+// from the bits and (1 - 2^-24) subtracted (an exact subtraction, Sterbenz).
+__device__ __forceinline__ float uniform_of(uint32_t w) {
+  return __uint_as_float(0x3f800000u | (w >> 9)) - __uint_as_float(0x3f7fffffu);
+}
+__device__ __forceinline__ float one_minus_uniform_of(uint32_t w) {
+  return __uint_as_float(0x3f800000u | ((w >> 9) ^ 0x7fffffu)) - __uint_as_float(0x3f7fffffu);
+}
+
+// ---------------------------------------------------------------------------
+// Floating point helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Packed bf16x2 maximum that propagates NaN.
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Order-preserving key of a float: larger value -> larger key; -0 and +0 map
+// to the same key.  NaN never reaches it (rows with NaN are rejected first).
+__device__ __forceinline__ uint32_t okey(float f) {
+  uint32_t b = __float_as_uint(f);
+  b = (b == 0x80000000u) ? 0u : b;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_okey(uint32_t k) {
+  const uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(b);
+}
+
+// 64-bit total-order key: (value key, then smaller index first).
+__device__ __forceinline__ unsigned long long key64(uint32_t vkey, uint32_t idx) {
+  return ((unsigned long long)vkey << 32) | (unsigned long long)(0xffffffffu - idx);
+}
+__device__ __forceinline__ uint32_t key64_idx(unsigned long long k) {
+  return 0xffffffffu - (uint32_t)(k & 0xffffffffull);
+}
+
+// ---------------------------------------------------------------------------
+// Warp and block reductions with a fixed combination order (deterministic).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Exponential-race state: best score s1 (entry v1) and runner-up s2, with the
+// margin weights t = (p + q) / E of both.
+// ---------------------------------------------------------------------------
+struct Race {
+  float s1, t1, s2, t2, s1lo;
+  uint32_t v1;
+};
+
+__device__ __forceinline__ void race_init(Race& r) {
+  r.s1 = -1.0f;
+  r.t1 = 0.0f;
+  r.s2 = -1.0f;
+  r.t2 = 0.0f;
+  r.s1lo = 0.0f;
+  r.v1 = 0xffffffffu;
+}
+
+// Score s = w / E with E = -ln U.  Because E >= 1 - U, an entry with
+// w < s1 * (1 - 2^-20) * (1 - U) cannot beat the current best and needs no
+// logarithm; the factor (1 - 2^-20) absorbs the rounding of the test itself.
+__device__ __forceinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
+  const float om = one_minus_uniform_of(word);
+  if (w >= r.s1lo * om) {
+    const float E = -log1pf(-om);
+    const float s = w / E;
+    const float t = (w + tq) / E;
+    if (s > r.s1 || (s == r.s1 && v < r.v1)) {
+      if (v != r.v1) {
+        r.s2 = r.s1;
+        r.t2 = r.t1;
+      }
+      r.s1 = s;
+      r.t1 = t;
+      r.v1 = v;
+      r.s1lo = s * 0.99999905f;
+    } else if (v != r.v1 && s > r.s2) {
+      r.s2 = s;
+      r.t2 = t;
+    }
+  }
+}
+
+__device__ __forceinline__ void race_merge(Race& a, const Race& b) {
+  if (b.v1 == a.v1) {
+    if (b.s2 > a.s2) { a.s2 = b.s2; a.t2 = b.t2; }
+    return;
+  }
+  const bool b_wins = (b.s1 > a.s1) || (b.s1 == a.s1 && b.v1 < a.v1);
+  if (b_wins) {
+    // old a.s1 competes with b.s2 for second place
+    float s2 = a.s1, t2 = a.t1;
+    if (b.s2 > s2) { s2 = b.s2; t2 = b.t2; }
+    a.s1 = b.s1; a.t1 = b.t1; a.v1 = b.v1; a.s2 = s2; a.t2 = t2;
+  } else {
+    if (b.s1 > a.s2) { a.s2 = b.s1; a.t2 = b.t1; }
+  }
+  a.s1lo = a.s1 * 0.99999905f;
+}
+
+__device__ __forceinline__ Race race_shfl(const Race& r, int src_lane_xor) {
+  Race o;
+  o.s1 = __shfl_xor_sync(0xffffffffu, r.s1, src_lane_xor);
+  o.t1 = __shfl_xor_sync(0xffffffffu, r.t1, src_lane_xor);
+  o.s2 = __shfl_xor_sync(0xffffffffu, r.s2, src_lane_xor);
+  o.t2 = __shfl_xor_sync(0xffffffffu, r.t2, src_lane_xor);
+  o.v1 = __shfl_xor_sync(0xffffffffu, r.v1, src_lane_xor);
+  o.s1lo = 0.0f;
+  return o;
+}
+
+// Deterministic warp merge: lane pairs combine in a fixed xor tree, and the
+// merge itself is order-insensitive for the winner (max score, then min index).
+__device__ __forceinline__ void warp_race_merge(Race& r) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    Race other = race_shfl(r, o);
+    // keep the lower lane's state first so both lanes compute the same result
+    if ((threadIdx.x & o) == 0) {
+      race_merge(r, other);
+    } else {
+      Race mine = r;
+      r = other;
+      race_merge(r, mine);
+    }
+  }
+}
+
+}  // namespace specv

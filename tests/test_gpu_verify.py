@@ -1,0 +1,219 @@
+"""GPU parity of spec_verify against the oracle (element by element).
+
+Runs through the C ABI (ctypes binding).  Sizes: the tiny, top-p and mixed
+workloads are compared on every row at their full sizes; the adversarial
+workload (256 rows, k=4, fp32) runs in full on the GPU and is compared on a
+sample of rows the oracle computes one by one.  Random small cases cover odd
+and tiny vocabularies, k = 0..4, both dtypes, every filter combination, the
+general threshold paths (top-k above the candidate limit, top-p without
+top-k), ties, masked entries and invalid inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as ov
+from speculative_decoding_verify_07_gb300 import synth
+from tests.gpu_harness import compare, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def test_device_philox_matches_oracle():
+    from oracle import philox
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    rng = np.random.default_rng(5)
+    n = 1 << 18
+    ctr = rng.integers(0, 2 ** 32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    ctr[:16] = 0
+    ctr[16:32] = 0xFFFFFFFF
+    for seed in (0, 0x0123456789ABCDEF, 2 ** 64 - 1):
+        dev = sv.philox4x32_10(torch.from_numpy(ctr.view(np.int32)).cuda(), seed)
+        got = dev.cpu().numpy().view(np.uint32)
+        exp = philox.philox4x32_10(ctr, philox.seed_key(seed))
+        assert np.array_equal(got, exp)
+
+
+def test_parity_tiny():
+    inp = synth.make_tiny()
+    compare(run_gpu(inp), run_oracle(inp), "tiny")
+
+
+def test_parity_topp_workload():
+    inp = synth.make_topp()
+    s = compare(run_gpu(inp), run_oracle(inp), "topp")
+    assert s["exempt"] <= 2
+
+
+def test_parity_mixed_workload():
+    inp = synth.make_mixed()
+    s = compare(run_gpu(inp), run_oracle(inp), "mixed")
+    assert s["exempt"] <= 4
+
+
+def test_parity_adversarial_sampled_rows():
+    inp = synth.make_adversarial()
+    gpu = run_gpu(inp)
+    rows = [0, 1, 2, 63, 64, 127, 128, 129, 200, 254, 255]
+    compare(gpu, run_oracle(inp, rows=rows), "adversarial")
+    # whole-batch properties: the first half rejects early, the second half accepts everything
+    assert np.mean(gpu["accept_len"][:128]) < 1.2
+    assert np.all(gpu["accept_len"][128:] >= 4)
+    assert np.all(gpu["flags"] & (ov.F_NAN | ov.F_BAD_TOKEN | ov.F_BAD_PARAM) == 0)
+
+
+class _Case:
+    def __init__(self, logits, q, drafts, T, K, P, seed, dtype):
+        self.logits, self.q, self.drafts = logits, q, drafts
+        self.temperature, self.top_k, self.top_p = T, K, P
+        self.seed, self.dtype = seed, dtype
+
+
+def _random_case(rng, B, k, V, dtype, param_mode):
+    logits = rng.normal(0, 2.5, size=(B, k + 1, V)).astype(np.float32)
+    if dtype == "bf16":
+        logits = synth.round_to_bf16(logits)
+    # coarse values for ties in some rows
+    for b in range(0, B, 3):
+        logits[b] = np.round(logits[b] * 2) / 2
+    if V > 4:
+        logits[1 % B, :, : V // 7] = -np.inf       # masked entries
+    q = np.empty((B, k, V), np.float32)
+    for b in range(B):
+        for j in range(k):
+            z = logits[b, j].astype(np.float64)
+            z = np.where(np.isfinite(z), z, -30.0) + rng.normal(0, 0.8, V)
+            e = np.exp(z - z.max())
+            q[b, j] = (e / e.sum()).astype(np.float32)
+    drafts = np.empty((B, k), np.int32)
+    for b in range(B):
+        for j in range(k):
+            drafts[b, j] = rng.choice(V, p=q[b, j].astype(np.float64) / q[b, j].sum())
+    T = np.ones(B, np.float32)
+    K = np.zeros(B, np.int32)
+    P = np.ones(B, np.float32)
+    for b in range(B):
+        mode = param_mode if param_mode != "mix" else ["greedy", "temp", "topk", "topp", "both",
+                                                          "bigk", "bigk_topp", "k1"][b % 8]
+        if mode == "greedy":
+            T[b] = 0.0
+        elif mode == "temp":
+            T[b] = 0.6
+        elif mode == "topk":
+            T[b], K[b] = 0.9, max(1, min(V - 1, 20))
+        elif mode == "topp":
+            T[b], P[b] = 1.1, 0.8
+        elif mode == "both":
+            T[b], K[b], P[b] = 0.7, max(1, min(V - 1, 40)), 0.9
+        elif mode == "bigk":
+            T[b], K[b] = 1.0, max(1, min(V - 1, 300))
+        elif mode == "bigk_topp":
+            T[b], K[b], P[b] = 0.8, max(1, min(V - 1, 500)), 0.95
+        elif mode == "k1":
+            T[b], K[b] = 1.0, 1
+    return _Case(logits, q, drafts, T, K, P, int(rng.integers(0, 2 ** 63)), dtype)
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 100, 1000, 4097, 33331])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_parity_random_small(V, dtype):
+    rng = np.random.default_rng(V * 7 + (dtype == "bf16"))
+    for k in (0, 1, 2, 4):
+        case = _random_case(rng, B=16, k=k, V=V, dtype=dtype, param_mode="mix")
+        compare(run_gpu(case), run_oracle(case), f"V={V} {dtype} k={k}")
+
+
+def test_parity_large_topk_and_topp_only():
+    rng = np.random.default_rng(123)
+    for mode in ("bigk", "bigk_topp", "topp", "both"):
+        case = _random_case(rng, B=8, k=2, V=50000, dtype="bf16", param_mode=mode)
+        compare(run_gpu(case), run_oracle(case), mode)
+
+
+def test_invalid_inputs_set_flags():
+    rng = np.random.default_rng(9)
+    case = _random_case(rng, B=8, k=2, V=513, dtype="f32", param_mode="temp")
+    case.logits[0, 1, 5] = np.nan
+    case.logits[1, 2, 7] = np.inf
+    case.logits[2, 0, :] = -np.inf
+    case.drafts[3, 1] = 513
+    case.drafts[4, 0] = -5
+    case.temperature[5] = -1.0
+    case.top_p[6] = 0.0
+    gpu = run_gpu(case)
+    compare(gpu, run_oracle(case), "invalid")
+    assert gpu["flags"][0] == ov.F_NAN and gpu["accept_len"][0] == 0
+    assert np.all(gpu["tokens"][0] == -1)
+    assert gpu["flags"][3] & ov.F_BAD_TOKEN and gpu["flags"][5] & ov.F_BAD_PARAM
+
+
+def test_empty_batch_and_workspace_left_clean():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    case = _random_case(np.random.default_rng(1), B=5, k=3, V=1000, dtype="bf16", param_mode="mix")
+    logits, q, x, params = to_device(case)
+    ws = sv.new_workspace(5, 3, 1000, "cuda")
+    for _ in range(3):
+        sv.spec_verify(logits, q, x, params, 7, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    e = torch.empty((0, 3, 1000), dtype=torch.bfloat16, device="cuda")
+    out = sv.spec_verify(e, torch.empty((0, 2, 1000), device="cuda"),
+                         torch.empty((0, 2), dtype=torch.int32, device="cuda"),
+                         sv.make_params([], [], [], "cuda"), 0)
+    assert out.tokens.shape == (0, 3)
+
+
+def test_deterministic_and_graph_replay_bit_identical():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    inp = synth.make_mixed(B=16, V=32768)
+    logits, q, x, params = to_device(inp)
+    ws = sv.new_workspace(16, 2, 32768, "cuda")
+    ref = sv.spec_verify(logits, q, x, params, 11, workspace=ws)
+    again = sv.spec_verify(logits, q, x, params, 11, workspace=ws)
+    torch.cuda.synchronize()
+    for name in ("tokens", "accept_len", "logprobs", "alpha", "flags"):
+        assert torch.equal(getattr(ref, name), getattr(again, name)), name
+    out = sv.VerifyOutputs(16, 2, "cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sv.spec_verify(logits, q, x, params, 11, out=out, workspace=ws)   # warm-up on the side stream
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(g):
+        sv.spec_verify(logits, q, x, params, 11, out=out, workspace=ws)
+    for name in ("tokens", "logprobs"):
+        getattr(out, name).fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    for name in ("tokens", "accept_len", "logprobs", "alpha", "flags"):
+        assert torch.equal(getattr(ref, name), getattr(out, name)), name
+
+
+def test_gpu_distribution_preserved_40k_rows():
+    """The page's criterion run on the GPU path: 40k rows, drafts drawn from q."""
+    from scipy import stats
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    V, k, B = 6, 2, 40000
+    rng = np.random.default_rng(4)
+    base = rng.normal(0, 1.2, size=(k + 1, V)).astype(np.float32)
+    qrow = rng.dirichlet(np.full(V, 0.6), size=k).astype(np.float32)
+    logits = np.broadcast_to(base, (B, k + 1, V)).copy()
+    q = np.broadcast_to(qrow, (B, k, V)).copy()
+    drafts = np.stack([rng.choice(V, size=B, p=qrow[j] / qrow[j].sum()) for j in range(k)], 1)
+    case = _Case(logits, q, drafts.astype(np.int32), np.ones(B, np.float32),
+                 np.zeros(B, np.int32), np.ones(B, np.float32), 77, "f32")
+    gpu = run_gpu(case)
+    p0 = ov.target_distribution(base[0].astype(np.float64), 1.0, 0, 1.0).p
+    c = np.bincount(gpu["tokens"][:, 0], minlength=V).astype(float)
+    tv = 0.5 * np.abs(c / B - p0).sum()
+    pv = stats.chisquare(c, p0 * B).pvalue
+    assert tv <= 0.015 and pv > 1e-3, (tv, pv)
+    # and the sampled rows agree with the oracle exactly
+    compare(gpu, run_oracle(case, rows=list(range(0, B, 997))), "40k")
