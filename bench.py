@@ -168,14 +168,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The slowest rank's value (the job's time is the slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank, world, elapsed_s):
+    """Weak scaling: every rank processes its own batch; throughput counts all ranks."""
+    return rows_per_rank * world / elapsed_s
 
 
 def cpu_oracle_sample(inp, n_rows=16, commit_rows=2):
@@ -352,8 +358,7 @@ def run_ours(args):
     r_commit = roof("commit_kernel", cbytes, tc, c_hash)
     r_verify = roof("verify_kernel", vbytes, tv, v_hash)
     dominant = r_commit if tc >= tv else r_verify
-    rows_total = B * world * n
-    value = rows_total / (elapsed_ms * 1e-3)
+    value = job_rows_per_s(B * n, world, elapsed_ms * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
         "steps": n, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed_ms / n, 4),
@@ -386,6 +391,48 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_only(args):
+    """Launch one kernel per step on the benchmark workload (for ncu captures)."""
+    import torch
+
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    from speculative_decoding_verify_07_gb300 import synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if args.only == "verify":
+        sets = []
+        for i in range(N_SETS):
+            inp = synth.make_mixed(seed_offset=100 * i)
+            sets.append((torch.from_numpy(inp.logits).to(torch.bfloat16).to(dev),
+                         torch.from_numpy(inp.q).to(dev), torch.from_numpy(inp.drafts).to(dev),
+                         sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev), inp.seed + i))
+        ws = sv.new_workspace(B, K, V, dev)
+        out = sv.VerifyOutputs(B, K, dev)
+        fn = lambda i: sv.spec_verify(*sets[i % N_SETS][:4], sets[i % N_SETS][4], out=out, workspace=ws)
+    else:
+        sh = synth.CommitShape(L=args.layers)
+        vrec = torch.zeros((sh.L, sh.B, sh.S, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
+        vconv = torch.zeros((sh.L, sh.B, sh.S, sh.W, sh.C), dtype=torch.int16, device=dev)
+        crec = torch.zeros((sh.L, sh.slots, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
+        cconv = torch.zeros((sh.L, sh.slots, sh.W, sh.C), dtype=torch.int16, device=dev)
+        acc = torch.from_numpy(synth.commit_indices(sh)[0]).to(dev)
+        slot = torch.arange(sh.B, dtype=torch.int32, device=dev)
+        fn = lambda i: sv.spec_commit(vrec, vconv, acc, slot, crec, cconv)
+    for i in range(max(args.warmup, 3)):
+        fn(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record()
+        fn(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    t = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    print(json.dumps({"only": args.only, "steps": args.steps, "mean_us": statistics.mean(t),
+                      "median_us": statistics.median(t), "min_us": min(t)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,9 +440,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["verify", "commit"], default=None,
+                    help="profiling aid: launch only one kernel per step, print its mean time")
+    ap.add_argument("--layers", type=int, default=24, help="profiling aid for --only commit")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 

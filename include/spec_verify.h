@@ -89,9 +89,11 @@ enum {
 
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
- * cudaMemsetAsync); every completed spec_verify call leaves it zero-filled
- * again, so one workspace serves any number of later calls on one stream.
- * Two calls that may run concurrently need two workspaces.                   */
+ * cudaMemsetAsync).  Every completed spec_verify call returns the words that
+ * must start at zero (a unit-queue counter, a cluster exit counter and one
+ * ticket per row) to zero; the per-unit records behind them are rewritten by
+ * every call.  So one workspace serves any number of later calls on one
+ * stream; two calls that may run concurrently need two workspaces.           */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.

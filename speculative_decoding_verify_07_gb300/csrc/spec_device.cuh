@@ -49,6 +49,18 @@ __device__ __forceinline__ float one_minus_uniform_of(uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
+// Asynchronous global->shared copies (16 bytes per instruction, L1 bypassed).
+// Completion is awaited with cp.async.wait_group, a hardware wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// ---------------------------------------------------------------------------
 // Floating point helpers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2(float x) {

@@ -37,6 +37,7 @@ namespace specv {
 constexpr int kCandCap = 1024;       // candidate buffer of the small top-k path
 constexpr int kTopkSmall = 128;      // top_k <= this uses the candidate path
 constexpr int kMaxC = 16;
+constexpr int kQD = 3;               // depth of the per-thread q prefetch ring
 
 struct WsHeader {
   uint32_t queue_next;
@@ -82,8 +83,10 @@ struct Args {
 // Shared-memory control block (the staged slice and the arrays follow it).
 struct alignas(16) Ctl {
   unsigned long long xch[2][8];          // cluster exchange (published per CTA)
-  unsigned long long hist[2][256];       // histogram (count or fixed-point mass), double buffered
-  unsigned long long total[256];         // cluster-reduced histogram
+  uint32_t hist[2][256];                 // counts (double buffered)
+  uint32_t mlo[2][256];                  // fixed-point mass, low words (double buffered)
+  uint32_t mhi[2][256];                  // fixed-point mass, high words
+  unsigned long long total[256];         // block- or cluster-reduced histogram
   unsigned long long bc64[8];            // block broadcast
   float wred[kWarps * 8];                // warp partials
   float bcf[8];
@@ -99,6 +102,7 @@ struct Smem {
   unsigned long long* cand;   // candidate keys (leader)
   float* list_e;              // leader: e of the kept candidates
   float* list_cum;            // leader: prefix sums
+  float* qring;               // kQD x kThreads x 8 floats: per-thread q prefetch ring
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -111,6 +115,7 @@ __host__ __device__ inline size_t smem_bytes(int slice_groups) {
   size_t lists = (size_t)2 * kTopkSmall * 4;
   off += align_up(gm > lists ? gm : lists, 128);
   off += (size_t)kCandCap * 8;
+  off += (size_t)kQD * kThreads * 8 * 4;
   return off;
 }
 
@@ -129,6 +134,8 @@ __device__ inline Smem carve(unsigned char* base, int slice_groups) {
   size_t lists = (size_t)2 * kTopkSmall * 4;
   off += align_up(gm > lists ? gm : lists, 128);
   s.cand = reinterpret_cast<unsigned long long*>(base + off);
+  off += (size_t)kCandCap * 8;
+  s.qring = reinterpret_cast<float*>(base + off);
   return s;
 }
 
@@ -317,13 +324,35 @@ __device__ Race cl_race(Cluster& K, Smem& S, const Race& mine) {
 
 // Sum a 256-bin histogram over the cluster into S.ctl->total (every CTA gets
 // the same totals).  The caller must have filled hist[slot] and synced the block.
-__device__ void cl_hist(Cluster& K, Smem& S, int slot) {
+__device__ void cl_hist(Cluster& K, Smem& S, int slot, bool mass = false) {
   K.cl.sync();
   const int t = threadIdx.x;
   unsigned long long s = 0;
-  for (int r = 0; r < K.C; ++r) s += *remote(K, &S.ctl->hist[slot][t], r);
+  for (int r = 0; r < K.C; ++r) {
+    if (mass) {
+      const unsigned long long lo = *remote(K, &S.ctl->mlo[slot][t], r);
+      const unsigned long long hi = *remote(K, &S.ctl->mhi[slot][t], r);
+      s += (hi << 32) + lo;
+    } else {
+      s += *remote(K, &S.ctl->hist[slot][t], r);
+    }
+  }
   S.ctl->total[t] = s;
   __syncthreads();
+}
+
+// Exact fixed-point mass accumulation with native 32-bit shared atomics: the
+// low word wraps, and the atomic that wraps it carries one into the high word.
+__device__ __forceinline__ void mass_add(uint32_t* lo, uint32_t* hi, unsigned long long fx) {
+  const uint32_t l = (uint32_t)fx;
+  const uint32_t h = (uint32_t)(fx >> 32);
+  const uint32_t old = atomicAdd(lo, l);
+  const uint32_t carry = (old + l < old) ? 1u : 0u;
+  if (h + carry) atomicAdd(hi, h + carry);
+}
+
+__device__ __forceinline__ unsigned long long mass_fixed(float e) {
+  return __float2ull_rz(e * 1099511627776.0f);   // e * 2^40, e in [0, 1]
 }
 
 // ---------------------------------------------------------------------------
@@ -412,12 +441,13 @@ __device__ void block_race(Smem& S, Race& r) {
 // returns b and the mass strictly above it.  Run by warp 0; result broadcast.
 // ---------------------------------------------------------------------------
 __device__ void select_from_top(Smem& S, unsigned long long need, int* out_bin,
-                                unsigned long long* out_above) {
+                                unsigned long long* out_above, const unsigned long long* bins = nullptr) {
+  const unsigned long long* tot = bins ? bins : S.ctl->total;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     // lane l owns bins 255-8l .. 248-8l (descending)
     unsigned long long own = 0;
-    for (int i = 0; i < 8; ++i) own += S.ctl->total[255 - 8 * lane - i];
+    for (int i = 0; i < 8; ++i) own += tot[255 - 8 * lane - i];
     // inclusive scan over lanes (lane 0 = top bins)
     unsigned long long inc = own;
 #pragma unroll
@@ -433,7 +463,7 @@ __device__ void select_from_top(Smem& S, unsigned long long need, int* out_bin,
       int b = 255 - 8 * lane;
       int chosen = 248 - 8 * lane;   // fallback: lowest bin of the lane
       for (int i = 0; i < 8; ++i) {
-        const unsigned long long t = S.ctl->total[b - i];
+        const unsigned long long t = tot[b - i];
         if (above + t >= need) { chosen = b - i; break; }
         if (i == 7) { chosen = b - i; break; }
         above += t;
@@ -480,6 +510,98 @@ __device__ void select_from_bin0(Smem& S, unsigned long long need, int* out_bin,
   *out_bin = S.ctl->bci[2];
   *out_above = S.ctl->bc64[1];
   __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Rank select on distances from the maximum.  Values are described by their
+// distance d = key(max) - key(v) >= 0 in the order-key space (key = the 16-bit
+// bf16 pattern order or the 32-bit float order), so the largest values have
+// the smallest distances.  kth_distance finds the distance of the value of
+// 1-based rank `need` (counting multiplicity) among the values that `each`
+// enumerates (per CTA, or over the whole cluster when kCluster).  The first
+// histogram gives every distance below 255 << s0 a bin and lumps the tail
+// without touching it, so only values near the top cost an atomic; the
+// selected bin is refined 8 bits at a time.  If the rank lies in the tail, a
+// plain top-down radix over all bits takes over.  On return `need` is the
+// rank inside the group of values at exactly that distance.
+// ---------------------------------------------------------------------------
+template <bool kCluster, typename Each>
+__device__ uint32_t kth_distance(Cluster& K, Smem& S, Each each, unsigned long long& need, int s0,
+                                 int dbits, int& hs) {
+  auto reduce = [&](int slot) {
+    if (kCluster) {
+      cl_hist(K, S, slot);
+    } else {
+      S.ctl->total[threadIdx.x] = S.ctl->hist[slot][threadIdx.x];
+      __syncthreads();
+    }
+  };
+  // level 1: exact near-top bins, tail lumped
+  {
+    const int slot = hs++ & 1;
+    S.ctl->hist[slot][threadIdx.x] = 0;
+    __syncthreads();
+    const uint32_t lim = 255u << s0;
+    each([&](uint32_t d) {
+      if (d < lim) atomicAdd(&S.ctl->hist[slot][d >> s0], 1u);
+    });
+    __syncthreads();
+    reduce(slot);
+    int b;
+    unsigned long long below;
+    select_from_bin0(S, need, &b, &below);
+    if (b < 255) {
+      need -= below;
+      uint32_t base = (uint32_t)b << s0;
+      for (int s = s0 - 8; s >= 0; s -= 8) {
+        const int sl = hs++ & 1;
+        S.ctl->hist[sl][threadIdx.x] = 0;
+        __syncthreads();
+        const uint32_t span = 1u << (s + 8);
+        each([&](uint32_t d) {
+          if (d >= base && d - base < span) atomicAdd(&S.ctl->hist[sl][(d - base) >> s], 1u);
+        });
+        __syncthreads();
+        reduce(sl);
+        int bb;
+        unsigned long long bl;
+        select_from_bin0(S, need, &bb, &bl);
+        need -= bl;
+        base += (uint32_t)bb << s;
+      }
+      return base;
+    }
+  }
+  // tail: top-down radix over all distance bits
+  uint32_t prefix = 0u, mask = 0u;
+  for (int shift = dbits - 8; shift >= 0; shift -= 8) {
+    const int slot = hs++ & 1;
+    S.ctl->hist[slot][threadIdx.x] = 0;
+    __syncthreads();
+    each([&](uint32_t d) {
+      if ((d & mask) == prefix) atomicAdd(&S.ctl->hist[slot][(d >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    reduce(slot);
+    int b;
+    unsigned long long below;
+    select_from_bin0(S, need, &b, &below);
+    need -= below;
+    prefix |= (uint32_t)b << shift;
+    mask |= 255u << shift;
+  }
+  return prefix;
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t kf(float v) {
+  return kBF16 ? (okey(v) >> 16) : okey(v);
+}
+// Full 32-bit order key of the value whose kf() is k.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t full_key(uint32_t k) {
+  if (!kBF16) return k;
+  return (k << 16) | ((k & 0x8000u) ? 0u : 0xffffu);
 }
 
 // ---------------------------------------------------------------------------
@@ -577,47 +699,28 @@ __device__ uint32_t nth_tie_index(Cluster& K, Smem& S, const Unit& U, const Args
   return mm.x;
 }
 
-// Radix select of the element at 1-based rank `need` (from the top of the
-// total order) among elements with okey >= floor restricted to `outer`.
-// Count-weighted.  Returns the threshold describing the first `need` elements.
+// The first `need` elements of the total order (top-k over the whole unit):
+// the exact value by kth_distance over the cluster, then the index cut inside
+// that value's ties.
 template <bool kBF16>
-__device__ Thresh select_count(Cluster& K, Smem& S, const Unit& U, const Args& A,
+__device__ Thresh select_count(Cluster& K, Smem& S, const Unit& U, const Args& A, float m,
                                unsigned long long need) {
-  uint32_t prefix = 0, mask = 0;
-  const int first_shift = 24, last_shift = kBF16 ? 16 : 0;
-  int hs = 0;
-  for (int shift = first_shift; shift >= last_shift; shift -= 8) {
-    const int slot = hs++ & 1;
-    S.ctl->hist[slot][threadIdx.x] = 0;
-    __syncthreads();
+  const uint32_t km = kf<kBF16>(m);
+  auto each = [&](auto fn) {
     for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
       float v[8];
       load_group_values<kBF16>(S, gl, v);
       const int e0 = (U.g0 + gl) * 8;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t key = okey(v[i]);
-        if (e0 + i < A.V && (key & mask) == prefix)
-          atomicAdd(&S.ctl->hist[slot][(key >> shift) & 255], 1ull);
-      }
+      for (int i = 0; i < 8; ++i)
+        if (e0 + i < A.V) fn(km - kf<kBF16>(v[i]));
     }
-    __syncthreads();
-    cl_hist(K, S, slot);
-    int b;
-    unsigned long long above;
-    select_from_top(S, need, &b, &above);
-    need -= above;
-    prefix |= (uint32_t)b << shift;
-    mask |= 255u << shift;
-  }
-  uint32_t tkey = prefix;
-  if (kBF16) {
-    // all bf16 values with the same top 16 key bits have identical low bits
-    tkey |= (prefix & 0x80000000u) ? 0u : 0xffffu;
-  }
+  };
+  int hs = 0;
+  const uint32_t d = kth_distance<true>(K, S, each, need, kBF16 ? 0 : 16, kBF16 ? 16 : 32, hs);
   Thresh t;
-  t.tkey = tkey;
-  t.tidx = nth_tie_index<kBF16>(K, S, U, A, tkey, need);
+  t.tkey = full_key<kBF16>(km - d);
+  t.tidx = nth_tie_index<kBF16>(K, S, U, A, t.tkey, need);
   return t;
 }
 
@@ -719,62 +822,93 @@ __device__ AcceptInfo accept_test(const Args& A, const Unit& U, bool bf16, float
 }
 
 // ---------------------------------------------------------------------------
-// The small top-k path: candidates from the groups whose maximum reaches the
-// K-th largest group maximum, sorted exactly, then everything else on the list.
-// Returns false (in every CTA) when the candidates overflow the buffer.
+// The small top-k path, per CTA: every top-K element of the slice lies in a
+// group whose maximum is among the K largest group maxima of the slice, so
+// the K-th largest local group maximum tau bounds the local candidates
+// (elements >= tau, at most 8 per qualifying group).  They are sorted exactly
+// in the total order; the first K form the CTA's list.  Returns the list
+// length; *overflow is set when the candidates do not fit the buffer.
 // ---------------------------------------------------------------------------
+__device__ void bitonic_desc(unsigned long long* s, int n);
+
 template <bool kBF16>
-__device__ bool topk_candidates(Cluster& K, Smem& S, const Unit& U, const Args& A, int Ktop,
-                                uint32_t* out_count) {
-  // K-th largest group maximum (count with multiplicity) by radix select.
-  unsigned long long need = (unsigned long long)Ktop;
-  uint32_t prefix = 0, mask = 0;
-  uint32_t tau;
-  if ((long long)Ktop >= (long long)A.groups_total) {
-    tau = 0u;   // every group qualifies
-  } else {
+__device__ int local_topk(Cluster& K, Smem& S, const Unit& U, const Args& A, float m, int Ktop,
+                          bool* overflow) {
+  // tau: kf() of the K-th largest group maximum of this CTA (all groups when fewer)
+  uint32_t tau = 0u;
+  const uint32_t km = kf<kBF16>(m);
+  if (Ktop < U.ng) {
+    unsigned long long need = (unsigned long long)Ktop;
+    auto each = [&](auto fn) {
+      for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) fn(km - kf<kBF16>(S.gmax[gl]));
+    };
     int hs = 0;
-    for (int shift = 24; shift >= (kBF16 ? 16 : 0); shift -= 8) {
-      const int slot = hs++ & 1;
-      S.ctl->hist[slot][threadIdx.x] = 0;
-      __syncthreads();
-      for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
-        const uint32_t key = okey(S.gmax[gl]);
-        if ((key & mask) == prefix) atomicAdd(&S.ctl->hist[slot][(key >> shift) & 255], 1ull);
-      }
-      __syncthreads();
-      cl_hist(K, S, slot);
-      int b;
-      unsigned long long above;
-      select_from_top(S, need, &b, &above);
-      need -= above;
-      prefix |= (uint32_t)b << shift;
-      mask |= 255u << shift;
-    }
-    tau = prefix;   // compare on the selected high bits only (bf16: low bits are sign fill)
+    const uint32_t d = kth_distance<false>(K, S, each, need, kBF16 ? 0 : 16, kBF16 ? 16 : 32, hs);
+    tau = km - d;
   }
-  const uint32_t tmask = (Ktop >= A.groups_total) ? 0u : mask;
-  // Append candidate elements (value >= tau on the selected bits) to the leader.
-  uint32_t* lcount = remote(K, &S.ctl->cand_count, 0);
-  unsigned long long* lcand = remote(K, S.cand, 0);
+  if (threadIdx.x == 0) S.ctl->cand_count = 0;
+  __syncthreads();
   for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
-    if ((okey(S.gmax[gl]) & tmask) < tau) continue;
+    if (kf<kBF16>(S.gmax[gl]) < tau) continue;
     float v[8];
     load_group_values<kBF16>(S, gl, v);
     const int e0 = (U.g0 + gl) * 8;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t key = okey(v[i]);
-      if (e0 + i < A.V && (key & tmask) >= tau) {
-        const uint32_t slot = atomicAdd(lcount, 1u);
-        if (slot < (uint32_t)kCandCap) lcand[slot] = key64(key, (uint32_t)(e0 + i));
+      if (e0 + i < A.V && kf<kBF16>(v[i]) >= tau) {
+        const uint32_t slot = atomicAdd(&S.ctl->cand_count, 1u);
+        if (slot < (uint32_t)kCandCap) S.cand[slot] = key64(key, (uint32_t)(e0 + i));
       }
     }
   }
-  K.cl.sync();
-  const uint32_t count = *lcount;
-  *out_count = count;
-  return count <= (uint32_t)kCandCap;
+  __syncthreads();
+  const uint32_t count = S.ctl->cand_count;
+  *overflow = count > (uint32_t)kCandCap;
+  if (*overflow || count == 0) return 0;
+  int n = 1;
+  while (n < (int)count) n <<= 1;
+  for (int i = (int)count + threadIdx.x; i < n; i += kThreads) S.cand[i] = 0ull;
+  __syncthreads();
+  bitonic_desc(S.cand, n);
+  return min((int)count, Ktop);
+}
+
+// Number of entries of a descending list greater than key.
+__device__ __forceinline__ int count_greater(const unsigned long long* l, int n, unsigned long long key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (l[mid] > key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Leader: merge the C sorted per-CTA lists into the first Ktop entries of
+// S.cand (ranks by binary search; keys are unique).  Returns the list length.
+__device__ int merge_lists(Cluster& K, Smem& S, const int* counts, int Ktop) {
+  unsigned long long* mb = reinterpret_cast<unsigned long long*>(S.slice);
+  int off[kMaxC + 1];
+  off[0] = 0;
+  for (int c = 0; c < K.C; ++c) off[c + 1] = off[c] + counts[c];
+  const int total = off[K.C];
+  for (int c = 0; c < K.C; ++c) {
+    const unsigned long long* src = remote(K, S.cand, c);
+    for (int i = threadIdx.x; i < counts[c]; i += kThreads) mb[off[c] + i] = src[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < total; e += kThreads) {
+    int c = 0;
+    while (e >= off[c + 1]) ++c;
+    const unsigned long long key = mb[e];
+    int rank = e - off[c];
+    for (int d = 0; d < K.C && rank < Ktop; ++d)
+      if (d != c) rank += count_greater(mb + off[d], counts[d], key);
+    if (rank < Ktop) S.cand[rank] = key;
+  }
+  __syncthreads();
+  return min(total, Ktop);
 }
 
 // Bitonic sort of cand[0..n) descending (n a power of two), one CTA.
@@ -951,58 +1085,55 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
   const bool small_topk = !U.greedy && U.K > 0 && U.K <= kTopkSmall;
 
   // ---- stage: global -> shared, group maxima, max / argmax, NaN ----
+  // Every thread copies its own groups (cp.async, the whole slice in flight at
+  // once) and later passes read back exactly the groups the thread copied, so
+  // no block barrier is needed between staging and use.
   unsigned long long best = 0;   // key64 of (value, index)
   bool nan_seen = false;
   {
-    const unsigned char* gbase = reinterpret_cast<const unsigned char*>(A.logits) +
-                                 U.lrow * (kBF16 ? 2 : 4);
+    constexpr int ES = kBF16 ? 2 : 4;
+    const unsigned char* gbase = reinterpret_cast<const unsigned char*>(A.logits) + U.lrow * ES;
     for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
       const int e0 = (U.g0 + gl) * 8;
-      float v[8];
+      unsigned char* dst = S.slice + (size_t)gl * 8 * ES;
+      if (A.vec_logits && e0 + 8 <= A.V) {
+        cp_async16(dst, gbase + (size_t)e0 * ES);
+        if (!kBF16) cp_async16(dst + 16, gbase + (size_t)e0 * ES + 16);
+      } else if (kBF16) {
+        const uint16_t* p16 = reinterpret_cast<const uint16_t*>(gbase);
+        uint32_t h[8];
+        for (int i = 0; i < 8; ++i) h[i] = (e0 + i < A.V) ? p16[e0 + i] : 0xff80u;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                                   h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      } else {
+        const float* p32 = reinterpret_cast<const float*>(gbase);
+        float t[8];
+        for (int i = 0; i < 8; ++i) t[i] = (e0 + i < A.V) ? p32[e0 + i] : -INFINITY;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(t[0], t[1], t[2], t[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(t[4], t[5], t[6], t[7]);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
+      const int e0 = (U.g0 + gl) * 8;
       float gm;
       if (kBF16) {
-        uint4 w;
-        if (A.vec_logits && e0 + 8 <= A.V) {
-          w = __ldcs(reinterpret_cast<const uint4*>(gbase + (size_t)e0 * 2));
-        } else {
-          uint32_t h[8];
-          const uint16_t* p16 = reinterpret_cast<const uint16_t*>(gbase);
-          for (int i = 0; i < 8; ++i) h[i] = (e0 + i < A.V) ? p16[e0 + i] : 0xff80u;
-          w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                         h[6] | (h[7] << 16));
-        }
-        reinterpret_cast<uint4*>(S.slice)[gl] = w;
+        const uint4 w = reinterpret_cast<const uint4*>(S.slice)[gl];
         const uint32_t m2 = max_nan_bf16x2(max_nan_bf16x2(w.x, w.y), max_nan_bf16x2(w.z, w.w));
         gm = max_nan(bf16_lo(m2), bf16_hi(m2));
-        if (gm > from_okey((uint32_t)(best >> 32)) || best == 0) {
-          v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-          v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-          v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-          v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-        }
       } else {
-        float4 a, b;
-        if (A.vec_logits && e0 + 8 <= A.V) {
-          a = __ldcs(reinterpret_cast<const float4*>(gbase + (size_t)e0 * 4));
-          b = __ldcs(reinterpret_cast<const float4*>(gbase + (size_t)e0 * 4 + 16));
-        } else {
-          const float* p32 = reinterpret_cast<const float*>(gbase);
-          float t[8];
-          for (int i = 0; i < 8; ++i) t[i] = (e0 + i < A.V) ? p32[e0 + i] : -INFINITY;
-          a = make_float4(t[0], t[1], t[2], t[3]);
-          b = make_float4(t[4], t[5], t[6], t[7]);
-        }
-        reinterpret_cast<float4*>(S.slice)[2 * gl] = a;
-        reinterpret_cast<float4*>(S.slice)[2 * gl + 1] = b;
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        gm = max_nan(max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])),
-                     max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7])));
+        const float4 a = reinterpret_cast<const float4*>(S.slice)[2 * gl];
+        const float4 b = reinterpret_cast<const float4*>(S.slice)[2 * gl + 1];
+        gm = max_nan(max_nan(max_nan(a.x, a.y), max_nan(a.z, a.w)),
+                     max_nan(max_nan(b.x, b.y), max_nan(b.z, b.w)));
       }
       S.gmax[gl] = gm;
       if (gm != gm) {
         nan_seen = true;
       } else if (best == 0 || gm > from_okey((uint32_t)(best >> 32))) {
+        float v[8];
+        load_group_values<kBF16>(S, gl, v);
         int first = 0;
 #pragma unroll
         for (int i = 7; i >= 0; --i)
@@ -1074,16 +1205,22 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
 
   // ---------------- small top-k: candidate list ----------------
   if (small_topk) {
-    uint32_t count = 0;
-    const bool ok = topk_candidates<kBF16>(K, S, U, A, U.K, &count);
-    if (ok) {
+    bool ovf = false;
+    const int nloc = local_topk<kBF16>(K, S, U, A, m, U.K, &ovf);
+    const int slot = K.step++ & 1;
+    if (threadIdx.x == 0) S.ctl->xch[slot][0] = (unsigned long long)nloc | (ovf ? (1ull << 40) : 0ull);
+    K.cl.sync();
+    int counts[kMaxC];
+    bool any_ovf = false;
+    for (int c = 0; c < K.C; ++c) {
+      const unsigned long long w = *remote(K, &S.ctl->xch[slot][0], c);
+      counts[c] = (int)(w & 0xffffffffull);
+      any_ovf |= (w >> 40) != 0;
+    }
+    if (!any_ovf) {
       if (K.rank == 0) {
-        int n = 1;
-        while (n < (int)count) n <<= 1;
-        for (int i = (int)count + threadIdx.x; i < n; i += kThreads) S.cand[i] = 0ull;
-        __syncthreads();
-        bitonic_desc(S.cand, n);
-        if (threadIdx.x < 32) list_unit<kBF16>(S, U, A, m, am, min(U.K, (int)count), base_flags);
+        const int n_k = K.C > 1 ? merge_lists(K, S, counts, U.K) : counts[0];
+        if (threadIdx.x < 32) list_unit<kBF16>(S, U, A, m, am, n_k, base_flags);
       }
       return;
     }
@@ -1094,7 +1231,7 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
   Thresh th;
   th.tkey = 0u;
   th.tidx = 0xffffffffu;
-  if (U.K > 0) th = select_count<kBF16>(K, S, U, A, (unsigned long long)U.K);
+  if (U.K > 0) th = select_count<kBF16>(K, S, U, A, m, (unsigned long long)U.K);
   const bool filtered = U.K > 0 || U.P < 1.0f;
   const bool fused_bonus = !has_q && !filtered;
 
@@ -1109,9 +1246,11 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
   const bool topp = U.P < 1.0f;
   const int hslot = 0;
   if (topp) {
-    S.ctl->hist[hslot][threadIdx.x] = 0;
+    S.ctl->mlo[hslot][threadIdx.x] = 0;
+    S.ctl->mhi[hslot][threadIdx.x] = 0;
     __syncthreads();
   }
+  unsigned long long tail = 0;   // mass of the lumped last bin, kept in registers
   float z0 = 0.f, z1 = 0.f;
   for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
     float v[8];
@@ -1126,9 +1265,10 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
       e[i] = in ? ex2(x) : 0.f;
       if (i & 1) z1 += e[i]; else z0 += e[i];
       if (topp && e[i] > 0.f) {
-        int bin = __float2int_rz(fminf(-x * 8.0f, 255.0f));
-        const unsigned long long fx = __float2ull_rz(e[i] * 1099511627776.0f);
-        atomicAdd(&S.ctl->hist[hslot][bin], fx);
+        const int bin = __float2int_rz(fminf(-x * 8.0f, 255.0f));
+        const unsigned long long fx = mass_fixed(e[i]);
+        if (bin < 255) mass_add(&S.ctl->mlo[hslot][bin], &S.ctl->mhi[hslot][bin], fx);
+        else tail += fx;
       }
     }
     if (fused_bonus) {
@@ -1150,7 +1290,13 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
   uint32_t flags = base_flags;
   if (topp) {
     __syncthreads();
-    cl_hist(K, S, hslot);
+    tail = block_sum_u64(S, tail);
+    if (threadIdx.x == 0) {
+      S.ctl->mlo[hslot][255] = (uint32_t)tail;
+      S.ctl->mhi[hslot][255] = (uint32_t)(tail >> 32);
+    }
+    __syncthreads();
+    cl_hist(K, S, hslot, true);
     unsigned long long zk = 0;
     {
       // total mass: sum of the reduced histogram (every thread holds one bin)
@@ -1220,7 +1366,8 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
       const int nbits = 32 - __clz(span);
       const int shift = nbits > 8 ? nbits - 8 : 0;
       const int slot = hs++ & 1;
-      S.ctl->hist[slot][threadIdx.x] = 0;
+      S.ctl->mlo[slot][threadIdx.x] = 0;
+      S.ctl->mhi[slot][threadIdx.x] = 0;
       __syncthreads();
       for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
         float v[8];
@@ -1233,12 +1380,12 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
           if (key < lo || key > hi) continue;
           if (U.K > 0 && !kept(th, key, (uint32_t)(e0 + i))) continue;
           const float e = ex2((v[i] - m) * U.c);
-          const unsigned long long fx = __float2ull_rz(e * 1099511627776.0f);
-          atomicAdd(&S.ctl->hist[slot][(hi - key) >> shift], fx);
+          const uint32_t bin = (hi - key) >> shift;
+          mass_add(&S.ctl->mlo[slot][bin], &S.ctl->mhi[slot][bin], mass_fixed(e));
         }
       }
       __syncthreads();
-      cl_hist(K, S, slot);
+      cl_hist(K, S, slot, true);
       int sb;
       unsigned long long ab;
       select_from_bin0(S, rem, &sb, &ab);
@@ -1254,7 +1401,7 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
     const uint32_t tkey = hi;
     const float tv = from_okey(tkey);
     const float et = ex2((tv - m) * U.c);
-    const unsigned long long efx = __float2ull_rz(et * 1099511627776.0f);
+    const unsigned long long efx = mass_fixed(et);
     unsigned long long n_need = efx ? (rem + efx - 1) / efx : 1ull;
     if (n_need == 0) n_need = 1;
     // the n-th tie among kept elements; with a top-k threshold at the same key,
@@ -1312,15 +1459,38 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
       race_consider(race, 1.0f, 0.f, (uint32_t)am, word_of(pw, am & 3));
     }
     const float* qbase = A.q + U.qrow;
-    for (int gl = threadIdx.x; gl < U.ng; gl += kThreads) {
+    // q streams through a per-thread ring of kQD slots: group i of this thread
+    // is copied kQD-1 iterations before it is consumed (empty commits keep the
+    // group count uniform), so each thread keeps 64+ bytes of q in flight.
+    const bool qpipe = has_q && A.vec_q;
+    float* ring = S.qring + (size_t)threadIdx.x * 8;
+    auto q_issue = [&](int i) {
+      const int gl = threadIdx.x + i * kThreads;
+      if (gl < U.ng) {
+        const int e0 = (U.g0 + gl) * 8;
+        if (e0 + 8 <= A.V) {
+          float* d = ring + (size_t)(i % kQD) * kThreads * 8;
+          cp_async16(d, qbase + e0);
+          cp_async16(d + 4, qbase + e0 + 4);
+        }
+      }
+      cp_async_commit();
+    };
+    if (qpipe)
+      for (int i = 0; i < kQD - 1; ++i) q_issue(i);
+    int it = 0;
+    for (int gl = threadIdx.x; gl < U.ng; gl += kThreads, ++it) {
       float v[8];
       load_group_values<kBF16>(S, gl, v);
       const int e0 = (U.g0 + gl) * 8;
       float qv[8];
       if (has_q) {
-        if (A.vec_q && e0 + 8 <= A.V) {
-          const float4 qa = __ldcs(reinterpret_cast<const float4*>(qbase + e0));
-          const float4 qb = __ldcs(reinterpret_cast<const float4*>(qbase + e0 + 4));
+        if (qpipe && e0 + 8 <= A.V) {
+          q_issue(it + kQD - 1);
+          cp_async_wait<kQD - 1>();
+          const float* d = ring + (size_t)(it % kQD) * kThreads * 8;
+          const float4 qa = *reinterpret_cast<const float4*>(d);
+          const float4 qb = *reinterpret_cast<const float4*>(d + 4);
           qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
           qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
         } else {
@@ -1359,6 +1529,7 @@ __device__ void process_unit(Cluster& K, Smem& S, const Args& A, int unit) {
       }
     }
   }
+  cp_async_wait<0>();
   float alpha_v = 0.f;
   if (has_q) {
     const float2 ab = block_sum_f2(S, al0 + al1, 0.f);
@@ -1484,18 +1655,29 @@ static int plan(int V, int device, LaunchCfg* cfg) {
   static int cache_key[64][4];
   static int cache_val[64];
   static int cache_n = 0;
+  // The dynamic shared memory limit is a property of the kernel (per device),
+  // not of one launch: keep it at the largest size any launch has needed.
+  static int smem_set[64][2];
   std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return SPEC_E_CUDA;
+  auto kern = verify_kernel<kBF16>;
+  if (smem_set[device][kBF16] < (int)cfg->smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg->smem) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_E_CUDA;
+    }
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_E_CUDA;
+    }
+    smem_set[device][kBF16] = (int)cfg->smem;
+  }
   for (int i = 0; i < cache_n; ++i)
     if (cache_key[i][0] == device && cache_key[i][1] == C && cache_key[i][2] == (int)cfg->smem &&
         cache_key[i][3] == (int)kBF16) {
       cfg->max_clusters = cache_val[i];
       return SPEC_OK;
     }
-  auto kern = verify_kernel<kBF16>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg->smem) != cudaSuccess)
-    return SPEC_E_CUDA;
-  if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return SPEC_E_CUDA;
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   cudaLaunchAttribute at[1];
