@@ -165,6 +165,37 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
                 uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W,
                 int C, int slots, uint32_t* flags, void* cuda_stream);
 
+/* spec_verify_noalloc - spec_verify for callers that cannot allocate device
+ * memory.  The paper has no counterpart: this entry point exists for plugin
+ * or custom-op hosts that pass a kernel only its inputs and outputs, for
+ * engines whose allocator has reserved all of HBM, and for loops that cannot
+ * take the synchronisation of cudaMalloc/cudaFree.
+ *
+ * Arguments and outputs are those of spec_verify without the workspace: the
+ * scratch comes from an array of SPEC_NOALLOC_MAX_WORKSPACE bytes inside the
+ * library (a file-scope device array, held on every GPU that loads the
+ * library until the process exits).  The call allocates nothing.
+ *   - Limit: spec_verify_workspace_size(B, k, V) must not exceed
+ *     SPEC_NOALLOC_MAX_WORKSPACE (1 MiB: about 32,000 (row, position) units,
+ *     e.g. B = 4096 rows at k = 6); a larger batch returns SPEC_E_WORKSPACE
+ *     and enqueues nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call clears the part of the array it uses (cudaMemsetAsync on
+ *     cuda_stream) before the kernel, because the array keeps the previous
+ *     call's contents.
+ *   - All calls share the one array: two calls that can overlap on the GPU
+ *     (for example on two streams) race and corrupt each other's results;
+ *     order them on one stream or use spec_verify with separate workspaces.
+ * Errors: those of spec_verify, and SPEC_E_WORKSPACE for a batch beyond the
+ * limit.                                                                    */
+#define SPEC_NOALLOC_MAX_WORKSPACE (1u << 20)
+int spec_verify_noalloc(const void* logits, int logits_dtype, const float* draft_probs,
+                        const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
+                        int B, int k, int V, int32_t* tokens, int32_t* accept_len, float* logprobs,
+                        float* alpha, uint32_t* flags, void* cuda_stream);
+
 /* Diagnostic: out[i] = Philox4x32-10(ctr[i], key = (seed mod 2^32, seed >> 32))
  * for i < n, computed by the same device function spec_verify uses.  ctr and
  * out are device arrays of n uint4 (16-byte aligned).  Lets a test compare

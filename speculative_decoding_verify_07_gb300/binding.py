@@ -59,6 +59,8 @@ def _load():
     lib.spec_verify.restype = i32
     lib.spec_commit.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
     lib.spec_commit.restype = i32
+    lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_noalloc.restype = i32
     lib.spec_philox4x32_10.argtypes = [vp, u64, vp, ctypes.c_int64, vp]
     lib.spec_philox4x32_10.restype = i32
     lib.spec_status_string.argtypes = [i32]
@@ -169,6 +171,43 @@ def spec_verify(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.T
                          _ptr(workspace), workspace.numel(), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_verify")
+    return out
+
+
+def spec_verify_noalloc(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.Tensor,
+                        seed: int, out: VerifyOutputs | None = None, stream=None) -> VerifyOutputs:
+    """spec_verify with the library's own scratch array instead of a workspace.
+
+    For callers that cannot allocate device scratch; the library allocates
+    nothing either (see spec_verify_noalloc in spec_verify.h for the size
+    limit and for why overlapping calls race).  `out` may be preallocated.
+    """
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, k+1, V]")
+    B, k1, V = logits.shape
+    k = k1 - 1
+    dev = logits.device
+    if logits.dtype == torch.float32:
+        dt = SPEC_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    if k > 0:
+        _check(draft_probs, "draft_probs", torch.float32, (B, k, V), dev)
+        _check(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _check(params, "params", torch.int32, (B, 4), dev)
+    if out is None:
+        out = VerifyOutputs(B, k, dev)
+    rc = LIB.spec_verify_noalloc(_ptr(logits), dt, _ptr(draft_probs) if k > 0 else None,
+                                 _ptr(draft_tokens) if k > 0 else None, _ptr(params),
+                                 ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), B, k, V,
+                                 _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.logprobs),
+                                 _ptr(out.alpha) if k > 0 else None, _ptr(out.flags), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_verify_noalloc")
     return out
 
 

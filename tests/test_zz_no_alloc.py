@@ -1,0 +1,55 @@
+"""The allocation-free verify entry point, checked against spec_verify.
+
+Some callers cannot allocate device memory for the verify step's scratch:
+plugin or custom-op hosts that hand a kernel only its inputs and outputs,
+engines whose allocator has reserved all of HBM, loops that cannot take the
+synchronisation of cudaMalloc.  spec_verify_noalloc serves them from a fixed
+1 MiB array inside the library.  Two calls in a row must give the results of
+spec_verify with a caller-provided workspace, and a batch that needs more
+scratch than the array holds must be refused without launching anything.
+
+This file is collected last so that, if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_verify_07_gb300 import synth
+from tests.gpu_harness import ALPHA_TOL, LP_TOL, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def test_noalloc_matches_spec_verify_on_two_calls():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    inp = synth.make_mixed()                      # 64 rows, k=2, V=151936, bf16
+    logits, q, x, params = to_device(inp)
+    ref = sv.spec_verify(logits, q, x, params, inp.seed)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out = sv.spec_verify_noalloc(logits, q, x, params, inp.seed)
+        torch.cuda.synchronize()
+        assert torch.equal(out.tokens, ref.tokens)
+        assert torch.equal(out.accept_len, ref.accept_len)
+        assert torch.equal(out.flags, ref.flags)
+        assert float((out.logprobs - ref.logprobs).abs().max()) <= LP_TOL
+        assert float((out.alpha - ref.alpha).abs().max()) <= ALPHA_TOL
+
+
+def test_noalloc_refuses_a_batch_beyond_its_scratch():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    B, k, V = 40000, 16, 1000
+    assert sv.workspace_size(B, k, V) > (1 << 20)
+    fake = ctypes.c_void_p(4096)                 # never dereferenced: the size check comes first
+    rc = sv.LIB.spec_verify_noalloc(fake, sv.SPEC_BF16, fake, fake, fake, ctypes.c_uint64(0), B, k, V,
+                                    fake, fake, fake, fake, fake, None)
+    assert rc == sv.SPEC_E_WORKSPACE
