@@ -90,9 +90,9 @@ enum {
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
  * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (a unit-queue counter, a cluster exit counter and one
- * ticket per row) to zero; the per-unit records behind them are rewritten by
- * every call.  So one workspace serves any number of later calls on one
+ * must start at zero (two work-item counters, an exit counter, one ticket
+ * per row, and two tickets and a ready flag per (row, position)) to zero; the
+ * records behind them are rewritten before they are read by every call.  So one workspace serves any number of later calls on one
  * stream; two calls that may run concurrently need two workspaces.           */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
@@ -176,9 +176,10 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
  * library (a file-scope device array, held on every GPU that loads the
  * library until the process exits).  The call allocates nothing.
  *   - Limit: spec_verify_workspace_size(B, k, V) must not exceed
- *     SPEC_NOALLOC_MAX_WORKSPACE (1 MiB: about 32,000 (row, position) units,
- *     e.g. B = 4096 rows at k = 6); a larger batch returns SPEC_E_WORKSPACE
- *     and enqueues nothing.
+ *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 1.1 KB per
+ *     (row, position) unit and 8192-entry vocabulary chunk, so at V = 151936
+ *     about 400 units fit, e.g. 128 rows at k = 2); a larger batch returns
+ *     SPEC_E_WORKSPACE and enqueues nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.
@@ -190,7 +191,7 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
  *     order them on one stream or use spec_verify with separate workspaces.
  * Errors: those of spec_verify, and SPEC_E_WORKSPACE for a batch beyond the
  * limit.                                                                    */
-#define SPEC_NOALLOC_MAX_WORKSPACE (1u << 20)
+#define SPEC_NOALLOC_MAX_WORKSPACE (8u << 20)
 int spec_verify_noalloc(const void* logits, int logits_dtype, const float* draft_probs,
                         const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
                         int B, int k, int V, int32_t* tokens, int32_t* accept_len, float* logprobs,

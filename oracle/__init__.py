@@ -15,7 +15,8 @@ Parity status of each function (what pins it to something other than itself):
                          for tiny vocabularies, the marginal-preservation
                          theorem, chi-square at 40k trials, greedy = argmax,
                          alpha closed form, expected accept length against the
-                         pages' table (tests/test_oracle_chain.py).
+                         pages' table, the two-level race's winner law and its
+                         two-entry closed form (tests/test_oracle_chain.py).
   commit.commit          pinned: explicit per-element loops
                          (tests/test_oracle_commit.py).
 """

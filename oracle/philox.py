@@ -35,7 +35,8 @@ _MASK32 = np.uint64(0xFFFFFFFF)
 
 # Counter word 3 selects the use of a draw.
 STREAM_ACCEPT = 0  # u_j for the accept test of draft j:   ctr = (0, j, row, 0), word 0
-STREAM_RACE = 1    # U_v for the exponential race of v:    ctr = (v >> 2, pos, row, 1), word v & 3
+STREAM_RACE = 1    # U_v for the race inside a block:      ctr = (v >> 2, pos, row, 1), word v & 3
+STREAM_BLOCK = 2   # U_b for the race among blocks:        ctr = (b >> 2, pos, row, 2), word b & 3
 
 
 def seed_key(seed: int) -> tuple[int, int]:
@@ -91,17 +92,19 @@ def accept_uniform(seed: int, row: int, j: int) -> float:
     return float(uniform_from_word(w))
 
 
-def race_words(seed: int, row: int, pos: int, v: np.ndarray) -> np.ndarray:
-    """The race words for vocabulary entries `v` at verify position `pos`."""
+def race_words(seed: int, row: int, pos: int, v: np.ndarray, stream: int = STREAM_RACE) -> np.ndarray:
+    """The race words of indices `v` (vocabulary entries, or blocks with
+    stream=STREAM_BLOCK) at verify position `pos`."""
     v = np.asarray(v, dtype=np.int64)
     blocks = v >> 2
     ctr = np.stack([blocks, np.full_like(blocks, pos), np.full_like(blocks, row),
-                    np.full_like(blocks, STREAM_RACE)], axis=-1)
+                    np.full_like(blocks, stream)], axis=-1)
     out = philox4x32_10(ctr, seed_key(seed))
     return out[np.arange(len(v)), v & 3]
 
 
-def race_exponentials(seed: int, row: int, pos: int, v: np.ndarray) -> np.ndarray:
-    """E_v = -ln U_v, computed as -log1p(-(1 - U_v)) so U_v near 1 keeps full precision."""
-    w = race_words(seed, row, pos, v)
+def race_exponentials(seed: int, row: int, pos: int, v: np.ndarray,
+                      stream: int = STREAM_RACE) -> np.ndarray:
+    """E = -ln U, computed as -log1p(-(1 - U)) so U near 1 keeps full precision."""
+    w = race_words(seed, row, pos, v, stream)
     return -np.log1p(-one_minus_uniform_from_word(w))

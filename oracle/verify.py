@@ -152,29 +152,55 @@ def token_logprob(l: np.ndarray, t: PositionTarget, tok: int, T: float) -> float
     return float((l[tok] - m) / T - t.log_z)
 
 
-def exponential_race(r: np.ndarray, seed: int, row: int, pos: int):
+RACE_BLOCK = 256   # entries per block of the two-level race (READING)
+
+
+def _best_two(s: np.ndarray):
+    """Indices of the largest and second-largest score (first occurrence wins ties)."""
+    i1 = int(np.argmax(s))
+    if len(s) == 1:
+        return i1, -1
+    rest = s.copy()
+    rest[i1] = -np.inf
+    return i1, int(np.argmax(rest))
+
+
+def exponential_race(r: np.ndarray, seed: int, row: int, pos: int, unc: np.ndarray):
     """Gumbel-max draw from the unnormalised weights r [AReno, "Per-step optimizations"].
 
-    Every entry v with r_v > 0 gets E_v = -ln U_v from the Philox stream keyed
-    by (seed, row, position, v); the draw is argmax_v r_v / E_v, which selects
-    v with probability r_v / sum(r) (an exponential race; equivalently
-    argmax log r_v + G_v with Gumbel G_v = -ln E_v).  Ties go to the lowest
-    index (READING).
+    An exponential race: each competitor with weight w > 0 draws E = -ln U
+    from the Philox stream keyed by (seed, row, position) and the largest
+    score w / E wins; competitor i wins with probability w_i / sum(w)
+    (equivalently argmax log w + G with Gumbel G = -ln E).  READING: the race
+    runs in two levels so that only one block of entries needs a random
+    number per entry.  Level 1 races the blocks of RACE_BLOCK consecutive
+    indices with block weights W_b = sum of r over the block (stream 2);
+    level 2 races the entries of the winning block (stream 1).  The product
+    of the two winning probabilities is W_b / sum(W) * r_v / W_b = r_v /
+    sum(r), so the draw is exact.  Ties go to the lower index at both levels.
 
-    Returns (winner, s1, s2, v1, v2) with the best two scores and their entries
-    (s2 = -inf, v2 = -1 when only one entry competes).
+    unc[v] is the magnitude whose relative error of 1e-6 bounds the error of
+    r_v (p + q for a residual, p for a bonus draw); it sets the margin.
+    Returns (winner, margin_flag).
     """
     support = np.nonzero(r > 0)[0]
-    E = philox.race_exponentials(seed, row, pos, support)
-    s = r[support] / E
-    i1 = int(np.argmax(s))                # first maximum = lowest index
-    y = int(support[i1])
-    if len(support) == 1:
-        return y, float(s[i1]), -np.inf, y, -1, E
-    s_rest = s.copy()
-    s_rest[i1] = -np.inf
-    i2 = int(np.argmax(s_rest))
-    return y, float(s[i1]), float(s[i2]), y, int(support[i2]), E[[i1, i2]]
+    blocks = support // RACE_BLOCK
+    ub, inv = np.unique(blocks, return_inverse=True)
+    W = np.bincount(inv, weights=r[support])
+    Wu = np.bincount(inv, weights=unc[support])
+    Eb = philox.race_exponentials(seed, row, pos, ub, stream=philox.STREAM_BLOCK)
+    sb = W / Eb
+    b1, b2 = _best_two(sb)
+    margin = False
+    if b2 >= 0 and sb[b1] - sb[b2] < MARGIN * (Wu[b1] / Eb[b1] + Wu[b2] / Eb[b2]):
+        margin = True
+    inb = support[blocks == ub[b1]]
+    E = philox.race_exponentials(seed, row, pos, inb)
+    s = r[inb] / E
+    i1, i2 = _best_two(s)
+    if i2 >= 0 and s[i1] - s[i2] < MARGIN * (unc[inb[i1]] / E[i1] + unc[inb[i2]] / E[i2]):
+        margin = True
+    return int(inb[i1]), margin
 
 
 def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
@@ -265,13 +291,11 @@ def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
         flags |= F_RESIDUAL_EMPTY
         r = p_a.copy()
         q_a = np.zeros(V)
-    y, s1, s2, v1, v2, E12 = exponential_race(r, seed, row, a)
-    if v2 >= 0:
-        # READING: a draw is uncertain when the best two scores r/E differ by
-        # less than a relative error of MARGIN in p and q would move them.
-        slack = MARGIN * ((p_a[v1] + q_a[v1]) / E12[0] + (p_a[v2] + q_a[v2]) / E12[1])
-        if s1 - s2 < slack:
-            flags |= F_MARGIN_DRAW
+    # READING: a draw is uncertain when the best two scores at either level
+    # differ by less than a relative error of MARGIN in p and q would move them.
+    y, draw_margin = exponential_race(r, seed, row, a, p_a + q_a)
+    if draw_margin:
+        flags |= F_MARGIN_DRAW
 
     for j in range(a):
         tokens[j] = drafts_r[j]

@@ -162,11 +162,14 @@ def test_empty_batch_and_workspace_left_clean():
     for _ in range(3):
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
-    # the counters (256-byte header) and the per-row tickets are back at zero
-    assert int(ws[: 256 + 5 * 4].count_nonzero()) == 0
-    # a dirty record area does not matter: results stay identical
+    # the counters (256-byte header), the per-row tickets and the per-unit
+    # tickets and ready flags (each array padded to 256 bytes) are back at zero
+    B, U = 5, 5 * 4
+    zero_prefix = 256 + 256 * ((B * 4 + 255) // 256) + 3 * 256 * ((U * 4 + 255) // 256)
+    assert int(ws[:zero_prefix].count_nonzero()) == 0
+    # dirty records behind them do not matter: results stay identical
     ref = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
-    ws[512:].fill_(0xAB)
+    ws[zero_prefix:].fill_(0xAB)
     again = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(ref.tokens, again.tokens) and torch.equal(ref.logprobs, again.logprobs)

@@ -134,10 +134,27 @@ def test_exact_enumeration_fixed_drafts():
 
 
 def test_race_closed_form_two_entries():
-    # For two competing weights the race picks entry 0 with probability r0/(r0+r1).
-    r = np.array([0.3, 0.7])
-    wins = sum(ov.exponential_race(r, seed=s, row=0, pos=0)[0] == 0 for s in range(20000))
-    assert abs(wins / 20000 - 0.3) < 5 * np.sqrt(0.21 / 20000)
+    # Two competing weights, in one block and in two blocks: entry a wins with
+    # probability r_a / (r_a + r_b) either way.
+    for b_index in (1, 700):
+        r = np.zeros(b_index + 1)
+        r[0], r[b_index] = 0.3, 0.7
+        wins = sum(ov.exponential_race(r, seed=s, row=0, pos=0, unc=r)[0] == 0 for s in range(20000))
+        assert abs(wins / 20000 - 0.3) < 5 * np.sqrt(0.21 / 20000), b_index
+
+
+def test_two_level_race_samples_the_weights_40k():
+    # Weights spread over three blocks of the two-level race (and several
+    # entries per block): the winner follows r / sum(r).
+    idx = np.array([3, 100, 255, 256, 400, 700, 701])
+    w = np.array([0.05, 0.2, 0.1, 0.15, 0.25, 0.05, 0.2])
+    r = np.zeros(800)
+    r[idx] = w
+    got = np.array([ov.exponential_race(r, seed=s, row=s % 5, pos=s % 3, unc=r)[0] for s in range(40000)])
+    counts = np.array([np.count_nonzero(got == i) for i in idx], dtype=float)
+    assert counts.sum() == 40000
+    tv, pv = _tv_and_chi2(counts, w)
+    assert tv <= 0.015 and pv > 1e-3, (tv, pv)
 
 
 def test_greedy_is_exact_argmax_chain():

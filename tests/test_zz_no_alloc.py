@@ -4,7 +4,7 @@ Some callers cannot allocate device memory for the verify step's scratch:
 plugin or custom-op hosts that hand a kernel only its inputs and outputs,
 engines whose allocator has reserved all of HBM, loops that cannot take the
 synchronisation of cudaMalloc.  spec_verify_noalloc serves them from a fixed
-1 MiB array inside the library.  Two calls in a row must give the results of
+8 MiB array inside the library.  Two calls in a row must give the results of
 spec_verify with a caller-provided workspace, and a batch that needs more
 scratch than the array holds must be refused without launching anything.
 
@@ -47,8 +47,8 @@ def test_noalloc_matches_spec_verify_on_two_calls():
 
 def test_noalloc_refuses_a_batch_beyond_its_scratch():
     from speculative_decoding_verify_07_gb300 import binding as sv
-    B, k, V = 40000, 16, 1000
-    assert sv.workspace_size(B, k, V) > (1 << 20)
+    B, k, V = 4000, 16, 151936
+    assert sv.workspace_size(B, k, V) > (8 << 20)
     fake = ctypes.c_void_p(4096)                 # never dereferenced: the size check comes first
     rc = sv.LIB.spec_verify_noalloc(fake, sv.SPEC_BF16, fake, fake, fake, ctypes.c_uint64(0), B, k, V,
                                     fake, fake, fake, fake, fake, None)
