@@ -1,0 +1,632 @@
+// spec_verify, general path: rows whose kept set needs a global threshold
+// search (top-p without a small top-k, or a top-k above the candidate-list
+// limit).  One CTA settles one (row, position) unit in passes over its logit
+// row (the first from HBM, later ones mostly from L2): max and argmax, an
+// exact rank select for top-k, a fixed-point mass histogram refined to the
+// exact top-p crossing key, the tie rank by index, Z over the kept set, the
+// accept test, alpha, and the two-level exponential race for the draw.  The
+// streaming kernel runs these units first, CTA by CTA, when a batch has any.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify_common.cuh"
+
+namespace specv {
+
+// Shared memory of a CTA on the general path.
+struct alignas(16) GenShm {
+  uint32_t hist[2][256];
+  uint32_t mlo[2][256];
+  uint32_t mhi[2][256];
+  unsigned long long total[256];
+  unsigned long long bc64[8];
+  float wred[kWarps * 8];
+  float bcf[8];
+  int bci[16];
+};
+
+// ---------------------------------------------------------------------------
+// Block reductions (fixed combination order, so results are reproducible).
+// Each returns its result in every thread.
+// ---------------------------------------------------------------------------
+__device__ float block_sum(GenShm& S, float a) {
+  a = warp_sum(a);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) S.wred[w] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float x = 0.f;
+    for (int i = 0; i < kWarps; ++i) x += S.wred[i];
+    S.bcf[7] = x;
+  }
+  __syncthreads();
+  const float r = S.bcf[7];
+  __syncthreads();
+  return r;
+}
+
+__device__ unsigned long long block_max_u64(GenShm& S, unsigned long long v) {
+  v = warp_max_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  unsigned long long* buf = reinterpret_cast<unsigned long long*>(S.wred);
+  if (l == 0) buf[w] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long x = 0;
+    for (int i = 0; i < kWarps; ++i) x = buf[i] > x ? buf[i] : x;
+    S.bc64[7] = x;
+  }
+  __syncthreads();
+  const unsigned long long r = S.bc64[7];
+  __syncthreads();
+  return r;
+}
+
+__device__ unsigned long long block_sum_u64(GenShm& S, unsigned long long v) {
+  v = warp_sum_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  unsigned long long* buf = reinterpret_cast<unsigned long long*>(S.wred);
+  if (l == 0) buf[w] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long x = 0;
+    for (int i = 0; i < kWarps; ++i) x += buf[i];
+    S.bc64[7] = x;
+  }
+  __syncthreads();
+  const unsigned long long r = S.bc64[7];
+  __syncthreads();
+  return r;
+}
+
+__device__ uint2 block_minmax_u32(GenShm& S, uint32_t mn, uint32_t mx) {
+  uint32_t a = ~mn, b = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  uint32_t* wb = reinterpret_cast<uint32_t*>(S.wred);
+  if ((threadIdx.x & 31) == 0) {
+    wb[2 * (threadIdx.x >> 5)] = a;
+    wb[2 * (threadIdx.x >> 5) + 1] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t aa = 0, bb = 0;
+    for (int i = 0; i < kWarps; ++i) {
+      aa = max(aa, wb[2 * i]);
+      bb = max(bb, wb[2 * i + 1]);
+    }
+    S.bci[12] = (int)~aa;
+    S.bci[13] = (int)bb;
+  }
+  __syncthreads();
+  const uint2 r = make_uint2((uint32_t)S.bci[12], (uint32_t)S.bci[13]);
+  __syncthreads();
+  return r;
+}
+
+__device__ Race block_race(GenShm& S, Race r) {
+  warp_race_merge(r);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  float* f = S.wred;
+  if (l == 0) {
+    f[w * 5 + 0] = r.s1;
+    f[w * 5 + 1] = r.t1;
+    f[w * 5 + 2] = r.s2;
+    f[w * 5 + 3] = r.t2;
+    f[w * 5 + 4] = __uint_as_float(r.v1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Race a;
+    race_init(a);
+    for (int i = 0; i < kWarps; ++i) {
+      Race b;
+      b.s1 = f[i * 5 + 0];
+      b.t1 = f[i * 5 + 1];
+      b.s2 = f[i * 5 + 2];
+      b.t2 = f[i * 5 + 3];
+      b.v1 = __float_as_uint(f[i * 5 + 4]);
+      b.s1lo = 0.f;
+      race_merge(a, b);
+    }
+    S.bcf[0] = a.s1;
+    S.bcf[1] = a.t1;
+    S.bcf[2] = a.s2;
+    S.bcf[3] = a.t2;
+    S.bci[0] = (int)a.v1;
+  }
+  __syncthreads();
+  Race o;
+  o.s1 = S.bcf[0];
+  o.t1 = S.bcf[1];
+  o.s2 = S.bcf[2];
+  o.t2 = S.bcf[3];
+  o.v1 = (uint32_t)S.bci[0];
+  o.s1lo = 0.f;
+  __syncthreads();
+  return o;
+}
+
+// Histogram selection on S.total (bin 0 = the top of the order): the bin
+// where the cumulative weight from bin 0 reaches `need`, and the weight of
+// the bins before it.  Warp 0 scans; the result is broadcast.
+__device__ void select_from_bin0(GenShm& S, unsigned long long need, int* out_bin,
+                                 unsigned long long* out_above) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned long long own = 0;
+    for (int i = 0; i < 8; ++i) own += S.total[8 * lane + i];
+    unsigned long long inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const unsigned long long exc = inc - own;
+    const unsigned ball = __ballot_sync(0xffffffffu, inc >= need);
+    const int src = ball ? (__ffs(ball) - 1) : 31;
+    if (lane == src) {
+      unsigned long long above = exc;
+      int chosen = 8 * lane + 7;
+      for (int i = 0; i < 8; ++i) {
+        const unsigned long long t = S.total[8 * lane + i];
+        if (above + t >= need || i == 7) {
+          chosen = 8 * lane + i;
+          break;
+        }
+        above += t;
+      }
+      S.bci[2] = chosen;
+      S.bc64[1] = above;
+    }
+  }
+  __syncthreads();
+  *out_bin = S.bci[2];
+  *out_above = S.bc64[1];
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Rank select on distances from the maximum (one CTA).  Values are described
+// by d = key(max) - key(v) >= 0 in the order-key space, so the largest values
+// have the smallest distances.  Finds the distance of the value at 1-based
+// rank `need` (counting multiplicity) among the values `each` enumerates.
+// The first histogram gives every distance below 255 << s0 its own bin and
+// lumps the tail without an atomic; the chosen bin is refined 8 bits at a
+// time; a rank in the tail falls back to a top-down radix over all bits.  On
+// return `need` is the rank inside the group at exactly that distance.
+// ---------------------------------------------------------------------------
+template <typename Each>
+__device__ uint32_t kth_distance(GenShm& S, Each each, unsigned long long& need, int s0, int dbits) {
+  auto reduce = [&](int slot) {
+    S.total[threadIdx.x] = S.hist[slot][threadIdx.x];
+    __syncthreads();
+  };
+  int hs = 0;
+  {
+    const int slot = hs++ & 1;
+    S.hist[slot][threadIdx.x] = 0;
+    __syncthreads();
+    const uint32_t lim = 255u << s0;
+    each([&](uint32_t d) {
+      if (d < lim) atomicAdd(&S.hist[slot][d >> s0], 1u);
+    });
+    __syncthreads();
+    reduce(slot);
+    int b;
+    unsigned long long below;
+    select_from_bin0(S, need, &b, &below);
+    if (b < 255) {
+      need -= below;
+      uint32_t base = (uint32_t)b << s0;
+      for (int s = s0 - 8; s >= 0; s -= 8) {
+        const int sl = hs++ & 1;
+        S.hist[sl][threadIdx.x] = 0;
+        __syncthreads();
+        const uint32_t span = 1u << (s + 8);
+        each([&](uint32_t d) {
+          if (d >= base && d - base < span) atomicAdd(&S.hist[sl][(d - base) >> s], 1u);
+        });
+        __syncthreads();
+        reduce(sl);
+        int bb;
+        unsigned long long bl;
+        select_from_bin0(S, need, &bb, &bl);
+        need -= bl;
+        base += (uint32_t)bb << s;
+      }
+      return base;
+    }
+  }
+  uint32_t prefix = 0u, mask = 0u;
+  for (int shift = dbits - 8; shift >= 0; shift -= 8) {
+    const int slot = hs++ & 1;
+    S.hist[slot][threadIdx.x] = 0;
+    __syncthreads();
+    each([&](uint32_t d) {
+      if ((d & mask) == prefix) atomicAdd(&S.hist[slot][(d >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    reduce(slot);
+    int b;
+    unsigned long long below;
+    select_from_bin0(S, need, &b, &below);
+    need -= below;
+    prefix |= (uint32_t)b << shift;
+    mask |= 255u << shift;
+  }
+  return prefix;
+}
+
+// Exact fixed-point mass accumulation with native 32-bit shared atomics: the
+// low word wraps, and the atomic that wraps it carries one into the high word.
+__device__ __forceinline__ void mass_add(uint32_t* lo, uint32_t* hi, unsigned long long fx) {
+  const uint32_t l = (uint32_t)fx;
+  const uint32_t h = (uint32_t)(fx >> 32);
+  const uint32_t old = atomicAdd(lo, l);
+  const uint32_t carry = (old + l < old) ? 1u : 0u;
+  if (h + carry) atomicAdd(hi, h + carry);
+}
+__device__ __forceinline__ unsigned long long mass_fixed(float e) {
+  return __float2ull_rz(e * 1099511627776.0f);   // e * 2^40, e in [0, 1]
+}
+
+// Level 1 over a whole row, one CTA: every warp-row of 32 groups is one race
+// block.  Returns the winning block's race state (v1 = block) in every thread.
+template <bool kBF16>
+__device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
+                                const Thresh* th) {
+  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  const int G = (A.V + 7) / 8;
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  Race r;
+  race_init(r);
+  for (int base = 0; base < G; base += kThreads) {
+    const int g = base + threadIdx.x;
+    float w8 = 0.f, u8 = 0.f;
+    if (g < G) {
+      float w[8], tq[8];
+      race_weights<kBF16>(A, lrow, qrow, g, m, c, invZ, mode, th, w, tq);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (w[j] > 0.f) {
+          w8 += w[j];
+          u8 += w[j] + tq[j];
+        }
+    }
+    const float W = warp_sum(w8), U = warp_sum(u8);
+    if (lane == 0 && W > 0.f) {
+      const uint32_t b = (uint32_t)(base / (kRaceBlock / 8) + wp);
+      race_consider(r, W, U - W, b, block_word(A, row, pos, b));
+    }
+  }
+  return block_race(S, r);
+}
+
+// The full two-level draw over a row by one CTA; returns the drawn entry
+// (or 0xffffffff when every weight is 0) and sets *margin.
+template <bool kBF16>
+__device__ uint32_t draw_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
+                             const Thresh* th, bool* margin) {
+  const Race l1 = race_blocks_row<kBF16>(A, S, row, pos, m, c, invZ, mode, th);
+  if (l1.s1 < 0.f) {
+    *margin = false;
+    return 0xffffffffu;
+  }
+  if (threadIdx.x < 32) {
+    const Race l2 = race_in_block<kBF16>(A, row, pos, l1.v1, m, c, invZ, mode, th);
+    if (threadIdx.x == 0) {
+      S.bci[8] = (int)l2.v1;
+      S.bci[9] = (draw_margin(l1) || draw_margin(l2)) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  const uint32_t y = (uint32_t)S.bci[8];
+  *margin = S.bci[9] != 0;
+  __syncthreads();
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// The general path: one CTA settles a unit whose kept set needs a global
+// threshold (top-p without a small top-k, or a large top-k), in passes over
+// the logit row (the first from HBM, later ones mostly from L2).  The kept
+// set is a prefix of the total order, described by a Thresh.
+// ---------------------------------------------------------------------------
+
+// Index of the n-th (1-based) entry of the row, in index order, whose order
+// key is tkey; 0xffffffff when there are fewer.
+template <bool kBF16>
+__device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_t tkey, unsigned long long n) {
+  const int G = (A.V + 7) / 8;
+  unsigned long long need = n;
+  uint32_t found = 0xffffffffu;
+  for (int base = 0; base < G; base += kThreads) {
+    const int g = base + threadIdx.x;
+    int c = 0;
+    float v[8];
+    if (g < G) {
+      load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (g * 8 + i < A.V && okey(v[i]) == tkey) ++c;
+    }
+    int inc = c;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    int* wsum = reinterpret_cast<int*>(S.wred);
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    int woff = 0, rowtot = 0;
+    for (int i = 0; i < kWarps; ++i) {
+      if (i < w) woff += wsum[i];
+      rowtot += wsum[i];
+    }
+    const int exc = woff + inc - c;
+    if (c > 0 && need > (unsigned long long)exc && need <= (unsigned long long)(exc + c)) {
+      int want = (int)(need - exc);
+      for (int i = 0; i < 8; ++i) {
+        if (g * 8 + i < A.V && okey(v[i]) == tkey && --want == 0) {
+          S.bci[3] = g * 8 + i;
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    if (need <= (unsigned long long)rowtot) {
+      found = (uint32_t)S.bci[3];
+      __syncthreads();
+      break;
+    }
+    need -= (unsigned long long)rowtot;
+    __syncthreads();
+  }
+  return found;
+}
+
+template <bool kBF16>
+__device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int row, int pos, const RowCfg& cfg) {
+  const size_t lrow = (size_t)u * A.V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  const bool has_q = pos < A.k;
+  const int G = (A.V + 7) / 8;
+  // pass 1: max, argmax, NaN
+  unsigned long long best = 0;
+  bool nan_seen = false;
+  for (int g = threadIdx.x; g < G; g += kThreads) {
+    float v[8];
+    load_group<kBF16>(A, lrow, g, true, v);
+    const float gm = group_max(v);
+    if (gm != gm) {
+      nan_seen = true;
+    } else if (best == 0 || gm > from_okey((uint32_t)(best >> 32))) {
+      int first = 0;
+#pragma unroll
+      for (int i = 7; i >= 0; --i)
+        if (v[i] == gm) first = i;
+      best = key64(okey(gm), (uint32_t)(g * 8 + first));
+    }
+  }
+  if (nan_seen) best = ~0ull;
+  best = block_max_u64(S, best);
+  const float m = from_okey((uint32_t)(best >> 32));
+  const int am = (int)key64_idx(best);
+  if (best == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
+    if (threadIdx.x == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    __syncthreads();
+    return;
+  }
+  uint32_t flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
+  const float c = cfg.c;
+  const uint32_t km = kf<kBF16>(m);
+
+  // top-k threshold
+  Thresh th;
+  th.tkey = 0u;
+  th.tidx = 0xffffffffu;
+  if (cfg.K > 0) {
+    unsigned long long need = (unsigned long long)cfg.K;
+    auto each = [&](auto fn) {
+      for (int g = threadIdx.x; g < G; g += kThreads) {
+        float v[8];
+        load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (g * 8 + i < A.V) fn(km - kf<kBF16>(v[i]));
+      }
+    };
+    const uint32_t d = kth_distance(S, each, need, kBF16 ? 0 : 16, kBF16 ? 16 : 32);
+    th.tkey = full_key<kBF16>(km - d);
+    th.tidx = nth_tie_index<kBF16>(A, S, lrow, th.tkey, need);
+  }
+  const bool topp = cfg.P < 1.0f;
+
+  // Z pass over the top-k set; with top-p also a fixed-point mass histogram
+  // binned by log2 of the weight in steps of 1/8 (the last bin in registers).
+  const int hslot = 0;
+  S.mlo[hslot][threadIdx.x] = 0;
+  S.mhi[hslot][threadIdx.x] = 0;
+  __syncthreads();
+  unsigned long long tail = 0;
+  float z0 = 0.f, z1 = 0.f;
+  for (int g = threadIdx.x; g < G; g += kThreads) {
+    float v[8];
+    load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float x = (v[i] - m) * c;
+      const bool in = (g * 8 + i < A.V) && (cfg.K == 0 || kept(th, okey(v[i]), (uint32_t)(g * 8 + i)));
+      const float e = in ? ex2(x) : 0.f;
+      if (i & 1) z1 += e; else z0 += e;
+      if (topp && e > 0.f) {
+        const int bin = __float2int_rz(fminf(-x * 8.0f, 255.0f));
+        const unsigned long long fx = mass_fixed(e);
+        if (bin < 255) mass_add(&S.mlo[hslot][bin], &S.mhi[hslot][bin], fx);
+        else tail += fx;
+      }
+    }
+  }
+  float Zs;
+  if (topp) {
+    __syncthreads();
+    tail = block_sum_u64(S, tail);
+    if (threadIdx.x == 0) {
+      S.mlo[hslot][255] = (uint32_t)tail;
+      S.mhi[hslot][255] = (uint32_t)(tail >> 32);
+    }
+    __syncthreads();
+    S.total[threadIdx.x] = ((unsigned long long)S.mhi[hslot][threadIdx.x] << 32) + S.mlo[hslot][threadIdx.x];
+    __syncthreads();
+    const unsigned long long zk = block_sum_u64(S, S.total[threadIdx.x]);
+    const unsigned long long target = (unsigned long long)ceil((double)cfg.P * (double)zk);
+    int b;
+    unsigned long long above;
+    select_from_bin0(S, target, &b, &above);
+    // key range of bin b
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+      float v[8];
+      load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (g * 8 + i >= A.V) continue;
+        const uint32_t key = okey(v[i]);
+        if (cfg.K > 0 && !kept(th, key, (uint32_t)(g * 8 + i))) continue;
+        const float x = (v[i] - m) * c;
+        if (!(ex2(x) > 0.f)) continue;
+        if (__float2int_rz(fminf(-x * 8.0f, 255.0f)) == b) {
+          kmin = min(kmin, key);
+          kmax = max(kmax, key);
+        }
+      }
+    }
+    const uint2 mm = block_minmax_u32(S, kmin, kmax);
+    uint32_t lo = mm.x, hi = mm.y;
+    unsigned long long rem = target - above;
+    int hs = 1;
+    while (hi > lo) {
+      const uint32_t span = hi - lo;
+      const int nbits = 32 - __clz(span);
+      const int shift = nbits > 8 ? nbits - 8 : 0;
+      const int slot = hs++ & 1;
+      S.mlo[slot][threadIdx.x] = 0;
+      S.mhi[slot][threadIdx.x] = 0;
+      __syncthreads();
+      for (int g = threadIdx.x; g < G; g += kThreads) {
+        float v[8];
+        load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (g * 8 + i >= A.V) continue;
+          const uint32_t key = okey(v[i]);
+          if (key < lo || key > hi) continue;
+          if (cfg.K > 0 && !kept(th, key, (uint32_t)(g * 8 + i))) continue;
+          const uint32_t bin = (hi - key) >> shift;
+          mass_add(&S.mlo[slot][bin], &S.mhi[slot][bin], mass_fixed(ex2((v[i] - m) * c)));
+        }
+      }
+      __syncthreads();
+      S.total[threadIdx.x] = ((unsigned long long)S.mhi[slot][threadIdx.x] << 32) + S.mlo[slot][threadIdx.x];
+      __syncthreads();
+      int sb;
+      unsigned long long ab;
+      select_from_bin0(S, rem, &sb, &ab);
+      rem -= ab;
+      above += ab;
+      const uint32_t nhi = hi - ((uint32_t)sb << shift);
+      const uint32_t span_lo = ((uint32_t)(sb + 1) << shift) - 1u;
+      const uint32_t nlo = (hi - lo > span_lo) ? max(lo, hi - span_lo) : lo;
+      hi = nhi;
+      lo = max(nlo, lo);
+      if (shift == 0) lo = hi;
+    }
+    const uint32_t tkey = hi;
+    const float et = ex2((from_okey(tkey) - m) * c);
+    const unsigned long long efx = mass_fixed(et);
+    unsigned long long n_need = efx ? (rem + efx - 1) / efx : 1ull;
+    if (n_need == 0) n_need = 1;
+    // with a top-k threshold at the same key, the ties top-k keeps are a
+    // prefix of the ties in index order, so the rank carries over
+    th.tidx = nth_tie_index<kBF16>(A, S, lrow, tkey, n_need);
+    th.tkey = tkey;
+    const unsigned long long zs_fx = above + n_need * efx;
+    Zs = (float)((double)zs_fx * (1.0 / 1099511627776.0));
+    const double at = (double)zs_fx / (double)zk;
+    const double bef = (double)(zs_fx - efx) / (double)zk;
+    if (fabs(at - (double)cfg.P) < 1e-6 || fabs((double)cfg.P - bef) < 1e-6) flags |= SPEC_F_MARGIN_TOPP;
+  } else {
+    Zs = block_sum(S, z0 + z1);
+  }
+  const float invZ = 1.0f / Zs;
+  const float lnZ = logf(Zs);
+
+  // accept test (every thread computes the same)
+  AcceptInfo ai;
+  ai.accept = false;
+  ai.valid = true;
+  ai.margin = false;
+  ai.lx = 0.f;
+  bool need_race = !has_q;
+  if (has_q) {
+    ai = accept_test(A, row, pos, kBF16, false, am, m, c, Zs, &th);
+    need_race = !ai.accept;
+  }
+  // alpha pass
+  float al0 = 0.f, al1 = 0.f;
+  if (has_q) {
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+      float v[8], qv[8];
+      load_group<kBF16>(A, lrow, g, true, v);
+      load_q8(A, qrow, g * 8, qv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool in = (g * 8 + i < A.V) && kept(th, okey(v[i]), (uint32_t)(g * 8 + i));
+        const float p = in ? ex2((v[i] - m) * c) * invZ : 0.f;
+        if (i & 1) al1 += fminf(p, qv[i]); else al0 += fminf(p, qv[i]);
+      }
+    }
+  }
+  const float alpha_v = has_q ? block_sum(S, al0 + al1) : 0.f;
+  // the draw: residual after a rejection, p at the bonus position
+  uint32_t draw_flags = 0;
+  uint32_t y = 0xffffffffu;
+  if (need_race) {
+    bool mg = false;
+    y = draw_row<kBF16>(A, S, row, pos, m, c, invZ, has_q ? RW_RESIDUAL : RW_BONUS, &th, &mg);
+    if (y == 0xffffffffu) {
+      draw_flags |= SPEC_F_RESIDUAL_EMPTY;
+      y = draw_row<kBF16>(A, S, row, pos, m, c, invZ, RW_P, &th, &mg);
+    }
+    if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
+  }
+  if (threadIdx.x == 0) {
+    UnitRecord rec = empty_record(flags);
+    if (has_q) {
+      if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
+      if (ai.margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
+      rec.accept = ai.accept ? 1 : 0;
+      rec.lp_x = ai.valid ? (ai.lx - m) * cfg.invT - lnZ : 0.f;
+      rec.alpha = alpha_v;
+    }
+    if (need_race) {
+      const uint32_t yy = y < (uint32_t)A.V ? y : (uint32_t)am;
+      rec.y = (int32_t)yy;
+      rec.lp_y = (load_logit(A, kBF16, lrow + yy) - m) * cfg.invT - lnZ;
+      rec.draw_flags = draw_flags;
+    }
+    commit_record(A, u, row, rec);
+  }
+  __syncthreads();
+}
+
+}  // namespace specv

@@ -1,0 +1,503 @@
+// Device-side pieces shared by the verify kernels (sm_103a): workspace
+// layout, kernel arguments, row classification, loads, the accept test, the
+// exponential race and the per-row finalize.
+//
+// Method: inclusionAI/AReno PR #550, "feat(engine): MTP training loss and
+// speculative decoding for bailing_v3", "What does this PR do?" Phase 2
+// (sampler-equivalent target distribution, exact chain rejection sampling,
+// unchanged logprobs), table "Per-step optimizations" (Gumbel-max draws,
+// one-pass logprobs, no host syncs) and table "On-policy accept probability"
+// (alpha = sum min(p, q)).  Ties follow InfiniTensor/InfiniLM PR #588, "feat:
+// add mtp draft models for speculative decoding", section 4.1 (exact bf16
+// ties flip argmax between kernel paths, so the order is defined: larger
+// logit first, then smaller index).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/spec_verify.h"
+#include "spec_device.cuh"
+
+namespace specv {
+
+constexpr int kRaceBlock = 256;            // entries per block of the two-level race
+constexpr int kTopkSmall = 128;            // top_k <= this: candidate-list path
+constexpr long long kSpinLimit = 1ll << 22;
+
+// Streaming geometry.  Every warp of the streaming kernel owns two buffers
+// of kSlot bytes; an A item is one buffer of logits, a B item one buffer of
+// logits plus the matching draft probabilities.  Items cover whole race
+// blocks of 256 entries.
+constexpr int kSlot = 12288;
+template <bool kBF16>
+struct Geo {
+  static constexpr int es = kBF16 ? 2 : 4;                         // logit bytes
+  static constexpr int EA = kSlot / es;                            // A item entries (6144 / 3072)
+  static constexpr int EB = (kSlot / (es + 4)) / kRaceBlock * kRaceBlock;   // B item entries (2048 / 1536)
+  static constexpr int NBA = EA / kRaceBlock;                      // blocks per A item
+  static constexpr int NBB = EB / kRaceBlock;                      // blocks per B item
+  static constexpr int SPI = EA / 64;                              // 64-entry super-groups per A item
+};
+
+enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
+
+struct WsHeader {
+  uint32_t next;          // next streaming ticket
+  uint32_t ctas_done;     // CTAs that left the kernel
+  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait gave up
+  uint32_t pad0;
+  uint32_t n_class[4];    // rows per class (written by the plan kernel for large batches)
+  uint32_t gnext;         // next general-path unit
+  uint32_t pad[55];
+};
+
+struct ChunkRec {         // 48 bytes, one per (unit, A item)
+  float m;                // chunk max (NaN when the chunk holds a NaN)
+  uint32_t amax;          // first index of the chunk max
+  float z;                // sum of exp((l - m_chunk) * c)
+  uint32_t pad0;
+  float s1, t1, s2, t2;   // level-1 race over the chunk's blocks, relative to the chunk max (bonus units)
+  uint32_t v1;
+  uint32_t pad[3];
+};
+
+struct UnitState {        // 32 bytes: what the B items of a drafted unfiltered unit need
+  float m, invZ, lnZ, lp_x;
+  int32_t accept;
+  uint32_t flags;         // BAD_TOKEN | MARGIN_ACCEPT | BAD_PARAM of this unit
+  uint32_t invalid;       // the unit is invalid (NaN); its record is already written
+  int32_t am;
+};
+
+struct BRec {             // 32 bytes per (unit, B item)
+  float alpha, s1, t1, s2, t2;
+  uint32_t v1;
+  uint32_t pad[2];
+};
+
+struct UnitRecord {       // 32 bytes, one per unit, read by the row finaliser
+  uint32_t flags;
+  int32_t accept;
+  float lp_x;
+  float alpha;
+  int32_t y;
+  float lp_y;
+  uint32_t draw_flags;
+  uint32_t pad;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Per-unit record counts, sized for the larger of the two logit dtypes.
+__host__ __device__ inline int max_nca(int V) { return ceil_div(V, Geo<false>::EA); }
+__host__ __device__ inline int max_ncb(int V) { return ceil_div(V, Geo<false>::EB); }
+__host__ __device__ inline int max_nsm(int V) {
+  const int a = ceil_div(V, Geo<true>::EA) * Geo<true>::SPI;
+  const int b = ceil_div(V, Geo<false>::EA) * Geo<false>::SPI;
+  return a > b ? a : b;
+}
+
+struct Layout {
+  size_t row_ticket, a_ticket, b_ticket, ready, crec, ust, brec, urec, smax, order, total;
+};
+
+__host__ __device__ inline Layout ws_layout(int B, int k, int V) {
+  const size_t U = (size_t)B * (k + 1);
+  Layout L;
+  size_t off = sizeof(WsHeader);
+  L.row_ticket = off; off = align_up(off + (size_t)B * 4, 256);
+  L.a_ticket = off; off = align_up(off + U * 4, 256);
+  L.b_ticket = off; off = align_up(off + U * 4, 256);
+  L.ready = off; off = align_up(off + U * 4, 256);
+  L.crec = off; off = align_up(off + U * max_nca(V) * sizeof(ChunkRec), 256);
+  L.ust = off; off = align_up(off + U * sizeof(UnitState), 256);
+  L.brec = off; off = align_up(off + U * max_ncb(V) * sizeof(BRec), 256);
+  L.urec = off; off = align_up(off + U * sizeof(UnitRecord), 256);
+  L.smax = off; off = align_up(off + U * max_nsm(V) * 4, 256);
+  L.order = off; off = align_up(off + (size_t)B * 4, 256);
+  L.total = off;
+  return L;
+}
+
+struct Args {
+  const void* logits;
+  const float* q;
+  const int32_t* drafts;
+  const spec_params_t* params;
+  int32_t* tokens;
+  int32_t* accept_len;
+  float* logprobs;
+  float* alpha;
+  uint32_t* flags;
+  WsHeader* ws;
+  uint32_t* row_ticket;
+  uint32_t* a_ticket;
+  uint32_t* b_ticket;
+  uint32_t* ready;
+  ChunkRec* crec;
+  UnitState* ust;
+  BRec* brec;
+  UnitRecord* urec;
+  float* smax;
+  uint32_t* order;        // rows by class, for batches too large for shared memory
+  uint32_t key0, key1;
+  int B, k, V, U;
+  int NCA, NCB, NSM;      // record strides per unit: A items, B items, super-group maxima
+  int n_ctas;             // streaming CTAs
+  int global_order;       // the row order comes from the plan kernel
+  int vec_logits;
+  int vec_q;
+};
+
+// ---------------------------------------------------------------------------
+// Row configuration.
+// ---------------------------------------------------------------------------
+struct RowCfg {
+  int type;
+  bool bad_param;
+  int K;        // active top-k (0 = off)
+  float P;      // active top-p (1 = off)
+  float c;      // log2(e) / T (log2(e) for greedy)
+  float invT;   // 1 / T (1 for greedy)
+};
+
+__device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
+  RowCfg r;
+  const float T = prm.temperature;
+  const float P = prm.top_p;
+  const bool T_ok = (T == 0.0f) || (isfinite(T) && T >= 1.17549435e-38f);
+  const bool P_ok = isfinite(P) && P > 0.0f && P <= 1.0f;
+  r.bad_param = !(T_ok && P_ok);
+  const bool greedy = r.bad_param || T == 0.0f;
+  r.K = (prm.top_k > 0 && prm.top_k < V) ? prm.top_k : 0;
+  r.P = (greedy || P >= 1.0f) ? 1.0f : P;
+  r.c = greedy ? kLog2e : kLog2e / T;
+  r.invT = greedy ? 1.0f : 1.0f / T;
+  if (greedy) r.type = UT_GREEDY;
+  else if (r.K > 0 && r.K <= kTopkSmall) r.type = UT_TOPK;
+  else if (r.K == 0 && r.P >= 1.0f) r.type = UT_DENSE;
+  else r.type = UT_GENERAL;
+  return r;
+}
+
+// Row configuration packed in 16 bytes (kept in shared memory per row).
+struct RowPack {
+  float c, invT, P;
+  uint32_t tk;            // type | bad_param << 2 | K << 8
+};
+__device__ __forceinline__ RowPack pack_cfg(const RowCfg& r) {
+  RowPack p;
+  p.c = r.c;
+  p.invT = r.invT;
+  p.P = r.P;
+  p.tk = (uint32_t)r.type | (r.bad_param ? 4u : 0u) | ((uint32_t)r.K << 8);
+  return p;
+}
+__device__ __forceinline__ RowCfg unpack_cfg(const RowPack& p) {
+  RowCfg r;
+  r.c = p.c;
+  r.invT = p.invT;
+  r.P = p.P;
+  r.type = (int)(p.tk & 3u);
+  r.bad_param = (p.tk & 4u) != 0;
+  r.K = (int)(p.tk >> 8);
+  return r;
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t kf(float v) {
+  return kBF16 ? (okey(v) >> 16) : okey(v);
+}
+template <bool kBF16>
+__device__ __forceinline__ uint32_t full_key(uint32_t k) {
+  if (!kBF16) return k;
+  return (k << 16) | ((k & 0x8000u) ? 0u : 0xffffu);
+}
+
+// ---------------------------------------------------------------------------
+// Loading logits and draft probabilities.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_logit(const Args& A, bool bf16, size_t off) {
+  if (bf16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(A.logits)[off] << 16);
+  return reinterpret_cast<const float*>(A.logits)[off];
+}
+
+// Eight values of group g (entries 8g..8g+7) of a logit row; entries past V
+// read as -inf.  keep: leave the lines in L2 for a later re-read.
+template <bool kBF16>
+__device__ __forceinline__ void load_group(const Args& A, size_t lrow, int g, bool keep, float v[8]) {
+  const int e0 = g * 8;
+  if (kBF16) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(A.logits) + lrow;
+    uint4 w;
+    if (A.vec_logits && e0 + 8 <= A.V) {
+      const uint4* p4 = reinterpret_cast<const uint4*>(p + e0);
+      w = keep ? __ldcg(p4) : __ldcs(p4);
+    } else {
+      uint32_t h[8];
+      for (int i = 0; i < 8; ++i) h[i] = (e0 + i < A.V) ? p[e0 + i] : 0xff80u;
+      w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    }
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+  } else {
+    const float* p = reinterpret_cast<const float*>(A.logits) + lrow;
+    if (A.vec_logits && e0 + 8 <= A.V) {
+      const float4* p4 = reinterpret_cast<const float4*>(p + e0);
+      const float4 a = keep ? __ldcg(p4) : __ldcs(p4);
+      const float4 b = keep ? __ldcg(p4 + 1) : __ldcs(p4 + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+      for (int i = 0; i < 8; ++i) v[i] = (e0 + i < A.V) ? p[e0 + i] : -INFINITY;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_q8(const Args& A, size_t qrow, int e0, float qv[8]) {
+  const float* p = A.q + qrow;
+  if (A.vec_q && e0 + 8 <= A.V) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p + e0));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p + e0 + 4));
+    qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w;
+    qv[4] = b.x; qv[5] = b.y; qv[6] = b.z; qv[7] = b.w;
+  } else {
+    for (int i = 0; i < 8; ++i) qv[i] = (e0 + i < A.V) ? p[e0 + i] : 0.f;
+  }
+}
+
+__device__ __forceinline__ float group_max(const float v[8]) {
+  return max_nan(max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])),
+                 max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7])));
+}
+
+// ---------------------------------------------------------------------------
+// Records and the per-row finalize.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ void finalize_row(const Args& A, int row) {
+  const int k = A.k;
+  const UnitRecord* R = A.urec + (size_t)row * (k + 1);
+  uint32_t uflags = 0;
+  bool invalid = false;
+  for (int j = 0; j <= k; ++j) {
+    const uint32_t f = __ldcg(&R[j].flags);
+    uflags |= f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP);
+    invalid |= (f & SPEC_F_NAN) != 0;
+  }
+  int32_t* tok = A.tokens + (size_t)row * (k + 1);
+  float* lp = A.logprobs + (size_t)row * (k + 1);
+  if (invalid) {
+    for (int j = 0; j <= k; ++j) {
+      tok[j] = -1;
+      lp[j] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) A.alpha[(size_t)row * k + j] = 0.f;
+    A.accept_len[row] = 0;
+    A.flags[row] = SPEC_F_NAN;
+    return;
+  }
+  int a = k;
+  for (int j = 0; j < k; ++j) {
+    uflags |= __ldcg(&R[j].flags) & SPEC_F_MARGIN_ACCEPT;
+    if (!__ldcg(&R[j].accept)) {
+      a = j;
+      break;
+    }
+  }
+  for (int j = 0; j < a; ++j) {
+    tok[j] = A.drafts[(size_t)row * k + j];
+    lp[j] = __ldcg(&R[j].lp_x);
+  }
+  tok[a] = __ldcg(&R[a].y);
+  lp[a] = __ldcg(&R[a].lp_y);
+  uflags |= __ldcg(&R[a].draw_flags);
+  for (int j = a + 1; j <= k; ++j) {
+    tok[j] = -1;
+    lp[j] = 0.f;
+  }
+  for (int j = 0; j < k; ++j) A.alpha[(size_t)row * k + j] = __ldcg(&R[j].alpha);
+  A.accept_len[row] = a + 1;
+  A.flags[row] = uflags;
+}
+
+// One thread: publish a unit's record; the last unit of the row finalizes it.
+static __device__ __noinline__ void commit_record(const Args& A, int u, int row, const UnitRecord& rec) {
+  A.urec[u] = rec;
+  const uint32_t old = atomic_add_acq_rel(&A.row_ticket[row], 1u);
+  if (old == (uint32_t)A.k) {
+    finalize_row(A, row);
+    A.row_ticket[row] = 0;   // leave the workspace clean for the next call
+  }
+}
+
+__device__ __forceinline__ UnitRecord empty_record(uint32_t flags) {
+  UnitRecord r;
+  r.flags = flags;
+  r.accept = 0;
+  r.lp_x = 0.f;
+  r.alpha = 0.f;
+  r.y = -1;
+  r.lp_y = 0.f;
+  r.draw_flags = 0;
+  r.pad = 0;
+  return r;
+}
+
+struct AcceptInfo {
+  bool valid, accept, margin;
+  int x;
+  float px, qx, lx;
+};
+
+// Accept test of the draft at (row, pos): accept iff u*q(x) < p(x), with the
+// sign of u*q - p taken exactly by one fma.  p(x) = exp((l_x - m) / T) / Z
+// when x is kept (kept_th == nullptr keeps everything); greedy: p(x) = 1 if
+// x is the argmax, else 0.
+struct Thresh {
+  uint32_t tkey;
+  uint32_t tidx;
+};
+__device__ __forceinline__ bool kept(const Thresh& t, uint32_t key, uint32_t v) {
+  return key > t.tkey || (key == t.tkey && v <= t.tidx);
+}
+
+static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, int pos, bool bf16, bool greedy, int am,
+                                  float m, float c, float Zs, const Thresh* kept_th) {
+  AcceptInfo ai;
+  ai.x = A.drafts[(size_t)row * A.k + pos];
+  ai.valid = ai.x >= 0 && ai.x < A.V;
+  ai.lx = 0.f;
+  ai.px = 0.f;
+  ai.qx = 0.f;
+  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  if (ai.valid) {
+    ai.lx = load_logit(A, bf16, lrow + ai.x);
+    ai.qx = A.q[qrow + ai.x];
+    if (greedy) {
+      ai.px = (ai.x == am) ? 1.0f : 0.0f;
+    } else {
+      const bool in = kept_th ? kept(*kept_th, okey(ai.lx), (uint32_t)ai.x) : true;
+      ai.px = in ? ex2((ai.lx - m) * c) / Zs : 0.0f;
+    }
+  }
+  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
+  const float u = uniform_of(w.x);
+  const float d = fmaf(u, ai.qx, -ai.px);
+  ai.accept = d < 0.0f;
+  ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
+  return ai;
+}
+
+__device__ __forceinline__ uint32_t race_word(const Args& A, int row, int pos, uint32_t v) {
+  const uint4 w = philox4x32_10(make_uint4(v >> 2, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
+  return word_of(w, v & 3);
+}
+
+// Race over the 8 weights of one group (two Philox blocks), skipping empty halves.
+__device__ __forceinline__ void race_group(const Args& A, int row, int pos, int e0, const float w[8],
+                                           const float tq[8], Race& r) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float* wh = w + 4 * h;
+    if (wh[0] > 0.f || wh[1] > 0.f || wh[2] > 0.f || wh[3] > 0.f) {
+      const uint32_t blk = (uint32_t)((e0 >> 2) + h);
+      const uint4 ww = philox4x32_10(make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
+      if (wh[0] > 0.f) race_consider(r, wh[0], tq[4 * h + 0], blk * 4 + 0, ww.x);
+      if (wh[1] > 0.f) race_consider(r, wh[1], tq[4 * h + 1], blk * 4 + 1, ww.y);
+      if (wh[2] > 0.f) race_consider(r, wh[2], tq[4 * h + 2], blk * 4 + 2, ww.z);
+      if (wh[3] > 0.f) race_consider(r, wh[3], tq[4 * h + 3], blk * 4 + 3, ww.w);
+    }
+  }
+}
+
+__device__ __forceinline__ bool draw_margin(const Race& r) {
+  return r.s2 >= 0.f && (r.s1 - r.s2) < kMargin * (r.t1 + r.t2);
+}
+
+// The draw is a two-level exponential race: level 1 races the blocks of
+// kRaceBlock consecutive entries with their total weights (one Philox word
+// per block, stream 2), level 2 races the entries of the winning block
+// (stream 1).  Block b then wins with probability W_b / sum W and entry v of
+// it with r_v / W_b, so v is drawn with probability r_v / sum r exactly,
+// while only one block needs a random number per entry.
+__device__ __forceinline__ uint32_t block_word(const Args& A, int row, int pos, uint32_t b) {
+  const uint4 w = philox4x32_10(make_uint4(b >> 2, (uint32_t)pos, (uint32_t)row, 2u), A.key0, A.key1);
+  return word_of(w, b & 3);
+}
+
+enum { RW_BONUS = 0, RW_RESIDUAL = 1, RW_P = 2 };
+
+// Weights of the 8 entries of group g: RW_BONUS / RW_P use exp2((l - m) c)
+// (margin weight: the same), RW_RESIDUAL uses max(p - q, 0) with
+// p = exp2((l - m) c) * invZ (margin weight p + q).  Entries outside the
+// kept set (th) or past V weigh 0.  Returns in w[] and tq[] = margin - w.
+template <bool kBF16>
+__device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t qrow, int g, float m, float c,
+                                             float invZ, int mode, const Thresh* th, float w[8], float tq[8]) {
+  float v[8], qv[8];
+  load_group<kBF16>(A, lrow, g, true, v);
+  if (mode == RW_RESIDUAL) {
+    load_q8(A, qrow, g * 8, qv);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qv[j] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool in = (g * 8 + j < A.V) && (th == nullptr || kept(*th, okey(v[j]), (uint32_t)(g * 8 + j)));
+    const float e = in ? ex2((v[j] - m) * c) : 0.f;
+    if (mode == RW_RESIDUAL) {
+      const float p = e * invZ;
+      w[j] = fmaxf(p - qv[j], 0.f);
+      tq[j] = 2.0f * qv[j];
+    } else {
+      w[j] = e;
+      tq[j] = 0.f;
+    }
+  }
+}
+
+// Level 2: the race among the entries of block b, run by one warp (the
+// result is in every lane).
+template <bool kBF16>
+__device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint32_t b, float m, float c, float invZ, int mode,
+                              const Thresh* th) {
+  const int lane = threadIdx.x & 31;
+  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  const int G = (A.V + 7) / 8;
+  Race r;
+  race_init(r);
+  if (b >= (uint32_t)((A.V + kRaceBlock - 1) / kRaceBlock)) return r;   // no block won (all weights 0)
+  const int g = (int)b * (kRaceBlock / 8) + lane;
+  if (g < G) {
+    float w[8], tq[8];
+    race_weights<kBF16>(A, lrow, qrow, g, m, c, invZ, mode, th, w, tq);
+    race_group(A, row, pos, g * 8, w, tq, r);
+  }
+  warp_race_merge(r);
+  return r;
+}
+
+// Level 1 over a whole row, one CTA: every warp-row of 32 groups is one race
+
+__device__ __forceinline__ void race_scale(Race& r, float sc) {
+  if (r.s1 >= 0.f) r.s1 *= sc;
+  if (r.s2 >= 0.f) r.s2 *= sc;
+  r.t1 *= sc;
+  r.t2 *= sc;
+}
+
+// ---------------------------------------------------------------------------
+// Launcher.
+// ---------------------------------------------------------------------------
+template <bool kBF16>
+int launch_stream(const Args& A, cudaStream_t stream);
+
+}  // namespace specv
