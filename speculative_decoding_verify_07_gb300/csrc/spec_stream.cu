@@ -28,8 +28,9 @@
 //     top-p, the accept test, alpha and the draw on that list.
 //
 // Tickets are ordered: A items of drafted unfiltered units first, then top-k
-// units, then the B items, then bonus unfiltered and greedy units, so the B
-// items find their unit state ready and the expensive finalisers run early.
+// units and bonus unfiltered positions, then the B items, then greedy units,
+// so the B items find their unit state ready and the expensive finalisers
+// run early.
 // A warp processes its tickets in increasing order and A items never wait, so
 // every wait of a B item ends.  All reductions use a fixed order; no
 // floating-point atomics are used, so results are bit-reproducible.
@@ -50,6 +51,7 @@ constexpr int kOrderSmem = 1024;       // batches up to this many rows keep orde
 constexpr int kSgCap = 256;            // top-k finaliser: super-groups gathered
 constexpr int kCandCap = 512;          // top-k finaliser: candidate entries
 constexpr int kStage = 128;            // per-warp staging floats
+constexpr int kStatic = 3;             // fixed tickets per warp before the counter is used
 constexpr unsigned kFull = 0xffffffffu;
 
 struct OrderScratch {
@@ -70,16 +72,17 @@ struct alignas(128) StreamShm {
 };
 static_assert(sizeof(GenShm) <= kSW * 2 * kSlot, "general scratch exceeds the buffers");
 
-// Top-k finaliser scratch inside the consumed buffer (byte offsets).  The
-// unit's super-group maxima are staged at the start while the threshold is
-// found; the candidate list reuses that space once the super-groups are listed.
-constexpr int kScrMax = 10240;                      // staged maxima (bytes)
+// Top-k finaliser scratch inside a consumed buffer (byte offsets).  The
+// unit's super-group maxima are staged at the start and turned into order
+// keys while the threshold is found; once the super-groups are listed, the
+// candidate list and then the kept list reuse that space.
+constexpr int kScrMax = 10240;                      // staged maxima / keys (bytes)
 constexpr int kScrHist = kScrMax;                   // 256 x u32
 constexpr int kScrSg = kScrHist + 1024;             // kSgCap x u32
 constexpr int kScrCand = 0;                         // kCandCap x u64
-constexpr int kScrList = kScrCand + kCandCap * 8;   // 5 x kTopkSmall x 4 B
+constexpr int kScrList = kScrCand + kCandCap * 8;   // kTopkSmall x 16 B entries, then cum and e
 static_assert(kScrSg + kSgCap * 4 <= kSlot, "finaliser scratch exceeds a buffer");
-static_assert(kScrList + 5 * kTopkSmall * 4 <= kScrHist, "list overlaps the histogram");
+static_assert(kScrList + kTopkSmall * 24 <= kScrHist, "list overlaps the histogram");
 
 // ---------------------------------------------------------------------------
 // Row order: rows of each class, stably, as [unfiltered][small top-k][greedy]
@@ -200,18 +203,18 @@ __device__ __forceinline__ Item map_ticket(const Args& A, const Plan& P, uint32_
     row = (int)P.order[P.nD + j / k1];
     pos = j % k1;
     kind = 1;
-  } else if ((s -= P.s1) < P.s2) {      // drafted unfiltered units: B items
-    const int j = s / P.NCB;
-    c = s - j * P.NCB;
-    row = (int)P.order[j / k];
-    pos = j % k;
-    kind = 2;
-  } else if ((s -= P.s2) < P.s3) {      // unfiltered bonus positions
+  } else if ((s -= P.s1) < P.s2) {      // unfiltered bonus positions
     const int j = s / P.NCA;
     c = s - j * P.NCA;
     row = (int)P.order[j];
     pos = k;
     kind = 1;
+  } else if ((s -= P.s2) < P.s3) {      // drafted unfiltered units: B items
+    const int j = s / P.NCB;
+    c = s - j * P.NCB;
+    row = (int)P.order[j / k];
+    pos = j % k;
+    kind = 2;
   } else if ((s -= P.s3) < P.s4) {      // greedy units
     const int j = s / P.NCA;
     c = s - j * P.NCA;
@@ -512,24 +515,47 @@ __device__ __forceinline__ uint32_t kfk(float v) {
   return kBF16 ? (okey(v) >> 16) : okey(v);
 }
 
+// Key of super-group maximum s: from the staged keys in shared memory, or
+// from the records in global memory when they were too many to stage.
+template <bool kBF16, bool kStaged>
+__device__ __forceinline__ uint32_t key_load(const uint32_t* skeys, const float* gvals, int s) {
+  if (kStaged) return skeys[s];
+  return kfk<kBF16>(__ldcg(gvals + s));
+}
+
+// Histogram of d = kmax - key over the entries with (d & mask) == prefix,
+// bins (d >> shift) & 255 (or d >> shift below `lim` when lim != 0).
+template <bool kBF16, bool kStaged>
+__device__ __forceinline__ void warp_hist(const uint32_t* skeys, const float* gvals, int nsm, uint32_t kmax,
+                                          uint32_t* hist, uint32_t lo, uint32_t span, int shift) {
+  warp_clear(hist, 256);
+  for (int base = threadIdx.x & 31; base < nsm; base += 128) {
+    uint32_t d[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = base + 32 * j;
+      d[j] = s < nsm ? kmax - key_load<kBF16, kStaged>(skeys, gvals, s) : 0xffffffffu;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (d[j] >= lo && d[j] - lo < span) atomicAdd(&hist[(d[j] - lo) >> shift], 1u);
+  }
+  __syncwarp();
+}
+
 // A key tau no larger than the K-th largest of the unit's super-group maxima
 // (counting multiplicity): a histogram of the distance d = kmax - key, first
 // with fine bins next to the maximum, refined 8 bits at a time while the bin
 // holding rank K is wide and crowded; exact for bf16 in the usual case.
-template <bool kBF16, typename KeyAt>
-__device__ __noinline__ uint32_t warp_kth_key(KeyAt key_at, int nsm, uint32_t kmax, uint32_t K, uint32_t* hist) {
+template <bool kBF16, bool kStaged>
+__device__ __noinline__ uint32_t warp_kth_key(const uint32_t* skeys, const float* gvals, int nsm, uint32_t kmax,
+                                              uint32_t K, uint32_t* hist) {
   const int s0 = kBF16 ? 0 : 16;
   const int dbits = kBF16 ? 16 : 32;
   uint32_t need = K;
-  warp_clear(hist, 256);
-  const uint32_t lim = 255u << s0;
-  for (int s = threadIdx.x & 31; s < nsm; s += 32) {
-    const uint32_t d = kmax - key_at(s);
-    if (d < lim) atomicAdd(&hist[d >> s0], 1u);
-  }
-  __syncwarp();
+  warp_hist<kBF16, kStaged>(skeys, gvals, nsm, kmax, hist, 0u, 255u << s0, s0);
   uint32_t below;
-  int b = warp_select_bin(hist, need, &below);
+  const int b = warp_select_bin(hist, need, &below);
   if (b < 255) {
     need -= below;
     uint32_t cnt = hist[b];
@@ -538,13 +564,7 @@ __device__ __noinline__ uint32_t warp_kth_key(KeyAt key_at, int nsm, uint32_t km
     while (sh > 0 && cnt > 64) {
       sh -= 8;
       __syncwarp();
-      warp_clear(hist, 256);
-      const uint32_t span = 1u << (sh + 8);
-      for (int s = threadIdx.x & 31; s < nsm; s += 32) {
-        const uint32_t d = kmax - key_at(s);
-        if (d >= lo && d - lo < span) atomicAdd(&hist[(d - lo) >> sh], 1u);
-      }
-      __syncwarp();
+      warp_hist<kBF16, kStaged>(skeys, gvals, nsm, kmax, hist, lo, 1u << (sh + 8), sh);
       uint32_t bl;
       const int bb = warp_select_bin(hist, need, &bl);
       need -= bl;
@@ -557,20 +577,16 @@ __device__ __noinline__ uint32_t warp_kth_key(KeyAt key_at, int nsm, uint32_t km
     return kmax - dmax;
   }
   // rank K lies far from the maximum: top-down radix over every bit of d
-  uint32_t prefix = 0u, mask = 0u;
+  uint32_t prefix = 0u;
   for (int shift = dbits - 8; shift >= 0; shift -= 8) {
     __syncwarp();
-    warp_clear(hist, 256);
-    for (int s = threadIdx.x & 31; s < nsm; s += 32) {
-      const uint32_t d = kmax - key_at(s);
-      if ((d & mask) == prefix) atomicAdd(&hist[(d >> shift) & 255u], 1u);
-    }
-    __syncwarp();
+    // entries whose bits above `shift + 8` equal the prefix: d in [prefix, prefix + 2^(shift+8))
+    const uint32_t span = (shift + 8 >= 32) ? 0xffffffffu : (1u << (shift + 8));
+    warp_hist<kBF16, kStaged>(skeys, gvals, nsm, kmax, hist, prefix, span, shift);
     uint32_t bl;
     const int bb = warp_select_bin(hist, need, &bl);
     need -= bl;
     prefix |= (uint32_t)bb << shift;
-    mask |= 255u << shift;
     if (shift > 0 && hist[bb] <= 64) {
       uint32_t dmax = prefix | ((1u << shift) - 1u);
       if (dmax > kmax) dmax = kmax;
@@ -693,25 +709,25 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
                                       uint32_t& parity) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
-  const RowCfg& cfg = it.cfg;
+  const RowCfg cfg = it.cfg;
   const int u = it.u, row = it.row, pos = it.pos;
   const bool has_q = pos < A.k;
-  const int NC = ceil_div(A.V, G::EA);
+  const int V = A.V;
+  const int NC = ceil_div(V, G::EA);
   const int nsm = NC * G::SPI;
   const float* sm = A.smax + (size_t)u * A.NSM;
-  const size_t lrow = (size_t)u * A.V;
-  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  const size_t lrow = (size_t)u * V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)V;
   uint32_t* hist = reinterpret_cast<uint32_t*>(scr + kScrHist);
   uint32_t* sg = reinterpret_cast<uint32_t*>(scr + kScrSg);
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(scr + kScrCand);
-  float* l_e = reinterpret_cast<float*>(scr + kScrList);
-  float* l_cum = l_e + kTopkSmall;
-  float* l_w = l_cum + kTopkSmall;
-  float* l_u = l_w + kTopkSmall;
-  uint32_t* l_i = reinterpret_cast<uint32_t*>(l_u + kTopkSmall);
+  float4* l4 = reinterpret_cast<float4*>(scr + kScrList);           // (index bits, w, w + tq, 0)
+  float* l_cum = reinterpret_cast<float*>(scr + kScrList + kTopkSmall * 16);
+  float* l_e = l_cum + kTopkSmall;
+  // the draft token goes out first; its logit and q follow once it is back
+  const int x = has_q ? A.drafts[(size_t)row * A.k + pos] : -1;
   // stage the maxima in shared memory with one bulk copy (the records were
   // published before the unit ticket this warp acquired)
-  const float* smx = reinterpret_cast<const float*>(scr);
   const bool staged = nsm * 4 <= kScrMax;
   if (staged) {
     if (lane == 0) {
@@ -723,19 +739,29 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
     parity ^= 1u;
     if (!ok) return;
   }
-  auto val_at = [&](int s) -> float { return staged ? smx[s] : __ldcg(sm + s); };
-  auto key_at = [&](int s) -> uint32_t { return kfk<kBF16>(val_at(s)); };
-
-  // unit maximum; NaN
+  uint32_t* keys = reinterpret_cast<uint32_t*>(scr);
+  // order keys (in place when staged); the unit maximum; NaN
   uint32_t kmax = 0u;
   bool nan = false;
-  for (int s = lane; s < nsm; s += 32) {
-    const float x = val_at(s);
-    if (x != x) nan = true;
-    else kmax = max(kmax, kfk<kBF16>(x));
+  for (int base = lane; base < nsm; base += 128) {
+    float xv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = base + 32 * j;
+      xv[j] = s < nsm ? (staged ? reinterpret_cast<const float*>(scr)[s] : __ldcg(sm + s)) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = base + 32 * j;
+      const uint32_t kk = kfk<kBF16>(xv[j]);
+      if (xv[j] != xv[j]) nan = true;
+      else kmax = max(kmax, kk);
+      if (staged && s < nsm) keys[s] = kk;
+    }
   }
   nan = __any_sync(kFull, nan);
   kmax = warp_max_u32(kmax);
+  __syncwarp();
   const float m = from_okey(full_key<kBF16>(kmax));
   if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
     if (lane == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
@@ -743,18 +769,34 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
     return;
   }
   const uint32_t K = (uint32_t)cfg.K;
-  const uint32_t tau = (K < (uint32_t)nsm) ? warp_kth_key<kBF16>(key_at, nsm, kmax, K, hist) : 0u;
+  uint32_t tau = 0u;
+  if (K < (uint32_t)nsm)
+    tau = staged ? warp_kth_key<kBF16, true>(keys, sm, nsm, kmax, K, hist)
+                 : warp_kth_key<kBF16, false>(keys, sm, nsm, kmax, K, hist);
+  // the accept test's loads overlap the gather below
+  const bool xvalid = x >= 0 && x < V;
+  const float lx = xvalid ? load_logit(A, kBF16, lrow + x) : 0.f;
+  const float qx = xvalid ? A.q[qrow + x] : 0.f;
   // the qualifying super-groups
   int nsg = 0;
-  for (int base = 0; base < nsm; base += 32) {
-    const int s = base + lane;
-    const bool ok = s < nsm && key_at(s) >= tau;
-    const unsigned b = __ballot_sync(kFull, ok);
-    if (ok) {
-      const int p = nsg + __popc(b & ((1u << lane) - 1u));
-      if (p < kSgCap) sg[p] = (uint32_t)s;
+  for (int base = 0; base < nsm; base += 128) {
+    uint32_t kk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = base + 32 * j + lane;
+      kk[j] = s >= nsm ? 0u : (staged ? key_load<kBF16, true>(keys, sm, s) : key_load<kBF16, false>(keys, sm, s));
     }
-    nsg += __popc(b);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = base + 32 * j + lane;
+      const bool ok = s < nsm && kk[j] >= tau;
+      const unsigned b = __ballot_sync(kFull, ok);
+      if (ok) {
+        const int p = nsg + __popc(b & ((1u << lane) - 1u));
+        if (p < kSgCap) sg[p] = (uint32_t)s;
+      }
+      nsg += __popc(b);
+    }
   }
   __syncwarp();
   bool overflow = nsg > kSgCap;
@@ -763,19 +805,20 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
     // gather their entries >= tau; super-group r of a chunk is block r/4,
     // lanes 8(r%4)..8(r%4)+7, i.e. entries [32q, 32q+32) and [128+32q,
     // 128+32q+32) of the block with q = r%4
-    for (int base = 0; base < nsg * 8; base += 128) {
+    const int ngr = nsg * 8;
+    for (int base = 0; base < ngr; base += 128) {
       float v[4][8];
       int e[4];
       bool act[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int i = base + 32 * h + lane;
-        act[h] = i < nsg * 8;
+        act[h] = i < ngr;
         e[h] = 0;
         if (act[h]) {
-          const int s = (int)sg[i >> 3];
+          const int sgi = (int)sg[i >> 3];
           const int gi = i & 7;
-          const int c = s / G::SPI, r = s - c * G::SPI;
+          const int c = sgi / G::SPI, r = sgi - c * G::SPI;
           e[h] = c * G::EA + (r >> 2) * kRaceBlock + (gi >> 2) * 128 + (r & 3) * 32 + (gi & 3) * 8;
           load_group<kBF16>(A, lrow, e[h] >> 3, true, v[h]);
         }
@@ -784,7 +827,7 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
       for (int h = 0; h < 4; ++h) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const bool up = act[h] && e[h] + j < A.V && kfk<kBF16>(v[h][j]) >= tau;
+          const bool up = act[h] && e[h] + j < V && kfk<kBF16>(v[h][j]) >= tau;
           const unsigned b = __ballot_sync(kFull, up);
           if (up) {
             const int p = count + __popc(b & ((1u << lane) - 1u));
@@ -824,6 +867,7 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
       e4[j] = ex2((from_okey((uint32_t)(key >> 32)) - m) * cfg.c);
     }
   }
+  __syncwarp();   // the candidate space is reused by the list from here on
   {
     // inclusive prefix sums in list order (fixed order)
     float run = 0.f;
@@ -846,7 +890,6 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
       if (i < n_k) {
         l_e[i] = e4[j];
         l_cum[i] = loc + cum4[j];
-        l_i[i] = i4[j];
       }
     }
   }
@@ -881,13 +924,8 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
   }
   float alpha_v = 0.f;
   bool need_race = !has_q;
-  AcceptInfo ai;
-  ai.valid = true;
-  ai.accept = false;
-  ai.margin = false;
-  ai.lx = 0.f;
+  bool accept = false, margin = false;
   if (has_q) {
-    const int x = A.drafts[(size_t)row * A.k + pos];
     int xi = -1;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -898,17 +936,13 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
 #pragma unroll
     for (int j = 0; j < 4; ++j) al += fminf(p4[j], q4[j]);
     alpha_v = warp_sum(al);
-    ai.x = x;
-    ai.valid = x >= 0 && x < A.V;
-    ai.px = xi >= 0 ? l_e[xi] / Zs : 0.f;
-    ai.qx = ai.valid ? A.q[qrow + x] : 0.f;
-    ai.lx = ai.valid ? load_logit(A, kBF16, lrow + x) : 0.f;
+    const float px = xi >= 0 ? l_e[xi] / Zs : 0.f;
     const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
     const float uu = uniform_of(w.x);
-    const float d = fmaf(uu, ai.qx, -ai.px);
-    ai.accept = d < 0.0f;
-    ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
-    need_race = !ai.accept;
+    const float d = fmaf(uu, qx, -px);
+    accept = d < 0.0f;
+    margin = (px > 0.0f && px < 1.0f && fabsf(d) < kMargin);
+    need_race = !accept;
   }
   // the draw: the two-level race over the kept entries (blocks by index)
   uint32_t draw_flags = 0;
@@ -922,10 +956,7 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
         const int i = 4 * lane + j;
         w4[j] = (has_q && !use_p) ? fmaxf(p4[j] - q4[j], 0.f) : p4[j];
         t4[j] = (has_q && !use_p) ? 2.0f * q4[j] : 0.f;
-        if (i < n_s) {
-          l_w[i] = w4[j];
-          l_u[i] = w4[j] + t4[j];
-        }
+        if (i < n_s) l4[i] = make_float4(__uint_as_float(i4[j]), w4[j], w4[j] + t4[j], 0.f);
       }
       __syncwarp();
       // level 1: the first list entry of each block races for its block, with
@@ -939,12 +970,13 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
           const uint32_t b = i4[j] / kRaceBlock;
           bool rep = true;
           float W = 0.f, U = 0.f;
-#pragma unroll 8
+#pragma unroll 4
           for (int jj = 0; jj < n_s; ++jj) {
-            if (l_i[jj] / kRaceBlock == b && l_w[jj] > 0.f) {
+            const float4 L = l4[jj];
+            if (__float_as_uint(L.x) / kRaceBlock == b && L.y > 0.f) {
               if (jj < i) rep = false;
-              W += l_w[jj];
-              U += l_u[jj];
+              W += L.y;
+              U += L.z;
             }
           }
           if (rep) race_consider(r1, W, U - W, b, block_word(A, row, pos, b));
@@ -974,14 +1006,14 @@ __device__ __noinline__ void fin_topk(const Args& A, const Item& it, unsigned ch
   if (lane == 0) {
     UnitRecord rec = empty_record(flags);
     if (has_q) {
-      if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
-      if (ai.margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
-      rec.accept = ai.accept ? 1 : 0;
-      rec.lp_x = ai.valid ? (ai.lx - m) * cfg.invT - lnZ : 0.f;
+      if (!xvalid) rec.flags |= SPEC_F_BAD_TOKEN;
+      if (margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
+      rec.accept = accept ? 1 : 0;
+      rec.lp_x = xvalid ? (lx - m) * cfg.invT - lnZ : 0.f;
       rec.alpha = alpha_v;
     }
     if (need_race) {
-      const uint32_t yy = y < (uint32_t)A.V ? y : (uint32_t)am;
+      const uint32_t yy = y < (uint32_t)V ? y : (uint32_t)am;
       rec.y = (int32_t)yy;
       rec.lp_y = (load_logit(A, kBF16, lrow + yy) - m) * cfg.invT - lnZ;
       rec.draw_flags = draw_flags;
@@ -1022,12 +1054,26 @@ __device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, fl
   return l2.v1;
 }
 
+__device__ __forceinline__ UnitState load_state(const Args& A, int u) {
+  UnitState st;
+  st.m = __ldcg(&A.ust[u].m);
+  st.invZ = __ldcg(&A.ust[u].invZ);
+  st.lnZ = __ldcg(&A.ust[u].lnZ);
+  st.lp_x = __ldcg(&A.ust[u].lp_x);
+  st.accept = __ldcg(&A.ust[u].accept);
+  st.flags = __ldcg(&A.ust[u].flags);
+  st.invalid = __ldcg(&A.ust[u].invalid);
+  st.am = __ldcg(&A.ust[u].am);
+  return st;
+}
+
 template <bool kBF16>
-__device__ __noinline__ void fin_b(const Args& A, const Item& it, const UnitState& st) {
+__device__ __noinline__ void fin_b(const Args& A, const Item& it) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int u = it.u, row = it.row, pos = it.pos;
   const RowCfg& cfg = it.cfg;
+  const UnitState st = load_state(A, u);
   if (st.invalid) {   // the A finaliser wrote the record already
     if (lane == 0) {
       A.b_ticket[u] = 0;
@@ -1090,11 +1136,13 @@ __device__ __noinline__ void fin_b(const Args& A, const Item& it, const UnitStat
 }
 
 // ---------------------------------------------------------------------------
-// Item processing (one warp).
+// Item processing (one warp).  An item's record is stored when the item ends;
+// its unit ticket is taken one item later (the release then finds the store
+// long completed) and read one item after that, when the finaliser of a
+// completed unit runs with the buffer just consumed as scratch.
 // ---------------------------------------------------------------------------
 template <bool kBF16>
-__device__ void a_item(const Args& A, const Item& it, unsigned char* buf, float* stage, unsigned long long* bar,
-                       uint32_t& parity) {
+__device__ void a_compute(const Args& A, const Item& it, const unsigned char* buf, float* stage, ChunkRec& rec) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
@@ -1113,107 +1161,94 @@ __device__ void a_item(const Args& A, const Item& it, unsigned char* buf, float*
     __syncwarp();
     float* dst = A.smax + (size_t)it.u * A.NSM + (size_t)it.c * G::SPI;
     for (int s = lane; s < G::SPI; s += 32) dst[s] = s < nb * 4 ? stage[s] : -INFINITY;
-    __threadfence();   // every writer publishes before the ticket
-    __syncwarp();
-  } else {
-    // greedy and unfiltered: max and first argmax, then the softmax sum
-    // relative to the chunk max; at an unfiltered bonus position also the
-    // block weights and the level-1 race of the chunk's blocks
-    float lm = -INFINITY;
-    int lb = 0;
-    bool nan = false;
+    return;
+  }
+  // greedy and unfiltered: max and first argmax, then the softmax sum
+  // relative to the chunk max; at an unfiltered bonus position also the
+  // block weights and the level-1 race of the chunk's blocks
+  float lm = -INFINITY;
+  int lb = 0;
+  bool nan = false;
 #pragma unroll 4
-    for (int b = 0; b < nb; ++b) {
-      const float gm = sgroup_max<kBF16>(buf, b, lane);
-      nan |= gm != gm;
-      if (gm > lm) {
-        lm = gm;
-        lb = b;
-      }
-    }
-    nan = __any_sync(kFull, nan);
-    const float mc = warp_max_f(lm);
-    uint32_t idx = 0xffffffffu;
-    if (lm == mc) {
-      float v[8];
-      sload<kBF16>(buf, lb, lane, v);
-#pragma unroll
-      for (int j = 7; j >= 0; --j)
-        if (v[j] == lm) idx = (uint32_t)(e0 + slot_entry(lb, lane, j));
-    }
-    idx = warp_min_u32(idx);
-    float z = 0.f;
-    Race r;
-    race_init(r);
-    const bool live = !nan && mc > -INFINITY && mc < INFINITY;
-    const bool bonus = cfg.type == UT_DENSE && it.pos == A.k;
-    if (live) {
-      const float c = cfg.c;
-      if (!bonus) {
-        float z0 = 0.f, z1 = 0.f;
-#pragma unroll 2
-        for (int b = 0; b < nb; ++b) {
-          float v[8];
-          sload<kBF16>(buf, b, lane, v);
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            z0 += ex2((v[j] - mc) * c);
-            z1 += ex2((v[j + 1] - mc) * c);
-          }
-        }
-        z = warp_sum(z0 + z1);
-      } else {
-        float myW = 0.f;
-        for (int b = 0; b < nb; ++b) {
-          float v[8];
-          sload<kBF16>(buf, b, lane, v);
-          float s8 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) s8 += ex2((v[j] - mc) * c);
-          const float W = warp_sum(s8);
-          z += W;
-          if (lane == b) myW = W;
-        }
-        if (myW > 0.f) {
-          const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
-          race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
-        }
-        warp_race_merge(r);
-      }
-    }
-    if (lane == 0) {
-      ChunkRec rec;
-      rec.m = nan ? __uint_as_float(0x7fc00000u) : mc;
-      rec.amax = idx;
-      rec.z = z;
-      rec.pad0 = 0;
-      rec.s1 = r.s1;
-      rec.t1 = r.t1;
-      rec.s2 = r.s2;
-      rec.t2 = r.t2;
-      rec.v1 = r.v1;
-      rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
-      A.crec[(size_t)it.u * A.NCA + it.c] = rec;
+  for (int b = 0; b < nb; ++b) {
+    const float gm = sgroup_max<kBF16>(buf, b, lane);
+    nan |= gm != gm;
+    if (gm > lm) {
+      lm = gm;
+      lb = b;
     }
   }
-  uint32_t t = 0;
-  if (lane == 0) t = atomic_add_acq_rel(&A.a_ticket[it.u], 1u);
-  t = __shfl_sync(kFull, t, 0);
-  if (t != (uint32_t)(ceil_div(A.V, G::EA) - 1)) return;
-  if (lane == 0) A.a_ticket[it.u] = 0;
-  __syncwarp();
-  if (cfg.type == UT_TOPK) fin_topk<kBF16>(A, it, buf, bar, parity);
-  else fin_stats<kBF16>(A, it);
+  nan = __any_sync(kFull, nan);
+  const float mc = warp_max_f(lm);
+  uint32_t idx = 0xffffffffu;
+  if (lm == mc) {
+    float v[8];
+    sload<kBF16>(buf, lb, lane, v);
+#pragma unroll
+    for (int j = 7; j >= 0; --j)
+      if (v[j] == lm) idx = (uint32_t)(e0 + slot_entry(lb, lane, j));
+  }
+  idx = warp_min_u32(idx);
+  float z = 0.f;
+  Race r;
+  race_init(r);
+  const bool live = !nan && mc > -INFINITY && mc < INFINITY;
+  const bool bonus = cfg.type == UT_DENSE && it.pos == A.k;
+  if (live) {
+    const float c = cfg.c;
+    if (!bonus) {
+      float z0 = 0.f, z1 = 0.f;
+#pragma unroll 2
+      for (int b = 0; b < nb; ++b) {
+        float v[8];
+        sload<kBF16>(buf, b, lane, v);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          z0 += ex2((v[j] - mc) * c);
+          z1 += ex2((v[j + 1] - mc) * c);
+        }
+      }
+      z = warp_sum(z0 + z1);
+    } else {
+      float myW = 0.f;
+      for (int b = 0; b < nb; ++b) {
+        float v[8];
+        sload<kBF16>(buf, b, lane, v);
+        float s8 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s8 += ex2((v[j] - mc) * c);
+        const float W = warp_sum(s8);
+        z += W;
+        if (lane == b) myW = W;
+      }
+      if (myW > 0.f) {
+        const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
+        race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
+      }
+      warp_race_merge(r);
+    }
+  }
+  rec.m = nan ? __uint_as_float(0x7fc00000u) : mc;
+  rec.amax = idx;
+  rec.z = z;
+  rec.pad0 = 0;
+  rec.s1 = r.s1;
+  rec.t1 = r.t1;
+  rec.s2 = r.s2;
+  rec.t2 = r.t2;
+  rec.v1 = r.v1;
+  rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
 }
 
 template <bool kBF16>
-__device__ void b_item(const Args& A, const Item& it, unsigned char* buf) {
+__device__ void b_compute(const Args& A, const Item& it, const unsigned char* buf, BRec& br) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EB;
   const RowCfg& cfg = it.cfg;
-  // the unit state (bounded wait; every A item was claimed before any B item)
+  // the unit state (bounded wait; every A item was claimed before any B item,
+  // and a warp resolves its pending A tickets before it starts a B item)
   if (lane == 0) {
     long long spins = 0;
     while (load_acquire(&A.ready[it.u]) == 0u) {
@@ -1225,15 +1260,7 @@ __device__ void b_item(const Args& A, const Item& it, unsigned char* buf) {
     }
   }
   __syncwarp();
-  UnitState st;
-  st.m = __ldcg(&A.ust[it.u].m);
-  st.invZ = __ldcg(&A.ust[it.u].invZ);
-  st.lnZ = __ldcg(&A.ust[it.u].lnZ);
-  st.lp_x = __ldcg(&A.ust[it.u].lp_x);
-  st.accept = __ldcg(&A.ust[it.u].accept);
-  st.flags = __ldcg(&A.ust[it.u].flags);
-  st.invalid = __ldcg(&A.ust[it.u].invalid);
-  st.am = __ldcg(&A.ust[it.u].am);
+  const UnitState st = load_state(A, it.u);
   const bool need_race = !st.accept;
   const float* qb = reinterpret_cast<const float*>(buf + G::EB * G::es);
   float alpha_c = 0.f, myW = 0.f, myU = 0.f;
@@ -1271,22 +1298,57 @@ __device__ void b_item(const Args& A, const Item& it, unsigned char* buf) {
     race_consider(r, myW, myU - myW, blk, block_word(A, it.row, it.pos, blk));
   }
   warp_race_merge(r);
-  uint32_t t = 0;
-  if (lane == 0) {
-    BRec br;
-    br.alpha = alpha_c;
-    br.s1 = r.s1;
-    br.t1 = r.t1;
-    br.s2 = r.s2;
-    br.t2 = r.t2;
-    br.v1 = r.v1;
-    br.pad[0] = br.pad[1] = 0;
-    A.brec[(size_t)it.u * A.NCB + it.c] = br;
-    t = atomic_add_acq_rel(&A.b_ticket[it.u], 1u);
-  }
+  br.alpha = alpha_c;
+  br.s1 = r.s1;
+  br.t1 = r.t1;
+  br.s2 = r.s2;
+  br.t2 = r.t2;
+  br.v1 = r.v1;
+  br.pad[0] = br.pad[1] = 0;
+}
+
+// A processed item whose unit ticket is still to be taken or read.
+struct Pending {
+  Item it;                  // kind 0: none
+  uint32_t t;               // the ticket value (lane 0), once taken
+};
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t* ticket_of(const Args& A, const Item& it) {
+  return it.kind == 1 ? A.a_ticket + it.u : A.b_ticket + it.u;
+}
+template <bool kBF16>
+__device__ __forceinline__ uint32_t last_ticket(const Args& A, const Item& it) {
+  return (uint32_t)(it.kind == 1 ? ceil_div(A.V, Geo<kBF16>::EA) : ceil_div(A.V, Geo<kBF16>::EB)) - 1u;
+}
+
+// Lane 0's ticket value t (valid in lane 0 only) decides whether this warp
+// settles the item's unit; the finaliser's scratch is a consumed buffer.
+template <bool kBF16>
+__device__ void settle(const Args& A, const Item& it, uint32_t t, unsigned char* scr, unsigned long long* bar,
+                       uint32_t& parity) {
   t = __shfl_sync(kFull, t, 0);
-  if (t != (uint32_t)(ceil_div(A.V, G::EB) - 1)) return;
-  fin_b<kBF16>(A, it, st);
+  if (t != last_ticket<kBF16>(A, it)) return;
+  if (it.kind == 1) {
+    if ((threadIdx.x & 31) == 0) A.a_ticket[it.u] = 0;
+    __syncwarp();
+    if (it.cfg.type == UT_TOPK) fin_topk<kBF16>(A, it, scr, bar, parity);
+    else fin_stats<kBF16>(A, it);
+  } else {
+    fin_b<kBF16>(A, it);
+  }
+}
+
+// Take the pending tickets now and settle what they complete.
+template <bool kBF16>
+__device__ void flush(const Args& A, Pending& p0, Pending& p1, unsigned char* scr, unsigned long long* bar,
+                      uint32_t& parity) {
+  uint32_t t0 = 0;
+  if ((threadIdx.x & 31) == 0 && p0.it.kind != 0) t0 = atomic_add_acq_rel(ticket_of<kBF16>(A, p0.it), 1u);
+  if (p1.it.kind != 0) settle<kBF16>(A, p1.it, p1.t, scr, bar, parity);
+  if (p0.it.kind != 0) settle<kBF16>(A, p0.it, t0, scr, bar, parity);
+  p0.it.kind = 0;
+  p1.it.kind = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -1298,10 +1360,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(const Args A) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   StreamShm& S = *reinterpret_cast<StreamShm*>(smem_raw);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  // the warp's first two tickets go out before the prologue
-  uint32_t t01 = 0;
   if (lane == 0) {
-    t01 = atomicAdd(&A.ws->next, 2u);
     mbar_init(&S.bar[w][0], 1);
     mbar_init(&S.bar[w][1], 1);
   }
@@ -1346,32 +1405,61 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(const Args A) {
   P.NCB = ceil_div(A.V, G::EB);
   P.s0 = P.nD * A.k * P.NCA;
   P.s1 = P.nT * (A.k + 1) * P.NCA;
-  P.s2 = P.nD * A.k * P.NCB;
-  P.s3 = P.nD * P.NCA;
+  P.s2 = P.nD * P.NCA;
+  P.s3 = P.nD * A.k * P.NCB;
   P.s4 = P.nG * (A.k + 1) * P.NCA;
-  t01 = __shfl_sync(kFull, t01, 0);
+  // The first kStatic tickets of each warp are fixed (warp g takes g, g + NW,
+  // g + 2 NW, with NW warps in the grid), so the launch starts without a
+  // burst of atomics on one counter; later tickets come from the counter.
+  const uint32_t nw = (uint32_t)A.n_ctas * kSW;
+  const uint32_t gw = (uint32_t)blockIdx.x * kSW + (uint32_t)w;
+  int nstat = 2;   // static tickets used so far
   // slot a holds the oldest outstanding ticket, slot b the next one
-  Item ia = map_ticket<kBF16>(A, P, t01);
-  Item ib = map_ticket<kBF16>(A, P, t01 + 1);
+  Item ia = map_ticket<kBF16>(A, P, gw);
+  Item ib = map_ticket<kBF16>(A, P, gw + nw);
   unsigned char* bufa = S.buf[w][0];
   unsigned char* bufb = S.buf[w][1];
   unsigned long long* bara = &S.bar[w][0];
   unsigned long long* barb = &S.bar[w][1];
   uint32_t para = 0u, parb = 0u;
-  uint32_t tn = 0;
+  uint32_t tn = gw + 2 * nw;
   if (lane == 0) {
     issue<kBF16>(A, ia, bufa, bara);
     issue<kBF16>(A, ib, bufb, barb);
-    if (ib.kind != 0) tn = atomicAdd(&A.ws->next, 1u);
   }
+  Pending p0, p1;
+  p0.it.kind = 0;
+  p1.it.kind = 0;
+  p0.t = p1.t = 0;
+  bool ok = true;
   while (ia.kind != 0) {
-    if (!wait_buffer(A, bara, para)) break;
+    if (!wait_buffer(A, bara, para)) {
+      ok = false;
+      break;
+    }
     para ^= 1u;
     if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || (ia.n & (kRaceBlock - 1)) != 0)
       fill_tail<kBF16>(A, ia, bufa);
-    if (ia.kind == 1) a_item<kBF16>(A, ia, bufa, S.stage[w], bara, para);
-    else b_item<kBF16>(A, ia, bufa);
+    ChunkRec rec;
+    BRec br;
+    if (ia.kind == 1) a_compute<kBF16>(A, ia, bufa, S.stage[w], rec);
+    else b_compute<kBF16>(A, ia, bufa, br);
+    // the ticket of the item before (its record was stored an item ago)
+    uint32_t t0 = 0;
+    if (lane == 0 && p0.it.kind != 0) t0 = atomic_add_acq_rel(ticket_of<kBF16>(A, p0.it), 1u);
+    // this item's record
+    if (lane == 0) {
+      if (ia.kind == 2) A.brec[(size_t)ia.u * A.NCB + ia.c] = br;
+      else if (ia.cfg.type != UT_TOPK) A.crec[(size_t)ia.u * A.NCA + ia.c] = rec;
+    }
     __syncwarp();
+    // the ticket taken an item ago
+    if (p1.it.kind != 0) settle<kBF16>(A, p1.it, p1.t, bufa, bara, para);
+    p1.it = p0.it;
+    p1.t = t0;
+    p0.it = ia;
+    // B items wait on A finalisers: settle pending A items before one starts
+    if (ib.kind == 2 && (p0.it.kind == 1 || p1.it.kind == 1)) flush<kBF16>(A, p0, p1, bufa, bara, para);
     // refill the consumed buffer with the next ticket, then rotate the slots
     const uint32_t t = __shfl_sync(kFull, tn, 0);
     Item in;
@@ -1379,8 +1467,15 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(const Args A) {
     if (ib.kind != 0) in = map_ticket<kBF16>(A, P, t);
     if (lane == 0) {
       issue<kBF16>(A, in, bufa, bara);
-      if (in.kind != 0) tn = atomicAdd(&A.ws->next, 1u);
+      if (in.kind != 0) {
+        if (nstat + 1 < kStatic) {
+          tn = gw + (uint32_t)(nstat + 1) * nw;
+        } else {
+          tn = atomicAdd(&A.ws->next, 1u) + (uint32_t)kStatic * nw;
+        }
+      }
     }
+    ++nstat;
     ia = ib;
     ib = in;
     unsigned char* tb = bufa;
@@ -1393,6 +1488,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(const Args A) {
     para = parb;
     parb = tp;
   }
+  if (ok) flush<kBF16>(A, p0, p1, bufa, bara, para);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
