@@ -90,8 +90,8 @@ enum {
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
  * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (two work-item counters, an exit counter, one ticket
- * per row, and two tickets and a ready flag per (row, position)) to zero; the
+ * must start at zero (a count of listed units, an exit counter, one ticket
+ * per row and one ticket per (row, position)) to zero; the
  * records behind them are rewritten before they are read by every call.  So one workspace serves any number of later calls on one
  * stream; two calls that may run concurrently need two workspaces.           */
 size_t spec_verify_workspace_size(int B, int k, int V);
@@ -176,8 +176,8 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
  * library (a file-scope device array, held on every GPU that loads the
  * library until the process exits).  The call allocates nothing.
  *   - Limit: spec_verify_workspace_size(B, k, V) must not exceed
- *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 1.1 KB per
- *     (row, position) unit and 8192-entry vocabulary chunk, so at V = 151936
+ *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 140 bytes
+ *     per (row, position) unit per 1024 vocabulary entries, so at V = 151936
  *     about 400 units fit, e.g. 128 rows at k = 2); a larger batch returns
  *     SPEC_E_WORKSPACE and enqueues nothing.
  *   - The first call on each device looks up the array's device address

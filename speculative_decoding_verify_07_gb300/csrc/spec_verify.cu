@@ -1,11 +1,13 @@
 // spec_verify: batched speculative-decoding verify sampler for sm_103a --
 // argument checks, workspace carving and the launch.
 //
-// One persistent kernel (spec_stream.cu) settles every row on the caller's
-// stream with no host synchronisation: rows whose kept set needs a global
-// threshold search (top-p without a small top-k, or a large top-k) run first
-// on whole CTAs (spec_general.cuh); greedy rows, rows with a small top-k and
-// unfiltered rows stream through per-warp work items.
+// Three kernels on the caller's stream, chained by programmatic dependent
+// launch, with no host synchronisation: the stats kernel streams every logit
+// row once (spec_stream.cu), the unit kernel settles every (row, position)
+// with one CTA (spec_unit.cu; rows that need a global threshold search take
+// the general path, spec_general.cuh), and the B pass streams the draft
+// probabilities of drafted positions over unfiltered distributions
+// (spec_stream.cu).
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -40,7 +42,7 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
     return SPEC_E_ALIGN;
   const specv::Layout L = specv::ws_layout(B, k, V);
   if (workspace_bytes < L.total) return SPEC_E_WORKSPACE;
-  // tickets of the streaming kernel (A items of every unit, B items of every drafted unit)
+  // items of the streaming kernels (A items of every unit, B items of every drafted unit)
   const long long items = (long long)B * (k + 1) * specv::max_nca(V) + (long long)B * k * specv::max_ncb(V);
   if (items > 0x7fffffffLL) return SPEC_E_DIM;
   const int arc = specv::check_arch();
@@ -60,15 +62,13 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   A.ws = reinterpret_cast<specv::WsHeader*>(ws);
   A.row_ticket = reinterpret_cast<uint32_t*>(ws + L.row_ticket);
-  A.a_ticket = reinterpret_cast<uint32_t*>(ws + L.a_ticket);
   A.b_ticket = reinterpret_cast<uint32_t*>(ws + L.b_ticket);
-  A.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
   A.crec = reinterpret_cast<specv::ChunkRec*>(ws + L.crec);
   A.ust = reinterpret_cast<specv::UnitState*>(ws + L.ust);
   A.brec = reinterpret_cast<specv::BRec*>(ws + L.brec);
   A.urec = reinterpret_cast<specv::UnitRecord*>(ws + L.urec);
   A.smax = reinterpret_cast<float*>(ws + L.smax);
-  A.order = reinterpret_cast<uint32_t*>(ws + L.order);
+  A.dlist = reinterpret_cast<uint32_t*>(ws + L.dlist);
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);
   A.B = B;
@@ -81,5 +81,10 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   A.vec_logits = aligned(logits, 16) && ((size_t)V * es) % 16 == 0;
   A.vec_q = k > 0 && aligned(draft_probs, 16) && (V % 4) == 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
-  return logits_dtype == SPEC_BF16 ? specv::launch_stream<true>(A, st) : specv::launch_stream<false>(A, st);
+  const bool bf16 = logits_dtype == SPEC_BF16;
+  int rc = bf16 ? specv::launch_stats<true>(A, st) : specv::launch_stats<false>(A, st);
+  if (rc != SPEC_OK) return rc;
+  rc = bf16 ? specv::launch_units<true>(A, st) : specv::launch_units<false>(A, st);
+  if (rc != SPEC_OK) return rc;
+  return bf16 ? specv::launch_bpass<true>(A, st) : specv::launch_bpass<false>(A, st);
 }

@@ -24,18 +24,19 @@ namespace specv {
 
 constexpr int kRaceBlock = 256;            // entries per block of the two-level race
 constexpr int kTopkSmall = 128;            // top_k <= this: candidate-list path
+constexpr int kMaxNsmTopk = 4096;          // ... when the super-group maxima of a row fit the finaliser
 constexpr long long kSpinLimit = 1ll << 22;
 
-// Streaming geometry.  Every warp of the streaming kernel owns two buffers
+// Streaming geometry.  Every warp of the streaming kernels owns two buffers
 // of kSlot bytes; an A item is one buffer of logits, a B item one buffer of
 // logits plus the matching draft probabilities.  Items cover whole race
-// blocks of 256 entries.
-constexpr int kSlot = 12288;
+// blocks of 256 entries; a super-group is 64 consecutive entries.
+constexpr int kSlot = 6144;
 template <bool kBF16>
 struct Geo {
   static constexpr int es = kBF16 ? 2 : 4;                         // logit bytes
-  static constexpr int EA = kSlot / es;                            // A item entries (6144 / 3072)
-  static constexpr int EB = (kSlot / (es + 4)) / kRaceBlock * kRaceBlock;   // B item entries (2048 / 1536)
+  static constexpr int EA = kSlot / es;                            // A item entries (3072 / 1536)
+  static constexpr int EB = (kSlot / (es + 4)) / kRaceBlock * kRaceBlock;   // B item entries (1024 / 768)
   static constexpr int NBA = EA / kRaceBlock;                      // blocks per A item
   static constexpr int NBB = EB / kRaceBlock;                      // blocks per B item
   static constexpr int SPI = EA / 64;                              // 64-entry super-groups per A item
@@ -44,13 +45,10 @@ struct Geo {
 enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
 
 struct WsHeader {
-  uint32_t next;          // next streaming ticket
-  uint32_t ctas_done;     // CTAs that left the kernel
-  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait gave up
-  uint32_t pad0;
-  uint32_t n_class[4];    // rows per class (written by the plan kernel for large batches)
-  uint32_t gnext;         // next general-path unit
-  uint32_t pad[55];
+  uint32_t n_dense;       // drafted unfiltered units listed for the B pass
+  uint32_t ctas_done;     // B-pass CTAs that left the kernel
+  uint32_t error;         // bit 1: a copy wait gave up
+  uint32_t pad[61];
 };
 
 struct ChunkRec {         // 48 bytes, one per (unit, A item)
@@ -101,7 +99,7 @@ __host__ __device__ inline int max_nsm(int V) {
 }
 
 struct Layout {
-  size_t row_ticket, a_ticket, b_ticket, ready, crec, ust, brec, urec, smax, order, total;
+  size_t row_ticket, b_ticket, crec, ust, brec, urec, smax, dlist, total;
 };
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
@@ -109,15 +107,13 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   Layout L;
   size_t off = sizeof(WsHeader);
   L.row_ticket = off; off = align_up(off + (size_t)B * 4, 256);
-  L.a_ticket = off; off = align_up(off + U * 4, 256);
   L.b_ticket = off; off = align_up(off + U * 4, 256);
-  L.ready = off; off = align_up(off + U * 4, 256);
   L.crec = off; off = align_up(off + U * max_nca(V) * sizeof(ChunkRec), 256);
   L.ust = off; off = align_up(off + U * sizeof(UnitState), 256);
   L.brec = off; off = align_up(off + U * max_ncb(V) * sizeof(BRec), 256);
   L.urec = off; off = align_up(off + U * sizeof(UnitRecord), 256);
   L.smax = off; off = align_up(off + U * max_nsm(V) * 4, 256);
-  L.order = off; off = align_up(off + (size_t)B * 4, 256);
+  L.dlist = off; off = align_up(off + U * 4, 256);
   L.total = off;
   return L;
 }
@@ -134,20 +130,17 @@ struct Args {
   uint32_t* flags;
   WsHeader* ws;
   uint32_t* row_ticket;
-  uint32_t* a_ticket;
   uint32_t* b_ticket;
-  uint32_t* ready;
   ChunkRec* crec;
   UnitState* ust;
   BRec* brec;
   UnitRecord* urec;
   float* smax;
-  uint32_t* order;        // rows by class, for batches too large for shared memory
+  uint32_t* dlist;        // drafted unfiltered units, listed by the unit kernel for the B pass
   uint32_t key0, key1;
   int B, k, V, U;
   int NCA, NCB, NSM;      // record strides per unit: A items, B items, super-group maxima
   int n_ctas;             // streaming CTAs
-  int global_order;       // the row order comes from the plan kernel
   int vec_logits;
   int vec_q;
 };
@@ -177,7 +170,7 @@ __device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
   r.c = greedy ? kLog2e : kLog2e / T;
   r.invT = greedy ? 1.0f : 1.0f / T;
   if (greedy) r.type = UT_GREEDY;
-  else if (r.K > 0 && r.K <= kTopkSmall) r.type = UT_TOPK;
+  else if (r.K > 0 && r.K <= kTopkSmall && max_nsm(V) <= kMaxNsmTopk) r.type = UT_TOPK;
   else if (r.K == 0 && r.P >= 1.0f) r.type = UT_DENSE;
   else r.type = UT_GENERAL;
   return r;
@@ -497,7 +490,16 @@ __device__ __forceinline__ void race_scale(Race& r, float sc) {
 // ---------------------------------------------------------------------------
 // Launcher.
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a dependent grid may start while this grid
+// runs; it waits for this grid's completion (and memory) before reading.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <bool kBF16>
-int launch_stream(const Args& A, cudaStream_t stream);
+int launch_stats(const Args& A, cudaStream_t stream);
+template <bool kBF16>
+int launch_units(const Args& A, cudaStream_t stream);
+template <bool kBF16>
+int launch_bpass(const Args& A, cudaStream_t stream);
 
 }  // namespace specv
