@@ -192,18 +192,18 @@ __device__ __forceinline__ Item map_a(const Args& A, const RowPack* cfgs, uint32
   it.row = u / (A.k + 1);
   it.pos = u - it.row * (A.k + 1);
   it.n = min(G::EA, A.V - it.c * G::EA);
-  it.cfg = row_cfg(A, cfgs, it.row);
-  it.kind = it.cfg.type == UT_GENERAL ? 3 : 1;   // general rows are read by the unit kernel itself
+  it.kind = 1;   // the row configuration is looked up when the item is reduced
   return it;
 }
 
 template <bool kBF16>
-__device__ void a_compute(const Args& A, const Item& it, const unsigned char* buf, float* stage) {
+__device__ void a_compute(const Args& A, const Item& it, const unsigned char* buf, float* stage, const RowPack* cfgs) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EA;
-  const RowCfg& cfg = it.cfg;
+  const RowCfg cfg = row_cfg(A, cfgs, it.row);
+  if (cfg.type == UT_GENERAL) return;   // general rows are read by the unit kernel itself
   if (cfg.type == UT_TOPK) {
     // maxima of the 64-entry super-groups: super-group r of block b holds
     // entries [64r, 64r+64), i.e. the first (r < 2) or second half of lanes
@@ -318,45 +318,38 @@ __global__ void __launch_bounds__(kSThreads, 1) stats_kernel(const Args A) {
   // the unit kernel may be scheduled now; it waits for this grid's results
   pdl_trigger();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (lane == 0) {
-    mbar_init(&S.bar[w][0], 1);
-    mbar_init(&S.bar[w][1], 1);
-  }
-  build_cfg(A, S.cfg);
-  fence_mbar_init();
-  __syncthreads();
   const uint32_t nw = (uint32_t)A.n_ctas * kSW;
   const uint32_t total = (uint32_t)A.U * (uint32_t)ceil_div(A.V, G::EA);
   uint32_t t = (uint32_t)blockIdx.x * kSW + (uint32_t)w;
-  auto next_item = [&](uint32_t& tt) -> Item {
-    Item it = map_a<kBF16>(A, S.cfg, tt, total);
-    while (it.kind == 3) {
-      tt += nw;
-      it = map_a<kBF16>(A, S.cfg, tt, total);
-    }
-    tt += nw;
-    return it;
-  };
-  Item ia = next_item(t);
-  Item ib = next_item(t);
+  Item ia = map_a<kBF16>(A, S.cfg, t, total);
+  Item ib = map_a<kBF16>(A, S.cfg, t + nw, total);
+  t += 2 * nw;
   unsigned char* bufa = S.buf[w][0];
   unsigned char* bufb = S.buf[w][1];
   unsigned long long* bara = &S.bar[w][0];
   unsigned long long* barb = &S.bar[w][1];
   uint32_t para = 0u, parb = 0u;
+  // the first two copies go out before the row configurations are read
   if (lane == 0) {
+    mbar_init(bara, 1);
+    mbar_init(barb, 1);
+    fence_mbar_init();
     issue<kBF16>(A, ia, bufa, bara);
     issue<kBF16>(A, ib, bufb, barb);
   }
+  build_cfg(A, S.cfg);
   while (ia.kind != 0) {
     if (!wait_buffer(A, bara, para)) break;
     para ^= 1u;
     if (!A.vec_logits || (ia.n & (kRaceBlock - 1)) != 0) fill_tail<kBF16>(A, ia, bufa);
-    a_compute<kBF16>(A, ia, bufa, S.stage[w]);
+    a_compute<kBF16>(A, ia, bufa, S.stage[w], S.cfg);
     __syncwarp();
     Item in;
     in.kind = 0;
-    if (ib.kind != 0) in = next_item(t);
+    if (ib.kind != 0) {
+      in = map_a<kBF16>(A, S.cfg, t, total);
+      t += nw;
+    }
     if (lane == 0) issue<kBF16>(A, in, bufa, bara);
     ia = ib;
     ib = in;

@@ -33,8 +33,16 @@ constexpr int kGPC = 1024;                 // qualifying super-groups held
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kMaxNsmTopk * 4 <= kMergeCap / 2 * 8, "super-group maxima exceed the buffer");
 
+// The draft token of the unit and its logit and q, read before the stats
+// kernel's records are awaited (they are inputs).
+struct Pre {
+  int x, valid;
+  float lx, qx;
+};
+
 struct alignas(16) UnitShm {
   GenShm g;
+  Pre pre;
   uint32_t cand_count;
   float gmax[kGPC];
   float list_e[kTopkSmall];
@@ -64,23 +72,51 @@ __device__ void bitonic_desc(unsigned long long* s, int n) {
 }
 
 
+// Accept test of the draft at (row, pos) from prefetched operands: accept iff
+// u*q(x) < p(x), the sign of u*q - p taken exactly by one fma; greedy:
+// p(x) = 1 if x is the argmax, else 0.
+__device__ __forceinline__ AcceptInfo accept_pre(const Args& A, int row, int pos, const Pre& pr, bool greedy, int am,
+                                                 float m, float c, float Zs) {
+  AcceptInfo ai;
+  ai.x = pr.x;
+  ai.valid = pr.valid != 0;
+  ai.lx = pr.lx;
+  ai.qx = pr.qx;
+  ai.px = 0.f;
+  if (ai.valid) ai.px = greedy ? (ai.x == am ? 1.0f : 0.0f) : ex2((ai.lx - m) * c) / Zs;
+  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
+  const float u = uniform_of(w.x);
+  const float d = fmaf(u, ai.qx, -ai.px);
+  ai.accept = d < 0.0f;
+  ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
+  return ai;
+}
+
 template <bool kBF16>
-__device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, const RowCfg& cfg, const Pre& pr) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
   const int NC = ceil_div(A.V, G::EA);
   const ChunkRec* R = A.crec + (size_t)u * A.NCA;
+  // one pass over the records: each lane keeps its max, the first chunk
+  // holding it, and its share of the softmax sum relative to that max
   bool nan = false;
-  float m = -INFINITY;
+  float m = -INFINITY, zl = 0.f;
   int cm = 0x7fffffff;
   for (int c = lane; c < NC; c += 32) {
     const float mc = __ldcg(&R[c].m);
+    const float zc = __ldcg(&R[c].z);
     if (mc != mc) {
       nan = true;
-    } else if (mc > m) {
-      m = mc;
-      cm = c;
+    } else if (mc > -INFINITY) {
+      if (mc > m) {
+        zl = (m > -INFINITY ? zl * ex2((m - mc) * cfg.c) : 0.f) + zc;
+        m = mc;
+        cm = c;
+      } else {
+        zl += zc * ex2((mc - m) * cfg.c);
+      }
     }
   }
   nan = __any_sync(kFull, nan);
@@ -95,15 +131,11 @@ __device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, c
     __syncwarp();
     return;
   }
+  const float m_lane = m;
   m = mw;
   const int am = (int)__ldcg(&R[cfirst].amax);
-  // the softmax sum rescaled to the unit max (lane partials in chunk order)
-  float Z = 0.f;
-  for (int c = lane; c < NC; c += 32) {
-    const float mc = __ldcg(&R[c].m);
-    if (mc > -INFINITY) Z += __ldcg(&R[c].z) * ex2((mc - m) * cfg.c);
-  }
-  Z = warp_sum(Z);
+  // the softmax sum rescaled to the unit max (fixed lane order)
+  const float Z = warp_sum(cm != 0x7fffffff ? zl * ex2((m_lane - m) * cfg.c) : 0.f);
   const float lnZ = logf(Z);
   if (cfg.type == UT_GREEDY) {
     if (lane == 0) {
@@ -111,7 +143,7 @@ __device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, c
       bool need_draw = !has_q;
       float q_am = 0.f;
       if (has_q) {
-        const AcceptInfo ai = accept_test(A, row, pos, kBF16, true, am, m, cfg.c, 1.f, nullptr);
+        const AcceptInfo ai = accept_pre(A, row, pos, pr, true, am, m, cfg.c, 1.f);
         if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
         rec.accept = ai.accept ? 1 : 0;
         rec.lp_x = ai.valid ? (ai.lx - m) - lnZ : 0.f;
@@ -163,7 +195,7 @@ __device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, c
   }
   // drafted: accept test, then publish the state for the B items
   if (lane == 0) {
-    const AcceptInfo ai = accept_test(A, row, pos, kBF16, false, am, m, cfg.c, Z, nullptr);
+    const AcceptInfo ai = accept_pre(A, row, pos, pr, false, am, m, cfg.c, Z);
     UnitState st;
     st.m = m;
     st.invZ = 1.0f / Z;
@@ -192,9 +224,11 @@ __device__ __noinline__ void list_unit(const Args& A, UnitShm& S, int u, int row
   const int t = threadIdx.x;
   float e = 0.f;
   uint32_t idx = 0;
+  float q_pre = 0.f;
   if (t < n_k) {
     const unsigned long long key = S.cand[t];
     idx = key64_idx(key);
+    if (has_q) q_pre = A.q[qrow + idx];   // in flight while the list is settled
     e = ex2((from_okey((uint32_t)(key >> 32)) - m) * cfg.c);
     S.list_e[t] = e;
   }
@@ -235,10 +269,10 @@ __device__ __noinline__ void list_unit(const Args& A, UnitShm& S, int u, int row
   const float lnZ = logf(Zs);
   const bool mine = t < n_s;
   const float p = mine ? e * invZ : 0.f;
-  const float qv = (mine && has_q) ? A.q[qrow + idx] : 0.f;
+  const float qv = mine ? q_pre : 0.f;
   int x = -1;
   if (has_q) {
-    x = A.drafts[(size_t)row * A.k + pos];
+    x = S.pre.x;
     if (t == 0) S.g.bci[5] = -1;
     __syncthreads();
     if (mine && idx == (uint32_t)x) S.g.bci[5] = t;
@@ -256,8 +290,8 @@ __device__ __noinline__ void list_unit(const Args& A, UnitShm& S, int u, int row
     ai.x = x;
     ai.valid = x >= 0 && x < A.V;
     ai.px = xi >= 0 ? S.list_e[xi] / Zs : 0.f;
-    ai.qx = ai.valid ? A.q[qrow + x] : 0.f;
-    ai.lx = ai.valid ? load_logit(A, kBF16, lrow + x) : 0.f;
+    ai.qx = S.pre.qx;
+    ai.lx = S.pre.lx;
     const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
     const float uu = uniform_of(w.x);
     const float d = fmaf(uu, ai.qx, -ai.px);
@@ -349,13 +383,23 @@ __device__ __noinline__ void finalize_topk(const Args& A, UnitShm& S, int u, int
   // maxima into shared memory; the unit max; NaN
   unsigned long long best = 0;
   bool nan_seen = false;
-  for (int s = threadIdx.x; s < nsm; s += kThreads) {
-    const float x = __ldcg(src + s);
-    sm[s] = x;
-    if (x != x) nan_seen = true;
-    else {
-      const unsigned long long kk = ((unsigned long long)okey(x) << 32) | (0xffffffffu - (uint32_t)s);
-      best = kk > best ? kk : best;
+  for (int base = threadIdx.x; base < nsm; base += 8 * kThreads) {
+    float xs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int s = base + i * kThreads;
+      xs[i] = s < nsm ? __ldcg(src + s) : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int s = base + i * kThreads;
+      if (s >= nsm) continue;
+      sm[s] = xs[i];
+      if (xs[i] != xs[i]) nan_seen = true;
+      else {
+        const unsigned long long kk = ((unsigned long long)okey(xs[i]) << 32) | (0xffffffffu - (uint32_t)s);
+        best = kk > best ? kk : best;
+      }
     }
   }
   if (nan_seen) best = ~0ull;
@@ -382,9 +426,16 @@ __device__ __noinline__ void finalize_topk(const Args& A, UnitShm& S, int u, int
     S.g.bci[6] = 0;
   }
   __syncthreads();
-  for (int s = threadIdx.x; s < nsm; s += kThreads) {
-    if (kf<kBF16>(sm[s]) >= tau) {
-      const int slot = atomicAdd(&S.g.bci[6], 1);
+  const int lane = threadIdx.x & 31;
+  for (int base = 0; base < nsm; base += kThreads) {
+    const int s = base + threadIdx.x;
+    const bool ok = s < nsm && kf<kBF16>(sm[s]) >= tau;
+    const unsigned b = __ballot_sync(0xffffffffu, ok);
+    int off = 0;
+    if (lane == 0 && b) off = atomicAdd(&S.g.bci[6], __popc(b));
+    off = __shfl_sync(0xffffffffu, off, 0);
+    if (ok) {
+      const int slot = off + __popc(b & ((1u << lane) - 1u));
       if (slot < kGPC) sg[slot] = s;
     }
   }
@@ -392,17 +443,31 @@ __device__ __noinline__ void finalize_topk(const Args& A, UnitShm& S, int u, int
   const int nsg = S.g.bci[6];
   bool ovf = nsg > kGPC;
   if (!ovf) {
-    for (int e = threadIdx.x; e < nsg * 8; e += kThreads) {
-      const int s = sg[e >> 3];
-      const int g = s * 8 + (e & 7);      // super-group s covers groups 8s..8s+7
-      if (g >= G) continue;
+    for (int base = 0; base < nsg * 8; base += kThreads) {
+      const int e = base + threadIdx.x;
+      const int g = e < nsg * 8 ? sg[e >> 3] * 8 + (e & 7) : G;   // super-group s covers groups 8s..8s+7
       float v[8];
-      load_group<kBF16>(A, lrow, g, true, v);
+      if (g < G) load_group<kBF16>(A, lrow, g, true, v);
+      int ups = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (g * 8 + j < A.V && kf<kBF16>(v[j]) >= tau) {
-          const uint32_t slot = atomicAdd(&S.cand_count, 1u);
-          if (slot < (uint32_t)(kMergeCap / 2)) cand[slot] = key64(okey(v[j]), (uint32_t)(g * 8 + j));
+      for (int j = 0; j < 8; ++j) ups += (g < G && g * 8 + j < A.V && kf<kBF16>(v[j]) >= tau) ? 1 : 0;
+      // one shared atomic per warp: an exclusive scan of the lanes' counts
+      int inc = ups;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      uint32_t off = 0;
+      if (lane == 31 && inc) off = atomicAdd(&S.cand_count, (uint32_t)inc);
+      off = __shfl_sync(0xffffffffu, off, 31) + (uint32_t)(inc - ups);
+      if (ups) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (g * 8 + j < A.V && kf<kBF16>(v[j]) >= tau) {
+            if (off < (uint32_t)(kMergeCap / 2)) cand[off] = key64(okey(v[j]), (uint32_t)(g * 8 + j));
+            ++off;
+          }
         }
       }
     }
@@ -432,14 +497,32 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Args A) {
   const RowCfg cfg = classify(A.params[row], A.V);
   // the B pass may be scheduled now; it waits for this grid's results
   pdl_trigger();
+  // the draft token, its logit and q are inputs: read them before waiting
+  if (threadIdx.x == 0) {
+    Pre pr;
+    pr.x = -1;
+    pr.valid = 0;
+    pr.lx = 0.f;
+    pr.qx = 0.f;
+    if (pos < A.k) {
+      pr.x = A.drafts[(size_t)row * A.k + pos];
+      pr.valid = pr.x >= 0 && pr.x < A.V;
+      if (pr.valid) {
+        pr.lx = load_logit(A, kBF16, (size_t)u * A.V + pr.x);
+        pr.qx = A.q[((size_t)row * A.k + pos) * (size_t)A.V + pr.x];
+      }
+    }
+    S.pre = pr;
+  }
   // the stats kernel's records
   pdl_wait();
+  __syncthreads();
   if (cfg.type == UT_GENERAL) {
     unit_general<kBF16>(A, S.g, u, row, pos, cfg);
   } else if (cfg.type == UT_TOPK) {
     finalize_topk<kBF16>(A, S, u, row, pos, cfg);
   } else if (threadIdx.x < 32) {
-    fin_stats<kBF16>(A, u, row, pos, cfg);
+    fin_stats<kBF16>(A, u, row, pos, cfg, S.pre);
   }
 }
 
