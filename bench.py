@@ -33,10 +33,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "spec-verify rows/s at V=151936,k=2; achieved HBM GB/s vs GB300 peak"
-# spec_verify launches three kernels (stats, unit, B pass); their sources
-VERIFY_SOURCES = ["spec_verify.cu", "spec_stream.cu", "spec_unit.cu", "spec_general.cuh",
+# spec_verify launches one cooperative kernel; its sources
+VERIFY_SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_settle.cuh", "spec_general.cuh",
                   "spec_verify_common.cuh", "spec_device.cuh"]
-VERIFY_LAUNCHES = 3
+VERIFY_LAUNCHES = 1
 B, K, V = 64, 2, 151936
 N_SETS = 4   # rotating verify input sets (each ~136 MB, together > L2)
 

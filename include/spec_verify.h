@@ -90,10 +90,12 @@ enum {
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
  * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (a count of listed units, an exit counter, one ticket
- * per row and one ticket per (row, position)) to zero; the
- * records behind them are rewritten before they are read by every call.  So one workspace serves any number of later calls on one
- * stream; two calls that may run concurrently need two workspaces.           */
+ * must start at zero (the 256-byte header of counters, one ticket
+ * per row, and per (row, position) unit a ticket and a ready flag) to
+ * zero; the records behind them are rewritten before they
+ * are read by every call.  So one workspace serves any number of later
+ * calls on one stream; two calls that may run concurrently need two
+ * workspaces.                                                               */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.

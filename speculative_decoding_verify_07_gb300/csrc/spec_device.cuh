@@ -88,6 +88,26 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
       : "memory");
   return ok != 0;
 }
+// The same with an L2 cache policy (createpolicy), e.g. evict-first for data
+// read once, so streamed inputs do not push reused lines out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, unsigned long long* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
@@ -216,7 +236,7 @@ __device__ __forceinline__ void race_init(Race& r) {
 // Score s = w / E with E = -ln U.  Because E >= 1 - U, an entry with
 // w < s1 * (1 - 2^-20) * (1 - U) cannot beat the current best and needs no
 // logarithm; the factor (1 - 2^-20) absorbs the rounding of the test itself.
-static __device__ __noinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
+__device__ __forceinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
   const float om = one_minus_uniform_of(word);
   if (w >= r.s1lo * om) {
     const float E = -log1pf(-om);
@@ -268,7 +288,7 @@ __device__ __forceinline__ Race race_shfl(const Race& r, int src_lane_xor) {
 
 // Deterministic warp merge: lane pairs combine in a fixed xor tree, and the
 // merge itself is order-insensitive for the winner (max score, then min index).
-static __device__ __noinline__ void warp_race_merge(Race& r) {
+__device__ __forceinline__ void warp_race_merge(Race& r) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     Race other = race_shfl(r, o);

@@ -1,11 +1,11 @@
 // spec_verify, general path: rows whose kept set needs a global threshold
 // search (top-p without a small top-k, or a top-k above the candidate-list
-// limit).  One CTA settles one (row, position) unit in passes over its logit
-// row (the first from HBM, later ones mostly from L2): max and argmax, an
+// limit).  One settle group (256 threads) settles one (row, position) unit
+// in passes over its logit row (the first from HBM, later ones mostly from L2): max and argmax, an
 // exact rank select for top-k, a fixed-point mass histogram refined to the
 // exact top-p crossing key, the tie rank by index, Z over the kept set, the
 // accept test, alpha, and the two-level exponential race for the draw.  The
-// streaming kernel runs these units first, CTA by CTA, when a batch has any.
+// settle groups take these units before any other.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -15,7 +15,7 @@
 
 namespace specv {
 
-// Shared memory of a CTA on the general path.
+// Shared memory of a settle group on the general path.
 struct alignas(16) GenShm {
   uint32_t hist[2][256];
   uint32_t mlo[2][256];
@@ -33,51 +33,73 @@ struct alignas(16) GenShm {
 // ---------------------------------------------------------------------------
 __device__ float block_sum(GenShm& S, float a) {
   a = warp_sum(a);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = ctid() >> 5, l = ctid() & 31;
   if (l == 0) S.wred[w] = a;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  csync();
+  if (ctid() == 0) {
     float x = 0.f;
     for (int i = 0; i < kWarps; ++i) x += S.wred[i];
     S.bcf[7] = x;
   }
-  __syncthreads();
+  csync();
   const float r = S.bcf[7];
-  __syncthreads();
+  csync();
   return r;
+}
+
+// Exclusive prefix sum of x over the CTA in thread order; *total = the sum.
+__device__ int block_exclusive_scan(GenShm& S, int x, int* total) {
+  const int w = ctid() >> 5, l = ctid() & 31;
+  int inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (l >= o) inc += y;
+  }
+  int* ws = S.bci;   // kWarps <= 16 entries
+  if (l == 31) ws[w] = inc;
+  csync();
+  int off = 0, tot = 0;
+  for (int i = 0; i < kWarps; ++i) {
+    if (i < w) off += ws[i];
+    tot += ws[i];
+  }
+  csync();
+  *total = tot;
+  return off + inc - x;
 }
 
 __device__ unsigned long long block_max_u64(GenShm& S, unsigned long long v) {
   v = warp_max_u64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = ctid() >> 5, l = ctid() & 31;
   unsigned long long* buf = reinterpret_cast<unsigned long long*>(S.wred);
   if (l == 0) buf[w] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  csync();
+  if (ctid() == 0) {
     unsigned long long x = 0;
     for (int i = 0; i < kWarps; ++i) x = buf[i] > x ? buf[i] : x;
     S.bc64[7] = x;
   }
-  __syncthreads();
+  csync();
   const unsigned long long r = S.bc64[7];
-  __syncthreads();
+  csync();
   return r;
 }
 
 __device__ unsigned long long block_sum_u64(GenShm& S, unsigned long long v) {
   v = warp_sum_u64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = ctid() >> 5, l = ctid() & 31;
   unsigned long long* buf = reinterpret_cast<unsigned long long*>(S.wred);
   if (l == 0) buf[w] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  csync();
+  if (ctid() == 0) {
     unsigned long long x = 0;
     for (int i = 0; i < kWarps; ++i) x += buf[i];
     S.bc64[7] = x;
   }
-  __syncthreads();
+  csync();
   const unsigned long long r = S.bc64[7];
-  __syncthreads();
+  csync();
   return r;
 }
 
@@ -89,12 +111,12 @@ __device__ uint2 block_minmax_u32(GenShm& S, uint32_t mn, uint32_t mx) {
     b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
   }
   uint32_t* wb = reinterpret_cast<uint32_t*>(S.wred);
-  if ((threadIdx.x & 31) == 0) {
-    wb[2 * (threadIdx.x >> 5)] = a;
-    wb[2 * (threadIdx.x >> 5) + 1] = b;
+  if ((ctid() & 31) == 0) {
+    wb[2 * (ctid() >> 5)] = a;
+    wb[2 * (ctid() >> 5) + 1] = b;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  csync();
+  if (ctid() == 0) {
     uint32_t aa = 0, bb = 0;
     for (int i = 0; i < kWarps; ++i) {
       aa = max(aa, wb[2 * i]);
@@ -103,15 +125,15 @@ __device__ uint2 block_minmax_u32(GenShm& S, uint32_t mn, uint32_t mx) {
     S.bci[12] = (int)~aa;
     S.bci[13] = (int)bb;
   }
-  __syncthreads();
+  csync();
   const uint2 r = make_uint2((uint32_t)S.bci[12], (uint32_t)S.bci[13]);
-  __syncthreads();
+  csync();
   return r;
 }
 
 __device__ Race block_race(GenShm& S, Race r) {
   warp_race_merge(r);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int w = ctid() >> 5, l = ctid() & 31;
   float* f = S.wred;
   if (l == 0) {
     f[w * 5 + 0] = r.s1;
@@ -120,35 +142,21 @@ __device__ Race block_race(GenShm& S, Race r) {
     f[w * 5 + 3] = r.t2;
     f[w * 5 + 4] = __uint_as_float(r.v1);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Race a;
-    race_init(a);
-    for (int i = 0; i < kWarps; ++i) {
-      Race b;
-      b.s1 = f[i * 5 + 0];
-      b.t1 = f[i * 5 + 1];
-      b.s2 = f[i * 5 + 2];
-      b.t2 = f[i * 5 + 3];
-      b.v1 = __float_as_uint(f[i * 5 + 4]);
-      b.s1lo = 0.f;
-      race_merge(a, b);
-    }
-    S.bcf[0] = a.s1;
-    S.bcf[1] = a.t1;
-    S.bcf[2] = a.s2;
-    S.bcf[3] = a.t2;
-    S.bci[0] = (int)a.v1;
-  }
-  __syncthreads();
+  csync();
+  // every warp merges the warps' results itself (lanes 0..kWarps-1; the
+  // winner and runner-up do not depend on the merge order)
   Race o;
-  o.s1 = S.bcf[0];
-  o.t1 = S.bcf[1];
-  o.s2 = S.bcf[2];
-  o.t2 = S.bcf[3];
-  o.v1 = (uint32_t)S.bci[0];
+  race_init(o);
+  if (l < kWarps) {
+    o.s1 = f[l * 5 + 0];
+    o.t1 = f[l * 5 + 1];
+    o.s2 = f[l * 5 + 2];
+    o.t2 = f[l * 5 + 3];
+    o.v1 = __float_as_uint(f[l * 5 + 4]);
+  }
+  warp_race_merge(o);
   o.s1lo = 0.f;
-  __syncthreads();
+  csync();
   return o;
 }
 
@@ -157,8 +165,8 @@ __device__ Race block_race(GenShm& S, Race r) {
 // the bins before it.  Warp 0 scans; the result is broadcast.
 __device__ void select_from_bin0(GenShm& S, unsigned long long need, int* out_bin,
                                  unsigned long long* out_above) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  if (ctid() < 32) {
+    const int lane = ctid();
     unsigned long long own = 0;
     for (int i = 0; i < 8; ++i) own += S.total[8 * lane + i];
     unsigned long long inc = own;
@@ -185,14 +193,14 @@ __device__ void select_from_bin0(GenShm& S, unsigned long long need, int* out_bi
       S.bc64[1] = above;
     }
   }
-  __syncthreads();
+  csync();
   *out_bin = S.bci[2];
   *out_above = S.bc64[1];
-  __syncthreads();
+  csync();
 }
 
 // ---------------------------------------------------------------------------
-// Rank select on distances from the maximum (one CTA).  Values are described
+// Rank select on distances from the maximum (one settle group).  Values are described
 // by d = key(max) - key(v) >= 0 in the order-key space, so the largest values
 // have the smallest distances.  Finds the distance of the value at 1-based
 // rank `need` (counting multiplicity) among the values `each` enumerates.
@@ -204,19 +212,19 @@ __device__ void select_from_bin0(GenShm& S, unsigned long long need, int* out_bi
 template <typename Each>
 __device__ uint32_t kth_distance(GenShm& S, Each each, unsigned long long& need, int s0, int dbits) {
   auto reduce = [&](int slot) {
-    S.total[threadIdx.x] = S.hist[slot][threadIdx.x];
-    __syncthreads();
+    S.total[ctid()] = S.hist[slot][ctid()];
+    csync();
   };
   int hs = 0;
   {
     const int slot = hs++ & 1;
-    S.hist[slot][threadIdx.x] = 0;
-    __syncthreads();
+    S.hist[slot][ctid()] = 0;
+    csync();
     const uint32_t lim = 255u << s0;
     each([&](uint32_t d) {
       if (d < lim) atomicAdd(&S.hist[slot][d >> s0], 1u);
     });
-    __syncthreads();
+    csync();
     reduce(slot);
     int b;
     unsigned long long below;
@@ -226,13 +234,13 @@ __device__ uint32_t kth_distance(GenShm& S, Each each, unsigned long long& need,
       uint32_t base = (uint32_t)b << s0;
       for (int s = s0 - 8; s >= 0; s -= 8) {
         const int sl = hs++ & 1;
-        S.hist[sl][threadIdx.x] = 0;
-        __syncthreads();
+        S.hist[sl][ctid()] = 0;
+        csync();
         const uint32_t span = 1u << (s + 8);
         each([&](uint32_t d) {
           if (d >= base && d - base < span) atomicAdd(&S.hist[sl][(d - base) >> s], 1u);
         });
-        __syncthreads();
+        csync();
         reduce(sl);
         int bb;
         unsigned long long bl;
@@ -246,12 +254,12 @@ __device__ uint32_t kth_distance(GenShm& S, Each each, unsigned long long& need,
   uint32_t prefix = 0u, mask = 0u;
   for (int shift = dbits - 8; shift >= 0; shift -= 8) {
     const int slot = hs++ & 1;
-    S.hist[slot][threadIdx.x] = 0;
-    __syncthreads();
+    S.hist[slot][ctid()] = 0;
+    csync();
     each([&](uint32_t d) {
       if ((d & mask) == prefix) atomicAdd(&S.hist[slot][(d >> shift) & 255u], 1u);
     });
-    __syncthreads();
+    csync();
     reduce(slot);
     int b;
     unsigned long long below;
@@ -276,7 +284,7 @@ __device__ __forceinline__ unsigned long long mass_fixed(float e) {
   return __float2ull_rz(e * 1099511627776.0f);   // e * 2^40, e in [0, 1]
 }
 
-// Level 1 over a whole row, one CTA: every warp-row of 32 groups is one race
+// Level 1 over a whole row, one settle group: every warp-row of 32 groups is one race
 // block.  Returns the winning block's race state (v1 = block) in every thread.
 template <bool kBF16>
 __device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
@@ -284,11 +292,11 @@ __device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, floa
   const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const int G = (A.V + 7) / 8;
-  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int lane = ctid() & 31, wp = ctid() >> 5;
   Race r;
   race_init(r);
   for (int base = 0; base < G; base += kThreads) {
-    const int g = base + threadIdx.x;
+    const int g = base + ctid();
     float w8 = 0.f, u8 = 0.f;
     if (g < G) {
       float w[8], tq[8];
@@ -309,7 +317,7 @@ __device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, floa
   return block_race(S, r);
 }
 
-// The full two-level draw over a row by one CTA; returns the drawn entry
+// The full two-level draw over a row by one settle group; returns the drawn entry
 // (or 0xffffffff when every weight is 0) and sets *margin.
 template <bool kBF16>
 __device__ uint32_t draw_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
@@ -319,22 +327,22 @@ __device__ uint32_t draw_row(const Args& A, GenShm& S, int row, int pos, float m
     *margin = false;
     return 0xffffffffu;
   }
-  if (threadIdx.x < 32) {
+  if (ctid() < 32) {
     const Race l2 = race_in_block<kBF16>(A, row, pos, l1.v1, m, c, invZ, mode, th);
-    if (threadIdx.x == 0) {
+    if (ctid() == 0) {
       S.bci[8] = (int)l2.v1;
       S.bci[9] = (draw_margin(l1) || draw_margin(l2)) ? 1 : 0;
     }
   }
-  __syncthreads();
+  csync();
   const uint32_t y = (uint32_t)S.bci[8];
   *margin = S.bci[9] != 0;
-  __syncthreads();
+  csync();
   return y;
 }
 
 // ---------------------------------------------------------------------------
-// The general path: one CTA settles a unit whose kept set needs a global
+// The general path: one settle group settles a unit whose kept set needs a global
 // threshold (top-p without a small top-k, or a large top-k), in passes over
 // the logit row (the first from HBM, later ones mostly from L2).  The kept
 // set is a prefix of the total order, described by a Thresh.
@@ -348,7 +356,7 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
   unsigned long long need = n;
   uint32_t found = 0xffffffffu;
   for (int base = 0; base < G; base += kThreads) {
-    const int g = base + threadIdx.x;
+    const int g = base + ctid();
     int c = 0;
     float v[8];
     if (g < G) {
@@ -358,7 +366,7 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
         if (g * 8 + i < A.V && okey(v[i]) == tkey) ++c;
     }
     int inc = c;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lane = ctid() & 31, w = ctid() >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, inc, o);
@@ -366,7 +374,7 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
     }
     int* wsum = reinterpret_cast<int*>(S.wred);
     if (lane == 31) wsum[w] = inc;
-    __syncthreads();
+    csync();
     int woff = 0, rowtot = 0;
     for (int i = 0; i < kWarps; ++i) {
       if (i < w) woff += wsum[i];
@@ -382,14 +390,14 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
         }
       }
     }
-    __syncthreads();
+    csync();
     if (need <= (unsigned long long)rowtot) {
       found = (uint32_t)S.bci[3];
-      __syncthreads();
+      csync();
       break;
     }
     need -= (unsigned long long)rowtot;
-    __syncthreads();
+    csync();
   }
   return found;
 }
@@ -403,7 +411,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   // pass 1: max, argmax, NaN
   unsigned long long best = 0;
   bool nan_seen = false;
-  for (int g = threadIdx.x; g < G; g += kThreads) {
+  for (int g = ctid(); g < G; g += kThreads) {
     float v[8];
     load_group<kBF16>(A, lrow, g, true, v);
     const float gm = group_max(v);
@@ -422,8 +430,8 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   const float m = from_okey((uint32_t)(best >> 32));
   const int am = (int)key64_idx(best);
   if (best == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
-    if (threadIdx.x == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
-    __syncthreads();
+    if (ctid() == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    csync();
     return;
   }
   uint32_t flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
@@ -437,7 +445,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   if (cfg.K > 0) {
     unsigned long long need = (unsigned long long)cfg.K;
     auto each = [&](auto fn) {
-      for (int g = threadIdx.x; g < G; g += kThreads) {
+      for (int g = ctid(); g < G; g += kThreads) {
         float v[8];
         load_group<kBF16>(A, lrow, g, true, v);
 #pragma unroll
@@ -454,12 +462,12 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   // Z pass over the top-k set; with top-p also a fixed-point mass histogram
   // binned by log2 of the weight in steps of 1/8 (the last bin in registers).
   const int hslot = 0;
-  S.mlo[hslot][threadIdx.x] = 0;
-  S.mhi[hslot][threadIdx.x] = 0;
-  __syncthreads();
+  S.mlo[hslot][ctid()] = 0;
+  S.mhi[hslot][ctid()] = 0;
+  csync();
   unsigned long long tail = 0;
   float z0 = 0.f, z1 = 0.f;
-  for (int g = threadIdx.x; g < G; g += kThreads) {
+  for (int g = ctid(); g < G; g += kThreads) {
     float v[8];
     load_group<kBF16>(A, lrow, g, true, v);
 #pragma unroll
@@ -478,23 +486,23 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   }
   float Zs;
   if (topp) {
-    __syncthreads();
+    csync();
     tail = block_sum_u64(S, tail);
-    if (threadIdx.x == 0) {
+    if (ctid() == 0) {
       S.mlo[hslot][255] = (uint32_t)tail;
       S.mhi[hslot][255] = (uint32_t)(tail >> 32);
     }
-    __syncthreads();
-    S.total[threadIdx.x] = ((unsigned long long)S.mhi[hslot][threadIdx.x] << 32) + S.mlo[hslot][threadIdx.x];
-    __syncthreads();
-    const unsigned long long zk = block_sum_u64(S, S.total[threadIdx.x]);
+    csync();
+    S.total[ctid()] = ((unsigned long long)S.mhi[hslot][ctid()] << 32) + S.mlo[hslot][ctid()];
+    csync();
+    const unsigned long long zk = block_sum_u64(S, S.total[ctid()]);
     const unsigned long long target = (unsigned long long)ceil((double)cfg.P * (double)zk);
     int b;
     unsigned long long above;
     select_from_bin0(S, target, &b, &above);
     // key range of bin b
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int g = threadIdx.x; g < G; g += kThreads) {
+    for (int g = ctid(); g < G; g += kThreads) {
       float v[8];
       load_group<kBF16>(A, lrow, g, true, v);
 #pragma unroll
@@ -519,10 +527,10 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
       const int nbits = 32 - __clz(span);
       const int shift = nbits > 8 ? nbits - 8 : 0;
       const int slot = hs++ & 1;
-      S.mlo[slot][threadIdx.x] = 0;
-      S.mhi[slot][threadIdx.x] = 0;
-      __syncthreads();
-      for (int g = threadIdx.x; g < G; g += kThreads) {
+      S.mlo[slot][ctid()] = 0;
+      S.mhi[slot][ctid()] = 0;
+      csync();
+      for (int g = ctid(); g < G; g += kThreads) {
         float v[8];
         load_group<kBF16>(A, lrow, g, true, v);
 #pragma unroll
@@ -535,9 +543,9 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
           mass_add(&S.mlo[slot][bin], &S.mhi[slot][bin], mass_fixed(ex2((v[i] - m) * c)));
         }
       }
-      __syncthreads();
-      S.total[threadIdx.x] = ((unsigned long long)S.mhi[slot][threadIdx.x] << 32) + S.mlo[slot][threadIdx.x];
-      __syncthreads();
+      csync();
+      S.total[ctid()] = ((unsigned long long)S.mhi[slot][ctid()] << 32) + S.mlo[slot][ctid()];
+      csync();
       int sb;
       unsigned long long ab;
       select_from_bin0(S, rem, &sb, &ab);
@@ -584,7 +592,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   // alpha pass
   float al0 = 0.f, al1 = 0.f;
   if (has_q) {
-    for (int g = threadIdx.x; g < G; g += kThreads) {
+    for (int g = ctid(); g < G; g += kThreads) {
       float v[8], qv[8];
       load_group<kBF16>(A, lrow, g, true, v);
       load_q8(A, qrow, g * 8, qv);
@@ -609,7 +617,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
     }
     if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
   }
-  if (threadIdx.x == 0) {
+  if (ctid() == 0) {
     UnitRecord rec = empty_record(flags);
     if (has_q) {
       if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
@@ -626,7 +634,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
     }
     commit_record(A, u, row, rec);
   }
-  __syncthreads();
+  csync();
 }
 
 }  // namespace specv

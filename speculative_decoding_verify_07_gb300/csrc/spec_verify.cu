@@ -1,13 +1,14 @@
 // spec_verify: batched speculative-decoding verify sampler for sm_103a --
 // argument checks, workspace carving and the launch.
 //
-// Three kernels on the caller's stream, chained by programmatic dependent
-// launch, with no host synchronisation: the stats kernel streams every logit
-// row once (spec_stream.cu), the unit kernel settles every (row, position)
-// with one CTA (spec_unit.cu; rows that need a global threshold search take
-// the general path, spec_general.cuh), and the B pass streams the draft
-// probabilities of drafted positions over unfiltered distributions
-// (spec_stream.cu).
+// One persistent kernel on the caller's stream, with no host
+// synchronisation (spec_kernel.cu): streaming warps reduce every logit row
+// once and stream the draft probabilities of drafted positions over
+// unfiltered distributions, while a settle group per CTA settles each
+// (row, position) as soon as its chunks are reduced (spec_settle.cuh; rows
+// that need a global threshold search take the general path,
+// spec_general.cuh).  Batches beyond 512 rows get a one-CTA planning kernel
+// first.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -63,12 +64,13 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   A.ws = reinterpret_cast<specv::WsHeader*>(ws);
   A.row_ticket = reinterpret_cast<uint32_t*>(ws + L.row_ticket);
   A.b_ticket = reinterpret_cast<uint32_t*>(ws + L.b_ticket);
+  A.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
   A.crec = reinterpret_cast<specv::ChunkRec*>(ws + L.crec);
   A.ust = reinterpret_cast<specv::UnitState*>(ws + L.ust);
   A.brec = reinterpret_cast<specv::BRec*>(ws + L.brec);
   A.urec = reinterpret_cast<specv::UnitRecord*>(ws + L.urec);
   A.smax = reinterpret_cast<float*>(ws + L.smax);
-  A.dlist = reinterpret_cast<uint32_t*>(ws + L.dlist);
+  A.order = reinterpret_cast<uint32_t*>(ws + L.order);
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);
   A.B = B;
@@ -81,10 +83,5 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   A.vec_logits = aligned(logits, 16) && ((size_t)V * es) % 16 == 0;
   A.vec_q = k > 0 && aligned(draft_probs, 16) && (V % 4) == 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
-  const bool bf16 = logits_dtype == SPEC_BF16;
-  int rc = bf16 ? specv::launch_stats<true>(A, st) : specv::launch_stats<false>(A, st);
-  if (rc != SPEC_OK) return rc;
-  rc = bf16 ? specv::launch_units<true>(A, st) : specv::launch_units<false>(A, st);
-  if (rc != SPEC_OK) return rc;
-  return bf16 ? specv::launch_bpass<true>(A, st) : specv::launch_bpass<false>(A, st);
+  return logits_dtype == SPEC_BF16 ? specv::launch_verify<true>(A, st) : specv::launch_verify<false>(A, st);
 }

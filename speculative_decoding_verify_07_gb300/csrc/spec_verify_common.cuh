@@ -45,11 +45,21 @@ struct Geo {
 enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
 
 struct WsHeader {
-  uint32_t n_dense;       // drafted unfiltered units listed for the B pass
-  uint32_t ctas_done;     // B-pass CTAs that left the kernel
-  uint32_t error;         // bit 1: a copy wait gave up
-  uint32_t pad[61];
+  uint32_t gnext;         // next general-path unit
+  uint32_t arrived;       // CTAs through the grid barrier
+  uint32_t ctas_done;     // CTAs that left the kernel
+  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait; bit 2: the grid barrier
+  uint32_t pad0[4];
+  uint32_t n_class[4];    // rows per class (batches above the shared-memory order limit)
+  uint32_t pad[52];
 };
+
+// Settle groups of the general path: each half of a CTA (256 threads) runs
+// the group-wide code on its own named barrier (ids 1 and 2).
+__device__ __forceinline__ int ctid() { return (int)(threadIdx.x & 255u); }
+__device__ __forceinline__ void csync() {
+  asm volatile("bar.sync %0, 256;" ::"r"(1 + (int)(threadIdx.x >> 8)) : "memory");
+}
 
 struct ChunkRec {         // 48 bytes, one per (unit, A item)
   float m;                // chunk max (NaN when the chunk holds a NaN)
@@ -99,7 +109,7 @@ __host__ __device__ inline int max_nsm(int V) {
 }
 
 struct Layout {
-  size_t row_ticket, b_ticket, crec, ust, brec, urec, smax, dlist, total;
+  size_t row_ticket, b_ticket, ready, crec, ust, brec, urec, smax, order, total;
 };
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
@@ -108,12 +118,13 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   size_t off = sizeof(WsHeader);
   L.row_ticket = off; off = align_up(off + (size_t)B * 4, 256);
   L.b_ticket = off; off = align_up(off + U * 4, 256);
+  L.ready = off; off = align_up(off + U * 4, 256);
   L.crec = off; off = align_up(off + U * max_nca(V) * sizeof(ChunkRec), 256);
   L.ust = off; off = align_up(off + U * sizeof(UnitState), 256);
   L.brec = off; off = align_up(off + U * max_ncb(V) * sizeof(BRec), 256);
   L.urec = off; off = align_up(off + U * sizeof(UnitRecord), 256);
   L.smax = off; off = align_up(off + U * max_nsm(V) * 4, 256);
-  L.dlist = off; off = align_up(off + U * 4, 256);
+  L.order = off; off = align_up(off + (size_t)B * 4, 256);
   L.total = off;
   return L;
 }
@@ -130,17 +141,19 @@ struct Args {
   uint32_t* flags;
   WsHeader* ws;
   uint32_t* row_ticket;
-  uint32_t* b_ticket;
+  uint32_t* b_ticket;     // B items done per drafted unfiltered unit
+  uint32_t* ready;        // the unit state of a drafted unfiltered unit is published
   ChunkRec* crec;
   UnitState* ust;
   BRec* brec;
   UnitRecord* urec;
   float* smax;
-  uint32_t* dlist;        // drafted unfiltered units, listed by the unit kernel for the B pass
+  uint32_t* order;        // rows by class (batches above the shared-memory order limit)
   uint32_t key0, key1;
   int B, k, V, U;
   int NCA, NCB, NSM;      // record strides per unit: A items, B items, super-group maxima
-  int n_ctas;             // streaming CTAs
+  int n_ctas;             // CTAs of the kernel
+  int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;
 };
@@ -490,16 +503,7 @@ __device__ __forceinline__ void race_scale(Race& r, float sc) {
 // ---------------------------------------------------------------------------
 // Launcher.
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch: a dependent grid may start while this grid
-// runs; it waits for this grid's completion (and memory) before reading.
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 template <bool kBF16>
-int launch_stats(const Args& A, cudaStream_t stream);
-template <bool kBF16>
-int launch_units(const Args& A, cudaStream_t stream);
-template <bool kBF16>
-int launch_bpass(const Args& A, cudaStream_t stream);
+int launch_verify(const Args& A, cudaStream_t stream);
 
 }  // namespace specv

@@ -162,10 +162,11 @@ def test_empty_batch_and_workspace_left_clean():
     for _ in range(3):
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
-    # the counters (256-byte header), the per-row tickets and the per-unit
-    # tickets (each array padded to 256 bytes) are back at zero
+    # the counters (256-byte header), the per-row tickets and the two
+    # per-unit arrays (B-item tickets and state-ready flags; each array
+    # padded to 256 bytes) are back at zero
     B, U = 5, 5 * 4
-    zero_prefix = 256 + 256 * ((B * 4 + 255) // 256) + 256 * ((U * 4 + 255) // 256)
+    zero_prefix = 256 + 256 * ((B * 4 + 255) // 256) + 2 * 256 * ((U * 4 + 255) // 256)
     assert int(ws[:zero_prefix].count_nonzero()) == 0
     # dirty records behind them do not matter: results stay identical
     ref = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
