@@ -90,12 +90,12 @@ enum {
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
  * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (the 256-byte header of counters, one ticket
- * per row, and per (row, position) unit a ticket and a ready flag) to
- * zero; the records behind them are rewritten before they
- * are read by every call.  So one workspace serves any number of later
- * calls on one stream; two calls that may run concurrently need two
- * workspaces.                                                               */
+ * must start at zero (the counters at the start of the 256-byte header and
+ * one ticket per row) to zero and advances an epoch word in the header;
+ * every record behind them carries the epoch of the call that wrote it, so
+ * stale or foreign contents are never read as this call's.  One workspace
+ * serves any number of later calls on one stream; two calls that may run
+ * concurrently need two workspaces.                                         */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.
@@ -178,9 +178,9 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
  * library (a file-scope device array, held on every GPU that loads the
  * library until the process exits).  The call allocates nothing.
  *   - Limit: spec_verify_workspace_size(B, k, V) must not exceed
- *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 140 bytes
+ *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 170 bytes
  *     per (row, position) unit per 1024 vocabulary entries, so at V = 151936
- *     about 400 units fit, e.g. 128 rows at k = 2); a larger batch returns
+ *     about 325 units fit, e.g. 108 rows at k = 2); a larger batch returns
  *     SPEC_E_WORKSPACE and enqueues nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call

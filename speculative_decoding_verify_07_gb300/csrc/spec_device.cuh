@@ -21,8 +21,10 @@ constexpr float kMargin = 1e-6f;
 // (X0,X1,X2,X3) -> (hi(M1 X2)^X1^K0, lo(M1 X2), hi(M0 X0)^X3^K1, lo(M0 X0)),
 // and bumps the key by the Weyl constants; ten rounds.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
+// Out of line with a rolled loop: the verify kernel runs it from many
+// places, and a small body keeps the instruction stream short.
+static __device__ __noinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll 1
   for (int i = 0; i < 10; ++i) {
     const uint32_t lo0 = 0xD2511F53u * c.x;
     const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
@@ -236,7 +238,7 @@ __device__ __forceinline__ void race_init(Race& r) {
 // Score s = w / E with E = -ln U.  Because E >= 1 - U, an entry with
 // w < s1 * (1 - 2^-20) * (1 - U) cannot beat the current best and needs no
 // logarithm; the factor (1 - 2^-20) absorbs the rounding of the test itself.
-__device__ __forceinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
+static __device__ __noinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
   const float om = one_minus_uniform_of(word);
   if (w >= r.s1lo * om) {
     const float E = -log1pf(-om);
@@ -288,8 +290,8 @@ __device__ __forceinline__ Race race_shfl(const Race& r, int src_lane_xor) {
 
 // Deterministic warp merge: lane pairs combine in a fixed xor tree, and the
 // merge itself is order-insensitive for the winner (max score, then min index).
-__device__ __forceinline__ void warp_race_merge(Race& r) {
-#pragma unroll
+static __device__ __noinline__ void warp_race_merge(Race& r) {
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     Race other = race_shfl(r, o);
     // keep the lower lane's state first so both lanes compute the same result

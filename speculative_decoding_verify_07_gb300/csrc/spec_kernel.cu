@@ -1,29 +1,34 @@
 // spec_verify: the verify kernel (sm_103a).
 //
 // One persistent CTA of 16 warps per SM, launched cooperatively (all CTAs
-// resident), in two phases split by one grid barrier:
-//   * Stream phase.  Every warp owns two 6 KB shared-memory buffers and has
-//     the copy engine stream its next item into one (cp.async.bulk completed
-//     on an mbarrier) while it reduces the other with warp collectives.  An A
-//     item is a chunk of one unit's logits (3072 bf16 / 1536 fp32): max and
-//     first argmax, the softmax sum relative to the chunk max, at an
-//     unfiltered bonus position the level-1 race of the chunk's 256-entry
-//     blocks, for a small top-k the maxima of its 64-entry super-groups.
-//     Items are dealt round robin over the warps of all SMs; a warp stores
-//     its records with plain stores and takes no ticket.
-//   * Settle phase.  Each settle task is one unit, settled by one warp
-//     (spec_settle.cuh): drafted unfiltered units first (they publish the
-//     state the B items wait for), then small top-k units, bonus positions
-//     and greedy units.  The other warps stream the B items of the drafted
-//     unfiltered units (1024 bf16 / 768 fp32 logits, from L2, plus q):
-//     alpha = sum min(p, q) and the level-1 race of the residual; each warp
-//     takes a contiguous range, reads a unit's state once per run, and the
-//     warp that completes a unit settles it.  Rows that need a global
-//     threshold search (spec_general.cuh) are taken last by half-CTA groups.
+// resident, so warps may wait on one another).  Nothing in it waits on a
+// barrier across CTAs and nothing stores with a fence: results pass between
+// warps as 64-bit words tagged with the call's epoch, which a reader polls.
+//   * Stream warps.  Each owns two 6 KB shared-memory buffers and has the
+//     copy engine stream its next item into one (cp.async.bulk completed on
+//     an mbarrier) while it reduces the other with warp collectives.  The
+//     items of all units form one sequence, dealt round robin over the
+//     stream warps of all SMs:
+//       A items of drafted unfiltered units, of small top-k units, of
+//       unfiltered bonus positions; B items of drafted unfiltered units; A
+//       items of greedy units.
+//     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
+//     max, the softmax sum relative to the chunk max, for greedy units the
+//     first argmax, at a bonus position the level-1 race of the chunk's
+//     256-entry blocks, for a small top-k the chunk's first 8 entries in the
+//     total order.  A B item (1024 bf16 / 768 fp32 logits, read again from
+//     L2, plus q) takes the unit state from its tagged words and computes
+//     alpha = sum min(p, q) and the level-1 race of the residual.
+//   * Settle warps (the first warps of every SM).  Each takes its units in
+//     the same class order, waits for their records and settles them
+//     (spec_settle.cuh); a drafted unfiltered unit publishes its state for
+//     the B items and is finished after them.
+//   * Rows that need a global threshold search (spec_general.cuh) are taken
+//     last by half-CTA groups.
 // The last settled unit of a row resolves the accept chain and writes the
-// row's outputs.  Every wait is bounded and ends with an error bit; reductions
-// have a fixed order and no floating-point atomics are used, so results are
-// bit-reproducible.
+// row's outputs.  Every wait is bounded and ends with an error bit;
+// reductions have a fixed order and no floating-point atomics are used, so
+// results are bit-reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,9 +44,8 @@ namespace specv {
 constexpr int kSW = 16;                // warps per CTA
 constexpr int kAllThreads = kSW * 32;
 constexpr int kOrderSmem = 512;        // batches up to this many rows keep order and configs in shared memory
-constexpr int kStage = 64;             // per-warp staging floats (super-group maxima of an item)
+constexpr int kStage = 64;             // per-warp staging of a top-k item's candidates
 constexpr unsigned kFull = 0xffffffffu;
-static_assert(Geo<true>::SPI <= kStage && Geo<false>::SPI <= kStage, "staging too small");
 static_assert(kAllThreads == 2 * kThreads, "two general-path groups per CTA");
 
 struct OrderScratch {
@@ -53,14 +57,15 @@ struct OrderScratch {
 struct alignas(128) VShm {
   union {
     unsigned char buf[kSW][2][kSlot];  // stream buffers; a settle warp's pair is its top-k scratch
-    GenShm gen[2];                     // general-path groups, after the settle phase
+    GenShm gen[2];                     // general-path groups, at the end
   };
   unsigned long long bar[kSW][2];
-  float stage[kSW][kStage];
+  u64 stage[kSW][kStage];
   uint32_t order[kOrderSmem];
   RowPack cfg[kOrderSmem];
   OrderScratch ord;
   int gtask[2];
+  uint32_t tag;
 };
 static_assert(sizeof(GenShm) * 2 <= sizeof(unsigned char) * kSW * 2 * kSlot, "general scratch");
 
@@ -101,8 +106,6 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
 
 static_assert(kOrderSmem == kAllThreads, "one placement round for a shared-memory order");
 
-static_assert(kOrderSmem == kAllThreads, "one placement round for a shared-memory order");
-
 // Batches of up to kOrderSmem rows: every CTA classifies the rows into
 // shared memory (one parameter load per row).
 __device__ __noinline__ void build_order_smem(const Args& A, uint32_t* order, RowPack* cfgs, OrderScratch& O) {
@@ -124,8 +127,8 @@ __device__ __noinline__ void build_order_smem(const Args& A, uint32_t* order, Ro
 }
 
 // Larger batches: CTA 0 writes the order and the class counts into the
-// workspace before the grid barrier; the other CTAs read them after it.
-__device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O) {
+// workspace and publishes them with the call's tag; the other CTAs wait for it.
+__device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, uint32_t tag) {
   const int tid = threadIdx.x;
   if (tid < 4) {
     O.n_class[tid] = 0;
@@ -139,6 +142,11 @@ __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O) 
     place_round(A.order, O, r, r < A.B ? classify(A.params[r], A.V).type : -1);
   }
   if (tid < 4) A.ws->n_class[tid] = (uint32_t)O.n_class[tid];
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    store_release(&A.ws->order_tag, tag);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -149,6 +157,7 @@ struct Plan {
   const RowPack* cfg;       // per-row configs in shared memory (null: classify from the parameters)
   int nD, nT, nG, nX;       // rows: unfiltered, small top-k, greedy, general
   int NCA, NCB;
+  uint32_t sDD, sTK, sDB, sB, sGR;   // segments of the item sequence
 };
 
 // A work item.  kind: 0 none, 1 A item, 2 B item.
@@ -162,61 +171,58 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row
   return P.cfg ? unpack_cfg(P.cfg[row]) : classify(A.params[row], A.V);
 }
 
-// A item of ticket t in unit order (every unit, no configuration needed).
+
+// Item t of the sequence [A: drafted unfiltered][A: small top-k][A: bonus
+// positions][B: drafted unfiltered][A: greedy].
 template <bool kBF16>
-__device__ __forceinline__ Item map_a_raw(const Args& A, int NCA, uint32_t t) {
+__device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
-  if (t >= (uint32_t)A.U * (uint32_t)NCA) return it;
-  it.u = (int)(t / (uint32_t)NCA);
-  it.c = (int)t - it.u * NCA;
-  it.row = it.u / (A.k + 1);
-  it.pos = it.u - it.row * (A.k + 1);
-  it.n = min(G::EA, A.V - it.c * G::EA);
-  it.reread = 1;
-  it.kind = 1;
-  return it;
-}
-
-// The next A item from ticket *t on (step nw), skipping rows of the general
-// path; reread marks drafted unfiltered units, whose B items read the logits again.
-template <bool kBF16>
-__device__ __forceinline__ Item next_a(const Args& A, const Plan& P, uint32_t& t, uint32_t nw) {
-  while (true) {
-    Item it = map_a_raw<kBF16>(A, P.NCA, t);
-    t += nw;
-    if (it.kind == 0) return it;
-    const RowCfg cfg = plan_cfg(A, P, it.row);
-    if (cfg.type == UT_GENERAL) continue;
-    it.reread = (cfg.type == UT_DENSE && it.pos < A.k) ? 1 : 0;
+  const int k = A.k, k1 = A.k + 1;
+  int row, pos, j;
+  uint32_t s = t;
+  it.reread = 0;
+  if (s < P.sDD) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[j / k];
+    pos = j % k;
+    it.reread = 1;
+    it.kind = 1;
+  } else if ((s -= P.sDD) < P.sTK) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[P.nD + j / k1];
+    pos = j % k1;
+    it.kind = 1;
+  } else if ((s -= P.sTK) < P.sDB) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[j];
+    pos = k;
+    it.kind = 1;
+  } else if ((s -= P.sDB) < P.sB) {
+    j = (int)(s / (uint32_t)P.NCB);
+    it.c = (int)s - j * P.NCB;
+    row = (int)P.order[j / k];
+    pos = j % k;
+    it.kind = 2;
+  } else if ((s -= P.sB) < P.sGR) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[P.nD + P.nT + j / k1];
+    pos = j % k1;
+    it.kind = 1;
+  } else {
     return it;
   }
-}
-
-template <bool kBF16>
-__device__ __forceinline__ Item map_b(const Args& A, const Plan& P, uint32_t t, uint32_t end) {
-  using G = Geo<kBF16>;
-  Item it;
-  it.kind = 0;
-  if (t >= end) return it;
-  const int j = (int)(t / (uint32_t)P.NCB);
-  it.c = (int)t - j * P.NCB;
-  it.row = (int)P.order[j / A.k];
-  it.pos = j % A.k;
-  it.u = it.row * (A.k + 1) + it.pos;
-  it.n = min(G::EB, A.V - it.c * G::EB);
-  it.kind = 2;
-  it.reread = 0;
+  it.row = row;
+  it.pos = pos;
+  it.u = row * k1 + pos;
+  it.n = it.kind == 1 ? min(G::EA, A.V - it.c * G::EA) : min(G::EB, A.V - it.c * G::EB);
   return it;
 }
-
-// The race helpers run once per item here: out of line, to keep the
-// streaming loops' registers free.
-static __device__ __noinline__ void race_consider_once(Race& r, float w, float tq, uint32_t v, uint32_t word) {
-  race_consider(r, w, tq, v, word);
-}
-static __device__ __noinline__ void warp_race_merge_once(Race& r) { warp_race_merge(r); }
 
 // Lane 0: post the copies of an item into buffer `buf`, completing on `bar`.
 template <bool kBF16>
@@ -318,242 +324,289 @@ __device__ __forceinline__ void sload_q(const float* qb, int b, int l, float q[8
   q[4] = c.x; q[5] = c.y; q[6] = c.z; q[7] = c.w;
 }
 
-// Maximum (NaN-propagating) of a lane's two halves of block b: slots 0..3
-// (entries 4l..4l+3) and slots 4..7 (entries 128+4l..128+4l+3).
+
+// Packed f32x2 arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ u64 pack2(float a, float b) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(u64 r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ u64 sub2(u64 a, u64 b) {
+  u64 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+  u64 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// exp2((a - m) c) of a pair, rounded like the scalar (a - m) * c.
+__device__ __forceinline__ u64 exp_pair(float a0, float a1, u64 m2, u64 c2) {
+  float x0, x1;
+  unpack2(mul2(sub2(pack2(a0, a1), m2), c2), x0, x1);
+  return pack2(ex2(x0), ex2(x1));
+}
+
+// ---------------------------------------------------------------------------
+// A items.  Lane layout: bf16 lane l reads entries 8l..8l+7 of every block of
+// 256 (one 16-byte shared load); fp32 lane l reads 4l..4l+3 and
+// 128+4l..128+4l+3 (two).
+// ---------------------------------------------------------------------------
 template <bool kBF16>
-__device__ __forceinline__ void shalf_max(const unsigned char* buf, int b, int l, float& h0, float& h1) {
+__device__ __forceinline__ int a_entry(int b, int lane, int j) {
+  return kBF16 ? b * kRaceBlock + 8 * lane + j : slot_entry(b, lane, j);
+}
+template <bool kBF16>
+__device__ __forceinline__ void a_vals(const unsigned char* buf, int b, int lane, float v[8]) {
   if (kBF16) {
-    const uint2 a = *reinterpret_cast<const uint2*>(buf + (b * kRaceBlock + 4 * l) * 2);
-    const uint2 c = *reinterpret_cast<const uint2*>(buf + (b * kRaceBlock + 128 + 4 * l) * 2);
-    const uint32_t ma = max_nan_bf16x2(a.x, a.y), mc = max_nan_bf16x2(c.x, c.y);
-    h0 = max_nan(bf16_lo(ma), bf16_hi(ma));
-    h1 = max_nan(bf16_lo(mc), bf16_hi(mc));
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + (b * kRaceBlock + 8 * lane) * 2);
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
   } else {
-    float v[8];
-    sload<false>(buf, b, l, v);
-    h0 = max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3]));
-    h1 = max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7]));
+    sload<false>(buf, b, lane, v);
   }
 }
 
-// Reduce A item `it`; the record (valid in lane 0) or, for a small top-k, the
-// super-group maxima (in `stage`) are stored by the caller.
+// Max (NaN-propagating) of the lane's 8 entries of block b.
 template <bool kBF16>
-__device__ void a_compute(const Args& A, const Item& it, const RowCfg& cfg, const unsigned char* buf, float* stage,
-                          ChunkRec& rec) {
+__device__ __forceinline__ float a_block_max(const unsigned char* buf, int b, int lane) {
+  if (kBF16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + (b * kRaceBlock + 8 * lane) * 2);
+    const uint32_t t = max_nan_bf16x2(max_nan_bf16x2(w.x, w.y), max_nan_bf16x2(w.z, w.w));
+    return max_nan(bf16_lo(t), bf16_hi(t));
+  } else {
+    float v[8];
+    sload<false>(buf, b, lane, v);
+    return max_nan(max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3])), max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7])));
+  }
+}
+
+// Greedy and unfiltered A item: the tagged record words (lanes 0..7).
+template <bool kBF16>
+__device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg,
+                                     const unsigned char* buf) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EA;
-  if (cfg.type == UT_TOPK) {
-    // maxima of the 64-entry super-groups: super-group r of block b holds
-    // entries [64r, 64r+64), i.e. the first (r < 2) or second half of lanes
-    // 16(r%2)..16(r%2)+15
-#pragma unroll 4
-    for (int b = 0; b < nb; ++b) {
-      float h0, h1;
-      shalf_max<kBF16>(buf, b, lane, h0, h1);
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) {
-        h0 = max_nan(h0, __shfl_xor_sync(kFull, h0, o));
-        h1 = max_nan(h1, __shfl_xor_sync(kFull, h1, o));
-      }
-      if ((lane & 15) == 0) {
-        stage[b * 4 + (lane >> 4)] = h0;
-        stage[b * 4 + 2 + (lane >> 4)] = h1;
-      }
-    }
-    __syncwarp();
-    for (int s = nb * 4 + lane; s < G::SPI; s += 32) stage[s] = -INFINITY;
-    __syncwarp();
-    return;
-  }
-  // greedy and unfiltered: max and first argmax, then the softmax sum
-  // relative to the chunk max; at an unfiltered bonus position also the
-  // block weights and the level-1 race of the chunk's blocks
+  // the lane's max and the first of its blocks reaching it
   float lm = -INFINITY;
-  int lb = 0;
-  bool nan = false;
-#pragma unroll 4
+  int bb = 0;
+#pragma unroll 2
   for (int b = 0; b < nb; ++b) {
-    float h0, h1;
-    shalf_max<kBF16>(buf, b, lane, h0, h1);
-    const float gm = max_nan(h0, h1);
-    nan |= gm != gm;
-    if (gm > lm) {
-      lm = gm;
-      lb = b;
-    }
+    const float g = a_block_max<kBF16>(buf, b, lane);
+    bb = g > lm ? b : bb;
+    lm = max_nan(lm, g);
   }
-  nan = __any_sync(kFull, nan);
+  const bool nan = __any_sync(kFull, lm != lm);
   const float mc = warp_max_f(lm);
+  const bool greedy = cfg.type == UT_GREEDY;
+  const bool bonus = !greedy && it.pos == A.k;
   uint32_t idx = 0xffffffffu;
-  if (lm == mc) {
-    float v[8];
-    sload<kBF16>(buf, lb, lane, v);
+  if (greedy && !nan) {
+    if (lm == mc) {
+      float v[8];
+      a_vals<kBF16>(buf, bb, lane, v);
 #pragma unroll
-    for (int j = 7; j >= 0; --j)
-      if (v[j] == lm) idx = (uint32_t)(e0 + slot_entry(lb, lane, j));
+      for (int j = 7; j >= 0; --j)
+        if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(bb, lane, j));
+    }
+    idx = warp_min_u32(idx);
   }
-  idx = warp_min_u32(idx);
   float z = 0.f;
   Race r;
   race_init(r);
   const bool live = !nan && mc > -INFINITY && mc < INFINITY;
-  const bool bonus = cfg.type == UT_DENSE && it.pos == A.k;
   if (live) {
-    const float c = cfg.c;
+    const u64 m2 = pack2(mc, mc), c2 = pack2(cfg.c, cfg.c);
     if (!bonus) {
-      float z0 = 0.f, z1 = 0.f;
+      u64 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
 #pragma unroll 2
       for (int b = 0; b < nb; ++b) {
         float v[8];
-        sload<kBF16>(buf, b, lane, v);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          z0 += ex2((v[j] - mc) * c);
-          z1 += ex2((v[j + 1] - mc) * c);
-        }
+        a_vals<kBF16>(buf, b, lane, v);
+        acc0 = add2(acc0, exp_pair(v[0], v[1], m2, c2));
+        acc1 = add2(acc1, exp_pair(v[2], v[3], m2, c2));
+        acc0 = add2(acc0, exp_pair(v[4], v[5], m2, c2));
+        acc1 = add2(acc1, exp_pair(v[6], v[7], m2, c2));
       }
-      z = warp_sum(z0 + z1);
+      float a0, a1, a2, a3;
+      unpack2(acc0, a0, a1);
+      unpack2(acc1, a2, a3);
+      z = warp_sum((a0 + a2) + (a1 + a3));
     } else {
+      // block weights (one warp sum per block), then the level-1 race
       float myW = 0.f;
+#pragma unroll 1
       for (int b = 0; b < nb; ++b) {
         float v[8];
-        sload<kBF16>(buf, b, lane, v);
-        float s8 = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s8 += ex2((v[j] - mc) * c);
-        const float W = warp_sum(s8);
+        a_vals<kBF16>(buf, b, lane, v);
+        u64 acc = add2(exp_pair(v[0], v[1], m2, c2), exp_pair(v[2], v[3], m2, c2));
+        acc = add2(acc, add2(exp_pair(v[4], v[5], m2, c2), exp_pair(v[6], v[7], m2, c2)));
+        float s0, s1;
+        unpack2(acc, s0, s1);
+        const float W = warp_sum(s0 + s1);
         z += W;
         if (lane == b) myW = W;
       }
       if (myW > 0.f) {
         const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
-        race_consider_once(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
+        race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
       }
-      warp_race_merge_once(r);
+      warp_race_merge(r);
     }
   }
-  {
-    rec.m = nan ? __uint_as_float(0x7fc00000u) : mc;
-    rec.amax = idx;
-    rec.z = z;
-    rec.pad0 = 0;
-    rec.s1 = r.s1;
-    rec.t1 = r.t1;
-    rec.s2 = r.s2;
-    rec.t2 = r.t2;
-    rec.v1 = r.v1;
-    rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
+  u64* rec = A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords;
+  uint32_t v = 0;
+  switch (lane) {
+    case 0: v = nan ? 0x7fc00000u : __float_as_uint(mc); break;
+    case 1: v = idx; break;
+    case 2: v = __float_as_uint(z); break;
+    case 3: v = __float_as_uint(r.s1); break;
+    case 4: v = __float_as_uint(r.t1); break;
+    case 5: v = __float_as_uint(r.s2); break;
+    case 6: v = __float_as_uint(r.t2); break;
+    case 7: v = r.v1; break;
+    default: break;
   }
+  if (lane < (bonus ? 8 : 3)) __stcg(rec + lane, tagw(tag, v));
+  __syncwarp();
 }
 
-__device__ __forceinline__ UnitState load_state(const Args& A, int u) {
-  UnitState st;
-  st.m = __ldcg(&A.ust[u].m);
-  st.invZ = __ldcg(&A.ust[u].invZ);
-  st.lnZ = __ldcg(&A.ust[u].lnZ);
-  st.lp_x = __ldcg(&A.ust[u].lp_x);
-  st.accept = __ldcg(&A.ust[u].accept);
-  st.flags = __ldcg(&A.ust[u].flags);
-  st.invalid = __ldcg(&A.ust[u].invalid);
-  st.am = __ldcg(&A.ust[u].am);
-  return st;
-}
-
-// Draw from p over a whole row by one warp (the fallback when a residual is
-// empty): each lane sums the weights of its own blocks (level 1), then the
-// winning block's entries race (level 2).
+// Small top-k A item: the chunk's first kList entries in the total order
+// (key, chunk-local index), tagged words in lanes 0..15.  Every such entry is
+// at least the 8th largest lane maximum t8, so only the entries >= t8 (in
+// blocks whose lane maximum reaches it) are staged and sorted.
 template <bool kBF16>
-__device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, float m, float c, bool* margin) {
+__device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it, const unsigned char* buf,
+                                    u64* stage) {
   const int lane = threadIdx.x & 31;
-  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
-  const int nblk = ceil_div(A.V, kRaceBlock);
-  const int G = (A.V + 7) / 8;
-  Race r1;
-  race_init(r1);
-  for (int b = lane; b < nblk; b += 32) {
-    float W = 0.f;
-    for (int g = b * (kRaceBlock / 8); g < (b + 1) * (kRaceBlock / 8) && g < G; ++g) {
-      float v[8];
-      load_group<kBF16>(A, lrow, g, true, v);
+  const int nb = ceil_div(it.n, kRaceBlock);
+  float lm = -INFINITY;
+#pragma unroll 2
+  for (int b = 0; b < nb; ++b) lm = max_nan(lm, a_block_max<kBF16>(buf, b, lane));
+  const bool nan = __any_sync(kFull, lm != lm);
+  uint32_t flags = nan ? kListNaN : 0u;
+  uint32_t nn = 0;
+  if (!nan) {
+    // t8: bitonic sort of the lane maxima, descending
+    float x = lm;
+#pragma unroll 1
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll 1
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const float o = __shfl_xor_sync(kFull, x, stride);
+        const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+        x = keep_max ? fmaxf(x, o) : fminf(x, o);
+      }
+    }
+    const float t8 = __shfl_sync(kFull, x, kList - 1);
+    const uint32_t T = max(okey(t8), okey(-INFINITY) + 1u);   // finite entries >= t8
+    // count the lane's entries >= T (only lanes whose max reaches T have
+    // any), one scan for the offsets, then write them
+    uint32_t cnt = 0;
+    const bool mine = okey(lm) >= T;
+    if (mine) {
+#pragma unroll 1
+      for (int b = 0; b < nb; ++b) {
+        float v[8];
+        a_vals<kBF16>(buf, b, lane, v);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) W += (g * 8 + j < A.V) ? ex2((v[j] - m) * c) : 0.f;
+        for (int j = 0; j < 8; ++j) cnt += okey(v[j]) >= T ? 1u : 0u;
+      }
     }
-    if (W > 0.f) race_consider(r1, W, 0.f, (uint32_t)b, block_word(A, row, pos, (uint32_t)b));
-  }
-  warp_race_merge(r1);
-  if (r1.s1 < 0.f) {
-    *margin = false;
-    return 0xffffffffu;
-  }
-  const Race l2 = race_in_block<kBF16>(A, row, pos, r1.v1, m, c, 1.f, RW_P, nullptr);
-  *margin = draw_margin(r1) || draw_margin(l2);
-  return l2.v1;
-}
-
-template <bool kBF16>
-__device__ __noinline__ void fin_b(const Args& A, const Item& it, const RowCfg& cfg, const UnitState& st) {
-  using G = Geo<kBF16>;
-  const int lane = threadIdx.x & 31;
-  const int u = it.u, row = it.row, pos = it.pos;
-  const int NC = ceil_div(A.V, G::EB);
-  const BRec* R = A.brec + (size_t)u * A.NCB;
-  const bool need_race = !st.accept;
-  float al = 0.f;
-  Race a;
-  race_init(a);
-  for (int c = lane; c < NC; c += 32) {
-    al += __ldcg(&R[c].alpha);
-    if (need_race) {
-      Race rb;
-      rb.s1 = __ldcg(&R[c].s1);
-      rb.t1 = __ldcg(&R[c].t1);
-      rb.s2 = __ldcg(&R[c].s2);
-      rb.t2 = __ldcg(&R[c].t2);
-      rb.v1 = __ldcg(&R[c].v1);
-      rb.s1lo = 0.f;
-      race_merge(a, rb);
+    uint32_t n = 0;
+    uint32_t p = warp_excl_scan(cnt, &n);
+    if (mine) {
+#pragma unroll 1
+      for (int b = 0; b < nb && p < (uint32_t)kStage; ++b) {
+        float v[8];
+        a_vals<kBF16>(buf, b, lane, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t key = okey(v[j]);
+          if (key >= T) {
+            if (p < (uint32_t)kStage) stage[p] = key64(key, (uint32_t)a_entry<kBF16>(b, lane, j));
+            ++p;
+          }
+        }
+      }
     }
-  }
-  const float alpha_v = warp_sum(al);
-  uint32_t draw_flags = 0;
-  uint32_t y = 0xffffffffu;
-  if (need_race) {
-    warp_race_merge(a);
-    if (a.s1 >= 0.f) {
-      const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr);
-      y = l2.v1;
-      if (draw_margin(a) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
+    __syncwarp();
+    if (n > (uint32_t)kStage) flags |= kListPartial;
+    nn = min(n, (uint32_t)kStage);
+    if (nn <= 32) {
+      // one candidate per lane: bitonic sort in registers, descending
+      u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
+#pragma unroll 1
+      for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll 1
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const u64 o = __shfl_xor_sync(kFull, a, stride);
+          const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+          a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
+        }
+      }
+      __syncwarp();
+      stage[lane] = a;
+      __syncwarp();
     } else {
-      draw_flags |= SPEC_F_RESIDUAL_EMPTY;
-      bool mg = false;
-      y = warp_draw_p<kBF16>(A, row, pos, st.m, cfg.c, &mg);
-      if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
+      warp_sort_desc(stage, (int)nn);
     }
   }
-  if (lane == 0) {
-    UnitRecord rec = empty_record(st.flags);
-    rec.accept = st.accept;
-    rec.lp_x = st.lp_x;
-    rec.alpha = alpha_v;
-    if (need_race) {
-      const uint32_t yy = y < (uint32_t)A.V ? y : (uint32_t)st.am;
-      rec.y = (int32_t)yy;
-      rec.lp_y = (load_logit(A, kBF16, (size_t)u * A.V + yy) - st.m) * cfg.invT - st.lnZ;
-      rec.draw_flags = draw_flags;
-    }
-    A.b_ticket[u] = 0;
-    A.ready[u] = 0;
-    commit_record(A, u, row, rec);
+  // word 2j: key of entry j (0 = none); word 2j + 1: its chunk-local index
+  const int j = lane >> 1;
+  uint32_t v = 0;
+  if (lane < 2 * kList) {
+    const bool has = (uint32_t)j < nn;
+    const u64 k = has ? stage[j] : 0ull;
+    if ((lane & 1) == 0) v = has ? (uint32_t)(k >> 32) : 0u;
+    else v = (has ? key64_idx(k) : kListIdx) | (j == 0 ? flags : 0u);
+    __stcg(A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords + lane, tagw(tag, v));
   }
   __syncwarp();
 }
 
+// ---------------------------------------------------------------------------
+// B items.
+// ---------------------------------------------------------------------------
+// The unit state words of a drafted unfiltered unit (loads in flight; checked
+// by state_ready).
+__device__ __forceinline__ void state_load(const Args& A, int u, u64 (&w)[kStateWords]) {
+#pragma unroll
+  for (int i = 0; i < kStateWords; ++i) w[i] = __ldcg(A.ust + (size_t)u * kStateWords + i);
+}
+__device__ __forceinline__ bool state_ok(const u64 (&w)[kStateWords], uint32_t tag) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < kStateWords; ++i) ok = ok && tag_ok(w[i], tag);
+  return ok;
+}
+__device__ __forceinline__ UnitState state_of(const u64 (&w)[kStateWords]) {
+  UnitState st;
+  st.m = wf(w[0]);
+  st.invZ = wf(w[1]);
+  st.lnZ = wf(w[2]);
+  st.lp_x = wf(w[3]);
+  st.accept = (int32_t)wu(w[4]);
+  st.flags = wu(w[5]);
+  st.invalid = wu(w[6]);
+  st.am = (int32_t)wu(w[7]);
+  return st;
+}
+
 template <bool kBF16>
-__device__ void b_compute(const Args& A, const Item& it, const RowCfg& cfg, const UnitState& st, const unsigned char* buf,
-                          BRec& br) {
+__device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg, const UnitState& st,
+                                    const unsigned char* buf) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
@@ -603,38 +656,27 @@ __device__ void b_compute(const Args& A, const Item& it, const RowCfg& cfg, cons
   race_init(r);
   if (need_race && myW > 0.f) {
     const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
-    race_consider_once(r, myW, myU - myW, blk, block_word(A, it.row, it.pos, blk));
+    race_consider(r, myW, myU - myW, blk, block_word(A, it.row, it.pos, blk));
   }
-  warp_race_merge_once(r);
-  br.alpha = alpha_c;
-  br.s1 = r.s1;
-  br.t1 = r.t1;
-  br.s2 = r.s2;
-  br.t2 = r.t2;
-  br.v1 = r.v1;
-  br.pad[0] = br.pad[1] = 0;
-}
-
-
-
-// ---------------------------------------------------------------------------
-// Phases.
-// ---------------------------------------------------------------------------
-// Results of A item `it` (plain stores; the grid barrier publishes them).
-template <bool kBF16>
-__device__ __forceinline__ void store_a(const Args& A, const Item& it, const RowCfg& cfg, const ChunkRec& rec,
-                                        const float* stage) {
-  using G = Geo<kBF16>;
-  const int lane = threadIdx.x & 31;
-  if (cfg.type == UT_TOPK) {
-    float* dst = A.smax + (size_t)it.u * A.NSM + (size_t)it.c * G::SPI;
-    for (int s = lane; s < G::SPI; s += 32) dst[s] = stage[s];
-  } else if (lane == 0) {
-    A.crec[(size_t)it.u * A.NCA + it.c] = rec;
+  warp_race_merge(r);
+  u64* rec = A.brec + ((size_t)it.u * A.NCB + it.c) * kBRecWords;
+  uint32_t v = 0;
+  switch (lane) {
+    case 0: v = __float_as_uint(alpha_c); break;
+    case 1: v = __float_as_uint(r.s1); break;
+    case 2: v = __float_as_uint(r.t1); break;
+    case 3: v = __float_as_uint(r.s2); break;
+    case 4: v = __float_as_uint(r.t2); break;
+    case 5: v = r.v1; break;
+    default: break;
   }
+  if (lane < 6) __stcg(rec + lane, tagw(tag, v));
   __syncwarp();
 }
 
+// ---------------------------------------------------------------------------
+// Warps.
+// ---------------------------------------------------------------------------
 struct Bufs {
   unsigned char* a;
   unsigned char* b;
@@ -654,146 +696,120 @@ struct Bufs {
   }
 };
 
-// Stream phase of one warp: A items t0, t0 + nw, ... (the first two are
-// already posted in ia, ib).
-template <bool kBF16>
-__device__ __noinline__ void stream_a(const Args& A, const Plan& P, VShm& S, int w, Bufs& B, Item ia, Item ib,
-                                      uint32_t t, uint32_t nw) {
-  while (ia.kind != 0) {
-    if (!wait_buffer(A, B.ba, B.pa)) return;
-    B.pa ^= 1u;
-    const RowCfg cfg = plan_cfg(A, P, ia.row);
-    if (cfg.type != UT_GENERAL) {
-      if (!A.vec_logits || (ia.n & (kRaceBlock - 1)) != 0) fill_tail<kBF16>(A, ia, B.a);
-      ChunkRec rec;
-      a_compute<kBF16>(A, ia, cfg, B.a, S.stage[w], rec);
-      store_a<kBF16>(A, ia, cfg, rec, S.stage[w]);
-    }
-    __syncwarp();
-    Item in;
-    in.kind = 0;
-    if (ib.kind != 0) in = next_a<kBF16>(A, P, t, nw);
-    if ((threadIdx.x & 31) == 0) issue<kBF16>(A, in, B.a, B.ba);
-    ia = ib;
-    ib = in;
-    B.rotate();
-  }
-}
 
-// One settle task: drafted unfiltered units, small top-k units, bonus
-// positions, greedy units.
+// A stream warp: items t0, t0 + nws, ... of the sequence.
 template <bool kBF16>
-__device__ __noinline__ void settle_task(const Args& A, const Plan& P, VShm& S, int w, int s) {
-  const int k = A.k, k1 = A.k + 1;
-  int row, pos;
-  if (s < P.nD * k) {
-    row = (int)P.order[s / k];
-    pos = s % k;
-  } else if ((s -= P.nD * k) < P.nT * k1) {
-    row = (int)P.order[P.nD + s / k1];
-    pos = s % k1;
-  } else if ((s -= P.nT * k1) < P.nD) {
-    row = (int)P.order[s];
-    pos = k;
-  } else {
-    s -= P.nD;
-    row = (int)P.order[P.nD + P.nT + s / k1];
-    pos = s % k1;
-  }
-  const int u = row * k1 + pos;
-  const RowCfg cfg = plan_cfg(A, P, row);
-  if (cfg.type == UT_TOPK) topk_settle<kBF16>(A, *reinterpret_cast<TopkScratch*>(S.buf[w][0]), u, row, pos, cfg);
-  else fin_stats<kBF16>(A, u, row, pos, cfg);
-}
-
-// B items of one warp: the contiguous range [tb, end).
-template <bool kBF16>
-__device__ __noinline__ void stream_b(const Args& A, const Plan& P, Bufs& B, uint32_t tb, uint32_t end) {
+__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w, uint32_t t,
+                                    uint32_t nws) {
   const int lane = threadIdx.x & 31;
-  Item ia = map_b<kBF16>(A, P, tb, end);
-  Item ib = map_b<kBF16>(A, P, tb + 1, end);
-  tb += 2;
+  const Plan P = P0;
+  Bufs B;
+  B.a = S.buf[w][0];
+  B.b = S.buf[w][1];
+  B.ba = &S.bar[w][0];
+  B.bb = &S.bar[w][1];
+  B.pa = 0u;
+  B.pb = 0u;
+  if (lane == 0) {
+    mbar_init(B.ba, 1);
+    mbar_init(B.bb, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  Item ia = map_item<kBF16>(A, P, t);
+  Item ib = map_item<kBF16>(A, P, t + nws);
+  t += 2 * nws;
   if (lane == 0) {
     issue<kBF16>(A, ia, B.a, B.ba);
     issue<kBF16>(A, ib, B.b, B.bb);
   }
-  Item run;                  // the unit whose chunks this warp is processing
-  run.kind = 0;
-  uint32_t run_n = 0;
-  UnitState st;
-  memset(&st, 0, sizeof(st));
-  RowCfg cfg = classify(A.params[0], A.V);
-  const uint32_t lastB = (uint32_t)P.NCB;
-  auto close_run = [&]() {
-    // add this warp's chunks of the finished run to the unit's ticket; the
-    // warp that completes the unit settles it
-    uint32_t old = 0;
-    if (lane == 0) old = atomic_add_acq_rel(&A.b_ticket[run.u], run_n);
-    old = __shfl_sync(kFull, old, 0);
-    __syncwarp();
-    if (old + run_n == lastB && !st.invalid) fin_b<kBF16>(A, run, cfg, st);
-    else if (old + run_n == lastB && lane == 0) {
-      A.b_ticket[run.u] = 0;
-      A.ready[run.u] = 0;
-    }
-    run.kind = 0;
-  };
   while (ia.kind != 0) {
-    if (run.kind != 0 && run.u != ia.u) close_run();
-    if (run.kind == 0) {
-      // the unit state (bounded wait: a settle warp publishes it)
-      if (lane == 0) {
-        long long spins = 0;
-        while (load_acquire(&A.ready[ia.u]) == 0u) {
-          if (++spins > kSpinLimit) {
-            atomicOr(&A.ws->error, 1u);
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      __syncwarp();
-      st = load_state(A, ia.u);
-      cfg = plan_cfg(A, P, ia.row);
-      run = ia;
-      run_n = 0;
-    }
+    const RowCfg cfg = plan_cfg(A, P, ia.row);
+    u64 sw[kStateWords];
+    if (ia.kind == 2) state_load(A, ia.u, sw);     // in flight during the copy wait
     if (!wait_buffer(A, B.ba, B.pa)) return;
     B.pa ^= 1u;
-    if (!A.vec_logits || !A.vec_q || (ia.n & (kRaceBlock - 1)) != 0) fill_tail<kBF16>(A, ia, B.a);
-    if (!st.invalid) {
-      BRec br;
-      b_compute<kBF16>(A, ia, cfg, st, B.a, br);
-      if (lane == 0) A.brec[(size_t)ia.u * A.NCB + ia.c] = br;
+    if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || (ia.n & (kRaceBlock - 1)) != 0) fill_tail<kBF16>(A, ia, B.a);
+    if (ia.kind == 1) {
+      if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, B.a, S.stage[w]);
+      else a_stats<kBF16>(A, tag, ia, cfg, B.a);
+    } else {
+      // the unit state (bounded wait: a settle warp publishes it)
+      long long spins = 0;
+      while (!__all_sync(kFull, state_ok(sw, tag))) {
+        if (++spins > kSpinLimit) {
+          if (lane == 0) atomicOr(&A.ws->error, 1u);
+          break;
+        }
+        __nanosleep(128);
+        state_load(A, ia.u, sw);
+      }
+      const UnitState st = state_of(sw);
+      if (!st.invalid) b_item<kBF16>(A, tag, ia, cfg, st, B.a);
     }
     __syncwarp();
-    ++run_n;
-    Item in = map_b<kBF16>(A, P, tb, end);
-    ++tb;
+    const Item in = map_item<kBF16>(A, P, t);
+    t += nws;
     if (lane == 0) issue<kBF16>(A, in, B.a, B.ba);
     ia = ib;
     ib = in;
     B.rotate();
   }
-  if (run.kind != 0) close_run();
 }
 
-// Grid barrier (all CTAs are resident: cooperative launch).  Bounded.
-__device__ __forceinline__ void grid_barrier(const Args& A) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&A.ws->arrived, 1u);
-    long long spins = 0;
-    while (load_acquire(&A.ws->arrived) < (uint32_t)A.n_ctas) {
-      if (++spins > kSpinLimit) {
-        atomicOr(&A.ws->error, 4u);
-        break;
+// A settle warp: tasks s0, s0 + nsw, ... in the order [drafted unfiltered:
+// state][small top-k][bonus positions][greedy][drafted unfiltered: B
+// records].  Every task before the last group waits only for A records, so
+// every state the B items wait for is published whatever the task spread.
+template <bool kBF16>
+__device__ __noinline__ void settle(const Args& A, const Plan& P, VShm& S, uint32_t tag, int w, uint32_t s0,
+                                    uint32_t nsw, uint32_t nS) {
+  const int k = A.k, k1 = A.k + 1;
+  for (uint32_t t = s0; t < nS; t += nsw) {
+    int s = (int)t, row, pos;
+    bool finish = false;
+    if (s < P.nD * k) {
+      row = (int)P.order[s / k];
+      pos = s % k;
+    } else if ((s -= P.nD * k) < P.nT * k1) {
+      row = (int)P.order[P.nD + s / k1];
+      pos = s % k1;
+    } else if ((s -= P.nT * k1) < P.nD) {
+      row = (int)P.order[s];
+      pos = k;
+    } else if ((s -= P.nD) < P.nG * k1) {
+      row = (int)P.order[P.nD + P.nT + s / k1];
+      pos = s % k1;
+    } else {
+      s -= P.nG * k1;
+      row = (int)P.order[s / k];
+      pos = s % k;
+      finish = true;
+    }
+    const int u = row * k1 + pos;
+    const RowCfg cfg = plan_cfg(A, P, row);
+    if (finish) {
+      // the published state (bounded wait), then the B records
+      u64 sw[kStateWords];
+      state_load(A, u, sw);
+      long long spins = 0;
+      while (!__all_sync(kFull, state_ok(sw, tag))) {
+        if (++spins > kSpinLimit) {
+          if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, 1u);
+          break;
+        }
+        __nanosleep(256);
+        state_load(A, u, sw);
       }
-      __nanosleep(64);
+      const UnitState st = state_of(sw);
+      if (!st.invalid) fin_b<kBF16>(A, tag, u, row, pos, cfg, st);
+    } else if (cfg.type == UT_TOPK) {
+      topk_settle<kBF16>(A, tag, *reinterpret_cast<TopkScratch*>(S.buf[w][0]), u, row, pos, cfg);
+    } else {
+      UnitState st;
+      fin_stats<kBF16>(A, tag, u, row, pos, cfg, st);
     }
   }
-  __syncthreads();
 }
 
 // General-path units, taken by the two half-CTA groups.
@@ -820,64 +836,53 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t nw = (uint32_t)A.n_ctas * kSW;
-  const uint32_t g = (uint32_t)w * (uint32_t)A.n_ctas + blockIdx.x;   // warps of a round spread over the SMs
-  Bufs B;
-  B.a = S.buf[w][0];
-  B.b = S.buf[w][1];
-  B.ba = &S.bar[w][0];
-  B.bb = &S.bar[w][1];
-  B.pa = 0u;
-  B.pb = 0u;
-  const int NCA = ceil_div(A.V, G::EA);
-  // the first two A items go out before anything else
-  Item ia = map_a_raw<kBF16>(A, NCA, g);
-  Item ib = map_a_raw<kBF16>(A, NCA, g + nw);
-  if (lane == 0) {
-    mbar_init(B.ba, 1);
-    mbar_init(B.bb, 1);
-    fence_mbar_init();
-    issue<kBF16>(A, ia, B.a, B.ba);
-    issue<kBF16>(A, ib, B.b, B.bb);
-  }
+  if (threadIdx.x == 0) S.tag = __ldcg(&A.ws->epoch) + 1u;
   Plan P;
-  P.NCA = NCA;
-  P.NCB = ceil_div(A.V, G::EB);
   if (!A.global_order) {
-    build_order_smem(A, S.order, S.cfg, S.ord);
+    build_order_smem(A, S.order, S.cfg, S.ord);     // synchronises the CTA
     P.order = S.order;
     P.cfg = S.cfg;
-  } else {
-    if (blockIdx.x == 0) build_order_global(A, S.ord);
-    P.order = A.order;
-    P.cfg = nullptr;
-  }
-  __syncthreads();
-  stream_a<kBF16>(A, P, S, w, B, ia, ib, g + 2 * nw, nw);
-  grid_barrier(A);
-  if (!A.global_order) {
     P.nD = S.ord.n_class[UT_DENSE];
     P.nT = S.ord.n_class[UT_TOPK];
     P.nG = S.ord.n_class[UT_GREEDY];
     P.nX = S.ord.n_class[UT_GENERAL];
   } else {
+    __syncthreads();
+    if (blockIdx.x == 0) build_order_global(A, S.ord, S.tag);
+    if (threadIdx.x == 0) {
+      long long spins = 0;
+      while (load_acquire(&A.ws->order_tag) != S.tag) {
+        if (++spins > kSpinLimit) {
+          atomicOr(&A.ws->error, 8u);
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __syncthreads();
+    P.order = A.order;
+    P.cfg = nullptr;
     P.nD = (int)__ldcg(&A.ws->n_class[UT_DENSE]);
     P.nT = (int)__ldcg(&A.ws->n_class[UT_TOPK]);
     P.nG = (int)__ldcg(&A.ws->n_class[UT_GREEDY]);
     P.nX = (int)__ldcg(&A.ws->n_class[UT_GENERAL]);
   }
-  // settle tasks on the first warps of every SM, B items on the rest
-  const uint32_t nS = (uint32_t)(P.nD * A.k + P.nT * (A.k + 1) + P.nD + P.nG * (A.k + 1));
-  const uint32_t nSW = min(nS, nw / 2u);
-  if (g < nSW) {
-    for (uint32_t s = g; s < nS; s += nSW) settle_task<kBF16>(A, P, S, w, (int)s);
+  const uint32_t tag = S.tag;
+  P.NCA = ceil_div(A.V, G::EA);
+  P.NCB = ceil_div(A.V, G::EB);
+  P.sDD = (uint32_t)(P.nD * A.k * P.NCA);
+  P.sTK = (uint32_t)(P.nT * (A.k + 1) * P.NCA);
+  P.sDB = (uint32_t)(P.nD * P.NCA);
+  P.sB = (uint32_t)(P.nD * A.k * P.NCB);
+  P.sGR = (uint32_t)(P.nG * (A.k + 1) * P.NCA);
+  const uint32_t nw = (uint32_t)A.n_ctas * kSW;
+  const uint32_t g = (uint32_t)w * (uint32_t)A.n_ctas + blockIdx.x;   // warps of a round spread over the SMs
+  const uint32_t nS = (uint32_t)(2 * P.nD * A.k + P.nT * (A.k + 1) + P.nD + P.nG * (A.k + 1));
+  const uint32_t nsw = min(nS, nw / 4u);
+  if (g < nsw) {
+    settle<kBF16>(A, P, S, tag, w, g, nsw, nS);
   } else {
-    const uint32_t totalB = (uint32_t)(P.nD * A.k) * (uint32_t)P.NCB;
-    const uint32_t nBW = nw - nSW;
-    const uint32_t per = (totalB + nBW - 1) / nBW;
-    const uint32_t tb = min(totalB, (g - nSW) * per);
-    const uint32_t end = min(totalB, tb + per);
-    if (tb < end) stream_b<kBF16>(A, P, B, tb, end);
+    stream<kBF16>(A, P, S, tag, w, g - nsw, nw - nsw);
   }
   if (P.nX > 0) {
     __syncthreads();
@@ -889,9 +894,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
     const uint32_t d = atomicAdd(&A.ws->ctas_done, 1u);
     if (d == (uint32_t)A.n_ctas - 1u) {
       A.ws->gnext = 0u;
-      A.ws->arrived = 0u;
       A.ws->ctas_done = 0u;
-      for (int i = 0; i < 4; ++i) A.ws->n_class[i] = 0u;
+      A.ws->epoch = tag;
       __threadfence();
     }
   }
@@ -929,7 +933,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   Args A = A0;
   A.n_ctas = n;
   A.global_order = A.B > kOrderSmem ? 1 : 0;
-  // cooperative launch: every CTA is resident, so the grid barrier ends
+  // cooperative launch: every CTA is resident, so every wait between warps ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)A.n_ctas);

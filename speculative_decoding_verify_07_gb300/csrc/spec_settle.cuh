@@ -1,19 +1,18 @@
-// spec_verify, settle code (sm_103a): what one warp does with a unit whose
-// chunk records are complete.
+// spec_verify, settle code (sm_103a): what one warp does with a unit once
+// its records carry the call's tag.
 //
-//   greedy and unfiltered units: merge the chunk records in chunk order --
-//     max, first argmax, the softmax sum rescaled to the unit max; greedy
-//     units and unfiltered bonus positions are settled at once (the bonus
-//     draw merges the chunks' level-1 block races and races the winning
-//     block's entries); a drafted unfiltered unit takes its accept test and
-//     publishes its state for the B items.
-//   small top-k units: every top-K entry lies in a 64-entry super-group
-//     whose maximum is among the K largest super-group maxima, so the K-th
-//     largest maximum bounds the candidates.  A histogram of the maxima's
-//     distances from the unit maximum gives that bound in one pass; the
-//     candidates are gathered from L2, the first K of the total order
-//     selected exactly and sorted, and top-p, the accept test, alpha and the
-//     draw run on that list.
+//   greedy and unfiltered units: merge the A records in chunk order -- max,
+//     first argmax, the softmax sum rescaled to the unit max; greedy units
+//     and unfiltered bonus positions are settled at once (the bonus draw
+//     merges the chunks' level-1 block races and races the winning block's
+//     entries); a drafted unfiltered unit takes its accept test, publishes
+//     its state for the B items, then merges their records (alpha and the
+//     residual draw).
+//   small top-k units: every A item lists the first 8 entries of its chunk
+//     in the total order.  A chunk whose listed 8th entry is below the K-th
+//     entry of the merged lists holds no further top-K entry, so the merged
+//     lists give the top-K set; other chunks are re-read from L2.  Top-p, the
+//     accept test, alpha and the draw run on the sorted list.
 //
 // The last settled unit of a row resolves the accept chain and writes the
 // row's outputs.
@@ -27,6 +26,55 @@
 namespace specv {
 
 constexpr unsigned kSettleFull = 0xffffffffu;
+
+// Bounded wait, by lane 0, until *p carries `tag`; every lane returns the
+// outcome.
+__device__ __forceinline__ bool wait_word(const Args& A, const u64* p, uint32_t tag) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    long long spins = 0;
+    while (!tag_ok(__ldcg(p), tag)) {
+      if (++spins > kSpinLimit) {
+        atomicOr(&A.ws->error, 4u);
+        ok = 0;
+        break;
+      }
+      __nanosleep(256);
+    }
+  }
+  return __shfl_sync(kSettleFull, ok, 0) != 0;
+}
+
+// The state of a drafted unfiltered unit as tagged words (lanes 0..7).
+__device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u, const UnitState& st) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v = 0;
+  switch (lane) {
+    case 0: v = __float_as_uint(st.m); break;
+    case 1: v = __float_as_uint(st.invZ); break;
+    case 2: v = __float_as_uint(st.lnZ); break;
+    case 3: v = __float_as_uint(st.lp_x); break;
+    case 4: v = (uint32_t)st.accept; break;
+    case 5: v = st.flags; break;
+    case 6: v = st.invalid; break;
+    case 7: v = (uint32_t)st.am; break;
+    default: break;
+  }
+  if (lane < kStateWords) __stcg(A.ust + (size_t)u * kStateWords + lane, tagw(tag, v));
+  __syncwarp();
+}
+
+// Warp loop guard for polling a set of words: true while another pass is
+// needed (not all lanes saw the tag); gives up after kSpinLimit passes.
+__device__ __forceinline__ bool poll_again(const Args& A, bool ok, long long& spins) {
+  if (__all_sync(kSettleFull, ok)) return false;
+  if (++spins > kSpinLimit) {
+    if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, 4u);
+    return false;
+  }
+  __nanosleep(256);
+  return true;
+}
 
 // The draft token of the unit and its logit and q (inputs).
 struct Pre {
@@ -72,33 +120,113 @@ __device__ __forceinline__ AcceptInfo accept_pre(const Args& A, int row, int pos
   return ai;
 }
 
+
+// First index of the row maximum, by one warp (only for a draw that found
+// no positive weight, which a valid row does not produce).
 template <bool kBF16>
-__device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ int row_argmax(const Args& A, size_t lrow) {
+  const int lane = threadIdx.x & 31;
+  const int G = (A.V + 7) / 8;
+  unsigned long long best = 0;
+  for (int g = lane; g < G; g += 32) {
+    float v[8];
+    load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (g * 8 + i >= A.V) continue;
+      const unsigned long long k = key64(okey(v[i]), (uint32_t)(g * 8 + i));
+      best = k > best ? k : best;
+    }
+  }
+  return (int)key64_idx(warp_max_u64(best));
+}
+
+// Draw from p over a whole row by one warp (the fallback when a residual is
+// empty): each lane sums the weights of its own blocks (level 1), then the
+// winning block's entries race (level 2).
+template <bool kBF16>
+__device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, float m, float c, bool* margin) {
+  const int lane = threadIdx.x & 31;
+  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
+  const int nblk = ceil_div(A.V, kRaceBlock);
+  const int G = (A.V + 7) / 8;
+  Race r1;
+  race_init(r1);
+  for (int b = lane; b < nblk; b += 32) {
+    float W = 0.f;
+    for (int g = b * (kRaceBlock / 8); g < (b + 1) * (kRaceBlock / 8) && g < G; ++g) {
+      float v[8];
+      load_group<kBF16>(A, lrow, g, true, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) W += (g * 8 + j < A.V) ? ex2((v[j] - m) * c) : 0.f;
+    }
+    if (W > 0.f) race_consider(r1, W, 0.f, (uint32_t)b, block_word(A, row, pos, (uint32_t)b));
+  }
+  warp_race_merge(r1);
+  if (r1.s1 < 0.f) {
+    *margin = false;
+    return 0xffffffffu;
+  }
+  const Race l2 = race_in_block<kBF16>(A, row, pos, r1.v1, m, c, 1.f, RW_P, nullptr);
+  *margin = draw_margin(r1) || draw_margin(l2);
+  return l2.v1;
+}
+
+// ---------------------------------------------------------------------------
+// Greedy and unfiltered units.
+// ---------------------------------------------------------------------------
+// Merges the A records.  Greedy units and bonus positions are settled here;
+// a drafted unfiltered unit publishes its state (also returned in st) and
+// the function returns true: its B records are merged next (fin_b).
+template <bool kBF16>
+__device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg,
+                                       UnitState& st) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
+  const bool greedy = cfg.type == UT_GREEDY;
+  const bool bonus = !greedy && !has_q;
   const int NC = ceil_div(A.V, G::EA);
-  const ChunkRec* R = A.crec + (size_t)u * A.NCA;
+  const u64* R = A.rec + (size_t)u * A.NCA * kRecWords;
+  const size_t lrow = (size_t)u * A.V;
   const Pre pr = load_pre<kBF16>(A, u, row, pos);   // lane 0's copy is the one used
   // one pass over the records: each lane keeps its max, the first chunk
   // holding it, and its share of the softmax sum relative to that max
   bool nan = false;
   float m = -INFINITY, zl = 0.f;
   int cm = 0x7fffffff;
-  for (int c = lane; c < NC; c += 32) {
-    const float mc = __ldcg(&R[c].m);
-    const float zc = __ldcg(&R[c].z);
-    if (mc != mc) {
-      nan = true;
-    } else if (mc > -INFINITY) {
-      if (mc > m) {
-        zl = (m > -INFINITY ? zl * ex2((m - mc) * cfg.c) : 0.f) + zc;
-        m = mc;
-        cm = c;
-      } else {
-        zl += zc * ex2((mc - m) * cfg.c);
+  if (wait_word(A, R + (size_t)(NC - 1) * kRecWords, tag)) {
+    long long spins = 0;
+    bool ok;
+    do {
+      ok = true;
+      nan = false;
+      m = -INFINITY;
+      zl = 0.f;
+      cm = 0x7fffffff;
+      for (int c = lane; c < NC; c += 32) {
+        const u64* r = R + (size_t)c * kRecWords;
+        const u64 w0 = __ldcg(r), w2 = __ldcg(r + 2);
+        ok = ok && tag_ok(w0, tag) && tag_ok(w2, tag);
+        if (greedy) ok = ok && tag_ok(__ldcg(r + 1), tag);
+        if (bonus) {
+#pragma unroll
+          for (int i = 3; i < 8; ++i) ok = ok && tag_ok(__ldcg(r + i), tag);
+        }
+        const float mc = wf(w0), zc = wf(w2);
+        if (mc != mc) {
+          nan = true;
+        } else if (mc > -INFINITY) {
+          if (mc > m) {
+            zl = (m > -INFINITY ? zl * ex2((m - mc) * cfg.c) : 0.f) + zc;
+            m = mc;
+            cm = c;
+          } else {
+            zl += zc * ex2((mc - m) * cfg.c);
+          }
+        }
       }
-    }
+    } while (poll_again(A, ok, spins));
   }
   nan = __any_sync(kSettleFull, nan);
   const float mw = warp_max_f(m);
@@ -106,26 +234,24 @@ __device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, c
   const bool invalid = nan || !(mw > -INFINITY) || !(mw < INFINITY);
   const uint32_t base_flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
   if (invalid) {
-    if (lane == 0) {
-      if (cfg.type == UT_DENSE && has_q) {
-        UnitState st;
-        memset(&st, 0, sizeof(st));
-        st.invalid = 1;
-        A.ust[u] = st;
-        store_release(&A.ready[u], 1u);
-      }
-      commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    if (cfg.type == UT_DENSE && has_q) {
+      // the B items skip an invalid unit
+      UnitState z;
+      memset(&z, 0, sizeof(z));
+      z.invalid = 1;
+      publish_state(A, tag, u, z);
     }
+    if (lane == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
     __syncwarp();
-    return;
+    return false;
   }
   const float m_lane = m;
   m = mw;
-  const int am = (int)__ldcg(&R[cfirst].amax);
   // the softmax sum rescaled to the unit max (fixed lane order)
   const float Z = warp_sum(cm != 0x7fffffff ? zl * ex2((m_lane - m) * cfg.c) : 0.f);
   const float lnZ = logf(Z);
-  if (cfg.type == UT_GREEDY) {
+  if (greedy) {
+    const int am = (int)wu(__ldcg(R + (size_t)cfirst * kRecWords + 1));
     if (lane == 0) {
       UnitRecord rec = empty_record(base_flags);
       bool need_draw = !has_q;
@@ -147,94 +273,133 @@ __device__ __noinline__ void fin_stats(const Args& A, int u, int row, int pos, c
       commit_record(A, u, row, rec);
     }
     __syncwarp();
-    return;
+    return false;
   }
-  // unfiltered
-  if (!has_q) {
-    // bonus: merge the chunks' block races (scaled to the unit max), then
-    // race the entries of the winning block
+  if (bonus) {
+    // merge the chunks' block races (scaled to the unit max), then race the
+    // entries of the winning block
     Race a;
     race_init(a);
     for (int c = lane; c < NC; c += 32) {
-      const float mc = __ldcg(&R[c].m);
+      const u64* r = R + (size_t)c * kRecWords;
+      const float mc = wf(__ldcg(r));
       const float sc = mc > -INFINITY ? ex2((mc - m) * cfg.c) : 0.f;
       Race b;
-      b.s1 = __ldcg(&R[c].s1);
-      b.t1 = __ldcg(&R[c].t1);
-      b.s2 = __ldcg(&R[c].s2);
-      b.t2 = __ldcg(&R[c].t2);
-      b.v1 = __ldcg(&R[c].v1);
+      b.s1 = wf(__ldcg(r + 3));
+      b.t1 = wf(__ldcg(r + 4));
+      b.s2 = wf(__ldcg(r + 5));
+      b.t2 = wf(__ldcg(r + 6));
+      b.v1 = wu(__ldcg(r + 7));
       b.s1lo = 0.f;
       race_scale(b, sc);
       race_merge(a, b);
     }
     warp_race_merge(a);
     const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr);
+    uint32_t y = l2.v1;
+    if (y >= (uint32_t)A.V) y = (uint32_t)row_argmax<kBF16>(A, lrow);
     if (lane == 0) {
       UnitRecord rec = empty_record(base_flags);
-      const uint32_t y = l2.v1 < (uint32_t)A.V ? l2.v1 : (uint32_t)am;
       rec.y = (int32_t)y;
-      rec.lp_y = (load_logit(A, kBF16, (size_t)u * A.V + y) - m) * cfg.invT - lnZ;
+      rec.lp_y = (load_logit(A, kBF16, lrow + y) - m) * cfg.invT - lnZ;
       if (draw_margin(a) || draw_margin(l2)) rec.draw_flags |= SPEC_F_MARGIN_DRAW;
       commit_record(A, u, row, rec);
     }
     __syncwarp();
-    return;
+    return false;
   }
   // drafted: accept test, then publish the state for the B items
+  AcceptInfo ai;
+  if (lane == 0) ai = accept_pre(A, row, pos, pr, false, -1, m, cfg.c, Z);
+  st.m = m;
+  st.invZ = 1.0f / Z;
+  st.lnZ = lnZ;
+  st.accept = __shfl_sync(kSettleFull, (lane == 0 && ai.accept) ? 1 : 0, 0);
+  st.lp_x = __shfl_sync(kSettleFull, lane == 0 ? (ai.valid ? (ai.lx - m) * cfg.invT - lnZ : 0.f) : 0.f, 0);
+  st.flags = __shfl_sync(kSettleFull,
+                         lane == 0 ? base_flags | (ai.valid ? 0u : SPEC_F_BAD_TOKEN) | (ai.margin ? SPEC_F_MARGIN_ACCEPT : 0u)
+                                   : 0u, 0);
+  st.invalid = 0;
+  st.am = -1;
+  publish_state(A, tag, u, st);
+  return true;
+}
+
+// A drafted unfiltered unit after its B items: alpha from the chunks' sums,
+// and after a rejection the residual draw from the chunks' level-1 races.
+template <bool kBF16>
+__device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg,
+                                   const UnitState& st) {
+  using G = Geo<kBF16>;
+  const int lane = threadIdx.x & 31;
+  const int NC = ceil_div(A.V, G::EB);
+  const u64* R = A.brec + (size_t)u * A.NCB * kBRecWords;
+  const bool need_race = !st.accept;
+  float al = 0.f;
+  Race a;
+  race_init(a);
+  if (wait_word(A, R + (size_t)(NC - 1) * kBRecWords, tag)) {
+    long long spins = 0;
+    bool ok;
+    do {
+      ok = true;
+      al = 0.f;
+      race_init(a);
+      for (int c = lane; c < NC; c += 32) {
+        const u64* r = R + (size_t)c * kBRecWords;
+        const u64 w0 = __ldcg(r);
+        ok = ok && tag_ok(w0, tag);
+        al += wf(w0);
+        if (need_race) {
+          u64 w[5];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) {
+            w[i] = __ldcg(r + 1 + i);
+            ok = ok && tag_ok(w[i], tag);
+          }
+          Race rb;
+          rb.s1 = wf(w[0]);
+          rb.t1 = wf(w[1]);
+          rb.s2 = wf(w[2]);
+          rb.t2 = wf(w[3]);
+          rb.v1 = wu(w[4]);
+          rb.s1lo = 0.f;
+          race_merge(a, rb);
+        }
+      }
+    } while (poll_again(A, ok, spins));
+  }
+  const float alpha_v = warp_sum(al);
+  uint32_t draw_flags = 0;
+  uint32_t y = 0xffffffffu;
+  if (need_race) {
+    warp_race_merge(a);
+    if (a.s1 >= 0.f) {
+      const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr);
+      y = l2.v1;
+      if (draw_margin(a) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
+    } else {
+      draw_flags |= SPEC_F_RESIDUAL_EMPTY;
+      bool mg = false;
+      y = warp_draw_p<kBF16>(A, row, pos, st.m, cfg.c, &mg);
+      if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
+    }
+    if (y >= (uint32_t)A.V) y = (uint32_t)row_argmax<kBF16>(A, (size_t)u * A.V);
+  }
   if (lane == 0) {
-    const AcceptInfo ai = accept_pre(A, row, pos, pr, false, am, m, cfg.c, Z);
-    UnitState st;
-    st.m = m;
-    st.invZ = 1.0f / Z;
-    st.lnZ = lnZ;
-    st.accept = ai.accept ? 1 : 0;
-    st.lp_x = ai.valid ? (ai.lx - m) * cfg.invT - lnZ : 0.f;
-    st.flags = base_flags | (ai.valid ? 0u : SPEC_F_BAD_TOKEN) | (ai.margin ? SPEC_F_MARGIN_ACCEPT : 0u);
-    st.invalid = 0;
-    st.am = am;
-    A.ust[u] = st;
-    store_release(&A.ready[u], 1u);
+    UnitRecord rec = empty_record(st.flags);
+    rec.accept = st.accept;
+    rec.lp_x = st.lp_x;
+    rec.alpha = alpha_v;
+    if (need_race) {
+      rec.y = (int32_t)y;
+      rec.lp_y = (load_logit(A, kBF16, (size_t)u * A.V + y) - st.m) * cfg.invT - st.lnZ;
+      rec.draw_flags = draw_flags;
+    }
+    commit_record(A, u, row, rec);
   }
   __syncwarp();
 }
-
-
-// ---------------------------------------------------------------------------
-// Small top-k, one warp.
-// ---------------------------------------------------------------------------
-constexpr int kCandCap = 256;              // candidates held for the sort path
-
-// Scratch of one warp: its two stream buffers.
-struct TopkScratch {
-  uint16_t sg[kMaxNsmTopk];                // super-group max keys (16-bit), then qualifying super-group ids
-  uint32_t hist[256];
-  unsigned long long cand[kCandCap];
-};
-static_assert(sizeof(TopkScratch) <= 2 * kSlot, "top-k scratch exceeds a warp's stream buffers");
-
-// The list phase reuses the super-group area.
-struct ListArrays {
-  uint32_t blk[kTopkSmall];
-  float w[kTopkSmall];
-  float wu[kTopkSmall];
-};
-static_assert(sizeof(ListArrays) <= sizeof(uint16_t) * kMaxNsmTopk, "list arrays exceed the super-group area");
-
-__device__ __forceinline__ uint32_t k16(float v) { return okey(v) >> 16; }
-
-// Smallest order key whose weight exp2((v - m) c) is positive (the weight is
-// monotone in the key); every lane computes the same.
-__device__ __forceinline__ uint32_t positive_key(float m, float c, uint32_t km) {
-  uint32_t lo = 0u, hi = km;
-  while (lo < hi) {
-    const uint32_t mid = lo + ((hi - lo) >> 1);
-    if (ex2((from_okey(mid) - m) * c) > 0.f) hi = mid;
-    else lo = mid + 1u;
-  }
-  return lo;
-}
-
 // First bin (from bin 0) where the running count over hist[0..256) reaches
 // `need` (>= 1); 256 when the total is below it.  *before = the count of the
 // bins before it.  Lane l scans bins 8l..8l+7.
@@ -275,32 +440,6 @@ __device__ __forceinline__ int warp_select_bin(const uint32_t* hist, uint32_t ne
   return __shfl_sync(kSettleFull, bin, src);
 }
 
-// Calls fn(g, v) on every lane for the groups of 8 entries of the listed
-// super-groups (4 super-groups per warp step, lane l on group 8 * id + (l & 7);
-// g < 0 on lanes past the list).  Steps are loaded four at a time.
-template <bool kBF16, typename F>
-__device__ __forceinline__ void sweep_groups(const Args& A, size_t lrow, const uint16_t* ids, int n_sg, F fn) {
-  const int lane = threadIdx.x & 31;
-  for (int base = 0; base < n_sg; base += 16) {
-    float v[4][8];
-    int g[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int j = base + 4 * s + (lane >> 3);
-      g[s] = j < n_sg ? (int)ids[j] * 8 + (lane & 7) : -1;
-      if (g[s] >= 0) {
-        load_group<kBF16>(A, lrow, g[s], true, v[s]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[s][i] = -INFINITY;
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      if (base + 4 * s < n_sg) fn(g[s], v[s]);
-  }
-}
-
 // Exclusive warp scan of a count; *total = the warp's sum.
 __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, uint32_t* total) {
   const int lane = threadIdx.x & 31;
@@ -314,80 +453,112 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, uint32_t* total) 
   return inc - x;
 }
 
-// Bitonic sort, descending, of 32 * R keys held R per lane (element
-// lane * R + r in register r).
-template <int R>
-__device__ __forceinline__ void warp_bitonic_desc(unsigned long long (&a)[R]) {
+// Descending bitonic sort of s[0..n) (n <= 256) in shared memory by one warp,
+// padded with zeros to a power of two >= 32; rolled loops keep it small.
+static __device__ __noinline__ void warp_sort_desc(u64* s, int n) {
   const int lane = threadIdx.x & 31;
-  constexpr int N = 32 * R;
-#pragma unroll
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int i = n + lane; i < N; i += 32) s[i] = 0ull;
+  __syncwarp();
+#pragma unroll 1
   for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < R) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int r2 = r ^ stride;
-          if (r2 > r) {
-            const int i = lane * R + r;
-            const bool desc = (i & size) == 0;
-            const unsigned long long x = a[r], y = a[r2];
-            const bool sw = desc ? (x < y) : (x > y);
-            a[r] = sw ? y : x;
-            a[r2] = sw ? x : y;
-          }
-        }
-      } else {
-        const int lx = stride / R;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int i = lane * R + r;
-          const unsigned long long o = __shfl_xor_sync(kSettleFull, a[r], lx);
-          const bool desc = (i & size) == 0;
-          const bool lower = (i & stride) == 0;
-          const bool keep_max = desc == lower;
-          a[r] = keep_max ? (o > a[r] ? o : a[r]) : (o < a[r] ? o : a[r]);
+#pragma unroll 1
+      for (int q = lane; q < (N >> 1); q += 32) {
+        const int lo = 2 * q - (q & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const u64 a = s[lo], b = s[hi];
+        if ((a < b) == desc) {
+          s[lo] = b;
+          s[hi] = a;
         }
       }
+      __syncwarp();
     }
   }
 }
 
-// Sort cand[0..n) (n <= 32 R, kept keys > 0) in place, descending.
-template <int R>
-__device__ __forceinline__ void sort_cands(unsigned long long* cand, int n) {
+// ---------------------------------------------------------------------------
+// Small top-k, one warp.
+// ---------------------------------------------------------------------------
+constexpr int kSel = 256;                  // candidates held for the sort
+
+// Scratch of one warp: its two stream buffers.
+struct TopkScratch {
+  u64 cand[kMaxListCand];                  // the A items' lists as total-order keys (0 = none)
+  uint32_t hist[256];
+  u64 sel[kSel];                           // the selected candidates
+  uint8_t cflag[kMaxListCand / kList];     // per chunk: bit 0 NaN, bit 1 partial list
+};
+static_assert(sizeof(TopkScratch) <= 2 * kSlot, "top-k scratch exceeds a warp's stream buffers");
+
+// The list phase reuses the candidate area.
+struct ListArrays {
+  uint32_t idx[kTopkSmall];
+  float val[kTopkSmall], e[kTopkSmall], cum[kTopkSmall], q[kTopkSmall], w[kTopkSmall], wu[kTopkSmall];
+};
+static_assert(sizeof(ListArrays) <= sizeof(u64) * kMaxListCand, "list arrays exceed the candidate area");
+
+// Calls fn(g, v) on every lane for groups 8 entries g = g0 + step * 32 + lane
+// (g < g1; lanes past the end get g = -1 and -inf values), loading four steps
+// ahead.
+template <bool kBF16, typename F>
+__device__ __forceinline__ void sweep_range(const Args& A, size_t lrow, int g0, int g1, F fn) {
   const int lane = threadIdx.x & 31;
-  unsigned long long a[R];
+  for (int base = g0; base < g1; base += 128) {
+    float v[4][8];
+    int g[4];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int i = lane * R + r;
-    a[r] = i < n ? cand[i] : 0ull;
-  }
-  warp_bitonic_desc<R>(a);
-  __syncwarp();
+    for (int s = 0; s < 4; ++s) {
+      g[s] = base + 32 * s + lane;
+      if (g[s] < g1) {
+        load_group<kBF16>(A, lrow, g[s], true, v[s]);
+      } else {
+        g[s] = -1;
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int i = lane * R + r;
-    if (i < n) cand[i] = a[r];
+        for (int i = 0; i < 8; ++i) v[s][i] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      if (base + 32 * s < g1) fn(g[s], v[s]);
   }
-  __syncwarp();
 }
 
-// Exact selection when more than kCandCap candidates pass the bound: the
-// K-th largest candidate key by radix passes over the listed super-groups
-// (8 bits at a time from the top), then the entries above it and the first
-// ties in index order, K in all, into cand[].
+// Appends, in the order of the calls, the entries whose bit is set in `keep`
+// (8 per lane, entries 8g..8g+7) to sel[*n ...] (up to kSel); *n counts all.
+__device__ __forceinline__ void append_entries(u64* sel, uint32_t* n, int g, uint32_t keep, const uint32_t* keys) {
+  uint32_t tot = 0;
+  uint32_t p = *n + warp_excl_scan((uint32_t)__popc(keep), &tot);
+  *n += tot;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if ((keep >> i) & 1u) {
+      if (p < (uint32_t)kSel) sel[p] = key64(keys[i], (uint32_t)(g * 8 + i));
+      ++p;
+    }
+}
+
+// Exact top-K (or every finite entry, when fewer) of the whole row into
+// sel[], by radix passes over the row (8 bits at a time from the top), then
+// the entries above the K-th key and the first ties in index order.  For rows
+// whose lists cannot settle the unit (masses of ties).  Returns the count.
 template <bool kBF16>
-__device__ __noinline__ void select_k_exact(const Args& A, TopkScratch& S, size_t lrow, int n_sg, uint32_t T32,
-                                            int K) {
+__device__ __noinline__ int select_k_row(const Args& A, TopkScratch& S, size_t lrow, int K) {
   const int lane = threadIdx.x & 31;
+  const int G = (A.V + 7) / 8;
+  const uint32_t T32 = okey(-INFINITY) + 1u;          // finite entries
   uint32_t prefix = 0u, mask = 0u, need = (uint32_t)K;
+  bool all = false;
   const int lowest = kBF16 ? 16 : 0;        // bf16 keys are fixed by their top 16 bits
   for (int shift = 24; shift >= lowest; shift -= 8) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) S.hist[8 * lane + i] = 0u;
     __syncwarp();
-    sweep_groups<kBF16>(A, lrow, S.sg, n_sg, [&](int g, const float* v) {
+    sweep_range<kBF16>(A, lrow, 0, G, [&](int g, const float* v) {
       if (g < 0) return;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -399,60 +570,57 @@ __device__ __noinline__ void select_k_exact(const Args& A, TopkScratch& S, size_
     __syncwarp();
     uint32_t before = 0;
     const int b = warp_select_bin(S.hist, need, &before);
-    need -= before;
-    prefix |= (uint32_t)(255 - min(b, 255)) << shift;
-    mask |= 255u << shift;
     __syncwarp();
+    if (b == 256) {            // fewer than K finite entries: all of them
+      all = true;
+      break;
+    }
+    need -= before;
+    prefix |= (uint32_t)(255 - b) << shift;
+    mask |= 255u << shift;
   }
-  uint32_t tkey = prefix;
-  if (kBF16) tkey = full_key<true>(prefix >> 16);
-  // `need` ties at tkey (in index order) complete the K entries above it
+  const uint32_t tkey = all ? T32 : (kBF16 ? full_key<true>(prefix >> 16) : prefix);
   uint32_t n_out = 0, ties_seen = 0;
-  sweep_groups<kBF16>(A, lrow, S.sg, n_sg, [&](int g, const float* v) {
+  sweep_range<kBF16>(A, lrow, 0, G, [&](int g, const float* v) {
     uint32_t gt = 0, eq = 0;
     uint32_t keys[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       keys[i] = okey(v[i]);
       const bool in = g >= 0 && g * 8 + i < A.V;
-      gt |= (in && keys[i] > tkey) ? (1u << i) : 0u;
-      eq |= (in && keys[i] == tkey) ? (1u << i) : 0u;
+      gt |= (in && (all ? keys[i] >= tkey : keys[i] > tkey)) ? (1u << i) : 0u;
+      eq |= (in && !all && keys[i] == tkey) ? (1u << i) : 0u;
     }
     uint32_t te = 0;
-    const uint32_t tbase = ties_seen + warp_excl_scan((uint32_t)__popc(eq), &te);
+    uint32_t r = ties_seen + warp_excl_scan((uint32_t)__popc(eq), &te);
     ties_seen += te;
-    // keep the ties of rank < need
     uint32_t keep = gt;
-    uint32_t r = tbase;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if ((eq >> i) & 1u) {
         if (r < need) keep |= 1u << i;
         ++r;
       }
-    uint32_t tk = 0;
-    uint32_t pos = n_out + warp_excl_scan((uint32_t)__popc(keep), &tk);
-    n_out += tk;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((keep >> i) & 1u) {
-        if (pos < (uint32_t)kCandCap) S.cand[pos] = key64(keys[i], (uint32_t)(g * 8 + i));
-        ++pos;
-      }
+    append_entries(S.sel, &n_out, g, keep, keys);
   });
   __syncwarp();
+  return (int)min(n_out, (uint32_t)kSel);
 }
 
 // Settle a small top-k unit with one warp.
 template <bool kBF16>
-__device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
+                                         const RowCfg& cfg) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
-  const int nsm = ceil_div(A.V, G::EA) * G::SPI;
+  const int NC = ceil_div(A.V, G::EA);
+  const int NL = NC * kList;
+  const u64* R = A.rec + (size_t)u * A.NCA * kRecWords;
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const float c = cfg.c;
+  const int K = cfg.K;
   // the accept test's operands are in flight while the list is built (lane 0)
   Pre pr;
   pr.x = -1;
@@ -461,182 +629,216 @@ __device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, i
   pr.qx = 0.f;
   if (lane == 0) pr = load_pre<kBF16>(A, u, row, pos);
 
-  // 1. super-group maxima -> 16-bit keys; the unit max; NaN
-  const float4* src = reinterpret_cast<const float4*>(A.smax + (size_t)u * A.NSM);
-  float mf = -INFINITY;
-  bool nan = false;
-  for (int base = 0; base < nsm; base += 4 * 128) {
-    float4 x[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int i = base + s * 128 + lane * 4;
-      x[s] = i < nsm ? __ldcg(src + (i >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int i = base + s * 128 + lane * 4;
-      if (i >= nsm) continue;
-      const float e[4] = {x[s].x, x[s].y, x[s].z, x[s].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        nan |= e[j] != e[j];
-        mf = fmaxf(mf, e[j]);
-        S.sg[i + j] = (uint16_t)k16(e[j]);
+  // 1. the chunks' lists (raw words into the candidate area, then keys in place)
+  uint32_t* raw = reinterpret_cast<uint32_t*>(S.cand);
+  uint8_t* cflag = S.cflag;
+  if (wait_word(A, R + (size_t)(NC - 1) * kRecWords, tag)) {
+    long long spins = 0;
+    bool ok;
+    do {
+      ok = true;
+      for (int i = lane; i < NC * kRecWords; i += 32) {
+        const u64 w = __ldcg(R + i);
+        ok = ok && tag_ok(w, tag);
+        raw[i] = wu(w);
       }
-    }
+    } while (poll_again(A, ok, spins));
+  }
+  __syncwarp();
+  for (int q = lane; q < NL; q += 32) {
+    const uint32_t key = raw[2 * q];
+    const uint32_t iw = raw[2 * q + 1];
+    const int ch = q / kList;
+    if ((q & (kList - 1)) == 0) cflag[ch] = (uint8_t)(((iw & kListNaN) ? 1u : 0u) | ((iw & kListPartial) ? 2u : 0u));
+    S.cand[q] = key ? key64(key, (uint32_t)(ch * G::EA) + (iw & kListIdx)) : 0ull;
+  }
+  __syncwarp();
+  bool nan = false, any_partial = false;
+  for (int ch = lane; ch < NC; ch += 32) {
+    nan |= (cflag[ch] & 1u) != 0;
+    any_partial |= (cflag[ch] & 2u) != 0;
   }
   nan = __any_sync(kSettleFull, nan);
-  const float m = warp_max_f(mf);
-  if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
+  any_partial = __any_sync(kSettleFull, any_partial);
+  unsigned long long top = 0;
+  for (int q = lane; q < NL; q += 32) top = S.cand[q] > top ? S.cand[q] : top;
+  top = warp_max_u64(top);
+  const float m = from_okey((uint32_t)(top >> 32));
+  if (nan || top == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
     if (lane == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
     __syncwarp();
     return;
   }
-  const uint32_t km = okey(m);
-  const uint32_t km16 = km >> 16;
-  const uint32_t kpos = positive_key(m, c, km);
-  const uint32_t kpos16 = kpos >> 16;
+  const int am = (int)key64_idx(top);
+
+  // 2. the K-th listed entry, from a histogram of 16-bit key distances to
+  // the max (bin 255 lumps the rest), then a sort of the entries at or
+  // above its 16-bit key
+  const uint32_t km16 = (uint32_t)(top >> 48);
+  __syncwarp();
 #pragma unroll
   for (int i = 0; i < 8; ++i) S.hist[8 * lane + i] = 0u;
   __syncwarp();
-
-  // 2. tau16: the K-th largest positive super-group key, from a histogram of
-  // distances to the unit max (the 255th bin lumps the rest)
-  for (int s = lane; s < nsm; s += 32) {
-    const uint32_t kk = S.sg[s];
-    if (kk >= kpos16) atomicAdd(&S.hist[min(km16 - kk, 255u)], 1u);
-  }
+  for (int q = lane; q < NL; q += 32)
+    if (S.cand[q]) atomicAdd(&S.hist[min(km16 - (uint32_t)(S.cand[q] >> 48), 255u)], 1u);
   __syncwarp();
   uint32_t before = 0;
-  const int b = warp_select_bin(S.hist, (uint32_t)cfg.K, &before);
+  const int b = warp_select_bin(S.hist, (uint32_t)K, &before);
   uint32_t tau16;
   if (b == 256) {
-    tau16 = kpos16;                          // fewer than K positive super-groups: all qualify
+    tau16 = 0u;                               // fewer than K listed entries: all
   } else if (b < 255) {
     tau16 = km16 - (uint32_t)b;
   } else {
-    // the K-th lies in the lumped tail: bisect the 16-bit key space
-    uint32_t lo = kpos16, hi = km16;           // count(key >= lo) >= K holds
+    uint32_t lo = 0u, hi = km16;              // count(key16 >= lo) >= K holds
     while (lo < hi) {
       const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
       uint32_t cnt = 0;
-      for (int s = lane; s < nsm; s += 32) cnt += S.sg[s] >= mid ? 1u : 0u;
+      for (int q = lane; q < NL; q += 32) cnt += (S.cand[q] && (uint32_t)(S.cand[q] >> 48) >= mid) ? 1u : 0u;
       cnt = __reduce_add_sync(kSettleFull, cnt);
-      if (cnt >= (uint32_t)cfg.K) lo = mid;
+      if (cnt >= (uint32_t)K) lo = mid;
       else hi = mid - 1u;
     }
     tau16 = lo;
   }
-  tau16 = max(tau16, kpos16);
-  const uint32_t T32 = max(tau16 << 16, kpos);
-
-  // 3. the qualifying super-groups, ids in increasing order (in place)
-  int n_sg = 0;
-  for (int base = 0; base < nsm; base += 32) {
-    const int s = base + lane;
-    const bool q = s < nsm && (uint32_t)S.sg[s] >= tau16;
-    const unsigned ball = __ballot_sync(kSettleFull, q);
-    __syncwarp();
-    if (q) S.sg[n_sg + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)s;
-    n_sg += __popc(ball);
-    __syncwarp();
-  }
-
-  // 4. candidates: entries with key >= T32 of those super-groups
   uint32_t n_c = 0;
-  sweep_groups<kBF16>(A, lrow, S.sg, n_sg, [&](int g, const float* v) {
-    uint32_t hit = 0;
-    uint32_t keys[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      keys[i] = okey(v[i]);
-      hit |= (g >= 0 && g * 8 + i < A.V && keys[i] >= T32) ? (1u << i) : 0u;
-    }
-    uint32_t tot = 0;
-    uint32_t p = n_c + warp_excl_scan((uint32_t)__popc(hit), &tot);
-    n_c += tot;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((hit >> i) & 1u) {
-        if (p < (uint32_t)kCandCap) S.cand[p] = key64(keys[i], (uint32_t)(g * 8 + i));
-        ++p;
-      }
-  });
+  for (int base = 0; base < NL; base += 32) {
+    const int q = base + lane;
+    const u64 k = q < NL ? S.cand[q] : 0ull;
+    const bool in = k && (uint32_t)(k >> 48) >= tau16;
+    const unsigned ball = __ballot_sync(kSettleFull, in);
+    const uint32_t p = n_c + __popc(ball & ((1u << lane) - 1u));
+    if (in && p < (uint32_t)kSel) S.sel[p] = k;
+    n_c += __popc(ball);
+  }
   __syncwarp();
-  int n_k;
-  if (n_c <= (uint32_t)kCandCap) {
-    if (n_c <= 128) sort_cands<4>(S.cand, (int)n_c);
-    else sort_cands<8>(S.cand, (int)n_c);
-    n_k = min((int)n_c, cfg.K);
-  } else {
-    select_k_exact<kBF16>(A, S, lrow, n_sg, T32, cfg.K);
-    n_k = cfg.K;
-    sort_cands<4>(S.cand, n_k);
+  int n_k = 0;
+  bool exact = n_c <= (uint32_t)kSel;
+  if (exact) {
+    warp_sort_desc(S.sel, (int)n_c);
+    // a chunk whose list is full and ends above the K-th entry may hold more
+    const u64 kappa = (int)n_c >= K ? S.sel[K - 1] : 0ull;
+    bool unsafe = false;
+    for (int ch = lane; ch < NC; ch += 32) {
+      const u64 last = S.cand[ch * kList + kList - 1];
+      unsafe |= (cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa);
+    }
+    if (__any_sync(kSettleFull, unsafe)) {
+      // re-read those chunks: their entries at or above kappa join the listed
+      // entries at or above kappa of the other chunks
+      uint32_t n = 0;
+      for (int base = 0; base < NL; base += 32) {
+        const int q = base + lane;
+        const u64 k = q < NL ? S.cand[q] : 0ull;
+        const int ch = q / kList;
+        const u64 last = q < NL ? S.cand[ch * kList + kList - 1] : 0ull;
+        const bool safe_ch = q < NL && (cflag[ch] & 2u) == 0 && !(last != 0ull && last > kappa);
+        const bool in = safe_ch && k != 0ull && k >= kappa;
+        const unsigned ball = __ballot_sync(kSettleFull, in);
+        const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
+        if (in && p < (uint32_t)kSel) S.sel[p] = k;
+        n += __popc(ball);
+      }
+      const uint32_t kk = (uint32_t)(kappa >> 32);
+      const uint32_t T = max(kk, okey(-INFINITY) + 1u);
+      for (int ch = 0; ch < NC; ++ch) {
+        const u64 last = S.cand[ch * kList + kList - 1];
+        if (!((cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa))) continue;
+        const int g0 = ch * (G::EA / 8);
+        const int g1 = min(ceil_div(A.V, 8), g0 + G::EA / 8);
+        sweep_range<kBF16>(A, lrow, g0, g1, [&](int g, const float* v) {
+          uint32_t keep = 0;
+          uint32_t keys[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            keys[i] = okey(v[i]);
+            const bool inr = g >= 0 && g * 8 + i < A.V && keys[i] >= T &&
+                             key64(keys[i], (uint32_t)(g * 8 + i)) >= kappa;
+            keep |= inr ? (1u << i) : 0u;
+          }
+          append_entries(S.sel, &n, g, keep, keys);
+        });
+      }
+      __syncwarp();
+      if (n <= (uint32_t)kSel) {
+        warp_sort_desc(S.sel, (int)n);
+        n_k = min((int)n, K);
+      } else {
+        exact = false;
+      }
+    } else {
+      n_k = min((int)n_c, K);
+    }
+  }
+  if (!exact) {
+    const int n = select_k_row<kBF16>(A, S, lrow, K);
+    warp_sort_desc(S.sel, n);
+    n_k = min(n, K);
   }
 
-  // 5. the list: lane l holds entries 4l..4l+3 of the first n_k
-  ListArrays& L = *reinterpret_cast<ListArrays*>(S.sg);
-  uint32_t idx[4];
-  float val[4], e[4], qv[4];
+  // 3. the list: entry i = 32 r + lane in round r, arrays in shared memory
+  ListArrays& L = *reinterpret_cast<ListArrays*>(S.cand);
+  const int nr = (n_k + 31) >> 5;
+  {
+    float qv[kTopkSmall / 32];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = 4 * lane + j;
-    const unsigned long long key = i < n_k ? S.cand[i] : 0ull;
-    idx[j] = key64_idx(key);
-    val[j] = from_okey((uint32_t)(key >> 32));
-    qv[j] = 0.f;
-    if (has_q && i < n_k) qv[j] = A.q[qrow + idx[j]];   // in flight while the list is settled
-    e[j] = i < n_k ? ex2((val[j] - m) * c) : 0.f;
+    for (int r = 0; r < kTopkSmall / 32; ++r) {      // q loads in flight together
+      const int i = 32 * r + lane;
+      qv[r] = (has_q && i < n_k) ? A.q[qrow + key64_idx(S.sel[i])] : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < kTopkSmall / 32; ++r) {
+      const int i = 32 * r + lane;
+      if (i < n_k) {
+        const u64 key = S.sel[i];
+        L.idx[i] = key64_idx(key);
+        L.val[i] = from_okey((uint32_t)(key >> 32));
+        L.e[i] = ex2((L.val[i] - m) * c);
+        L.q[i] = qv[r];
+      }
+    }
   }
-  const int am = (int)__shfl_sync(kSettleFull, idx[0], 0);
   pr.x = __shfl_sync(kSettleFull, pr.x, 0);
   pr.valid = __shfl_sync(kSettleFull, pr.valid, 0);
   pr.lx = __shfl_sync(kSettleFull, pr.lx, 0);
   pr.qx = __shfl_sync(kSettleFull, pr.qx, 0);
   // inclusive prefix sums in the total order (fixed order)
-  float cum[4];
-  cum[0] = e[0];
-  cum[1] = cum[0] + e[1];
-  cum[2] = cum[1] + e[2];
-  cum[3] = cum[2] + e[3];
-  float inc = cum[3];
+  float run = 0.f;
+#pragma unroll 1
+  for (int r = 0; r < nr; ++r) {
+    const int i = 32 * r + lane;
+    float inc = i < n_k ? L.e[i] : 0.f;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(kSettleFull, inc, o);
-    if (lane >= o) inc += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(kSettleFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (i < n_k) L.cum[i] = run + inc;
+    run += __shfl_sync(kSettleFull, inc, 31);
   }
-  const float off = inc - cum[3];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) cum[j] += off;
-  auto cum_at = [&](int i) {      // cum of entry i (every lane)
-    const int j = i & 3;
-    const float x = j == 0 ? cum[0] : (j == 1 ? cum[1] : (j == 2 ? cum[2] : cum[3]));
-    return __shfl_sync(kSettleFull, x, i >> 2);
-  };
-  const float Zk = cum_at(n_k - 1);
+  __syncwarp();
+  const float Zk = L.cum[n_k - 1];
   uint32_t flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
   int n_s = n_k;
   if (cfg.P < 1.0f) {
     const float target = cfg.P * Zk;
-    int first = 4;
-#pragma unroll
-    for (int j = 3; j >= 0; --j)
-      if (4 * lane + j < n_k && cum[j] >= target) first = j;
-    const unsigned ball = __ballot_sync(kSettleFull, first < 4);
-    if (ball) {
-      const int sl = __ffs(ball) - 1;
-      n_s = 4 * sl + __shfl_sync(kSettleFull, first, sl) + 1;
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+      const int i = 32 * r + lane;
+      const unsigned ball = __ballot_sync(kSettleFull, i < n_k && L.cum[i] >= target);
+      if (ball) {
+        n_s = 32 * r + __ffs(ball);
+        break;
+      }
     }
-    const float at = cum_at(n_s - 1) / Zk;
-    const float bef = n_s >= 2 ? cum_at(n_s - 2) / Zk : 0.f;
+    const float at = L.cum[n_s - 1] / Zk;
+    const float bef = n_s >= 2 ? L.cum[n_s - 2] / Zk : 0.f;
     if (fabsf(at - cfg.P) < kMargin || fabsf(cfg.P - bef) < kMargin) flags |= SPEC_F_MARGIN_TOPP;
   }
-  const float Zs = cum_at(n_s - 1);
+  const float Zs = L.cum[n_s - 1];
   const float invZ = 1.0f / Zs;
   const float lnZ = logf(Zs);
-  float p[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) p[j] = 4 * lane + j < n_s ? e[j] * invZ : 0.f;
+  const int ns_r = (n_s + 31) >> 5;
   float alpha_v = 0.f;
   AcceptInfo ai;
   ai.valid = true;
@@ -646,11 +848,12 @@ __device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, i
   bool need_race = !has_q;
   if (has_q) {
     float a = 0.f, ex = -1.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (4 * lane + j < n_s) {
-        a += fminf(p[j], qv[j]);
-        if (idx[j] == (uint32_t)pr.x) ex = e[j];
+#pragma unroll 1
+    for (int r = 0; r < ns_r; ++r) {
+      const int i = 32 * r + lane;
+      if (i < n_s) {
+        a += fminf(L.e[i] * invZ, L.q[i]);
+        if (L.idx[i] == (uint32_t)pr.x) ex = L.e[i];
       }
     }
     alpha_v = warp_sum(a);
@@ -668,22 +871,21 @@ __device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, i
     ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
     need_race = !ai.accept;
   }
-  // 6. the draw: the two-level race over the kept entries (blocks by index)
+  // 4. the draw: the two-level race over the kept entries (blocks by index)
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
   if (need_race) {
+#pragma unroll 1
     for (int attempt = 0; attempt < 2; ++attempt) {
       const bool use_p = attempt == 1;          // empty residual: draw from p
-      float w[4], tq[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool mine = 4 * lane + j < n_s;
-        w[j] = mine ? ((has_q && !use_p) ? fmaxf(p[j] - qv[j], 0.f) : p[j]) : 0.f;
-        tq[j] = (mine && has_q && !use_p) ? 2.0f * qv[j] : 0.f;
-        if (4 * lane + j < kTopkSmall) {
-          L.blk[4 * lane + j] = idx[j] / kRaceBlock;
-          L.w[4 * lane + j] = w[j];
-          L.wu[4 * lane + j] = w[j] + tq[j];
+#pragma unroll 1
+      for (int r = 0; r < ns_r; ++r) {
+        const int i = 32 * r + lane;
+        if (i < n_s) {
+          const float p = L.e[i] * invZ;
+          const float w = (has_q && !use_p) ? fmaxf(p - L.q[i], 0.f) : p;
+          L.w[i] = w;
+          L.wu[i] = w + ((has_q && !use_p) ? 2.0f * L.q[i] : 0.f);
         }
       }
       __syncwarp();
@@ -691,35 +893,40 @@ __device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, i
       // the block's weights summed in list order
       Race r1;
       race_init(r1);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = 4 * lane + j;
-        if (!(w[j] > 0.f)) continue;
-        const uint32_t bb = idx[j] / kRaceBlock;
-        bool rep = true;
-        float W = 0.f, U = 0.f;
-        for (int t = 0; t < n_s; ++t) {
-          if (L.blk[t] == bb && L.w[t] > 0.f) {
-            if (t < i) rep = false;
-            W += L.w[t];
-            U += L.wu[t];
+#pragma unroll 1
+      for (int r = 0; r < ns_r; ++r) {
+        const int i = 32 * r + lane;
+        if (i < n_s && L.w[i] > 0.f) {
+          const uint32_t bb = L.idx[i] / kRaceBlock;
+          bool rep = true;
+          float W = 0.f, U = 0.f;
+#pragma unroll 1
+          for (int t = 0; t < n_s; ++t) {
+            if (L.idx[t] / kRaceBlock == bb && L.w[t] > 0.f) {
+              if (t < i) rep = false;
+              W += L.w[t];
+              U += L.wu[t];
+            }
           }
+          if (rep) race_consider(r1, W, U - W, bb, block_word(A, row, pos, bb));
         }
-        if (rep) race_consider(r1, W, U - W, bb, block_word(A, row, pos, bb));
       }
       warp_race_merge(r1);
-      __syncwarp();
       if (r1.s1 < 0.f) {
         draw_flags |= SPEC_F_RESIDUAL_EMPTY;
+        __syncwarp();
         continue;
       }
       // level 2: the entries of the winning block
       Race r2;
       race_init(r2);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (w[j] > 0.f && idx[j] / kRaceBlock == r1.v1)
-          race_consider(r2, w[j], tq[j], idx[j], race_word(A, row, pos, idx[j]));
+#pragma unroll 1
+      for (int r = 0; r < ns_r; ++r) {
+        const int i = 32 * r + lane;
+        if (i < n_s && L.w[i] > 0.f && L.idx[i] / kRaceBlock == r1.v1)
+          race_consider(r2, L.w[i], (has_q && !use_p) ? 2.0f * L.q[i] : 0.f, L.idx[i],
+                        race_word(A, row, pos, L.idx[i]));
+      }
       warp_race_merge(r2);
       y = r2.v1;
       if (draw_margin(r1) || draw_margin(r2)) draw_flags |= SPEC_F_MARGIN_DRAW;
@@ -731,12 +938,14 @@ __device__ __noinline__ void topk_settle(const Args& A, TopkScratch& S, int u, i
   {
     float vv = 0.f;
     bool own = false;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (4 * lane + j < n_k && idx[j] == y) {
-        vv = val[j];
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+      const int i = 32 * r + lane;
+      if (i < n_k && L.idx[i] == y) {
+        vv = L.val[i];
         own = true;
       }
+    }
     const unsigned ob = __ballot_sync(kSettleFull, own);
     if (ob) vy = __shfl_sync(kSettleFull, vv, __ffs(ob) - 1);
   }

@@ -63,13 +63,10 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   A.ws = reinterpret_cast<specv::WsHeader*>(ws);
   A.row_ticket = reinterpret_cast<uint32_t*>(ws + L.row_ticket);
-  A.b_ticket = reinterpret_cast<uint32_t*>(ws + L.b_ticket);
-  A.ready = reinterpret_cast<uint32_t*>(ws + L.ready);
-  A.crec = reinterpret_cast<specv::ChunkRec*>(ws + L.crec);
-  A.ust = reinterpret_cast<specv::UnitState*>(ws + L.ust);
-  A.brec = reinterpret_cast<specv::BRec*>(ws + L.brec);
+  A.rec = reinterpret_cast<specv::u64*>(ws + L.rec);
+  A.ust = reinterpret_cast<specv::u64*>(ws + L.ust);
+  A.brec = reinterpret_cast<specv::u64*>(ws + L.brec);
   A.urec = reinterpret_cast<specv::UnitRecord*>(ws + L.urec);
-  A.smax = reinterpret_cast<float*>(ws + L.smax);
   A.order = reinterpret_cast<uint32_t*>(ws + L.order);
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);
@@ -79,7 +76,6 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   A.U = B * (k + 1);
   A.NCA = specv::max_nca(V);
   A.NCB = specv::max_ncb(V);
-  A.NSM = specv::max_nsm(V);
   A.vec_logits = aligned(logits, 16) && ((size_t)V * es) % 16 == 0;
   A.vec_q = k > 0 && aligned(draft_probs, 16) && (V % 4) == 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);

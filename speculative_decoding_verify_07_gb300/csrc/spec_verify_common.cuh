@@ -24,13 +24,13 @@ namespace specv {
 
 constexpr int kRaceBlock = 256;            // entries per block of the two-level race
 constexpr int kTopkSmall = 128;            // top_k <= this: candidate-list path
-constexpr int kMaxNsmTopk = 4096;          // ... when the super-group maxima of a row fit the finaliser
+constexpr int kMaxListCand = 1024;         // ... when the A items' candidate lists of a row fit a settle warp
 constexpr long long kSpinLimit = 1ll << 22;
 
-// Streaming geometry.  Every warp of the streaming kernels owns two buffers
-// of kSlot bytes; an A item is one buffer of logits, a B item one buffer of
-// logits plus the matching draft probabilities.  Items cover whole race
-// blocks of 256 entries; a super-group is 64 consecutive entries.
+// Streaming geometry.  Every streaming warp owns two buffers of kSlot
+// bytes; an A item is one buffer of logits, a B item one buffer of logits
+// plus the matching draft probabilities.  Items cover whole race blocks of
+// 256 entries.
 constexpr int kSlot = 6144;
 template <bool kBF16>
 struct Geo {
@@ -39,20 +39,22 @@ struct Geo {
   static constexpr int EB = (kSlot / (es + 4)) / kRaceBlock * kRaceBlock;   // B item entries (1024 / 768)
   static constexpr int NBA = EA / kRaceBlock;                      // blocks per A item
   static constexpr int NBB = EB / kRaceBlock;                      // blocks per B item
-  static constexpr int SPI = EA / 64;                              // 64-entry super-groups per A item
 };
 
 enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
 
 struct WsHeader {
   uint32_t gnext;         // next general-path unit
-  uint32_t arrived;       // CTAs through the grid barrier
   uint32_t ctas_done;     // CTAs that left the kernel
-  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait; bit 2: the grid barrier
+  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait; bit 2: a record wait; bit 3: the order wait
+  uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
   uint32_t pad0[4];
-  uint32_t n_class[4];    // rows per class (batches above the shared-memory order limit)
-  uint32_t pad[52];
+  uint32_t n_class[4];    // rows per class (large batches)
+  uint32_t pad[47];
+  uint32_t epoch;         // tag of the last completed call (records of this call carry epoch + 1)
+  uint32_t pad1[4];
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header");
 
 // Settle groups of the general path: each half of a CTA (256 threads) runs
 // the group-wide code on its own named barrier (ids 1 and 2).
@@ -61,17 +63,37 @@ __device__ __forceinline__ void csync() {
   asm volatile("bar.sync %0, 256;" ::"r"(1 + (int)(threadIdx.x >> 8)) : "memory");
 }
 
-struct ChunkRec {         // 48 bytes, one per (unit, A item)
-  float m;                // chunk max (NaN when the chunk holds a NaN)
-  uint32_t amax;          // first index of the chunk max
-  float z;                // sum of exp((l - m_chunk) * c)
-  uint32_t pad0;
-  float s1, t1, s2, t2;   // level-1 race over the chunk's blocks, relative to the chunk max (bonus units)
-  uint32_t v1;
-  uint32_t pad[3];
-};
+// Records pass between warps without fences: every 64-bit word carries the
+// call's tag in its high half and one 32-bit value in its low half, and a
+// reader takes a word as written once it carries the current tag (aligned
+// 64-bit accesses are single-copy atomic).
+//   A record, per (unit, A item), 16 words:
+//     greedy / unfiltered: [0] chunk max (NaN when the chunk holds a NaN),
+//       [1] first index of the chunk max (greedy), [2] sum of exp2((l - m) c)
+//       relative to the chunk max, [3..7] level-1 race of the chunk's blocks
+//       relative to the chunk max (s1, t1, s2, t2, v1; bonus positions);
+//     small top-k: [2j] order key and [2j + 1] chunk-local index of the
+//       chunk's j-th entry in the total order (j < 8; key 0 = none), with
+//       the flags kListNaN / kListPartial in word 1.
+//   B record, per (unit, B item), 8 words: [0] alpha, [1..5] level-1 race of
+//     the residual (s1, t1, s2, t2, v1).
+//   Unit state of a drafted unfiltered unit, 8 words: m, 1/Z, ln Z, the
+//     draft's logprob, accept, flags, invalid, argmax (see UnitState).
+constexpr int kRecWords = 16;
+constexpr int kBRecWords = 8;
+constexpr int kStateWords = 8;
+constexpr int kList = 8;                   // entries listed per top-k A item
+constexpr uint32_t kListNaN = 1u << 31;    // the chunk holds a NaN
+constexpr uint32_t kListPartial = 1u << 30;   // the list may miss entries above its last (re-scan the chunk)
+constexpr uint32_t kListIdx = (1u << 30) - 1u;
+typedef unsigned long long u64;
+__device__ __forceinline__ u64 tagw(uint32_t tag, uint32_t v) { return ((u64)tag << 32) | v; }
+__device__ __forceinline__ u64 tagf(uint32_t tag, float v) { return tagw(tag, __float_as_uint(v)); }
+__device__ __forceinline__ bool tag_ok(u64 w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+__device__ __forceinline__ float wf(u64 w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t wu(u64 w) { return (uint32_t)w; }
 
-struct UnitState {        // 32 bytes: what the B items of a drafted unfiltered unit need
+struct UnitState {        // what the B items of a drafted unfiltered unit need
   float m, invZ, lnZ, lp_x;
   int32_t accept;
   uint32_t flags;         // BAD_TOKEN | MARGIN_ACCEPT | BAD_PARAM of this unit
@@ -79,11 +101,6 @@ struct UnitState {        // 32 bytes: what the B items of a drafted unfiltered 
   int32_t am;
 };
 
-struct BRec {             // 32 bytes per (unit, B item)
-  float alpha, s1, t1, s2, t2;
-  uint32_t v1;
-  uint32_t pad[2];
-};
 
 struct UnitRecord {       // 32 bytes, one per unit, read by the row finaliser
   uint32_t flags;
@@ -102,14 +119,9 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // Per-unit record counts, sized for the larger of the two logit dtypes.
 __host__ __device__ inline int max_nca(int V) { return ceil_div(V, Geo<false>::EA); }
 __host__ __device__ inline int max_ncb(int V) { return ceil_div(V, Geo<false>::EB); }
-__host__ __device__ inline int max_nsm(int V) {
-  const int a = ceil_div(V, Geo<true>::EA) * Geo<true>::SPI;
-  const int b = ceil_div(V, Geo<false>::EA) * Geo<false>::SPI;
-  return a > b ? a : b;
-}
 
 struct Layout {
-  size_t row_ticket, b_ticket, ready, crec, ust, brec, urec, smax, order, total;
+  size_t row_ticket, rec, brec, ust, urec, order, total;
 };
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
@@ -117,13 +129,10 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   Layout L;
   size_t off = sizeof(WsHeader);
   L.row_ticket = off; off = align_up(off + (size_t)B * 4, 256);
-  L.b_ticket = off; off = align_up(off + U * 4, 256);
-  L.ready = off; off = align_up(off + U * 4, 256);
-  L.crec = off; off = align_up(off + U * max_nca(V) * sizeof(ChunkRec), 256);
-  L.ust = off; off = align_up(off + U * sizeof(UnitState), 256);
-  L.brec = off; off = align_up(off + U * max_ncb(V) * sizeof(BRec), 256);
+  L.rec = off; off = align_up(off + U * max_nca(V) * kRecWords * 8, 256);
+  L.brec = off; off = align_up(off + U * max_ncb(V) * kBRecWords * 8, 256);
+  L.ust = off; off = align_up(off + U * kStateWords * 8, 256);
   L.urec = off; off = align_up(off + U * sizeof(UnitRecord), 256);
-  L.smax = off; off = align_up(off + U * max_nsm(V) * 4, 256);
   L.order = off; off = align_up(off + (size_t)B * 4, 256);
   L.total = off;
   return L;
@@ -141,17 +150,14 @@ struct Args {
   uint32_t* flags;
   WsHeader* ws;
   uint32_t* row_ticket;
-  uint32_t* b_ticket;     // B items done per drafted unfiltered unit
-  uint32_t* ready;        // the unit state of a drafted unfiltered unit is published
-  ChunkRec* crec;
-  UnitState* ust;
-  BRec* brec;
+  u64* rec;               // A records
+  u64* brec;              // B records
+  u64* ust;               // unit states of drafted unfiltered units
   UnitRecord* urec;
-  float* smax;
   uint32_t* order;        // rows by class (batches above the shared-memory order limit)
   uint32_t key0, key1;
   int B, k, V, U;
-  int NCA, NCB, NSM;      // record strides per unit: A items, B items, super-group maxima
+  int NCA, NCB;           // record strides per unit: A items, B items
   int n_ctas;             // CTAs of the kernel
   int global_order;       // the row order lives in the workspace
   int vec_logits;
@@ -183,7 +189,7 @@ __device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
   r.c = greedy ? kLog2e : kLog2e / T;
   r.invT = greedy ? 1.0f : 1.0f / T;
   if (greedy) r.type = UT_GREEDY;
-  else if (r.K > 0 && r.K <= kTopkSmall && max_nsm(V) <= kMaxNsmTopk) r.type = UT_TOPK;
+  else if (r.K > 0 && r.K <= kTopkSmall && max_nca(V) * kList <= kMaxListCand) r.type = UT_TOPK;
   else if (r.K == 0 && r.P >= 1.0f) r.type = UT_DENSE;
   else r.type = UT_GENERAL;
   return r;

@@ -162,15 +162,17 @@ def test_empty_batch_and_workspace_left_clean():
     for _ in range(3):
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
-    # the counters (256-byte header), the per-row tickets and the two
-    # per-unit arrays (B-item tickets and state-ready flags; each array
-    # padded to 256 bytes) are back at zero
-    B, U = 5, 5 * 4
-    zero_prefix = 256 + 256 * ((B * 4 + 255) // 256) + 2 * 256 * ((U * 4 + 255) // 256)
-    assert int(ws[:zero_prefix].count_nonzero()) == 0
-    # dirty records behind them do not matter: results stay identical
+    # the header's counters (unit counter, exit counter, error bits) and the
+    # per-row tickets (padded to 256 bytes) are back at zero; the epoch word
+    # at the end of the header counts the calls
+    B = 5
+    assert int(ws[:12].count_nonzero()) == 0
+    assert int(ws[256:256 + 256 * ((B * 4 + 255) // 256)].count_nonzero()) == 0
+    assert int(ws[236:240].view(torch.int32).item()) == 3
+    # dirty records behind them do not matter: every record word carries the
+    # call's epoch, so results stay identical
     ref = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
-    ws[zero_prefix:].fill_(0xAB)
+    ws[256 + 256 * ((B * 4 + 255) // 256):].fill_(0xAB)
     again = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(ref.tokens, again.tokens) and torch.equal(ref.logprobs, again.logprobs)
