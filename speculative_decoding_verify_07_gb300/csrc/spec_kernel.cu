@@ -7,8 +7,8 @@
 //   * Stream warps.  Each owns two 6 KB shared-memory buffers and has the
 //     copy engine stream its next item into one (cp.async.bulk completed on
 //     an mbarrier) while it reduces the other with warp collectives.  The
-//     items of all units form one sequence, dealt round robin over the
-//     stream warps of all SMs:
+//     items of all units form one sequence, which the stream warps of all
+//     SMs take in order from one counter:
 //       A items of drafted unfiltered units, of small top-k units, of
 //       unfiltered bonus positions; B items of drafted unfiltered units; A
 //       items of greedy units.
@@ -391,6 +391,11 @@ __device__ __forceinline__ float a_block_max(const unsigned char* buf, int b, in
 }
 
 // Greedy and unfiltered A item: the tagged record words (lanes 0..7).
+// Greedy units and drafted positions take one pass: every lane keeps its
+// running max and its softmax sum relative to it (rescaled when the max
+// rises), and the lanes' sums are rescaled to the chunk max at the end.  A
+// bonus position needs the blocks' sums relative to the chunk max, so it
+// takes the max first.
 template <bool kBF16>
 __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg,
                                      const unsigned char* buf) {
@@ -398,53 +403,56 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EA;
-  // the lane's max and the first of its blocks reaching it
-  float lm = -INFINITY;
-  int bb = 0;
-#pragma unroll 2
-  for (int b = 0; b < nb; ++b) {
-    const float g = a_block_max<kBF16>(buf, b, lane);
-    bb = g > lm ? b : bb;
-    lm = max_nan(lm, g);
-  }
-  const bool nan = __any_sync(kFull, lm != lm);
-  const float mc = warp_max_f(lm);
+  const float c = cfg.c;
+  const u64 c2 = pack2(c, c);
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && it.pos == A.k;
-  uint32_t idx = 0xffffffffu;
-  if (greedy && !nan) {
-    if (lm == mc) {
-      float v[8];
-      a_vals<kBF16>(buf, bb, lane, v);
-#pragma unroll
-      for (int j = 7; j >= 0; --j)
-        if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(bb, lane, j));
-    }
-    idx = warp_min_u32(idx);
-  }
+  float lm = -INFINITY;     // running max of the lane (NaN aside)
+  int lb = 0;               // first block reaching it
+  bool nanl = false;
   float z = 0.f;
   Race r;
   race_init(r);
-  const bool live = !nan && mc > -INFINITY && mc < INFINITY;
-  if (live) {
-    const u64 m2 = pack2(mc, mc), c2 = pack2(cfg.c, cfg.c);
-    if (!bonus) {
-      u64 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+  float mc;
+  if (!bonus) {
+    u64 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+    u64 m2 = pack2(0.f, 0.f);
 #pragma unroll 2
-      for (int b = 0; b < nb; ++b) {
-        float v[8];
-        a_vals<kBF16>(buf, b, lane, v);
-        acc0 = add2(acc0, exp_pair(v[0], v[1], m2, c2));
-        acc1 = add2(acc1, exp_pair(v[2], v[3], m2, c2));
-        acc0 = add2(acc0, exp_pair(v[4], v[5], m2, c2));
-        acc1 = add2(acc1, exp_pair(v[6], v[7], m2, c2));
+    for (int b = 0; b < nb; ++b) {
+      const float bm = a_block_max<kBF16>(buf, b, lane);
+      nanl |= bm != bm;
+      if (bm > lm) {
+        if (lm > -INFINITY) {
+          const float sc = ex2((lm - bm) * c);
+          const u64 s2 = pack2(sc, sc);
+          acc0 = mul2(acc0, s2);
+          acc1 = mul2(acc1, s2);
+        }
+        lm = bm;
+        lb = b;
+        m2 = pack2(lm, lm);
       }
-      float a0, a1, a2, a3;
-      unpack2(acc0, a0, a1);
-      unpack2(acc1, a2, a3);
-      z = warp_sum((a0 + a2) + (a1 + a3));
-    } else {
+      float v[8];
+      a_vals<kBF16>(buf, b, lane, v);
+      acc0 = add2(acc0, exp_pair(v[0], v[1], m2, c2));
+      acc1 = add2(acc1, exp_pair(v[2], v[3], m2, c2));
+      acc0 = add2(acc0, exp_pair(v[4], v[5], m2, c2));
+      acc1 = add2(acc1, exp_pair(v[6], v[7], m2, c2));
+    }
+    mc = warp_max_f(lm);
+    float a0, a1, a2, a3;
+    unpack2(acc0, a0, a1);
+    unpack2(acc1, a2, a3);
+    const float zl = (a0 + a2) + (a1 + a3);
+    z = warp_sum(lm > -INFINITY ? zl * ex2((lm - mc) * c) : 0.f);
+  } else {
+#pragma unroll 2
+    for (int b = 0; b < nb; ++b) lm = max_nan(lm, a_block_max<kBF16>(buf, b, lane));
+    nanl = lm != lm;
+    mc = warp_max_f(lm);
+    if (mc > -INFINITY && mc < INFINITY) {
       // block weights (one warp sum per block), then the level-1 race
+      const u64 m2 = pack2(mc, mc);
       float myW = 0.f;
 #pragma unroll 1
       for (int b = 0; b < nb; ++b) {
@@ -465,6 +473,19 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
       warp_race_merge(r);
     }
   }
+  const bool nan = __any_sync(kFull, nanl);
+  uint32_t idx = 0xffffffffu;
+  if (greedy && !nan) {
+    // first index of the chunk max: in the lane's first block reaching it
+    if (lm == mc) {
+      float v[8];
+      a_vals<kBF16>(buf, lb, lane, v);
+#pragma unroll
+      for (int j = 7; j >= 0; --j)
+        if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(lb, lane, j));
+    }
+    idx = warp_min_u32(idx);
+  }
   u64* rec = A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords;
   uint32_t v = 0;
   switch (lane) {
@@ -482,10 +503,37 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   __syncwarp();
 }
 
+// Stages every finite entry >= t8 of the item (up to kStage; returns the
+// count of all), block by block.
+template <bool kBF16>
+__device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int lane, float t8, u64* stage) {
+  uint32_t n = 0;
+#pragma unroll 1
+  for (int b = 0; b < nb; ++b) {
+    float v[8];
+    a_vals<kBF16>(buf, b, lane, v);
+    uint32_t keep = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) keep |= (v[j] >= t8 && v[j] > -INFINITY) ? (1u << j) : 0u;
+    uint32_t tot = 0;
+    uint32_t p = n + warp_excl_scan((uint32_t)__popc(keep), &tot);
+    n += tot;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if ((keep >> j) & 1u) {
+        if (p < (uint32_t)kStage) stage[p] = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
+        ++p;
+      }
+  }
+  return n;
+}
+
 // Small top-k A item: the chunk's first kList entries in the total order
 // (key, chunk-local index), tagged words in lanes 0..15.  Every such entry is
-// at least the 8th largest lane maximum t8, so only the entries >= t8 (in
-// blocks whose lane maximum reaches it) are staged and sorted.
+// at least the 8th largest lane maximum t8; a lane keeps up to kLaneCand of
+// its entries >= t8 (blocks whose maximum is below t8 are skipped), and a
+// lane holding more marks the list partial.
+constexpr int kLaneCand = 4;
 template <bool kBF16>
 __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it, const unsigned char* buf,
                                     u64* stage) {
@@ -510,36 +558,35 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
       }
     }
     const float t8 = __shfl_sync(kFull, x, kList - 1);
-    const uint32_t T = max(okey(t8), okey(-INFINITY) + 1u);   // finite entries >= t8
-    // count the lane's entries >= T (only lanes whose max reaches T have
-    // any), one scan for the offsets, then write them
+    // candidates: finite entries >= t8, the lane's first kLaneCand kept
     uint32_t cnt = 0;
-    const bool mine = okey(lm) >= T;
-    if (mine) {
+    u64 k0 = 0ull, k1 = 0ull, k2 = 0ull, k3 = 0ull;
+    if (lm >= t8 && lm > -INFINITY) {
 #pragma unroll 1
       for (int b = 0; b < nb; ++b) {
+        if (!(a_block_max<kBF16>(buf, b, lane) >= t8)) continue;
         float v[8];
         a_vals<kBF16>(buf, b, lane, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cnt += okey(v[j]) >= T ? 1u : 0u;
+        for (int j = 0; j < 8; ++j)
+          if (v[j] >= t8 && v[j] > -INFINITY) {
+            k3 = k2;
+            k2 = k1;
+            k1 = k0;
+            k0 = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
+            ++cnt;
+          }
       }
     }
     uint32_t n = 0;
-    uint32_t p = warp_excl_scan(cnt, &n);
-    if (mine) {
-#pragma unroll 1
-      for (int b = 0; b < nb && p < (uint32_t)kStage; ++b) {
-        float v[8];
-        a_vals<kBF16>(buf, b, lane, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t key = okey(v[j]);
-          if (key >= T) {
-            if (p < (uint32_t)kStage) stage[p] = key64(key, (uint32_t)a_entry<kBF16>(b, lane, j));
-            ++p;
-          }
-        }
-      }
+    if (!__any_sync(kFull, cnt > (uint32_t)kLaneCand)) {
+      const uint32_t p = warp_excl_scan(cnt, &n);
+      if (cnt > 0) stage[p] = k0;
+      if (cnt > 1) stage[p + 1] = k1;
+      if (cnt > 2) stage[p + 2] = k2;
+      if (cnt > 3) stage[p + 3] = k3;
+    } else {
+      n = stage_all<kBF16>(buf, nb, lane, t8, stage);   // a lane holds more: every entry >= t8
     }
     __syncwarp();
     if (n > (uint32_t)kStage) flags |= kListPartial;
@@ -617,6 +664,7 @@ __device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it,
   const float m = st.m, invZ = st.invZ, c = cfg.c;
   if (!need_race) {
     // accepted draft: alpha only
+    const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
     float a0 = 0.f, a1 = 0.f;
     for (int b = 0; b < nb; ++b) {
       float v[8], q[8];
@@ -624,33 +672,38 @@ __device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it,
       sload_q(qb, b, lane, q);
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        a0 += fminf(ex2((v[j] - m) * c) * invZ, q[j]);
-        a1 += fminf(ex2((v[j + 1] - m) * c) * invZ, q[j + 1]);
+        float p0, p1;
+        unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);
+        a0 += fminf(p0, q[j]);
+        a1 += fminf(p1, q[j + 1]);
       }
     }
     alpha_c = warp_sum(a0 + a1);
   }
-  for (int b = 0; need_race && b < nb; ++b) {
-    float v[8], q[8];
-    sload<kBF16>(buf, b, lane, v);
-    sload_q(qb, b, lane, q);
-    float a8 = 0.f, w8 = 0.f, u8 = 0.f;
+  if (need_race) {
+    const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
+    float a8 = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      float v[8], q[8];
+      sload<kBF16>(buf, b, lane, v);
+      sload_q(qb, b, lane, q);
+      float w8 = 0.f, u8 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p = ex2((v[j] - m) * c) * invZ;   // padding: -inf -> 0
-      a8 += fminf(p, q[j]);
-      const float w = p - q[j];
-      if (w > 0.f) {
-        w8 += w;
-        u8 += p + q[j];
+      for (int j = 0; j < 8; j += 2) {
+        float p0, p1;
+        unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
+        a8 += fminf(p0, q[j]) + fminf(p1, q[j + 1]);
+        const float w0 = p0 - q[j], w1 = p1 - q[j + 1];
+        w8 += fmaxf(w0, 0.f) + fmaxf(w1, 0.f);
+        u8 += (w0 > 0.f ? p0 + q[j] : 0.f) + (w1 > 0.f ? p1 + q[j + 1] : 0.f);
+      }
+      const float Wb = warp_sum(w8), Ub = warp_sum(u8);
+      if (lane == b) {
+        myW = Wb;
+        myU = Ub;
       }
     }
-    alpha_c += warp_sum(a8);
-    const float Wb = warp_sum(w8), Ub = warp_sum(u8);
-    if (lane == b) {
-      myW = Wb;
-      myU = Ub;
-    }
+    alpha_c = warp_sum(a8);
   }
   Race r;
   race_init(r);
@@ -697,12 +750,12 @@ struct Bufs {
 };
 
 
-// A stream warp: items t0, t0 + nws, ... of the sequence.
+// A stream warp: items of the sequence, taken in order from a shared counter.
 template <bool kBF16>
-__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w, uint32_t t,
-                                    uint32_t nws) {
+__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
+  uint32_t t = 0;
   Bufs B;
   B.a = S.buf[w][0];
   B.b = S.buf[w][1];
@@ -716,14 +769,19 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
     fence_mbar_init();
   }
   __syncwarp();
+  // items are taken from one counter, two at first, then one per item
+  // processed (the ticket is in flight while the item is reduced)
+  if (lane == 0) t = atomicAdd(&A.ws->next_item, 2u);
+  t = __shfl_sync(kFull, t, 0);
   Item ia = map_item<kBF16>(A, P, t);
-  Item ib = map_item<kBF16>(A, P, t + nws);
-  t += 2 * nws;
+  Item ib = map_item<kBF16>(A, P, t + 1);
   if (lane == 0) {
     issue<kBF16>(A, ia, B.a, B.ba);
     issue<kBF16>(A, ib, B.b, B.bb);
   }
   while (ia.kind != 0) {
+    uint32_t tn = 0;
+    if (lane == 0 && ib.kind != 0) tn = atomicAdd(&A.ws->next_item, 1u);
     const RowCfg cfg = plan_cfg(A, P, ia.row);
     u64 sw[kStateWords];
     if (ia.kind == 2) state_load(A, ia.u, sw);     // in flight during the copy wait
@@ -748,8 +806,10 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
       if (!st.invalid) b_item<kBF16>(A, tag, ia, cfg, st, B.a);
     }
     __syncwarp();
-    const Item in = map_item<kBF16>(A, P, t);
-    t += nws;
+    tn = __shfl_sync(kFull, tn, 0);
+    Item in;
+    in.kind = 0;
+    if (ib.kind != 0) in = map_item<kBF16>(A, P, tn);
     if (lane == 0) issue<kBF16>(A, in, B.a, B.ba);
     ia = ib;
     ib = in;
@@ -882,7 +942,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
   if (g < nsw) {
     settle<kBF16>(A, P, S, tag, w, g, nsw, nS);
   } else {
-    stream<kBF16>(A, P, S, tag, w, g - nsw, nw - nsw);
+    stream<kBF16>(A, P, S, tag, w);
   }
   if (P.nX > 0) {
     __syncthreads();
@@ -894,6 +954,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
     const uint32_t d = atomicAdd(&A.ws->ctas_done, 1u);
     if (d == (uint32_t)A.n_ctas - 1u) {
       A.ws->gnext = 0u;
+      A.ws->next_item = 0u;
       A.ws->ctas_done = 0u;
       A.ws->epoch = tag;
       __threadfence();

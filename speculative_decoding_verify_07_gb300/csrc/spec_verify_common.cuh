@@ -48,7 +48,8 @@ struct WsHeader {
   uint32_t ctas_done;     // CTAs that left the kernel
   uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait; bit 2: a record wait; bit 3: the order wait
   uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
-  uint32_t pad0[4];
+  uint32_t next_item;     // next item of the stream sequence
+  uint32_t pad0[3];
   uint32_t n_class[4];    // rows per class (large batches)
   uint32_t pad[47];
   uint32_t epoch;         // tag of the last completed call (records of this call carry epoch + 1)

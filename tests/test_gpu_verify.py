@@ -162,11 +162,11 @@ def test_empty_batch_and_workspace_left_clean():
     for _ in range(3):
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
-    # the header's counters (unit counter, exit counter, error bits) and the
-    # per-row tickets (padded to 256 bytes) are back at zero; the epoch word
-    # at the end of the header counts the calls
+    # the header's counters (unit counter, exit counter, error bits, item
+    # counter) and the per-row tickets (padded to 256 bytes) are back at
+    # zero; the epoch word at the end of the header counts the calls
     B = 5
-    assert int(ws[:12].count_nonzero()) == 0
+    assert int(ws[:12].count_nonzero()) == 0 and int(ws[16:20].count_nonzero()) == 0
     assert int(ws[256:256 + 256 * ((B * 4 + 255) // 256)].count_nonzero()) == 0
     assert int(ws[236:240].view(torch.int32).item()) == 3
     # dirty records behind them do not matter: every record word carries the
