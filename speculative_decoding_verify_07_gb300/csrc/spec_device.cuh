@@ -238,28 +238,31 @@ __device__ __forceinline__ void race_init(Race& r) {
 // Score s = w / E with E = -ln U.  Because E >= 1 - U, an entry with
 // w < s1 * (1 - 2^-20) * (1 - U) cannot beat the current best and needs no
 // logarithm; the factor (1 - 2^-20) absorbs the rounding of the test itself.
-static __device__ __noinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
-  const float om = one_minus_uniform_of(word);
-  if (w >= r.s1lo * om) {
-    const float E = -log1pf(-om);
-    const float s = w / E;
-    const float t = (w + tq) / E;
-    if (s > r.s1 || (s == r.s1 && v < r.v1)) {
-      if (v != r.v1) {
-        r.s2 = r.s1;
-        r.t2 = r.t1;
-      }
-      r.s1 = s;
-      r.t1 = t;
-      r.v1 = v;
-      r.s1lo = s * 0.99999905f;
-    } else if (v != r.v1 && s > r.s2) {
-      r.s2 = s;
-      r.t2 = t;
+static __device__ __noinline__ Race race_update(Race r, float w, float tq, uint32_t v, float om) {
+  const float E = -log1pf(-om);
+  const float s = w / E;
+  const float t = (w + tq) / E;
+  if (s > r.s1 || (s == r.s1 && v < r.v1)) {
+    if (v != r.v1) {
+      r.s2 = r.s1;
+      r.t2 = r.t1;
     }
+    r.s1 = s;
+    r.t1 = t;
+    r.v1 = v;
+    r.s1lo = s * 0.99999905f;
+  } else if (v != r.v1 && s > r.s2) {
+    r.s2 = s;
+    r.t2 = t;
   }
+  return r;
 }
-
+// The cheap bound test inline, the logarithm out of line (the state stays
+// in registers either way).
+__device__ __forceinline__ void race_consider(Race& r, float w, float tq, uint32_t v, uint32_t word) {
+  const float om = one_minus_uniform_of(word);
+  if (w >= r.s1lo * om) r = race_update(r, w, tq, v, om);
+}
 __device__ __forceinline__ void race_merge(Race& a, const Race& b) {
   if (b.v1 == a.v1) {
     if (b.s2 > a.s2) { a.s2 = b.s2; a.t2 = b.t2; }
@@ -290,7 +293,7 @@ __device__ __forceinline__ Race race_shfl(const Race& r, int src_lane_xor) {
 
 // Deterministic warp merge: lane pairs combine in a fixed xor tree, and the
 // merge itself is order-insensitive for the winner (max score, then min index).
-static __device__ __noinline__ void warp_race_merge(Race& r) {
+static __device__ __noinline__ Race warp_race_merged(Race r) {
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     Race other = race_shfl(r, o);
@@ -303,6 +306,8 @@ static __device__ __noinline__ void warp_race_merge(Race& r) {
       race_merge(r, mine);
     }
   }
+  return r;
 }
+__device__ __forceinline__ void warp_race_merge(Race& r) { r = warp_race_merged(r); }
 
 }  // namespace specv

@@ -390,12 +390,10 @@ __device__ __forceinline__ float a_block_max(const unsigned char* buf, int b, in
   }
 }
 
-// Greedy and unfiltered A item: the tagged record words (lanes 0..7).
-// Greedy units and drafted positions take one pass: every lane keeps its
-// running max and its softmax sum relative to it (rescaled when the max
-// rises), and the lanes' sums are rescaled to the chunk max at the end.  A
-// bonus position needs the blocks' sums relative to the chunk max, so it
-// takes the max first.
+// Greedy and unfiltered A item: the tagged record words (lanes 0..7).  The
+// max first (the lane's max and the first block reaching it, for the
+// argmax), then the softmax sum relative to it -- at a bonus position per
+// block of 256, for the level-1 race.
 template <bool kBF16>
 __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg,
                                      const unsigned char* buf) {
@@ -404,65 +402,48 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EA;
   const float c = cfg.c;
-  const u64 c2 = pack2(c, c);
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && it.pos == A.k;
-  float lm = -INFINITY;     // running max of the lane (NaN aside)
-  int lb = 0;               // first block reaching it
-  bool nanl = false;
+  // max pass: the lane's max and the first of its blocks reaching it
+  float lm = -INFINITY;
+  int lb = 0;
+#pragma unroll 2
+  for (int b = 0; b < nb; ++b) {
+    const float bm = a_block_max<kBF16>(buf, b, lane);
+    lb = bm > lm ? b : lb;
+    lm = max_nan(lm, bm);
+  }
+  const bool nanl = lm != lm;
+  const float mc = warp_max_f(lm);
   float z = 0.f;
   Race r;
   race_init(r);
-  float mc;
-  if (!bonus) {
-    u64 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
-    u64 m2 = pack2(0.f, 0.f);
+  if (mc > -INFINITY && mc < INFINITY) {
+    if (!bonus) {
+      // the softmax sum relative to the chunk max
+      float z0 = 0.f, z1 = 0.f;
 #pragma unroll 2
-    for (int b = 0; b < nb; ++b) {
-      const float bm = a_block_max<kBF16>(buf, b, lane);
-      nanl |= bm != bm;
-      if (bm > lm) {
-        if (lm > -INFINITY) {
-          const float sc = ex2((lm - bm) * c);
-          const u64 s2 = pack2(sc, sc);
-          acc0 = mul2(acc0, s2);
-          acc1 = mul2(acc1, s2);
+      for (int b = 0; b < nb; ++b) {
+        float v[8];
+        a_vals<kBF16>(buf, b, lane, v);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          z0 += ex2((v[j] - mc) * c);
+          z1 += ex2((v[j + 1] - mc) * c);
         }
-        lm = bm;
-        lb = b;
-        m2 = pack2(lm, lm);
       }
-      float v[8];
-      a_vals<kBF16>(buf, b, lane, v);
-      acc0 = add2(acc0, exp_pair(v[0], v[1], m2, c2));
-      acc1 = add2(acc1, exp_pair(v[2], v[3], m2, c2));
-      acc0 = add2(acc0, exp_pair(v[4], v[5], m2, c2));
-      acc1 = add2(acc1, exp_pair(v[6], v[7], m2, c2));
-    }
-    mc = warp_max_f(lm);
-    float a0, a1, a2, a3;
-    unpack2(acc0, a0, a1);
-    unpack2(acc1, a2, a3);
-    const float zl = (a0 + a2) + (a1 + a3);
-    z = warp_sum(lm > -INFINITY ? zl * ex2((lm - mc) * c) : 0.f);
-  } else {
-#pragma unroll 2
-    for (int b = 0; b < nb; ++b) lm = max_nan(lm, a_block_max<kBF16>(buf, b, lane));
-    nanl = lm != lm;
-    mc = warp_max_f(lm);
-    if (mc > -INFINITY && mc < INFINITY) {
+      z = warp_sum(z0 + z1);
+    } else {
       // block weights (one warp sum per block), then the level-1 race
-      const u64 m2 = pack2(mc, mc);
       float myW = 0.f;
 #pragma unroll 1
       for (int b = 0; b < nb; ++b) {
         float v[8];
         a_vals<kBF16>(buf, b, lane, v);
-        u64 acc = add2(exp_pair(v[0], v[1], m2, c2), exp_pair(v[2], v[3], m2, c2));
-        acc = add2(acc, add2(exp_pair(v[4], v[5], m2, c2), exp_pair(v[6], v[7], m2, c2)));
-        float s0, s1;
-        unpack2(acc, s0, s1);
-        const float W = warp_sum(s0 + s1);
+        float s8 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s8 += ex2((v[j] - mc) * c);
+        const float W = warp_sum(s8);
         z += W;
         if (lane == b) myW = W;
       }
@@ -537,11 +518,16 @@ constexpr int kLaneCand = 4;
 template <bool kBF16>
 __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it, const unsigned char* buf,
                                     u64* stage) {
+  constexpr int NB = Geo<kBF16>::NBA;
   const int lane = threadIdx.x & 31;
   const int nb = ceil_div(it.n, kRaceBlock);
+  float bm[NB];
   float lm = -INFINITY;
-#pragma unroll 2
-  for (int b = 0; b < nb; ++b) lm = max_nan(lm, a_block_max<kBF16>(buf, b, lane));
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    bm[b] = b < nb ? a_block_max<kBF16>(buf, b, lane) : -INFINITY;
+    lm = max_nan(lm, bm[b]);
+  }
   const bool nan = __any_sync(kFull, lm != lm);
   uint32_t flags = nan ? kListNaN : 0u;
   uint32_t nn = 0;
@@ -558,33 +544,35 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
       }
     }
     const float t8 = __shfl_sync(kFull, x, kList - 1);
-    // candidates: finite entries >= t8, the lane's first kLaneCand kept
+    // the lane's blocks holding finite entries >= t8, then those entries
+    uint32_t hit = 0;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) hit |= (bm[b] >= t8 && bm[b] > -INFINITY) ? (1u << b) : 0u;
     uint32_t cnt = 0;
     u64 k0 = 0ull, k1 = 0ull, k2 = 0ull, k3 = 0ull;
-    if (lm >= t8 && lm > -INFINITY) {
 #pragma unroll 1
-      for (int b = 0; b < nb; ++b) {
-        if (!(a_block_max<kBF16>(buf, b, lane) >= t8)) continue;
-        float v[8];
-        a_vals<kBF16>(buf, b, lane, v);
+    while (hit) {
+      const int b = __ffs(hit) - 1;
+      hit &= hit - 1u;
+      float v[8];
+      a_vals<kBF16>(buf, b, lane, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (v[j] >= t8 && v[j] > -INFINITY) {
-            k3 = k2;
-            k2 = k1;
-            k1 = k0;
-            k0 = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
-            ++cnt;
-          }
-      }
+      for (int j = 0; j < 8; ++j)
+        if (v[j] >= t8 && v[j] > -INFINITY) {
+          k3 = k2;
+          k2 = k1;
+          k1 = k0;
+          k0 = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
+          ++cnt;
+        }
     }
     uint32_t n = 0;
     if (!__any_sync(kFull, cnt > (uint32_t)kLaneCand)) {
       const uint32_t p = warp_excl_scan(cnt, &n);
-      if (cnt > 0) stage[p] = k0;
-      if (cnt > 1) stage[p + 1] = k1;
-      if (cnt > 2) stage[p + 2] = k2;
-      if (cnt > 3) stage[p + 3] = k3;
+      if (cnt > 0 && p < (uint32_t)kStage) stage[p] = k0;
+      if (cnt > 1 && p + 1 < (uint32_t)kStage) stage[p + 1] = k1;
+      if (cnt > 2 && p + 2 < (uint32_t)kStage) stage[p + 2] = k2;
+      if (cnt > 3 && p + 3 < (uint32_t)kStage) stage[p + 3] = k3;
     } else {
       n = stage_all<kBF16>(buf, nb, lane, t8, stage);   // a lane holds more: every entry >= t8
     }
@@ -752,10 +740,10 @@ struct Bufs {
 
 // A stream warp: items of the sequence, taken in order from a shared counter.
 template <bool kBF16>
-__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w) {
+__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w, uint32_t gs,
+                                    uint32_t nws) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
-  uint32_t t = 0;
   Bufs B;
   B.a = S.buf[w][0];
   B.b = S.buf[w][1];
@@ -769,19 +757,18 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
     fence_mbar_init();
   }
   __syncwarp();
-  // items are taken from one counter, two at first, then one per item
-  // processed (the ticket is in flight while the item is reduced)
-  if (lane == 0) t = atomicAdd(&A.ws->next_item, 2u);
-  t = __shfl_sync(kFull, t, 0);
-  Item ia = map_item<kBF16>(A, P, t);
-  Item ib = map_item<kBF16>(A, P, t + 1);
+  // stream warp gs starts on items gs and nws + gs; later items are taken in
+  // order from one counter, one per item processed (the ticket is in flight
+  // while the item is reduced)
+  Item ia = map_item<kBF16>(A, P, gs);
+  Item ib = map_item<kBF16>(A, P, nws + gs);
   if (lane == 0) {
     issue<kBF16>(A, ia, B.a, B.ba);
     issue<kBF16>(A, ib, B.b, B.bb);
   }
   while (ia.kind != 0) {
     uint32_t tn = 0;
-    if (lane == 0 && ib.kind != 0) tn = atomicAdd(&A.ws->next_item, 1u);
+    if (lane == 0 && ib.kind != 0) tn = 2u * nws + atomicAdd(&A.ws->next_item, 1u);
     const RowCfg cfg = plan_cfg(A, P, ia.row);
     u64 sw[kStateWords];
     if (ia.kind == 2) state_load(A, ia.u, sw);     // in flight during the copy wait
@@ -936,13 +923,16 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
   P.sB = (uint32_t)(P.nD * A.k * P.NCB);
   P.sGR = (uint32_t)(P.nG * (A.k + 1) * P.NCA);
   const uint32_t nw = (uint32_t)A.n_ctas * kSW;
-  const uint32_t g = (uint32_t)w * (uint32_t)A.n_ctas + blockIdx.x;   // warps of a round spread over the SMs
+  // settle warps are taken first from the warps on each SM's first
+  // scheduler (w % 4 == 0), one per SM at a time, so the other schedulers
+  // run stream code only
+  const uint32_t g = (uint32_t)(w & 3) * (4u * (uint32_t)A.n_ctas) + (uint32_t)(w >> 2) * (uint32_t)A.n_ctas + blockIdx.x;
   const uint32_t nS = (uint32_t)(2 * P.nD * A.k + P.nT * (A.k + 1) + P.nD + P.nG * (A.k + 1));
   const uint32_t nsw = min(nS, nw / 4u);
   if (g < nsw) {
     settle<kBF16>(A, P, S, tag, w, g, nsw, nS);
   } else {
-    stream<kBF16>(A, P, S, tag, w);
+    stream<kBF16>(A, P, S, tag, w, g - nsw, nw - nsw);
   }
   if (P.nX > 0) {
     __syncthreads();
