@@ -9,9 +9,9 @@
 //     an mbarrier) while it reduces the other with warp collectives.  The
 //     items of all units form one sequence, which the stream warps of all
 //     SMs take in order from one counter:
-//       A items of drafted unfiltered units, of small top-k units, of
-//       unfiltered bonus positions; B items of drafted unfiltered units; A
-//       items of greedy units.
+//       A items of drafted unfiltered units, of unfiltered bonus positions,
+//       of small top-k units; B items of drafted unfiltered units; A items
+//       of greedy units.
 //     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
 //     max, the softmax sum relative to the chunk max, for greedy units the
 //     first argmax, at a bonus position the level-1 race of the chunk's
@@ -172,8 +172,9 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row
 }
 
 
-// Item t of the sequence [A: drafted unfiltered][A: small top-k][A: bonus
-// positions][B: drafted unfiltered][A: greedy].
+// Item t of the sequence [A: drafted unfiltered][A: bonus positions][A:
+// small top-k][B: drafted unfiltered][A: greedy]: the units whose settle
+// takes longest come first, and the B items end before the greedy items.
 template <bool kBF16>
 __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
@@ -190,19 +191,19 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
     pos = j % k;
     it.reread = 1;
     it.kind = 1;
-  } else if ((s -= P.sDD) < P.sTK) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[P.nD + j / k1];
-    pos = j % k1;
-    it.kind = 1;
-  } else if ((s -= P.sTK) < P.sDB) {
+  } else if ((s -= P.sDD) < P.sDB) {
     j = (int)(s / (uint32_t)P.NCA);
     it.c = (int)s - j * P.NCA;
     row = (int)P.order[j];
     pos = k;
     it.kind = 1;
-  } else if ((s -= P.sDB) < P.sB) {
+  } else if ((s -= P.sDB) < P.sTK) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[P.nD + j / k1];
+    pos = j % k1;
+    it.kind = 1;
+  } else if ((s -= P.sTK) < P.sB) {
     j = (int)(s / (uint32_t)P.NCB);
     it.c = (int)s - j * P.NCB;
     row = (int)P.order[j / k];
@@ -532,18 +533,18 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
   uint32_t flags = nan ? kListNaN : 0u;
   uint32_t nn = 0;
   if (!nan) {
-    // t8: bitonic sort of the lane maxima, descending
-    float x = lm;
+    // t8: take the largest lane maxima (with their multiplicity) until 8
+    uint32_t key = okey(lm), need = (uint32_t)kList, t8k = 0u;
 #pragma unroll 1
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll 1
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const float o = __shfl_xor_sync(kFull, x, stride);
-        const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
-        x = keep_max ? fmaxf(x, o) : fminf(x, o);
-      }
+    for (int i = 0; i < kList; ++i) {
+      const uint32_t mx = __reduce_max_sync(kFull, key);
+      const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
+      t8k = mx;
+      if (c >= need) break;
+      need -= c;
+      key = key == mx ? 0u : key;
     }
-    const float t8 = __shfl_sync(kFull, x, kList - 1);
+    const float t8 = from_okey(t8k);
     // the lane's blocks holding finite entries >= t8, then those entries
     uint32_t hit = 0;
 #pragma unroll
@@ -752,9 +753,8 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
   B.pa = 0u;
   B.pb = 0u;
   if (lane == 0) {
-    mbar_init(B.ba, 1);
+    mbar_init(B.ba, 1);    // issue() orders the inits before the copies (fence.proxy.async)
     mbar_init(B.bb, 1);
-    fence_mbar_init();
   }
   __syncwarp();
   // stream warp gs starts on items gs and nws + gs; later items are taken in
@@ -805,7 +805,7 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
 }
 
 // A settle warp: tasks s0, s0 + nsw, ... in the order [drafted unfiltered:
-// state][small top-k][bonus positions][greedy][drafted unfiltered: B
+// state][bonus positions][small top-k][greedy][drafted unfiltered: B
 // records].  Every task before the last group waits only for A records, so
 // every state the B items wait for is published whatever the task spread.
 template <bool kBF16>
@@ -818,13 +818,13 @@ __device__ __noinline__ void settle(const Args& A, const Plan& P, VShm& S, uint3
     if (s < P.nD * k) {
       row = (int)P.order[s / k];
       pos = s % k;
-    } else if ((s -= P.nD * k) < P.nT * k1) {
-      row = (int)P.order[P.nD + s / k1];
-      pos = s % k1;
-    } else if ((s -= P.nT * k1) < P.nD) {
+    } else if ((s -= P.nD * k) < P.nD) {
       row = (int)P.order[s];
       pos = k;
-    } else if ((s -= P.nD) < P.nG * k1) {
+    } else if ((s -= P.nD) < P.nT * k1) {
+      row = (int)P.order[P.nD + s / k1];
+      pos = s % k1;
+    } else if ((s -= P.nT * k1) < P.nG * k1) {
       row = (int)P.order[P.nD + P.nT + s / k1];
       pos = s % k1;
     } else {
