@@ -280,33 +280,36 @@ __device__ __forceinline__ void race_merge(Race& a, const Race& b) {
   a.s1lo = a.s1 * 0.99999905f;
 }
 
-__device__ __forceinline__ Race race_shfl(const Race& r, int src_lane_xor) {
-  Race o;
-  o.s1 = __shfl_xor_sync(0xffffffffu, r.s1, src_lane_xor);
-  o.t1 = __shfl_xor_sync(0xffffffffu, r.t1, src_lane_xor);
-  o.s2 = __shfl_xor_sync(0xffffffffu, r.s2, src_lane_xor);
-  o.t2 = __shfl_xor_sync(0xffffffffu, r.t2, src_lane_xor);
-  o.v1 = __shfl_xor_sync(0xffffffffu, r.v1, src_lane_xor);
-  o.s1lo = 0.0f;
-  return o;
-}
-
-// Deterministic warp merge: lane pairs combine in a fixed xor tree, and the
-// merge itself is order-insensitive for the winner (max score, then min index).
+// Warp merge by reductions: the winner is the largest score, ties to the
+// smaller entry; the runner-up is the largest of the other entries' best
+// scores and the winning entry's second score (a lane that raced the winning
+// entry too contributes its second).  Scores are positive, so their float
+// bits order like unsigned integers.  Every lane gets the result; it does not
+// depend on the lanes' order (ties of the runner-up go to the lowest lane).
 static __device__ __noinline__ Race warp_race_merged(Race r) {
-#pragma unroll 1
-  for (int o = 1; o < 32; o <<= 1) {
-    Race other = race_shfl(r, o);
-    // keep the lower lane's state first so both lanes compute the same result
-    if ((threadIdx.x & o) == 0) {
-      race_merge(r, other);
-    } else {
-      Race mine = r;
-      r = other;
-      race_merge(r, mine);
-    }
+  const unsigned full = 0xffffffffu;
+  const uint32_t sk = r.s1 >= 0.f ? __float_as_uint(r.s1) : 0u;
+  const uint32_t top = __reduce_max_sync(full, sk);
+  Race o;
+  race_init(o);
+  if (top == 0u) return o;
+  const uint32_t vb = __reduce_max_sync(full, sk == top ? ~r.v1 : 0u);
+  o.v1 = ~vb;
+  const int wl = __ffs(__ballot_sync(full, sk == top && r.v1 == o.v1)) - 1;
+  o.s1 = __shfl_sync(full, r.s1, wl);
+  o.t1 = __shfl_sync(full, r.t1, wl);
+  const bool same = r.v1 == o.v1;
+  const float cs = same ? r.s2 : r.s1;
+  const float ct = same ? r.t2 : r.t1;
+  const uint32_t ck = cs >= 0.f ? __float_as_uint(cs) : 0u;
+  const uint32_t sec = __reduce_max_sync(full, ck);
+  if (sec != 0u) {
+    const int sl = __ffs(__ballot_sync(full, ck == sec)) - 1;
+    o.s2 = __shfl_sync(full, cs, sl);
+    o.t2 = __shfl_sync(full, ct, sl);
   }
-  return r;
+  o.s1lo = o.s1 * 0.99999905f;
+  return o;
 }
 __device__ __forceinline__ void warp_race_merge(Race& r) { r = warp_race_merged(r); }
 

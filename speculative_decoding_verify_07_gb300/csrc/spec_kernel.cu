@@ -9,9 +9,9 @@
 //     an mbarrier) while it reduces the other with warp collectives.  The
 //     items of all units form one sequence, which the stream warps of all
 //     SMs take in order from one counter:
-//       A items of drafted unfiltered units, of unfiltered bonus positions,
-//       of small top-k units; B items of drafted unfiltered units; A items
-//       of greedy units.
+//       A items of small top-k units, of drafted unfiltered units, of
+//       unfiltered bonus positions; B items of drafted unfiltered units; A
+//       items of greedy units.
 //     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
 //     max, the softmax sum relative to the chunk max, for greedy units the
 //     first argmax, at a bonus position the level-1 race of the chunk's
@@ -172,9 +172,9 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row
 }
 
 
-// Item t of the sequence [A: drafted unfiltered][A: bonus positions][A:
-// small top-k][B: drafted unfiltered][A: greedy]: the units whose settle
-// takes longest come first, and the B items end before the greedy items.
+// Item t of the sequence [A: small top-k][A: drafted unfiltered][A: bonus
+// positions][B: drafted unfiltered][A: greedy]: the units whose settle takes
+// longest come first, and the B items end before the greedy items.
 template <bool kBF16>
 __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
@@ -184,7 +184,13 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
   int row, pos, j;
   uint32_t s = t;
   it.reread = 0;
-  if (s < P.sDD) {
+  if (s < P.sTK) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[P.nD + j / k1];
+    pos = j % k1;
+    it.kind = 1;
+  } else if ((s -= P.sTK) < P.sDD) {
     j = (int)(s / (uint32_t)P.NCA);
     it.c = (int)s - j * P.NCA;
     row = (int)P.order[j / k];
@@ -197,13 +203,7 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
     row = (int)P.order[j];
     pos = k;
     it.kind = 1;
-  } else if ((s -= P.sDB) < P.sTK) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[P.nD + j / k1];
-    pos = j % k1;
-    it.kind = 1;
-  } else if ((s -= P.sTK) < P.sB) {
+  } else if ((s -= P.sDB) < P.sB) {
     j = (int)(s / (uint32_t)P.NCB);
     it.c = (int)s - j * P.NCB;
     row = (int)P.order[j / k];
@@ -804,8 +804,8 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
   }
 }
 
-// A settle warp: tasks s0, s0 + nsw, ... in the order [drafted unfiltered:
-// state][bonus positions][small top-k][greedy][drafted unfiltered: B
+// A settle warp: tasks s0, s0 + nsw, ... in the order [small top-k]
+// [drafted unfiltered: state][bonus positions][greedy][drafted unfiltered: B
 // records].  Every task before the last group waits only for A records, so
 // every state the B items wait for is published whatever the task spread.
 template <bool kBF16>
@@ -815,16 +815,16 @@ __device__ __noinline__ void settle(const Args& A, const Plan& P, VShm& S, uint3
   for (uint32_t t = s0; t < nS; t += nsw) {
     int s = (int)t, row, pos;
     bool finish = false;
-    if (s < P.nD * k) {
+    if (s < P.nT * k1) {
+      row = (int)P.order[P.nD + s / k1];
+      pos = s % k1;
+    } else if ((s -= P.nT * k1) < P.nD * k) {
       row = (int)P.order[s / k];
       pos = s % k;
     } else if ((s -= P.nD * k) < P.nD) {
       row = (int)P.order[s];
       pos = k;
-    } else if ((s -= P.nD) < P.nT * k1) {
-      row = (int)P.order[P.nD + s / k1];
-      pos = s % k1;
-    } else if ((s -= P.nT * k1) < P.nG * k1) {
+    } else if ((s -= P.nD) < P.nG * k1) {
       row = (int)P.order[P.nD + P.nT + s / k1];
       pos = s % k1;
     } else {
