@@ -173,8 +173,9 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row
 
 
 // Item t of the sequence [A: small top-k][A: drafted unfiltered][A: bonus
-// positions][B: drafted unfiltered][A: greedy]: the units whose settle takes
-// longest come first, and the B items end before the greedy items.
+// positions][A: greedy][B: drafted unfiltered]: the units whose settle takes
+// longest come first, and the greedy items run while the states that the B
+// items need are published.
 template <bool kBF16>
 __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
@@ -203,18 +204,18 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
     row = (int)P.order[j];
     pos = k;
     it.kind = 1;
-  } else if ((s -= P.sDB) < P.sB) {
-    j = (int)(s / (uint32_t)P.NCB);
-    it.c = (int)s - j * P.NCB;
-    row = (int)P.order[j / k];
-    pos = j % k;
-    it.kind = 2;
-  } else if ((s -= P.sB) < P.sGR) {
+  } else if ((s -= P.sDB) < P.sGR) {
     j = (int)(s / (uint32_t)P.NCA);
     it.c = (int)s - j * P.NCA;
     row = (int)P.order[P.nD + P.nT + j / k1];
     pos = j % k1;
     it.kind = 1;
+  } else if ((s -= P.sGR) < P.sB) {
+    j = (int)(s / (uint32_t)P.NCB);
+    it.c = (int)s - j * P.NCB;
+    row = (int)P.order[j / k];
+    pos = j % k;
+    it.kind = 2;
   } else {
     return it;
   }

@@ -26,6 +26,10 @@
 namespace specv {
 
 constexpr unsigned kSettleFull = 0xffffffffu;
+// Record chunks a lane loads before merging any of them: A records in
+// fin_stats, B records in fin_b (one batch each at V = 151936).
+constexpr int kFinBatchA = 2;
+constexpr int kFinBatchB = 5;
 
 // Bounded wait, by lane 0, until *p carries `tag`; every lane returns the
 // outcome.
@@ -204,25 +208,47 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       m = -INFINITY;
       zl = 0.f;
       cm = 0x7fffffff;
-      for (int c = lane; c < NC; c += 32) {
-        const u64* r = R + (size_t)c * kRecWords;
-        const u64 w0 = __ldcg(r), w2 = __ldcg(r + 2);
-        ok = ok && tag_ok(w0, tag) && tag_ok(w2, tag);
-        if (greedy) ok = ok && tag_ok(__ldcg(r + 1), tag);
-        if (bonus) {
+      for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
+        // words 0..7 of the batch's chunks, all in flight before use (word 1
+        // only for greedy units, words 3..7 only for bonus positions)
+        u64 w[kFinBatchA][8];
 #pragma unroll
-          for (int i = 3; i < 8; ++i) ok = ok && tag_ok(__ldcg(r + i), tag);
+        for (int i = 0; i < kFinBatchA; ++i) {
+          const int c = c0 + 32 * i + lane;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[i][j] = 0ull;
+          if (c < NC) {
+            const u64* r = R + (size_t)c * kRecWords;
+            w[i][0] = __ldcg(r);
+            w[i][2] = __ldcg(r + 2);
+            if (greedy) w[i][1] = __ldcg(r + 1);
+            if (bonus) {
+#pragma unroll
+              for (int j = 3; j < 8; ++j) w[i][j] = __ldcg(r + j);
+            }
+          }
         }
-        const float mc = wf(w0), zc = wf(w2);
-        if (mc != mc) {
-          nan = true;
-        } else if (mc > -INFINITY) {
-          if (mc > m) {
-            zl = (m > -INFINITY ? zl * ex2((m - mc) * cfg.c) : 0.f) + zc;
-            m = mc;
-            cm = c;
-          } else {
-            zl += zc * ex2((mc - m) * cfg.c);
+#pragma unroll
+        for (int i = 0; i < kFinBatchA; ++i) {
+          const int c = c0 + 32 * i + lane;
+          if (c >= NC) continue;
+          ok = ok && tag_ok(w[i][0], tag) && tag_ok(w[i][2], tag);
+          if (greedy) ok = ok && tag_ok(w[i][1], tag);
+          if (bonus) {
+#pragma unroll
+            for (int j = 3; j < 8; ++j) ok = ok && tag_ok(w[i][j], tag);
+          }
+          const float mc = wf(w[i][0]), zc = wf(w[i][2]);
+          if (mc != mc) {
+            nan = true;
+          } else if (mc > -INFINITY) {
+            if (mc > m) {
+              zl = (m > -INFINITY ? zl * ex2((m - mc) * cfg.c) : 0.f) + zc;
+              m = mc;
+              cm = c;
+            } else {
+              zl += zc * ex2((mc - m) * cfg.c);
+            }
           }
         }
       }
@@ -280,19 +306,35 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
     // entries of the winning block
     Race a;
     race_init(a);
-    for (int c = lane; c < NC; c += 32) {
-      const u64* r = R + (size_t)c * kRecWords;
-      const float mc = wf(__ldcg(r));
-      const float sc = mc > -INFINITY ? ex2((mc - m) * cfg.c) : 0.f;
-      Race b;
-      b.s1 = wf(__ldcg(r + 3));
-      b.t1 = wf(__ldcg(r + 4));
-      b.s2 = wf(__ldcg(r + 5));
-      b.t2 = wf(__ldcg(r + 6));
-      b.v1 = wu(__ldcg(r + 7));
-      b.s1lo = 0.f;
-      race_scale(b, sc);
-      race_merge(a, b);
+    for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
+      u64 w[kFinBatchA][6];   // words 0 and 3..7 of the batch's chunks
+#pragma unroll
+      for (int i = 0; i < kFinBatchA; ++i) {
+        const int c = c0 + 32 * i + lane;
+#pragma unroll
+        for (int j = 0; j < 6; ++j) w[i][j] = 0ull;
+        if (c < NC) {
+          const u64* r = R + (size_t)c * kRecWords;
+          w[i][0] = __ldcg(r);
+#pragma unroll
+          for (int j = 1; j < 6; ++j) w[i][j] = __ldcg(r + 2 + j);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kFinBatchA; ++i) {
+        if (c0 + 32 * i + lane >= NC) continue;
+        const float mc = wf(w[i][0]);
+        const float sc = mc > -INFINITY ? ex2((mc - m) * cfg.c) : 0.f;
+        Race b;
+        b.s1 = wf(w[i][1]);
+        b.t1 = wf(w[i][2]);
+        b.s2 = wf(w[i][3]);
+        b.t2 = wf(w[i][4]);
+        b.v1 = wu(w[i][5]);
+        b.s1lo = 0.f;
+        race_scale(b, sc);
+        race_merge(a, b);
+      }
     }
     warp_race_merge(a);
     const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr);
@@ -345,26 +387,41 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
       ok = true;
       al = 0.f;
       race_init(a);
-      for (int c = lane; c < NC; c += 32) {
-        const u64* r = R + (size_t)c * kBRecWords;
-        const u64 w0 = __ldcg(r);
-        ok = ok && tag_ok(w0, tag);
-        al += wf(w0);
-        if (need_race) {
-          u64 w[5];
+      // each lane's chunks lane, lane + 32, ... in batches of kFinBatchB:
+      // the batch's words are all in flight before the first is merged
+      for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchB) {
+        u64 w[kFinBatchB][6];
 #pragma unroll
-          for (int i = 0; i < 5; ++i) {
-            w[i] = __ldcg(r + 1 + i);
-            ok = ok && tag_ok(w[i], tag);
+        for (int i = 0; i < kFinBatchB; ++i) {
+          const int c = c0 + 32 * i + lane;
+#pragma unroll
+          for (int j = 0; j < 6; ++j) w[i][j] = 0ull;
+          if (c < NC) {
+            const u64* r = R + (size_t)c * kBRecWords;
+            w[i][0] = __ldcg(r);
+            if (need_race) {
+#pragma unroll
+              for (int j = 1; j < 6; ++j) w[i][j] = __ldcg(r + j);
+            }
           }
-          Race rb;
-          rb.s1 = wf(w[0]);
-          rb.t1 = wf(w[1]);
-          rb.s2 = wf(w[2]);
-          rb.t2 = wf(w[3]);
-          rb.v1 = wu(w[4]);
-          rb.s1lo = 0.f;
-          race_merge(a, rb);
+        }
+#pragma unroll
+        for (int i = 0; i < kFinBatchB; ++i) {
+          if (c0 + 32 * i + lane >= NC) continue;
+          ok = ok && tag_ok(w[i][0], tag);
+          al += wf(w[i][0]);
+          if (need_race) {
+#pragma unroll
+            for (int j = 1; j < 6; ++j) ok = ok && tag_ok(w[i][j], tag);
+            Race rb;
+            rb.s1 = wf(w[i][1]);
+            rb.t1 = wf(w[i][2]);
+            rb.s2 = wf(w[i][3]);
+            rb.t2 = wf(w[i][4]);
+            rb.v1 = wu(w[i][5]);
+            rb.s1lo = 0.f;
+            race_merge(a, rb);
+          }
         }
       }
     } while (poll_again(A, ok, spins));
@@ -637,10 +694,22 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     bool ok;
     do {
       ok = true;
-      for (int i = lane; i < NC * kRecWords; i += 32) {
-        const u64 w = __ldcg(R + i);
-        ok = ok && tag_ok(w, tag);
-        raw[i] = wu(w);
+      // 8 words a lane in flight at a time
+      for (int i0 = 0; i0 < NC * kRecWords; i0 += 32 * 8) {
+        u64 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 32 * j + lane;
+          w[j] = i < NC * kRecWords ? __ldcg(R + i) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + 32 * j + lane;
+          if (i < NC * kRecWords) {
+            ok = ok && tag_ok(w[j], tag);
+            raw[i] = wu(w[j]);
+          }
+        }
       }
     } while (poll_again(A, ok, spins));
   }
