@@ -430,7 +430,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   const float m = from_okey((uint32_t)(best >> 32));
   const int am = (int)key64_idx(best);
   if (best == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
-    if (ctid() == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    if (ctid() < 32) commit_record(A, u, row, empty_record(SPEC_F_NAN));
     csync();
     return;
   }
@@ -617,8 +617,8 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
     }
     if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
   }
+  UnitRecord rec = empty_record(flags);
   if (ctid() == 0) {
-    UnitRecord rec = empty_record(flags);
     if (has_q) {
       if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
       if (ai.margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
@@ -632,8 +632,8 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
       rec.lp_y = (load_logit(A, kBF16, lrow + yy) - m) * cfg.invT - lnZ;
       rec.draw_flags = draw_flags;
     }
-    commit_record(A, u, row, rec);
   }
+  if (ctid() < 32) commit_record(A, u, row, rec);
   csync();
 }
 

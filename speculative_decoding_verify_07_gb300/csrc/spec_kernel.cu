@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
   using G = Geo<kBF16>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) S.tag = __ldcg(&A.ws->epoch) + 1u;
   Plan P;
   if (!A.global_order) {

@@ -267,8 +267,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       z.invalid = 1;
       publish_state(A, tag, u, z);
     }
-    if (lane == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
-    __syncwarp();
+    commit_record(A, u, row, empty_record(SPEC_F_NAN));
     return false;
   }
   const float m_lane = m;
@@ -278,8 +277,8 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
   const float lnZ = logf(Z);
   if (greedy) {
     const int am = (int)wu(__ldcg(R + (size_t)cfirst * kRecWords + 1));
+    UnitRecord rec = empty_record(base_flags);
     if (lane == 0) {
-      UnitRecord rec = empty_record(base_flags);
       bool need_draw = !has_q;
       float q_am = 0.f;
       if (has_q) {
@@ -296,9 +295,8 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
         rec.lp_y = -lnZ;
         if (has_q && !(1.0f - q_am > 0.0f)) rec.draw_flags |= SPEC_F_RESIDUAL_EMPTY;
       }
-      commit_record(A, u, row, rec);
     }
-    __syncwarp();
+    commit_record(A, u, row, rec);
     return false;
   }
   if (bonus) {
@@ -337,17 +335,18 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       }
     }
     warp_race_merge(a);
-    const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr);
+    float ly = 0.f;
+    const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
     uint32_t y = l2.v1;
-    if (y >= (uint32_t)A.V) y = (uint32_t)row_argmax<kBF16>(A, lrow);
+    const bool drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
+    if (!drawn) y = (uint32_t)row_argmax<kBF16>(A, lrow);
+    UnitRecord rec = empty_record(base_flags);
     if (lane == 0) {
-      UnitRecord rec = empty_record(base_flags);
       rec.y = (int32_t)y;
-      rec.lp_y = (load_logit(A, kBF16, lrow + y) - m) * cfg.invT - lnZ;
+      rec.lp_y = ((drawn ? ly : load_logit(A, kBF16, lrow + y)) - m) * cfg.invT - lnZ;
       if (draw_margin(a) || draw_margin(l2)) rec.draw_flags |= SPEC_F_MARGIN_DRAW;
-      commit_record(A, u, row, rec);
     }
-    __syncwarp();
+    commit_record(A, u, row, rec);
     return false;
   }
   // drafted: accept test, then publish the state for the B items
@@ -429,11 +428,14 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
   const float alpha_v = warp_sum(al);
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
+  float ly = 0.f;
+  bool drawn = false;   // ly holds the logit of y
   if (need_race) {
     warp_race_merge(a);
     if (a.s1 >= 0.f) {
-      const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr);
+      const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr, &ly);
       y = l2.v1;
+      drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
       if (draw_margin(a) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
     } else {
       draw_flags |= SPEC_F_RESIDUAL_EMPTY;
@@ -443,19 +445,18 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
     }
     if (y >= (uint32_t)A.V) y = (uint32_t)row_argmax<kBF16>(A, (size_t)u * A.V);
   }
+  UnitRecord rec = empty_record(st.flags);
   if (lane == 0) {
-    UnitRecord rec = empty_record(st.flags);
     rec.accept = st.accept;
     rec.lp_x = st.lp_x;
     rec.alpha = alpha_v;
     if (need_race) {
       rec.y = (int32_t)y;
-      rec.lp_y = (load_logit(A, kBF16, (size_t)u * A.V + y) - st.m) * cfg.invT - st.lnZ;
+      rec.lp_y = ((drawn ? ly : load_logit(A, kBF16, (size_t)u * A.V + y)) - st.m) * cfg.invT - st.lnZ;
       rec.draw_flags = draw_flags;
     }
-    commit_record(A, u, row, rec);
   }
-  __syncwarp();
+  commit_record(A, u, row, rec);
 }
 // First bin (from bin 0) where the running count over hist[0..256) reaches
 // `need` (>= 1); 256 when the total is below it.  *before = the count of the
@@ -734,8 +735,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   top = warp_max_u64(top);
   const float m = from_okey((uint32_t)(top >> 32));
   if (nan || top == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
-    if (lane == 0) commit_record(A, u, row, empty_record(SPEC_F_NAN));
-    __syncwarp();
+    commit_record(A, u, row, empty_record(SPEC_F_NAN));
     return;
   }
   const int am = (int)key64_idx(top);
@@ -1018,8 +1018,8 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     const unsigned ob = __ballot_sync(kSettleFull, own);
     if (ob) vy = __shfl_sync(kSettleFull, vv, __ffs(ob) - 1);
   }
+  UnitRecord rec = empty_record(flags);
   if (lane == 0) {
-    UnitRecord rec = empty_record(flags);
     if (has_q) {
       if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
       if (ai.margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
@@ -1033,9 +1033,8 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       rec.lp_y = ((ok ? vy : m) - m) * cfg.invT - lnZ;
       rec.draw_flags = draw_flags;
     }
-    commit_record(A, u, row, rec);
   }
-  __syncwarp();
+  commit_record(A, u, row, rec);
 }
 
 }  // namespace specv

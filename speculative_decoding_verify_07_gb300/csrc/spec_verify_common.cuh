@@ -292,60 +292,77 @@ __device__ __forceinline__ float group_max(const float v[8]) {
 // ---------------------------------------------------------------------------
 // Records and the per-row finalize.
 // ---------------------------------------------------------------------------
+// One warp, lane j reading unit j's record (k + 1 <= 32): the accepted
+// prefix ends at the first rejected draft; its tokens are the drafts, then
+// the draw of the first rejected unit (or the bonus draw).
 static __device__ __noinline__ void finalize_row(const Args& A, int row) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
   const int k = A.k;
-  const UnitRecord* R = A.urec + (size_t)row * (k + 1);
-  uint32_t uflags = 0;
-  bool invalid = false;
-  for (int j = 0; j <= k; ++j) {
-    const uint32_t f = __ldcg(&R[j].flags);
-    uflags |= f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP);
-    invalid |= (f & SPEC_F_NAN) != 0;
+  __syncwarp();   // orders the lanes' reads after lane 0's acquiring ticket
+  uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+  if (lane <= k) {
+    const uint4* r = reinterpret_cast<const uint4*>(A.urec + (size_t)row * (k + 1) + lane);
+    w0 = __ldcg(r);
+    w1 = __ldcg(r + 1);
   }
+  const uint32_t f = w0.x;
+  const bool acc = w0.y != 0u;
+  const float lp_x = __uint_as_float(w0.z), alpha = __uint_as_float(w0.w);
+  const int32_t y = (int32_t)w1.x;
+  const float lp_y = __uint_as_float(w1.y);
+  const uint32_t draw_flags = w1.z;
+  uint32_t uflags = __reduce_or_sync(full, f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP));
   int32_t* tok = A.tokens + (size_t)row * (k + 1);
   float* lp = A.logprobs + (size_t)row * (k + 1);
-  if (invalid) {
-    for (int j = 0; j <= k; ++j) {
-      tok[j] = -1;
-      lp[j] = 0.f;
+  if (uflags & SPEC_F_NAN) {
+    if (lane <= k) {
+      tok[lane] = -1;
+      lp[lane] = 0.f;
     }
-    for (int j = 0; j < k; ++j) A.alpha[(size_t)row * k + j] = 0.f;
-    A.accept_len[row] = 0;
-    A.flags[row] = SPEC_F_NAN;
+    if (lane < k) A.alpha[(size_t)row * k + lane] = 0.f;
+    if (lane == 0) {
+      A.accept_len[row] = 0;
+      A.flags[row] = SPEC_F_NAN;
+    }
     return;
   }
-  int a = k;
-  for (int j = 0; j < k; ++j) {
-    uflags |= __ldcg(&R[j].flags) & SPEC_F_MARGIN_ACCEPT;
-    if (!__ldcg(&R[j].accept)) {
-      a = j;
-      break;
-    }
+  const unsigned rej = __ballot_sync(full, lane < k && !acc);
+  const int a = rej ? __ffs(rej) - 1 : k;
+  uflags |= __reduce_or_sync(full, (lane < k && lane <= a) ? (f & SPEC_F_MARGIN_ACCEPT) : 0u);
+  uflags |= __shfl_sync(full, draw_flags, a);
+  if (lane < a) {
+    tok[lane] = A.drafts[(size_t)row * k + lane];
+    lp[lane] = lp_x;
+  } else if (lane == a) {
+    tok[lane] = y;
+    lp[lane] = lp_y;
+  } else if (lane <= k) {
+    tok[lane] = -1;
+    lp[lane] = 0.f;
   }
-  for (int j = 0; j < a; ++j) {
-    tok[j] = A.drafts[(size_t)row * k + j];
-    lp[j] = __ldcg(&R[j].lp_x);
+  if (lane < k) A.alpha[(size_t)row * k + lane] = alpha;
+  if (lane == 0) {
+    A.accept_len[row] = a + 1;
+    A.flags[row] = uflags;
   }
-  tok[a] = __ldcg(&R[a].y);
-  lp[a] = __ldcg(&R[a].lp_y);
-  uflags |= __ldcg(&R[a].draw_flags);
-  for (int j = a + 1; j <= k; ++j) {
-    tok[j] = -1;
-    lp[j] = 0.f;
-  }
-  for (int j = 0; j < k; ++j) A.alpha[(size_t)row * k + j] = __ldcg(&R[j].alpha);
-  A.accept_len[row] = a + 1;
-  A.flags[row] = uflags;
 }
 
-// One thread: publish a unit's record; the last unit of the row finalizes it.
+// One warp (converged): lane 0 publishes the unit's record (lane 0's `rec`);
+// the warp whose unit is the row's last finalizes the row.
 static __device__ __noinline__ void commit_record(const Args& A, int u, int row, const UnitRecord& rec) {
-  A.urec[u] = rec;
-  const uint32_t old = atomic_add_acq_rel(&A.row_ticket[row], 1u);
+  const int lane = threadIdx.x & 31;
+  uint32_t old = 0u;
+  if (lane == 0) {
+    A.urec[u] = rec;
+    old = atomic_add_acq_rel(&A.row_ticket[row], 1u);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
   if (old == (uint32_t)A.k) {
     finalize_row(A, row);
-    A.row_ticket[row] = 0;   // leave the workspace clean for the next call
+    if (lane == 0) A.row_ticket[row] = 0;   // leave the workspace clean for the next call
   }
+  __syncwarp();
 }
 
 __device__ __forceinline__ UnitRecord empty_record(uint32_t flags) {
@@ -412,23 +429,6 @@ __device__ __forceinline__ uint32_t race_word(const Args& A, int row, int pos, u
   return word_of(w, v & 3);
 }
 
-// Race over the 8 weights of one group (two Philox blocks), skipping empty halves.
-__device__ __forceinline__ void race_group(const Args& A, int row, int pos, int e0, const float w[8],
-                                           const float tq[8], Race& r) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const float* wh = w + 4 * h;
-    if (wh[0] > 0.f || wh[1] > 0.f || wh[2] > 0.f || wh[3] > 0.f) {
-      const uint32_t blk = (uint32_t)((e0 >> 2) + h);
-      const uint4 ww = philox4x32_10(make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
-      if (wh[0] > 0.f) race_consider(r, wh[0], tq[4 * h + 0], blk * 4 + 0, ww.x);
-      if (wh[1] > 0.f) race_consider(r, wh[1], tq[4 * h + 1], blk * 4 + 1, ww.y);
-      if (wh[2] > 0.f) race_consider(r, wh[2], tq[4 * h + 2], blk * 4 + 2, ww.z);
-      if (wh[3] > 0.f) race_consider(r, wh[3], tq[4 * h + 3], blk * 4 + 3, ww.w);
-    }
-  }
-}
-
 __device__ __forceinline__ bool draw_margin(const Race& r) {
   return r.s2 >= 0.f && (r.s1 - r.s2) < kMargin * (r.t1 + r.t2);
 }
@@ -446,21 +446,14 @@ __device__ __forceinline__ uint32_t block_word(const Args& A, int row, int pos, 
 
 enum { RW_BONUS = 0, RW_RESIDUAL = 1, RW_P = 2 };
 
-// Weights of the 8 entries of group g: RW_BONUS / RW_P use exp2((l - m) c)
-// (margin weight: the same), RW_RESIDUAL uses max(p - q, 0) with
-// p = exp2((l - m) c) * invZ (margin weight p + q).  Entries outside the
-// kept set (th) or past V weigh 0.  Returns in w[] and tq[] = margin - w.
-template <bool kBF16>
-__device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t qrow, int g, float m, float c,
-                                             float invZ, int mode, const Thresh* th, float w[8], float tq[8]) {
-  float v[8], qv[8];
-  load_group<kBF16>(A, lrow, g, true, v);
-  if (mode == RW_RESIDUAL) {
-    load_q8(A, qrow, g * 8, qv);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) qv[j] = 0.f;
-  }
+// Weights of the 8 entries of group g from its logits v[] (and q[] for
+// RW_RESIDUAL): RW_BONUS / RW_P use exp2((l - m) c) (margin weight: the
+// same), RW_RESIDUAL uses max(p - q, 0) with p = exp2((l - m) c) * invZ
+// (margin weight p + q).  Entries outside the kept set (th) or past V weigh
+// 0.  Returns in w[] and tq[] = margin - w.
+__device__ __forceinline__ void group_weights(const Args& A, int g, const float v[8], const float qv[8], float m,
+                                              float c, float invZ, int mode, const Thresh* th, float w[8],
+                                              float tq[8]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const bool in = (g * 8 + j < A.V) && (th == nullptr || kept(*th, okey(v[j]), (uint32_t)(g * 8 + j)));
@@ -476,11 +469,27 @@ __device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t 
   }
 }
 
+template <bool kBF16>
+__device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t qrow, int g, float m, float c,
+                                             float invZ, int mode, const Thresh* th, float w[8], float tq[8]) {
+  float v[8], qv[8];
+  load_group<kBF16>(A, lrow, g, true, v);
+  if (mode == RW_RESIDUAL) {
+    load_q8(A, qrow, g * 8, qv);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qv[j] = 0.f;
+  }
+  group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
+}
+
 // Level 2: the race among the entries of block b, run by one warp (the
-// result is in every lane).
+// result is in every lane).  The group's two Philox blocks are computed
+// while its loads are in flight.  *ly (if given) receives the logit of the
+// winning entry.
 template <bool kBF16>
 __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint32_t b, float m, float c, float invZ, int mode,
-                              const Thresh* th) {
+                              const Thresh* th, float* ly = nullptr) {
   const int lane = threadIdx.x & 31;
   const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
@@ -489,12 +498,35 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
   race_init(r);
   if (b >= (uint32_t)((A.V + kRaceBlock - 1) / kRaceBlock)) return r;   // no block won (all weights 0)
   const int g = (int)b * (kRaceBlock / 8) + lane;
+  float v[8], qv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = 0.f;
+    qv[j] = 0.f;
+  }
   if (g < G) {
+    load_group<kBF16>(A, lrow, g, true, v);
+    if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv);
+    const uint32_t blk = (uint32_t)g * 2u;   // Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
+    const uint4 p0 = philox4x32_10(make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
+    const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
     float w[8], tq[8];
-    race_weights<kBF16>(A, lrow, qrow, g, m, c, invZ, mode, th, w, tq);
-    race_group(A, row, pos, g * 8, w, tq, r);
+    group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
+    const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (w[j] > 0.f) race_consider(r, w[j], tq[j], (uint32_t)(g * 8 + j), pw[j]);
   }
   warp_race_merge(r);
+  if (ly != nullptr && r.s1 >= 0.f) {
+    // the winner's lane holds its logit
+    const int src = (int)(r.v1 >> 3) - (int)b * (kRaceBlock / 8);
+    const uint32_t jj = r.v1 & 7u;
+    float lv = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) lv = jj == (uint32_t)j ? v[j] : lv;
+    *ly = __shfl_sync(0xffffffffu, lv, src & 31);
+  }
   return r;
 }
 
