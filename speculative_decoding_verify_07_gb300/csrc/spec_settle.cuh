@@ -778,6 +778,8 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     const unsigned ball = __ballot_sync(kSettleFull, in);
     const uint32_t p = n_c + __popc(ball & ((1u << lane) - 1u));
     if (in && p < (uint32_t)kSel) S.sel[p] = k;
+    // the list reads q of its entries after the sort: start those lines now
+    if (in && has_q) prefetch_l2(A.q + qrow + key64_idx(k));
     n_c += __popc(ball);
   }
   __syncwarp();
@@ -958,26 +960,68 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
         }
       }
       __syncwarp();
-      // level 1: the first kept entry of each block races for its block, with
-      // the block's weights summed in list order
+      // level 1: every block holding a kept entry races once, with the
+      // block's weights summed in list order.  Blocks get the slots of a
+      // 256-entry table in shared memory (at most kTopkSmall blocks, so every
+      // probe ends); the entry whose insertion made a slot races for it.
+      uint32_t* bkey = S.hist;
+      float2* bsum = reinterpret_cast<float2*>(S.sel);
+      for (int t = lane; t < 256; t += 32) {
+        bkey[t] = 0xffffffffu;
+        bsum[t] = make_float2(0.f, 0.f);
+      }
+      __syncwarp();
+      int slot[kTopkSmall / 32];
+      bool owner[kTopkSmall / 32];
+#pragma unroll
+      for (int r = 0; r < kTopkSmall / 32; ++r) {
+        const int i = 32 * r + lane;
+        slot[r] = -1;
+        owner[r] = false;
+        if (r < ns_r && i < n_s && L.w[i] > 0.f) {
+          const uint32_t bb = L.idx[i] / kRaceBlock;
+          uint32_t h = (bb * 2654435761u) >> 24;
+#pragma unroll 1
+          for (int probe = 0; probe < 256; ++probe) {
+            const uint32_t old = atomicCAS(&bkey[h], 0xffffffffu, bb);
+            if (old == 0xffffffffu || old == bb) {
+              slot[r] = (int)h;
+              owner[r] = old == 0xffffffffu;
+              break;
+            }
+            h = (h + 1u) & 255u;
+          }
+        }
+      }
+      __syncwarp();
+      // round by round; lanes of one round sharing a slot add in lane order
+#pragma unroll
+      for (int r = 0; r < kTopkSmall / 32; ++r) {
+        if (r >= ns_r) break;
+        const int i = 32 * r + lane;
+        const bool has = slot[r] >= 0;
+        const unsigned grp = __match_any_sync(kSettleFull, has ? slot[r] : -1 - lane);
+        const int rank = __popc(grp & ((1u << lane) - 1u));
+        const int nrank = (int)__reduce_max_sync(kSettleFull, has ? (uint32_t)__popc(grp) : 0u);
+#pragma unroll 1
+        for (int it = 0; it < nrank; ++it) {
+          if (has && rank == it) {
+            float2 sm = bsum[slot[r]];
+            sm.x += L.w[i];
+            sm.y += L.wu[i];
+            bsum[slot[r]] = sm;
+          }
+          __syncwarp();
+        }
+      }
       Race r1;
       race_init(r1);
-#pragma unroll 1
-      for (int r = 0; r < ns_r; ++r) {
-        const int i = 32 * r + lane;
-        if (i < n_s && L.w[i] > 0.f) {
-          const uint32_t bb = L.idx[i] / kRaceBlock;
-          bool rep = true;
-          float W = 0.f, U = 0.f;
-#pragma unroll 1
-          for (int t = 0; t < n_s; ++t) {
-            if (L.idx[t] / kRaceBlock == bb && L.w[t] > 0.f) {
-              if (t < i) rep = false;
-              W += L.w[t];
-              U += L.wu[t];
-            }
-          }
-          if (rep) race_consider(r1, W, U - W, bb, block_word(A, row, pos, bb));
+#pragma unroll
+      for (int r = 0; r < kTopkSmall / 32; ++r) {
+        if (owner[r]) {
+          const uint32_t bb = L.idx[32 * r + lane] / kRaceBlock;
+          const float2 sm = bsum[slot[r]];
+          race_consider(r1, sm.x, sm.y - sm.x, bb, block_word(A, row, pos, bb));
         }
       }
       warp_race_merge(r1);
