@@ -37,6 +37,22 @@ static __device__ __noinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_
   return c;
 }
 
+// Two Philox blocks with the same key, their rounds interleaved (for a
+// caller that needs both at once).
+__device__ __forceinline__ void philox4x32_10_pair(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
+#pragma unroll 1
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t alo0 = 0xD2511F53u * a.x, ahi0 = __umulhi(0xD2511F53u, a.x);
+    const uint32_t alo1 = 0xCD9E8D57u * a.z, ahi1 = __umulhi(0xCD9E8D57u, a.z);
+    const uint32_t blo0 = 0xD2511F53u * b.x, bhi0 = __umulhi(0xD2511F53u, b.x);
+    const uint32_t blo1 = 0xCD9E8D57u * b.z, bhi1 = __umulhi(0xCD9E8D57u, b.z);
+    a = make_uint4(ahi1 ^ a.y ^ k0, alo1, ahi0 ^ a.w ^ k1, alo0);
+    b = make_uint4(bhi1 ^ b.y ^ k0, blo1, bhi0 ^ b.w ^ k1, blo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
   return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
 }
@@ -244,10 +260,7 @@ __device__ __forceinline__ void race_init(Race& r) {
 // Score s = w / E with E = -ln U.  Because E >= 1 - U, an entry with
 // w < s1 * (1 - 2^-20) * (1 - U) cannot beat the current best and needs no
 // logarithm; the factor (1 - 2^-20) absorbs the rounding of the test itself.
-static __device__ __noinline__ Race race_update(Race r, float w, float tq, uint32_t v, float om) {
-  const float E = -log1pf(-om);
-  const float s = w / E;
-  const float t = (w + tq) / E;
+__device__ __forceinline__ void race_apply(Race& r, float s, float t, uint32_t v) {
   if (s > r.s1 || (s == r.s1 && v < r.v1)) {
     if (v != r.v1) {
       r.s2 = r.s1;
@@ -261,6 +274,17 @@ static __device__ __noinline__ Race race_update(Race r, float w, float tq, uint3
     r.s2 = s;
     r.t2 = t;
   }
+}
+// The score and margin weight of an entry of weight w: s = w / E, t = (w + tq) / E.
+__device__ __forceinline__ void race_score(float w, float tq, float om, float& s, float& t) {
+  const float E = -log1pf(-om);
+  s = w / E;
+  t = (w + tq) / E;
+}
+static __device__ __noinline__ Race race_update(Race r, float w, float tq, uint32_t v, float om) {
+  float s, t;
+  race_score(w, tq, om, s, t);
+  race_apply(r, s, t, v);
   return r;
 }
 // The cheap bound test inline, the logarithm out of line (the state stays

@@ -199,6 +199,14 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
   bool nan = false;
   float m = -INFINITY, zl = 0.f;
   int cm = 0x7fffffff;
+  // words 0..7 of a batch of each lane's chunks (word 1 only for greedy
+  // units, words 3..7 only for bonus positions); with one batch they stay
+  // held for the bonus merge below
+  u64 w[kFinBatchA][8];
+#pragma unroll
+  for (int i = 0; i < kFinBatchA; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[i][j] = 0ull;
   if (wait_word(A, R + (size_t)(NC - 1) * kRecWords, tag)) {
     long long spins = 0;
     bool ok;
@@ -209,9 +217,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       zl = 0.f;
       cm = 0x7fffffff;
       for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
-        // words 0..7 of the batch's chunks, all in flight before use (word 1
-        // only for greedy units, words 3..7 only for bonus positions)
-        u64 w[kFinBatchA][8];
+        // the batch's words are all in flight before the first is used
 #pragma unroll
         for (int i = 0; i < kFinBatchA; ++i) {
           const int c = c0 + 32 * i + lane;
@@ -304,31 +310,36 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
     // entries of the winning block
     Race a;
     race_init(a);
+    const bool held = NC <= 32 * kFinBatchA;   // w holds every chunk's words
     for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
-      u64 w[kFinBatchA][6];   // words 0 and 3..7 of the batch's chunks
+      u64 x[kFinBatchA][6];   // words 0 and 3..7 of the batch's chunks
 #pragma unroll
       for (int i = 0; i < kFinBatchA; ++i) {
         const int c = c0 + 32 * i + lane;
 #pragma unroll
-        for (int j = 0; j < 6; ++j) w[i][j] = 0ull;
-        if (c < NC) {
-          const u64* r = R + (size_t)c * kRecWords;
-          w[i][0] = __ldcg(r);
+        for (int j = 0; j < 6; ++j) x[i][j] = 0ull;
+        if (held) {
+          x[i][0] = w[i][0];
 #pragma unroll
-          for (int j = 1; j < 6; ++j) w[i][j] = __ldcg(r + 2 + j);
+          for (int j = 1; j < 6; ++j) x[i][j] = w[i][2 + j];
+        } else if (c < NC) {
+          const u64* r = R + (size_t)c * kRecWords;
+          x[i][0] = __ldcg(r);
+#pragma unroll
+          for (int j = 1; j < 6; ++j) x[i][j] = __ldcg(r + 2 + j);
         }
       }
 #pragma unroll
       for (int i = 0; i < kFinBatchA; ++i) {
         if (c0 + 32 * i + lane >= NC) continue;
-        const float mc = wf(w[i][0]);
+        const float mc = wf(x[i][0]);
         const float sc = mc > -INFINITY ? ex2((mc - m) * cfg.c) : 0.f;
         Race b;
-        b.s1 = wf(w[i][1]);
-        b.t1 = wf(w[i][2]);
-        b.s2 = wf(w[i][3]);
-        b.t2 = wf(w[i][4]);
-        b.v1 = wu(w[i][5]);
+        b.s1 = wf(x[i][1]);
+        b.t1 = wf(x[i][2]);
+        b.s2 = wf(x[i][3]);
+        b.t2 = wf(x[i][4]);
+        b.v1 = wu(x[i][5]);
         b.s1lo = 0.f;
         race_scale(b, sc);
         race_merge(a, b);

@@ -508,8 +508,9 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
     load_group<kBF16>(A, lrow, g, true, v);
     if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv);
     const uint32_t blk = (uint32_t)g * 2u;   // Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
-    const uint4 p0 = philox4x32_10(make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
-    const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
+    uint4 p0 = make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u);
+    uint4 p1 = make_uint4(blk + 1u, (uint32_t)pos, (uint32_t)row, 1u);
+    philox4x32_10_pair(p0, p1, A.key0, A.key1);
     float w[8], tq[8];
     group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
     const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
