@@ -582,10 +582,12 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
     if (n > (uint32_t)kStage) flags |= kListPartial;
     nn = min(n, (uint32_t)kStage);
     if (nn <= 32) {
-      // one candidate per lane: bitonic sort in registers, descending
+      // one candidate per lane: bitonic sort in registers, descending over
+      // lanes 0..S-1, S the power of two >= nn (lanes from nn on hold 0)
       u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
+      const int S = nn <= 8u ? 8 : (nn <= 16u ? 16 : 32);
 #pragma unroll 1
-      for (int size = 2; size <= 32; size <<= 1) {
+      for (int size = 2; size <= S; size <<= 1) {
 #pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
           const u64 o = __shfl_xor_sync(kFull, a, stride);
