@@ -196,6 +196,21 @@ __device__ __forceinline__ uint32_t key64_idx(unsigned long long k) {
   return 0xffffffffu - (uint32_t)(k & 0xffffffffull);
 }
 
+// Word `lane` of eight (lanes 8..31 get a0): a chain of selects, so a warp
+// writing a small record does not branch per lane.
+__device__ __forceinline__ uint32_t lane_word8(int lane, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  uint32_t v = a0;
+  v = lane == 1 ? a1 : v;
+  v = lane == 2 ? a2 : v;
+  v = lane == 3 ? a3 : v;
+  v = lane == 4 ? a4 : v;
+  v = lane == 5 ? a5 : v;
+  v = lane == 6 ? a6 : v;
+  v = lane == 7 ? a7 : v;
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Warp and block reductions with a fixed combination order (deterministic).
 // ---------------------------------------------------------------------------

@@ -470,18 +470,9 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
     idx = warp_min_u32(idx);
   }
   u64* rec = A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords;
-  uint32_t v = 0;
-  switch (lane) {
-    case 0: v = nan ? 0x7fc00000u : __float_as_uint(mc); break;
-    case 1: v = idx; break;
-    case 2: v = __float_as_uint(z); break;
-    case 3: v = __float_as_uint(r.s1); break;
-    case 4: v = __float_as_uint(r.t1); break;
-    case 5: v = __float_as_uint(r.s2); break;
-    case 6: v = __float_as_uint(r.t2); break;
-    case 7: v = r.v1; break;
-    default: break;
-  }
+  const uint32_t v = lane_word8(lane, nan ? 0x7fc00000u : __float_as_uint(mc), idx, __float_as_uint(z),
+                                __float_as_uint(r.s1), __float_as_uint(r.t1), __float_as_uint(r.s2),
+                                __float_as_uint(r.t2), r.v1);
   if (lane < (bonus ? 8 : 3)) __stcg(rec + lane, tagw(tag, v));
   __syncwarp();
 }
@@ -705,16 +696,8 @@ __device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it,
   }
   warp_race_merge(r);
   u64* rec = A.brec + ((size_t)it.u * A.NCB + it.c) * kBRecWords;
-  uint32_t v = 0;
-  switch (lane) {
-    case 0: v = __float_as_uint(alpha_c); break;
-    case 1: v = __float_as_uint(r.s1); break;
-    case 2: v = __float_as_uint(r.t1); break;
-    case 3: v = __float_as_uint(r.s2); break;
-    case 4: v = __float_as_uint(r.t2); break;
-    case 5: v = r.v1; break;
-    default: break;
-  }
+  const uint32_t v = lane_word8(lane, __float_as_uint(alpha_c), __float_as_uint(r.s1), __float_as_uint(r.t1),
+                                __float_as_uint(r.s2), __float_as_uint(r.t2), r.v1, 0u, 0u);
   if (lane < 6) __stcg(rec + lane, tagw(tag, v));
   __syncwarp();
 }

@@ -52,18 +52,8 @@ __device__ __forceinline__ bool wait_word(const Args& A, const u64* p, uint32_t 
 // The state of a drafted unfiltered unit as tagged words (lanes 0..7).
 __device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u, const UnitState& st) {
   const int lane = threadIdx.x & 31;
-  uint32_t v = 0;
-  switch (lane) {
-    case 0: v = __float_as_uint(st.m); break;
-    case 1: v = __float_as_uint(st.invZ); break;
-    case 2: v = __float_as_uint(st.lnZ); break;
-    case 3: v = __float_as_uint(st.lp_x); break;
-    case 4: v = (uint32_t)st.accept; break;
-    case 5: v = st.flags; break;
-    case 6: v = st.invalid; break;
-    case 7: v = (uint32_t)st.am; break;
-    default: break;
-  }
+  const uint32_t v = lane_word8(lane, __float_as_uint(st.m), __float_as_uint(st.invZ), __float_as_uint(st.lnZ),
+                                __float_as_uint(st.lp_x), (uint32_t)st.accept, st.flags, st.invalid, (uint32_t)st.am);
   if (lane < kStateWords) __stcg(A.ust + (size_t)u * kStateWords + lane, tagw(tag, v));
   __syncwarp();
 }
