@@ -15,8 +15,8 @@
 //     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
 //     max, the softmax sum relative to the chunk max, for greedy units the
 //     first argmax, at a bonus position the level-1 race of the chunk's
-//     256-entry blocks, for a small top-k the chunk's first 8 entries in the
-//     total order.  A B item (1024 bf16 / 768 fp32 logits, read again from
+//     256-entry blocks, for a small top-k the chunk's 8 largest entries in
+//     the total order (the smallest last).  A B item (1024 bf16 / 768 fp32 logits, read again from
 //     L2, plus q) takes the unit state from its tagged words and computes
 //     alpha = sum min(p, q) and the level-1 race of the residual.
 //   * Settle warps (the first warps of every SM).  Each takes its units in
@@ -502,8 +502,9 @@ __device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int
   return n;
 }
 
-// Small top-k A item: the chunk's first kList entries in the total order
-// (key, chunk-local index), tagged words in lanes 0..15.  Every such entry is
+// Small top-k A item: the chunk's kList largest entries in the total order,
+// the smallest of them last when there are kList (key, chunk-local index),
+// tagged words in lanes 0..15.  Every such entry is
 // at least the 8th largest lane maximum t8; a lane keeps up to kLaneCand of
 // its entries >= t8 (blocks whose maximum is below t8 are skipped), and a
 // lane holding more marks the list partial.
@@ -572,15 +573,17 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
     __syncwarp();
     if (n > (uint32_t)kStage) flags |= kListPartial;
     nn = min(n, (uint32_t)kStage);
-    if (nn <= 32) {
-      // one candidate per lane: bitonic sort in registers, descending over
-      // lanes 0..S-1, S the power of two >= nn (lanes from nn on hold 0)
+    if (nn > (uint32_t)kList && nn <= 32) {
+      // one candidate per lane: a bitonic network in registers over lanes
+      // 0..S-1 (S the power of two >= nn; lanes from nn on hold 0) that sorts
+      // groups of S/2, then of the last merge only the half-cleaners down to
+      // stride 8: lanes 0..7 then hold the 8 largest (in no particular order)
       u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
-      const int S = nn <= 8u ? 8 : (nn <= 16u ? 16 : 32);
+      const int S = nn <= 16u ? 16 : 32;
 #pragma unroll 1
       for (int size = 2; size <= S; size <<= 1) {
 #pragma unroll 1
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int stride = size >> 1; stride > 0 && (size < S || stride >= kList); stride >>= 1) {
           const u64 o = __shfl_xor_sync(kFull, a, stride);
           const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
           a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
@@ -589,8 +592,23 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
       __syncwarp();
       stage[lane] = a;
       __syncwarp();
-    } else {
+    } else if (nn > 32) {
       warp_sort_desc(stage, (int)nn);
+    }
+    // nn <= 8: the staged candidates are the list.  A full list keeps its
+    // smallest entry in slot 7 (the keys are distinct: one lane matches).
+    if (nn >= (uint32_t)kList) {
+      const u64 mine = lane < kList ? stage[lane] : ~0ull;
+      const uint32_t mh = __reduce_min_sync(kFull, (uint32_t)(mine >> 32));
+      const uint32_t ml = __reduce_min_sync(kFull, (uint32_t)(mine >> 32) == mh ? (uint32_t)mine : 0xffffffffu);
+      const int at = __ffs(__ballot_sync(kFull, lane < kList && mine == (((u64)mh << 32) | ml))) - 1;
+      const u64 last = stage[kList - 1];
+      __syncwarp();
+      if (lane == at && at != kList - 1) {
+        stage[at] = last;
+        stage[kList - 1] = mine;
+      }
+      __syncwarp();
     }
   }
   // word 2j: key of entry j (0 = none); word 2j + 1: its chunk-local index
@@ -694,7 +712,7 @@ __device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it,
     const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
     race_consider(r, myW, myU - myW, blk, block_word(A, it.row, it.pos, blk));
   }
-  warp_race_merge(r);
+  if (need_race) warp_race_merge(r);   // accepted: the empty race as it is
   u64* rec = A.brec + ((size_t)it.u * A.NCB + it.c) * kBRecWords;
   const uint32_t v = lane_word8(lane, __float_as_uint(alpha_c), __float_as_uint(r.s1), __float_as_uint(r.t1),
                                 __float_as_uint(r.s2), __float_as_uint(r.t2), r.v1, 0u, 0u);

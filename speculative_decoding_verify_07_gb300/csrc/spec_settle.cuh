@@ -8,11 +8,12 @@
 //     entries); a drafted unfiltered unit takes its accept test, publishes
 //     its state for the B items, then merges their records (alpha and the
 //     residual draw).
-//   small top-k units: every A item lists the first 8 entries of its chunk
-//     in the total order.  A chunk whose listed 8th entry is below the K-th
-//     entry of the merged lists holds no further top-K entry, so the merged
-//     lists give the top-K set; other chunks are re-read from L2.  Top-p, the
-//     accept test, alpha and the draw run on the sorted list.
+//   small top-k units: every A item lists the 8 largest entries of its
+//     chunk in the total order, the smallest of them last.  A chunk whose
+//     smallest listed entry is below the K-th entry of the merged lists holds
+//     no further top-K entry, so the merged lists give the top-K set; other
+//     chunks are re-read from L2.  Top-p, the accept test, alpha and the draw
+//     run on the sorted list.
 //
 // The last settled unit of a row resolves the accept chain and writes the
 // row's outputs.

@@ -73,9 +73,10 @@ __device__ __forceinline__ void csync() {
 //       [1] first index of the chunk max (greedy), [2] sum of exp2((l - m) c)
 //       relative to the chunk max, [3..7] level-1 race of the chunk's blocks
 //       relative to the chunk max (s1, t1, s2, t2, v1; bonus positions);
-//     small top-k: [2j] order key and [2j + 1] chunk-local index of the
-//       chunk's j-th entry in the total order (j < 8; key 0 = none), with
-//       the flags kListNaN / kListPartial in word 1.
+//     small top-k: [2j] order key and [2j + 1] chunk-local index of one of
+//       the chunk's 8 largest entries in the total order (j < 8; the
+//       smallest at j = 7 when there are 8; key 0 = none), with the flags
+//       kListNaN / kListPartial in word 1.
 //   B record, per (unit, B item), 8 words: [0] alpha, [1..5] level-1 race of
 //     the residual (s1, t1, s2, t2, v1).
 //   Unit state of a drafted unfiltered unit, 8 words: m, 1/Z, ln Z, the
