@@ -502,6 +502,24 @@ __device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int
   return n;
 }
 
+// Bitonic network over lanes 0..S-1, fully unrolled: groups of S/2 sorted
+// (alternating directions), then of the last merge the half-cleaners down to
+// stride kList, which leave the kList largest keys in lanes 0..kList-1.
+template <int S>
+__device__ __forceinline__ u64 top8_network(u64 a, int lane) {
+#pragma unroll
+  for (int size = 2; size <= S; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (size == S && stride < kList) break;
+      const u64 o = __shfl_xor_sync(kFull, a, stride);
+      const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+      a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
+    }
+  }
+  return a;
+}
+
 // Small top-k A item: the chunk's kList largest entries in the total order,
 // the smallest of them last when there are kList (key, chunk-local index),
 // tagged words in lanes 0..15.  Every such entry is
@@ -528,14 +546,17 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
   if (!nan) {
     // t8: take the largest lane maxima (with their multiplicity) until 8
     uint32_t key = okey(lm), need = (uint32_t)kList, t8k = 0u;
-#pragma unroll 1
+    bool found = false;   // warp-uniform
+#pragma unroll
     for (int i = 0; i < kList; ++i) {
-      const uint32_t mx = __reduce_max_sync(kFull, key);
-      const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
-      t8k = mx;
-      if (c >= need) break;
-      need -= c;
-      key = key == mx ? 0u : key;
+      if (!found) {
+        const uint32_t mx = __reduce_max_sync(kFull, key);
+        const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
+        t8k = mx;
+        found = c >= need;
+        need -= found ? 0u : c;
+        key = key == mx ? 0u : key;
+      }
     }
     const float t8 = from_okey(t8k);
     // the lane's blocks holding finite entries >= t8, then those entries
@@ -579,16 +600,7 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
       // groups of S/2, then of the last merge only the half-cleaners down to
       // stride 8: lanes 0..7 then hold the 8 largest (in no particular order)
       u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
-      const int S = nn <= 16u ? 16 : 32;
-#pragma unroll 1
-      for (int size = 2; size <= S; size <<= 1) {
-#pragma unroll 1
-        for (int stride = size >> 1; stride > 0 && (size < S || stride >= kList); stride >>= 1) {
-          const u64 o = __shfl_xor_sync(kFull, a, stride);
-          const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
-          a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
-        }
-      }
+      a = nn <= 16u ? top8_network<16>(a, lane) : top8_network<32>(a, lane);
       __syncwarp();
       stage[lane] = a;
       __syncwarp();
