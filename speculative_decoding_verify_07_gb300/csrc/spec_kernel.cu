@@ -19,7 +19,8 @@
 //     the total order (the smallest last).  A B item (1024 bf16 / 768 fp32 logits, read again from
 //     L2, plus q) takes the unit state from its tagged words and computes
 //     alpha = sum min(p, q) and the level-1 race of the residual.
-//   * Settle warps (the first warps of every SM).  Each takes its units in
+//   * Settle warps (the first scheduler's warps, four per SM, on as many SMs
+//     as the tasks need).  Each takes its units in
 //     the same class order, waits for their records and settles them
 //     (spec_settle.cuh); a drafted unfiltered unit publishes its state for
 //     the B items and is finished after them.
@@ -939,10 +940,13 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
   P.sB = (uint32_t)(P.nD * A.k * P.NCB);
   P.sGR = (uint32_t)(P.nG * (A.k + 1) * P.NCA);
   const uint32_t nw = (uint32_t)A.n_ctas * kSW;
-  // settle warps are taken first from the warps on each SM's first
-  // scheduler (w % 4 == 0), one per SM at a time, so the other schedulers
-  // run stream code only
-  const uint32_t g = (uint32_t)(w & 3) * (4u * (uint32_t)A.n_ctas) + (uint32_t)(w >> 2) * (uint32_t)A.n_ctas + blockIdx.x;
+  // settle warps are the warps on the SMs' first schedulers (w % 4 == 0),
+  // four per SM: consecutive tasks (one class, neighbouring rows) settle on
+  // one SM, whose first scheduler then runs no stream warp, and the other
+  // schedulers run stream code only
+  const uint32_t g = (w & 3) == 0 ? blockIdx.x * 4u + (uint32_t)(w >> 2)
+                                   : 4u * (uint32_t)A.n_ctas + (uint32_t)((w & 3) - 1) * (4u * (uint32_t)A.n_ctas) +
+                                         (uint32_t)(w >> 2) * (uint32_t)A.n_ctas + blockIdx.x;
   const uint32_t nS = (uint32_t)(2 * P.nD * A.k + P.nT * (A.k + 1) + P.nD + P.nG * (A.k + 1));
   const uint32_t nsw = min(nS, nw / 4u);
   if (g < nsw) {

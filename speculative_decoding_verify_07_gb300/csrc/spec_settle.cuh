@@ -517,6 +517,34 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, uint32_t* total) 
 // padded with zeros to a power of two >= 32; rolled loops keep it small.
 static __device__ __noinline__ void warp_sort_desc(u64* s, int n) {
   const int lane = threadIdx.x & 31;
+  if (n <= 64) {
+    // in registers: lane holds entries lane and lane + 32; a pair at stride
+    // 32 is in one lane, other pairs are one shuffle apart.  The pair's
+    // lower entry keeps the larger key iff the pair's run descends.
+    u64 x0 = lane < n ? s[lane] : 0ull, x1 = lane + 32 < n ? s[lane + 32] : 0ull;
+#pragma unroll 1
+    for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll 1
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        if (stride == 32) {
+          const u64 hi = x0 > x1 ? x0 : x1, lo = x0 > x1 ? x1 : x0;
+          x0 = hi;   // size 64: one descending run
+          x1 = lo;
+        } else {
+          const u64 o0 = __shfl_xor_sync(kSettleFull, x0, stride), o1 = __shfl_xor_sync(kSettleFull, x1, stride);
+          const bool lower = (lane & stride) == 0;
+          const bool k0 = lower == ((lane & size) == 0), k1 = lower == (((lane + 32) & size) == 0);
+          x0 = k0 ? (o0 > x0 ? o0 : x0) : (o0 < x0 ? o0 : x0);
+          x1 = k1 ? (o1 > x1 ? o1 : x1) : (o1 < x1 ? o1 : x1);
+        }
+      }
+    }
+    __syncwarp();
+    s[lane] = x0;
+    s[lane + 32] = x1;
+    __syncwarp();
+    return;
+  }
   int N = 32;
   while (N < n) N <<= 1;
   for (int i = n + lane; i < N; i += 32) s[i] = 0ull;
