@@ -403,7 +403,8 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
 }
 
 template <bool kBF16>
-__device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag, int u, int row, int pos,
+                                          const RowCfg& cfg) {
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const bool has_q = pos < A.k;
@@ -430,7 +431,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
   const float m = from_okey((uint32_t)(best >> 32));
   const int am = (int)key64_idx(best);
   if (best == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
-    if (ctid() < 32) commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    if (ctid() < 32) commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
     csync();
     return;
   }
@@ -633,7 +634,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, int u, int r
       rec.draw_flags = draw_flags;
     }
   }
-  if (ctid() < 32) commit_record(A, u, row, rec);
+  if (ctid() < 32) commit_record(A, tag, u, row, rec);
   csync();
 }
 

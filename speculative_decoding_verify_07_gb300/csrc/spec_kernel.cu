@@ -890,7 +890,7 @@ __device__ __noinline__ void general_phase(const Args& A, const Plan& P, VShm& S
     csync();
     if (g >= nGU) break;
     const int row = (int)P.order[gbase + g / k1], pos = g % k1;
-    unit_general<kBF16>(A, S.gen[grp], row * k1 + pos, row, pos, plan_cfg(A, P, row));
+    unit_general<kBF16>(A, S.gen[grp], S.tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
   }
 }
 

@@ -264,7 +264,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       z.invalid = 1;
       publish_state(A, tag, u, z);
     }
-    commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
     return false;
   }
   const float m_lane = m;
@@ -293,7 +293,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
         if (has_q && !(1.0f - q_am > 0.0f)) rec.draw_flags |= SPEC_F_RESIDUAL_EMPTY;
       }
     }
-    commit_record(A, u, row, rec);
+    commit_record(A, tag, u, row, rec);
     return false;
   }
   if (bonus) {
@@ -348,7 +348,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       rec.lp_y = ((drawn ? ly : load_logit(A, kBF16, lrow + y)) - m) * cfg.invT - lnZ;
       if (draw_margin(a) || draw_margin(l2)) rec.draw_flags |= SPEC_F_MARGIN_DRAW;
     }
-    commit_record(A, u, row, rec);
+    commit_record(A, tag, u, row, rec);
     return false;
   }
   // drafted: accept test, then publish the state for the B items
@@ -458,7 +458,7 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
       rec.draw_flags = draw_flags;
     }
   }
-  commit_record(A, u, row, rec);
+  commit_record(A, tag, u, row, rec);
 }
 // First bin (from bin 0) where the running count over hist[0..256) reaches
 // `need` (>= 1); 256 when the total is below it.  *before = the count of the
@@ -765,7 +765,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   top = warp_max_u64(top);
   const float m = from_okey((uint32_t)(top >> 32));
   if (nan || top == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
-    commit_record(A, u, row, empty_record(SPEC_F_NAN));
+    commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
     return;
   }
   const int am = (int)key64_idx(top);
@@ -1108,7 +1108,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       rec.draw_flags = draw_flags;
     }
   }
-  commit_record(A, u, row, rec);
+  commit_record(A, tag, u, row, rec);
 }
 
 }  // namespace specv

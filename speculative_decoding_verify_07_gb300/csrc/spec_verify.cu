@@ -66,7 +66,7 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
   A.rec = reinterpret_cast<specv::u64*>(ws + L.rec);
   A.ust = reinterpret_cast<specv::u64*>(ws + L.ust);
   A.brec = reinterpret_cast<specv::u64*>(ws + L.brec);
-  A.urec = reinterpret_cast<specv::UnitRecord*>(ws + L.urec);
+  A.urec = reinterpret_cast<specv::u64*>(ws + L.urec);
   A.order = reinterpret_cast<uint32_t*>(ws + L.order);
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);

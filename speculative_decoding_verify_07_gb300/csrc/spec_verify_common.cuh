@@ -81,9 +81,12 @@ __device__ __forceinline__ void csync() {
 //     the residual (s1, t1, s2, t2, v1).
 //   Unit state of a drafted unfiltered unit, 8 words: m, 1/Z, ln Z, the
 //     draft's logprob, accept, flags, invalid, argmax (see UnitState).
+//   Unit record of a settled unit, 8 words: the fields of UnitRecord in
+//     order (the row finaliser reads them).
 constexpr int kRecWords = 16;
 constexpr int kBRecWords = 8;
 constexpr int kStateWords = 8;
+constexpr int kURecWords = 8;
 constexpr int kList = 8;                   // entries listed per top-k A item
 constexpr uint32_t kListNaN = 1u << 31;    // the chunk holds a NaN
 constexpr uint32_t kListPartial = 1u << 30;   // the list may miss entries above its last (re-scan the chunk)
@@ -104,7 +107,7 @@ struct UnitState {        // what the B items of a drafted unfiltered unit need
 };
 
 
-struct UnitRecord {       // 32 bytes, one per unit, read by the row finaliser
+struct UnitRecord {       // one per unit, published as kURecWords tagged words
   uint32_t flags;
   int32_t accept;
   float lp_x;
@@ -134,7 +137,7 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   L.rec = off; off = align_up(off + U * max_nca(V) * kRecWords * 8, 256);
   L.brec = off; off = align_up(off + U * max_ncb(V) * kBRecWords * 8, 256);
   L.ust = off; off = align_up(off + U * kStateWords * 8, 256);
-  L.urec = off; off = align_up(off + U * sizeof(UnitRecord), 256);
+  L.urec = off; off = align_up(off + U * kURecWords * 8, 256);
   L.order = off; off = align_up(off + (size_t)B * 4, 256);
   L.total = off;
   return L;
@@ -155,7 +158,7 @@ struct Args {
   u64* rec;               // A records
   u64* brec;              // B records
   u64* ust;               // unit states of drafted unfiltered units
-  UnitRecord* urec;
+  u64* urec;              // unit records
   uint32_t* order;        // rows by class (batches above the shared-memory order limit)
   uint32_t key0, key1;
   int B, k, V, U;
@@ -293,26 +296,41 @@ __device__ __forceinline__ float group_max(const float v[8]) {
 // ---------------------------------------------------------------------------
 // Records and the per-row finalize.
 // ---------------------------------------------------------------------------
-// One warp, lane j reading unit j's record (k + 1 <= 32): the accepted
-// prefix ends at the first rejected draft; its tokens are the drafts, then
-// the draw of the first rejected unit (or the bonus draw).
-static __device__ __noinline__ void finalize_row(const Args& A, int row) {
+// One warp, lane j reading unit j's record (k + 1 <= 32; bounded wait for
+// its tag): the accepted prefix ends at the first rejected draft; its tokens
+// are the drafts, then the draw of the first rejected unit (or the bonus
+// draw).
+static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_t tag) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int k = A.k;
-  __syncwarp();   // orders the lanes' reads after lane 0's acquiring ticket
-  uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
-  if (lane <= k) {
-    const uint4* r = reinterpret_cast<const uint4*>(A.urec + (size_t)row * (k + 1) + lane);
-    w0 = __ldcg(r);
-    w1 = __ldcg(r + 1);
+  const u64* R = A.urec + ((size_t)row * (k + 1) + lane) * kURecWords;
+  u64 w[7];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) w[i] = 0ull;
+  long long spins = 0;
+  while (true) {
+    bool ok = true;
+    if (lane <= k) {
+#pragma unroll
+      for (int i = 0; i < 7; ++i) {
+        w[i] = __ldcg(R + i);
+        ok = ok && tag_ok(w[i], tag);
+      }
+    }
+    if (__all_sync(full, ok)) break;
+    if (++spins > kSpinLimit) {
+      if (lane == 0) atomicOr(&A.ws->error, 4u);
+      break;
+    }
+    __nanosleep(64);
   }
-  const uint32_t f = w0.x;
-  const bool acc = w0.y != 0u;
-  const float lp_x = __uint_as_float(w0.z), alpha = __uint_as_float(w0.w);
-  const int32_t y = (int32_t)w1.x;
-  const float lp_y = __uint_as_float(w1.y);
-  const uint32_t draw_flags = w1.z;
+  const uint32_t f = wu(w[0]);
+  const bool acc = wu(w[1]) != 0u;
+  const float lp_x = wf(w[2]), alpha = wf(w[3]);
+  const int32_t y = (int32_t)wu(w[4]);
+  const float lp_y = wf(w[5]);
+  const uint32_t draw_flags = wu(w[6]);
   uint32_t uflags = __reduce_or_sync(full, f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP));
   int32_t* tok = A.tokens + (size_t)row * (k + 1);
   float* lp = A.logprobs + (size_t)row * (k + 1);
@@ -349,18 +367,24 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row) {
   }
 }
 
-// One warp (converged): lane 0 publishes the unit's record (lane 0's `rec`);
-// the warp whose unit is the row's last finalizes the row.
-static __device__ __noinline__ void commit_record(const Args& A, int u, int row, const UnitRecord& rec) {
+// One warp (converged): lanes 0..7 publish the unit's record (lane 0's
+// `rec`) as tagged words and lane 0 takes the row's ticket (relaxed: the
+// finaliser waits for the tags, not for an ordering); the warp whose unit is
+// the row's last finalizes the row.
+static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, int u, int row, const UnitRecord& rec) {
+  const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
+  const uint32_t v = lane_word8(lane, __shfl_sync(full, rec.flags, 0), __shfl_sync(full, (uint32_t)rec.accept, 0),
+                                __shfl_sync(full, __float_as_uint(rec.lp_x), 0),
+                                __shfl_sync(full, __float_as_uint(rec.alpha), 0), __shfl_sync(full, (uint32_t)rec.y, 0),
+                                __shfl_sync(full, __float_as_uint(rec.lp_y), 0), __shfl_sync(full, rec.draw_flags, 0),
+                                0u);
+  if (lane < kURecWords) __stcg(A.urec + (size_t)u * kURecWords + lane, tagw(tag, v));
   uint32_t old = 0u;
-  if (lane == 0) {
-    A.urec[u] = rec;
-    old = atomic_add_acq_rel(&A.row_ticket[row], 1u);
-  }
-  old = __shfl_sync(0xffffffffu, old, 0);
+  if (lane == 0) old = atomicAdd(&A.row_ticket[row], 1u);
+  old = __shfl_sync(full, old, 0);
   if (old == (uint32_t)A.k) {
-    finalize_row(A, row);
+    finalize_row(A, row, tag);
     if (lane == 0) A.row_ticket[row] = 0;   // leave the workspace clean for the next call
   }
   __syncwarp();
