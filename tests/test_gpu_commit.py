@@ -57,6 +57,26 @@ def test_commit_bad_indices_flagged_and_skipped():
     assert np.array_equal(gf.astype(np.uint32), ef)
 
 
+def test_commit_multi_chunk_blobs_with_tails():
+    """Blobs of 20 KiB (recurrent) and 16 KiB + 64 B (conv): several 16 KiB chunks per blob
+    with a short last chunk, plus a skipped row and out-of-range rows."""
+    vrec, vconv, acc, slot, crec, cconv = synth.make_commit_small(L=3, B=6, S=3, H=2, Dk=64, Dv=40, W=4,
+                                                                  C=2056, slots=8, seed=23)
+    acc = acc.copy()
+    slot = slot.copy()
+    acc[0] = 0
+    acc[1] = 3
+    acc[2] = 4      # beyond S: flagged and skipped
+    slot[3] = -1    # bad slot: flagged and skipped
+    acc[3] = 2
+    acc[4] = 1
+    er, ec, ef = oc.commit(vrec, vconv, acc, slot, crec, cconv)
+    gr, gc, gf = _run(vrec, vconv, acc, slot, crec, cconv)
+    assert np.array_equal(gr.view(np.uint32), er.view(np.uint32))
+    assert np.array_equal(gc, ec)
+    assert np.array_equal(gf.astype(np.uint32), ef)
+
+
 def test_commit_rec_only_conv_only_and_identity_slots():
     vrec, vconv, acc, _, crec, cconv = synth.make_commit_small(slots=5)
     er, ec, _ = oc.commit(vrec, vconv, acc, None, crec, cconv)
