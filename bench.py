@@ -382,8 +382,12 @@ def run_ours(args):
         "components": {
             "spec_verify": {"us": round(tv * 1e6, 2), "rows_per_s": round(B / tv, 1),
                             "gbs": r_verify["achieved"], "frac": r_verify["frac"],
-                            "dense_q_model_bytes": int(inps[0].logits.size * 2 + inps[0].q.size * 4)},
-            "spec_commit": {"us": round(tc * 1e6, 2), "gbs": r_commit["achieved"], "frac": r_commit["frac"]},
+                            "dense_q_model_bytes": int(inps[0].logits.size * 2 + inps[0].q.size * 4),
+                            "us_p50": round(statistics.median(t_verify) * 1e3, 2),
+                            "us_max": round(max(t_verify) * 1e3, 2)},
+            "spec_commit": {"us": round(tc * 1e6, 2), "gbs": r_commit["achieved"], "frac": r_commit["frac"],
+                            "us_p50": round(statistics.median(t_commit) * 1e3, 2),
+                            "us_max": round(max(t_commit) * 1e3, 2)},
             "mean_accept_len": float(acc.mean()),
         },
     }
