@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -110,7 +111,7 @@ class ClockSampler:
         self.proc = None
         self.thread = None
         self.samples = []
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"spec_clocks_{os.getpid()}.csv")
         self.index = index
 
     def _nvml(self):
