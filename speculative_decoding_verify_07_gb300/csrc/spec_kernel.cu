@@ -173,10 +173,10 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row
 }
 
 
-// Item t of the sequence [A: small top-k][A: drafted unfiltered][A: bonus
-// positions][A: greedy][B: drafted unfiltered]: the units whose settle takes
-// longest come first, and the greedy items run while the states that the B
-// items need are published.
+// Item t of the sequence [A: drafted unfiltered][A: small top-k][A: bonus
+// positions][A: greedy][B: drafted unfiltered]: the states that the B items
+// need are published early, the top-k units, whose settle takes longest,
+// follow, and the greedy items run before the B items.
 template <bool kBF16>
 __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
@@ -186,20 +186,20 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
   int row, pos, j;
   uint32_t s = t;
   it.reread = 0;
-  if (s < P.sTK) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[P.nD + j / k1];
-    pos = j % k1;
-    it.kind = 1;
-  } else if ((s -= P.sTK) < P.sDD) {
+  if (s < P.sDD) {
     j = (int)(s / (uint32_t)P.NCA);
     it.c = (int)s - j * P.NCA;
     row = (int)P.order[j / k];
     pos = j % k;
     it.reread = 1;
     it.kind = 1;
-  } else if ((s -= P.sDD) < P.sDB) {
+  } else if ((s -= P.sDD) < P.sTK) {
+    j = (int)(s / (uint32_t)P.NCA);
+    it.c = (int)s - j * P.NCA;
+    row = (int)P.order[P.nD + j / k1];
+    pos = j % k1;
+    it.kind = 1;
+  } else if ((s -= P.sTK) < P.sDB) {
     j = (int)(s / (uint32_t)P.NCA);
     it.c = (int)s - j * P.NCA;
     row = (int)P.order[j];
