@@ -9,9 +9,9 @@
 //     an mbarrier) while it reduces the other with warp collectives.  The
 //     items of all units form one sequence, which the stream warps of all
 //     SMs take in order from one counter:
-//       A items of small top-k units, of drafted unfiltered units, of
-//       unfiltered bonus positions; B items of drafted unfiltered units; A
-//       items of greedy units.
+//       A items of drafted unfiltered units, of small top-k units, of
+//       unfiltered bonus positions, of greedy units; B items of drafted
+//       unfiltered units.
 //     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
 //     max, the softmax sum relative to the chunk max, for greedy units the
 //     first argmax, at a bonus position the level-1 race of the chunk's
