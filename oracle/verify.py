@@ -74,7 +74,9 @@ class RowResult:
     # diagnostics used by the tests
     a: int = -1
     accept: list = field(default_factory=list)
-    margin_accept: list = field(default_factory=list)
+    margin_accept: list = field(default_factory=list)   # per accept test taken, in chain order
+    topp_margin: list = field(default_factory=list)     # per position 0..k
+    draw_margin: bool = False
 
 
 def total_order(l: np.ndarray) -> np.ndarray:
@@ -234,11 +236,13 @@ def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
         P = 1.0            # top-p disabled
 
     targets = []
+    topp_margin = []
     for j in range(k + 1):
         t = target_distribution(logits_r[j], T, K, P)
         if t.topp_margin:
             flags |= F_MARGIN_TOPP
         targets.append(t)
+        topp_margin.append(t.topp_margin)
 
     # alpha_j = sum_v min(p_j(v), q_j(v)) for every draft position
     # [AReno, accept-probability table].  READING: computed whether or not
@@ -303,33 +307,59 @@ def verify_row(logits_r: np.ndarray, q_r: np.ndarray, drafts_r: np.ndarray,
     tokens[a] = y
     logprobs[a] = token_logprob(logits_r[a], targets[a], y, T)
     res = RowResult(tokens, a + 1, logprobs, alpha, flags, a=a, accept=accept,
-                    margin_accept=margin_accept)
+                    margin_accept=margin_accept, topp_margin=topp_margin,
+                    draw_margin=bool(draw_margin))
     return res
 
 
 def verify(logits: np.ndarray, q: np.ndarray, drafts: np.ndarray,
            temperature: np.ndarray, top_k: np.ndarray, top_p: np.ndarray,
-           seed: int, rows=None) -> dict:
+           seed: int, rows=None, row_base: int = 0) -> dict:
     """Batched verify over `rows` (default: all rows).
 
     logits [B, k+1, V] and q [B, k, V] are converted to float64; the returned
     arrays are indexed like `rows`.
+
+    Row r of this batch draws its random numbers as row `row_base + r` of the
+    stream keyed by (seed, row, position).  READING: the benchmark spec keys the
+    stream by the row; a batch split into blocks of rows (one block per GPU)
+    reproduces the whole batch's draws when every block passes the index of
+    its first row as row_base.  The stream row is a 32-bit counter word, so
+    row_base + r wraps modulo 2^32.
+
+    Besides the outputs, the result holds each row's margin record: the
+    chain's reach `a`, the accept margins of the tests taken
+    (`margin_accept`, [rows, k], False past the chain), the top-p margins per
+    position (`topp_margin`, [rows, k+1]) and the draw margin (`draw_margin`).
     """
     B = logits.shape[0]
+    k = logits.shape[1] - 1
     rows = list(range(B)) if rows is None else list(rows)
     out = {"tokens": [], "accept_len": [], "logprobs": [], "alpha": [], "flags": [],
-           "rows": np.asarray(rows)}
+           "a": [], "margin_accept": [], "topp_margin": [], "draw_margin": [],
+           "rows": np.asarray(rows, dtype=np.int64)}
     for r in rows:
         res = verify_row(np.asarray(logits[r], dtype=np.float64),
                          np.asarray(q[r], dtype=np.float64), np.asarray(drafts[r]),
-                         float(temperature[r]), int(top_k[r]), float(top_p[r]), seed, r)
+                         float(temperature[r]), int(top_k[r]), float(top_p[r]), seed,
+                         (int(row_base) + int(r)) % (1 << 32))
         out["tokens"].append(res.tokens)
         out["accept_len"].append(res.accept_len)
         out["logprobs"].append(res.logprobs)
         out["alpha"].append(res.alpha)
         out["flags"].append(res.flags)
-    for key in ("tokens", "accept_len", "logprobs", "alpha", "flags"):
+        out["a"].append(res.a)
+        ma = np.zeros(k, dtype=bool)
+        ma[:len(res.margin_accept)] = res.margin_accept
+        out["margin_accept"].append(ma)
+        tm = np.zeros(k + 1, dtype=bool)
+        tm[:len(res.topp_margin)] = res.topp_margin
+        out["topp_margin"].append(tm)
+        out["draw_margin"].append(res.draw_margin)
+    for key in ("tokens", "accept_len", "logprobs", "alpha", "flags", "a", "draw_margin"):
         out[key] = np.asarray(out[key])
+    out["margin_accept"] = np.asarray(out["margin_accept"], dtype=bool).reshape(len(rows), k)
+    out["topp_margin"] = np.asarray(out["topp_margin"], dtype=bool).reshape(len(rows), k + 1)
     return out
 
 
