@@ -1,14 +1,13 @@
 #!/usr/bin/env python3
 """Benchmark of the speculative verify hot path on GB300.
 
-One step = one pass of the whole hot path over one synthetic batch:
-  spec_verify  on 64 rows, k=2, V=151936, bf16 logits, mixed per-row params
-               (25% greedy, 50% T=0.7 top-k 50 top-p 0.9, 25% T=1), exact
-               ties in 1% of positions;
-  spec_commit  of those 64 rows' accepted states (accept_len from the verify)
-               from a stacked verify buffer of 24 layers x 3 states of fp32
-               recurrent state 16x128x128 plus bf16 conv state 4x4096.
-Metric: rows/s (whole job), with HBM GB/s against the measured peak.
+One step = one spec_verify call on 64 rows, k=2, V=151936, bf16 logits,
+mixed per-row params (25% greedy, 50% T=0.7 top-k 50 top-p 0.9, 25% T=1),
+exact ties in 1% of positions.  Metric: spec-verify rows/s (whole job),
+with the verify's HBM GB/s against the measured peak.  Components: the same
+kernel on the tiny, top-p (16 rows, V=157184) and adversarial (256 rows,
+k=4, fp32) workloads, each with its own roofline, and spec_commit of
+64 rows x 24 layers of stacked recurrent/conv state.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -36,10 +35,12 @@ sys.path.insert(0, ROOT)
 METRIC = "spec-verify rows/s at V=151936,k=2; achieved HBM GB/s vs GB300 peak"
 # spec_verify launches one cooperative kernel; its sources
 VERIFY_SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_settle.cuh", "spec_general.cuh",
-                  "spec_verify_common.cuh", "spec_device.cuh"]
+                  "spec_common.cuh", "spec_device.cuh"]
 VERIFY_LAUNCHES = 1
 B, K, V = 64, 2, 151936
 N_SETS = 4   # rotating verify input sets (each ~136 MB, together > L2)
+WORKLOAD = ("spec_verify 64 rows k=2 V=151936 bf16, mixed params (25% greedy, 50% T0.7 top-k50 top-p0.9, "
+            "25% T1), exact ties in 1% of positions")
 
 
 def measured_peaks():
@@ -246,56 +247,162 @@ def job_rows_per_s(rows_per_rank, world, elapsed_s):
     return rows_per_rank * world / elapsed_s
 
 
-def cpu_oracle_sample(inp, n_rows=16, commit_rows=2):
-    """Time the oracle as it stands on a bounded sample of the workload."""
-    from oracle import commit as oc
-    from oracle import verify as ov
-    from speculative_decoding_verify_07_gb300 import synth
-    rows = list(range(n_rows))
-    t0 = time.perf_counter()
-    ov.verify(inp.logits, inp.q, inp.drafts, inp.temperature, inp.top_k, inp.top_p, inp.seed, rows=rows)
-    t_verify = (time.perf_counter() - t0) / n_rows
-    sh = synth.CommitShape()
-    rng = np.random.default_rng(0)
-    vrec = rng.standard_normal((sh.L, commit_rows, sh.S, sh.H, sh.Dk, sh.Dv), dtype=np.float32)
-    vconv = rng.integers(0, 1 << 16, size=(sh.L, commit_rows, sh.S, sh.W, sh.C), dtype=np.uint16)
-    crec = np.zeros((sh.L, commit_rows, sh.H, sh.Dk, sh.Dv), np.float32)
-    cconv = np.zeros((sh.L, commit_rows, sh.W, sh.C), np.uint16)
-    acc = np.full(commit_rows, 2, np.int32)
-    t0 = time.perf_counter()
-    oc.commit(vrec, vconv, acc, None, crec, cconv)
-    t_commit = (time.perf_counter() - t0) / commit_rows
-    per_row = t_verify + t_commit
-    return {"value": 1.0 / per_row, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle verify on {n_rows} of the 64 rows + oracle commit of {commit_rows} rows "
-                      f"(24 layers); {t_verify * 1e3:.1f} ms/row verify, {t_commit * 1e3:.1f} ms/row commit; "
-                      "single thread (NumPy)"}
+def _oracle_rows_worker(args):
+    """Pool worker: the oracle on rows of the mixed workload (inputs built in
+    the worker from their seed, outside the timed call)."""
+    name, kwargs, rows, seed_offset = args
+    return _ORACLE_INPUT.rows(rows)
+
+
+class _OracleInput:
+    def __init__(self):
+        self.inp = None
+
+    def build(self, name, kwargs):
+        from speculative_decoding_verify_07_gb300 import synth
+        self.inp = synth.make_verify(name, **kwargs)
+
+    def rows(self, rows):
+        from oracle import verify as ov
+        inp = self.inp
+        t0 = time.perf_counter()
+        ov.verify(inp.logits, inp.q, inp.drafts, inp.temperature, inp.top_k, inp.top_p, inp.seed, rows=rows)
+        return time.perf_counter() - t0
+
+
+_ORACLE_INPUT = _OracleInput()
+
+
+def _pool_init(name, kwargs):
+    _ORACLE_INPUT.build(name, kwargs)
+
+
+def _pool_ready(_):
+    return os.getpid()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_baseline(n_rows_all=None, n_rows_1t=4, workers=None):
+    """The oracle as it stands, timed on the host cores on bounded samples of
+    the mixed workload: one process per core over n_rows_all rows, and one
+    thread over n_rows_1t rows.  Input generation happens before the clocks."""
+    import multiprocessing as mp
+    workers = workers or host_cores()
+    n_rows_all = n_rows_all or max(2 * workers, 16)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers, initializer=_pool_init, initargs=("mixed", {})) as pool:
+        # every worker builds its copy of the inputs before the timed map
+        pool.map(_pool_ready, range(4 * workers), chunksize=1)
+        rows = list(range(64))
+        chunks = [[rows[(i * workers + w) % 64] for i in range(n_rows_all // workers)] for w in range(workers)]
+        t0 = time.perf_counter()
+        pool.map(_oracle_rows_worker, [("mixed", {}, c, 0) for c in chunks], chunksize=1)
+        wall = time.perf_counter() - t0
+    n_done = sum(len(c) for c in chunks)
+    _pool_init("mixed", {})
+    t1 = _ORACLE_INPUT.rows(list(range(n_rows_1t)))
+    return {
+        "value": n_done / wall, "unit": "rows/s", "cores": workers, "kind": "oracle",
+        "sample": f"oracle verify (NumPy float64) on {n_done} of the 64 mixed rows, one process per host "
+                  f"core ({workers} cores from sched_getaffinity), {wall:.2f} s wall",
+        "single_thread": {"value": n_rows_1t / t1, "unit": "rows/s", "cores": 1,
+                          "sample": f"{n_rows_1t} rows in one process, {t1 * 1e3 / n_rows_1t:.1f} ms/row"},
+    }
 
 
 def run_reference(args):
+    """The reference arm of this tier: the CPU oracle on the host cores."""
     rank = int(os.environ.get("RANK", 0))
     if rank != 0:
         return
-    from speculative_decoding_verify_07_gb300 import synth
-    inp = synth.make_mixed()
-    for _ in range(args.warmup):
-        cpu_oracle_sample(inp, n_rows=2, commit_rows=1)
-    t0 = time.perf_counter()
-    per = []
-    for _ in range(args.steps):
-        per.append(cpu_oracle_sample(inp, n_rows=4, commit_rows=1))
-    el = time.perf_counter() - t0
-    value = statistics.median(p["value"] for p in per)
+    import multiprocessing as mp
+    workers = host_cores()
+    ctx = mp.get_context("spawn")
+    per_step_rows = max(workers, 8)
+    with ctx.Pool(workers, initializer=_pool_init, initargs=("mixed", {})) as pool:
+        pool.map(_pool_ready, range(4 * workers), chunksize=1)
+
+        def one_step(i):
+            rows = [(i * per_step_rows + j) % 64 for j in range(per_step_rows)]
+            chunks = [rows[w::workers] for w in range(workers) if rows[w::workers]]
+            pool.map(_oracle_rows_worker, [("mixed", {}, c, 0) for c in chunks], chunksize=1)
+            return len(rows)
+
+        for i in range(args.warmup):
+            one_step(i)
+        t0 = time.perf_counter()
+        n = 0
+        for i in range(args.steps):
+            n += one_step(args.warmup + i)
+        el = time.perf_counter() - t0
+    value = n / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "mixed verify 64x2x151936 bf16 + commit 24L x 64 rows (sampled rows)",
-                       "sample_per_step": "oracle verify on 4 rows + oracle commit of 1 row"},
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": per[0]["sample"]},
+            "config": {"workload": WORKLOAD,
+                       "sample_per_step": f"oracle verify on {per_step_rows} of the 64 rows, one process per core"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": workers, "kind": "oracle",
+                             "sample": f"{per_step_rows} rows per step over {workers} processes"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+def _time_calls(fn, n, stream):
+    """Per-call device times (us) of fn(i) for i < n, CUDA events on `stream`."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(1_000_000)
+    for i in range(n):
+        ev[i][0].record(stream)
+        fn(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def _verify_sets(make, n_sets, dev):
+    import torch
+
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    sets, inps = [], []
+    for i in range(n_sets):
+        inp = make(seed_offset=100 * i)
+        inps.append(inp)
+        dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+        sets.append((torch.from_numpy(inp.logits).to(dt).to(dev), torch.from_numpy(inp.q).to(dev),
+                     torch.from_numpy(inp.drafts).to(dev),
+                     sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev), inp.seed + i))
+    return sets, inps
+
+
+def _component(sets, inps, n_steps, warmup, dev, peak, peak_kind, name, src_hash):
+    import torch
+
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    B_, k1, V_ = sets[0][0].shape
+    ws = sv.new_workspace(B_, k1 - 1, V_, dev)
+    out = sv.VerifyOutputs(B_, k1 - 1, dev)
+    fn = lambda i: sv.spec_verify(*sets[i % len(sets)][:4], sets[i % len(sets)][4], out=out, workspace=ws)
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    t = _time_calls(fn, n_steps, torch.cuda.current_stream())
+    nbytes = statistics.mean(verify_algorithmic_bytes(x) for x in inps)
+    us = statistics.mean(t)
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"workload": name, "us": round(us, 2), "us_p50": round(statistics.median(t), 2),
+            "us_min": round(min(t), 2), "rows_per_s": round(B_ / (us * 1e-6), 1),
+            "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1), "frac": round(ach / peak, 4),
+            "peak": peak, "peak_source": peak_kind, "traffic": traffic_record(name, src_hash),
+            "mean_accept_len": float(out.accept_len.float().mean().item())}
 
 
 def run_ours(args):
@@ -306,42 +413,24 @@ def run_ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peaks()
+    v_hash = kernel_source_hash(VERIFY_SOURCES)
 
-    # ---- inputs resident in HBM ----
-    sets = []
-    inps = []
-    for i in range(N_SETS):
-        inp = synth.make_mixed(seed_offset=100 * i)
-        inps.append(inp)
-        logits = torch.from_numpy(inp.logits).to(torch.bfloat16).to(dev)
-        q = torch.from_numpy(inp.q).to(dev)
-        x = torch.from_numpy(inp.drafts).to(dev)
-        params = sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev)
-        sets.append((logits, q, x, params, inp.seed + i))
-    sh = synth.CommitShape()
-    g = torch.Generator(device=dev)
-    g.manual_seed(1004 + rank)
-    vrec = torch.empty((sh.L, sh.B, sh.S, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
-    vrec.view(torch.int32).random_(generator=g)
-    vconv = torch.randint(-32768, 32767, (sh.L, sh.B, sh.S, sh.W, sh.C), dtype=torch.int16,
-                          device=dev, generator=g)
-    crec = torch.zeros((sh.L, sh.slots, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
-    cconv = torch.zeros((sh.L, sh.slots, sh.W, sh.C), dtype=torch.int16, device=dev)
-    slot = torch.arange(sh.B, dtype=torch.int32, device=dev)
+    # ---- the bench workload, inputs resident in HBM (4 sets of 136 MB: > L2) ----
+    sets, inps = _verify_sets(synth.make_mixed, N_SETS, dev)
     ws = sv.new_workspace(B, K, V, dev)
     out = sv.VerifyOutputs(B, K, dev)
 
     def step(i):
         logits, q, x, params, seed = sets[i % N_SETS]
-        sv.spec_verify(logits, q, x, params, seed, out=out, workspace=ws)
-        sv.spec_commit(vrec, vconv, out.accept_len, slot, crec, cconv, out.flags)
+        sv.spec_verify(logits, q, x, params, seed, out=out, workspace=ws, row_base=rank * B)
 
     for i in range(max(args.warmup, 3)):
         step(i)
     torch.cuda.synchronize()
 
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     stream = torch.cuda.current_stream()
     barrier(world)
@@ -354,12 +443,9 @@ def run_ours(args):
             torch.cuda._sleep(2_000_000)
         start.record(stream)
         for i in range(n):
-            logits, q, x, params, seed = sets[i % N_SETS]
             ev[i][0].record(stream)
-            sv.spec_verify(logits, q, x, params, seed, out=out, workspace=ws)
+            step(i)
             ev[i][1].record(stream)
-            sv.spec_commit(vrec, vconv, out.accept_len, slot, crec, cconv, out.flags)
-            ev[i][2].record(stream)
         end.record(stream)
         while not end.query():   # short sleeps: the clock sampler thread runs meanwhile
             time.sleep(0.0005)
@@ -367,18 +453,15 @@ def run_ours(args):
     barrier(world)
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
     t_verify = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
-    t_commit = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
     acc = out.accept_len.cpu().numpy()
 
     # ---- end to end through the public API with host buffers ----
     pin = lambda t: t.cpu().pin_memory()
-    h_sets = [(pin(s[0]), pin(s[1]), pin(s[2]), pin(s[3]), s[4]) for s in sets]
-    h_vrec, h_vconv = pin(vrec), pin(vconv)
-    d_out = {k: torch.empty_like(getattr(out, k), device="cpu").pin_memory()
-             for k in ("tokens", "accept_len", "logprobs", "alpha", "flags")}
+    h_sets = [(pin(s_[0]), pin(s_[1]), pin(s_[2]), pin(s_[3]), s_[4]) for s_ in sets]
+    d_out = {k_: torch.empty_like(getattr(out, k_), device="cpu").pin_memory()
+             for k_ in ("tokens", "accept_len", "logprobs", "alpha", "flags")}
     e2e_steps = max(3, min(n, 10))
-    h2d = sum(t.numel() * t.element_size() for t in h_sets[0][:4]) + \
-        h_vrec.numel() * 4 + h_vconv.numel() * 2
+    h2d = sum(t.numel() * t.element_size() for t in h_sets[0][:4])
     d2h = sum(t.numel() * t.element_size() for t in d_out.values())
     dl, dq, dx, dp = (torch.empty_like(t) for t in sets[0][:4])
 
@@ -388,10 +471,7 @@ def run_ours(args):
         dq.copy_(hq, non_blocking=True)
         dx.copy_(hx, non_blocking=True)
         dp.copy_(hp, non_blocking=True)
-        vrec.copy_(h_vrec, non_blocking=True)
-        vconv.copy_(h_vconv, non_blocking=True)
-        sv.spec_verify(dl, dq, dx, dp, seed, out=out, workspace=ws)
-        sv.spec_commit(vrec, vconv, out.accept_len, slot, crec, cconv, out.flags)
+        sv.spec_verify(dl, dq, dx, dp, seed, out=out, workspace=ws, row_base=rank * B)
         for k_, t in d_out.items():
             t.copy_(getattr(out, k_), non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -409,59 +489,84 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = measured_peaks()
     vbytes = statistics.mean(verify_algorithmic_bytes(inp) for inp in inps)
-    cbytes = sh.bytes_moved(int(np.count_nonzero(acc > 0)))
     tv = statistics.mean(t_verify) * 1e-3
-    tc = statistics.mean(t_commit) * 1e-3
-    v_hash = kernel_source_hash(VERIFY_SOURCES)
-    c_hash = kernel_source_hash(["spec_commit.cu"])
-
-    def roof(name, nbytes, t, h):
-        ach = nbytes / t / 1e9
-        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
-                "traffic": traffic_record(name, h), "algorithmic_bytes": int(nbytes),
-                "avg_us": round(t * 1e6, 2)}
-
-    r_commit = roof("commit_kernel", cbytes, tc, c_hash)
-    r_verify = roof("spec_verify", vbytes, tv, v_hash)
-    dominant = r_commit if tc >= tv else r_verify
+    ach = vbytes / tv / 1e9
+    roof = {"kernel": "spec_verify", "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
+            "traffic": traffic_record("spec_verify", v_hash), "algorithmic_bytes": int(vbytes),
+            "avg_us": round(tv * 1e6, 2), "us_p50": round(statistics.median(t_verify) * 1e3, 2),
+            "us_max": round(max(t_verify) * 1e3, 2),
+            "dense_q_bytes": int(inps[0].logits.size * 2 + inps[0].q.size * 4)}
+    del sets
+    components = {"mean_accept_len_mixed": float(acc.mean())}
+    if not args.no_components:
+        # the other verify workloads (their own roofline), and the commit
+        tiny_sets, tiny_inps = _verify_sets(synth.make_tiny, 1, dev)
+        components["tiny_latency"] = _component(tiny_sets, tiny_inps, 50, 5, dev, peak, peak_kind,
+                                                "spec_verify_tiny", v_hash)
+        tp_sets, tp_inps = _verify_sets(synth.make_topp, 6, dev)
+        components["topp_16x3x157184"] = _component(tp_sets, tp_inps, 12, 3, dev, peak, peak_kind,
+                                                    "spec_verify_topp", v_hash)
+        del tp_sets
+        ad_sets, ad_inps = _verify_sets(synth.make_adversarial, 1, dev)
+        components["adversarial_256x5x151936_f32"] = _component(ad_sets, ad_inps, 5, 2, dev, peak, peak_kind,
+                                                                "spec_verify_adversarial", v_hash)
+        del ad_sets
+        components["spec_commit"] = commit_component(dev, peak, peak_kind, acc)
     value = job_rows_per_s(B * n, world, elapsed_ms * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
         "steps": n, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed_ms / n, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "verify 64 rows k=2 V=151936 bf16 mixed params (25% greedy, "
-                               "50% T0.7 top-k50 top-p0.9, 25% T1) + commit 24 layers x 64 rows "
-                               "(16x128x128 fp32 + 4x4096 bf16 per layer, 3 states)",
-                   "l2": f"verify inputs rotate over {N_SETS} sets of 136 MB; commit reads a 4.98 GB buffer",
-                   "parallelism": f"rows sharded per GPU (dp{world})"},
+        "config": {"workload": WORKLOAD,
+                   "l2": f"inputs rotate over {N_SETS} sets of 136 MB (> 129 MB L2)",
+                   "parallelism": f"rows sharded per GPU (dp{world}, row_base = rank x 64)"},
         "clocks": clk.summary(),
         "e2e": {"value": round(B * world * e2e_steps / e2e_s, 1), "unit": "rows/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": (VERIFY_LAUNCHES + 1) * n,
-        "roofline": dominant,
-        "roofline_verify": r_verify,
-        "components": {
-            "spec_verify": {"us": round(tv * 1e6, 2), "rows_per_s": round(B / tv, 1),
-                            "gbs": r_verify["achieved"], "frac": r_verify["frac"],
-                            "dense_q_model_bytes": int(inps[0].logits.size * 2 + inps[0].q.size * 4),
-                            "us_p50": round(statistics.median(t_verify) * 1e3, 2),
-                            "us_max": round(max(t_verify) * 1e3, 2)},
-            "spec_commit": {"us": round(tc * 1e6, 2), "gbs": r_commit["achieved"], "frac": r_commit["frac"],
-                            "us_p50": round(statistics.median(t_commit) * 1e3, 2),
-                            "us_max": round(max(t_commit) * 1e3, 2)},
-            "mean_accept_len": float(acc.mean()),
-        },
+        "gpu_launches": VERIFY_LAUNCHES * n,
+        "roofline": roof,
+        "components": components,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(inps[0])
+        line["cpu_baseline"] = cpu_oracle_baseline()
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def commit_component(dev, peak, peak_kind, acc_mixed):
+    """spec_commit on the 24-layer, 64-row state workload (4.98 GB verify buffer)."""
+    import torch
+
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    from speculative_decoding_verify_07_gb300 import synth
+    sh = synth.CommitShape()
+    g = torch.Generator(device=dev)
+    g.manual_seed(1004)
+    vrec = torch.empty((sh.L, sh.B, sh.S, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
+    vrec.view(torch.int32).random_(generator=g)
+    vconv = torch.randint(-32768, 32767, (sh.L, sh.B, sh.S, sh.W, sh.C), dtype=torch.int16,
+                          device=dev, generator=g)
+    crec = torch.zeros((sh.L, sh.slots, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
+    cconv = torch.zeros((sh.L, sh.slots, sh.W, sh.C), dtype=torch.int16, device=dev)
+    slot = torch.arange(sh.B, dtype=torch.int32, device=dev)
+    accl = torch.from_numpy(synth.commit_indices(sh)[0]).to(dev)
+    fn = lambda i: sv.spec_commit(vrec, vconv, accl, slot, crec, cconv)
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    t = _time_calls(fn, 10, torch.cuda.current_stream())
+    nbytes = sh.bytes_moved(int((accl > 0).sum().item()))
+    us = statistics.mean(t)
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"workload": "commit 64 rows x 24 layers (16x128x128 fp32 + 4x4096 bf16), accept_len U{1,2,3}",
+            "us": round(us, 2), "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1),
+            "frac": round(ach / peak, 4), "peak_source": peak_kind,
+            "traffic": traffic_record("commit_kernel", kernel_source_hash(["spec_commit.cu"]))}
 
 
 def run_only(args):
@@ -513,6 +618,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--only", choices=["verify", "commit"], default=None,
                     help="profiling aid: launch only one kernel per step, print its mean time")
     ap.add_argument("--layers", type=int, default=24, help="profiling aid for --only commit")

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define SPEC_ABI_VERSION 1
+#define SPEC_ABI_VERSION 2
 
 /* Largest vocabulary and draft length accepted by spec_verify. */
 #define SPEC_MAX_V 524288
@@ -84,18 +84,33 @@ enum {
   SPEC_F_BAD_TOKEN = 16,      /* a draft token outside [0, V): that draft is rejected */
   SPEC_F_BAD_PARAM = 32,      /* invalid temperature/top_p: row decoded greedily */
   SPEC_F_RESIDUAL_EMPTY = 64, /* max(p - q, 0) was all zero: drew from p instead */
-  SPEC_F_BAD_IDX = 128        /* spec_commit: accept_len or cache slot out of range */
+  SPEC_F_BAD_IDX = 128,       /* spec_commit: accept_len or cache slot out of range */
+  SPEC_F_TIMEOUT = 256        /* a bounded wait inside the kernel gave up before the
+                                 row's inputs were reduced: the row is invalid
+                                 (tokens -1, accept_len 0); see the workspace notes */
 };
 
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
  * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (the counters at the start of the 256-byte header and
- * one ticket per row) to zero and advances an epoch word in the header;
- * every record behind them carries the epoch of the call that wrote it, so
- * stale or foreign contents are never read as this call's.  One workspace
- * serves any number of later calls on one stream; two calls that may run
- * concurrently need two workspaces.                                         */
+ * must start at zero (the counters at the start of the 256-byte header, one
+ * ticket per row and two tile counters per (row, position)) to zero and
+ * advances an epoch word in the header; every record behind them carries
+ * the tag of the call that wrote it (never 0), so stale or foreign contents
+ * are never read as this call's.  One workspace serves any number of later
+ * calls on one stream (re-zero it once every 2^32 - 1 calls, when the tag
+ * comes round again); two calls that may run concurrently need two
+ * workspaces.
+ * Two words of the 256-byte header are for diagnosis and testing:
+ *   bytes 20..23  must stay 0.  A nonzero value makes the finalize of row 0
+ *                 wait for records that never arrive, so that the row comes
+ *                 back with SPEC_F_TIMEOUT after the wait's bound (a few
+ *                 hundred milliseconds); it exists to test that path.
+ *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
+ *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
+ *                 settle or finalize wait for records, 8 the row-order wait
+ *                 of batches above 256 rows, 16 the settle queue); 0 when
+ *                 every wait ended normally.                                */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.
@@ -114,9 +129,16 @@ size_t spec_verify_workspace_size(int B, int k, int V);
  *   draft_tokens  [B, k] int32 draft tokens x_j.  May be NULL when k == 0.
  *   params        [B] spec_params_t.
  *   seed          key of the Philox4x32-10 stream.  The accept uniform of
- *                 draft j in row r comes from counter (0, j, r, 0); the race
+ *                 draft j in row r comes from counter (0, j, R, 0); the race
  *                 uniform of vocabulary entry v at position j from counter
- *                 (v >> 2, j, r, 1), word v & 3; U = ((w >> 9) + 1/2) * 2^-23.
+ *                 (v >> 2, j, R, 1), word v & 3; the race uniform of the
+ *                 256-entry block b at position j from counter
+ *                 (b >> 2, j, R, 2), word b & 3; U = ((w >> 9) + 1/2) * 2^-23.
+ *                 R = row_base + r.
+ *   row_base      the stream row of this call's row 0.  A batch split into
+ *                 blocks of rows (one block per GPU, or per call) draws
+ *                 exactly what the whole batch draws in one call when every
+ *                 block passes the index of its first row here.
  * Outputs (device), all written for every row:
  *   tokens        [B, k+1] int32: x_0..x_{a-1}, then the drawn token, then -1.
  *   accept_len    [B] int32: a + 1 (accepted drafts plus the drawn token);
@@ -126,7 +148,9 @@ size_t spec_verify_workspace_size(int B, int k, int V);
  *                 decoding the raw log-softmax); 0 after the drawn token.
  *   alpha         [B, k] float32: sum_v min(p_j(v), q_j(v)) for every j.
  *                 May be NULL when k == 0.
- *   flags         [B] uint32: SPEC_F_* bits.
+ *   flags         [B] uint32: SPEC_F_* bits.  A row with SPEC_F_NAN or
+ *                 SPEC_F_TIMEOUT is invalid: tokens -1, accept_len 0,
+ *                 logprobs and alpha 0.
  * workspace / workspace_bytes: device scratch of at least
  *   spec_verify_workspace_size(B, k, V) bytes, zero-filled before first use.
  * Errors: SPEC_E_NULL, SPEC_E_DIM (B < 0, k outside [0, SPEC_MAX_K], V outside
@@ -135,9 +159,9 @@ size_t spec_verify_workspace_size(int B, int k, int V);
  * B == 0 returns SPEC_OK without enqueuing work.                             */
 int spec_verify(const void* logits, int logits_dtype, const float* draft_probs,
                 const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
-                int B, int k, int V, int32_t* tokens, int32_t* accept_len, float* logprobs,
-                float* alpha, uint32_t* flags, void* workspace, size_t workspace_bytes,
-                void* cuda_stream);
+                uint32_t row_base, int B, int k, int V, int32_t* tokens, int32_t* accept_len,
+                float* logprobs, float* alpha, uint32_t* flags, void* workspace,
+                size_t workspace_bytes, void* cuda_stream);
 
 /* spec_commit - gather each row's accepted verify state into its cache slot.
  *
@@ -167,6 +191,37 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
                 uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W,
                 int C, int slots, uint32_t* flags, void* cuda_stream);
 
+/* spec_commit_swap - the zero-copy commit: a fully accepted row trades slot
+ * numbers instead of copying its state.
+ *
+ * Source: InfiniTensor/InfiniLM PR #588, "feat: add mtp draft models for
+ * speculative decoding", section 2 item 5 (the verify forward reads the
+ * row's committed state slot and writes a scratch state slot; on full
+ * accept the two slot numbers are swapped in O(1); on partial accept the
+ * accepted position's state is brought into the committed slot -- there by
+ * replay, here by a gather from the stacked verify buffer).
+ *
+ * Layout: of the S = k + 1 states of row r, the first S - 1 are stacked in
+ *   verify_rec [L, B, S-1, H, Dk, Dv] float32 / verify_conv [L, B, S-1, W, C]
+ *   16-bit, and the last one (after every fed token) is already in cache
+ *   slot scratch_slot[r] of cache_rec [L, slots, H, Dk, Dv] / cache_conv
+ *   [L, slots, W, C], where the verify forward wrote it.
+ *   slot_of_row [B] int32 (in/out): the row's committed slot.
+ *   scratch_slot [B] int32 (in/out): the row's scratch slot.
+ * For each row r with a = accept_len[r]:
+ *   a == S      : slot_of_row[r] and scratch_slot[r] trade values (nothing is copied);
+ *   1 <= a < S  : cache[l, slot_of_row[r]] = verify[l, r, a - 1] for every layer l;
+ *   a == 0      : nothing.
+ * A row with a outside [0, S], a slot outside [0, slots), or equal committed
+ * and scratch slots gets SPEC_F_BAD_IDX in flags (if given) and is left
+ * alone.  Rows naming the same slot race.  verify_rec / verify_conv may be
+ * NULL for a state kind the model does not have, as in spec_commit.
+ * Errors: SPEC_E_NULL, SPEC_E_DIM, SPEC_E_ALIGN, SPEC_E_ARCH, SPEC_E_CUDA.  */
+int spec_commit_swap(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
+                     int32_t* slot_of_row, int32_t* scratch_slot, float* cache_rec,
+                     uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W, int C,
+                     int slots, uint32_t* flags, void* cuda_stream);
+
 /* spec_verify_noalloc - spec_verify for callers that cannot allocate device
  * memory.  The paper has no counterpart: this entry point exists for plugin
  * or custom-op hosts that pass a kernel only its inputs and outputs, for
@@ -182,9 +237,14 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
  *     per (row, position) unit per 1024 vocabulary entries, so at V = 151936
  *     about 325 units fit, e.g. 108 rows at k = 2); a larger batch returns
  *     SPEC_E_WORKSPACE and enqueues nothing.
+ *   - Arguments are checked exactly as spec_verify checks them, before
+ *     anything is enqueued: a refused call enqueues nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     (cudaGetSymbolAddress) with that device current and keeps it; make
+ *     that first call before any stream capture begins.  The kept address
+ *     belongs to the device's context at that time: after cudaDeviceReset on
+ *     that device it is stale, so do not call this entry point again in the
+ *     same process after a device reset.
  *   - Every call clears the part of the array it uses (cudaMemsetAsync on
  *     cuda_stream) before the kernel, because the array keeps the previous
  *     call's contents.
@@ -196,8 +256,9 @@ int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
 #define SPEC_NOALLOC_MAX_WORKSPACE (8u << 20)
 int spec_verify_noalloc(const void* logits, int logits_dtype, const float* draft_probs,
                         const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
-                        int B, int k, int V, int32_t* tokens, int32_t* accept_len, float* logprobs,
-                        float* alpha, uint32_t* flags, void* cuda_stream);
+                        uint32_t row_base, int B, int k, int V, int32_t* tokens,
+                        int32_t* accept_len, float* logprobs, float* alpha, uint32_t* flags,
+                        void* cuda_stream);
 
 /* Diagnostic: out[i] = Philox4x32-10(ctr[i], key = (seed mod 2^32, seed >> 32))
  * for i < n, computed by the same device function spec_verify uses.  ctr and

@@ -35,6 +35,7 @@ F_BAD_TOKEN = 16
 F_BAD_PARAM = 32
 F_RESIDUAL_EMPTY = 64
 F_BAD_IDX = 128
+F_TIMEOUT = 256
 
 SPEC_MAX_V = 524288
 SPEC_MAX_K = 16
@@ -55,11 +56,14 @@ def _load():
     vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
     lib.spec_verify_workspace_size.argtypes = [i32, i32, i32]
     lib.spec_verify_workspace_size.restype = sz
-    lib.spec_verify.argtypes = [vp, i32, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    u32 = ctypes.c_uint32
+    lib.spec_verify.argtypes = [vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.spec_verify.restype = i32
     lib.spec_commit.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
     lib.spec_commit.restype = i32
-    lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.spec_commit_swap.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
+    lib.spec_commit_swap.restype = i32
+    lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_noalloc.restype = i32
     lib.spec_philox4x32_10.argtypes = [vp, u64, vp, ctypes.c_int64, vp]
     lib.spec_philox4x32_10.restype = i32
@@ -136,11 +140,14 @@ def new_workspace(B: int, k: int, V: int, device) -> torch.Tensor:
 
 def spec_verify(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.Tensor, seed: int,
                 out: VerifyOutputs | None = None, workspace: torch.Tensor | None = None,
-                stream=None) -> VerifyOutputs:
+                stream=None, row_base: int = 0) -> VerifyOutputs:
     """Run the verify step; inputs and outputs are CUDA tensors (see spec_verify.h).
 
     logits [B, k+1, V] float32 or bfloat16; draft_probs [B, k, V] float32;
     draft_tokens [B, k] int32; params [B, 4] int32 from make_params().
+    row_base: the stream row of this batch's first row (row r draws as row
+    row_base + r), so that a batch split into row blocks reproduces the
+    whole batch's draws.
     """
     if logits.dim() != 3:
         raise ValueError("logits must be [B, k+1, V]")
@@ -165,7 +172,8 @@ def spec_verify(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.T
         workspace = new_workspace(B, k, V, dev)
     rc = LIB.spec_verify(_ptr(logits), dt, _ptr(draft_probs) if k > 0 else None,
                          _ptr(draft_tokens) if k > 0 else None, _ptr(params),
-                         ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), B, k, V,
+                         ctypes.c_uint64(int(seed) & (2 ** 64 - 1)),
+                         ctypes.c_uint32(int(row_base) & 0xFFFFFFFF), B, k, V,
                          _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.logprobs),
                          _ptr(out.alpha) if k > 0 else None, _ptr(out.flags),
                          _ptr(workspace), workspace.numel(), _stream(stream))
@@ -175,7 +183,8 @@ def spec_verify(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.T
 
 
 def spec_verify_noalloc(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.Tensor,
-                        seed: int, out: VerifyOutputs | None = None, stream=None) -> VerifyOutputs:
+                        seed: int, out: VerifyOutputs | None = None, stream=None,
+                        row_base: int = 0) -> VerifyOutputs:
     """spec_verify with the library's own scratch array instead of a workspace.
 
     For callers that cannot allocate device scratch; the library allocates
@@ -203,7 +212,8 @@ def spec_verify_noalloc(logits: torch.Tensor, draft_probs, draft_tokens, params:
         out = VerifyOutputs(B, k, dev)
     rc = LIB.spec_verify_noalloc(_ptr(logits), dt, _ptr(draft_probs) if k > 0 else None,
                                  _ptr(draft_tokens) if k > 0 else None, _ptr(params),
-                                 ctypes.c_uint64(int(seed) & (2 ** 64 - 1)), B, k, V,
+                                 ctypes.c_uint64(int(seed) & (2 ** 64 - 1)),
+                                 ctypes.c_uint32(int(row_base) & 0xFFFFFFFF), B, k, V,
                                  _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.logprobs),
                                  _ptr(out.alpha) if k > 0 else None, _ptr(out.flags), _stream(stream))
     if rc != SPEC_OK:
@@ -256,6 +266,56 @@ def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cach
                          _ptr(flags), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_commit")
+
+
+def spec_commit_swap(verify_rec, verify_conv, accept_len, slot_of_row, scratch_slot, cache_rec, cache_conv,
+                     flags=None, stream=None):
+    """Zero-copy commit (see spec_commit_swap in spec_verify.h).
+
+    verify_rec [L, B, S-1, H, Dk, Dv] float32 or None; verify_conv [L, B, S-1, W, C]
+    16-bit or None: the first S - 1 states of each row; the last state of row
+    r is already in cache slot scratch_slot[r].  slot_of_row and scratch_slot
+    [B] int32 are updated in place (a fully accepted row trades them).
+    """
+    ref = verify_rec if verify_rec is not None else verify_conv
+    if ref is None:
+        raise ValueError("nothing to commit")
+    L, B, Sm1 = ref.shape[:3]
+    S = Sm1 + 1
+    if verify_rec is not None:
+        _, _, _, H, Dk, Dv = verify_rec.shape
+        slots = cache_rec.shape[1]
+        if verify_rec.dtype != torch.float32 or cache_rec.dtype != torch.float32:
+            raise TypeError("recurrent state must be float32")
+        if tuple(cache_rec.shape) != (L, slots, H, Dk, Dv):
+            raise ValueError("cache_rec shape mismatch")
+    else:
+        H = Dk = Dv = 1
+    if verify_conv is not None:
+        _, _, _, W, C = verify_conv.shape
+        if verify_rec is None:
+            slots = cache_conv.shape[1]
+        if tuple(verify_conv.shape[:3]) != (L, B, Sm1):
+            raise ValueError("verify_conv and verify_rec disagree on [L, B, S-1]")
+        if verify_conv.element_size() != 2 or cache_conv.element_size() != 2:
+            raise TypeError("conv state must be a 16-bit type")
+        if tuple(cache_conv.shape) != (L, slots, W, C):
+            raise ValueError("cache_conv shape mismatch")
+    else:
+        W = C = 1
+    for t, nm in ((verify_rec, "verify_rec"), (verify_conv, "verify_conv"), (cache_rec, "cache_rec"),
+                  (cache_conv, "cache_conv")):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous")
+    dev = accept_len.device
+    _check(accept_len, "accept_len", torch.int32, (B,), dev)
+    _check(slot_of_row, "slot_of_row", torch.int32, (B,), dev)
+    _check(scratch_slot, "scratch_slot", torch.int32, (B,), dev)
+    rc = LIB.spec_commit_swap(_ptr(verify_rec), _ptr(verify_conv), _ptr(accept_len), _ptr(slot_of_row),
+                              _ptr(scratch_slot), _ptr(cache_rec), _ptr(cache_conv), L, B, S, H, Dk, Dv, W, C,
+                              slots, _ptr(flags), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_commit_swap")
 
 
 def philox4x32_10(ctr: torch.Tensor, seed: int, stream=None) -> torch.Tensor:

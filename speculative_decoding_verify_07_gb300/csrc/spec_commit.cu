@@ -9,6 +9,13 @@
 // a copy job is a 16 KiB chunk of one (layer, row) state blob, recurrent or
 // conv, and each CTA moves one job with 128-bit streaming loads and stores.
 // Rows whose accept_len is 0 are skipped; bad indices set SPEC_F_BAD_IDX.
+//
+// spec_commit_swap is the zero-copy variant of InfiniTensor/InfiniLM PR #588,
+// "feat: add mtp draft models for speculative decoding", section 2 item 5
+// (scratch state slot, O(1) slot swap on full accept, replay on partial
+// accept): the last state of a row already sits in its scratch cache slot,
+// so a fully accepted row only trades slot numbers, and the same kernel
+// gathers the accepted state of the other rows.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -27,12 +34,16 @@ struct CommitArgs {
   const unsigned char* vconv;
   const int32_t* accept_len;
   const int32_t* slot;
+  int32_t* swap_slot;     // swap mode: each row's committed slot (traded on full accept)
+  int32_t* swap_scratch;  // swap mode: each row's scratch slot
   unsigned char* crec;
   unsigned char* cconv;
   uint32_t* flags;
   long long rec_bytes;    // bytes of one (layer, row, state) recurrent blob
   long long conv_bytes;   // bytes of one conv blob
   int L, B, S, slots;
+  int SV;                              // states per row in the verify buffers (S, or S - 1 in swap mode)
+  int swap;
   long long rec_chunks, conv_chunks;   // chunks per blob
   int rec_vec, conv_vec;               // 16-byte vector path allowed
 };
@@ -48,17 +59,34 @@ __global__ void __launch_bounds__(kCopyThreads) commit_kernel(const CommitArgs A
   const int r = (int)(lr - (long long)l * A.B);
 
   const int acc = A.accept_len[r];
-  const int slot = A.slot ? A.slot[r] : r;
-  const bool bad = acc < 0 || acc > A.S || slot < 0 || slot >= A.slots;
-  if (A.flags && l == 0 && c == 0 && threadIdx.x == 0 && bad) atomicOr(&A.flags[r], (uint32_t)SPEC_F_BAD_IDX);
+  int slot, scratch = -1;
+  if (A.swap) {
+    // a full accept's first job trades the slots while the row's other jobs
+    // read them: either value pair passes the same range check
+    slot = A.swap_slot[r];
+    scratch = A.swap_scratch[r];
+  } else {
+    slot = A.slot ? A.slot[r] : r;
+  }
+  bool bad = acc < 0 || acc > A.S || slot < 0 || slot >= A.slots;
+  if (A.swap) bad = bad || scratch < 0 || scratch >= A.slots || scratch == slot;
+  const bool lead = l == 0 && c == 0 && threadIdx.x == 0;
+  if (A.flags && lead && bad) atomicOr(&A.flags[r], (uint32_t)SPEC_F_BAD_IDX);
   if (bad || acc == 0) return;
+  if (A.swap && acc == A.S) {
+    if (lead) {
+      A.swap_slot[r] = scratch;
+      A.swap_scratch[r] = slot;
+    }
+    return;
+  }
   const int s = acc - 1;
 
   const bool is_rec = c < A.rec_chunks;
   if (!is_rec) c -= A.rec_chunks;
   const long long blob = is_rec ? A.rec_bytes : A.conv_bytes;
   const unsigned char* src = (is_rec ? A.vrec : A.vconv) +
-                             (((long long)l * A.B + r) * A.S + s) * blob;
+                             (((long long)l * A.B + r) * A.SV + s) * blob;
   unsigned char* dst = (is_rec ? A.crec : A.cconv) + ((long long)l * A.slots + slot) * blob;
   const long long off = c * kChunk;
   const long long n = min(kChunk, blob - off);
@@ -91,11 +119,12 @@ __global__ void __launch_bounds__(kCopyThreads) commit_kernel(const CommitArgs A
 
 static inline bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
-                           const int32_t* accept_len, const int32_t* cache_slot, float* cache_rec,
-                           uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W,
-                           int C, int slots, uint32_t* flags, void* cuda_stream) {
+static int commit_launch(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
+                         const int32_t* cache_slot, int32_t* swap_slot, int32_t* swap_scratch, float* cache_rec,
+                         uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W, int C, int slots,
+                         uint32_t* flags, void* cuda_stream) {
   using namespace specv;
+  const bool swap = swap_slot != nullptr;
   if (L < 0 || B < 0 || S < 1 || slots < 0) return SPEC_E_DIM;
   if (verify_rec && (H < 1 || Dk < 1 || Dv < 1)) return SPEC_E_DIM;
   if (verify_conv && (W < 1 || C < 1)) return SPEC_E_DIM;
@@ -104,9 +133,10 @@ extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
   if (!verify_rec && !verify_conv) return SPEC_E_NULL;
   if (verify_rec && !cache_rec) return SPEC_E_NULL;
   if (verify_conv && !cache_conv) return SPEC_E_NULL;
-  if (!cache_slot && slots < B) return SPEC_E_DIM;
+  if (swap && !swap_scratch) return SPEC_E_NULL;
+  if (!swap && !cache_slot && slots < B) return SPEC_E_DIM;
   if (!aligned_to(accept_len, 4) || (cache_slot && !aligned_to(cache_slot, 4)) ||
-      (flags && !aligned_to(flags, 4)))
+      (flags && !aligned_to(flags, 4)) || (swap && (!aligned_to(swap_slot, 4) || !aligned_to(swap_scratch, 4))))
     return SPEC_E_ALIGN;
   if (verify_rec && (!aligned_to(verify_rec, 4) || !aligned_to(cache_rec, 4))) return SPEC_E_ALIGN;
   if (verify_conv && (!aligned_to(verify_conv, 2) || !aligned_to(cache_conv, 2))) return SPEC_E_ALIGN;
@@ -119,6 +149,9 @@ extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
   A.vconv = reinterpret_cast<const unsigned char*>(verify_conv);
   A.accept_len = accept_len;
   A.slot = cache_slot;
+  A.swap_slot = swap_slot;
+  A.swap_scratch = swap_scratch;
+  A.swap = swap ? 1 : 0;
   A.crec = reinterpret_cast<unsigned char*>(cache_rec);
   A.cconv = reinterpret_cast<unsigned char*>(cache_conv);
   A.flags = flags;
@@ -127,6 +160,7 @@ extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
   A.L = L;
   A.B = B;
   A.S = S;
+  A.SV = swap ? S - 1 : S;
   A.slots = slots;
   A.rec_chunks = (A.rec_bytes + kChunk - 1) / kChunk;
   A.conv_chunks = (A.conv_bytes + kChunk - 1) / kChunk;
@@ -142,4 +176,23 @@ extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
                   reinterpret_cast<cudaStream_t>(cuda_stream)>>>(A);
   if (cudaGetLastError() != cudaSuccess) return SPEC_E_CUDA;
   return SPEC_OK;
+}
+
+extern "C" int spec_commit(const float* verify_rec, const uint16_t* verify_conv,
+                           const int32_t* accept_len, const int32_t* cache_slot, float* cache_rec,
+                           uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W,
+                           int C, int slots, uint32_t* flags, void* cuda_stream) {
+  return commit_launch(verify_rec, verify_conv, accept_len, cache_slot, nullptr, nullptr, cache_rec, cache_conv, L, B,
+                       S, H, Dk, Dv, W, C, slots, flags, cuda_stream);
+}
+
+extern "C" int spec_commit_swap(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
+                                int32_t* slot_of_row, int32_t* scratch_slot, float* cache_rec,
+                                uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W, int C,
+                                int slots, uint32_t* flags, void* cuda_stream) {
+  if (L < 0 || B < 0 || S < 1 || slots < 0) return SPEC_E_DIM;
+  if (L == 0 || B == 0) return SPEC_OK;
+  if (!slot_of_row || !scratch_slot) return SPEC_E_NULL;
+  return commit_launch(verify_rec, verify_conv, accept_len, nullptr, slot_of_row, scratch_slot, cache_rec,
+                       cache_conv, L, B, S, H, Dk, Dv, W, C, slots, flags, cuda_stream);
 }

@@ -1,6 +1,6 @@
-// Device-side pieces shared by the verify kernels (sm_103a): workspace
-// layout, kernel arguments, row classification, loads, the accept test, the
-// exponential race and the per-row finalize.
+// Device-side pieces shared by the verify kernel (sm_103a): tile geometry,
+// workspace layout, kernel arguments, row classification, loads, the accept
+// test, the exponential race and the per-row finalize.
 //
 // Method: inclusionAI/AReno PR #550, "feat(engine): MTP training loss and
 // speculative decoding for bailing_v3", "What does this PR do?" Phase 2
@@ -15,6 +15,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stddef.h>
 #include <string.h>
 
 #include "../../include/spec_verify.h"
@@ -24,41 +25,66 @@ namespace specv {
 
 constexpr int kRaceBlock = 256;            // entries per block of the two-level race
 constexpr int kTopkSmall = 128;            // top_k <= this: candidate-list path
-constexpr int kMaxListCand = 1024;         // ... when the A items' candidate lists of a row fit a settle warp
-constexpr long long kSpinLimit = 1ll << 22;
+constexpr int kMaxListCand = 640;          // ... when the tiles' candidate lists of a row fit a settle warp
+// Polls of a bounded wait before it gives up (with a short sleep per poll:
+// a few hundred milliseconds in all).
+constexpr long long kSpinLimit = 1ll << 21;
 
-// Streaming geometry.  Every streaming warp owns two buffers of kSlot
-// bytes; an A item is one buffer of logits, a B item one buffer of logits
-// plus the matching draft probabilities.  Items cover whole race blocks of
-// 256 entries.
-constexpr int kSlot = 6144;
+// Tile geometry.  Every stream warp owns two shared buffers of kSlot bytes.
+// An A tile is one buffer of logits; a B tile is logits (read again, from
+// L2) plus the matching draft probabilities.  Tiles cover whole race blocks
+// of 256 entries.
+constexpr int kSlot = 8704;
 template <bool kBF16>
 struct Geo {
   static constexpr int es = kBF16 ? 2 : 4;                         // logit bytes
-  static constexpr int EA = kSlot / es;                            // A item entries (3072 / 1536)
-  static constexpr int EB = (kSlot / (es + 4)) / kRaceBlock * kRaceBlock;   // B item entries (1024 / 768)
-  static constexpr int NBA = EA / kRaceBlock;                      // blocks per A item
-  static constexpr int NBB = EB / kRaceBlock;                      // blocks per B item
+  static constexpr int EA = kBF16 ? 4352 : 2048;                   // A tile entries (17 / 8 blocks)
+  static constexpr int EB = kBF16 ? 1280 : 1024;                   // B tile entries (5 / 4 blocks)
+  static constexpr int NBA = EA / kRaceBlock;
+  static constexpr int NBB = EB / kRaceBlock;
+  static_assert(EA * es <= kSlot, "A tile exceeds a buffer");
+  static_assert(EB * (es + 4) <= kSlot, "B tile exceeds a buffer");
+  static_assert((EB * es) % 16 == 0, "q part of a B tile must start 16-byte aligned");
 };
 
 enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
 
+// Error bits of WsHeader::error (OR-ed during a call; moved to last_error by
+// the call's last CTA).
+enum {
+  ERR_STATE_WAIT = 1,      // a B tile gave up waiting for its unit's state
+  ERR_COPY_WAIT = 2,       // a tile's bulk copy did not complete
+  ERR_RECORD_WAIT = 4,     // a settle or finalize gave up waiting for records
+  ERR_ORDER_WAIT = 8,      // a CTA gave up waiting for the row order
+  ERR_QUEUE = 16           // a settle-queue wait gave up
+};
+
 struct WsHeader {
   uint32_t gnext;         // next general-path unit
   uint32_t ctas_done;     // CTAs that left the kernel
-  uint32_t error;         // bit 0: a unit-state wait gave up; bit 1: a copy wait; bit 2: a record wait; bit 3: the order wait
+  uint32_t error;         // ERR_* bits of the running call
   uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
   uint32_t next_item;     // next item of the stream sequence
-  uint32_t pad0[3];
+  uint32_t inject;        // test hook: nonzero makes the finalize of row 0 wait for a tag nothing writes
+  uint32_t last_error;    // ERR_* bits of the last completed call
+  uint32_t pad0;
   uint32_t n_class[4];    // rows per class (large batches)
   uint32_t pad[47];
-  uint32_t epoch;         // tag of the last completed call (records of this call carry epoch + 1)
+  uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
   uint32_t pad1[4];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header");
+static_assert(offsetof(WsHeader, epoch) == 236, "epoch word");
 
-// Settle groups of the general path: each half of a CTA (256 threads) runs
-// the group-wide code on its own named barrier (ids 1 and 2).
+// The tag of the call after the one tagged `epoch` (0 is never a tag, so a
+// zero-filled workspace holds no tagged word).
+__device__ __forceinline__ uint32_t next_tag(uint32_t epoch) {
+  const uint32_t t = epoch + 1u;
+  return t == 0u ? 1u : t;
+}
+
+// General-path group: the CTA's first kThreads (256) threads run the
+// group-wide code on a named barrier of their own.
 __device__ __forceinline__ int ctid() { return (int)(threadIdx.x & 255u); }
 __device__ __forceinline__ void csync() {
   asm volatile("bar.sync %0, 256;" ::"r"(1 + (int)(threadIdx.x >> 8)) : "memory");
@@ -68,29 +94,30 @@ __device__ __forceinline__ void csync() {
 // call's tag in its high half and one 32-bit value in its low half, and a
 // reader takes a word as written once it carries the current tag (aligned
 // 64-bit accesses are single-copy atomic).
-//   A record, per (unit, A item), 16 words:
-//     greedy / unfiltered: [0] chunk max (NaN when the chunk holds a NaN),
-//       [1] first index of the chunk max (greedy), [2] sum of exp2((l - m) c)
-//       relative to the chunk max, [3..7] level-1 race of the chunk's blocks
-//       relative to the chunk max (s1, t1, s2, t2, v1; bonus positions);
-//     small top-k: [2j] order key and [2j + 1] chunk-local index of one of
-//       the chunk's 8 largest entries in the total order (j < 8; the
+//   A record, per (unit, A tile), 16 words:
+//     greedy / unfiltered: [0] tile max (NaN when the tile holds a NaN, the
+//       timeout NaN when the tile's copy gave up), [1] first index of the
+//       tile max (greedy), [2] sum of exp2((l - m) c) relative to the tile
+//       max, [3..7] level-1 race of the tile's blocks relative to the tile
+//       max (s1, t1, s2, t2, v1; bonus positions);
+//     small top-k: [2j] order key and [2j + 1] tile-local index of one of
+//       the tile's 8 largest entries in the total order (j < 8; the
 //       smallest at j = 7 when there are 8; key 0 = none), with the flags
-//       kListNaN / kListPartial in word 1.
-//   B record, per (unit, B item), 8 words: [0] alpha, [1..5] level-1 race of
-//     the residual (s1, t1, s2, t2, v1).
-//   Unit state of a drafted unfiltered unit, 8 words: m, 1/Z, ln Z, the
-//     draft's logprob, accept, flags, invalid, argmax (see UnitState).
-//   Unit record of a settled unit, 8 words: the fields of UnitRecord in
-//     order (the row finaliser reads them).
+//       kListNaN / kListPartial / kListTimeout in word 1.
+//   B record, per (unit, B tile), 8 words: [0] alpha (the timeout NaN when
+//     the tile gave up), [1..5] level-1 race of the residual.
+//   Unit state of a drafted unfiltered unit, 8 words: see UnitState.
+//   Unit record of a settled unit, 8 words: see UnitRecord.
 constexpr int kRecWords = 16;
 constexpr int kBRecWords = 8;
 constexpr int kStateWords = 8;
 constexpr int kURecWords = 8;
-constexpr int kList = 8;                   // entries listed per top-k A item
-constexpr uint32_t kListNaN = 1u << 31;    // the chunk holds a NaN
-constexpr uint32_t kListPartial = 1u << 30;   // the list may miss entries above its last (re-scan the chunk)
-constexpr uint32_t kListIdx = (1u << 30) - 1u;
+constexpr int kList = 8;                   // entries listed per top-k A tile
+constexpr uint32_t kListNaN = 1u << 31;    // the tile holds a NaN
+constexpr uint32_t kListPartial = 1u << 30;   // the list may miss entries above its last (re-scan the tile)
+constexpr uint32_t kListTimeout = 1u << 29;   // the tile's copy gave up
+constexpr uint32_t kListIdx = (1u << 29) - 1u;
+constexpr uint32_t kTimeoutNaN = 0x7fbadbadu;  // a quiet NaN marking a tile that gave up
 typedef unsigned long long u64;
 __device__ __forceinline__ u64 tagw(uint32_t tag, uint32_t v) { return ((u64)tag << 32) | v; }
 __device__ __forceinline__ u64 tagf(uint32_t tag, float v) { return tagw(tag, __float_as_uint(v)); }
@@ -98,14 +125,13 @@ __device__ __forceinline__ bool tag_ok(u64 w, uint32_t tag) { return (uint32_t)(
 __device__ __forceinline__ float wf(u64 w) { return __uint_as_float((uint32_t)w); }
 __device__ __forceinline__ uint32_t wu(u64 w) { return (uint32_t)w; }
 
-struct UnitState {        // what the B items of a drafted unfiltered unit need
+struct UnitState {        // what the B tiles of a drafted unfiltered unit need
   float m, invZ, lnZ, lp_x;
   int32_t accept;
-  uint32_t flags;         // BAD_TOKEN | MARGIN_ACCEPT | BAD_PARAM of this unit
-  uint32_t invalid;       // the unit is invalid (NaN); its record is already written
+  uint32_t flags;         // BAD_TOKEN | MARGIN_ACCEPT | BAD_PARAM | TIMEOUT of this unit
+  uint32_t invalid;       // the unit is invalid (NaN or timeout); its record is already written
   int32_t am;
 };
-
 
 struct UnitRecord {       // one per unit, published as kURecWords tagged words
   uint32_t flags;
@@ -121,12 +147,12 @@ struct UnitRecord {       // one per unit, published as kURecWords tagged words
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Per-unit record counts, sized for the larger of the two logit dtypes.
-__host__ __device__ inline int max_nca(int V) { return ceil_div(V, Geo<false>::EA); }
-__host__ __device__ inline int max_ncb(int V) { return ceil_div(V, Geo<false>::EB); }
+// Per-unit record counts, sized for the logit dtype with more tiles (fp32).
+__host__ __device__ inline int max_nta(int V) { return ceil_div(V, Geo<false>::EA); }
+__host__ __device__ inline int max_ntb(int V) { return ceil_div(V, Geo<false>::EB); }
 
 struct Layout {
-  size_t row_ticket, rec, brec, ust, urec, order, total;
+  size_t row_ticket, ucnt, rec, brec, ust, urec, order, total;
 };
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
@@ -134,8 +160,9 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   Layout L;
   size_t off = sizeof(WsHeader);
   L.row_ticket = off; off = align_up(off + (size_t)B * 4, 256);
-  L.rec = off; off = align_up(off + U * max_nca(V) * kRecWords * 8, 256);
-  L.brec = off; off = align_up(off + U * max_ncb(V) * kBRecWords * 8, 256);
+  L.ucnt = off; off = align_up(off + U * 2 * 4, 256);
+  L.rec = off; off = align_up(off + U * max_nta(V) * kRecWords * 8, 256);
+  L.brec = off; off = align_up(off + U * max_ntb(V) * kBRecWords * 8, 256);
   L.ust = off; off = align_up(off + U * kStateWords * 8, 256);
   L.urec = off; off = align_up(off + U * kURecWords * 8, 256);
   L.order = off; off = align_up(off + (size_t)B * 4, 256);
@@ -155,19 +182,53 @@ struct Args {
   uint32_t* flags;
   WsHeader* ws;
   uint32_t* row_ticket;
+  uint32_t* ucnt;         // per unit: tiles done, A pass [U] then B pass [U]
   u64* rec;               // A records
   u64* brec;              // B records
   u64* ust;               // unit states of drafted unfiltered units
   u64* urec;              // unit records
   uint32_t* order;        // rows by class (batches above the shared-memory order limit)
   uint32_t key0, key1;
+  uint32_t row_base;      // row r of this call draws as row row_base + r of the stream
   int B, k, V, U;
-  int NCA, NCB;           // record strides per unit: A items, B items
+  int NTA, NTB;           // record strides per unit: A tiles, B tiles
   int n_ctas;             // CTAs of the kernel
+  int n_settle;           // settle CTAs: blocks 0, stride, 2 stride, ... (n_settle of them)
+  int settle_stride;
   int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;
 };
+
+// Timeline stamps (global timer, ns) of an instrumented build compiled with
+// SPEC_TIMELINE; empty otherwise.  Slots: per CTA start and end, per stream
+// warp first data and end, per settle warp end, per unit the last A ticket,
+// settle-A start and end, last B ticket, settle-B start and end, per row the
+// finalize, per item its end.
+enum {
+  TL_CTA_START = 0, TL_CTA_END = 160, TL_FIRST_DATA = 320, TL_STREAM_END = 2368, TL_SETTLE_END = 4416,
+  TL_ATICK = 4672, TL_SA_START = 6720, TL_SA_END = 8768, TL_BTICK = 10816, TL_SB_START = 12864,
+  TL_SB_END = 14912, TL_FINAL = 16960, TL_ITEM = 17984, TL_PHASE = 34368, TL_SIZE = 34368 + 2048 * 8
+};
+#ifdef SPEC_TIMELINE
+static __device__ unsigned long long g_tl[TL_SIZE];
+__device__ __forceinline__ void tl_stamp(int slot, int i, int lim) {
+  if (i >= 0 && i < lim) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_tl[slot + i] = t;
+  }
+}
+#define TL(slot, i, lim) tl_stamp((slot), (i), (lim))
+// phase p (0..7) of the settle of unit u
+#define TLP(u, p) do { if ((threadIdx.x & 31) == 0 && (u) < 2048) tl_stamp(TL_PHASE + (u) * 8 + (p), 0, 1); } while (0)
+#else
+#define TL(slot, i, lim) ((void)0)
+#define TLP(u, p) ((void)0)
+#endif
+
+// The row index the random streams are keyed by.
+__device__ __forceinline__ uint32_t srow(const Args& A, int row) { return A.row_base + (uint32_t)row; }
 
 // ---------------------------------------------------------------------------
 // Row configuration.
@@ -194,7 +255,7 @@ __device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
   r.c = greedy ? kLog2e : kLog2e / T;
   r.invT = greedy ? 1.0f : 1.0f / T;
   if (greedy) r.type = UT_GREEDY;
-  else if (r.K > 0 && r.K <= kTopkSmall && max_nca(V) * kList <= kMaxListCand) r.type = UT_TOPK;
+  else if (r.K > 0 && r.K <= kTopkSmall && max_nta(V) * kList <= kMaxListCand) r.type = UT_TOPK;
   else if (r.K == 0 && r.P >= 1.0f) r.type = UT_DENSE;
   else r.type = UT_GENERAL;
   return r;
@@ -279,8 +340,8 @@ __device__ __forceinline__ void load_group(const Args& A, size_t lrow, int g, bo
 __device__ __forceinline__ void load_q8(const Args& A, size_t qrow, int e0, float qv[8]) {
   const float* p = A.q + qrow;
   if (A.vec_q && e0 + 8 <= A.V) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p + e0));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p + e0 + 4));
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p + e0));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p + e0 + 4));
     qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w;
     qv[4] = b.x; qv[5] = b.y; qv[6] = b.z; qv[7] = b.w;
   } else {
@@ -299,28 +360,33 @@ __device__ __forceinline__ float group_max(const float v[8]) {
 // One warp, lane j reading unit j's record (k + 1 <= 32; bounded wait for
 // its tag): the accepted prefix ends at the first rejected draft; its tokens
 // are the drafts, then the draw of the first rejected unit (or the bonus
-// draw).
+// draw).  A row whose records did not all arrive, or that holds a unit that
+// gave up a wait, is written as invalid with SPEC_F_TIMEOUT.
 static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_t tag) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int k = A.k;
   const u64* R = A.urec + ((size_t)row * (k + 1) + lane) * kURecWords;
+  // test hook: row 0 waits for a tag that no record carries
+  const uint32_t want = (row == 0 && __ldcg(&A.ws->inject) != 0u) ? (tag ^ 0x80000000u) : tag;
   u64 w[7];
 #pragma unroll
   for (int i = 0; i < 7; ++i) w[i] = 0ull;
   long long spins = 0;
+  bool timed_out = false;
   while (true) {
     bool ok = true;
     if (lane <= k) {
 #pragma unroll
       for (int i = 0; i < 7; ++i) {
         w[i] = __ldcg(R + i);
-        ok = ok && tag_ok(w[i], tag);
+        ok = ok && tag_ok(w[i], want);
       }
     }
     if (__all_sync(full, ok)) break;
     if (++spins > kSpinLimit) {
-      if (lane == 0) atomicOr(&A.ws->error, 4u);
+      if (lane == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+      timed_out = true;
       break;
     }
     __nanosleep(64);
@@ -331,10 +397,13 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
   const int32_t y = (int32_t)wu(w[4]);
   const float lp_y = wf(w[5]);
   const uint32_t draw_flags = wu(w[6]);
-  uint32_t uflags = __reduce_or_sync(full, f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP));
+  uint32_t uflags = __reduce_or_sync(
+      full, lane <= k ? (f & (SPEC_F_NAN | SPEC_F_BAD_PARAM | SPEC_F_BAD_TOKEN | SPEC_F_MARGIN_TOPP | SPEC_F_TIMEOUT)) : 0u);
   int32_t* tok = A.tokens + (size_t)row * (k + 1);
   float* lp = A.logprobs + (size_t)row * (k + 1);
-  if (uflags & SPEC_F_NAN) {
+  if (timed_out || (uflags & (SPEC_F_NAN | SPEC_F_TIMEOUT))) {
+    const uint32_t rf = timed_out || (uflags & SPEC_F_TIMEOUT) ? (SPEC_F_TIMEOUT | (uflags & SPEC_F_NAN))
+                                                                : SPEC_F_NAN;
     if (lane <= k) {
       tok[lane] = -1;
       lp[lane] = 0.f;
@@ -342,7 +411,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
     if (lane < k) A.alpha[(size_t)row * k + lane] = 0.f;
     if (lane == 0) {
       A.accept_len[row] = 0;
-      A.flags[row] = SPEC_F_NAN;
+      A.flags[row] = rf;
     }
     return;
   }
@@ -385,6 +454,7 @@ static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, i
   old = __shfl_sync(full, old, 0);
   if (old == (uint32_t)A.k) {
     finalize_row(A, row, tag);
+    if (lane == 0) TL(TL_FINAL, row, 1024);
     if (lane == 0) A.row_ticket[row] = 0;   // leave the workspace clean for the next call
   }
   __syncwarp();
@@ -409,10 +479,8 @@ struct AcceptInfo {
   float px, qx, lx;
 };
 
-// Accept test of the draft at (row, pos): accept iff u*q(x) < p(x), with the
-// sign of u*q - p taken exactly by one fma.  p(x) = exp((l_x - m) / T) / Z
-// when x is kept (kept_th == nullptr keeps everything); greedy: p(x) = 1 if
-// x is the argmax, else 0.
+// The kept set is a prefix of the total order: entries with a larger key,
+// and the entries at the threshold key up to index tidx.
 struct Thresh {
   uint32_t tkey;
   uint32_t tidx;
@@ -421,8 +489,19 @@ __device__ __forceinline__ bool kept(const Thresh& t, uint32_t key, uint32_t v) 
   return key > t.tkey || (key == t.tkey && v <= t.tidx);
 }
 
+// The accept uniform u_j of draft `pos` in row `row`: Philox counter
+// (0, pos, row, 0), word 0.
+__device__ __forceinline__ float accept_uniform(const Args& A, int row, int pos) {
+  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, srow(A, row), 0u), A.key0, A.key1);
+  return uniform_of(w.x);
+}
+
+// Accept test of the draft at (row, pos): accept iff u*q(x) < p(x), with the
+// sign of u*q - p taken exactly by one fma.  p(x) = exp((l_x - m) / T) / Z
+// when x is kept (kept_th == nullptr keeps everything); greedy: p(x) = 1 if
+// x is the argmax, else 0.
 static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, int pos, bool bf16, bool greedy, int am,
-                                  float m, float c, float Zs, const Thresh* kept_th) {
+                                                      float m, float c, float Zs, const Thresh* kept_th) {
   AcceptInfo ai;
   ai.x = A.drafts[(size_t)row * A.k + pos];
   ai.valid = ai.x >= 0 && ai.x < A.V;
@@ -441,16 +520,17 @@ static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, in
       ai.px = in ? ex2((ai.lx - m) * c) / Zs : 0.0f;
     }
   }
-  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
-  const float u = uniform_of(w.x);
+  const float u = accept_uniform(A, row, pos);
   const float d = fmaf(u, ai.qx, -ai.px);
   ai.accept = d < 0.0f;
   ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
   return ai;
 }
 
+// Race uniform words.  Entry v at position pos: counter (v >> 2, pos, row,
+// 1), word v & 3.  Block b (level 1): counter (b >> 2, pos, row, 2), word b & 3.
 __device__ __forceinline__ uint32_t race_word(const Args& A, int row, int pos, uint32_t v) {
-  const uint4 w = philox4x32_10(make_uint4(v >> 2, (uint32_t)pos, (uint32_t)row, 1u), A.key0, A.key1);
+  const uint4 w = philox4x32_10(make_uint4(v >> 2, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
   return word_of(w, v & 3);
 }
 
@@ -465,7 +545,7 @@ __device__ __forceinline__ bool draw_margin(const Race& r) {
 // it with r_v / W_b, so v is drawn with probability r_v / sum r exactly,
 // while only one block needs a random number per entry.
 __device__ __forceinline__ uint32_t block_word(const Args& A, int row, int pos, uint32_t b) {
-  const uint4 w = philox4x32_10(make_uint4(b >> 2, (uint32_t)pos, (uint32_t)row, 2u), A.key0, A.key1);
+  const uint4 w = philox4x32_10(make_uint4(b >> 2, (uint32_t)pos, srow(A, row), 2u), A.key0, A.key1);
   return word_of(w, b & 3);
 }
 
@@ -513,8 +593,8 @@ __device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t 
 // while its loads are in flight.  *ly (if given) receives the logit of the
 // winning entry.
 template <bool kBF16>
-__device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint32_t b, float m, float c, float invZ, int mode,
-                              const Thresh* th, float* ly = nullptr) {
+__device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint32_t b, float m, float c, float invZ,
+                                           int mode, const Thresh* th, float* ly = nullptr) {
   const int lane = threadIdx.x & 31;
   const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
@@ -533,8 +613,8 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
     load_group<kBF16>(A, lrow, g, true, v);
     if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv);
     const uint32_t blk = (uint32_t)g * 2u;   // Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
-    uint4 p0 = make_uint4(blk, (uint32_t)pos, (uint32_t)row, 1u);
-    uint4 p1 = make_uint4(blk + 1u, (uint32_t)pos, (uint32_t)row, 1u);
+    uint4 p0 = make_uint4(blk, (uint32_t)pos, srow(A, row), 1u);
+    uint4 p1 = make_uint4(blk + 1u, (uint32_t)pos, srow(A, row), 1u);
     philox4x32_10_pair(p0, p1, A.key0, A.key1);
     float w[8], tq[8];
     group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
@@ -555,8 +635,6 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
   }
   return r;
 }
-
-// Level 1 over a whole row, one CTA: every warp-row of 32 groups is one race
 
 __device__ __forceinline__ void race_scale(Race& r, float sc) {
   if (r.s1 >= 0.f) r.s1 *= sc;

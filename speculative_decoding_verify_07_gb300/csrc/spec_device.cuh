@@ -141,6 +141,13 @@ __device__ __forceinline__ uint32_t load_acquire(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// A relaxed device-scope load that the compiler may not merge with another
+// (for polling a word other warps update).
+__device__ __forceinline__ uint32_t load_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void store_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -158,6 +165,13 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   float d;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
   return d;
+}
+
+// Warp-wide maximum that propagates NaN (one instruction on sm_100 and later).
+__device__ __forceinline__ float warp_max_nan(float v) {
+  float r;
+  asm("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // Packed bf16x2 maximum that propagates NaN.
@@ -240,6 +254,30 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// Transposed warp sum of N (a power of two <= 32) values per lane: lane L
+// returns the sum over all lanes of their value number L mod N.  A butterfly:
+// at each level a lane keeps the half of its values its lane bit selects
+// and adds its partner's copy of them (N - 1 shuffles), then the groups of
+// N lanes are summed.  t is overwritten.  The combination order is fixed.
+template <int N>
+__device__ __forceinline__ float warp_transpose_sum(float (&t)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = N / 2; h >= 1; h >>= 1) {
+    const bool up = (lane & h) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? t[i] : t[i + h];
+      const float keep = up ? t[i + h] : t[i];
+      t[i] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+    }
+  }
+  float r = t[0];
+#pragma unroll
+  for (int o = N; o < 32; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
 
 // ---------------------------------------------------------------------------

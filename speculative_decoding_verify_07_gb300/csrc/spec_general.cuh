@@ -11,7 +11,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "spec_verify_common.cuh"
+#include "spec_common.cuh"
 
 namespace specv {
 

@@ -1,82 +1,114 @@
 // spec_verify: the verify kernel (sm_103a).
 //
-// One persistent CTA of 16 warps per SM, launched cooperatively (all CTAs
-// resident, so warps may wait on one another).  Nothing in it waits on a
-// barrier across CTAs and nothing stores with a fence: results pass between
-// warps as 64-bit words tagged with the call's epoch, which a reader polls.
-//   * Stream warps.  Each owns two 6 KB shared-memory buffers and has the
-//     copy engine stream its next item into one (cp.async.bulk completed on
-//     an mbarrier) while it reduces the other with warp collectives.  The
-//     items of all units form one sequence, which the stream warps of all
-//     SMs take in order from one counter:
-//       A items of drafted unfiltered units, of small top-k units, of
-//       unfiltered bonus positions, of greedy units; B items of drafted
-//       unfiltered units.
-//     An A item is a chunk of one unit's logits (3072 bf16 / 1536 fp32):
-//     max, the softmax sum relative to the chunk max, for greedy units the
-//     first argmax, at a bonus position the level-1 race of the chunk's
-//     256-entry blocks, for a small top-k the chunk's 8 largest entries in
-//     the total order (the smallest last).  A B item (1024 bf16 / 768 fp32 logits, read again from
-//     L2, plus q) takes the unit state from its tagged words and computes
-//     alpha = sum min(p, q) and the level-1 race of the residual.
-//   * Settle warps (the first scheduler's warps, four per SM, on as many SMs
-//     as the tasks need).  Each takes its units in
-//     the same class order, waits for their records and settles them
-//     (spec_settle.cuh); a drafted unfiltered unit publishes its state for
-//     the B items and is finished after them.
+// One persistent CTA of 12 warps per SM, launched cooperatively (every CTA
+// is resident, so warps may wait on one another; every such wait is
+// bounded).  CTAs take one of two roles, so that each SM runs one kind of
+// code and keeps it in its instruction cache:
+//   * Stream CTAs (about 9 in 10).  Each of their 12 warps owns two 8.5 KB
+//     shared-memory buffers and has the copy engine fill one
+//     (cp.async.bulk completed on an mbarrier) while it reduces the other.
+//     The tiles of all units form one sequence of segments, taken in order
+//     from one counter:
+//       unfiltered rows in waves: A tiles of the wave's drafted positions
+//       and bonus positions, then the B tiles of the wave before;
+//       A tiles of small top-k rows; A tiles of greedy rows; the B tiles of
+//       the last unfiltered wave (placed inside the top-k or greedy tiles,
+//       a fixed number of tiles after that wave's A tiles).
+//     An A tile (4352 bf16 / 2048 fp32 logits of one unit) yields the tile
+//     max, the softmax sum relative to it, the first argmax (greedy), the
+//     level-1 race of its 256-entry blocks (bonus positions) or the 8
+//     largest entries in the total order (small top-k).  A B tile (1280 /
+//     1024 logits, read again from L2, plus q) computes alpha = sum min(p, q)
+//     and the level-1 race of the residual from the unit's published state.
+//     After a tile's record the warp adds one to the unit's tile count (a
+//     reduction nobody waits for).
+//   * Settle CTAs (about 1 in 10, every stride-th block).  Their warps take
+//     the settle tasks -- one per unit after its A tiles, one per drafted
+//     unfiltered unit after its B tiles -- in the order of the sequence,
+//     task t to settle warp t mod (warps); a warp waits for its task's tile
+//     count, settles the unit (spec_settle.cuh) and clears the count.  Tasks
+//     come in the order their tiles do, and a B tile only waits for a state
+//     that an earlier task publishes, so every wait ends.  The last settled
+//     unit of a row resolves its accept chain and writes the row's outputs.
 //   * Rows that need a global threshold search (spec_general.cuh) are taken
-//     last by half-CTA groups.
-// The last settled unit of a row resolves the accept chain and writes the
-// row's outputs.  Every wait is bounded and ends with an error bit;
-// reductions have a fixed order and no floating-point atomics are used, so
-// results are bit-reproducible.
+//     last by the CTAs' first 256 threads.
+// Results pass between warps as 64-bit words tagged with the call's epoch,
+// which a reader polls; nothing stores with a fence and no CTA waits at a
+// grid barrier.  Reductions have a fixed order and no floating-point
+// atomics are used, so results are bit-reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <mutex>
 
+#include "spec_common.cuh"
 #include "spec_general.cuh"
 #include "spec_host.h"
 #include "spec_settle.cuh"
-#include "spec_verify_common.cuh"
 
 namespace specv {
 
-constexpr int kSW = 16;                // warps per CTA
-constexpr int kAllThreads = kSW * 32;
-constexpr int kOrderSmem = 512;        // batches up to this many rows keep order and configs in shared memory
-constexpr int kStage = 64;             // per-warp staging of a top-k item's candidates
+constexpr int kNW = 12;                // warps per CTA (stream warps of a stream CTA, settle warps of a settle CTA)
+constexpr int kAllThreads = kNW * 32;
+constexpr int kOrderSmem = 256;        // batches up to this many rows keep order and configs in shared memory
+constexpr int kStage = 64;             // per-warp staging of a top-k tile's candidates
+constexpr int kMaxSeg = 128;           // segments of the item sequence
+constexpr int kMaxWaves = 40;
+constexpr int kSettleEvery = 9;        // one settle CTA per this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
-static_assert(kAllThreads == 2 * kThreads, "two general-path groups per CTA");
+static_assert(kAllThreads >= kOrderSmem, "one placement round for a shared-memory order");
+static_assert(kAllThreads >= kThreads, "the general phase uses the first kThreads threads");
+
+// A segment of the item sequence: `nrows` rows from index `first` of the
+// class order, each contributing the units at positions pos_lo ..
+// pos_lo + upr - 1, each unit `tiles` tiles of one kind.
+struct Seg {
+  uint32_t start;     // first item of the segment
+  uint32_t first;
+  uint32_t nrows;
+  uint32_t packed;    // tiles | pos_lo << 16 | upr << 21 | kind << 26 (0 A, 1 B)
+};
 
 struct OrderScratch {
   int n_class[4];
   int run[4];
-  int scan[kSW][4];
+  int scan[kNW][4];
 };
 
 struct alignas(128) VShm {
   union {
-    unsigned char buf[kSW][2][kSlot];  // stream buffers; a settle warp's pair is its top-k scratch
-    GenShm gen[2];                     // general-path groups, at the end
+    struct {
+      unsigned char buf[kNW][2][kSlot];  // stream buffers
+      u64 stage[kNW][kStage];            // top-k tile staging
+    } s;
+    TopkScratch tk[kNW];                 // settle scratch (settle CTAs)
+    GenShm gen;                          // general-path group, after the roles
   };
-  unsigned long long bar[kSW][2];
-  u64 stage[kSW][kStage];
+  unsigned long long bar[kNW][2];
+  Seg seg[kMaxSeg];
+  uint32_t tstart[kMaxSeg];              // first settle task of each segment
   uint32_t order[kOrderSmem];
   RowPack cfg[kOrderSmem];
   OrderScratch ord;
-  int gtask[2];
+  int nseg;
+  uint32_t ntasks;
+  int gtask;
   uint32_t tag;
 };
-static_assert(sizeof(GenShm) * 2 <= sizeof(unsigned char) * kSW * 2 * kSlot, "general scratch");
+
+static_assert(sizeof(VShm) <= 232448, "shared memory of a CTA exceeds 227 KB");
 
 // ---------------------------------------------------------------------------
-// Row order: rows of each class, stably, as [unfiltered][small top-k][greedy]
-// [general].
+// Row order: rows of each class, stably, as [unfiltered][small top-k]
+// [general][greedy].
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int class_rank(int cl) {
+  return cl == UT_DENSE ? 0 : (cl == UT_TOPK ? 1 : (cl == UT_GENERAL ? 2 : 3));
+}
 __device__ __forceinline__ int class_base(const OrderScratch& O, int cl) {
-  const int nD = O.n_class[UT_DENSE], nT = O.n_class[UT_TOPK], nG = O.n_class[UT_GREEDY];
-  return cl == UT_DENSE ? 0 : (cl == UT_TOPK ? nD : (cl == UT_GREEDY ? nD + nT : nD + nT + nG));
+  const int nD = O.n_class[UT_DENSE], nT = O.n_class[UT_TOPK], nX = O.n_class[UT_GENERAL];
+  const int r = class_rank(cl);
+  return r == 0 ? 0 : (r == 1 ? nD : (r == 2 ? nD + nT : nD + nT + nX));
 }
 
 // Stable placement of one round of kAllThreads rows (cl < 0: no row).
@@ -99,13 +131,11 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
   __syncthreads();
   if (tid < 4) {
     int s = 0;
-    for (int ww = 0; ww < kSW; ++ww) s += O.scan[ww][tid];
+    for (int ww = 0; ww < kNW; ++ww) s += O.scan[ww][tid];
     O.run[tid] += s;
   }
   __syncthreads();
 }
-
-static_assert(kOrderSmem == kAllThreads, "one placement round for a shared-memory order");
 
 // Batches of up to kOrderSmem rows: every CTA classifies the rows into
 // shared memory (one parameter load per row).
@@ -151,78 +181,137 @@ __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, 
 }
 
 // ---------------------------------------------------------------------------
-// Work items.
+// The item sequence.
 // ---------------------------------------------------------------------------
 struct Plan {
   const uint32_t* order;
   const RowPack* cfg;       // per-row configs in shared memory (null: classify from the parameters)
+  const Seg* seg;
+  int nseg;
   int nD, nT, nG, nX;       // rows: unfiltered, small top-k, greedy, general
-  int NCA, NCB;
-  uint32_t sDD, sTK, sDB, sB, sGR;   // segments of the item sequence
+  int NTA, NTB;             // tiles per unit of this call's dtype
 };
 
-// A work item.  kind: 0 none, 1 A item, 2 B item.
+// A work item.  kind: 0 none, 1 A tile, 2 B tile.
 struct Item {
   int kind;
+  uint32_t t;               // index in the sequence
   int reread;               // the logits are read again later (default L2 policy)
-  int row, pos, u, c, n;    // unit, chunk, valid entries in the item
+  int row, pos, u, c, n;    // unit, tile, valid entries in the tile
+  int ntiles;               // tiles of this kind in the unit
 };
 
 __device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row) {
   return P.cfg ? unpack_cfg(P.cfg[row]) : classify(A.params[row], A.V);
 }
 
+__device__ __forceinline__ Seg make_seg(uint32_t first, uint32_t nrows, int pos_lo, int upr, int tiles, int kind) {
+  Seg s;
+  s.start = 0;
+  s.first = first;
+  s.nrows = nrows;
+  s.packed = (uint32_t)tiles | ((uint32_t)pos_lo << 16) | ((uint32_t)upr << 21) | ((uint32_t)kind << 26);
+  return s;
+}
+__device__ __forceinline__ uint32_t seg_items(const Seg& s) {
+  return s.nrows * ((s.packed >> 21) & 31u) * (s.packed & 0xffffu);
+}
 
-// Item t of the sequence [A: drafted unfiltered][A: small top-k][A: bonus
-// positions][A: greedy][B: drafted unfiltered]: the states that the B items
-// need are published early, the top-k units, whose settle takes longest,
-// follow, and the greedy items run before the B items.
+// The segment table (thread 0 of every CTA builds the same one):
+//   for each wave i of unfiltered rows: A(drafts of i), A(bonus of i), then
+//   B(drafts of i - 1); A(small top-k rows); A(greedy rows), with the B tiles
+//   of the last wave inserted at a row boundary of the top-k or greedy
+//   segment at least `b_delay` items after that wave's A tiles (at the end
+//   if there are not that many).
+__device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
+                                            int NTB, uint32_t b_delay) {
+  if (threadIdx.x != 0) return;
+  const int k = A.k, k1 = A.k + 1;
+  Seg* sg = S.seg;
+  int n = 0;
+  int nw = 0, Rw = 1;
+  if (nD > 0) {
+    // a wave's A tiles are about b_delay items
+    const uint32_t row_items = (uint32_t)k1 * (uint32_t)NTA;
+    Rw = (int)max(1u, b_delay / max(1u, row_items));
+    Rw = max(Rw, ceil_div(nD, kMaxWaves));
+    nw = ceil_div(nD, Rw);
+  }
+  for (int i = 0; i < nw; ++i) {
+    const uint32_t f = (uint32_t)(i * Rw), nr = (uint32_t)min(Rw, nD - i * Rw);
+    if (k > 0) sg[n++] = make_seg(f, nr, 0, k, NTA, 0);
+    sg[n++] = make_seg(f, nr, k, 1, NTA, 0);
+    if (i >= 1 && k > 0) {
+      const uint32_t fp = (uint32_t)((i - 1) * Rw);
+      sg[n++] = make_seg(fp, (uint32_t)Rw, 0, k, NTB, 1);
+    }
+  }
+  // the remaining A segments (top-k, greedy), split once for the last B wave
+  const bool lastB = nw > 0 && k > 0;
+  const uint32_t lf = (uint32_t)((nw - 1) * Rw), lnr = lastB ? (uint32_t)(nD - (nw - 1) * Rw) : 0u;
+  uint32_t since = 0;       // items after the last wave's A tiles
+  bool placed = !lastB;
+  const uint32_t firsts[2] = {(uint32_t)nD, (uint32_t)(nD + nT + nX)};
+  const int counts[2] = {nT, nG};
+  for (int s = 0; s < 2; ++s) {
+    uint32_t f = firsts[s];
+    uint32_t nr = (uint32_t)counts[s];
+    const uint32_t per_row = (uint32_t)k1 * (uint32_t)NTA;
+    if (nr == 0) continue;
+    if (!placed && since + nr * per_row >= b_delay) {
+      const uint32_t need = b_delay > since ? b_delay - since : 0u;
+      const uint32_t r1 = min(nr, (need + per_row - 1) / per_row);
+      if (r1 > 0) sg[n++] = make_seg(f, r1, 0, k1, NTA, 0);
+      sg[n++] = make_seg(lf, lnr, 0, k, NTB, 1);
+      placed = true;
+      f += r1;
+      nr -= r1;
+      since += r1 * per_row;
+    }
+    if (nr > 0) sg[n++] = make_seg(f, nr, 0, k1, NTA, 0);
+    since += nr * per_row;
+  }
+  if (!placed) sg[n++] = make_seg(lf, lnr, 0, k, NTB, 1);
+  uint32_t start = 0, tasks = 0;
+  for (int i = 0; i < n; ++i) {
+    sg[i].start = start;
+    start += seg_items(sg[i]);
+    S.tstart[i] = tasks;
+    tasks += sg[i].nrows * ((sg[i].packed >> 21) & 31u);
+  }
+  S.nseg = n;
+  S.ntasks = tasks;
+}
+
+// Item t of the sequence.
 template <bool kBF16>
 __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
-  const int k = A.k, k1 = A.k + 1;
-  int row, pos, j;
-  uint32_t s = t;
-  it.reread = 0;
-  if (s < P.sDD) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[j / k];
-    pos = j % k;
-    it.reread = 1;
-    it.kind = 1;
-  } else if ((s -= P.sDD) < P.sTK) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[P.nD + j / k1];
-    pos = j % k1;
-    it.kind = 1;
-  } else if ((s -= P.sTK) < P.sDB) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[j];
-    pos = k;
-    it.kind = 1;
-  } else if ((s -= P.sDB) < P.sGR) {
-    j = (int)(s / (uint32_t)P.NCA);
-    it.c = (int)s - j * P.NCA;
-    row = (int)P.order[P.nD + P.nT + j / k1];
-    pos = j % k1;
-    it.kind = 1;
-  } else if ((s -= P.sGR) < P.sB) {
-    j = (int)(s / (uint32_t)P.NCB);
-    it.c = (int)s - j * P.NCB;
-    row = (int)P.order[j / k];
-    pos = j % k;
-    it.kind = 2;
-  } else {
-    return it;
+  // the last segment whose start is <= t
+  int lo = 0, hi = P.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.seg[mid].start <= t) lo = mid;
+    else hi = mid - 1;
   }
-  it.row = row;
-  it.pos = pos;
-  it.u = row * k1 + pos;
+  const Seg s = P.seg[lo];
+  it.t = t;
+  if (P.nseg == 0 || t < s.start || t - s.start >= seg_items(s)) return it;
+  const uint32_t tiles = s.packed & 0xffffu, pos_lo = (s.packed >> 16) & 31u, upr = (s.packed >> 21) & 31u;
+  const int kind = (int)((s.packed >> 26) & 1u);
+  const uint32_t off = t - s.start;
+  const uint32_t j = off / tiles;
+  it.c = (int)(off - j * tiles);
+  const uint32_t ri = j / upr;
+  it.row = (int)P.order[s.first + ri];
+  it.pos = (int)(pos_lo + (j - ri * upr));
+  it.u = it.row * (A.k + 1) + it.pos;
+  it.kind = kind == 0 ? 1 : 2;
+  it.ntiles = (int)tiles;
+  // logits of a drafted unfiltered unit are read again by its B tiles
+  it.reread = (kind == 0 && it.pos < A.k && plan_cfg(A, P, it.row).type == UT_DENSE) ? 1 : 0;
   it.n = it.kind == 1 ? min(G::EA, A.V - it.c * G::EA) : min(G::EB, A.V - it.c * G::EB);
   return it;
 }
@@ -235,7 +324,7 @@ __device__ __forceinline__ void issue(const Args& A, const Item& it, unsigned ch
   const unsigned char* lg = reinterpret_cast<const unsigned char*>(A.logits);
   fence_proxy_async();
   // inputs read once are marked evict-first in L2, so they do not push out the
-  // records, the kernels' code and the logits the B pass reads again
+  // records and the logits the B tiles read again
   const uint64_t once = l2_policy_evict_first();
   if (it.kind == 1) {
     const uint32_t bl = A.vec_logits ? ((uint32_t)(it.n * G::es) & ~15u) : 0u;
@@ -260,23 +349,25 @@ __device__ __forceinline__ void issue(const Args& A, const Item& it, unsigned ch
 __device__ __forceinline__ bool wait_buffer(const Args& A, unsigned long long* bar, uint32_t parity) {
   long long spins = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (++spins == kSpinLimit) {
-      if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, 2u);
+    if (++spins > kSpinLimit) {
+      if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, (uint32_t)ERR_COPY_WAIT);
+      return false;
     }
-    if (spins > 2 * kSpinLimit) return false;
+    if (spins > 64) __nanosleep(32);
   }
   return true;
 }
 
 // The part of an item the bulk copy did not cover: the ragged tail (read
-// with plain loads), and padding up to the end of the last block (-inf
-// logits, zero q).  With rows that are not 16-byte aligned, everything.
+// with plain loads), and padding up to the end of the tile (-inf logits,
+// zero q), so that every tile is reduced over all its blocks.  With rows
+// that are not 16-byte aligned, everything.
 template <bool kBF16>
 __device__ __noinline__ void fill_tail(const Args& A, const Item& it, unsigned char* buf) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int E = it.kind == 1 ? G::EA : G::EB;
-  const int end = ceil_div(it.n, kRaceBlock) * kRaceBlock;
+  const int end = E;
   const int done = A.vec_logits ? (int)(((uint32_t)(it.n * G::es) & ~15u) / G::es) : 0;
   const size_t lrow = (size_t)it.u * A.V + (size_t)it.c * E;
   for (int e = done + lane; e < end; e += 32) {
@@ -327,7 +418,6 @@ __device__ __forceinline__ void sload_q(const float* qb, int b, int l, float q[8
   q[4] = c.x; q[5] = c.y; q[6] = c.z; q[7] = c.w;
 }
 
-
 // Packed f32x2 arithmetic (two lanes of work per instruction).
 __device__ __forceinline__ u64 pack2(float a, float b) {
   u64 r;
@@ -360,7 +450,7 @@ __device__ __forceinline__ u64 exp_pair(float a0, float a1, u64 m2, u64 c2) {
 }
 
 // ---------------------------------------------------------------------------
-// A items.  Lane layout: bf16 lane l reads entries 8l..8l+7 of every block of
+// A tiles.  Lane layout: bf16 lane l reads entries 8l..8l+7 of every block of
 // 256 (one 16-byte shared load); fp32 lane l reads 4l..4l+3 and
 // 128+4l..128+4l+3 (two).
 // ---------------------------------------------------------------------------
@@ -393,74 +483,117 @@ __device__ __forceinline__ float a_block_max(const unsigned char* buf, int b, in
   }
 }
 
-// Greedy and unfiltered A item: the tagged record words (lanes 0..7).  The
-// max first (the lane's max and the first block reaching it, for the
-// argmax), then the softmax sum relative to it -- at a bonus position per
-// block of 256, for the level-1 race.
+// Greedy and unfiltered A tile: the tagged record words (lanes 0..7).  The
+// lane's entries of every block are held in registers (tiles are padded to
+// whole tiles): the max first (NaN-propagating; the first block reaching it
+// for the argmax), then the softmax sum relative to it -- at a bonus
+// position per block of 256, for the level-1 race.
+template <bool kBF16>
+__device__ __forceinline__ void a_block(const unsigned char* buf, int b, int lane, uint32_t (&w)[kBF16 ? 4 : 8]) {
+  if (kBF16) {
+    const uint4 x = *reinterpret_cast<const uint4*>(buf + (b * kRaceBlock + 8 * lane) * 2);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+  } else {
+    const uint4 x = *reinterpret_cast<const uint4*>(buf + (b * kRaceBlock + 4 * lane) * 4);
+    const uint4 y = *reinterpret_cast<const uint4*>(buf + (b * kRaceBlock + 128 + 4 * lane) * 4);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
+  }
+}
+// Entry j (0..7) of a lane's block words as a float.
+template <bool kBF16>
+__device__ __forceinline__ float a_val(const uint32_t* w, int j) {
+  if (kBF16) return (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
+  return __uint_as_float(w[j]);
+}
+// Max (NaN-propagating) of a lane's block words.
+template <bool kBF16>
+__device__ __forceinline__ float a_wmax(const uint32_t* w) {
+  if (kBF16) {
+    const uint32_t t = max_nan_bf16x2(max_nan_bf16x2(w[0], w[1]), max_nan_bf16x2(w[2], w[3]));
+    return max_nan(bf16_lo(t), bf16_hi(t));
+  }
+  return max_nan(max_nan(max_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                         max_nan(__uint_as_float(w[2]), __uint_as_float(w[3]))),
+                 max_nan(max_nan(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                         max_nan(__uint_as_float(w[6]), __uint_as_float(w[7]))));
+}
+// Sum of exp2((v - m) c) over a lane's 8 block entries, as two packed halves.
+template <bool kBF16>
+__device__ __forceinline__ u64 a_wexp(const uint32_t* w, u64 m2, u64 c2) {
+  const u64 e0 = exp_pair(a_val<kBF16>(w, 0), a_val<kBF16>(w, 1), m2, c2);
+  const u64 e1 = exp_pair(a_val<kBF16>(w, 2), a_val<kBF16>(w, 3), m2, c2);
+  const u64 e2 = exp_pair(a_val<kBF16>(w, 4), a_val<kBF16>(w, 5), m2, c2);
+  const u64 e3 = exp_pair(a_val<kBF16>(w, 6), a_val<kBF16>(w, 7), m2, c2);
+  return add2(add2(e0, e1), add2(e2, e3));
+}
+
 template <bool kBF16>
 __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg,
                                      const unsigned char* buf) {
   using G = Geo<kBF16>;
+  constexpr int NB = G::NBA;
+  constexpr int NW = kBF16 ? 4 : 8;
   const int lane = threadIdx.x & 31;
-  const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EA;
   const float c = cfg.c;
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && it.pos == A.k;
-  // max pass: the lane's max and the first of its blocks reaching it
+  uint32_t w[NB][NW];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) a_block<kBF16>(buf, b, lane, w[b]);
+  // the lane max, and for the argmax the first block reaching it
   float lm = -INFINITY;
   int lb = 0;
-#pragma unroll 2
-  for (int b = 0; b < nb; ++b) {
-    const float bm = a_block_max<kBF16>(buf, b, lane);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const float bm = a_wmax<kBF16>(w[b]);
     lb = bm > lm ? b : lb;
     lm = max_nan(lm, bm);
   }
-  const bool nanl = lm != lm;
-  const float mc = warp_max_f(lm);
+  const float mc = warp_max_nan(lm);
+  const bool nan = mc != mc;
   float z = 0.f;
   Race r;
   race_init(r);
   if (mc > -INFINITY && mc < INFINITY) {
+    const u64 m2 = pack2(mc, mc), c2 = pack2(c, c);
     if (!bonus) {
-      // the softmax sum relative to the chunk max
-      float z0 = 0.f, z1 = 0.f;
-#pragma unroll 2
-      for (int b = 0; b < nb; ++b) {
-        float v[8];
-        a_vals<kBF16>(buf, b, lane, v);
+      // the softmax sum relative to the tile max
+      u64 za = pack2(0.f, 0.f), zb = pack2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          z0 += ex2((v[j] - mc) * c);
-          z1 += ex2((v[j + 1] - mc) * c);
-        }
+      for (int b = 0; b < NB; b += 2) {
+        za = add2(za, a_wexp<kBF16>(w[b], m2, c2));
+        if (b + 1 < NB) zb = add2(zb, a_wexp<kBF16>(w[b + 1], m2, c2));
       }
-      z = warp_sum(z0 + z1);
+      float a0, a1, b0, b1;
+      unpack2(za, a0, a1);
+      unpack2(zb, b0, b1);
+      z = warp_sum((a0 + a1) + (b0 + b1));
     } else {
-      // block weights (one warp sum per block), then the level-1 race
-      float myW = 0.f;
-#pragma unroll 1
-      for (int b = 0; b < nb; ++b) {
-        float v[8];
-        a_vals<kBF16>(buf, b, lane, v);
-        float s8 = 0.f;
+      // block weights by a transposed warp sum, then the level-1 race
+      constexpr int NP = NB <= 8 ? 8 : (NB <= 16 ? 16 : 32);
+      float ps[NP];
+      float tot = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s8 += ex2((v[j] - mc) * c);
-        const float W = warp_sum(s8);
-        z += W;
-        if (lane == b) myW = W;
+      for (int b = 0; b < NP; ++b) {
+        float s0 = 0.f, s1 = 0.f;
+        if (b < NB) unpack2(a_wexp<kBF16>(w[b], m2, c2), s0, s1);
+        ps[b] = s0 + s1;
+        tot += ps[b];
       }
-      if (myW > 0.f) {
+      z = warp_sum(tot);
+      const float myW = warp_transpose_sum<NP>(ps);   // lane b: the weight of block b
+      if (lane < NB && myW > 0.f) {
         const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
         race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
       }
       warp_race_merge(r);
     }
   }
-  const bool nan = __any_sync(kFull, nanl);
   uint32_t idx = 0xffffffffu;
   if (greedy && !nan) {
-    // first index of the chunk max: in the lane's first block reaching it
+    // first index of the tile max: in the lane's first block reaching it
     if (lm == mc) {
       float v[8];
       a_vals<kBF16>(buf, lb, lane, v);
@@ -468,9 +601,9 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
       for (int j = 7; j >= 0; --j)
         if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(lb, lane, j));
     }
-    idx = warp_min_u32(idx);
+    idx = __reduce_min_sync(kFull, idx);
   }
-  u64* rec = A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords;
+  u64* rec = A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords;
   const uint32_t v = lane_word8(lane, nan ? 0x7fc00000u : __float_as_uint(mc), idx, __float_as_uint(z),
                                 __float_as_uint(r.s1), __float_as_uint(r.t1), __float_as_uint(r.s2),
                                 __float_as_uint(r.t2), r.v1);
@@ -478,7 +611,7 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   __syncwarp();
 }
 
-// Stages every finite entry >= t8 of the item (up to kStage; returns the
+// Stages every finite entry >= t8 of the tile (up to kStage; returns the
 // count of all), block by block.
 template <bool kBF16>
 __device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int lane, float t8, u64* stage) {
@@ -521,24 +654,24 @@ __device__ __forceinline__ u64 top8_network(u64 a, int lane) {
   return a;
 }
 
-// Small top-k A item: the chunk's kList largest entries in the total order,
-// the smallest of them last when there are kList (key, chunk-local index),
-// tagged words in lanes 0..15.  Every such entry is
-// at least the 8th largest lane maximum t8; a lane keeps up to kLaneCand of
-// its entries >= t8 (blocks whose maximum is below t8 are skipped), and a
-// lane holding more marks the list partial.
+// Small top-k A tile: the tile's kList largest entries in the total order,
+// the smallest of them last when there are kList (key, tile-local index),
+// tagged words in lanes 0..15.  Every such entry is at least the 8th largest
+// lane maximum t8; a lane keeps up to kLaneCand of its entries >= t8 (blocks
+// whose maximum is below t8 are skipped), and a lane holding more makes the
+// warp stage every entry >= t8 (beyond kStage the list is marked partial).
 constexpr int kLaneCand = 4;
 template <bool kBF16>
 __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it, const unsigned char* buf,
                                     u64* stage) {
   constexpr int NB = Geo<kBF16>::NBA;
   const int lane = threadIdx.x & 31;
-  const int nb = ceil_div(it.n, kRaceBlock);
+  const int nb = NB;   // tiles are padded to whole tiles
   float bm[NB];
   float lm = -INFINITY;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
-    bm[b] = b < nb ? a_block_max<kBF16>(buf, b, lane) : -INFINITY;
+    bm[b] = a_block_max<kBF16>(buf, b, lane);
     lm = max_nan(lm, bm[b]);
   }
   const bool nan = __any_sync(kFull, lm != lm);
@@ -624,7 +757,7 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
       __syncwarp();
     }
   }
-  // word 2j: key of entry j (0 = none); word 2j + 1: its chunk-local index
+  // word 2j: key of entry j (0 = none); word 2j + 1: its tile-local index
   const int j = lane >> 1;
   uint32_t v = 0;
   if (lane < 2 * kList) {
@@ -632,104 +765,102 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
     const u64 k = has ? stage[j] : 0ull;
     if ((lane & 1) == 0) v = has ? (uint32_t)(k >> 32) : 0u;
     else v = (has ? key64_idx(k) : kListIdx) | (j == 0 ? flags : 0u);
-    __stcg(A.rec + ((size_t)it.u * A.NCA + it.c) * kRecWords + lane, tagw(tag, v));
+    __stcg(A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords + lane, tagw(tag, v));
+  }
+  __syncwarp();
+}
+
+// The record of a tile whose copy or wait gave up: its unit is settled as
+// timed out.
+__device__ __noinline__ void timeout_record(const Args& A, uint32_t tag, const Item& it, bool topk) {
+  const int lane = threadIdx.x & 31;
+  if (it.kind == 1) {
+    u64* rec = A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords;
+    uint32_t v = 0;
+    if (topk) v = (lane & 1) ? (kListIdx | (lane == 1 ? kListTimeout : 0u)) : 0u;
+    else v = lane == 0 ? kTimeoutNaN : 0u;
+    if (lane < kRecWords) __stcg(rec + lane, tagw(tag, v));
+  } else {
+    u64* rec = A.brec + ((size_t)it.u * A.NTB + it.c) * kBRecWords;
+    if (lane < 6) __stcg(rec + lane, tagw(tag, lane == 0 ? kTimeoutNaN : 0u));
   }
   __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// B items.
+// B tiles.
 // ---------------------------------------------------------------------------
-// The unit state words of a drafted unfiltered unit (loads in flight; checked
-// by state_ready).
-__device__ __forceinline__ void state_load(const Args& A, int u, u64 (&w)[kStateWords]) {
-#pragma unroll
-  for (int i = 0; i < kStateWords; ++i) w[i] = __ldcg(A.ust + (size_t)u * kStateWords + i);
-}
-__device__ __forceinline__ bool state_ok(const u64 (&w)[kStateWords], uint32_t tag) {
-  bool ok = true;
-#pragma unroll
-  for (int i = 0; i < kStateWords; ++i) ok = ok && tag_ok(w[i], tag);
-  return ok;
-}
-__device__ __forceinline__ UnitState state_of(const u64 (&w)[kStateWords]) {
-  UnitState st;
-  st.m = wf(w[0]);
-  st.invZ = wf(w[1]);
-  st.lnZ = wf(w[2]);
-  st.lp_x = wf(w[3]);
-  st.accept = (int32_t)wu(w[4]);
-  st.flags = wu(w[5]);
-  st.invalid = wu(w[6]);
-  st.am = (int32_t)wu(w[7]);
-  return st;
-}
-
 template <bool kBF16>
-__device__ __noinline__ void b_item(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg, const UnitState& st,
+__device__ __noinline__ void b_tile(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg, const UnitState& st,
                                     const unsigned char* buf) {
   using G = Geo<kBF16>;
+  constexpr int NB = G::NBB;
+  constexpr int NP = NB <= 4 ? 4 : 8;
   const int lane = threadIdx.x & 31;
-  const int nb = ceil_div(it.n, kRaceBlock);
   const int e0 = it.c * G::EB;
   const bool need_race = !st.accept;
   const float* qb = reinterpret_cast<const float*>(buf + G::EB * G::es);
-  float alpha_c = 0.f, myW = 0.f, myU = 0.f;
   const float m = st.m, invZ = st.invZ, c = cfg.c;
+  const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
+  // the lane's entries of every block (logits and q), in registers
+  float v[NB][8], q[NB][8];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    sload<kBF16>(buf, b, lane, v[b]);
+    sload_q(qb, b, lane, q[b]);
+  }
+  float alpha_c, myW = 0.f, myQ = 0.f;
   if (!need_race) {
     // accepted draft: alpha only
-    const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
     float a0 = 0.f, a1 = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      float v[8], q[8];
-      sload<kBF16>(buf, b, lane, v);
-      sload_q(qb, b, lane, q);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         float p0, p1;
-        unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);
-        a0 += fminf(p0, q[j]);
-        a1 += fminf(p1, q[j + 1]);
+        unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);
+        a0 += fminf(p0, q[b][j]);
+        a1 += fminf(p1, q[b][j + 1]);
       }
     }
     alpha_c = warp_sum(a0 + a1);
-  }
-  if (need_race) {
-    const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
+  } else {
+    // alpha, and per block the residual weight W = sum max(p - q, 0) and
+    // the q under it (the draw margin's weight is W + 2 sum q over w > 0)
     float a8 = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      float v[8], q[8];
-      sload<kBF16>(buf, b, lane, v);
-      sload_q(qb, b, lane, q);
-      float w8 = 0.f, u8 = 0.f;
+    float wsum[NP], qsum[NP];
 #pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        float p0, p1;
-        unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
-        a8 += fminf(p0, q[j]) + fminf(p1, q[j + 1]);
-        const float w0 = p0 - q[j], w1 = p1 - q[j + 1];
-        w8 += fmaxf(w0, 0.f) + fmaxf(w1, 0.f);
-        u8 += (w0 > 0.f ? p0 + q[j] : 0.f) + (w1 > 0.f ? p1 + q[j + 1] : 0.f);
+    for (int b = 0; b < NP; ++b) {
+      float w8 = 0.f, q8 = 0.f;
+      if (b < NB) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float p0, p1;
+          unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
+          a8 += fminf(p0, q[b][j]) + fminf(p1, q[b][j + 1]);
+          const float d0 = p0 - q[b][j], d1 = p1 - q[b][j + 1];
+          w8 += fmaxf(d0, 0.f) + fmaxf(d1, 0.f);
+          q8 += (d0 > 0.f ? q[b][j] : 0.f) + (d1 > 0.f ? q[b][j + 1] : 0.f);
+        }
       }
-      const float Wb = warp_sum(w8), Ub = warp_sum(u8);
-      if (lane == b) {
-        myW = Wb;
-        myU = Ub;
-      }
+      wsum[b] = w8;
+      qsum[b] = q8;
     }
     alpha_c = warp_sum(a8);
+    myW = warp_transpose_sum<NP>(wsum);
+    myQ = warp_transpose_sum<NP>(qsum);
   }
   Race r;
   race_init(r);
-  if (need_race && myW > 0.f) {
+  if (need_race && lane < NB && myW > 0.f) {
     const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
-    race_consider(r, myW, myU - myW, blk, block_word(A, it.row, it.pos, blk));
+    race_consider(r, myW, 2.0f * myQ, blk, block_word(A, it.row, it.pos, blk));
   }
   if (need_race) warp_race_merge(r);   // accepted: the empty race as it is
-  u64* rec = A.brec + ((size_t)it.u * A.NCB + it.c) * kBRecWords;
-  const uint32_t v = lane_word8(lane, __float_as_uint(alpha_c), __float_as_uint(r.s1), __float_as_uint(r.t1),
-                                __float_as_uint(r.s2), __float_as_uint(r.t2), r.v1, 0u, 0u);
-  if (lane < 6) __stcg(rec + lane, tagw(tag, v));
+  u64* rec = A.brec + ((size_t)it.u * A.NTB + it.c) * kBRecWords;
+  const uint32_t wv = lane_word8(lane, __float_as_uint(alpha_c), __float_as_uint(r.s1), __float_as_uint(r.t1),
+                                 __float_as_uint(r.s2), __float_as_uint(r.t2), r.v1, 0u, 0u);
+  if (lane < 6) __stcg(rec + lane, tagw(tag, wv));
   __syncwarp();
 }
 
@@ -755,18 +886,19 @@ struct Bufs {
   }
 };
 
-
-// A stream warp: items of the sequence, taken in order from a shared counter.
+// A stream warp: items of the sequence, the first two by its index, later
+// ones from one counter (the next ticket is in flight while a tile is
+// reduced).  After a tile's record, one is added to the unit's tile count.
 template <bool kBF16>
-__device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int w, uint32_t gs,
-                                    uint32_t nws) {
+__device__ __noinline__ void stream_loop(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int sw, uint32_t gs,
+                                         uint32_t nws) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
   Bufs B;
-  B.a = S.buf[w][0];
-  B.b = S.buf[w][1];
-  B.ba = &S.bar[w][0];
-  B.bb = &S.bar[w][1];
+  B.a = S.s.buf[sw][0];
+  B.b = S.s.buf[sw][1];
+  B.ba = &S.bar[sw][0];
+  B.bb = &S.bar[sw][1];
   B.pa = 0u;
   B.pb = 0u;
   if (lane == 0) {
@@ -774,134 +906,173 @@ __device__ __noinline__ void stream(const Args& A, const Plan& P0, VShm& S, uint
     mbar_init(B.bb, 1);
   }
   __syncwarp();
-  // stream warp gs starts on items gs and nws + gs; later items are taken in
-  // order from one counter, one per item processed (the ticket is in flight
-  // while the item is reduced)
   Item ia = map_item<kBF16>(A, P, gs);
   Item ib = map_item<kBF16>(A, P, nws + gs);
-  if (lane == 0) {
-    issue<kBF16>(A, ia, B.a, B.ba);
-    issue<kBF16>(A, ib, B.b, B.bb);
-  }
+  // the first buffer alone: the first data arrives behind half the bytes a
+  // second copy per warp would put in flight; the second copy is posted as
+  // soon as it has (below)
+  if (lane == 0) issue<kBF16>(A, ia, B.a, B.ba);
+  bool broken = false;
+  bool first = true;
   while (ia.kind != 0) {
     uint32_t tn = 0;
-    if (lane == 0 && ib.kind != 0) tn = 2u * nws + atomicAdd(&A.ws->next_item, 1u);
+    const bool take = ib.kind != 0 && !broken;   // warp-uniform
+    if (lane == 0 && take) tn = 2u * nws + atomicAdd(&A.ws->next_item, 1u);
     const RowCfg cfg = plan_cfg(A, P, ia.row);
-    u64 sw[kStateWords];
-    if (ia.kind == 2) state_load(A, ia.u, sw);     // in flight during the copy wait
-    if (!wait_buffer(A, B.ba, B.pa)) return;
-    B.pa ^= 1u;
-    if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || (ia.n & (kRaceBlock - 1)) != 0) fill_tail<kBF16>(A, ia, B.a);
-    if (ia.kind == 1) {
-      if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, B.a, S.stage[w]);
-      else a_stats<kBF16>(A, tag, ia, cfg, B.a);
+    u64 sw8[kStateWords];
+    if (ia.kind == 2) state_load(A, ia.u, sw8);     // in flight during the copy wait
+    const bool ok = !broken && wait_buffer(A, B.ba, B.pa);
+    if (first) {
+      if (lane == 0 && ok) TL(TL_FIRST_DATA, (int)gs, 2048);
+      if (lane == 0 && ok) issue<kBF16>(A, ib, B.b, B.bb);
+      first = false;
+    }
+    if (!ok) {
+      // the buffer's copy never completed: mark this tile and stop taking new ones
+      broken = true;
+      timeout_record(A, tag, ia, cfg.type == UT_TOPK);
     } else {
-      // the unit state (bounded wait: a settle warp publishes it)
-      long long spins = 0;
-      while (!__all_sync(kFull, state_ok(sw, tag))) {
-        if (++spins > kSpinLimit) {
-          if (lane == 0) atomicOr(&A.ws->error, 1u);
-          break;
+      B.pa ^= 1u;
+      if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || ia.n != (ia.kind == 1 ? Geo<kBF16>::EA : Geo<kBF16>::EB))
+        fill_tail<kBF16>(A, ia, B.a);
+      if (ia.kind == 1) {
+        if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, B.a, S.s.stage[sw]);
+        else a_stats<kBF16>(A, tag, ia, cfg, B.a);
+      } else {
+        // the unit state (bounded wait: a settle warp publishes it)
+        long long spins = 0;
+        bool st_ok = true;
+        while (!__all_sync(kFull, state_ok(sw8, tag))) {
+          if (++spins > kSpinLimit) {
+            if (lane == 0) atomicOr(&A.ws->error, (uint32_t)ERR_STATE_WAIT);
+            st_ok = false;
+            break;
+          }
+          __nanosleep(128);
+          state_load(A, ia.u, sw8);
         }
-        __nanosleep(128);
-        state_load(A, ia.u, sw);
+        if (!st_ok) {
+          timeout_record(A, tag, ia, false);
+        } else {
+          const UnitState st = state_of(sw8);
+          if (!st.invalid) b_tile<kBF16>(A, tag, ia, cfg, st, B.a);
+        }
       }
-      const UnitState st = state_of(sw);
-      if (!st.invalid) b_item<kBF16>(A, tag, ia, cfg, st, B.a);
     }
     __syncwarp();
+    if (lane == 0) {
+      TL(TL_ITEM, (int)ia.t, 16384);
+      atomicAdd(&A.ucnt[(ia.kind == 2 ? A.U : 0) + ia.u], 1u);   // result unused: a reduction
+    }
     tn = __shfl_sync(kFull, tn, 0);
     Item in;
     in.kind = 0;
-    if (ib.kind != 0) in = map_item<kBF16>(A, P, tn);
-    if (lane == 0) issue<kBF16>(A, in, B.a, B.ba);
+    if (take) in = map_item<kBF16>(A, P, tn);   // after a failed copy: mapped, marked, not copied
+    if (lane == 0 && !broken) issue<kBF16>(A, in, B.a, B.ba);
     ia = ib;
     ib = in;
     B.rotate();
   }
+  if (lane == 0) TL(TL_STREAM_END, (int)gs, 2048);
 }
 
-// A settle warp: tasks s0, s0 + nsw, ... in the order [small top-k]
-// [drafted unfiltered: state][bonus positions][greedy][drafted unfiltered: B
-// records].  Every task before the last group waits only for A records, so
-// every state the B items wait for is published whatever the task spread.
+// Settle task t: the unit and kind (settle-A after its A tiles, settle-B
+// after its B tiles) and the tile count to wait for.
+struct Task {
+  int u, row, pos, ntiles, kind;   // kind 1: A, 2: B
+};
+__device__ __forceinline__ Task map_task(const Args& A, const Plan& P, const VShm& S, uint32_t t) {
+  int lo = 0, hi = P.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (S.tstart[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const Seg s = P.seg[lo];
+  const uint32_t upr = (s.packed >> 21) & 31u, pos_lo = (s.packed >> 16) & 31u;
+  const uint32_t j = t - S.tstart[lo];
+  const uint32_t ri = j / upr;
+  Task k;
+  k.row = (int)P.order[s.first + ri];
+  k.pos = (int)(pos_lo + (j - ri * upr));
+  k.u = k.row * (A.k + 1) + k.pos;
+  k.ntiles = (int)(s.packed & 0xffffu);
+  k.kind = ((s.packed >> 26) & 1u) ? 2 : 1;
+  return k;
+}
+
+// A settle warp: tasks g, g + nst, ... in sequence order; each waits for its
+// unit's tile count, settles the unit and clears the count.
 template <bool kBF16>
-__device__ __noinline__ void settle(const Args& A, const Plan& P, VShm& S, uint32_t tag, int w, uint32_t s0,
-                                    uint32_t nsw, uint32_t nS) {
-  const int k = A.k, k1 = A.k + 1;
-  for (uint32_t t = s0; t < nS; t += nsw) {
-    int s = (int)t, row, pos;
-    bool finish = false;
-    if (s < P.nT * k1) {
-      row = (int)P.order[P.nD + s / k1];
-      pos = s % k1;
-    } else if ((s -= P.nT * k1) < P.nD * k) {
-      row = (int)P.order[s / k];
-      pos = s % k;
-    } else if ((s -= P.nD * k) < P.nD) {
-      row = (int)P.order[s];
-      pos = k;
-    } else if ((s -= P.nD) < P.nG * k1) {
-      row = (int)P.order[P.nD + P.nT + s / k1];
-      pos = s % k1;
-    } else {
-      s -= P.nG * k1;
-      row = (int)P.order[s / k];
-      pos = s % k;
-      finish = true;
-    }
-    const int u = row * k1 + pos;
-    const RowCfg cfg = plan_cfg(A, P, row);
-    if (finish) {
-      // the published state (bounded wait), then the B records
-      u64 sw[kStateWords];
-      state_load(A, u, sw);
+__device__ __noinline__ void settle_loop(const Args& A, const Plan& P, VShm& S, uint32_t tag, int w, uint32_t g,
+                                         uint32_t nst) {
+  const int lane = threadIdx.x & 31;
+  TopkScratch& TS = S.tk[w];
+  for (uint32_t t = g; t < S.ntasks; t += nst) {
+    const Task k = map_task(A, P, S, t);
+    uint32_t* cnt = &A.ucnt[(k.kind == 2 ? A.U : 0) + k.u];
+    bool ready = true;
+    if (lane == 0) {
       long long spins = 0;
-      while (!__all_sync(kFull, state_ok(sw, tag))) {
-        if (++spins > kSpinLimit) {
-          if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, 1u);
+      while (load_relaxed(cnt) != (uint32_t)k.ntiles) {
+        if (++spins > 16ll * kSpinLimit) {
+          atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+          ready = false;
           break;
         }
-        __nanosleep(256);
-        state_load(A, u, sw);
+        __nanosleep(spins > 64 ? 128 : 32);
       }
-      const UnitState st = state_of(sw);
-      if (!st.invalid) fin_b<kBF16>(A, tag, u, row, pos, cfg, st);
-    } else if (cfg.type == UT_TOPK) {
-      topk_settle<kBF16>(A, tag, *reinterpret_cast<TopkScratch*>(S.buf[w][0]), u, row, pos, cfg);
-    } else {
-      UnitState st;
-      fin_stats<kBF16>(A, tag, u, row, pos, cfg, st);
     }
+    ready = __shfl_sync(kFull, ready ? 1 : 0, 0) != 0;
+    const RowCfg cfg = plan_cfg(A, P, k.row);
+    if (lane == 0) TL(k.kind == 2 ? TL_SB_START : TL_SA_START, k.u, 2048);
+    if (!ready) {
+      commit_record(A, tag, k.u, k.row, empty_record(SPEC_F_TIMEOUT));   // the records' polls would give up too
+    } else if (k.kind == 2) {
+      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg);
+    } else if (cfg.type == UT_TOPK) {
+      topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg);
+    } else {
+      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg);
+    }
+    if (lane == 0) {
+      TL(k.kind == 2 ? TL_SB_END : TL_SA_END, k.u, 2048);
+      *cnt = 0u;   // leave the workspace clean for the next call
+    }
+    __syncwarp();
   }
+  if (lane == 0) TL(TL_SETTLE_END, (int)g, 256);
 }
 
-// General-path units, taken by the two half-CTA groups.
+// General-path units, taken by the CTA's first kThreads threads.
 template <bool kBF16>
-__device__ __noinline__ void general_phase(const Args& A, const Plan& P, VShm& S) {
+__device__ __noinline__ void general_phase(const Args& A, const Plan& P, VShm& S, uint32_t tag) {
   const int k1 = A.k + 1;
   const int nGU = P.nX * k1;
-  const int gbase = P.nD + P.nT + P.nG;
-  const int grp = threadIdx.x >> 8;
+  const int gbase = P.nD + P.nT;
   while (true) {
-    if (ctid() == 0) S.gtask[grp] = (int)atomicAdd(&A.ws->gnext, 1u);
+    if (ctid() == 0) S.gtask = (int)atomicAdd(&A.ws->gnext, 1u);
     csync();
-    const int g = S.gtask[grp];
+    const int g = S.gtask;
     csync();
     if (g >= nGU) break;
     const int row = (int)P.order[gbase + g / k1], pos = g % k1;
-    unit_general<kBF16>(A, S.gen[grp], S.tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
+    unit_general<kBF16>(A, S.gen, tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
   }
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
+__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A, uint32_t b_delay) {
   using G = Geo<kBF16>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
   const int w = threadIdx.x >> 5;
-  if (threadIdx.x == 0) S.tag = __ldcg(&A.ws->epoch) + 1u;
+  if (threadIdx.x == 0) {
+    S.tag = next_tag(__ldcg(&A.ws->epoch));
+    S.gtask = 0;
+  }
   Plan P;
+  bool order_ok = true;
   if (!A.global_order) {
     build_order_smem(A, S.order, S.cfg, S.ord);     // synchronises the CTA
     P.order = S.order;
@@ -917,13 +1088,15 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
       long long spins = 0;
       while (load_acquire(&A.ws->order_tag) != S.tag) {
         if (++spins > kSpinLimit) {
-          atomicOr(&A.ws->error, 8u);
+          atomicOr(&A.ws->error, (uint32_t)ERR_ORDER_WAIT);
+          S.gtask = -1;
           break;
         }
         __nanosleep(128);
       }
     }
     __syncthreads();
+    order_ok = S.gtask != -1;
     P.order = A.order;
     P.cfg = nullptr;
     P.nD = (int)__ldcg(&A.ws->n_class[UT_DENSE]);
@@ -932,40 +1105,44 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
     P.nX = (int)__ldcg(&A.ws->n_class[UT_GENERAL]);
   }
   const uint32_t tag = S.tag;
-  P.NCA = ceil_div(A.V, G::EA);
-  P.NCB = ceil_div(A.V, G::EB);
-  P.sDD = (uint32_t)(P.nD * A.k * P.NCA);
-  P.sTK = (uint32_t)(P.nT * (A.k + 1) * P.NCA);
-  P.sDB = (uint32_t)(P.nD * P.NCA);
-  P.sB = (uint32_t)(P.nD * A.k * P.NCB);
-  P.sGR = (uint32_t)(P.nG * (A.k + 1) * P.NCA);
-  const uint32_t nw = (uint32_t)A.n_ctas * kSW;
-  // settle warps are the warps on the SMs' first schedulers (w % 4 == 0),
-  // four per SM: consecutive tasks (one class, neighbouring rows) settle on
-  // one SM, whose first scheduler then runs no stream warp, and the other
-  // schedulers run stream code only
-  const uint32_t g = (w & 3) == 0 ? blockIdx.x * 4u + (uint32_t)(w >> 2)
-                                   : 4u * (uint32_t)A.n_ctas + (uint32_t)((w & 3) - 1) * (4u * (uint32_t)A.n_ctas) +
-                                         (uint32_t)(w >> 2) * (uint32_t)A.n_ctas + blockIdx.x;
-  const uint32_t nS = (uint32_t)(2 * P.nD * A.k + P.nT * (A.k + 1) + P.nD + P.nG * (A.k + 1));
-  const uint32_t nsw = min(nS, nw / 4u);
-  if (g < nsw) {
-    settle<kBF16>(A, P, S, tag, w, g, nsw, nS);
-  } else {
-    stream<kBF16>(A, P, S, tag, w, g - nsw, nw - nsw);
+  P.NTA = ceil_div(A.V, G::EA);
+  P.NTB = ceil_div(A.V, G::EB);
+  build_segments(A, S, P.nD, P.nT, P.nX, P.nG, P.NTA, P.NTB, b_delay);
+  __syncthreads();
+  P.seg = S.seg;
+  P.nseg = S.nseg;
+  if (threadIdx.x == 0) TL(TL_CTA_START, (int)blockIdx.x, 160);
+  if (order_ok) {
+    const int bx = (int)blockIdx.x;
+    const bool settle_cta = (bx % A.settle_stride) == 0 && bx / A.settle_stride < A.n_settle;
+    if (settle_cta) {
+      const uint32_t nst = (uint32_t)A.n_settle * kNW;
+      settle_loop<kBF16>(A, P, S, tag, w, (uint32_t)(bx / A.settle_stride) * kNW + (uint32_t)w, nst);
+    } else {
+      // stream CTA rank: blocks before this one, minus the settle CTAs among them
+      const int srank = bx - min(A.n_settle, bx / A.settle_stride + 1);
+      const int n_stream = A.n_ctas - A.n_settle;
+      const uint32_t nws = (uint32_t)n_stream * kNW;
+      // consecutive items go to different SMs
+      stream_loop<kBF16>(A, P, S, tag, w, (uint32_t)w * (uint32_t)n_stream + (uint32_t)srank, nws);
+    }
   }
-  if (P.nX > 0) {
+  if (P.nX > 0 && order_ok) {
     __syncthreads();
-    general_phase<kBF16>(A, P, S);
+    if (threadIdx.x < kThreads) general_phase<kBF16>(A, P, S, tag);
   }
   __syncthreads();
+  if (threadIdx.x == 0) TL(TL_CTA_END, (int)blockIdx.x, 160);
   if (threadIdx.x == 0) {
     __threadfence();
     const uint32_t d = atomicAdd(&A.ws->ctas_done, 1u);
     if (d == (uint32_t)A.n_ctas - 1u) {
+      __threadfence();
       A.ws->gnext = 0u;
       A.ws->next_item = 0u;
       A.ws->ctas_done = 0u;
+      A.ws->last_error = __ldcg(&A.ws->error);
+      A.ws->error = 0u;
       A.ws->epoch = tag;
       __threadfence();
     }
@@ -975,6 +1152,10 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const Args A) {
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
+// Items of A tiles between the end of an unfiltered wave's A tiles and its
+// B tiles: the wave's settles (a few microseconds) finish meanwhile.
+constexpr uint32_t kBDelayItems = 1600;
+
 template <bool kBF16>
 int launch_verify(const Args& A0, cudaStream_t stream) {
   static std::mutex mu;
@@ -997,13 +1178,16 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
         cudaGetLastError();
         return SPEC_E_CUDA;
       }
-      cached[dev] = per_sm * sms;
+      cached[dev] = sms;   // one CTA per SM
     }
     n = cached[dev];
   }
   Args A = A0;
   A.n_ctas = n;
+  A.n_settle = n >= 2 * kSettleEvery ? n / kSettleEvery : 1;
+  A.settle_stride = n / A.n_settle;
   A.global_order = A.B > kOrderSmem ? 1 : 0;
+  uint32_t b_delay = kBDelayItems;
   // cooperative launch: every CTA is resident, so every wait between warps ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -1016,7 +1200,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, A) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, A, b_delay) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_E_CUDA;
   }
@@ -1027,3 +1211,16 @@ template int launch_verify<true>(const Args&, cudaStream_t);
 template int launch_verify<false>(const Args&, cudaStream_t);
 
 }  // namespace specv
+
+#ifdef SPEC_TIMELINE
+// Instrumented builds only: copy the timeline stamps to `out` (host,
+// TL_SIZE words) after a synchronize, and clear them.
+extern "C" int spec_timeline_read(unsigned long long* out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPEC_E_CUDA;
+  if (cudaMemcpyFromSymbol(out, specv::g_tl, sizeof(unsigned long long) * specv::TL_SIZE) != cudaSuccess)
+    return SPEC_E_CUDA;
+  static unsigned long long zero[specv::TL_SIZE];
+  if (cudaMemcpyToSymbol(specv::g_tl, zero, sizeof(zero)) != cudaSuccess) return SPEC_E_CUDA;
+  return SPEC_OK;
+}
+#endif

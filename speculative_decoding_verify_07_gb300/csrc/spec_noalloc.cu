@@ -10,13 +10,14 @@
 // file-scope device array of SPEC_NOALLOC_MAX_WORKSPACE bytes, present on
 // every GPU that loads the library until the process exits.  The caller still
 // passes every input and output buffer.  The verify step itself is the same
-// spec_verify call, handed this array as its workspace.
+// kernel spec_verify launches, handed this array as its workspace.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <mutex>
 
 #include "../../include/spec_verify.h"
+#include "spec_host.h"
 
 namespace {
 
@@ -52,23 +53,24 @@ int scratch_address(void** out) {
 
 extern "C" int spec_verify_noalloc(const void* logits, int logits_dtype, const float* draft_probs,
                                    const int32_t* draft_tokens, const spec_params_t* params,
-                                   uint64_t seed, int B, int k, int V, int32_t* tokens,
+                                   uint64_t seed, uint32_t row_base, int B, int k, int V, int32_t* tokens,
                                    int32_t* accept_len, float* logprobs, float* alpha,
                                    uint32_t* flags, void* cuda_stream) {
+  // every argument check of spec_verify first: a refused call enqueues nothing
   if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return SPEC_E_DIM;
   const size_t need = spec_verify_workspace_size(B, k, V);
   if (need > (size_t)SPEC_NOALLOC_MAX_WORKSPACE) return SPEC_E_WORKSPACE;
-  if (B == 0)
-    return spec_verify(logits, logits_dtype, draft_probs, draft_tokens, params, seed, B, k, V, tokens,
-                       accept_len, logprobs, alpha, flags, nullptr, 0, cuda_stream);
+  const int rc = specv::verify_check(logits, logits_dtype, draft_probs, draft_tokens, params, B, k, V, tokens,
+                                     accept_len, logprobs, alpha, flags, false, nullptr, 0);
+  if (rc != SPEC_OK || B == 0) return rc;
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
-  if (rc != SPEC_OK) return rc;
+  const int ra = scratch_address(&scratch);
+  if (ra != SPEC_OK) return ra;
   // The array keeps the previous call's contents; clear the part this call uses.
   if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_E_CUDA;
   }
-  return spec_verify(logits, logits_dtype, draft_probs, draft_tokens, params, seed, B, k, V, tokens,
-                     accept_len, logprobs, alpha, flags, scratch, SPEC_NOALLOC_MAX_WORKSPACE, cuda_stream);
+  return specv::verify_launch(logits, logits_dtype, draft_probs, draft_tokens, params, seed, row_base, B, k, V,
+                              tokens, accept_len, logprobs, alpha, flags, scratch, cuda_stream);
 }

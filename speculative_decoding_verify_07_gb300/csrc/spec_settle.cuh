@@ -1,54 +1,39 @@
 // spec_verify, settle code (sm_103a): what one warp does with a unit once
-// its records carry the call's tag.
+// every tile of it has been reduced (the stream warp that reduced the last
+// tile queues the unit on its CTA's settle warps).
 //
-//   greedy and unfiltered units: merge the A records in chunk order -- max,
+//   greedy and unfiltered units: merge the A records in tile order -- max,
 //     first argmax, the softmax sum rescaled to the unit max; greedy units
 //     and unfiltered bonus positions are settled at once (the bonus draw
-//     merges the chunks' level-1 block races and races the winning block's
-//     entries); a drafted unfiltered unit takes its accept test, publishes
-//     its state for the B items, then merges their records (alpha and the
-//     residual draw).
-//   small top-k units: every A item lists the 8 largest entries of its
-//     chunk in the total order, the smallest of them last.  A chunk whose
+//     merges the tiles' level-1 block races and races the winning block's
+//     entries); a drafted unfiltered unit takes its accept test and
+//     publishes its state for the B tiles; once those are reduced, its B
+//     records are merged (alpha and the residual draw).
+//   small top-k units: every A tile lists the 8 largest entries of its
+//     tile in the total order, the smallest of them last.  A tile whose
 //     smallest listed entry is below the K-th entry of the merged lists holds
 //     no further top-K entry, so the merged lists give the top-K set; other
-//     chunks are re-read from L2.  Top-p, the accept test, alpha and the draw
+//     tiles are re-read from L2.  Top-p, the accept test, alpha and the draw
 //     run on the sorted list.
 //
-// The last settled unit of a row resolves the accept chain and writes the
-// row's outputs.
+// Every record poll is bounded; a unit whose records do not all arrive, or
+// one of whose tiles gave up a wait, is settled as invalid with
+// SPEC_F_TIMEOUT.  The last settled unit of a row resolves the accept chain
+// and writes the row's outputs.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "spec_verify_common.cuh"
+#include "spec_common.cuh"
 
 namespace specv {
 
 constexpr unsigned kSettleFull = 0xffffffffu;
-// Record chunks a lane loads before merging any of them: A records in
+// Record tiles a lane loads before merging any of them: A records in
 // fin_stats, B records in fin_b (one batch each at V = 151936).
 constexpr int kFinBatchA = 2;
-constexpr int kFinBatchB = 5;
-
-// Bounded wait, by lane 0, until *p carries `tag`; every lane returns the
-// outcome.
-__device__ __forceinline__ bool wait_word(const Args& A, const u64* p, uint32_t tag) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
-    long long spins = 0;
-    while (!tag_ok(__ldcg(p), tag)) {
-      if (++spins > kSpinLimit) {
-        atomicOr(&A.ws->error, 4u);
-        ok = 0;
-        break;
-      }
-      __nanosleep(256);
-    }
-  }
-  return __shfl_sync(kSettleFull, ok, 0) != 0;
-}
+constexpr int kFinBatchB = 4;
 
 // The state of a drafted unfiltered unit as tagged words (lanes 0..7).
 __device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u, const UnitState& st) {
@@ -60,18 +45,21 @@ __device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u
 }
 
 // Warp loop guard for polling a set of words: true while another pass is
-// needed (not all lanes saw the tag); gives up after kSpinLimit passes.
-__device__ __forceinline__ bool poll_again(const Args& A, bool ok, long long& spins) {
+// needed (not all lanes saw the tag); gives up after kSpinLimit passes and
+// sets *timed_out.
+__device__ __forceinline__ bool poll_again(const Args& A, bool ok, long long& spins, bool* timed_out) {
   if (__all_sync(kSettleFull, ok)) return false;
   if (++spins > kSpinLimit) {
-    if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, 4u);
+    if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+    *timed_out = true;
     return false;
   }
-  __nanosleep(256);
+  __nanosleep(64);
   return true;
 }
 
-// The draft token of the unit and its logit and q (inputs).
+// The draft token of the unit and its logit and q (inputs, loaded before
+// the records are merged so that the loads are in flight meanwhile).
 struct Pre {
   int x, valid;
   float lx, qx;
@@ -107,14 +95,12 @@ __device__ __forceinline__ AcceptInfo accept_pre(const Args& A, int row, int pos
   ai.qx = pr.qx;
   ai.px = 0.f;
   if (ai.valid) ai.px = greedy ? (ai.x == am ? 1.0f : 0.0f) : ex2((ai.lx - m) * c) / Zs;
-  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
-  const float u = uniform_of(w.x);
+  const float u = accept_uniform(A, row, pos);
   const float d = fmaf(u, ai.qx, -ai.px);
   ai.accept = d < 0.0f;
   ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
   return ai;
 }
-
 
 // First index of the row maximum, by one warp (only for a draw that found
 // no positive weight, which a valid row does not produce).
@@ -171,26 +157,25 @@ __device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, fl
 // Greedy and unfiltered units.
 // ---------------------------------------------------------------------------
 // Merges the A records.  Greedy units and bonus positions are settled here;
-// a drafted unfiltered unit publishes its state (also returned in st) and
-// the function returns true: its B records are merged next (fin_b).
+// a drafted unfiltered unit publishes its state: its B records are merged
+// later (fin_b).
 template <bool kBF16>
-__device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg,
-                                       UnitState& st) {
+__device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && !has_q;
-  const int NC = ceil_div(A.V, G::EA);
-  const u64* R = A.rec + (size_t)u * A.NCA * kRecWords;
+  const int NT = ceil_div(A.V, G::EA);
+  const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
   const size_t lrow = (size_t)u * A.V;
   const Pre pr = load_pre<kBF16>(A, u, row, pos);   // lane 0's copy is the one used
-  // one pass over the records: each lane keeps its max, the first chunk
+  // one pass over the records: each lane keeps its max, the first tile
   // holding it, and its share of the softmax sum relative to that max
-  bool nan = false;
+  bool nan = false, tmo = false, timed_out = false;
   float m = -INFINITY, zl = 0.f;
   int cm = 0x7fffffff;
-  // words 0..7 of a batch of each lane's chunks (word 1 only for greedy
+  // words 0..7 of a batch of each lane's tiles (word 1 only for greedy
   // units, words 3..7 only for bonus positions); with one batch they stay
   // held for the bonus merge below
   u64 w[kFinBatchA][8];
@@ -198,23 +183,24 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
   for (int i = 0; i < kFinBatchA; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[i][j] = 0ull;
-  if (wait_word(A, R + (size_t)(NC - 1) * kRecWords, tag)) {
+  {
     long long spins = 0;
     bool ok;
     do {
       ok = true;
       nan = false;
+      tmo = false;
       m = -INFINITY;
       zl = 0.f;
       cm = 0x7fffffff;
-      for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
+      for (int c0 = 0; c0 < NT; c0 += 32 * kFinBatchA) {
         // the batch's words are all in flight before the first is used
 #pragma unroll
         for (int i = 0; i < kFinBatchA; ++i) {
           const int c = c0 + 32 * i + lane;
 #pragma unroll
           for (int j = 0; j < 8; ++j) w[i][j] = 0ull;
-          if (c < NC) {
+          if (c < NT) {
             const u64* r = R + (size_t)c * kRecWords;
             w[i][0] = __ldcg(r);
             w[i][2] = __ldcg(r + 2);
@@ -228,7 +214,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
 #pragma unroll
         for (int i = 0; i < kFinBatchA; ++i) {
           const int c = c0 + 32 * i + lane;
-          if (c >= NC) continue;
+          if (c >= NT) continue;
           ok = ok && tag_ok(w[i][0], tag) && tag_ok(w[i][2], tag);
           if (greedy) ok = ok && tag_ok(w[i][1], tag);
           if (bonus) {
@@ -236,7 +222,9 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
             for (int j = 3; j < 8; ++j) ok = ok && tag_ok(w[i][j], tag);
           }
           const float mc = wf(w[i][0]), zc = wf(w[i][2]);
-          if (mc != mc) {
+          if (wu(w[i][0]) == kTimeoutNaN) {
+            tmo = true;
+          } else if (mc != mc) {
             nan = true;
           } else if (mc > -INFINITY) {
             if (mc > m) {
@@ -249,23 +237,27 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
           }
         }
       }
-    } while (poll_again(A, ok, spins));
+    } while (poll_again(A, ok, spins, &timed_out));
   }
+  TLP(u, 1);
   nan = __any_sync(kSettleFull, nan);
+  tmo = __any_sync(kSettleFull, tmo) || timed_out;
   const float mw = warp_max_f(m);
   const int cfirst = (int)warp_min_u32((m == mw && cm != 0x7fffffff) ? (uint32_t)cm : 0xffffffffu);
-  const bool invalid = nan || !(mw > -INFINITY) || !(mw < INFINITY);
+  const bool invalid = tmo || nan || !(mw > -INFINITY) || !(mw < INFINITY);
   const uint32_t base_flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
   if (invalid) {
+    const uint32_t f = tmo ? SPEC_F_TIMEOUT : SPEC_F_NAN;
     if (cfg.type == UT_DENSE && has_q) {
-      // the B items skip an invalid unit
+      // the B tiles skip an invalid unit
       UnitState z;
       memset(&z, 0, sizeof(z));
       z.invalid = 1;
+      z.flags = f;
       publish_state(A, tag, u, z);
     }
-    commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
-    return false;
+    commit_record(A, tag, u, row, empty_record(f));
+    return;
   }
   const float m_lane = m;
   m = mw;
@@ -274,6 +266,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
   const float lnZ = logf(Z);
   if (greedy) {
     const int am = (int)wu(__ldcg(R + (size_t)cfirst * kRecWords + 1));
+    TLP(u, 2);
     UnitRecord rec = empty_record(base_flags);
     if (lane == 0) {
       bool need_draw = !has_q;
@@ -293,17 +286,18 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
         if (has_q && !(1.0f - q_am > 0.0f)) rec.draw_flags |= SPEC_F_RESIDUAL_EMPTY;
       }
     }
+    TLP(u, 3);
     commit_record(A, tag, u, row, rec);
-    return false;
+    return;
   }
   if (bonus) {
-    // merge the chunks' block races (scaled to the unit max), then race the
+    // merge the tiles' block races (scaled to the unit max), then race the
     // entries of the winning block
     Race a;
     race_init(a);
-    const bool held = NC <= 32 * kFinBatchA;   // w holds every chunk's words
-    for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchA) {
-      u64 x[kFinBatchA][6];   // words 0 and 3..7 of the batch's chunks
+    const bool held = NT <= 32 * kFinBatchA;   // w holds every tile's words
+    for (int c0 = 0; c0 < NT; c0 += 32 * kFinBatchA) {
+      u64 x[kFinBatchA][6];   // words 0 and 3..7 of the batch's tiles
 #pragma unroll
       for (int i = 0; i < kFinBatchA; ++i) {
         const int c = c0 + 32 * i + lane;
@@ -313,7 +307,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
           x[i][0] = w[i][0];
 #pragma unroll
           for (int j = 1; j < 6; ++j) x[i][j] = w[i][2 + j];
-        } else if (c < NC) {
+        } else if (c < NT) {
           const u64* r = R + (size_t)c * kRecWords;
           x[i][0] = __ldcg(r);
 #pragma unroll
@@ -322,7 +316,7 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       }
 #pragma unroll
       for (int i = 0; i < kFinBatchA; ++i) {
-        if (c0 + 32 * i + lane >= NC) continue;
+        if (c0 + 32 * i + lane >= NT) continue;
         const float mc = wf(x[i][0]);
         const float sc = mc > -INFINITY ? ex2((mc - m) * cfg.c) : 0.f;
         Race b;
@@ -337,8 +331,10 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       }
     }
     warp_race_merge(a);
+    TLP(u, 2);
     float ly = 0.f;
     const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
+    TLP(u, 3);
     uint32_t y = l2.v1;
     const bool drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
     if (!drawn) y = (uint32_t)row_argmax<kBF16>(A, lrow);
@@ -348,12 +344,14 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
       rec.lp_y = ((drawn ? ly : load_logit(A, kBF16, lrow + y)) - m) * cfg.invT - lnZ;
       if (draw_margin(a) || draw_margin(l2)) rec.draw_flags |= SPEC_F_MARGIN_DRAW;
     }
+    TLP(u, 4);
     commit_record(A, tag, u, row, rec);
-    return false;
+    return;
   }
-  // drafted: accept test, then publish the state for the B items
+  // drafted: accept test, then publish the state for the B tiles
   AcceptInfo ai;
   if (lane == 0) ai = accept_pre(A, row, pos, pr, false, -1, m, cfg.c, Z);
+  UnitState st;
   st.m = m;
   st.invZ = 1.0f / Z;
   st.lnZ = lnZ;
@@ -365,39 +363,78 @@ __device__ __noinline__ bool fin_stats(const Args& A, uint32_t tag, int u, int r
   st.invalid = 0;
   st.am = -1;
   publish_state(A, tag, u, st);
-  return true;
 }
 
-// A drafted unfiltered unit after its B items: alpha from the chunks' sums,
-// and after a rejection the residual draw from the chunks' level-1 races.
+// The unit state words of a drafted unfiltered unit.
+__device__ __forceinline__ void state_load(const Args& A, int u, u64 (&w)[kStateWords]) {
+#pragma unroll
+  for (int i = 0; i < kStateWords; ++i) w[i] = __ldcg(A.ust + (size_t)u * kStateWords + i);
+}
+__device__ __forceinline__ bool state_ok(const u64 (&w)[kStateWords], uint32_t tag) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < kStateWords; ++i) ok = ok && tag_ok(w[i], tag);
+  return ok;
+}
+__device__ __forceinline__ UnitState state_of(const u64 (&w)[kStateWords]) {
+  UnitState st;
+  st.m = wf(w[0]);
+  st.invZ = wf(w[1]);
+  st.lnZ = wf(w[2]);
+  st.lp_x = wf(w[3]);
+  st.accept = (int32_t)wu(w[4]);
+  st.flags = wu(w[5]);
+  st.invalid = wu(w[6]);
+  st.am = (int32_t)wu(w[7]);
+  return st;
+}
+
+// A drafted unfiltered unit after its B tiles: alpha from the tiles' sums,
+// and after a rejection the residual draw from the tiles' level-1 races.
+// The state was published before any B tile of the unit ran, so it is
+// read without a wait.
 template <bool kBF16>
-__device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg,
-                                   const UnitState& st) {
+__device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
-  const int NC = ceil_div(A.V, G::EB);
-  const u64* R = A.brec + (size_t)u * A.NCB * kBRecWords;
+  u64 sw[kStateWords];
+  state_load(A, u, sw);
+  bool timed_out = false;
+  {
+    long long spins = 0;
+    while (poll_again(A, state_ok(sw, tag), spins, &timed_out)) state_load(A, u, sw);
+  }
+  const UnitState st = state_of(sw);
+  if (timed_out) {
+    commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    return;
+  }
+  if (st.invalid) return;   // its record was committed with the state
+  const int NT = ceil_div(A.V, G::EB);
+  const u64* R = A.brec + (size_t)u * A.NTB * kBRecWords;
   const bool need_race = !st.accept;
   float al = 0.f;
+  bool tmo = false;
   Race a;
   race_init(a);
-  if (wait_word(A, R + (size_t)(NC - 1) * kBRecWords, tag)) {
+  {
     long long spins = 0;
     bool ok;
     do {
       ok = true;
       al = 0.f;
+      tmo = false;
       race_init(a);
-      // each lane's chunks lane, lane + 32, ... in batches of kFinBatchB:
+      // each lane's tiles lane, lane + 32, ... in batches of kFinBatchB:
       // the batch's words are all in flight before the first is merged
-      for (int c0 = 0; c0 < NC; c0 += 32 * kFinBatchB) {
+      for (int c0 = 0; c0 < NT; c0 += 32 * kFinBatchB) {
         u64 w[kFinBatchB][6];
 #pragma unroll
         for (int i = 0; i < kFinBatchB; ++i) {
           const int c = c0 + 32 * i + lane;
 #pragma unroll
           for (int j = 0; j < 6; ++j) w[i][j] = 0ull;
-          if (c < NC) {
+          if (c < NT) {
             const u64* r = R + (size_t)c * kBRecWords;
             w[i][0] = __ldcg(r);
             if (need_race) {
@@ -408,8 +445,9 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
         }
 #pragma unroll
         for (int i = 0; i < kFinBatchB; ++i) {
-          if (c0 + 32 * i + lane >= NC) continue;
+          if (c0 + 32 * i + lane >= NT) continue;
           ok = ok && tag_ok(w[i][0], tag);
+          if (wu(w[i][0]) == kTimeoutNaN) tmo = true;
           al += wf(w[i][0]);
           if (need_race) {
 #pragma unroll
@@ -425,7 +463,12 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
           }
         }
       }
-    } while (poll_again(A, ok, spins));
+    } while (poll_again(A, ok, spins, &timed_out));
+  }
+  TLP(u, 6);
+  if (__any_sync(kSettleFull, tmo) || timed_out) {
+    commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    return;
   }
   const float alpha_v = warp_sum(al);
   uint32_t draw_flags = 0;
@@ -447,6 +490,7 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
     }
     if (y >= (uint32_t)A.V) y = (uint32_t)row_argmax<kBF16>(A, (size_t)u * A.V);
   }
+  TLP(u, 7);
   UnitRecord rec = empty_record(st.flags);
   if (lane == 0) {
     rec.accept = st.accept;
@@ -460,6 +504,7 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
   }
   commit_record(A, tag, u, row, rec);
 }
+
 // First bin (from bin 0) where the running count over hist[0..256) reaches
 // `need` (>= 1); 256 when the total is below it.  *before = the count of the
 // bins before it.  Lane l scans bins 8l..8l+7.
@@ -574,14 +619,13 @@ static __device__ __noinline__ void warp_sort_desc(u64* s, int n) {
 // ---------------------------------------------------------------------------
 constexpr int kSel = 256;                  // candidates held for the sort
 
-// Scratch of one warp: its two stream buffers.
+// Scratch of one settle warp.
 struct TopkScratch {
-  u64 cand[kMaxListCand];                  // the A items' lists as total-order keys (0 = none)
+  u64 cand[kMaxListCand];                  // the A tiles' lists as total-order keys (0 = none)
   uint32_t hist[256];
   u64 sel[kSel];                           // the selected candidates
-  uint8_t cflag[kMaxListCand / kList];     // per chunk: bit 0 NaN, bit 1 partial list
+  uint8_t cflag[kMaxListCand / kList];     // per tile: bit 0 NaN, bit 1 partial list, bit 2 timeout
 };
-static_assert(sizeof(TopkScratch) <= 2 * kSlot, "top-k scratch exceeds a warp's stream buffers");
 
 // The list phase reuses the candidate area.
 struct ListArrays {
@@ -702,9 +746,9 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
-  const int NC = ceil_div(A.V, G::EA);
-  const int NL = NC * kList;
-  const u64* R = A.rec + (size_t)u * A.NCA * kRecWords;
+  const int NT = ceil_div(A.V, G::EA);
+  const int NL = NT * kList;
+  const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const float c = cfg.c;
@@ -717,49 +761,59 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   pr.qx = 0.f;
   if (lane == 0) pr = load_pre<kBF16>(A, u, row, pos);
 
-  // 1. the chunks' lists (raw words into the candidate area, then keys in place)
+  // 1. the tiles' lists (raw words into the candidate area, then keys in place)
   uint32_t* raw = reinterpret_cast<uint32_t*>(S.cand);
   uint8_t* cflag = S.cflag;
-  if (wait_word(A, R + (size_t)(NC - 1) * kRecWords, tag)) {
+  bool timed_out = false;
+  {
     long long spins = 0;
     bool ok;
     do {
       ok = true;
       // 8 words a lane in flight at a time
-      for (int i0 = 0; i0 < NC * kRecWords; i0 += 32 * 8) {
+      for (int i0 = 0; i0 < NT * kRecWords; i0 += 32 * 8) {
         u64 w[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int i = i0 + 32 * j + lane;
-          w[j] = i < NC * kRecWords ? __ldcg(R + i) : 0ull;
+          w[j] = i < NT * kRecWords ? __ldcg(R + i) : 0ull;
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int i = i0 + 32 * j + lane;
-          if (i < NC * kRecWords) {
+          if (i < NT * kRecWords) {
             ok = ok && tag_ok(w[j], tag);
             raw[i] = wu(w[j]);
           }
         }
       }
-    } while (poll_again(A, ok, spins));
+    } while (poll_again(A, ok, spins, &timed_out));
   }
   __syncwarp();
+  TLP(u, 1);
   for (int q = lane; q < NL; q += 32) {
     const uint32_t key = raw[2 * q];
     const uint32_t iw = raw[2 * q + 1];
     const int ch = q / kList;
-    if ((q & (kList - 1)) == 0) cflag[ch] = (uint8_t)(((iw & kListNaN) ? 1u : 0u) | ((iw & kListPartial) ? 2u : 0u));
+    if ((q & (kList - 1)) == 0)
+      cflag[ch] = (uint8_t)(((iw & kListNaN) ? 1u : 0u) | ((iw & kListPartial) ? 2u : 0u) |
+                            ((iw & kListTimeout) ? 4u : 0u));
     S.cand[q] = key ? key64(key, (uint32_t)(ch * G::EA) + (iw & kListIdx)) : 0ull;
   }
   __syncwarp();
-  bool nan = false, any_partial = false;
-  for (int ch = lane; ch < NC; ch += 32) {
+  bool nan = false, any_partial = false, tmo = timed_out;
+  for (int ch = lane; ch < NT; ch += 32) {
     nan |= (cflag[ch] & 1u) != 0;
     any_partial |= (cflag[ch] & 2u) != 0;
+    tmo |= (cflag[ch] & 4u) != 0;
   }
   nan = __any_sync(kSettleFull, nan);
   any_partial = __any_sync(kSettleFull, any_partial);
+  tmo = __any_sync(kSettleFull, tmo);
+  if (tmo) {
+    commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    return;
+  }
   unsigned long long top = 0;
   for (int q = lane; q < NL; q += 32) top = S.cand[q] > top ? S.cand[q] : top;
   top = warp_max_u64(top);
@@ -817,16 +871,16 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   bool exact = n_c <= (uint32_t)kSel;
   if (exact) {
     warp_sort_desc(S.sel, (int)n_c);
-    // a chunk whose list is full and ends above the K-th entry may hold more
+    // a tile whose list is full and ends above the K-th entry may hold more
     const u64 kappa = (int)n_c >= K ? S.sel[K - 1] : 0ull;
     bool unsafe = false;
-    for (int ch = lane; ch < NC; ch += 32) {
+    for (int ch = lane; ch < NT; ch += 32) {
       const u64 last = S.cand[ch * kList + kList - 1];
       unsafe |= (cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa);
     }
     if (__any_sync(kSettleFull, unsafe)) {
-      // re-read those chunks: their entries at or above kappa join the listed
-      // entries at or above kappa of the other chunks
+      // re-read those tiles: their entries at or above kappa join the listed
+      // entries at or above kappa of the other tiles
       uint32_t n = 0;
       for (int base = 0; base < NL; base += 32) {
         const int q = base + lane;
@@ -842,7 +896,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       }
       const uint32_t kk = (uint32_t)(kappa >> 32);
       const uint32_t T = max(kk, okey(-INFINITY) + 1u);
-      for (int ch = 0; ch < NC; ++ch) {
+      for (int ch = 0; ch < NT; ++ch) {
         const u64 last = S.cand[ch * kList + kList - 1];
         if (!((cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa))) continue;
         const int g0 = ch * (G::EA / 8);
@@ -877,6 +931,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     n_k = min(n, K);
   }
 
+  TLP(u, 2);
   // 3. the list: entry i = 32 r + lane in round r, arrays in shared memory
   ListArrays& L = *reinterpret_cast<ListArrays*>(S.cand);
   const int nr = (n_k + 31) >> 5;
@@ -965,13 +1020,13 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     ai.px = hb ? exx / Zs : 0.f;
     ai.qx = pr.qx;
     ai.lx = pr.lx;
-    const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)row, 0u), A.key0, A.key1);
-    const float uu = uniform_of(w.x);
+    const float uu = accept_uniform(A, row, pos);
     const float d = fmaf(uu, ai.qx, -ai.px);
     ai.accept = d < 0.0f;
     ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
     need_race = !ai.accept;
   }
+  TLP(u, 3);
   // 4. the draw: the two-level race over the kept entries (blocks by index)
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
@@ -1076,6 +1131,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       break;
     }
   }
+  TLP(u, 4);
   // the logit of the drawn entry, from the list
   float vy = m;
   {
@@ -1108,6 +1164,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       rec.draw_flags = draw_flags;
     }
   }
+  TLP(u, 5);
   commit_record(A, tag, u, row, rec);
 }
 

@@ -23,7 +23,7 @@ def lib():
         build.build()
     L = ctypes.CDLL(LIB)
     vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
-    L.spec_verify.argtypes = [vp, i32, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_verify.argtypes = [vp, i32, vp, vp, vp, u64, ctypes.c_uint32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_verify.restype = i32
     L.spec_commit.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
     L.spec_commit.restype = i32
@@ -55,7 +55,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.spec_version() == 1
+    assert lib.spec_version() == 2
     for code in range(0, -8, -1):
         s = lib.spec_status_string(code).decode()
         assert s and s != "unknown status code"
@@ -71,11 +71,11 @@ P = 4096   # a fake, aligned, non-null address; validation fails before any dere
 
 
 def _verify(lib, **kw):
-    a = dict(logits=P, dt=1, q=P, x=P, params=P, seed=0, B=4, k=2, V=1000, tok=P, acc=P, lp=P,
-             alpha=P, flags=P, ws=P, wsb=1 << 20, stream=None)
+    a = dict(logits=P, dt=1, q=P, x=P, params=P, seed=0, row_base=0, B=4, k=2, V=1000, tok=P, acc=P,
+             lp=P, alpha=P, flags=P, ws=P, wsb=1 << 20, stream=None)
     a.update(kw)
-    return lib.spec_verify(a["logits"], a["dt"], a["q"], a["x"], a["params"], a["seed"], a["B"],
-                           a["k"], a["V"], a["tok"], a["acc"], a["lp"], a["alpha"], a["flags"],
+    return lib.spec_verify(a["logits"], a["dt"], a["q"], a["x"], a["params"], a["seed"], a["row_base"],
+                           a["B"], a["k"], a["V"], a["tok"], a["acc"], a["lp"], a["alpha"], a["flags"],
                            a["ws"], a["wsb"], a["stream"])
 
 
@@ -96,6 +96,32 @@ def test_verify_argument_errors(lib):
     assert _verify(lib, wsb=16) == -5
     # valid arguments reach the CUDA runtime, which has no device here
     assert _verify(lib) in (-6, -7)
+    assert _verify(lib, row_base=2 ** 32 - 1) in (-6, -7)
+
+
+def _noalloc(lib, **kw):
+    vp, i32, u32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64
+    lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_noalloc.restype = i32
+    a = dict(logits=P, dt=1, q=P, x=P, params=P, seed=0, row_base=0, B=4, k=2, V=1000, tok=P, acc=P,
+             lp=P, alpha=P, flags=P, stream=None)
+    a.update(kw)
+    return lib.spec_verify_noalloc(a["logits"], a["dt"], a["q"], a["x"], a["params"], a["seed"],
+                                   a["row_base"], a["B"], a["k"], a["V"], a["tok"], a["acc"], a["lp"],
+                                   a["alpha"], a["flags"], a["stream"])
+
+
+def test_noalloc_checks_arguments_before_touching_cuda(lib):
+    # a refused call returns before any CUDA call (here: before the runtime
+    # would report that there is no device), so it enqueues nothing
+    assert _noalloc(lib, logits=None) == -1
+    assert _noalloc(lib, flags=None) == -1
+    assert _noalloc(lib, tok=P + 2) == -4
+    assert _noalloc(lib, dt=9) == -3
+    assert _noalloc(lib, k=17) == -2
+    assert _noalloc(lib, B=4000, k=16, V=151936) == -5   # beyond the library's scratch
+    assert _noalloc(lib, B=0) == 0
+    assert _noalloc(lib) in (-6, -7)
 
 
 def _commit(lib, **kw):

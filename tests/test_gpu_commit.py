@@ -114,3 +114,69 @@ def test_commit_full_size_sampled():
                         np.zeros_like(vconv[l, r, s].cpu().numpy())[None, None])
         assert np.array_equal(dst, exp[0][0, 0])
         assert np.array_equal(cconv[l, slot[r]].cpu().numpy(), exp[1][0, 0])
+
+
+def _swap_inputs(L=3, B=8, S=3, H=2, Dk=64, Dv=40, W=4, C=2056, slots=20, seed=31):
+    rng = np.random.default_rng(seed)
+    vrec = rng.standard_normal((L, B, S - 1, H, Dk, Dv)).astype(np.float32)
+    vconv = rng.integers(0, 1 << 16, size=(L, B, S - 1, W, C), dtype=np.uint16)
+    crec = rng.standard_normal((L, slots, H, Dk, Dv)).astype(np.float32)
+    cconv = rng.integers(0, 1 << 16, size=(L, slots, W, C), dtype=np.uint16)
+    perm = rng.permutation(slots)
+    return vrec, vconv, crec, cconv, perm[:B].astype(np.int32), perm[B:2 * B].astype(np.int32)
+
+
+def test_commit_swap_matches_oracle():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    vrec, vconv, crec, cconv, sl, sc = _swap_inputs()
+    acc = np.array([3, 1, 2, 0, 3, 2, 4, 1], np.int32)     # full, partial, skip, bad (4 > S)
+    sc = sc.copy()
+    sc[7] = sl[7]                                           # equal slots: bad
+    er, ec, esl, esc, ef = oc.commit_swap(vrec, vconv, acc, sl, sc, crec, cconv)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    t_crec, t_cconv = d(crec), d(cconv.view(np.int16))
+    t_sl, t_sc = d(sl), d(sc)
+    t_flags = torch.zeros(8, dtype=torch.int32, device="cuda")
+    sv.spec_commit_swap(d(vrec), d(vconv.view(np.int16)), d(acc), t_sl, t_sc, t_crec, t_cconv, t_flags)
+    torch.cuda.synchronize()
+    assert np.array_equal(t_crec.cpu().numpy().view(np.uint32), er.view(np.uint32))
+    assert np.array_equal(t_cconv.cpu().numpy().view(np.uint16), ec)
+    assert np.array_equal(t_sl.cpu().numpy(), esl) and np.array_equal(t_sc.cpu().numpy(), esc)
+    assert np.array_equal(t_flags.cpu().numpy().astype(np.uint32), ef)
+
+
+def test_commit_swap_full_size_moves_only_partial_rows():
+    """The 24-layer, 64-row workload with a scratch slot per row: full accepts
+    trade slots, partial accepts gather; sampled blobs checked."""
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    sh = synth.CommitShape(slots=128)
+    acc, _ = synth.commit_indices(sh)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    vrec = torch.empty((sh.L, sh.B, sh.S - 1, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device="cuda")
+    vrec.view(torch.int32).random_(generator=g)
+    vconv = torch.randint(-32768, 32767, (sh.L, sh.B, sh.S - 1, sh.W, sh.C), dtype=torch.int16,
+                          device="cuda", generator=g)
+    crec = torch.empty((sh.L, sh.slots, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device="cuda")
+    crec.view(torch.int32).random_(generator=g)
+    cconv = torch.randint(-32768, 32767, (sh.L, sh.slots, sh.W, sh.C), dtype=torch.int16, device="cuda",
+                          generator=g)
+    sl0 = np.arange(sh.B, dtype=np.int32)
+    sc0 = np.arange(sh.B, 2 * sh.B, dtype=np.int32)
+    t_sl, t_sc = torch.from_numpy(sl0).cuda(), torch.from_numpy(sc0).cuda()
+    acc_t = torch.from_numpy(acc).cuda()
+    before = crec.clone(), cconv.clone()
+    sv.spec_commit_swap(vrec, vconv, acc_t, t_sl, t_sc, crec, cconv)
+    torch.cuda.synchronize()
+    nsl, nsc = t_sl.cpu().numpy(), t_sc.cpu().numpy()
+    full = acc == sh.S
+    assert np.array_equal(nsl[full], sc0[full]) and np.array_equal(nsc[full], sl0[full])
+    assert np.array_equal(nsl[~full], sl0[~full])
+    rng = np.random.default_rng(1)
+    for l, r in [(0, 0), (sh.L - 1, sh.B - 1)] + [tuple(x) for x in rng.integers(0, [sh.L, sh.B], (20, 2))]:
+        if full[r]:
+            # nothing moved: the scratch slot (now committed) keeps its bytes
+            assert torch.equal(crec[l, nsl[r]].view(torch.int32), before[0][l, nsl[r]].view(torch.int32))
+        else:
+            assert torch.equal(crec[l, nsl[r]].view(torch.int32), vrec[l, r, acc[r] - 1].view(torch.int32))
+            assert torch.equal(cconv[l, nsl[r]], vconv[l, r, acc[r] - 1])

@@ -1,12 +1,15 @@
 """GPU parity of spec_verify against the oracle (element by element).
 
-Runs through the C ABI (ctypes binding).  Sizes: the tiny, top-p and mixed
-workloads are compared on every row at their full sizes; the adversarial
-workload (256 rows, k=4, fp32) runs in full on the GPU and is compared on a
-sample of rows the oracle computes one by one.  Random small cases cover odd
-and tiny vocabularies, k = 0..4, both dtypes, every filter combination, the
-general threshold paths (top-k above the candidate limit, top-p without
-top-k), ties, masked entries and invalid inputs.
+Runs through the C ABI (ctypes binding).  Sizes: the tiny, top-p, mixed and
+adversarial workloads are compared on every row at their full sizes (the
+oracle over the adversarial workload's 256 rows runs in a process pool).
+Random small cases cover odd and tiny vocabularies, k = 0..4, both dtypes,
+every filter combination, the general threshold paths (top-k above the
+candidate limit, top-p without top-k), ties, masked entries and invalid
+inputs; top-k 8, 9, 127, 128 and 129 at V = 151936 with exact ties at the
+K-th entry cover the hand-over between the candidate lists and the general
+path.  A batch split into row blocks with row_base must equal the whole
+batch bit for bit, and a wait that runs out must come back as a flagged row.
 """
 import numpy as np
 import pytest
@@ -14,7 +17,8 @@ import torch
 
 from oracle import verify as ov
 from speculative_decoding_verify_07_gb300 import synth
-from tests.gpu_harness import compare, run_gpu, run_oracle, to_device
+from tests.gpu_harness import compare, host_outputs, run_gpu, run_oracle, to_device
+from tests.oracle_pool import oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -53,19 +57,46 @@ def test_parity_topp_workload():
 
 def test_parity_mixed_workload():
     inp = synth.make_mixed()
-    s = compare(run_gpu(inp), run_oracle(inp), "mixed")
-    assert s["exempt"] <= 4
+    compare(run_gpu(inp), run_oracle(inp), "mixed")
 
 
-def test_parity_adversarial_sampled_rows():
+def test_parity_adversarial_all_rows():
     inp = synth.make_adversarial()
     gpu = run_gpu(inp)
-    rows = [0, 1, 2, 63, 64, 127, 128, 129, 200, 254, 255]
-    compare(gpu, run_oracle(inp, rows=rows), "adversarial")
+    orc = oracle_rows("adversarial", range(256))
+    s = compare(gpu, orc, "adversarial")
     # whole-batch properties: the first half rejects early, the second half accepts everything
     assert np.mean(gpu["accept_len"][:128]) < 1.2
     assert np.all(gpu["accept_len"][128:] >= 4)
     assert np.all(gpu["flags"] & (ov.F_NAN | ov.F_BAD_TOKEN | ov.F_BAD_PARAM) == 0)
+    assert s["rows"] == 256
+
+
+def _ktie_case(K, B=4, k=2, V=151936, seed=0):
+    """Mixed-recipe bf16 logits with top-k K; in every (row, position) the
+    K-th largest value is copied onto three tokens ranked below K, so equal
+    keys straddle the K-th entry of the total order."""
+    rng = np.random.default_rng(500 + K + seed)
+    logits = synth.round_to_bf16(synth._spiked_logits(rng, B, k + 1, V))
+    for b in range(B):
+        for j in range(k + 1):
+            row = logits[b, j]
+            order = np.argsort(-row, kind="stable")
+            v = row[order[K - 1]]
+            for dst in rng.choice(order[K + 10:], size=3, replace=False):
+                row[dst] = v
+    q = synth._noisy_q(rng, logits, k, 0.7)
+    drafts = synth._sample_rows(rng, q.astype(np.float64))
+    T = np.full(B, 0.8, np.float32)
+    Kk = np.full(B, K, np.int32)
+    P = np.array([1.0 if b % 2 == 0 else 0.9 for b in range(B)], np.float32)
+    return _Case(logits, q, drafts, T, Kk, P, 1000 + K, "bf16")
+
+
+@pytest.mark.parametrize("K", [8, 9, 127, 128, 129])
+def test_parity_topk_boundary_with_ties(K):
+    case = _ktie_case(K)
+    compare(run_gpu(case), run_oracle(case), f"top-k {K} ties")
 
 
 class _Case:
@@ -163,16 +194,20 @@ def test_empty_batch_and_workspace_left_clean():
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
     # the header's counters (unit counter, exit counter, error bits, item
-    # counter) and the per-row tickets (padded to 256 bytes) are back at
-    # zero; the epoch word at the end of the header counts the calls
-    B = 5
+    # counter), the per-row tickets (padded to 256 bytes) and the two tile
+    # counters per (row, position) (padded to 256 bytes) are back at zero;
+    # the epoch word at the end of the header counts the calls
+    B, U = 5, 5 * 4
+    tickets = 256
+    counters = tickets + 256 * ((B * 4 + 255) // 256)
+    records = counters + 256 * ((U * 8 + 255) // 256)
     assert int(ws[:12].count_nonzero()) == 0 and int(ws[16:20].count_nonzero()) == 0
-    assert int(ws[256:256 + 256 * ((B * 4 + 255) // 256)].count_nonzero()) == 0
+    assert int(ws[tickets:records].count_nonzero()) == 0
     assert int(ws[236:240].view(torch.int32).item()) == 3
     # dirty records behind them do not matter: every record word carries the
-    # call's epoch, so results stay identical
+    # call's tag, so results stay identical
     ref = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
-    ws[256 + 256 * ((B * 4 + 255) // 256):].fill_(0xAB)
+    ws[records:].fill_(0xAB)
     again = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(ref.tokens, again.tokens) and torch.equal(ref.logprobs, again.logprobs)
@@ -208,6 +243,44 @@ def test_deterministic_and_graph_replay_bit_identical():
     torch.cuda.synchronize()
     for name in ("tokens", "accept_len", "logprobs", "alpha", "flags"):
         assert torch.equal(getattr(ref, name), getattr(out, name)), name
+
+
+def test_row_base_split_equals_whole_batch():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    inp = synth.make_mixed(B=16, V=32768)
+    logits, q, x, params = to_device(inp)
+    whole = host_outputs(sv.spec_verify(logits, q, x, params, 19))
+    lo = host_outputs(sv.spec_verify(logits[:9], q[:9], x[:9], params[:9], 19, row_base=0))
+    hi = host_outputs(sv.spec_verify(logits[9:], q[9:], x[9:], params[9:], 19, row_base=9))
+    torch.cuda.synchronize()
+    for key in ("tokens", "accept_len", "logprobs", "alpha", "flags"):
+        assert np.array_equal(np.concatenate([lo[key], hi[key]]), whole[key]), key
+    # and the second block matches the oracle run on that block with the same base
+    orc_hi = ov.verify(inp.logits[9:], inp.q[9:], inp.drafts[9:], inp.temperature[9:], inp.top_k[9:],
+                       inp.top_p[9:], 19, row_base=9)
+    compare(hi, orc_hi, "row_base 9")
+    compare(whole, run_oracle(inp, seed=19), "whole")
+
+
+def test_timed_out_wait_flags_the_row_and_leaves_the_context_usable():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    case = _random_case(np.random.default_rng(31), B=4, k=2, V=4096, dtype="bf16", param_mode="mix")
+    logits, q, x, params = to_device(case)
+    ws = sv.new_workspace(4, 2, 4096, "cuda")
+    ws[20:24].view(torch.int32).fill_(1)        # test hook: row 0's finalize waits for nothing
+    out = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
+    torch.cuda.synchronize()
+    assert out["flags"][0] & sv.F_TIMEOUT and out["accept_len"][0] == 0
+    assert np.all(out["tokens"][0] == -1)
+    assert int(ws[24:28].view(torch.int32).item()) & 4       # the record-wait bit of the last call
+    orc = run_oracle(case, rows=[1, 2, 3])
+    compare(out, orc, "rows after the timeout")
+    # the same workspace, hook cleared: every row comes back normally
+    ws[20:24].view(torch.int32).fill_(0)
+    again = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
+    torch.cuda.synchronize()
+    compare(again, run_oracle(case), "after the timeout")
+    assert int(ws[24:28].view(torch.int32).item()) == 0
 
 
 def test_gpu_distribution_preserved_40k_rows():

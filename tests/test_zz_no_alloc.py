@@ -50,6 +50,30 @@ def test_noalloc_refuses_a_batch_beyond_its_scratch():
     B, k, V = 4000, 16, 151936
     assert sv.workspace_size(B, k, V) > (8 << 20)
     fake = ctypes.c_void_p(4096)                 # never dereferenced: the size check comes first
-    rc = sv.LIB.spec_verify_noalloc(fake, sv.SPEC_BF16, fake, fake, fake, ctypes.c_uint64(0), B, k, V,
-                                    fake, fake, fake, fake, fake, None)
+    rc = sv.LIB.spec_verify_noalloc(fake, sv.SPEC_BF16, fake, fake, fake, ctypes.c_uint64(0),
+                                    ctypes.c_uint32(0), B, k, V, fake, fake, fake, fake, fake, None)
     assert rc == sv.SPEC_E_WORKSPACE
+
+
+def test_noalloc_refuses_a_null_pointer_before_enqueuing():
+    # The argument checks come before the scratch is cleared on the stream:
+    # a refused call returns its argument error and leaves the next call's
+    # results as they would be without it.
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    inp = synth.make_mixed(B=8, V=4096)
+    logits, q, x, params = to_device(inp)
+    ref = sv.spec_verify(logits, q, x, params, inp.seed)
+    out = sv.VerifyOutputs(8, 2, "cuda")
+    rc = sv.LIB.spec_verify_noalloc(None, sv.SPEC_BF16, ctypes.c_void_p(q.data_ptr()),
+                                    ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(params.data_ptr()),
+                                    ctypes.c_uint64(inp.seed), ctypes.c_uint32(0), 8, 2, 4096,
+                                    ctypes.c_void_p(out.tokens.data_ptr()),
+                                    ctypes.c_void_p(out.accept_len.data_ptr()),
+                                    ctypes.c_void_p(out.logprobs.data_ptr()),
+                                    ctypes.c_void_p(out.alpha.data_ptr()),
+                                    ctypes.c_void_p(out.flags.data_ptr()),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == sv.SPEC_E_NULL
+    got = sv.spec_verify_noalloc(logits, q, x, params, inp.seed)
+    torch.cuda.synchronize()
+    assert torch.equal(got.tokens, ref.tokens) and torch.equal(got.accept_len, ref.accept_len)
