@@ -34,11 +34,11 @@ constexpr long long kSpinLimit = 1ll << 21;
 // An A tile is one buffer of logits; a B tile is logits (read again, from
 // L2) plus the matching draft probabilities.  Tiles cover whole race blocks
 // of 256 entries.
-constexpr int kSlot = 8704;
+constexpr int kSlot = 8192;
 template <bool kBF16>
 struct Geo {
   static constexpr int es = kBF16 ? 2 : 4;                         // logit bytes
-  static constexpr int EA = kBF16 ? 4352 : 2048;                   // A tile entries (17 / 8 blocks)
+  static constexpr int EA = kBF16 ? 4096 : 2048;                   // A tile entries (16 / 8 blocks; 8 KB)
   static constexpr int EB = kBF16 ? 1280 : 1024;                   // B tile entries (5 / 4 blocks)
   static constexpr int NBA = EA / kRaceBlock;
   static constexpr int NBB = EB / kRaceBlock;
@@ -440,7 +440,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
 // `rec`) as tagged words and lane 0 takes the row's ticket (relaxed: the
 // finaliser waits for the tags, not for an ordering); the warp whose unit is
 // the row's last finalizes the row.
-static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, int u, int row, const UnitRecord& rec) {
+static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, int u, int row, UnitRecord rec) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const uint32_t v = lane_word8(lane, __shfl_sync(full, rec.flags, 0), __shfl_sync(full, (uint32_t)rec.accept, 0),

@@ -404,7 +404,7 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
 
 template <bool kBF16>
 __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag, int u, int row, int pos,
-                                          const RowCfg& cfg) {
+                                          RowCfg cfg) {
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const bool has_q = pos < A.k;

@@ -201,7 +201,7 @@ struct Item {
   int ntiles;               // tiles of this kind in the unit
 };
 
-__device__ __forceinline__ RowCfg plan_cfg(const Args& A, const Plan& P, int row) {
+__device__ __forceinline__ RowCfg plan_cfg(const Args& A, Plan P, int row) {
   return P.cfg ? unpack_cfg(P.cfg[row]) : classify(A.params[row], A.V);
 }
 
@@ -285,7 +285,7 @@ __device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int 
 
 // Item t of the sequence.
 template <bool kBF16>
-__device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t t) {
+__device__ __forceinline__ Item map_item(const Args& A, Plan P, uint32_t t) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
@@ -310,15 +310,16 @@ __device__ __forceinline__ Item map_item(const Args& A, const Plan& P, uint32_t 
   it.u = it.row * (A.k + 1) + it.pos;
   it.kind = kind == 0 ? 1 : 2;
   it.ntiles = (int)tiles;
-  // logits of a drafted unfiltered unit are read again by its B tiles
-  it.reread = (kind == 0 && it.pos < A.k && plan_cfg(A, P, it.row).type == UT_DENSE) ? 1 : 0;
+  // logits of an unfiltered unit are read again: by its B tiles (drafted
+  // positions) or by its draw's level-2 race (bonus position)
+  it.reread = (kind == 0 && plan_cfg(A, P, it.row).type == UT_DENSE) ? 1 : 0;
   it.n = it.kind == 1 ? min(G::EA, A.V - it.c * G::EA) : min(G::EB, A.V - it.c * G::EB);
   return it;
 }
 
 // Lane 0: post the copies of an item into buffer `buf`, completing on `bar`.
 template <bool kBF16>
-__device__ __forceinline__ void issue(const Args& A, const Item& it, unsigned char* buf, unsigned long long* bar) {
+__device__ __forceinline__ void issue(const Args& A, Item it, unsigned char* buf, unsigned long long* bar) {
   using G = Geo<kBF16>;
   if (it.kind == 0) return;
   const unsigned char* lg = reinterpret_cast<const unsigned char*>(A.logits);
@@ -363,7 +364,7 @@ __device__ __forceinline__ bool wait_buffer(const Args& A, unsigned long long* b
 // zero q), so that every tile is reduced over all its blocks.  With rows
 // that are not 16-byte aligned, everything.
 template <bool kBF16>
-__device__ __noinline__ void fill_tail(const Args& A, const Item& it, unsigned char* buf) {
+__device__ __noinline__ void fill_tail(const Args& A, Item it, unsigned char* buf) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int E = it.kind == 1 ? G::EA : G::EB;
@@ -518,18 +519,61 @@ __device__ __forceinline__ float a_wmax(const uint32_t* w) {
                  max_nan(max_nan(__uint_as_float(w[4]), __uint_as_float(w[5])),
                          max_nan(__uint_as_float(w[6]), __uint_as_float(w[7]))));
 }
+// exp2((v - m) c) of the two bf16 entries of one word, as a packed pair:
+// the two floats are built from the word's halves, (v - m) c is one packed
+// subtract and one packed multiply (rounded like the scalar form).
+__device__ __forceinline__ u64 exp_bf16x2(uint32_t w, u64 m2, u64 c2) {
+  u64 r;
+  asm("{\n"
+      " .reg .b32 lo, hi;\n"
+      " .reg .b64 p, d, x;\n"
+      " shl.b32 lo, %1, 16;\n"
+      " and.b32 hi, %1, 0xffff0000;\n"
+      " mov.b64 p, {lo, hi};\n"
+      " sub.rn.f32x2 d, p, %2;\n"
+      " mul.rn.f32x2 x, d, %3;\n"
+      " mov.b64 {lo, hi}, x;\n"
+      " ex2.approx.ftz.f32 lo, lo;\n"
+      " ex2.approx.ftz.f32 hi, hi;\n"
+      " mov.b64 %0, {lo, hi};\n"
+      "}"
+      : "=l"(r)
+      : "r"(w), "l"(m2), "l"(c2));
+  return r;
+}
 // Sum of exp2((v - m) c) over a lane's 8 block entries, as two packed halves.
 template <bool kBF16>
 __device__ __forceinline__ u64 a_wexp(const uint32_t* w, u64 m2, u64 c2) {
+  if (kBF16) {
+    const u64 e0 = exp_bf16x2(w[0], m2, c2), e1 = exp_bf16x2(w[1], m2, c2);
+    const u64 e2 = exp_bf16x2(w[2], m2, c2), e3 = exp_bf16x2(w[3], m2, c2);
+    return add2(add2(e0, e1), add2(e2, e3));
+  }
   const u64 e0 = exp_pair(a_val<kBF16>(w, 0), a_val<kBF16>(w, 1), m2, c2);
   const u64 e1 = exp_pair(a_val<kBF16>(w, 2), a_val<kBF16>(w, 3), m2, c2);
   const u64 e2 = exp_pair(a_val<kBF16>(w, 4), a_val<kBF16>(w, 5), m2, c2);
   const u64 e3 = exp_pair(a_val<kBF16>(w, 6), a_val<kBF16>(w, 7), m2, c2);
   return add2(add2(e0, e1), add2(e2, e3));
 }
+// Max (NaN-propagating) of a lane's entries over all blocks: for bf16 a
+// packed running maximum, unpacked once.
+template <bool kBF16, int NB, int NW>
+__device__ __forceinline__ float a_lane_max(const uint32_t (&w)[NB][NW]) {
+  if (kBF16) {
+    uint32_t m = 0xff80ff80u;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(w[b][0], w[b][1]), max_nan_bf16x2(w[b][2], w[b][3])));
+    return max_nan(bf16_lo(m), bf16_hi(m));
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) m = max_nan(m, a_wmax<kBF16>(w[b]));
+  return m;
+}
 
 template <bool kBF16>
-__device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg,
+__device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCfg cfg,
                                      const unsigned char* buf) {
   using G = Geo<kBF16>;
   constexpr int NB = G::NBA;
@@ -542,15 +586,8 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   uint32_t w[NB][NW];
 #pragma unroll
   for (int b = 0; b < NB; ++b) a_block<kBF16>(buf, b, lane, w[b]);
-  // the lane max, and for the argmax the first block reaching it
-  float lm = -INFINITY;
-  int lb = 0;
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    const float bm = a_wmax<kBF16>(w[b]);
-    lb = bm > lm ? b : lb;
-    lm = max_nan(lm, bm);
-  }
+  // the lane max
+  const float lm = a_lane_max<kBF16, NB, NW>(w);
   const float mc = warp_max_nan(lm);
   const bool nan = mc != mc;
   float z = 0.f;
@@ -593,8 +630,12 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
   }
   uint32_t idx = 0xffffffffu;
   if (greedy && !nan) {
-    // first index of the tile max: in the lane's first block reaching it
+    // first index of the tile max: in the first block of a lane holding it
     if (lm == mc) {
+      int lb = NB - 1;
+#pragma unroll
+      for (int b = NB - 1; b >= 0; --b)
+        if (a_wmax<kBF16>(w[b]) == lm) lb = b;
       float v[8];
       a_vals<kBF16>(buf, lb, lane, v);
 #pragma unroll
@@ -602,6 +643,9 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, const Item& it
         if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(lb, lane, j));
     }
     idx = __reduce_min_sync(kFull, idx);
+    // the settle reads q at the unit's argmax, one of the tiles' argmaxes
+    if (lane == 0 && it.pos < A.k && idx < (uint32_t)A.V)
+      prefetch_l2(A.q + ((size_t)it.row * A.k + it.pos) * (size_t)A.V + idx);
   }
   u64* rec = A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords;
   const uint32_t v = lane_word8(lane, nan ? 0x7fc00000u : __float_as_uint(mc), idx, __float_as_uint(z),
@@ -662,7 +706,7 @@ __device__ __forceinline__ u64 top8_network(u64 a, int lane) {
 // warp stage every entry >= t8 (beyond kStage the list is marked partial).
 constexpr int kLaneCand = 4;
 template <bool kBF16>
-__device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it, const unsigned char* buf,
+__device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const unsigned char* buf,
                                     u64* stage) {
   constexpr int NB = Geo<kBF16>::NBA;
   const int lane = threadIdx.x & 31;
@@ -772,7 +816,7 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, const Item& it,
 
 // The record of a tile whose copy or wait gave up: its unit is settled as
 // timed out.
-__device__ __noinline__ void timeout_record(const Args& A, uint32_t tag, const Item& it, bool topk) {
+__device__ __noinline__ void timeout_record(const Args& A, uint32_t tag, Item it, bool topk) {
   const int lane = threadIdx.x & 31;
   if (it.kind == 1) {
     u64* rec = A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords;
@@ -791,7 +835,7 @@ __device__ __noinline__ void timeout_record(const Args& A, uint32_t tag, const I
 // B tiles.
 // ---------------------------------------------------------------------------
 template <bool kBF16>
-__device__ __noinline__ void b_tile(const Args& A, uint32_t tag, const Item& it, const RowCfg& cfg, const UnitState& st,
+__device__ __noinline__ void b_tile(const Args& A, uint32_t tag, Item it, RowCfg cfg, UnitState st,
                                     const unsigned char* buf) {
   using G = Geo<kBF16>;
   constexpr int NB = G::NBB;
@@ -890,7 +934,7 @@ struct Bufs {
 // ones from one counter (the next ticket is in flight while a tile is
 // reduced).  After a tile's record, one is added to the unit's tile count.
 template <bool kBF16>
-__device__ __noinline__ void stream_loop(const Args& A, const Plan& P0, VShm& S, uint32_t tag, int sw, uint32_t gs,
+__device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32_t tag, int sw, uint32_t gs,
                                          uint32_t nws) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
@@ -981,7 +1025,7 @@ __device__ __noinline__ void stream_loop(const Args& A, const Plan& P0, VShm& S,
 struct Task {
   int u, row, pos, ntiles, kind;   // kind 1: A, 2: B
 };
-__device__ __forceinline__ Task map_task(const Args& A, const Plan& P, const VShm& S, uint32_t t) {
+__device__ __forceinline__ Task map_task(const Args& A, Plan P, const VShm& S, uint32_t t) {
   int lo = 0, hi = P.nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -1004,13 +1048,23 @@ __device__ __forceinline__ Task map_task(const Args& A, const Plan& P, const VSh
 // A settle warp: tasks g, g + nst, ... in sequence order; each waits for its
 // unit's tile count, settles the unit and clears the count.
 template <bool kBF16>
-__device__ __noinline__ void settle_loop(const Args& A, const Plan& P, VShm& S, uint32_t tag, int w, uint32_t g,
+__device__ __noinline__ void settle_loop(const Args& A, Plan P, VShm& S, uint32_t tag, int w, uint32_t g,
                                          uint32_t nst) {
   const int lane = threadIdx.x & 31;
   TopkScratch& TS = S.tk[w];
   for (uint32_t t = g; t < S.ntasks; t += nst) {
     const Task k = map_task(A, P, S, t);
     uint32_t* cnt = &A.ucnt[(k.kind == 2 ? A.U : 0) + k.u];
+    // what the settle needs besides the records is loaded while the tiles
+    // are still being reduced: the draft and its logit and q (settle-A), or
+    // the unit's published state (settle-B)
+    Pre pr;
+    StateWords sw8;
+    if (k.kind == 2) {
+      state_load(A, k.u, sw8.w);
+    } else {
+      pr = load_pre<kBF16>(A, k.u, k.row, k.pos);
+    }
     bool ready = true;
     if (lane == 0) {
       long long spins = 0;
@@ -1029,11 +1083,11 @@ __device__ __noinline__ void settle_loop(const Args& A, const Plan& P, VShm& S, 
     if (!ready) {
       commit_record(A, tag, k.u, k.row, empty_record(SPEC_F_TIMEOUT));   // the records' polls would give up too
     } else if (k.kind == 2) {
-      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg);
+      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg, sw8);
     } else if (cfg.type == UT_TOPK) {
-      topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg);
+      topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg, pr);
     } else {
-      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg);
+      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg, pr);
     }
     if (lane == 0) {
       TL(k.kind == 2 ? TL_SB_END : TL_SA_END, k.u, 2048);
@@ -1046,7 +1100,7 @@ __device__ __noinline__ void settle_loop(const Args& A, const Plan& P, VShm& S, 
 
 // General-path units, taken by the CTA's first kThreads threads.
 template <bool kBF16>
-__device__ __noinline__ void general_phase(const Args& A, const Plan& P, VShm& S, uint32_t tag) {
+__device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint32_t tag) {
   const int k1 = A.k + 1;
   const int nGU = P.nX * k1;
   const int gbase = P.nD + P.nT;

@@ -36,7 +36,7 @@ constexpr int kFinBatchA = 2;
 constexpr int kFinBatchB = 4;
 
 // The state of a drafted unfiltered unit as tagged words (lanes 0..7).
-__device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u, const UnitState& st) {
+__device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u, UnitState st) {
   const int lane = threadIdx.x & 31;
   const uint32_t v = lane_word8(lane, __float_as_uint(st.m), __float_as_uint(st.invZ), __float_as_uint(st.lnZ),
                                 __float_as_uint(st.lp_x), (uint32_t)st.accept, st.flags, st.invalid, (uint32_t)st.am);
@@ -160,7 +160,8 @@ __device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, fl
 // a drafted unfiltered unit publishes its state: its B records are merged
 // later (fin_b).
 template <bool kBF16>
-__device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, RowCfg cfg,
+                                       Pre pr) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
@@ -169,7 +170,6 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
   const int NT = ceil_div(A.V, G::EA);
   const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
   const size_t lrow = (size_t)u * A.V;
-  const Pre pr = load_pre<kBF16>(A, u, row, pos);   // lane 0's copy is the one used
   // one pass over the records: each lane keeps its max, the first tile
   // holding it, and its share of the softmax sum relative to that max
   bool nan = false, tmo = false, timed_out = false;
@@ -365,6 +365,11 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
   publish_state(A, tag, u, st);
 }
 
+// The unit state words of a drafted unfiltered unit, as loaded.
+struct StateWords {
+  u64 w[kStateWords];
+};
+
 // The unit state words of a drafted unfiltered unit.
 __device__ __forceinline__ void state_load(const Args& A, int u, u64 (&w)[kStateWords]) {
 #pragma unroll
@@ -394,11 +399,13 @@ __device__ __forceinline__ UnitState state_of(const u64 (&w)[kStateWords]) {
 // The state was published before any B tile of the unit ran, so it is
 // read without a wait.
 template <bool kBF16>
-__device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, const RowCfg& cfg) {
+__device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, RowCfg cfg,
+                                   StateWords sw0) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   u64 sw[kStateWords];
-  state_load(A, u, sw);
+#pragma unroll
+  for (int i = 0; i < kStateWords; ++i) sw[i] = sw0.w[i];
   bool timed_out = false;
   {
     long long spins = 0;
@@ -742,7 +749,7 @@ __device__ __noinline__ int select_k_row(const Args& A, TopkScratch& S, size_t l
 // Settle a small top-k unit with one warp.
 template <bool kBF16>
 __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
-                                         const RowCfg& cfg) {
+                                         RowCfg cfg, Pre pre) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
@@ -753,13 +760,8 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const float c = cfg.c;
   const int K = cfg.K;
-  // the accept test's operands are in flight while the list is built (lane 0)
-  Pre pr;
-  pr.x = -1;
-  pr.valid = 0;
-  pr.lx = 0.f;
-  pr.qx = 0.f;
-  if (lane == 0) pr = load_pre<kBF16>(A, u, row, pos);
+  // the accept test's operands (loaded before the unit's tiles were done)
+  Pre pr = pre;
 
   // 1. the tiles' lists (raw words into the candidate area, then keys in place)
   uint32_t* raw = reinterpret_cast<uint32_t*>(S.cand);
