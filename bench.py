@@ -413,6 +413,8 @@ def run_ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
+    # weak scaling: the job's batch is world x B rows, this rank verifies its block
+    row_lo, _ = sv.row_block(B * world, world, rank)
     peak, peak_kind = measured_peaks()
     v_hash = kernel_source_hash(VERIFY_SOURCES)
 
@@ -423,7 +425,7 @@ def run_ours(args):
 
     def step(i):
         logits, q, x, params, seed = sets[i % N_SETS]
-        sv.spec_verify(logits, q, x, params, seed, out=out, workspace=ws, row_base=rank * B)
+        sv.spec_verify(logits, q, x, params, seed, out=out, workspace=ws, row_base=row_lo)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -471,7 +473,7 @@ def run_ours(args):
         dq.copy_(hq, non_blocking=True)
         dx.copy_(hx, non_blocking=True)
         dp.copy_(hp, non_blocking=True)
-        sv.spec_verify(dl, dq, dx, dp, seed, out=out, workspace=ws, row_base=rank * B)
+        sv.spec_verify(dl, dq, dx, dp, seed, out=out, workspace=ws, row_base=row_lo)
         for k_, t in d_out.items():
             t.copy_(getattr(out, k_), non_blocking=True)
         torch.cuda.current_stream().synchronize()

@@ -270,6 +270,33 @@ int spec_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_
 /* Human-readable text for a status code (static storage). */
 const char* spec_status_string(int code);
 
+/* spec_verify_commit - spec_verify and spec_commit in one launch.
+ *
+ * Source: inclusionAI/AReno PR #550, "What does this PR do?" Phase 2 (the
+ * verify step decides each row's accept length; the accepted position's
+ * recurrent and conv states are then copied into the row's cache slot) and
+ * table "Per-step optimizations" (fewer, larger kernels per decode step).
+ *
+ * Exactly the results of spec_verify(...) followed on the same stream by
+ * spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec,
+ * cache_conv, L, B, k + 1, H, Dk, Dv, W, C, slots, flags, stream): the
+ * verify outputs, the cache contents and SPEC_F_BAD_IDX in flags.  In the
+ * one cooperative launch a row's state is copied as soon as the row is
+ * finalized, while other rows are still being verified.
+ *   Arguments 1-17: as spec_verify (the workspace is required).
+ *   verify_rec, verify_conv, cache_slot, cache_rec, cache_conv, L, H, Dk, Dv,
+ *   W, C, slots: as spec_commit, with S = k + 1 states per row; L == 0
+ *   verifies only.
+ * Errors: those of spec_verify, then those of spec_commit; a refused call
+ * enqueues nothing. */
+int spec_verify_commit(const void* logits, int logits_dtype, const float* draft_probs,
+                       const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
+                       uint32_t row_base, int B, int k, int V, int32_t* tokens, int32_t* accept_len,
+                       float* logprobs, float* alpha, uint32_t* flags, void* workspace,
+                       size_t workspace_bytes, const float* verify_rec, const uint16_t* verify_conv,
+                       const int32_t* cache_slot, float* cache_rec, uint16_t* cache_conv, int L, int H,
+                       int Dk, int Dv, int W, int C, int slots, void* cuda_stream);
+
 /* SPEC_ABI_VERSION of the loaded library. */
 int spec_version(void);
 

@@ -90,6 +90,19 @@ def workspace_size(B: int, k: int, V: int) -> int:
     return int(LIB.spec_verify_workspace_size(int(B), int(k), int(V)))
 
 
+def row_block(total_rows: int, world: int, rank: int):
+    """Rows [lo, hi) of a batch of `total_rows` that rank `rank` of `world`
+    verifies, as contiguous blocks (the first total_rows % world ranks take
+    one row more).  The rank passes row_base = lo, so that every row draws the
+    random numbers of its place in the whole batch and the shards together
+    give exactly the single-call result."""
+    if world < 1 or not 0 <= rank < world or total_rows < 0:
+        raise ValueError(f"bad shard: {total_rows} rows, rank {rank} of {world}")
+    base, extra = divmod(int(total_rows), int(world))
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 

@@ -119,11 +119,10 @@ __global__ void __launch_bounds__(kCopyThreads) commit_kernel(const CommitArgs A
 
 static inline bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-static int commit_launch(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
-                         const int32_t* cache_slot, int32_t* swap_slot, int32_t* swap_scratch, float* cache_rec,
-                         uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W, int C, int slots,
-                         uint32_t* flags, void* cuda_stream) {
-  using namespace specv;
+int specv::commit_check(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
+                        const int32_t* cache_slot, const int32_t* swap_slot, const int32_t* swap_scratch,
+                        const float* cache_rec, const uint16_t* cache_conv, int L, int B, int S, int H, int Dk,
+                        int Dv, int W, int C, int slots, const uint32_t* flags) {
   const bool swap = swap_slot != nullptr;
   if (L < 0 || B < 0 || S < 1 || slots < 0) return SPEC_E_DIM;
   if (verify_rec && (H < 1 || Dk < 1 || Dv < 1)) return SPEC_E_DIM;
@@ -140,6 +139,18 @@ static int commit_launch(const float* verify_rec, const uint16_t* verify_conv, c
     return SPEC_E_ALIGN;
   if (verify_rec && (!aligned_to(verify_rec, 4) || !aligned_to(cache_rec, 4))) return SPEC_E_ALIGN;
   if (verify_conv && (!aligned_to(verify_conv, 2) || !aligned_to(cache_conv, 2))) return SPEC_E_ALIGN;
+  return SPEC_OK;
+}
+
+static int commit_launch(const float* verify_rec, const uint16_t* verify_conv, const int32_t* accept_len,
+                         const int32_t* cache_slot, int32_t* swap_slot, int32_t* swap_scratch, float* cache_rec,
+                         uint16_t* cache_conv, int L, int B, int S, int H, int Dk, int Dv, int W, int C, int slots,
+                         uint32_t* flags, void* cuda_stream) {
+  using namespace specv;
+  const bool swap = swap_slot != nullptr;
+  const int rc = commit_check(verify_rec, verify_conv, accept_len, cache_slot, swap_slot, swap_scratch, cache_rec,
+                              cache_conv, L, B, S, H, Dk, Dv, W, C, slots, flags);
+  if (rc != SPEC_OK || L == 0 || B == 0) return rc;
   const int arc = check_arch();
   if (arc != SPEC_OK) return arc;
 

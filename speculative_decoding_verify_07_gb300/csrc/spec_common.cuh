@@ -69,7 +69,9 @@ struct WsHeader {
   uint32_t last_error;    // ERR_* bits of the last completed call
   uint32_t pad0;
   uint32_t n_class[4];    // rows per class (large batches)
-  uint32_t pad[47];
+  uint32_t commit_next;   // fused commit: next copy job
+  uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
+  uint32_t pad[45];
   uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
   uint32_t pad1[4];
 };
@@ -152,7 +154,7 @@ __host__ __device__ inline int max_nta(int V) { return ceil_div(V, Geo<false>::E
 __host__ __device__ inline int max_ntb(int V) { return ceil_div(V, Geo<false>::EB); }
 
 struct Layout {
-  size_t row_ticket, ucnt, rec, brec, ust, urec, order, total;
+  size_t row_ticket, ucnt, rec, brec, ust, urec, order, done, total;
 };
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
@@ -166,9 +168,27 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   L.ust = off; off = align_up(off + U * kStateWords * 8, 256);
   L.urec = off; off = align_up(off + U * kURecWords * 8, 256);
   L.order = off; off = align_up(off + (size_t)B * 4, 256);
+  L.done = off; off = align_up(off + (size_t)B * 8, 256);
   L.total = off;
   return L;
 }
+
+// The commit fused into the verify launch (spec_verify_commit): each row's
+// accepted state, gathered as in spec_commit once the row is finalized.
+constexpr long long kJobBytes = 64 * 1024;   // fused commit: bytes of one copy job
+
+struct FusedCommit {
+  const unsigned char* vrec;    // verify_rec [L, B, S, H, Dk, Dv] fp32 (null: none)
+  const unsigned char* vconv;   // verify_conv [L, B, S, W, C] 16-bit (null: none)
+  const int32_t* slot;          // cache_slot [B] (null: slot r)
+  unsigned char* crec;          // cache_rec [L, slots, H, Dk, Dv]
+  unsigned char* cconv;         // cache_conv [L, slots, W, C]
+  long long rec_bytes, conv_bytes;   // bytes of one (layer, row, state) blob
+  int L, slots;
+  int rec_jobs, conv_jobs;      // copy jobs per blob
+  int bulk;                     // pointers and blob sizes 16-byte aligned: bulk copies through shared memory
+  int on;
+};
 
 struct Args {
   const void* logits;
@@ -198,6 +218,8 @@ struct Args {
   int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;
+  u64* done;              // fused commit: finalized rows in order, tagged (row << 5 | accept_len)
+  FusedCommit fc;
 };
 
 // Timeline stamps (global timer, ns) of an instrumented build compiled with
@@ -362,6 +384,16 @@ __device__ __forceinline__ float group_max(const float v[8]) {
 // are the drafts, then the draw of the first rejected unit (or the bonus
 // draw).  A row whose records did not all arrive, or that holds a unit that
 // gave up a wait, is written as invalid with SPEC_F_TIMEOUT.
+// Fused commit: append a finalized row to the done queue (lane 0), after
+// its outputs (the commit ORs SPEC_F_BAD_IDX into the row's flags later).
+__device__ __forceinline__ void enqueue_done(const Args& A, int row, int acc_len, uint32_t tag) {
+  if ((threadIdx.x & 31) == 0) {
+    __threadfence();
+    const uint32_t i = atomicAdd(&A.ws->done_count, 1u);
+    __stcg(A.done + i, tagw(tag, ((uint32_t)row << 5) | (uint32_t)acc_len));
+  }
+}
+
 static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_t tag) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
@@ -413,6 +445,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
       A.accept_len[row] = 0;
       A.flags[row] = rf;
     }
+    if (A.fc.on) enqueue_done(A, row, 0, tag);
     return;
   }
   const unsigned rej = __ballot_sync(full, lane < k && !acc);
@@ -434,6 +467,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
     A.accept_len[row] = a + 1;
     A.flags[row] = uflags;
   }
+  if (A.fc.on) enqueue_done(A, row, a + 1, tag);
 }
 
 // One warp (converged): lanes 0..7 publish the unit's record (lane 0's

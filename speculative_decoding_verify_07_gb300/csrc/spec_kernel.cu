@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "spec_common.cuh"
+#include "spec_fused.cuh"
 #include "spec_general.cuh"
 #include "spec_host.h"
 #include "spec_settle.cuh"
@@ -52,8 +53,8 @@ constexpr int kNW = 12;                // warps per CTA (stream warps of a strea
 constexpr int kAllThreads = kNW * 32;
 constexpr int kOrderSmem = 256;        // batches up to this many rows keep order and configs in shared memory
 constexpr int kStage = 64;             // per-warp staging of a top-k tile's candidates
-constexpr int kMaxSeg = 128;           // segments of the item sequence
 constexpr int kMaxWaves = 40;
+constexpr int kMaxSeg = 4 * kMaxWaves + 8;   // segments of the item sequence (2 A and at most 2 more per wave, 2 classes)
 constexpr int kSettleEvery = 9;        // one settle CTA per this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kAllThreads >= kOrderSmem, "one placement round for a shared-memory order");
@@ -85,8 +86,10 @@ struct alignas(128) VShm {
     GenShm gen;                          // general-path group, after the roles
   };
   unsigned long long bar[kNW][2];
+  unsigned long long cbar[kNW][2];       // fused commit: the warps' copy barriers
   Seg seg[kMaxSeg];
   uint32_t tstart[kMaxSeg];              // first settle task of each segment
+  uint32_t bready[kMaxWaves];            // segment building: when each wave's B tiles fall due
   uint32_t order[kOrderSmem];
   RowPack cfg[kOrderSmem];
   OrderScratch ord;
@@ -201,8 +204,11 @@ struct Item {
   int ntiles;               // tiles of this kind in the unit
 };
 
+// Classification from the parameters (batches whose configs are not kept in
+// shared memory), out of line: it holds two divisions.
+__device__ __noinline__ RowCfg classify_row(const Args& A, int row) { return classify(A.params[row], A.V); }
 __device__ __forceinline__ RowCfg plan_cfg(const Args& A, Plan P, int row) {
-  return P.cfg ? unpack_cfg(P.cfg[row]) : classify(A.params[row], A.V);
+  return P.cfg ? unpack_cfg(P.cfg[row]) : classify_row(A, row);
 }
 
 __device__ __forceinline__ Seg make_seg(uint32_t first, uint32_t nrows, int pos_lo, int upr, int tiles, int kind) {
@@ -217,65 +223,63 @@ __device__ __forceinline__ uint32_t seg_items(const Seg& s) {
   return s.nrows * ((s.packed >> 21) & 31u) * (s.packed & 0xffffu);
 }
 
-// The segment table (thread 0 of every CTA builds the same one):
-//   for each wave i of unfiltered rows: A(drafts of i), A(bonus of i), then
-//   B(drafts of i - 1); A(small top-k rows); A(greedy rows), with the B tiles
-//   of the last wave inserted at a row boundary of the top-k or greedy
-//   segment at least `b_delay` items after that wave's A tiles (at the end
-//   if there are not that many).
+// The segment table (thread 0 of every CTA builds the same one).  The A
+// tiles come class by class, the classes with the longest settles first:
+// unfiltered rows in waves (each wave's drafted positions, then its bonus
+// positions), small top-k rows, greedy rows.  The B tiles of a wave wait in
+// a queue until `b_delay` items have been placed after the wave's A tiles
+// (the wave's settles finish meanwhile) and are then inserted at the next
+// row boundary; waves still waiting at the end come last.
 __device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
                                             int NTB, uint32_t b_delay) {
   if (threadIdx.x != 0) return;
   const int k = A.k, k1 = A.k + 1;
   Seg* sg = S.seg;
   int n = 0;
+  uint32_t pos = 0;   // items placed so far
   int nw = 0, Rw = 1;
   if (nD > 0) {
-    // a wave's A tiles are about b_delay items
+    // a wave's A tiles are about b_delay items; waves of equal size
     const uint32_t row_items = (uint32_t)k1 * (uint32_t)NTA;
     Rw = (int)max(1u, b_delay / max(1u, row_items));
     Rw = max(Rw, ceil_div(nD, kMaxWaves));
     nw = ceil_div(nD, Rw);
+    Rw = ceil_div(nD, nw);
+    nw = ceil_div(nD, Rw);
   }
+  uint32_t* ready = S.bready;   // waves [bh, bt) wait for their B tiles: the item count they wait for
+  int bh = 0, bt = 0;
+  auto place = [&](Seg sgm) {
+    sgm.start = pos;
+    pos += seg_items(sgm);
+    sg[n++] = sgm;
+  };
+  auto place_b = [&](int w) {
+    place(make_seg((uint32_t)(w * Rw), (uint32_t)min(Rw, nD - w * Rw), 0, k, NTB, 1));
+  };
+  // rows [f, f + nr) of an A class, split where a B wave falls due
+  auto place_rows = [&](uint32_t f, uint32_t nr, int pos_lo, int upr) {
+    const uint32_t per_row = (uint32_t)upr * (uint32_t)NTA;
+    while (nr > 0) {
+      while (bh < bt && pos >= ready[bh]) place_b(bh++);
+      uint32_t take = nr;
+      if (bh < bt) take = min(nr, (ready[bh] - pos + per_row - 1u) / per_row);
+      place(make_seg(f, take, pos_lo, upr, NTA, 0));
+      f += take;
+      nr -= take;
+    }
+  };
   for (int i = 0; i < nw; ++i) {
     const uint32_t f = (uint32_t)(i * Rw), nr = (uint32_t)min(Rw, nD - i * Rw);
-    if (k > 0) sg[n++] = make_seg(f, nr, 0, k, NTA, 0);
-    sg[n++] = make_seg(f, nr, k, 1, NTA, 0);
-    if (i >= 1 && k > 0) {
-      const uint32_t fp = (uint32_t)((i - 1) * Rw);
-      sg[n++] = make_seg(fp, (uint32_t)Rw, 0, k, NTB, 1);
-    }
+    if (k > 0) place_rows(f, nr, 0, k);
+    place_rows(f, nr, k, 1);
+    if (k > 0) ready[bt++] = pos + b_delay;
   }
-  // the remaining A segments (top-k, greedy), split once for the last B wave
-  const bool lastB = nw > 0 && k > 0;
-  const uint32_t lf = (uint32_t)((nw - 1) * Rw), lnr = lastB ? (uint32_t)(nD - (nw - 1) * Rw) : 0u;
-  uint32_t since = 0;       // items after the last wave's A tiles
-  bool placed = !lastB;
-  const uint32_t firsts[2] = {(uint32_t)nD, (uint32_t)(nD + nT + nX)};
-  const int counts[2] = {nT, nG};
-  for (int s = 0; s < 2; ++s) {
-    uint32_t f = firsts[s];
-    uint32_t nr = (uint32_t)counts[s];
-    const uint32_t per_row = (uint32_t)k1 * (uint32_t)NTA;
-    if (nr == 0) continue;
-    if (!placed && since + nr * per_row >= b_delay) {
-      const uint32_t need = b_delay > since ? b_delay - since : 0u;
-      const uint32_t r1 = min(nr, (need + per_row - 1) / per_row);
-      if (r1 > 0) sg[n++] = make_seg(f, r1, 0, k1, NTA, 0);
-      sg[n++] = make_seg(lf, lnr, 0, k, NTB, 1);
-      placed = true;
-      f += r1;
-      nr -= r1;
-      since += r1 * per_row;
-    }
-    if (nr > 0) sg[n++] = make_seg(f, nr, 0, k1, NTA, 0);
-    since += nr * per_row;
-  }
-  if (!placed) sg[n++] = make_seg(lf, lnr, 0, k, NTB, 1);
-  uint32_t start = 0, tasks = 0;
+  place_rows((uint32_t)nD, (uint32_t)nT, 0, k1);
+  place_rows((uint32_t)(nD + nT + nX), (uint32_t)nG, 0, k1);
+  while (bh < bt) place_b(bh++);
+  uint32_t tasks = 0;
   for (int i = 0; i < n; ++i) {
-    sg[i].start = start;
-    start += seg_items(sg[i]);
     S.tstart[i] = tasks;
     tasks += sg[i].nrows * ((sg[i].packed >> 21) & 31u);
   }
@@ -285,7 +289,7 @@ __device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int 
 
 // Item t of the sequence.
 template <bool kBF16>
-__device__ __forceinline__ Item map_item(const Args& A, Plan P, uint32_t t) {
+__device__ __noinline__ Item map_item(const Args& A, Plan P, uint32_t t) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
@@ -555,20 +559,31 @@ __device__ __forceinline__ u64 a_wexp(const uint32_t* w, u64 m2, u64 c2) {
   const u64 e3 = exp_pair(a_val<kBF16>(w, 6), a_val<kBF16>(w, 7), m2, c2);
   return add2(add2(e0, e1), add2(e2, e3));
 }
-// Max (NaN-propagating) of a lane's entries over all blocks: for bf16 a
-// packed running maximum, unpacked once.
-template <bool kBF16, int NB, int NW>
-__device__ __forceinline__ float a_lane_max(const uint32_t (&w)[NB][NW]) {
+// The loops over a tile's blocks are rolled (two blocks per iteration) and
+// read the tile from shared memory once per pass: the stream code stays
+// small enough for the instruction cache, which matters more here than the
+// second read of the buffer.
+template <bool kBF16>
+__device__ __forceinline__ float a_tile_lane_max(const unsigned char* buf, int lane) {
+  constexpr int NB = Geo<kBF16>::NBA;
+  constexpr int NW = kBF16 ? 4 : 8;
   if (kBF16) {
     uint32_t m = 0xff80ff80u;
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(w[b][0], w[b][1]), max_nan_bf16x2(w[b][2], w[b][3])));
+#pragma unroll 2
+    for (int b = 0; b < NB; ++b) {
+      uint32_t w[NW];
+      a_block<kBF16>(buf, b, lane, w);
+      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(w[0], w[1]), max_nan_bf16x2(w[2], w[3])));
+    }
     return max_nan(bf16_lo(m), bf16_hi(m));
   }
   float m = -INFINITY;
-#pragma unroll
-  for (int b = 0; b < NB; ++b) m = max_nan(m, a_wmax<kBF16>(w[b]));
+#pragma unroll 2
+  for (int b = 0; b < NB; ++b) {
+    uint32_t w[NW];
+    a_block<kBF16>(buf, b, lane, w);
+    m = max_nan(m, a_wmax<kBF16>(w));
+  }
   return m;
 }
 
@@ -578,16 +593,14 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
   using G = Geo<kBF16>;
   constexpr int NB = G::NBA;
   constexpr int NW = kBF16 ? 4 : 8;
+  static_assert(NB % 2 == 0 && NB <= 32, "blocks of a tile: an even count, one per lane at most");
   const int lane = threadIdx.x & 31;
   const int e0 = it.c * G::EA;
   const float c = cfg.c;
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && it.pos == A.k;
-  uint32_t w[NB][NW];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) a_block<kBF16>(buf, b, lane, w[b]);
-  // the lane max
-  const float lm = a_lane_max<kBF16, NB, NW>(w);
+  // the lane max, then the tile max (NaN-propagating)
+  const float lm = a_tile_lane_max<kBF16>(buf, lane);
   const float mc = warp_max_nan(lm);
   const bool nan = mc != mc;
   float z = 0.f;
@@ -598,29 +611,31 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
     if (!bonus) {
       // the softmax sum relative to the tile max
       u64 za = pack2(0.f, 0.f), zb = pack2(0.f, 0.f);
-#pragma unroll
+#pragma unroll 1
       for (int b = 0; b < NB; b += 2) {
-        za = add2(za, a_wexp<kBF16>(w[b], m2, c2));
-        if (b + 1 < NB) zb = add2(zb, a_wexp<kBF16>(w[b + 1], m2, c2));
+        uint32_t w[NW];
+        a_block<kBF16>(buf, b, lane, w);
+        za = add2(za, a_wexp<kBF16>(w, m2, c2));
+        a_block<kBF16>(buf, b + 1, lane, w);
+        zb = add2(zb, a_wexp<kBF16>(w, m2, c2));
       }
       float a0, a1, b0, b1;
       unpack2(za, a0, a1);
       unpack2(zb, b0, b1);
       z = warp_sum((a0 + a1) + (b0 + b1));
     } else {
-      // block weights by a transposed warp sum, then the level-1 race
-      constexpr int NP = NB <= 8 ? 8 : (NB <= 16 ? 16 : 32);
-      float ps[NP];
-      float tot = 0.f;
-#pragma unroll
-      for (int b = 0; b < NP; ++b) {
-        float s0 = 0.f, s1 = 0.f;
-        if (b < NB) unpack2(a_wexp<kBF16>(w[b], m2, c2), s0, s1);
-        ps[b] = s0 + s1;
-        tot += ps[b];
+      // block weights (lane b keeps block b's), their sum, then the level-1 race
+      float myW = 0.f;
+#pragma unroll 1
+      for (int b = 0; b < NB; ++b) {
+        uint32_t w[NW];
+        a_block<kBF16>(buf, b, lane, w);
+        float s0, s1;
+        unpack2(a_wexp<kBF16>(w, m2, c2), s0, s1);
+        const float Wb = warp_sum(s0 + s1);
+        z += Wb;
+        myW = lane == b ? Wb : myW;
       }
-      z = warp_sum(tot);
-      const float myW = warp_transpose_sum<NP>(ps);   // lane b: the weight of block b
       if (lane < NB && myW > 0.f) {
         const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
         race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
@@ -632,15 +647,17 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
   if (greedy && !nan) {
     // first index of the tile max: in the first block of a lane holding it
     if (lm == mc) {
-      int lb = NB - 1;
+#pragma unroll 1
+      for (int b = 0; b < NB; ++b) {
+        uint32_t w[NW];
+        a_block<kBF16>(buf, b, lane, w);
+        if (a_wmax<kBF16>(w) == mc) {
 #pragma unroll
-      for (int b = NB - 1; b >= 0; --b)
-        if (a_wmax<kBF16>(w[b]) == lm) lb = b;
-      float v[8];
-      a_vals<kBF16>(buf, lb, lane, v);
-#pragma unroll
-      for (int j = 7; j >= 0; --j)
-        if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(lb, lane, j));
+          for (int j = 7; j >= 0; --j)
+            if (a_val<kBF16>(w, j) == mc) idx = (uint32_t)(e0 + a_entry<kBF16>(b, lane, j));
+          break;
+        }
+      }
     }
     idx = __reduce_min_sync(kFull, idx);
     // the settle reads q at the unit's argmax, one of the tiles' argmaxes
@@ -680,16 +697,16 @@ __device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int
   return n;
 }
 
-// Bitonic network over lanes 0..S-1, fully unrolled: groups of S/2 sorted
-// (alternating directions), then of the last merge the half-cleaners down to
-// stride kList, which leave the kList largest keys in lanes 0..kList-1.
-template <int S>
-__device__ __forceinline__ u64 top8_network(u64 a, int lane) {
-#pragma unroll
-  for (int size = 2; size <= S; size <<= 1) {
-#pragma unroll
+// Bitonic network over the warp's 32 lanes (rolled: small code): groups of
+// 16 sorted (alternating directions), then of the last merge the
+// half-cleaners down to stride kList, which leave the kList largest keys in
+// lanes 0..kList-1.
+__device__ __noinline__ u64 top8_network(u64 a, int lane) {
+#pragma unroll 1
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll 1
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (size == S && stride < kList) break;
+      if (size == 32 && stride < kList) break;
       const u64 o = __shfl_xor_sync(kFull, a, stride);
       const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
       a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
@@ -709,55 +726,49 @@ template <bool kBF16>
 __device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const unsigned char* buf,
                                     u64* stage) {
   constexpr int NB = Geo<kBF16>::NBA;
+  constexpr int NW = kBF16 ? 4 : 8;
   const int lane = threadIdx.x & 31;
   const int nb = NB;   // tiles are padded to whole tiles
-  float bm[NB];
-  float lm = -INFINITY;
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    bm[b] = a_block_max<kBF16>(buf, b, lane);
-    lm = max_nan(lm, bm[b]);
-  }
+  const float lm = a_tile_lane_max<kBF16>(buf, lane);
   const bool nan = __any_sync(kFull, lm != lm);
   uint32_t flags = nan ? kListNaN : 0u;
   uint32_t nn = 0;
   if (!nan) {
     // t8: take the largest lane maxima (with their multiplicity) until 8
     uint32_t key = okey(lm), need = (uint32_t)kList, t8k = 0u;
-    bool found = false;   // warp-uniform
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < kList; ++i) {
-      if (!found) {
-        const uint32_t mx = __reduce_max_sync(kFull, key);
-        const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
-        t8k = mx;
-        found = c >= need;
-        need -= found ? 0u : c;
-        key = key == mx ? 0u : key;
-      }
+      const uint32_t mx = __reduce_max_sync(kFull, key);
+      const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
+      t8k = mx;
+      if (c >= need) break;
+      need -= c;
+      key = key == mx ? 0u : key;
     }
     const float t8 = from_okey(t8k);
-    // the lane's blocks holding finite entries >= t8, then those entries
-    uint32_t hit = 0;
-#pragma unroll
-    for (int b = 0; b < NB; ++b) hit |= (bm[b] >= t8 && bm[b] > -INFINITY) ? (1u << b) : 0u;
+    // the lane's finite entries >= t8, block by block (blocks whose maximum
+    // is below t8 hold none)
     uint32_t cnt = 0;
     u64 k0 = 0ull, k1 = 0ull, k2 = 0ull, k3 = 0ull;
+    if (lm >= t8 && lm > -INFINITY) {
 #pragma unroll 1
-    while (hit) {
-      const int b = __ffs(hit) - 1;
-      hit &= hit - 1u;
-      float v[8];
-      a_vals<kBF16>(buf, b, lane, v);
+      for (int b = 0; b < NB; ++b) {
+        uint32_t w[NW];
+        a_block<kBF16>(buf, b, lane, w);
+        const float bm = a_wmax<kBF16>(w);
+        if (!(bm >= t8 && bm > -INFINITY)) continue;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (v[j] >= t8 && v[j] > -INFINITY) {
-          k3 = k2;
-          k2 = k1;
-          k1 = k0;
-          k0 = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
-          ++cnt;
+        for (int j = 0; j < 8; ++j) {
+          const float v = a_val<kBF16>(w, j);
+          if (v >= t8 && v > -INFINITY) {
+            k3 = k2;
+            k2 = k1;
+            k1 = k0;
+            k0 = key64(okey(v), (uint32_t)a_entry<kBF16>(b, lane, j));
+            ++cnt;
+          }
         }
+      }
     }
     uint32_t n = 0;
     if (!__any_sync(kFull, cnt > (uint32_t)kLaneCand)) {
@@ -773,12 +784,10 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const 
     if (n > (uint32_t)kStage) flags |= kListPartial;
     nn = min(n, (uint32_t)kStage);
     if (nn > (uint32_t)kList && nn <= 32) {
-      // one candidate per lane: a bitonic network in registers over lanes
-      // 0..S-1 (S the power of two >= nn; lanes from nn on hold 0) that sorts
-      // groups of S/2, then of the last merge only the half-cleaners down to
-      // stride 8: lanes 0..7 then hold the 8 largest (in no particular order)
+      // one candidate per lane (lanes from nn on hold 0): a bitonic network
+      // in registers leaves the 8 largest in lanes 0..7 (in no particular order)
       u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
-      a = nn <= 16u ? top8_network<16>(a, lane) : top8_network<32>(a, lane);
+      a = top8_network(a, lane);
       __syncwarp();
       stage[lane] = a;
       __syncwarp();
@@ -810,6 +819,10 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const 
     if ((lane & 1) == 0) v = has ? (uint32_t)(k >> 32) : 0u;
     else v = (has ? key64_idx(k) : kListIdx) | (j == 0 ? flags : 0u);
     __stcg(A.rec + ((size_t)it.u * A.NTA + it.c) * kRecWords + lane, tagw(tag, v));
+    // the settle reads q at the listed entries: bring those lines into L2 now
+    const uint32_t gi = (uint32_t)(it.c * Geo<kBF16>::EA) + (has ? key64_idx(k) : 0u);
+    if ((lane & 1) && has && it.pos < A.k && gi < (uint32_t)A.V)
+      prefetch_l2(A.q + ((size_t)it.row * A.k + it.pos) * (size_t)A.V + gi);
   }
   __syncwarp();
 }
@@ -839,61 +852,42 @@ __device__ __noinline__ void b_tile(const Args& A, uint32_t tag, Item it, RowCfg
                                     const unsigned char* buf) {
   using G = Geo<kBF16>;
   constexpr int NB = G::NBB;
-  constexpr int NP = NB <= 4 ? 4 : 8;
+  static_assert(NB <= 32, "one block per lane at most");
   const int lane = threadIdx.x & 31;
   const int e0 = it.c * G::EB;
   const bool need_race = !st.accept;
   const float* qb = reinterpret_cast<const float*>(buf + G::EB * G::es);
   const float m = st.m, invZ = st.invZ, c = cfg.c;
   const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
-  // the lane's entries of every block (logits and q), in registers
-  float v[NB][8], q[NB][8];
-#pragma unroll
+  // alpha per lane over the lane's entries in block order; after a rejection
+  // also per block the residual weight W = sum max(p - q, 0) and the q
+  // under it (the draw margin's weight is W + 2 sum q over w > 0), lane b
+  // keeping block b's
+  float a8 = 0.f, myW = 0.f, myQ = 0.f;
+#pragma unroll 1
   for (int b = 0; b < NB; ++b) {
-    sload<kBF16>(buf, b, lane, v[b]);
-    sload_q(qb, b, lane, q[b]);
-  }
-  float alpha_c, myW = 0.f, myQ = 0.f;
-  if (!need_race) {
-    // accepted draft: alpha only
-    float a0 = 0.f, a1 = 0.f;
+    float v[8], q[8];
+    sload<kBF16>(buf, b, lane, v);
+    sload_q(qb, b, lane, q);
+    float w8 = 0.f, q8 = 0.f;
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-#pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        float p0, p1;
-        unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);
-        a0 += fminf(p0, q[b][j]);
-        a1 += fminf(p1, q[b][j + 1]);
+    for (int j = 0; j < 8; j += 2) {
+      float p0, p1;
+      unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
+      a8 += fminf(p0, q[j]) + fminf(p1, q[j + 1]);
+      if (need_race) {
+        const float d0 = p0 - q[j], d1 = p1 - q[j + 1];
+        w8 += fmaxf(d0, 0.f) + fmaxf(d1, 0.f);
+        q8 += (d0 > 0.f ? q[j] : 0.f) + (d1 > 0.f ? q[j + 1] : 0.f);
       }
     }
-    alpha_c = warp_sum(a0 + a1);
-  } else {
-    // alpha, and per block the residual weight W = sum max(p - q, 0) and
-    // the q under it (the draw margin's weight is W + 2 sum q over w > 0)
-    float a8 = 0.f;
-    float wsum[NP], qsum[NP];
-#pragma unroll
-    for (int b = 0; b < NP; ++b) {
-      float w8 = 0.f, q8 = 0.f;
-      if (b < NB) {
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float p0, p1;
-          unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
-          a8 += fminf(p0, q[b][j]) + fminf(p1, q[b][j + 1]);
-          const float d0 = p0 - q[b][j], d1 = p1 - q[b][j + 1];
-          w8 += fmaxf(d0, 0.f) + fmaxf(d1, 0.f);
-          q8 += (d0 > 0.f ? q[b][j] : 0.f) + (d1 > 0.f ? q[b][j + 1] : 0.f);
-        }
-      }
-      wsum[b] = w8;
-      qsum[b] = q8;
+    if (need_race) {
+      const float Wb = warp_sum(w8), Qb = warp_sum(q8);
+      myW = lane == b ? Wb : myW;
+      myQ = lane == b ? Qb : myQ;
     }
-    alpha_c = warp_sum(a8);
-    myW = warp_transpose_sum<NP>(wsum);
-    myQ = warp_transpose_sum<NP>(qsum);
   }
+  const float alpha_c = warp_sum(a8);
   Race r;
   race_init(r);
   if (need_race && lane < NB && myW > 0.f) {
@@ -1186,6 +1180,13 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     if (threadIdx.x < kThreads) general_phase<kBF16>(A, P, S, tag);
   }
   __syncthreads();
+  if (A.fc.on && order_ok) {
+    // the fused commit: every warp copies rows as they are finalized (not
+    // after a copy wait that gave up: that copy may still land in a buffer)
+    const bool copy_failed = (__shfl_sync(kFull, __ldcg(&A.ws->error), 0) & (uint32_t)ERR_COPY_WAIT) != 0u;
+    if (!copy_failed) commit_phase(A, tag, S.s.buf[w][0], S.s.buf[w][1], S.cbar[w]);
+    __syncthreads();
+  }
   if (threadIdx.x == 0) TL(TL_CTA_END, (int)blockIdx.x, 160);
   if (threadIdx.x == 0) {
     __threadfence();
@@ -1194,6 +1195,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
       __threadfence();
       A.ws->gnext = 0u;
       A.ws->next_item = 0u;
+      A.ws->commit_next = 0u;
+      A.ws->done_count = 0u;
       A.ws->ctas_done = 0u;
       A.ws->last_error = __ldcg(&A.ws->error);
       A.ws->error = 0u;

@@ -72,5 +72,5 @@ extern "C" int spec_verify_noalloc(const void* logits, int logits_dtype, const f
     return SPEC_E_CUDA;
   }
   return specv::verify_launch(logits, logits_dtype, draft_probs, draft_tokens, params, seed, row_base, B, k, V,
-                              tokens, accept_len, logprobs, alpha, flags, scratch, cuda_stream);
+                              tokens, accept_len, logprobs, alpha, flags, scratch, cuda_stream, nullptr);
 }

@@ -631,15 +631,10 @@ struct TopkScratch {
   u64 cand[kMaxListCand];                  // the A tiles' lists as total-order keys (0 = none)
   uint32_t hist[256];
   u64 sel[kSel];                           // the selected candidates
+  float qsel[kSel];                        // q of the selected candidates
   uint8_t cflag[kMaxListCand / kList];     // per tile: bit 0 NaN, bit 1 partial list, bit 2 timeout
 };
-
-// The list phase reuses the candidate area.
-struct ListArrays {
-  uint32_t idx[kTopkSmall];
-  float val[kTopkSmall], e[kTopkSmall], cum[kTopkSmall], q[kTopkSmall], w[kTopkSmall], wu[kTopkSmall];
-};
-static_assert(sizeof(ListArrays) <= sizeof(u64) * kMaxListCand, "list arrays exceed the candidate area");
+static_assert(kTopkSmall <= 256 && kTopkSmall % 32 == 0, "the list is held 32 entries per round");
 
 // Calls fn(g, v) on every lane for groups 8 entries g = g0 + step * 32 + lane
 // (g < g1; lanes past the end get g = -1 and -inf values), loading four steps
@@ -746,257 +741,348 @@ __device__ __noinline__ int select_k_row(const Args& A, TopkScratch& S, size_t l
   return (int)min(n_out, (uint32_t)kSel);
 }
 
+// Candidates a lane holds (round r: candidate 32 r + lane): a small top-k
+// unit has at most kMaxListCand / kList tiles of fp32 logits, half as many of bf16.
+template <bool kBF16>
+struct CandRounds {
+  static constexpr int value = (kBF16 ? kMaxListCand / 2 : kMaxListCand) / 32;
+};
+static_assert(Geo<true>::EA == 2 * Geo<false>::EA, "bf16 tiles hold twice the entries");
+constexpr int kListRounds = kTopkSmall / 32;     // list entries a lane holds
+static_assert(kMaxListCand % 32 == 0 && kList == 8, "lane l holds list slot l mod 8 of its tiles");
+
+// Number of candidates (over the warp) whose 32-bit value key is >= t (t >= 1;
+// an empty slot holds 0).
+template <int CR>
+__device__ __forceinline__ uint32_t count_key_ge(const u64 (&cand)[CR], int nrd, uint32_t t) {
+  uint32_t n = 0;
+#pragma unroll
+  for (int i = 0; i < CR; ++i)
+    if (i < nrd) n += (uint32_t)(cand[i] >> 32) >= t ? 1u : 0u;
+  return __reduce_add_sync(kSettleFull, n);
+}
+
+// Entry j of a list held 32 per round (j warp-uniform).
+__device__ __forceinline__ float list_get(const float (&a)[kListRounds], int j) {
+  float v = a[0];
+#pragma unroll
+  for (int r = 1; r < kListRounds; ++r) v = (j >> 5) == r ? a[r] : v;
+  return __shfl_sync(kSettleFull, v, j & 31);
+}
+__device__ __forceinline__ uint32_t list_get(const uint32_t (&a)[kListRounds], int j) {
+  uint32_t v = a[0];
+#pragma unroll
+  for (int r = 1; r < kListRounds; ++r) v = (j >> 5) == r ? a[r] : v;
+  return __shfl_sync(kSettleFull, v, j & 31);
+}
+
+// The K-th largest listed entry in the total order (0 when fewer than K are
+// listed), by bisection on the value key, then on the index among ties.
+template <bool kBF16, int CR>
+__device__ __forceinline__ u64 kth_listed(const u64 (&cand)[CR], int nrd, uint32_t K, uint32_t V) {
+  if (count_key_ge(cand, nrd, 1u) < K) return 0ull;
+  // the largest value key t with count(key >= t) >= K (bf16 keys: the top 16 bits decide)
+  uint32_t tkey;
+  if (kBF16) {
+    uint32_t lo = 0u, hi = 0xffffu;
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
+      if (count_key_ge(cand, nrd, max(mid << 16, 1u)) >= K) lo = mid;
+      else hi = mid - 1u;
+    }
+    tkey = full_key<true>(lo);
+  } else {
+    uint32_t lo = 1u, hi = 0xffffffffu;
+    while (lo < hi) {
+      const uint32_t mid = lo + (uint32_t)(((u64)hi - lo + 1ull) >> 1);
+      if (count_key_ge(cand, nrd, mid) >= K) lo = mid;
+      else hi = mid - 1u;
+    }
+    tkey = lo;
+  }
+  const uint32_t n_gt = tkey == 0xffffffffu ? 0u : count_key_ge(cand, nrd, tkey + 1u);
+  const uint32_t need = K - n_gt;   // >= 1 entries at the key, smallest indices first
+  const uint32_t n_eq = count_key_ge(cand, nrd, tkey) - n_gt;
+  uint32_t low = 0xffffffffu;
+#pragma unroll
+  for (int i = 0; i < CR; ++i)
+    if (i < nrd && (uint32_t)(cand[i] >> 32) == tkey) low = min(low, (uint32_t)cand[i]);
+  low = __reduce_min_sync(kSettleFull, low);
+  if (n_eq == need) return ((u64)tkey << 32) | low;   // every entry at the key is kept
+  // the need-th largest low word (0xffffffff - index) among the entries at tkey
+  uint32_t lo = low, hi = 0xffffffffu;
+  while (lo < hi) {
+    const uint32_t mid = lo + (uint32_t)(((u64)hi - lo + 1ull) >> 1);
+    uint32_t n = 0;
+#pragma unroll
+    for (int i = 0; i < CR; ++i)
+      if (i < nrd) n += ((uint32_t)(cand[i] >> 32) == tkey && (uint32_t)cand[i] >= mid) ? 1u : 0u;
+    if (__reduce_add_sync(kSettleFull, n) >= need) lo = mid;
+    else hi = mid - 1u;
+  }
+  return ((u64)tkey << 32) | lo;
+}
+
+// The exact top-K of a small top-k unit when a tile may hold more top-K
+// entries than it listed (a full list ending above kappa, or one marked
+// partial): those tiles are re-read (their entries at or above kappa join
+// the listed entries at or above kappa of the other tiles), or, when that
+// gives more than kSel entries (masses of ties), the whole row by radix
+// passes.  Leaves the K (or all, when fewer) largest sorted in S.sel with
+// their q in S.qsel; returns their count.
+template <bool kBF16, int CR>
+__device__ __noinline__ int topk_rescan(const Args& A, TopkScratch& S, const u64 (&cand)[CR], const u64* R, int nrd,
+                                        int NT, int NL, u64 kappa, int K, size_t lrow, size_t qrow, bool has_q) {
+  using G = Geo<kBF16>;
+  const int lane = threadIdx.x & 31;
+  int n_k = 0;
+#pragma unroll
+  for (int i = 0; i < CR; ++i)
+    if (i < nrd && 32 * i + lane < NL) S.cand[32 * i + lane] = cand[i];
+  for (int ch = lane; ch < NT; ch += 32) {
+    const uint32_t iw = (uint32_t)__ldcg(R + (size_t)ch * kRecWords + 1);
+    S.cflag[ch] = (uint8_t)((iw & kListPartial) ? 2u : 0u);
+  }
+  __syncwarp();
+  uint32_t n = 0;
+  bool exact = true;
+  for (int base = 0; base < NL; base += 32) {
+    const int q = base + lane;
+    const u64 k = q < NL ? S.cand[q] : 0ull;
+    const int ch = q / kList;
+    const u64 last = q < NL ? S.cand[ch * kList + kList - 1] : 0ull;
+    const bool safe_ch = q < NL && (S.cflag[ch] & 2u) == 0 && !(last != 0ull && last > kappa);
+    const bool in = safe_ch && k != 0ull && k >= kappa;
+    const unsigned ball = __ballot_sync(kSettleFull, in);
+    const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
+    if (in && p < (uint32_t)kSel) S.sel[p] = k;
+    n += __popc(ball);
+  }
+  const uint32_t T = max((uint32_t)(kappa >> 32), okey(-INFINITY) + 1u);
+  for (int ch = 0; ch < NT; ++ch) {
+    const u64 last = S.cand[ch * kList + kList - 1];
+    if (!((S.cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa))) continue;
+    const int g0 = ch * (G::EA / 8);
+    const int g1 = min(ceil_div(A.V, 8), g0 + G::EA / 8);
+    sweep_range<kBF16>(A, lrow, g0, g1, [&](int g, const float* v) {
+      uint32_t keep = 0;
+      uint32_t keys[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        keys[i] = okey(v[i]);
+        const bool inr = g >= 0 && g * 8 + i < A.V && keys[i] >= T && key64(keys[i], (uint32_t)(g * 8 + i)) >= kappa;
+        keep |= inr ? (1u << i) : 0u;
+      }
+      append_entries(S.sel, &n, g, keep, keys);
+    });
+  }
+  __syncwarp();
+  if (n <= (uint32_t)kSel) {
+    warp_sort_desc(S.sel, (int)n);
+    n_k = min((int)n, K);
+  } else {
+    exact = false;
+  }
+  if (!exact) {
+    const int nn = select_k_row<kBF16>(A, S, lrow, K);
+    warp_sort_desc(S.sel, nn);
+    n_k = min(nn, K);
+  }
+  for (int i = lane; i < n_k; i += 32) S.qsel[i] = has_q ? A.q[qrow + key64_idx(S.sel[i])] : 0.f;
+  __syncwarp();
+  return n_k;
+}
+
 // Settle a small top-k unit with one warp.
+//   1. The tiles' lists into registers (candidate 32 r + lane in round r, so
+//      lane l holds list slot l mod 8 of its tiles), and q at every listed
+//      entry (loads in flight while the list is settled).
+//   2. kappa, the K-th listed entry, by bisection.  A tile whose list is
+//      full and ends above kappa, or is marked partial, may hold more top-K
+//      entries: then the tile is re-read (the listed entries at or above
+//      kappa of the other tiles join its entries at or above kappa).
+//   3. The kept entries in the total order (rank by counting), prefix sums
+//      for top-p, alpha, the accept test, and the two-level race over the
+//      kept entries, all in registers.
 template <bool kBF16>
 __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
                                          RowCfg cfg, Pre pre) {
   using G = Geo<kBF16>;
+  constexpr int CR = CandRounds<kBF16>::value;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
   const int NT = ceil_div(A.V, G::EA);
   const int NL = NT * kList;
+  const int nrd = ceil_div(NL, 32);
   const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const float c = cfg.c;
   const int K = cfg.K;
-  // the accept test's operands (loaded before the unit's tiles were done)
   Pre pr = pre;
+  pr.x = __shfl_sync(kSettleFull, pr.x, 0);
+  pr.valid = __shfl_sync(kSettleFull, pr.valid, 0);
+  pr.lx = __shfl_sync(kSettleFull, pr.lx, 0);
+  pr.qx = __shfl_sync(kSettleFull, pr.qx, 0);
 
-  // 1. the tiles' lists (raw words into the candidate area, then keys in place)
-  uint32_t* raw = reinterpret_cast<uint32_t*>(S.cand);
-  uint8_t* cflag = S.cflag;
+  // 1. the lists
+  u64 cand[CR];
+  uint32_t lflags = 0;   // kListNaN / kListPartial / kListTimeout of the lane's tiles
   bool timed_out = false;
   {
     long long spins = 0;
     bool ok;
     do {
       ok = true;
-      // 8 words a lane in flight at a time
-      for (int i0 = 0; i0 < NT * kRecWords; i0 += 32 * 8) {
-        u64 w[8];
+      lflags = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + 32 * j + lane;
-          w[j] = i < NT * kRecWords ? __ldcg(R + i) : 0ull;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + 32 * j + lane;
-          if (i < NT * kRecWords) {
-            ok = ok && tag_ok(w[j], tag);
-            raw[i] = wu(w[j]);
-          }
+      for (int i = 0; i < CR; ++i) {
+        cand[i] = 0ull;
+        const int q = 32 * i + lane;
+        if (i < nrd && q < NL) {
+          const u64* r = R + (size_t)(q >> 3) * kRecWords + 2 * (q & 7);
+          const u64 wk = __ldcg(r), wi = __ldcg(r + 1);
+          ok = ok && tag_ok(wk, tag) && tag_ok(wi, tag);
+          const uint32_t key = (uint32_t)wk, iw = (uint32_t)wi;
+          lflags |= iw & (kListNaN | kListPartial | kListTimeout);
+          cand[i] = key ? key64(key, (uint32_t)((q >> 3) * G::EA) + (iw & kListIdx)) : 0ull;
         }
       }
     } while (poll_again(A, ok, spins, &timed_out));
   }
-  __syncwarp();
   TLP(u, 1);
-  for (int q = lane; q < NL; q += 32) {
-    const uint32_t key = raw[2 * q];
-    const uint32_t iw = raw[2 * q + 1];
-    const int ch = q / kList;
-    if ((q & (kList - 1)) == 0)
-      cflag[ch] = (uint8_t)(((iw & kListNaN) ? 1u : 0u) | ((iw & kListPartial) ? 2u : 0u) |
-                            ((iw & kListTimeout) ? 4u : 0u));
-    S.cand[q] = key ? key64(key, (uint32_t)(ch * G::EA) + (iw & kListIdx)) : 0ull;
-  }
-  __syncwarp();
-  bool nan = false, any_partial = false, tmo = timed_out;
-  for (int ch = lane; ch < NT; ch += 32) {
-    nan |= (cflag[ch] & 1u) != 0;
-    any_partial |= (cflag[ch] & 2u) != 0;
-    tmo |= (cflag[ch] & 4u) != 0;
-  }
-  nan = __any_sync(kSettleFull, nan);
-  any_partial = __any_sync(kSettleFull, any_partial);
-  tmo = __any_sync(kSettleFull, tmo);
-  if (tmo) {
+  const uint32_t allf = __reduce_or_sync(kSettleFull, lflags);
+  if ((allf & kListTimeout) || timed_out) {
     commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
     return;
   }
-  unsigned long long top = 0;
-  for (int q = lane; q < NL; q += 32) top = S.cand[q] > top ? S.cand[q] : top;
+  // q at every listed entry, in flight while the list is settled
+  float qc[CR];
+#pragma unroll
+  for (int i = 0; i < CR; ++i) {
+    const uint32_t v = key64_idx(cand[i]);
+    qc[i] = (has_q && cand[i] && v < (uint32_t)A.V) ? __ldcg(A.q + qrow + v) : 0.f;
+  }
+  u64 top = 0ull;
+#pragma unroll
+  for (int i = 0; i < CR; ++i) top = cand[i] > top ? cand[i] : top;
   top = warp_max_u64(top);
   const float m = from_okey((uint32_t)(top >> 32));
-  if (nan || top == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
+  if ((allf & kListNaN) || top == 0ull || !(m > -INFINITY) || !(m < INFINITY)) {
     commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
     return;
   }
   const int am = (int)key64_idx(top);
 
-  // 2. the K-th listed entry, from a histogram of 16-bit key distances to
-  // the max (bin 255 lumps the rest), then a sort of the entries at or
-  // above its 16-bit key
-  const uint32_t km16 = (uint32_t)(top >> 48);
-  __syncwarp();
+  // 2. kappa; tiles that may hold more
+  const u64 kappa = kth_listed<kBF16, CR>(cand, nrd, (uint32_t)K, (uint32_t)A.V);
+  TLP(u, 2);
+  bool unsafe = (allf & kListPartial) != 0;
+  if ((lane & 7) == 7) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) S.hist[8 * lane + i] = 0u;
-  __syncwarp();
-  for (int q = lane; q < NL; q += 32)
-    if (S.cand[q]) atomicAdd(&S.hist[min(km16 - (uint32_t)(S.cand[q] >> 48), 255u)], 1u);
-  __syncwarp();
-  uint32_t before = 0;
-  const int b = warp_select_bin(S.hist, (uint32_t)K, &before);
-  uint32_t tau16;
-  if (b == 256) {
-    tau16 = 0u;                               // fewer than K listed entries: all
-  } else if (b < 255) {
-    tau16 = km16 - (uint32_t)b;
-  } else {
-    uint32_t lo = 0u, hi = km16;              // count(key16 >= lo) >= K holds
-    while (lo < hi) {
-      const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
-      uint32_t cnt = 0;
-      for (int q = lane; q < NL; q += 32) cnt += (S.cand[q] && (uint32_t)(S.cand[q] >> 48) >= mid) ? 1u : 0u;
-      cnt = __reduce_add_sync(kSettleFull, cnt);
-      if (cnt >= (uint32_t)K) lo = mid;
-      else hi = mid - 1u;
-    }
-    tau16 = lo;
+    for (int i = 0; i < CR; ++i) unsafe |= cand[i] != 0ull && cand[i] > kappa;
   }
-  uint32_t n_c = 0;
-  for (int base = 0; base < NL; base += 32) {
-    const int q = base + lane;
-    const u64 k = q < NL ? S.cand[q] : 0ull;
-    const bool in = k && (uint32_t)(k >> 48) >= tau16;
-    const unsigned ball = __ballot_sync(kSettleFull, in);
-    const uint32_t p = n_c + __popc(ball & ((1u << lane) - 1u));
-    if (in && p < (uint32_t)kSel) S.sel[p] = k;
-    // the list reads q of its entries after the sort: start those lines now
-    if (in && has_q) prefetch_l2(A.q + qrow + key64_idx(k));
-    n_c += __popc(ball);
-  }
-  __syncwarp();
+  unsafe = __any_sync(kSettleFull, unsafe);
   int n_k = 0;
-  bool exact = n_c <= (uint32_t)kSel;
-  if (exact) {
-    warp_sort_desc(S.sel, (int)n_c);
-    // a tile whose list is full and ends above the K-th entry may hold more
-    const u64 kappa = (int)n_c >= K ? S.sel[K - 1] : 0ull;
-    bool unsafe = false;
-    for (int ch = lane; ch < NT; ch += 32) {
-      const u64 last = S.cand[ch * kList + kList - 1];
-      unsafe |= (cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa);
-    }
-    if (__any_sync(kSettleFull, unsafe)) {
-      // re-read those tiles: their entries at or above kappa join the listed
-      // entries at or above kappa of the other tiles
-      uint32_t n = 0;
-      for (int base = 0; base < NL; base += 32) {
-        const int q = base + lane;
-        const u64 k = q < NL ? S.cand[q] : 0ull;
-        const int ch = q / kList;
-        const u64 last = q < NL ? S.cand[ch * kList + kList - 1] : 0ull;
-        const bool safe_ch = q < NL && (cflag[ch] & 2u) == 0 && !(last != 0ull && last > kappa);
-        const bool in = safe_ch && k != 0ull && k >= kappa;
+  const u64* lk;
+  const float* lq;
+  if (!unsafe) {
+    // the kept entries (exactly min(K, listed)): compact, then each goes to
+    // its rank (the number of kept entries above it)
+    uint32_t n = 0;
+#pragma unroll
+    for (int i = 0; i < CR; ++i) {
+      if (i < nrd) {
+        const bool in = cand[i] != 0ull && cand[i] >= kappa;
         const unsigned ball = __ballot_sync(kSettleFull, in);
         const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
-        if (in && p < (uint32_t)kSel) S.sel[p] = k;
+        if (in) {
+          S.sel[p] = cand[i];
+          S.qsel[p] = qc[i];
+        }
         n += __popc(ball);
       }
-      const uint32_t kk = (uint32_t)(kappa >> 32);
-      const uint32_t T = max(kk, okey(-INFINITY) + 1u);
-      for (int ch = 0; ch < NT; ++ch) {
-        const u64 last = S.cand[ch * kList + kList - 1];
-        if (!((cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa))) continue;
-        const int g0 = ch * (G::EA / 8);
-        const int g1 = min(ceil_div(A.V, 8), g0 + G::EA / 8);
-        sweep_range<kBF16>(A, lrow, g0, g1, [&](int g, const float* v) {
-          uint32_t keep = 0;
-          uint32_t keys[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            keys[i] = okey(v[i]);
-            const bool inr = g >= 0 && g * 8 + i < A.V && keys[i] >= T &&
-                             key64(keys[i], (uint32_t)(g * 8 + i)) >= kappa;
-            keep |= inr ? (1u << i) : 0u;
-          }
-          append_entries(S.sel, &n, g, keep, keys);
-        });
-      }
-      __syncwarp();
-      if (n <= (uint32_t)kSel) {
-        warp_sort_desc(S.sel, (int)n);
-        n_k = min((int)n, K);
-      } else {
-        exact = false;
-      }
-    } else {
-      n_k = min((int)n_c, K);
     }
+    __syncwarp();
+    n_k = (int)n;
+    u64 e[kListRounds];
+    float eq[kListRounds];
+    uint32_t rk[kListRounds];
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      const int i = 32 * r + lane;
+      e[r] = i < n_k ? S.sel[i] : 0ull;
+      eq[r] = i < n_k ? S.qsel[i] : 0.f;
+      rk[r] = 0u;
+    }
+#pragma unroll 4
+    for (int j = 0; j < n_k; ++j) {
+      const u64 kj = S.sel[j];
+#pragma unroll
+      for (int r = 0; r < kListRounds; ++r) rk[r] += kj > e[r] ? 1u : 0u;
+    }
+    u64* sk = S.cand;
+    float* sq = reinterpret_cast<float*>(S.hist);
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r)
+      if (32 * r + lane < n_k) {
+        sk[rk[r]] = e[r];
+        sq[rk[r]] = eq[r];
+      }
+    __syncwarp();
+    lk = sk;
+    lq = sq;
+  } else {
+    n_k = topk_rescan<kBF16, CR>(A, S, cand, R, nrd, NT, NL, kappa, K, lrow, qrow, has_q);
+    lk = S.sel;
+    lq = S.qsel;
   }
-  if (!exact) {
-    const int n = select_k_row<kBF16>(A, S, lrow, K);
-    warp_sort_desc(S.sel, n);
-    n_k = min(n, K);
-  }
+  TLP(u, 3);
 
-  TLP(u, 2);
-  // 3. the list: entry i = 32 r + lane in round r, arrays in shared memory
-  ListArrays& L = *reinterpret_cast<ListArrays*>(S.cand);
-  const int nr = (n_k + 31) >> 5;
-  {
-    float qv[kTopkSmall / 32];
-#pragma unroll
-    for (int r = 0; r < kTopkSmall / 32; ++r) {      // q loads in flight together
-      const int i = 32 * r + lane;
-      qv[r] = (has_q && i < n_k) ? A.q[qrow + key64_idx(S.sel[i])] : 0.f;
-    }
-#pragma unroll
-    for (int r = 0; r < kTopkSmall / 32; ++r) {
-      const int i = 32 * r + lane;
-      if (i < n_k) {
-        const u64 key = S.sel[i];
-        L.idx[i] = key64_idx(key);
-        L.val[i] = from_okey((uint32_t)(key >> 32));
-        L.e[i] = ex2((L.val[i] - m) * c);
-        L.q[i] = qv[r];
-      }
-    }
-  }
-  pr.x = __shfl_sync(kSettleFull, pr.x, 0);
-  pr.valid = __shfl_sync(kSettleFull, pr.valid, 0);
-  pr.lx = __shfl_sync(kSettleFull, pr.lx, 0);
-  pr.qx = __shfl_sync(kSettleFull, pr.qx, 0);
-  // inclusive prefix sums in the total order (fixed order)
+  // 3. the list, entry 32 r + lane in round r
+  uint32_t idx[kListRounds];
+  float val[kListRounds], ev[kListRounds], qv[kListRounds], cum[kListRounds];
   float run = 0.f;
-#pragma unroll 1
-  for (int r = 0; r < nr; ++r) {
+#pragma unroll
+  for (int r = 0; r < kListRounds; ++r) {
     const int i = 32 * r + lane;
-    float inc = i < n_k ? L.e[i] : 0.f;
+    const bool in = i < n_k;
+    const u64 key = in ? lk[i] : 0ull;
+    idx[r] = in ? key64_idx(key) : 0xffffffffu;
+    val[r] = in ? from_okey((uint32_t)(key >> 32)) : 0.f;
+    ev[r] = in ? ex2((val[r] - m) * c) : 0.f;
+    qv[r] = in ? lq[i] : 0.f;
+    // inclusive prefix sums in the total order (fixed order)
+    float inc = ev[r];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(kSettleFull, inc, o);
       if (lane >= o) inc += y;
     }
-    if (i < n_k) L.cum[i] = run + inc;
+    cum[r] = run + inc;
     run += __shfl_sync(kSettleFull, inc, 31);
   }
   __syncwarp();
-  const float Zk = L.cum[n_k - 1];
+  TLP(u, 4);
+  const float Zk = list_get(cum, n_k - 1);
   uint32_t flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
   int n_s = n_k;
   if (cfg.P < 1.0f) {
     const float target = cfg.P * Zk;
-#pragma unroll 1
-    for (int r = 0; r < nr; ++r) {
-      const int i = 32 * r + lane;
-      const unsigned ball = __ballot_sync(kSettleFull, i < n_k && L.cum[i] >= target);
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      const unsigned ball = __ballot_sync(kSettleFull, 32 * r + lane < n_k && cum[r] >= target);
       if (ball) {
-        n_s = 32 * r + __ffs(ball);
-        break;
+        n_s = min(n_s, 32 * r + __ffs(ball));
       }
     }
-    const float at = L.cum[n_s - 1] / Zk;
-    const float bef = n_s >= 2 ? L.cum[n_s - 2] / Zk : 0.f;
+    const float at = list_get(cum, n_s - 1) / Zk;
+    const float bef = n_s >= 2 ? list_get(cum, n_s - 2) / Zk : 0.f;
     if (fabsf(at - cfg.P) < kMargin || fabsf(cfg.P - bef) < kMargin) flags |= SPEC_F_MARGIN_TOPP;
   }
-  const float Zs = L.cum[n_s - 1];
+  const float Zs = list_get(cum, n_s - 1);
   const float invZ = 1.0f / Zs;
   const float lnZ = logf(Zs);
-  const int ns_r = (n_s + 31) >> 5;
   float alpha_v = 0.f;
   AcceptInfo ai;
   ai.valid = true;
@@ -1006,12 +1092,11 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   bool need_race = !has_q;
   if (has_q) {
     float a = 0.f, ex = -1.f;
-#pragma unroll 1
-    for (int r = 0; r < ns_r; ++r) {
-      const int i = 32 * r + lane;
-      if (i < n_s) {
-        a += fminf(L.e[i] * invZ, L.q[i]);
-        if (L.idx[i] == (uint32_t)pr.x) ex = L.e[i];
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      if (32 * r + lane < n_s) {
+        a += fminf(ev[r] * invZ, qv[r]);
+        if (idx[r] == (uint32_t)pr.x) ex = ev[r];
       }
     }
     alpha_v = warp_sum(a);
@@ -1028,125 +1113,93 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
     need_race = !ai.accept;
   }
-  TLP(u, 3);
+  TLP(u, 5);
   // 4. the draw: the two-level race over the kept entries (blocks by index)
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
   if (need_race) {
+    float* Lw = reinterpret_cast<float*>(S.sel);
+    float* Lu = Lw + kTopkSmall;
+    uint32_t* Lb = reinterpret_cast<uint32_t*>(Lu + kTopkSmall);
 #pragma unroll 1
     for (int attempt = 0; attempt < 2; ++attempt) {
-      const bool use_p = attempt == 1;          // empty residual: draw from p
-#pragma unroll 1
-      for (int r = 0; r < ns_r; ++r) {
+      const bool resid = has_q && attempt == 0;   // attempt 1: an empty residual, draw from p
+      float w[kListRounds], wu[kListRounds];
+      uint32_t bl[kListRounds];
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < kListRounds; ++r) {
         const int i = 32 * r + lane;
-        if (i < n_s) {
-          const float p = L.e[i] * invZ;
-          const float w = (has_q && !use_p) ? fmaxf(p - L.q[i], 0.f) : p;
-          L.w[i] = w;
-          L.wu[i] = w + ((has_q && !use_p) ? 2.0f * L.q[i] : 0.f);
+        const bool in = i < n_s;
+        const float p = ev[r] * invZ;
+        w[r] = in ? (resid ? fmaxf(p - qv[r], 0.f) : p) : 0.f;
+        wu[r] = w[r] + ((in && resid) ? 2.0f * qv[r] : 0.f);
+        bl[r] = idx[r] / kRaceBlock;
+        if (i < kTopkSmall) {
+          Lw[i] = w[r];
+          Lu[i] = wu[r];
+          Lb[i] = bl[r];
         }
       }
       __syncwarp();
-      // level 1: every block holding a kept entry races once, with the
-      // block's weights summed in list order.  Blocks get the slots of a
-      // 256-entry table in shared memory (at most kTopkSmall blocks, so every
-      // probe ends); the entry whose insertion made a slot races for it.
-      uint32_t* bkey = S.hist;
-      float2* bsum = reinterpret_cast<float2*>(S.sel);
-      for (int t = lane; t < 256; t += 32) {
-        bkey[t] = 0xffffffffu;
-        bsum[t] = make_float2(0.f, 0.f);
-      }
-      __syncwarp();
-      int slot[kTopkSmall / 32];
-      bool owner[kTopkSmall / 32];
+      // level 1: a block's weights summed in list order; the block's first
+      // entry with weight races for it
+      float W[kListRounds], WU[kListRounds];
+      bool owner[kListRounds];
 #pragma unroll
-      for (int r = 0; r < kTopkSmall / 32; ++r) {
-        const int i = 32 * r + lane;
-        slot[r] = -1;
-        owner[r] = false;
-        if (r < ns_r && i < n_s && L.w[i] > 0.f) {
-          const uint32_t bb = L.idx[i] / kRaceBlock;
-          uint32_t h = (bb * 2654435761u) >> 24;
-#pragma unroll 1
-          for (int probe = 0; probe < 256; ++probe) {
-            const uint32_t old = atomicCAS(&bkey[h], 0xffffffffu, bb);
-            if (old == 0xffffffffu || old == bb) {
-              slot[r] = (int)h;
-              owner[r] = old == 0xffffffffu;
-              break;
+      for (int r = 0; r < kListRounds; ++r) {
+        W[r] = 0.f;
+        WU[r] = 0.f;
+        owner[r] = w[r] > 0.f;
+      }
+#pragma unroll 2
+      for (int j = 0; j < n_s; ++j) {
+        const float wj = Lw[j], uj = Lu[j];
+        const uint32_t bj = Lb[j];
+        if (wj > 0.f) {
+#pragma unroll
+          for (int r = 0; r < kListRounds; ++r)
+            if (bj == bl[r]) {
+              W[r] += wj;
+              WU[r] += uj;
+              if (j < 32 * r + lane) owner[r] = false;
             }
-            h = (h + 1u) & 255u;
-          }
-        }
-      }
-      __syncwarp();
-      // round by round; lanes of one round sharing a slot add in lane order
-#pragma unroll
-      for (int r = 0; r < kTopkSmall / 32; ++r) {
-        if (r >= ns_r) break;
-        const int i = 32 * r + lane;
-        const bool has = slot[r] >= 0;
-        const unsigned grp = __match_any_sync(kSettleFull, has ? slot[r] : -1 - lane);
-        const int rank = __popc(grp & ((1u << lane) - 1u));
-        const int nrank = (int)__reduce_max_sync(kSettleFull, has ? (uint32_t)__popc(grp) : 0u);
-#pragma unroll 1
-        for (int it = 0; it < nrank; ++it) {
-          if (has && rank == it) {
-            float2 sm = bsum[slot[r]];
-            sm.x += L.w[i];
-            sm.y += L.wu[i];
-            bsum[slot[r]] = sm;
-          }
-          __syncwarp();
         }
       }
       Race r1;
       race_init(r1);
 #pragma unroll
-      for (int r = 0; r < kTopkSmall / 32; ++r) {
-        if (owner[r]) {
-          const uint32_t bb = L.idx[32 * r + lane] / kRaceBlock;
-          const float2 sm = bsum[slot[r]];
-          race_consider(r1, sm.x, sm.y - sm.x, bb, block_word(A, row, pos, bb));
-        }
-      }
+      for (int r = 0; r < kListRounds; ++r)
+        if (owner[r]) race_consider(r1, W[r], WU[r] - W[r], bl[r], block_word(A, row, pos, bl[r]));
       warp_race_merge(r1);
       if (r1.s1 < 0.f) {
         draw_flags |= SPEC_F_RESIDUAL_EMPTY;
-        __syncwarp();
         continue;
       }
       // level 2: the entries of the winning block
       Race r2;
       race_init(r2);
-#pragma unroll 1
-      for (int r = 0; r < ns_r; ++r) {
-        const int i = 32 * r + lane;
-        if (i < n_s && L.w[i] > 0.f && L.idx[i] / kRaceBlock == r1.v1)
-          race_consider(r2, L.w[i], (has_q && !use_p) ? 2.0f * L.q[i] : 0.f, L.idx[i],
-                        race_word(A, row, pos, L.idx[i]));
-      }
+#pragma unroll
+      for (int r = 0; r < kListRounds; ++r)
+        if (w[r] > 0.f && bl[r] == r1.v1) race_consider(r2, w[r], wu[r] - w[r], idx[r], race_word(A, row, pos, idx[r]));
       warp_race_merge(r2);
       y = r2.v1;
       if (draw_margin(r1) || draw_margin(r2)) draw_flags |= SPEC_F_MARGIN_DRAW;
       break;
     }
   }
-  TLP(u, 4);
+  TLP(u, 6);
   // the logit of the drawn entry, from the list
   float vy = m;
   {
     float vv = 0.f;
     bool own = false;
-#pragma unroll 1
-    for (int r = 0; r < nr; ++r) {
-      const int i = 32 * r + lane;
-      if (i < n_k && L.idx[i] == y) {
-        vv = L.val[i];
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r)
+      if (32 * r + lane < n_k && idx[r] == y) {
+        vv = val[r];
         own = true;
       }
-    }
     const unsigned ob = __ballot_sync(kSettleFull, own);
     if (ob) vy = __shfl_sync(kSettleFull, vv, __ffs(ob) - 1);
   }
@@ -1166,7 +1219,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       rec.draw_flags = draw_flags;
     }
   }
-  TLP(u, 5);
+  TLP(u, 7);
   commit_record(A, tag, u, row, rec);
 }
 

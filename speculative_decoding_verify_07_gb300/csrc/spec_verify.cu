@@ -51,7 +51,7 @@ int verify_check(const void* logits, int logits_dtype, const float* draft_probs,
 int verify_launch(const void* logits, int logits_dtype, const float* draft_probs, const int32_t* draft_tokens,
                   const spec_params_t* params, uint64_t seed, uint32_t row_base, int B, int k, int V,
                   int32_t* tokens, int32_t* accept_len, float* logprobs, float* alpha, uint32_t* flags,
-                  void* workspace, void* cuda_stream) {
+                  void* workspace, void* cuda_stream, const FusedCommit* fc) {
   const size_t es = logits_dtype == SPEC_BF16 ? 2 : 4;
   const Layout L = ws_layout(B, k, V);
   Args A;
@@ -74,6 +74,8 @@ int verify_launch(const void* logits, int logits_dtype, const float* draft_probs
   A.ust = reinterpret_cast<u64*>(ws + L.ust);
   A.urec = reinterpret_cast<u64*>(ws + L.urec);
   A.order = reinterpret_cast<uint32_t*>(ws + L.order);
+  A.done = reinterpret_cast<u64*>(ws + L.done);
+  if (fc) A.fc = *fc;
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);
   A.row_base = row_base;
@@ -100,5 +102,44 @@ extern "C" int spec_verify(const void* logits, int logits_dtype, const float* dr
                                      accept_len, logprobs, alpha, flags, true, workspace, workspace_bytes);
   if (rc != SPEC_OK || B == 0) return rc;
   return specv::verify_launch(logits, logits_dtype, draft_probs, draft_tokens, params, seed, row_base, B, k, V,
-                              tokens, accept_len, logprobs, alpha, flags, workspace, cuda_stream);
+                              tokens, accept_len, logprobs, alpha, flags, workspace, cuda_stream, nullptr);
+}
+
+extern "C" int spec_verify_commit(const void* logits, int logits_dtype, const float* draft_probs,
+                                  const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
+                                  uint32_t row_base, int B, int k, int V, int32_t* tokens, int32_t* accept_len,
+                                  float* logprobs, float* alpha, uint32_t* flags, void* workspace,
+                                  size_t workspace_bytes, const float* verify_rec, const uint16_t* verify_conv,
+                                  const int32_t* cache_slot, float* cache_rec, uint16_t* cache_conv, int L, int H,
+                                  int Dk, int Dv, int W, int C, int slots, void* cuda_stream) {
+  using namespace specv;
+  int rc = verify_check(logits, logits_dtype, draft_probs, draft_tokens, params, B, k, V, tokens, accept_len,
+                        logprobs, alpha, flags, true, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  const int S = k + 1;
+  rc = commit_check(verify_rec, verify_conv, accept_len, cache_slot, nullptr, nullptr, cache_rec, cache_conv, L, B, S,
+                    H, Dk, Dv, W, C, slots, flags);
+  if (rc != SPEC_OK || B == 0) return rc;
+  FusedCommit F;
+  memset(&F, 0, sizeof(F));
+  if (L > 0) {
+    F.vrec = reinterpret_cast<const unsigned char*>(verify_rec);
+    F.vconv = reinterpret_cast<const unsigned char*>(verify_conv);
+    F.slot = cache_slot;
+    F.crec = reinterpret_cast<unsigned char*>(cache_rec);
+    F.cconv = reinterpret_cast<unsigned char*>(cache_conv);
+    F.rec_bytes = verify_rec ? (long long)H * Dk * Dv * 4 : 0;
+    F.conv_bytes = verify_conv ? (long long)W * C * 2 : 0;
+    F.L = L;
+    F.slots = slots;
+    F.rec_jobs = (int)((F.rec_bytes + kJobBytes - 1) / kJobBytes);
+    F.conv_jobs = (int)((F.conv_bytes + kJobBytes - 1) / kJobBytes);
+    F.bulk = (!verify_rec || (aligned(verify_rec, 16) && aligned(cache_rec, 16) && F.rec_bytes % 16 == 0)) &&
+             (!verify_conv || (aligned(verify_conv, 16) && aligned(cache_conv, 16) && F.conv_bytes % 16 == 0));
+    const long long jobs = (long long)B * L * (F.rec_jobs + F.conv_jobs);
+    if (jobs > 0x7fffffffLL) return SPEC_E_DIM;
+    F.on = jobs > 0 ? 1 : 0;
+  }
+  return verify_launch(logits, logits_dtype, draft_probs, draft_tokens, params, seed, row_base, B, k, V, tokens,
+                       accept_len, logprobs, alpha, flags, workspace, cuda_stream, &F);
 }
