@@ -565,10 +565,68 @@ def commit_component(dev, peak, peak_kind, acc_mixed):
     nbytes = sh.bytes_moved(int((accl > 0).sum().item()))
     us = statistics.mean(t)
     ach = nbytes / (us * 1e-6) / 1e9
-    return {"workload": "commit 64 rows x 24 layers (16x128x128 fp32 + 4x4096 bf16), accept_len U{1,2,3}",
-            "us": round(us, 2), "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1),
-            "frac": round(ach / peak, 4), "peak_source": peak_kind,
-            "traffic": traffic_record("commit_kernel", kernel_source_hash(["spec_commit.cu"]))}
+    res = {"workload": "commit 64 rows x 24 layers (16x128x128 fp32 + 4x4096 bf16), accept_len U{1,2,3}",
+           "us": round(us, 2), "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1),
+           "frac": round(ach / peak, 4), "peak_source": peak_kind,
+           "traffic": traffic_record("commit_kernel", kernel_source_hash(["spec_commit.cu"]))}
+
+    # the commit fused into the verify launch, against verify + commit as two launches
+    inp = synth.make_mixed(seed_offset=700)
+    logits = torch.from_numpy(inp.logits).to(torch.bfloat16).to(dev)
+    q = torch.from_numpy(inp.q).to(dev)
+    x = torch.from_numpy(inp.drafts).to(dev)
+    params = sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev)
+    ws = sv.new_workspace(B, K, V, dev)
+    out = sv.VerifyOutputs(B, K, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # inputs leave L2 between calls
+
+    def two(i):
+        flush.fill_(i & 255)
+        sv.spec_verify(logits, q, x, params, inp.seed, out=out, workspace=ws)
+        sv.spec_commit(vrec, vconv, out.accept_len, slot, crec, cconv)
+
+    def fused(i):
+        flush.fill_(i & 255)
+        sv.spec_verify_commit(logits, q, x, params, inp.seed, vrec, vconv, slot, crec, cconv, out=out, workspace=ws)
+
+    def flush_only(i):
+        flush.fill_(i & 255)
+
+    for fn_ in (two, fused, flush_only):
+        for i in range(3):
+            fn_(i)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    t_two = statistics.mean(_time_calls(two, 8, st))
+    t_fused = statistics.mean(_time_calls(fused, 8, st))
+    t_flush = statistics.mean(_time_calls(flush_only, 8, st))
+    live = int((out.accept_len > 0).sum().item())
+    res["verify_commit_fused"] = {
+        "workload": "spec_verify 64x3x151936 bf16 mixed + commit 64 rows x 24 layers, one launch vs two",
+        "us_fused": round(t_fused - t_flush, 2), "us_two_launches": round(t_two - t_flush, 2),
+        "saved_us": round(t_two - t_fused, 2), "commit_bytes": int(sh.bytes_moved(live))}
+    del flush
+
+    # the zero-copy commit: full accepts trade slots, only partial ones copy
+    vrec_s = vrec[:, :, :sh.S - 1].contiguous()
+    vconv_s = vconv[:, :, :sh.S - 1].contiguous()
+    crec_s = torch.zeros((sh.L, 2 * sh.B, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
+    cconv_s = torch.zeros((sh.L, 2 * sh.B, sh.W, sh.C), dtype=torch.int16, device=dev)
+    slot_of_row = torch.arange(sh.B, dtype=torch.int32, device=dev)
+    scratch = torch.arange(sh.B, 2 * sh.B, dtype=torch.int32, device=dev)
+    fn_s = lambda i: sv.spec_commit_swap(vrec_s, vconv_s, accl, slot_of_row, scratch, crec_s, cconv_s)
+    for i in range(3):
+        fn_s(i)
+    torch.cuda.synchronize()
+    t_s = statistics.mean(_time_calls(fn_s, 10, st))
+    partial = int(((accl > 0) & (accl < sh.S)).sum().item())
+    swap_bytes = sh.bytes_moved(partial)
+    res["commit_swap"] = {
+        "workload": "spec_commit_swap, same states, scratch slot per row (accept_len U{1,2,3})",
+        "us": round(t_s, 2), "algorithmic_bytes": int(swap_bytes),
+        "bytes_saved_vs_copy": int(nbytes - swap_bytes), "rows_swapped": int((accl == sh.S).sum().item()),
+        "gbs": round(swap_bytes / (t_s * 1e-6) / 1e9, 1)}
+    return res
 
 
 def run_only(args):

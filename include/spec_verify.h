@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define SPEC_ABI_VERSION 2
+#define SPEC_ABI_VERSION 3
 
 /* Largest vocabulary and draft length accepted by spec_verify. */
 #define SPEC_MAX_V 524288
@@ -109,7 +109,7 @@ enum {
  *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
  *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
  *                 settle or finalize wait for records, 8 the row-order wait
- *                 of batches above 256 rows, 16 the settle queue); 0 when
+ *                 of batches above 256 rows, 16 a grid barrier); 0 when
  *                 every wait ended normally.                                */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
@@ -287,8 +287,8 @@ const char* spec_status_string(int code);
  *   verify_rec, verify_conv, cache_slot, cache_rec, cache_conv, L, H, Dk, Dv,
  *   W, C, slots: as spec_commit, with S = k + 1 states per row; L == 0
  *   verifies only.
- * Errors: those of spec_verify, then those of spec_commit; a refused call
- * enqueues nothing. */
+ * Errors: those of spec_commit and of spec_verify; every argument is checked
+ * before the device is queried, and a refused call enqueues nothing. */
 int spec_verify_commit(const void* logits, int logits_dtype, const float* draft_probs,
                        const int32_t* draft_tokens, const spec_params_t* params, uint64_t seed,
                        uint32_t row_base, int B, int k, int V, int32_t* tokens, int32_t* accept_len,

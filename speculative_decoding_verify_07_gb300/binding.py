@@ -63,6 +63,9 @@ def _load():
     lib.spec_commit.restype = i32
     lib.spec_commit_swap.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [i32] * 9 + [vp, vp]
     lib.spec_commit_swap.restype = i32
+    lib.spec_verify_commit.argtypes = ([vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz]
+                                       + [vp] * 5 + [i32] * 7 + [vp])
+    lib.spec_verify_commit.restype = i32
     lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_noalloc.restype = i32
     lib.spec_philox4x32_10.argtypes = [vp, u64, vp, ctypes.c_int64, vp]
@@ -234,14 +237,8 @@ def spec_verify_noalloc(logits: torch.Tensor, draft_probs, draft_tokens, params:
     return out
 
 
-def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cache_conv,
-                flags=None, stream=None):
-    """Commit accepted states (see spec_commit in spec_verify.h).
-
-    verify_rec [L, B, S, H, Dk, Dv] float32 or None; verify_conv [L, B, S, W, C]
-    16-bit (bfloat16/int16) or None; accept_len [B] int32; cache_slot [B] int32
-    or None; cache_rec [L, slots, H, Dk, Dv]; cache_conv [L, slots, W, C].
-    """
+def _commit_dims(verify_rec, verify_conv, cache_rec, cache_conv):
+    """(L, B, S, H, Dk, Dv, W, C, slots) of the commit buffers, checked."""
     if verify_rec is not None:
         L, B, S, H, Dk, Dv = verify_rec.shape
         slots = cache_rec.shape[1]
@@ -270,6 +267,18 @@ def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cach
                   (cache_conv, "cache_conv")):
         if t is not None and not t.is_contiguous():
             raise ValueError(f"{nm} must be contiguous")
+    return L, B, S, H, Dk, Dv, W, C, slots
+
+
+def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cache_conv,
+                flags=None, stream=None):
+    """Commit accepted states (see spec_commit in spec_verify.h).
+
+    verify_rec [L, B, S, H, Dk, Dv] float32 or None; verify_conv [L, B, S, W, C]
+    16-bit (bfloat16/int16) or None; accept_len [B] int32; cache_slot [B] int32
+    or None; cache_rec [L, slots, H, Dk, Dv]; cache_conv [L, slots, W, C].
+    """
+    L, B, S, H, Dk, Dv, W, C, slots = _commit_dims(verify_rec, verify_conv, cache_rec, cache_conv)
     dev = accept_len.device
     _check(accept_len, "accept_len", torch.int32, (B,), dev)
     if cache_slot is not None:
@@ -279,6 +288,53 @@ def spec_commit(verify_rec, verify_conv, accept_len, cache_slot, cache_rec, cach
                          _ptr(flags), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_commit")
+
+
+def spec_verify_commit(logits: torch.Tensor, draft_probs, draft_tokens, params: torch.Tensor, seed: int,
+                       verify_rec, verify_conv, cache_slot, cache_rec, cache_conv,
+                       out: VerifyOutputs | None = None, workspace: torch.Tensor | None = None,
+                       stream=None, row_base: int = 0) -> VerifyOutputs:
+    """spec_verify and spec_commit in one launch (see spec_verify_commit in
+    spec_verify.h): the verify outputs, and each row's accepted state
+    copied into its cache slot; S = k + 1 states per row."""
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, k+1, V]")
+    B, k1, V = logits.shape
+    k = k1 - 1
+    dev = logits.device
+    if logits.dtype == torch.float32:
+        dt = SPEC_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    if k > 0:
+        _check(draft_probs, "draft_probs", torch.float32, (B, k, V), dev)
+        _check(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _check(params, "params", torch.int32, (B, 4), dev)
+    L, Bc, S, H, Dk, Dv, W, C, slots = _commit_dims(verify_rec, verify_conv, cache_rec, cache_conv)
+    if (Bc, S) != (B, k1):
+        raise ValueError("state buffers must be [L, B, k+1, ...]")
+    if cache_slot is not None:
+        _check(cache_slot, "cache_slot", torch.int32, (B,), dev)
+    if out is None:
+        out = VerifyOutputs(B, k, dev)
+    if workspace is None:
+        workspace = new_workspace(B, k, V, dev)
+    rc = LIB.spec_verify_commit(_ptr(logits), dt, _ptr(draft_probs) if k > 0 else None,
+                                _ptr(draft_tokens) if k > 0 else None, _ptr(params),
+                                ctypes.c_uint64(int(seed) & (2 ** 64 - 1)),
+                                ctypes.c_uint32(int(row_base) & 0xFFFFFFFF), B, k, V,
+                                _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.logprobs),
+                                _ptr(out.alpha) if k > 0 else None, _ptr(out.flags),
+                                _ptr(workspace), workspace.numel(),
+                                _ptr(verify_rec), _ptr(verify_conv), _ptr(cache_slot), _ptr(cache_rec),
+                                _ptr(cache_conv), L, H, Dk, Dv, W, C, slots, _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_verify_commit")
+    return out
 
 
 def spec_commit_swap(verify_rec, verify_conv, accept_len, slot_of_row, scratch_slot, cache_rec, cache_conv,

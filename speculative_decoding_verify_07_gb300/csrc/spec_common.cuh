@@ -29,6 +29,7 @@ constexpr int kMaxListCand = 640;          // ... when the tiles' candidate list
 // Polls of a bounded wait before it gives up (with a short sleep per poll:
 // a few hundred milliseconds in all).
 constexpr long long kSpinLimit = 1ll << 21;
+constexpr int kCtaWarps = 12;              // warps of a verify CTA
 
 // Tile geometry.  Every stream warp owns two shared buffers of kSlot bytes.
 // An A tile is one buffer of logits; a B tile is logits (read again, from
@@ -56,7 +57,7 @@ enum {
   ERR_COPY_WAIT = 2,       // a tile's bulk copy did not complete
   ERR_RECORD_WAIT = 4,     // a settle or finalize gave up waiting for records
   ERR_ORDER_WAIT = 8,      // a CTA gave up waiting for the row order
-  ERR_QUEUE = 16           // a settle-queue wait gave up
+  ERR_BARRIER = 16         // a grid barrier wait gave up
 };
 
 struct WsHeader {
@@ -64,14 +65,16 @@ struct WsHeader {
   uint32_t ctas_done;     // CTAs that left the kernel
   uint32_t error;         // ERR_* bits of the running call
   uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
-  uint32_t next_item;     // next item of the stream sequence
+  uint32_t pad_item;
   uint32_t inject;        // test hook: nonzero makes the finalize of row 0 wait for a tag nothing writes
   uint32_t last_error;    // ERR_* bits of the last completed call
   uint32_t pad0;
   uint32_t n_class[4];    // rows per class (large batches)
   uint32_t commit_next;   // fused commit: next copy job
   uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
-  uint32_t pad[45];
+  uint32_t bar;           // grid barrier arrivals of the running call
+  uint32_t settle_next;   // next warp-settled unit of the settle pass
+  uint32_t pad[43];
   uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
   uint32_t pad1[4];
 };
@@ -213,8 +216,6 @@ struct Args {
   int B, k, V, U;
   int NTA, NTB;           // record strides per unit: A tiles, B tiles
   int n_ctas;             // CTAs of the kernel
-  int n_settle;           // settle CTAs: blocks 0, stride, 2 stride, ... (n_settle of them)
-  int settle_stride;
   int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;
@@ -230,7 +231,8 @@ struct Args {
 enum {
   TL_CTA_START = 0, TL_CTA_END = 160, TL_FIRST_DATA = 320, TL_STREAM_END = 2368, TL_SETTLE_END = 4416,
   TL_ATICK = 4672, TL_SA_START = 6720, TL_SA_END = 8768, TL_BTICK = 10816, TL_SB_START = 12864,
-  TL_SB_END = 14912, TL_FINAL = 16960, TL_ITEM = 17984, TL_PHASE = 34368, TL_SIZE = 34368 + 2048 * 8
+  TL_SB_END = 14912, TL_FINAL = 16960, TL_ITEM = 17984, TL_PHASE = 34368, TL_ISTART = 34368 + 2048 * 8,
+  TL_IWARP = TL_ISTART + 16384, TL_SIZE = TL_IWARP + 16384
 };
 #ifdef SPEC_TIMELINE
 static __device__ unsigned long long g_tl[TL_SIZE];
@@ -646,16 +648,26 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
   if (g < G) {
     load_group<kBF16>(A, lrow, g, true, v);
     if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv);
-    const uint32_t blk = (uint32_t)g * 2u;   // Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
-    uint4 p0 = make_uint4(blk, (uint32_t)pos, srow(A, row), 1u);
-    uint4 p1 = make_uint4(blk + 1u, (uint32_t)pos, srow(A, row), 1u);
-    philox4x32_10_pair(p0, p1, A.key0, A.key1);
+    // the Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
+    const uint32_t blk = (uint32_t)g * 2u;
+    const uint4 p0 = philox4x32_10(make_uint4(blk, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
+    const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
     float w[8], tq[8];
     group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
-    const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    // one race step per entry, in a rolled loop (small code)
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+      float wj = w[0], tj = tq[0];
+      uint32_t pj = p0.x;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (w[j] > 0.f) race_consider(r, w[j], tq[j], (uint32_t)(g * 8 + j), pw[j]);
+      for (int t = 1; t < 8; ++t)
+        if (j == t) {
+          wj = w[t];
+          tj = tq[t];
+          pj = t < 4 ? word_of(p0, t) : word_of(p1, t - 4);
+        }
+      if (wj > 0.f) race_consider(r, wj, tj, (uint32_t)(g * 8 + j), pj);
+    }
   }
   warp_race_merge(r);
   if (ly != nullptr && r.s1 >= 0.f) {

@@ -37,22 +37,6 @@ static __device__ __noinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_
   return c;
 }
 
-// Two Philox blocks with the same key, their rounds interleaved (for a
-// caller that needs both at once).
-__device__ __forceinline__ void philox4x32_10_pair(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
-#pragma unroll 1
-  for (int i = 0; i < 10; ++i) {
-    const uint32_t alo0 = 0xD2511F53u * a.x, ahi0 = __umulhi(0xD2511F53u, a.x);
-    const uint32_t alo1 = 0xCD9E8D57u * a.z, ahi1 = __umulhi(0xCD9E8D57u, a.z);
-    const uint32_t blo0 = 0xD2511F53u * b.x, bhi0 = __umulhi(0xD2511F53u, b.x);
-    const uint32_t blo1 = 0xCD9E8D57u * b.z, bhi1 = __umulhi(0xCD9E8D57u, b.z);
-    a = make_uint4(ahi1 ^ a.y ^ k0, alo1, ahi0 ^ a.w ^ k1, alo0);
-    b = make_uint4(bhi1 ^ b.y ^ k0, blo1, bhi0 ^ b.w ^ k1, blo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
   return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
 }

@@ -1,41 +1,33 @@
 // spec_verify: the verify kernel (sm_103a).
 //
 // One persistent CTA of 12 warps per SM, launched cooperatively (every CTA
-// is resident, so warps may wait on one another; every such wait is
-// bounded).  CTAs take one of two roles, so that each SM runs one kind of
-// code and keeps it in its instruction cache:
-//   * Stream CTAs (about 9 in 10).  Each of their 12 warps owns two 8.5 KB
-//     shared-memory buffers and has the copy engine fill one
-//     (cp.async.bulk completed on an mbarrier) while it reduces the other.
-//     The tiles of all units form one sequence of segments, taken in order
-//     from one counter:
-//       unfiltered rows in waves: A tiles of the wave's drafted positions
-//       and bonus positions, then the B tiles of the wave before;
-//       A tiles of small top-k rows; A tiles of greedy rows; the B tiles of
-//       the last unfiltered wave (placed inside the top-k or greedy tiles,
-//       a fixed number of tiles after that wave's A tiles).
-//     An A tile (4352 bf16 / 2048 fp32 logits of one unit) yields the tile
-//     max, the softmax sum relative to it, the first argmax (greedy), the
-//     level-1 race of its 256-entry blocks (bonus positions) or the 8
-//     largest entries in the total order (small top-k).  A B tile (1280 /
-//     1024 logits, read again from L2, plus q) computes alpha = sum min(p, q)
-//     and the level-1 race of the residual from the unit's published state.
-//     After a tile's record the warp adds one to the unit's tile count (a
-//     reduction nobody waits for).
-//   * Settle CTAs (about 1 in 10, every stride-th block).  Their warps take
-//     the settle tasks -- one per unit after its A tiles, one per drafted
-//     unfiltered unit after its B tiles -- in the order of the sequence,
-//     task t to settle warp t mod (warps); a warp waits for its task's tile
-//     count, settles the unit (spec_settle.cuh) and clears the count.  Tasks
-//     come in the order their tiles do, and a B tile only waits for a state
-//     that an earlier task publishes, so every wait ends.  The last settled
-//     unit of a row resolves its accept chain and writes the row's outputs.
-//   * Rows that need a global threshold search (spec_general.cuh) are taken
-//     last by the CTAs' first 256 threads.
-// Results pass between warps as 64-bit words tagged with the call's epoch,
-// which a reader polls; nothing stores with a fence and no CTA waits at a
-// grid barrier.  Reductions have a fixed order and no floating-point
-// atomics are used, so results are bit-reproducible.
+// is resident, so CTAs may wait on one another; every such wait is
+// bounded).  The work runs in passes separated by grid barriers, so that
+// each pass runs one kind of code on every SM and the latency-bound settles
+// never queue behind the stream's copies:
+//   1. A pass.  Every warp owns two 8 KB shared-memory buffers and has the
+//      copy engine fill one (cp.async.bulk completed on an mbarrier) while
+//      it reduces the other; the A tiles of all units (4096 bf16 / 2048
+//      fp32 logits) are taken from one counter, class by class (small
+//      top-k, greedy, unfiltered rows last, so that their logits are still
+//      in L2 for the B pass).  A tile yields its max, the softmax sum
+//      relative to it, the first argmax (greedy), the level-1 race of its
+//      256-entry blocks (bonus positions) or its 8 largest entries in the
+//      total order (small top-k), as tagged record words.
+//   2. Settles.  One warp per unit (spec_settle.cuh): greedy and small
+//      top-k units and bonus positions are settled; a drafted unfiltered
+//      unit takes its accept test and publishes its state.  Warps without a
+//      unit bring the q rows of the B pass into L2 meanwhile.
+//   3. B pass (drafted positions of unfiltered rows only).  A B tile (1280
+//      bf16 / 1024 fp32 logits, read again from L2, plus q) computes alpha =
+//      sum min(p, q) and the level-1 race of the residual from the state.
+//   4. Their settles: alpha and the residual draw.
+// The last settled unit of a row resolves its accept chain and writes the
+// row's outputs.  Rows that need a global threshold search
+// (spec_general.cuh) are taken last by the CTAs' first 256 threads, and the
+// fused commit (spec_fused.cuh) follows.  Results pass between warps as
+// 64-bit words tagged with the call's epoch; reductions have a fixed order
+// and no floating-point atomics are used, so results are bit-reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,26 +41,13 @@
 
 namespace specv {
 
-constexpr int kNW = 12;                // warps per CTA (stream warps of a stream CTA, settle warps of a settle CTA)
+constexpr int kNW = kCtaWarps;         // warps per CTA
 constexpr int kAllThreads = kNW * 32;
 constexpr int kOrderSmem = 256;        // batches up to this many rows keep order and configs in shared memory
 constexpr int kStage = 64;             // per-warp staging of a top-k tile's candidates
-constexpr int kMaxWaves = 40;
-constexpr int kMaxSeg = 4 * kMaxWaves + 8;   // segments of the item sequence (2 A and at most 2 more per wave, 2 classes)
-constexpr int kSettleEvery = 9;        // one settle CTA per this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kAllThreads >= kOrderSmem, "one placement round for a shared-memory order");
 static_assert(kAllThreads >= kThreads, "the general phase uses the first kThreads threads");
-
-// A segment of the item sequence: `nrows` rows from index `first` of the
-// class order, each contributing the units at positions pos_lo ..
-// pos_lo + upr - 1, each unit `tiles` tiles of one kind.
-struct Seg {
-  uint32_t start;     // first item of the segment
-  uint32_t first;
-  uint32_t nrows;
-  uint32_t packed;    // tiles | pos_lo << 16 | upr << 21 | kind << 26 (0 A, 1 B)
-};
 
 struct OrderScratch {
   int n_class[4];
@@ -82,19 +61,17 @@ struct alignas(128) VShm {
       unsigned char buf[kNW][2][kSlot];  // stream buffers
       u64 stage[kNW][kStage];            // top-k tile staging
     } s;
-    TopkScratch tk[kNW];                 // settle scratch (settle CTAs)
+    TopkCtaShm tkc;                      // settle scratch of a small top-k unit
     GenShm gen;                          // general-path group, after the roles
   };
-  unsigned long long bar[kNW][2];
+  unsigned long long bar[kNW][2];        // the warps' stream-buffer barriers
+  uint32_t par[kNW][2];                  // their phase parities (carried from the A pass to the B pass)
+  uint32_t broken[kNW];                  // a copy wait of the warp gave up: its buffers are not used again
+  uint32_t ticket[2];                    // the CTA's item counters of the A and B passes
   unsigned long long cbar[kNW][2];       // fused commit: the warps' copy barriers
-  Seg seg[kMaxSeg];
-  uint32_t tstart[kMaxSeg];              // first settle task of each segment
-  uint32_t bready[kMaxWaves];            // segment building: when each wave's B tiles fall due
   uint32_t order[kOrderSmem];
   RowPack cfg[kOrderSmem];
   OrderScratch ord;
-  int nseg;
-  uint32_t ntasks;
   int gtask;
   uint32_t tag;
 };
@@ -184,13 +161,13 @@ __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, 
 }
 
 // ---------------------------------------------------------------------------
-// The item sequence.
+// Work of the phases.  Units are taken class by class: small top-k rows,
+// greedy rows, then unfiltered rows (whose logits the B pass reads again, so
+// they are the last to enter L2); each row contributes its k + 1 positions.
 // ---------------------------------------------------------------------------
 struct Plan {
-  const uint32_t* order;
+  const uint32_t* order;    // rows by class: [unfiltered][small top-k][general][greedy]
   const RowPack* cfg;       // per-row configs in shared memory (null: classify from the parameters)
-  const Seg* seg;
-  int nseg;
   int nD, nT, nG, nX;       // rows: unfiltered, small top-k, greedy, general
   int NTA, NTB;             // tiles per unit of this call's dtype
 };
@@ -198,10 +175,9 @@ struct Plan {
 // A work item.  kind: 0 none, 1 A tile, 2 B tile.
 struct Item {
   int kind;
-  uint32_t t;               // index in the sequence
+  uint32_t t;               // index in its pass
   int reread;               // the logits are read again later (default L2 policy)
   int row, pos, u, c, n;    // unit, tile, valid entries in the tile
-  int ntiles;               // tiles of this kind in the unit
 };
 
 // Classification from the parameters (batches whose configs are not kept in
@@ -211,113 +187,48 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, Plan P, int row) {
   return P.cfg ? unpack_cfg(P.cfg[row]) : classify_row(A, row);
 }
 
-__device__ __forceinline__ Seg make_seg(uint32_t first, uint32_t nrows, int pos_lo, int upr, int tiles, int kind) {
-  Seg s;
-  s.start = 0;
-  s.first = first;
-  s.nrows = nrows;
-  s.packed = (uint32_t)tiles | ((uint32_t)pos_lo << 16) | ((uint32_t)upr << 21) | ((uint32_t)kind << 26);
-  return s;
+// Row ri of the A pass order: small top-k, greedy, unfiltered.
+__device__ __forceinline__ int a_row(const Plan& P, int ri) {
+  if (ri < P.nT) return (int)P.order[P.nD + ri];
+  ri -= P.nT;
+  if (ri < P.nG) return (int)P.order[P.nD + P.nT + P.nX + ri];
+  return (int)P.order[ri - P.nG];
 }
-__device__ __forceinline__ uint32_t seg_items(const Seg& s) {
-  return s.nrows * ((s.packed >> 21) & 31u) * (s.packed & 0xffffu);
-}
+__device__ __forceinline__ int a_units(const Args& A, const Plan& P) { return (P.nT + P.nG + P.nD) * (A.k + 1); }
+__device__ __forceinline__ int b_units(const Args& A, const Plan& P) { return P.nD * A.k; }
 
-// The segment table (thread 0 of every CTA builds the same one).  The A
-// tiles come class by class, the classes with the longest settles first:
-// unfiltered rows in waves (each wave's drafted positions, then its bonus
-// positions), small top-k rows, greedy rows.  The B tiles of a wave wait in
-// a queue until `b_delay` items have been placed after the wave's A tiles
-// (the wave's settles finish meanwhile) and are then inserted at the next
-// row boundary; waves still waiting at the end come last.
-__device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
-                                            int NTB, uint32_t b_delay) {
-  if (threadIdx.x != 0) return;
-  const int k = A.k, k1 = A.k + 1;
-  Seg* sg = S.seg;
-  int n = 0;
-  uint32_t pos = 0;   // items placed so far
-  int nw = 0, Rw = 1;
-  if (nD > 0) {
-    // a wave's A tiles are about b_delay items; waves of equal size
-    const uint32_t row_items = (uint32_t)k1 * (uint32_t)NTA;
-    Rw = (int)max(1u, b_delay / max(1u, row_items));
-    Rw = max(Rw, ceil_div(nD, kMaxWaves));
-    nw = ceil_div(nD, Rw);
-    Rw = ceil_div(nD, nw);
-    nw = ceil_div(nD, Rw);
-  }
-  uint32_t* ready = S.bready;   // waves [bh, bt) wait for their B tiles: the item count they wait for
-  int bh = 0, bt = 0;
-  auto place = [&](Seg sgm) {
-    sgm.start = pos;
-    pos += seg_items(sgm);
-    sg[n++] = sgm;
-  };
-  auto place_b = [&](int w) {
-    place(make_seg((uint32_t)(w * Rw), (uint32_t)min(Rw, nD - w * Rw), 0, k, NTB, 1));
-  };
-  // rows [f, f + nr) of an A class, split where a B wave falls due
-  auto place_rows = [&](uint32_t f, uint32_t nr, int pos_lo, int upr) {
-    const uint32_t per_row = (uint32_t)upr * (uint32_t)NTA;
-    while (nr > 0) {
-      while (bh < bt && pos >= ready[bh]) place_b(bh++);
-      uint32_t take = nr;
-      if (bh < bt) take = min(nr, (ready[bh] - pos + per_row - 1u) / per_row);
-      place(make_seg(f, take, pos_lo, upr, NTA, 0));
-      f += take;
-      nr -= take;
-    }
-  };
-  for (int i = 0; i < nw; ++i) {
-    const uint32_t f = (uint32_t)(i * Rw), nr = (uint32_t)min(Rw, nD - i * Rw);
-    if (k > 0) place_rows(f, nr, 0, k);
-    place_rows(f, nr, k, 1);
-    if (k > 0) ready[bt++] = pos + b_delay;
-  }
-  place_rows((uint32_t)nD, (uint32_t)nT, 0, k1);
-  place_rows((uint32_t)(nD + nT + nX), (uint32_t)nG, 0, k1);
-  while (bh < bt) place_b(bh++);
-  uint32_t tasks = 0;
-  for (int i = 0; i < n; ++i) {
-    S.tstart[i] = tasks;
-    tasks += sg[i].nrows * ((sg[i].packed >> 21) & 31u);
-  }
-  S.nseg = n;
-  S.ntasks = tasks;
-}
-
-// Item t of the sequence.
+// Item t of a pass: A tiles (pass 1) of every unit in the A pass order, or
+// B tiles (pass 2) of the drafted positions of unfiltered rows.
 template <bool kBF16>
-__device__ __noinline__ Item map_item(const Args& A, Plan P, uint32_t t) {
+__device__ __forceinline__ Item map_item(const Args& A, const Plan& P, int pass, uint32_t t, uint32_t n_items) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
-  // the last segment whose start is <= t
-  int lo = 0, hi = P.nseg - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.seg[mid].start <= t) lo = mid;
-    else hi = mid - 1;
-  }
-  const Seg s = P.seg[lo];
   it.t = t;
-  if (P.nseg == 0 || t < s.start || t - s.start >= seg_items(s)) return it;
-  const uint32_t tiles = s.packed & 0xffffu, pos_lo = (s.packed >> 16) & 31u, upr = (s.packed >> 21) & 31u;
-  const int kind = (int)((s.packed >> 26) & 1u);
-  const uint32_t off = t - s.start;
-  const uint32_t j = off / tiles;
-  it.c = (int)(off - j * tiles);
-  const uint32_t ri = j / upr;
-  it.row = (int)P.order[s.first + ri];
-  it.pos = (int)(pos_lo + (j - ri * upr));
+  if (t >= n_items) return it;
+  // a unit's tiles are taken in a rotated order (by the unit's index), so
+  // that the CTAs taking items at a fixed stride do not all get the same
+  // tile of every unit (the last tile of a unit is the partial one)
+  if (pass == 1) {
+    const uint32_t j = t / (uint32_t)P.NTA;
+    it.c = (int)((t - j * (uint32_t)P.NTA + j) % (uint32_t)P.NTA);
+    const uint32_t ri = j / (uint32_t)(A.k + 1);
+    it.pos = (int)(j - ri * (uint32_t)(A.k + 1));
+    it.row = a_row(P, (int)ri);
+    it.kind = 1;
+    it.reread = (int)ri >= P.nT + P.nG ? 1 : 0;   // unfiltered: the B tiles or the bonus draw read it again
+    it.n = min(G::EA, A.V - it.c * G::EA);
+  } else {
+    const uint32_t j = t / (uint32_t)P.NTB;
+    it.c = (int)((t - j * (uint32_t)P.NTB + j) % (uint32_t)P.NTB);
+    const uint32_t ri = j / (uint32_t)A.k;
+    it.pos = (int)(j - ri * (uint32_t)A.k);
+    it.row = (int)P.order[ri];
+    it.kind = 2;
+    it.reread = 0;
+    it.n = min(G::EB, A.V - it.c * G::EB);
+  }
   it.u = it.row * (A.k + 1) + it.pos;
-  it.kind = kind == 0 ? 1 : 2;
-  it.ntiles = (int)tiles;
-  // logits of an unfiltered unit are read again: by its B tiles (drafted
-  // positions) or by its draw's level-2 race (bonus position)
-  it.reread = (kind == 0 && plan_cfg(A, P, it.row).type == UT_DENSE) ? 1 : 0;
-  it.n = it.kind == 1 ? min(G::EA, A.V - it.c * G::EA) : min(G::EB, A.V - it.c * G::EB);
   return it;
 }
 
@@ -365,17 +276,20 @@ __device__ __forceinline__ bool wait_buffer(const Args& A, unsigned long long* b
 
 // The part of an item the bulk copy did not cover: the ragged tail (read
 // with plain loads), and padding up to the end of the tile (-inf logits,
-// zero q), so that every tile is reduced over all its blocks.  With rows
-// that are not 16-byte aligned, everything.
+// zero q; 16-byte stores from the first 16-byte boundary), so that every
+// tile is reduced over all its blocks.  With rows that are not 16-byte
+// aligned, everything.
 template <bool kBF16>
 __device__ __noinline__ void fill_tail(const Args& A, Item it, unsigned char* buf) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const int E = it.kind == 1 ? G::EA : G::EB;
-  const int end = E;
   const int done = A.vec_logits ? (int)(((uint32_t)(it.n * G::es) & ~15u) / G::es) : 0;
   const size_t lrow = (size_t)it.u * A.V + (size_t)it.c * E;
-  for (int e = done + lane; e < end; e += 32) {
+  constexpr int per16 = 16 / G::es;   // entries per 16 bytes
+  // entries [done, n), then -inf up to the next 16-byte boundary
+  const int vb = min(E, (it.n + per16 - 1) / per16 * per16);
+  for (int e = done + lane; e < vb; e += 32) {
     if (kBF16) {
       const uint16_t h = e < it.n ? reinterpret_cast<const uint16_t*>(A.logits)[lrow + e] : (uint16_t)0xff80u;
       reinterpret_cast<uint16_t*>(buf)[e] = h;
@@ -383,11 +297,16 @@ __device__ __noinline__ void fill_tail(const Args& A, Item it, unsigned char* bu
       reinterpret_cast<float*>(buf)[e] = e < it.n ? reinterpret_cast<const float*>(A.logits)[lrow + e] : -INFINITY;
     }
   }
+  const uint32_t ni = kBF16 ? 0xff80ff80u : 0xff800000u;
+  const uint4 ninf = make_uint4(ni, ni, ni, ni);
+  for (int v = vb / per16 + lane; v < E / per16; v += 32) reinterpret_cast<uint4*>(buf)[v] = ninf;
   if (it.kind == 2) {
     float* qb = reinterpret_cast<float*>(buf + G::EB * G::es);
     const int dq = A.vec_q ? (int)(((uint32_t)(it.n * 4) & ~15u) / 4) : 0;
     const size_t qrow = ((size_t)it.row * A.k + it.pos) * (size_t)A.V + (size_t)it.c * G::EB;
-    for (int e = dq + lane; e < end; e += 32) qb[e] = e < it.n ? A.q[qrow + e] : 0.f;
+    const int vq = min(E, (it.n + 3) / 4 * 4);
+    for (int e = dq + lane; e < vq; e += 32) qb[e] = e < it.n ? A.q[qrow + e] : 0.f;
+    for (int v = vq / 4 + lane; v < E / 4; v += 32) reinterpret_cast<uint4*>(qb)[v] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncwarp();
 }
@@ -559,31 +478,20 @@ __device__ __forceinline__ u64 a_wexp(const uint32_t* w, u64 m2, u64 c2) {
   const u64 e3 = exp_pair(a_val<kBF16>(w, 6), a_val<kBF16>(w, 7), m2, c2);
   return add2(add2(e0, e1), add2(e2, e3));
 }
-// The loops over a tile's blocks are rolled (two blocks per iteration) and
-// read the tile from shared memory once per pass: the stream code stays
-// small enough for the instruction cache, which matters more here than the
-// second read of the buffer.
-template <bool kBF16>
-__device__ __forceinline__ float a_tile_lane_max(const unsigned char* buf, int lane) {
-  constexpr int NB = Geo<kBF16>::NBA;
-  constexpr int NW = kBF16 ? 4 : 8;
+// Max (NaN-propagating) of a lane's entries over all blocks: for bf16 a
+// packed running maximum, unpacked once.
+template <bool kBF16, int NB, int NW>
+__device__ __forceinline__ float a_lane_max(const uint32_t (&w)[NB][NW]) {
   if (kBF16) {
     uint32_t m = 0xff80ff80u;
-#pragma unroll 2
-    for (int b = 0; b < NB; ++b) {
-      uint32_t w[NW];
-      a_block<kBF16>(buf, b, lane, w);
-      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(w[0], w[1]), max_nan_bf16x2(w[2], w[3])));
-    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      m = max_nan_bf16x2(m, max_nan_bf16x2(max_nan_bf16x2(w[b][0], w[b][1]), max_nan_bf16x2(w[b][2], w[b][3])));
     return max_nan(bf16_lo(m), bf16_hi(m));
   }
   float m = -INFINITY;
-#pragma unroll 2
-  for (int b = 0; b < NB; ++b) {
-    uint32_t w[NW];
-    a_block<kBF16>(buf, b, lane, w);
-    m = max_nan(m, a_wmax<kBF16>(w));
-  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) m = max_nan(m, a_wmax<kBF16>(w[b]));
   return m;
 }
 
@@ -593,14 +501,16 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
   using G = Geo<kBF16>;
   constexpr int NB = G::NBA;
   constexpr int NW = kBF16 ? 4 : 8;
-  static_assert(NB % 2 == 0 && NB <= 32, "blocks of a tile: an even count, one per lane at most");
   const int lane = threadIdx.x & 31;
   const int e0 = it.c * G::EA;
   const float c = cfg.c;
   const bool greedy = cfg.type == UT_GREEDY;
   const bool bonus = !greedy && it.pos == A.k;
-  // the lane max, then the tile max (NaN-propagating)
-  const float lm = a_tile_lane_max<kBF16>(buf, lane);
+  uint32_t w[NB][NW];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) a_block<kBF16>(buf, b, lane, w[b]);
+  // the lane max
+  const float lm = a_lane_max<kBF16, NB, NW>(w);
   const float mc = warp_max_nan(lm);
   const bool nan = mc != mc;
   float z = 0.f;
@@ -611,31 +521,29 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
     if (!bonus) {
       // the softmax sum relative to the tile max
       u64 za = pack2(0.f, 0.f), zb = pack2(0.f, 0.f);
-#pragma unroll 1
+#pragma unroll
       for (int b = 0; b < NB; b += 2) {
-        uint32_t w[NW];
-        a_block<kBF16>(buf, b, lane, w);
-        za = add2(za, a_wexp<kBF16>(w, m2, c2));
-        a_block<kBF16>(buf, b + 1, lane, w);
-        zb = add2(zb, a_wexp<kBF16>(w, m2, c2));
+        za = add2(za, a_wexp<kBF16>(w[b], m2, c2));
+        if (b + 1 < NB) zb = add2(zb, a_wexp<kBF16>(w[b + 1], m2, c2));
       }
       float a0, a1, b0, b1;
       unpack2(za, a0, a1);
       unpack2(zb, b0, b1);
       z = warp_sum((a0 + a1) + (b0 + b1));
     } else {
-      // block weights (lane b keeps block b's), their sum, then the level-1 race
-      float myW = 0.f;
-#pragma unroll 1
-      for (int b = 0; b < NB; ++b) {
-        uint32_t w[NW];
-        a_block<kBF16>(buf, b, lane, w);
-        float s0, s1;
-        unpack2(a_wexp<kBF16>(w, m2, c2), s0, s1);
-        const float Wb = warp_sum(s0 + s1);
-        z += Wb;
-        myW = lane == b ? Wb : myW;
+      // block weights by a transposed warp sum, then the level-1 race
+      constexpr int NP = NB <= 8 ? 8 : (NB <= 16 ? 16 : 32);
+      float ps[NP];
+      float tot = 0.f;
+#pragma unroll
+      for (int b = 0; b < NP; ++b) {
+        float s0 = 0.f, s1 = 0.f;
+        if (b < NB) unpack2(a_wexp<kBF16>(w[b], m2, c2), s0, s1);
+        ps[b] = s0 + s1;
+        tot += ps[b];
       }
+      z = warp_sum(tot);
+      const float myW = warp_transpose_sum<NP>(ps);   // lane b: the weight of block b
       if (lane < NB && myW > 0.f) {
         const uint32_t blk = (uint32_t)(e0 / kRaceBlock + lane);
         race_consider(r, myW, 0.f, blk, block_word(A, it.row, it.pos, blk));
@@ -647,17 +555,15 @@ __device__ __noinline__ void a_stats(const Args& A, uint32_t tag, Item it, RowCf
   if (greedy && !nan) {
     // first index of the tile max: in the first block of a lane holding it
     if (lm == mc) {
-#pragma unroll 1
-      for (int b = 0; b < NB; ++b) {
-        uint32_t w[NW];
-        a_block<kBF16>(buf, b, lane, w);
-        if (a_wmax<kBF16>(w) == mc) {
+      int lb = NB - 1;
 #pragma unroll
-          for (int j = 7; j >= 0; --j)
-            if (a_val<kBF16>(w, j) == mc) idx = (uint32_t)(e0 + a_entry<kBF16>(b, lane, j));
-          break;
-        }
-      }
+      for (int b = NB - 1; b >= 0; --b)
+        if (a_wmax<kBF16>(w[b]) == lm) lb = b;
+      float v[8];
+      a_vals<kBF16>(buf, lb, lane, v);
+#pragma unroll
+      for (int j = 7; j >= 0; --j)
+        if (v[j] == lm) idx = (uint32_t)(e0 + a_entry<kBF16>(lb, lane, j));
     }
     idx = __reduce_min_sync(kFull, idx);
     // the settle reads q at the unit's argmax, one of the tiles' argmaxes
@@ -697,16 +603,16 @@ __device__ __noinline__ uint32_t stage_all(const unsigned char* buf, int nb, int
   return n;
 }
 
-// Bitonic network over the warp's 32 lanes (rolled: small code): groups of
-// 16 sorted (alternating directions), then of the last merge the
-// half-cleaners down to stride kList, which leave the kList largest keys in
-// lanes 0..kList-1.
-__device__ __noinline__ u64 top8_network(u64 a, int lane) {
-#pragma unroll 1
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll 1
+// Bitonic network over lanes 0..S-1, fully unrolled: groups of S/2 sorted
+// (alternating directions), then of the last merge the half-cleaners down to
+// stride kList, which leave the kList largest keys in lanes 0..kList-1.
+template <int S>
+__device__ __forceinline__ u64 top8_network(u64 a, int lane) {
+#pragma unroll
+  for (int size = 2; size <= S; size <<= 1) {
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (size == 32 && stride < kList) break;
+      if (size == S && stride < kList) break;
       const u64 o = __shfl_xor_sync(kFull, a, stride);
       const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
       a = keep_max ? (o > a ? o : a) : (o < a ? o : a);
@@ -726,49 +632,55 @@ template <bool kBF16>
 __device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const unsigned char* buf,
                                     u64* stage) {
   constexpr int NB = Geo<kBF16>::NBA;
-  constexpr int NW = kBF16 ? 4 : 8;
   const int lane = threadIdx.x & 31;
   const int nb = NB;   // tiles are padded to whole tiles
-  const float lm = a_tile_lane_max<kBF16>(buf, lane);
+  float bm[NB];
+  float lm = -INFINITY;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    bm[b] = a_block_max<kBF16>(buf, b, lane);
+    lm = max_nan(lm, bm[b]);
+  }
   const bool nan = __any_sync(kFull, lm != lm);
   uint32_t flags = nan ? kListNaN : 0u;
   uint32_t nn = 0;
   if (!nan) {
     // t8: take the largest lane maxima (with their multiplicity) until 8
     uint32_t key = okey(lm), need = (uint32_t)kList, t8k = 0u;
-#pragma unroll 1
+    bool found = false;   // warp-uniform
+#pragma unroll
     for (int i = 0; i < kList; ++i) {
-      const uint32_t mx = __reduce_max_sync(kFull, key);
-      const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
-      t8k = mx;
-      if (c >= need) break;
-      need -= c;
-      key = key == mx ? 0u : key;
+      if (!found) {
+        const uint32_t mx = __reduce_max_sync(kFull, key);
+        const uint32_t c = (uint32_t)__popc(__ballot_sync(kFull, key == mx));
+        t8k = mx;
+        found = c >= need;
+        need -= found ? 0u : c;
+        key = key == mx ? 0u : key;
+      }
     }
     const float t8 = from_okey(t8k);
-    // the lane's finite entries >= t8, block by block (blocks whose maximum
-    // is below t8 hold none)
+    // the lane's blocks holding finite entries >= t8, then those entries
+    uint32_t hit = 0;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) hit |= (bm[b] >= t8 && bm[b] > -INFINITY) ? (1u << b) : 0u;
     uint32_t cnt = 0;
     u64 k0 = 0ull, k1 = 0ull, k2 = 0ull, k3 = 0ull;
-    if (lm >= t8 && lm > -INFINITY) {
 #pragma unroll 1
-      for (int b = 0; b < NB; ++b) {
-        uint32_t w[NW];
-        a_block<kBF16>(buf, b, lane, w);
-        const float bm = a_wmax<kBF16>(w);
-        if (!(bm >= t8 && bm > -INFINITY)) continue;
+    while (hit) {
+      const int b = __ffs(hit) - 1;
+      hit &= hit - 1u;
+      float v[8];
+      a_vals<kBF16>(buf, b, lane, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float v = a_val<kBF16>(w, j);
-          if (v >= t8 && v > -INFINITY) {
-            k3 = k2;
-            k2 = k1;
-            k1 = k0;
-            k0 = key64(okey(v), (uint32_t)a_entry<kBF16>(b, lane, j));
-            ++cnt;
-          }
+      for (int j = 0; j < 8; ++j)
+        if (v[j] >= t8 && v[j] > -INFINITY) {
+          k3 = k2;
+          k2 = k1;
+          k1 = k0;
+          k0 = key64(okey(v[j]), (uint32_t)a_entry<kBF16>(b, lane, j));
+          ++cnt;
         }
-      }
     }
     uint32_t n = 0;
     if (!__any_sync(kFull, cnt > (uint32_t)kLaneCand)) {
@@ -784,10 +696,12 @@ __device__ __noinline__ void a_list(const Args& A, uint32_t tag, Item it, const 
     if (n > (uint32_t)kStage) flags |= kListPartial;
     nn = min(n, (uint32_t)kStage);
     if (nn > (uint32_t)kList && nn <= 32) {
-      // one candidate per lane (lanes from nn on hold 0): a bitonic network
-      // in registers leaves the 8 largest in lanes 0..7 (in no particular order)
+      // one candidate per lane: a bitonic network in registers over lanes
+      // 0..S-1 (S the power of two >= nn; lanes from nn on hold 0) that sorts
+      // groups of S/2, then of the last merge only the half-cleaners down to
+      // stride 8: lanes 0..7 then hold the 8 largest (in no particular order)
       u64 a = (uint32_t)lane < nn ? stage[lane] : 0ull;
-      a = top8_network(a, lane);
+      a = nn <= 16u ? top8_network<16>(a, lane) : top8_network<32>(a, lane);
       __syncwarp();
       stage[lane] = a;
       __syncwarp();
@@ -852,42 +766,61 @@ __device__ __noinline__ void b_tile(const Args& A, uint32_t tag, Item it, RowCfg
                                     const unsigned char* buf) {
   using G = Geo<kBF16>;
   constexpr int NB = G::NBB;
-  static_assert(NB <= 32, "one block per lane at most");
+  constexpr int NP = NB <= 4 ? 4 : 8;
   const int lane = threadIdx.x & 31;
   const int e0 = it.c * G::EB;
   const bool need_race = !st.accept;
   const float* qb = reinterpret_cast<const float*>(buf + G::EB * G::es);
   const float m = st.m, invZ = st.invZ, c = cfg.c;
   const u64 m2 = pack2(m, m), c2 = pack2(c, c), z2 = pack2(invZ, invZ);
-  // alpha per lane over the lane's entries in block order; after a rejection
-  // also per block the residual weight W = sum max(p - q, 0) and the q
-  // under it (the draw margin's weight is W + 2 sum q over w > 0), lane b
-  // keeping block b's
-  float a8 = 0.f, myW = 0.f, myQ = 0.f;
-#pragma unroll 1
-  for (int b = 0; b < NB; ++b) {
-    float v[8], q[8];
-    sload<kBF16>(buf, b, lane, v);
-    sload_q(qb, b, lane, q);
-    float w8 = 0.f, q8 = 0.f;
+  // the lane's entries of every block (logits and q), in registers
+  float v[NB][8], q[NB][8];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      float p0, p1;
-      unpack2(mul2(exp_pair(v[j], v[j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
-      a8 += fminf(p0, q[j]) + fminf(p1, q[j + 1]);
-      if (need_race) {
-        const float d0 = p0 - q[j], d1 = p1 - q[j + 1];
-        w8 += fmaxf(d0, 0.f) + fmaxf(d1, 0.f);
-        q8 += (d0 > 0.f ? q[j] : 0.f) + (d1 > 0.f ? q[j + 1] : 0.f);
+  for (int b = 0; b < NB; ++b) {
+    sload<kBF16>(buf, b, lane, v[b]);
+    sload_q(qb, b, lane, q[b]);
+  }
+  float alpha_c, myW = 0.f, myQ = 0.f;
+  if (!need_race) {
+    // accepted draft: alpha only
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        float p0, p1;
+        unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);
+        a0 += fminf(p0, q[b][j]);
+        a1 += fminf(p1, q[b][j + 1]);
       }
     }
-    if (need_race) {
-      const float Wb = warp_sum(w8), Qb = warp_sum(q8);
-      myW = lane == b ? Wb : myW;
-      myQ = lane == b ? Qb : myQ;
+    alpha_c = warp_sum(a0 + a1);
+  } else {
+    // alpha, and per block the residual weight W = sum max(p - q, 0) and
+    // the q under it (the draw margin's weight is W + 2 sum q over w > 0)
+    float a8 = 0.f;
+    float wsum[NP], qsum[NP];
+#pragma unroll
+    for (int b = 0; b < NP; ++b) {
+      float w8 = 0.f, q8 = 0.f;
+      if (b < NB) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float p0, p1;
+          unpack2(mul2(exp_pair(v[b][j], v[b][j + 1], m2, c2), z2), p0, p1);   // padding: -inf -> 0
+          a8 += fminf(p0, q[b][j]) + fminf(p1, q[b][j + 1]);
+          const float d0 = p0 - q[b][j], d1 = p1 - q[b][j + 1];
+          w8 += fmaxf(d0, 0.f) + fmaxf(d1, 0.f);
+          q8 += (d0 > 0.f ? q[b][j] : 0.f) + (d1 > 0.f ? q[b][j + 1] : 0.f);
+        }
+      }
+      wsum[b] = w8;
+      qsum[b] = q8;
     }
+    alpha_c = warp_sum(a8);
+    myW = warp_transpose_sum<NP>(wsum);
+    myQ = warp_transpose_sum<NP>(qsum);
   }
-  const float alpha_c = warp_sum(a8);
   Race r;
   race_init(r);
   if (need_race && lane < NB && myW > 0.f) {
@@ -902,82 +835,64 @@ __device__ __noinline__ void b_tile(const Args& A, uint32_t tag, Item it, RowCfg
   __syncwarp();
 }
 
-// ---------------------------------------------------------------------------
-// Warps.
-// ---------------------------------------------------------------------------
-struct Bufs {
-  unsigned char* a;
-  unsigned char* b;
-  unsigned long long* ba;
-  unsigned long long* bb;
-  uint32_t pa, pb;
-  __device__ __forceinline__ void rotate() {
-    unsigned char* tb = a;
-    a = b;
-    b = tb;
-    unsigned long long* tr = ba;
-    ba = bb;
-    bb = tr;
-    const uint32_t tp = pa;
-    pa = pb;
-    pb = tp;
-  }
-};
-
-// A stream warp: items of the sequence, the first two by its index, later
-// ones from one counter (the next ticket is in flight while a tile is
-// reduced).  After a tile's record, one is added to the unit's tile count.
+// A stream warp in one pass (1: A tiles, 2: B tiles).  Item t of the pass
+// belongs to CTA t mod n_ctas; a CTA's warps take its items j = 0, 1, ...
+// (item blockIdx + n_ctas j): the first two by the warp's index, later ones
+// from a shared-memory counter (no global counter for all SMs to contend
+// on).  Of the warp's two buffers one is filled by the copy engine while the
+// other is reduced; the barriers' parities carry over from pass to pass.
 template <bool kBF16>
-__device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32_t tag, int sw, uint32_t gs,
-                                         uint32_t nws) {
+__device__ __noinline__ void stream_pass(const Args& A, Plan P0, VShm& S, uint32_t tag, int w, uint32_t gw,
+                                         int pass, uint32_t n_items, uint32_t* ticket) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
-  Bufs B;
-  B.a = S.s.buf[sw][0];
-  B.b = S.s.buf[sw][1];
-  B.ba = &S.bar[sw][0];
-  B.bb = &S.bar[sw][1];
-  B.pa = 0u;
-  B.pb = 0u;
-  if (lane == 0) {
-    mbar_init(B.ba, 1);    // issue() orders the inits before the copies (fence.proxy.async)
-    mbar_init(B.bb, 1);
-  }
-  __syncwarp();
-  Item ia = map_item<kBF16>(A, P, gs);
-  Item ib = map_item<kBF16>(A, P, nws + gs);
+  unsigned char* bufa = S.s.buf[w][0];
+  unsigned char* bufb = S.s.buf[w][1];
+  unsigned long long* bara = &S.bar[w][0];
+  unsigned long long* barb = &S.bar[w][1];
+  uint32_t pa = S.par[w][0], pb = S.par[w][1];
+  bool swapped = false;
+  bool broken = S.broken[w] != 0u;
+  const uint32_t nc = (uint32_t)A.n_ctas, cb = blockIdx.x;
+  Item ia = map_item<kBF16>(A, P, pass, cb + nc * (uint32_t)w, n_items);
+  Item ib = map_item<kBF16>(A, P, pass, cb + nc * (uint32_t)(kNW + w), n_items);
   // the first buffer alone: the first data arrives behind half the bytes a
   // second copy per warp would put in flight; the second copy is posted as
   // soon as it has (below)
-  if (lane == 0) issue<kBF16>(A, ia, B.a, B.ba);
-  bool broken = false;
+  if (lane == 0 && !broken) issue<kBF16>(A, ia, bufa, bara);
   bool first = true;
   while (ia.kind != 0) {
     uint32_t tn = 0;
     const bool take = ib.kind != 0 && !broken;   // warp-uniform
-    if (lane == 0 && take) tn = 2u * nws + atomicAdd(&A.ws->next_item, 1u);
+    if (lane == 0 && take) tn = cb + nc * (2u * kNW + atomicAdd(ticket, 1u));
     const RowCfg cfg = plan_cfg(A, P, ia.row);
     u64 sw8[kStateWords];
     if (ia.kind == 2) state_load(A, ia.u, sw8);     // in flight during the copy wait
-    const bool ok = !broken && wait_buffer(A, B.ba, B.pa);
+    const bool ok = !broken && wait_buffer(A, bara, pa);
     if (first) {
-      if (lane == 0 && ok) TL(TL_FIRST_DATA, (int)gs, 2048);
-      if (lane == 0 && ok) issue<kBF16>(A, ib, B.b, B.bb);
+      if (lane == 0 && ok && pass == 1) TL(TL_FIRST_DATA, (int)gw, 2048);
+      if (lane == 0 && ok) issue<kBF16>(A, ib, bufb, barb);
       first = false;
     }
+#ifdef SPEC_TIMELINE
+    if (lane == 0 && pass == 1) {
+      TL(TL_ISTART, (int)ia.t, 16384);
+      if (ia.t < 16384u) g_tl[TL_IWARP + ia.t] = gw + 1u;
+    }
+#endif
     if (!ok) {
       // the buffer's copy never completed: mark this tile and stop taking new ones
       broken = true;
       timeout_record(A, tag, ia, cfg.type == UT_TOPK);
     } else {
-      B.pa ^= 1u;
+      pa ^= 1u;
       if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || ia.n != (ia.kind == 1 ? Geo<kBF16>::EA : Geo<kBF16>::EB))
-        fill_tail<kBF16>(A, ia, B.a);
+        fill_tail<kBF16>(A, ia, bufa);
       if (ia.kind == 1) {
-        if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, B.a, S.s.stage[sw]);
-        else a_stats<kBF16>(A, tag, ia, cfg, B.a);
+        if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, bufa, S.s.stage[w]);
+        else a_stats<kBF16>(A, tag, ia, cfg, bufa);
       } else {
-        // the unit state (bounded wait: a settle warp publishes it)
+        // the unit state, published before this pass (bounded wait all the same)
         long long spins = 0;
         bool st_ok = true;
         while (!__all_sync(kFull, state_ok(sw8, tag))) {
@@ -993,103 +908,116 @@ __device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32
           timeout_record(A, tag, ia, false);
         } else {
           const UnitState st = state_of(sw8);
-          if (!st.invalid) b_tile<kBF16>(A, tag, ia, cfg, st, B.a);
+          if (!st.invalid) b_tile<kBF16>(A, tag, ia, cfg, st, bufa);
         }
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      TL(TL_ITEM, (int)ia.t, 16384);
-      atomicAdd(&A.ucnt[(ia.kind == 2 ? A.U : 0) + ia.u], 1u);   // result unused: a reduction
-    }
+    if (lane == 0 && pass == 1) TL(TL_ITEM, (int)ia.t, 16384);
     tn = __shfl_sync(kFull, tn, 0);
     Item in;
     in.kind = 0;
-    if (take) in = map_item<kBF16>(A, P, tn);   // after a failed copy: mapped, marked, not copied
-    if (lane == 0 && !broken) issue<kBF16>(A, in, B.a, B.ba);
+    if (take) in = map_item<kBF16>(A, P, pass, tn, n_items);   // after a failed copy: mapped, marked, not copied
+    if (lane == 0 && !broken) issue<kBF16>(A, in, bufa, bara);
     ia = ib;
     ib = in;
-    B.rotate();
+    unsigned char* tb = bufa;
+    bufa = bufb;
+    bufb = tb;
+    unsigned long long* tr = bara;
+    bara = barb;
+    barb = tr;
+    const uint32_t tp = pa;
+    pa = pb;
+    pb = tp;
+    swapped = !swapped;
   }
-  if (lane == 0) TL(TL_STREAM_END, (int)gs, 2048);
+  if (lane == 0) {
+    S.par[w][0] = swapped ? pb : pa;
+    S.par[w][1] = swapped ? pa : pb;
+    S.broken[w] = broken ? 1u : 0u;
+    if (pass == 1) TL(TL_STREAM_END, (int)gw, 2048);
+  }
+  __syncwarp();
 }
 
-// Settle task t: the unit and kind (settle-A after its A tiles, settle-B
-// after its B tiles) and the tile count to wait for.
-struct Task {
-  int u, row, pos, ntiles, kind;   // kind 1: A, 2: B
-};
-__device__ __forceinline__ Task map_task(const Args& A, Plan P, const VShm& S, uint32_t t) {
-  int lo = 0, hi = P.nseg - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (S.tstart[mid] <= t) lo = mid;
-    else hi = mid - 1;
-  }
-  const Seg s = P.seg[lo];
-  const uint32_t upr = (s.packed >> 21) & 31u, pos_lo = (s.packed >> 16) & 31u;
-  const uint32_t j = t - S.tstart[lo];
-  const uint32_t ri = j / upr;
-  Task k;
-  k.row = (int)P.order[s.first + ri];
-  k.pos = (int)(pos_lo + (j - ri * upr));
-  k.u = k.row * (A.k + 1) + k.pos;
-  k.ntiles = (int)(s.packed & 0xffffu);
-  k.kind = ((s.packed >> 26) & 1u) ? 2 : 1;
-  return k;
-}
-
-// A settle warp: tasks g, g + nst, ... in sequence order; each waits for its
-// unit's tile count, settles the unit and clears the count.
+// The settle pass after the A pass: small top-k units by whole CTAs (unit
+// i by CTA i mod n_ctas), the other units by single warps from a counter.
 template <bool kBF16>
-__device__ __noinline__ void settle_loop(const Args& A, Plan P, VShm& S, uint32_t tag, int w, uint32_t g,
-                                         uint32_t nst) {
+__device__ __noinline__ void settle_pass_a(const Args& A, Plan P, VShm& S, uint32_t tag) {
   const int lane = threadIdx.x & 31;
-  TopkScratch& TS = S.tk[w];
-  for (uint32_t t = g; t < S.ntasks; t += nst) {
-    const Task k = map_task(A, P, S, t);
-    uint32_t* cnt = &A.ucnt[(k.kind == 2 ? A.U : 0) + k.u];
-    // what the settle needs besides the records is loaded while the tiles
-    // are still being reduced: the draft and its logit and q (settle-A), or
-    // the unit's published state (settle-B)
-    Pre pr;
-    StateWords sw8;
-    if (k.kind == 2) {
-      state_load(A, k.u, sw8.w);
-    } else {
-      pr = load_pre<kBF16>(A, k.u, k.row, k.pos);
-    }
-    bool ready = true;
-    if (lane == 0) {
-      long long spins = 0;
-      while (load_relaxed(cnt) != (uint32_t)k.ntiles) {
-        if (++spins > 16ll * kSpinLimit) {
-          atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
-          ready = false;
-          break;
-        }
-        __nanosleep(spins > 64 ? 128 : 32);
-      }
-    }
-    ready = __shfl_sync(kFull, ready ? 1 : 0, 0) != 0;
-    const RowCfg cfg = plan_cfg(A, P, k.row);
-    if (lane == 0) TL(k.kind == 2 ? TL_SB_START : TL_SA_START, k.u, 2048);
-    if (!ready) {
-      commit_record(A, tag, k.u, k.row, empty_record(SPEC_F_TIMEOUT));   // the records' polls would give up too
-    } else if (k.kind == 2) {
-      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg, sw8);
-    } else if (cfg.type == UT_TOPK) {
-      topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg, pr);
-    } else {
-      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg, pr);
-    }
-    if (lane == 0) {
-      TL(k.kind == 2 ? TL_SB_END : TL_SA_END, k.u, 2048);
-      *cnt = 0u;   // leave the workspace clean for the next call
-    }
+  const int k1 = A.k + 1;
+  const int nTU = P.nT * k1;
+  for (int i = (int)blockIdx.x; i < nTU; i += A.n_ctas) {
+    __syncthreads();   // warp 0 has finished the CTA's previous unit
+    const int ri = i / k1, pos = i - (i / k1) * k1;
+    const int row = a_row(P, ri);
+    const int u = row * k1 + pos;
+    const RowCfg cfg = plan_cfg(A, P, row);
+    if (threadIdx.x == 0) TL(TL_SA_START, u, 2048);
+    topk_settle_cta<kBF16>(A, tag, S.tkc, u, row, pos, cfg);
+    if (threadIdx.x == 0) TL(TL_SA_END, u, 2048);
+  }
+  const uint32_t nu = (uint32_t)a_units(A, P);
+  while (true) {
+    uint32_t j = 0;
+    if (lane == 0) j = atomicAdd(&A.ws->settle_next, 1u);
+    j = __shfl_sync(kFull, j, 0) + (uint32_t)nTU;
+    if (j >= nu) break;
+    const uint32_t ri = j / (uint32_t)k1;
+    const int pos = (int)(j - ri * (uint32_t)k1);
+    const int row = a_row(P, (int)ri);
+    const int u = row * k1 + pos;
+    const RowCfg cfg = plan_cfg(A, P, row);
+    if (lane == 0) TL(TL_SA_START, u, 2048);
+    const Pre pr = load_pre<kBF16>(A, u, row, pos);
+    fin_stats<kBF16>(A, tag, u, row, pos, cfg, pr);
+    if (lane == 0) TL(TL_SA_END, u, 2048);
     __syncwarp();
   }
-  if (lane == 0) TL(TL_SETTLE_END, (int)g, 256);
+}
+
+// The settle pass after the B pass: one warp per drafted unfiltered unit.
+template <bool kBF16>
+__device__ __noinline__ void settle_pass_b(const Args& A, Plan P, uint32_t tag, uint32_t gw, uint32_t nwarps) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t nu = (uint32_t)b_units(A, P);
+  for (uint32_t j = gw; j < nu; j += nwarps) {
+    const uint32_t ri = j / (uint32_t)A.k;
+    const int pos = (int)(j - ri * (uint32_t)A.k);
+    const int row = (int)P.order[ri];
+    const int u = row * (A.k + 1) + pos;
+    const RowCfg cfg = plan_cfg(A, P, row);
+    if (lane == 0) TL(TL_SB_START, u, 2048);
+    StateWords sw8;
+    state_load(A, u, sw8.w);
+    fin_b<kBF16>(A, tag, u, row, pos, cfg, sw8);
+    if (lane == 0) TL(TL_SB_END, u, 2048);
+    __syncwarp();
+  }
+}
+
+// Every CTA arrives before any leaves (the launch is cooperative, so all are
+// resident).  The count only grows within a call: barrier i waits for
+// i x n_ctas arrivals.  Bounded: a wait that gives up sets ERR_BARRIER and
+// the CTA goes on (the record polls after it then give up too, and the rows
+// come back with SPEC_F_TIMEOUT).
+__device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&A.ws->bar, 1u);
+    long long spins = 0;
+    while (load_acquire(&A.ws->bar) < target) {
+      if (++spins > 16ll * kSpinLimit) {
+        atomicOr(&A.ws->error, (uint32_t)ERR_BARRIER);
+        break;
+      }
+      __nanosleep(spins > 16 ? 128 : 16);
+    }
+    __threadfence();
+  }
+  __syncthreads();
 }
 
 // General-path units, taken by the CTA's first kThreads threads.
@@ -1110,14 +1038,23 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A, uint32_t b_delay) {
+__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A) {
   using G = Geo<kBF16>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
-  const int w = threadIdx.x >> 5;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     S.tag = next_tag(__ldcg(&A.ws->epoch));
     S.gtask = 0;
+    S.ticket[0] = 0u;
+    S.ticket[1] = 0u;
+  }
+  if (lane == 0) {
+    mbar_init(&S.bar[w][0], 1);    // issue() orders the inits before the copies (fence.proxy.async)
+    mbar_init(&S.bar[w][1], 1);
+    S.par[w][0] = 0u;
+    S.par[w][1] = 0u;
+    S.broken[w] = 0u;
   }
   Plan P;
   bool order_ok = true;
@@ -1155,24 +1092,23 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   const uint32_t tag = S.tag;
   P.NTA = ceil_div(A.V, G::EA);
   P.NTB = ceil_div(A.V, G::EB);
-  build_segments(A, S, P.nD, P.nT, P.nX, P.nG, P.NTA, P.NTB, b_delay);
   __syncthreads();
-  P.seg = S.seg;
-  P.nseg = S.nseg;
   if (threadIdx.x == 0) TL(TL_CTA_START, (int)blockIdx.x, 160);
+  // warp gw of nwarps: consecutive indices on different SMs
+  const uint32_t nwarps = (uint32_t)A.n_ctas * kNW;
+  const uint32_t gw = (uint32_t)w * (uint32_t)A.n_ctas + blockIdx.x;
+  const uint32_t nb = (uint32_t)b_units(A, P) * (uint32_t)P.NTB;
   if (order_ok) {
-    const int bx = (int)blockIdx.x;
-    const bool settle_cta = (bx % A.settle_stride) == 0 && bx / A.settle_stride < A.n_settle;
-    if (settle_cta) {
-      const uint32_t nst = (uint32_t)A.n_settle * kNW;
-      settle_loop<kBF16>(A, P, S, tag, w, (uint32_t)(bx / A.settle_stride) * kNW + (uint32_t)w, nst);
-    } else {
-      // stream CTA rank: blocks before this one, minus the settle CTAs among them
-      const int srank = bx - min(A.n_settle, bx / A.settle_stride + 1);
-      const int n_stream = A.n_ctas - A.n_settle;
-      const uint32_t nws = (uint32_t)n_stream * kNW;
-      // consecutive items go to different SMs
-      stream_loop<kBF16>(A, P, S, tag, w, (uint32_t)w * (uint32_t)n_stream + (uint32_t)srank, nws);
+    // A pass, then every unit's settle (the B pass's q into L2 meanwhile)
+    stream_pass<kBF16>(A, P, S, tag, w, gw, 1, (uint32_t)a_units(A, P) * (uint32_t)P.NTA, &S.ticket[0]);
+    grid_barrier(A, (uint32_t)A.n_ctas);
+    settle_pass_a<kBF16>(A, P, S, tag);
+    if (nb > 0) {
+      // B pass over the drafted unfiltered units, then their settles
+      grid_barrier(A, 2u * (uint32_t)A.n_ctas);
+      stream_pass<kBF16>(A, P, S, tag, w, gw, 2, nb, &S.ticket[1]);
+      grid_barrier(A, 3u * (uint32_t)A.n_ctas);
+      settle_pass_b<kBF16>(A, P, tag, gw, nwarps);
     }
   }
   if (P.nX > 0 && order_ok) {
@@ -1194,7 +1130,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     if (d == (uint32_t)A.n_ctas - 1u) {
       __threadfence();
       A.ws->gnext = 0u;
-      A.ws->next_item = 0u;
+      A.ws->bar = 0u;
+      A.ws->settle_next = 0u;
       A.ws->commit_next = 0u;
       A.ws->done_count = 0u;
       A.ws->ctas_done = 0u;
@@ -1209,10 +1146,6 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-// Items of A tiles between the end of an unfiltered wave's A tiles and its
-// B tiles: the wave's settles (a few microseconds) finish meanwhile.
-constexpr uint32_t kBDelayItems = 1600;
-
 template <bool kBF16>
 int launch_verify(const Args& A0, cudaStream_t stream) {
   static std::mutex mu;
@@ -1241,10 +1174,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   }
   Args A = A0;
   A.n_ctas = n;
-  A.n_settle = n >= 2 * kSettleEvery ? n / kSettleEvery : 1;
-  A.settle_stride = n / A.n_settle;
   A.global_order = A.B > kOrderSmem ? 1 : 0;
-  uint32_t b_delay = kBDelayItems;
   // cooperative launch: every CTA is resident, so every wait between warps ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -1257,7 +1187,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, A, b_delay) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, A) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_E_CUDA;
   }

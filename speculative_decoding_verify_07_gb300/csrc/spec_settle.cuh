@@ -1,14 +1,13 @@
 // spec_verify, settle code (sm_103a): what one warp does with a unit once
-// every tile of it has been reduced (the stream warp that reduced the last
-// tile queues the unit on its CTA's settle warps).
+// every tile of it has been reduced.
 //
 //   greedy and unfiltered units: merge the A records in tile order -- max,
 //     first argmax, the softmax sum rescaled to the unit max; greedy units
 //     and unfiltered bonus positions are settled at once (the bonus draw
 //     merges the tiles' level-1 block races and races the winning block's
 //     entries); a drafted unfiltered unit takes its accept test and
-//     publishes its state for the B tiles; once those are reduced, its B
-//     records are merged (alpha and the residual draw).
+//     publishes its state for the B tiles; after the B pass its B records
+//     are merged (alpha and the residual draw).
 //   small top-k units: every A tile lists the 8 largest entries of its
 //     tile in the total order, the smallest of them last.  A tile whose
 //     smallest listed entry is below the K-th entry of the merged lists holds
@@ -741,109 +740,33 @@ __device__ __noinline__ int select_k_row(const Args& A, TopkScratch& S, size_t l
   return (int)min(n_out, (uint32_t)kSel);
 }
 
-// Candidates a lane holds (round r: candidate 32 r + lane): a small top-k
-// unit has at most kMaxListCand / kList tiles of fp32 logits, half as many of bf16.
-template <bool kBF16>
-struct CandRounds {
-  static constexpr int value = (kBF16 ? kMaxListCand / 2 : kMaxListCand) / 32;
+static_assert(kList == 8, "list slot q mod 8 of tile q / 8");
+
+// CTA scratch of a small top-k settle.
+struct TopkCtaShm {
+  TopkScratch ts;                  // the lists (tile-major), the selection, its q
+  u64 fk[kMaxListCand];            // the listed entries at or above tau
+  u64 wmax[kCtaWarps];             // per-warp reductions
+  uint32_t wcnt[kCtaWarps];
+  uint32_t tau;                    // a value key at or below the K-th listed entry
+  uint32_t nf;                     // entries in fk
 };
-static_assert(Geo<true>::EA == 2 * Geo<false>::EA, "bf16 tiles hold twice the entries");
-constexpr int kListRounds = kTopkSmall / 32;     // list entries a lane holds
-static_assert(kMaxListCand % 32 == 0 && kList == 8, "lane l holds list slot l mod 8 of its tiles");
-
-// Number of candidates (over the warp) whose 32-bit value key is >= t (t >= 1;
-// an empty slot holds 0).
-template <int CR>
-__device__ __forceinline__ uint32_t count_key_ge(const u64 (&cand)[CR], int nrd, uint32_t t) {
-  uint32_t n = 0;
-#pragma unroll
-  for (int i = 0; i < CR; ++i)
-    if (i < nrd) n += (uint32_t)(cand[i] >> 32) >= t ? 1u : 0u;
-  return __reduce_add_sync(kSettleFull, n);
-}
-
-// Entry j of a list held 32 per round (j warp-uniform).
-__device__ __forceinline__ float list_get(const float (&a)[kListRounds], int j) {
-  float v = a[0];
-#pragma unroll
-  for (int r = 1; r < kListRounds; ++r) v = (j >> 5) == r ? a[r] : v;
-  return __shfl_sync(kSettleFull, v, j & 31);
-}
-__device__ __forceinline__ uint32_t list_get(const uint32_t (&a)[kListRounds], int j) {
-  uint32_t v = a[0];
-#pragma unroll
-  for (int r = 1; r < kListRounds; ++r) v = (j >> 5) == r ? a[r] : v;
-  return __shfl_sync(kSettleFull, v, j & 31);
-}
-
-// The K-th largest listed entry in the total order (0 when fewer than K are
-// listed), by bisection on the value key, then on the index among ties.
-template <bool kBF16, int CR>
-__device__ __forceinline__ u64 kth_listed(const u64 (&cand)[CR], int nrd, uint32_t K, uint32_t V) {
-  if (count_key_ge(cand, nrd, 1u) < K) return 0ull;
-  // the largest value key t with count(key >= t) >= K (bf16 keys: the top 16 bits decide)
-  uint32_t tkey;
-  if (kBF16) {
-    uint32_t lo = 0u, hi = 0xffffu;
-    while (lo < hi) {
-      const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
-      if (count_key_ge(cand, nrd, max(mid << 16, 1u)) >= K) lo = mid;
-      else hi = mid - 1u;
-    }
-    tkey = full_key<true>(lo);
-  } else {
-    uint32_t lo = 1u, hi = 0xffffffffu;
-    while (lo < hi) {
-      const uint32_t mid = lo + (uint32_t)(((u64)hi - lo + 1ull) >> 1);
-      if (count_key_ge(cand, nrd, mid) >= K) lo = mid;
-      else hi = mid - 1u;
-    }
-    tkey = lo;
-  }
-  const uint32_t n_gt = tkey == 0xffffffffu ? 0u : count_key_ge(cand, nrd, tkey + 1u);
-  const uint32_t need = K - n_gt;   // >= 1 entries at the key, smallest indices first
-  const uint32_t n_eq = count_key_ge(cand, nrd, tkey) - n_gt;
-  uint32_t low = 0xffffffffu;
-#pragma unroll
-  for (int i = 0; i < CR; ++i)
-    if (i < nrd && (uint32_t)(cand[i] >> 32) == tkey) low = min(low, (uint32_t)cand[i]);
-  low = __reduce_min_sync(kSettleFull, low);
-  if (n_eq == need) return ((u64)tkey << 32) | low;   // every entry at the key is kept
-  // the need-th largest low word (0xffffffff - index) among the entries at tkey
-  uint32_t lo = low, hi = 0xffffffffu;
-  while (lo < hi) {
-    const uint32_t mid = lo + (uint32_t)(((u64)hi - lo + 1ull) >> 1);
-    uint32_t n = 0;
-#pragma unroll
-    for (int i = 0; i < CR; ++i)
-      if (i < nrd) n += ((uint32_t)(cand[i] >> 32) == tkey && (uint32_t)cand[i] >= mid) ? 1u : 0u;
-    if (__reduce_add_sync(kSettleFull, n) >= need) lo = mid;
-    else hi = mid - 1u;
-  }
-  return ((u64)tkey << 32) | lo;
-}
+constexpr int kCandPerThread = (kMaxListCand + kCtaWarps * 32 - 1) / (kCtaWarps * 32);
 
 // The exact top-K of a small top-k unit when a tile may hold more top-K
 // entries than it listed (a full list ending above kappa, or one marked
 // partial): those tiles are re-read (their entries at or above kappa join
 // the listed entries at or above kappa of the other tiles), or, when that
 // gives more than kSel entries (masses of ties), the whole row by radix
-// passes.  Leaves the K (or all, when fewer) largest sorted in S.sel with
-// their q in S.qsel; returns their count.
-template <bool kBF16, int CR>
-__device__ __noinline__ int topk_rescan(const Args& A, TopkScratch& S, const u64 (&cand)[CR], const u64* R, int nrd,
-                                        int NT, int NL, u64 kappa, int K, size_t lrow, size_t qrow, bool has_q) {
+// passes.  One warp; the lists are in S.cand and S.cflag.  Leaves the K (or
+// all, when fewer) largest sorted in S.sel with their q in S.qsel; returns
+// their count.
+template <bool kBF16>
+__device__ __noinline__ int topk_rescan(const Args& A, TopkScratch& S, int NT, int NL, u64 kappa, int K, size_t lrow,
+                                        size_t qrow, bool has_q) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   int n_k = 0;
-#pragma unroll
-  for (int i = 0; i < CR; ++i)
-    if (i < nrd && 32 * i + lane < NL) S.cand[32 * i + lane] = cand[i];
-  for (int ch = lane; ch < NT; ch += 32) {
-    const uint32_t iw = (uint32_t)__ldcg(R + (size_t)ch * kRecWords + 1);
-    S.cflag[ch] = (uint8_t)((iw & kListPartial) ? 2u : 0u);
-  }
-  __syncwarp();
   uint32_t n = 0;
   bool exact = true;
   for (int base = 0; base < NL; base += 32) {
@@ -893,196 +816,80 @@ __device__ __noinline__ int topk_rescan(const Args& A, TopkScratch& S, const u64
   return n_k;
 }
 
-// Settle a small top-k unit with one warp.
-//   1. The tiles' lists into registers (candidate 32 r + lane in round r, so
-//      lane l holds list slot l mod 8 of its tiles), and q at every listed
-//      entry (loads in flight while the list is settled).
-//   2. kappa, the K-th listed entry, by bisection.  A tile whose list is
-//      full and ends above kappa, or is marked partial, may hold more top-K
-//      entries: then the tile is re-read (the listed entries at or above
-//      kappa of the other tiles join its entries at or above kappa).
-//   3. The kept entries in the total order (rank by counting), prefix sums
-//      for top-p, alpha, the accept test, and the two-level race over the
-//      kept entries, all in registers.
+// The rest of a small top-k settle, by one warp, from the kept entries in
+// the total order (keys lk[0..n_k), their q in lq): prefix sums for top-p,
+// alpha, the accept test, the two-level race over the kept entries, the
+// unit record.  S.sel is scratch here (lk and lq are read first).
 template <bool kBF16>
-__device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
-                                         RowCfg cfg, Pre pre) {
-  using G = Geo<kBF16>;
-  constexpr int CR = CandRounds<kBF16>::value;
+__device__ __noinline__ void topk_tail(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
+                                       RowCfg cfg, Pre pr, const u64* lk, const float* lq, int n_k, float m, int am) {
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
-  const int NT = ceil_div(A.V, G::EA);
-  const int NL = NT * kList;
-  const int nrd = ceil_div(NL, 32);
-  const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
-  const size_t lrow = (size_t)u * A.V;
-  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const float c = cfg.c;
-  const int K = cfg.K;
-  Pre pr = pre;
   pr.x = __shfl_sync(kSettleFull, pr.x, 0);
   pr.valid = __shfl_sync(kSettleFull, pr.valid, 0);
   pr.lx = __shfl_sync(kSettleFull, pr.lx, 0);
   pr.qx = __shfl_sync(kSettleFull, pr.qx, 0);
-
-  // 1. the lists
-  u64 cand[CR];
-  uint32_t lflags = 0;   // kListNaN / kListPartial / kListTimeout of the lane's tiles
-  bool timed_out = false;
-  {
-    long long spins = 0;
-    bool ok;
-    do {
-      ok = true;
-      lflags = 0;
-#pragma unroll
-      for (int i = 0; i < CR; ++i) {
-        cand[i] = 0ull;
-        const int q = 32 * i + lane;
-        if (i < nrd && q < NL) {
-          const u64* r = R + (size_t)(q >> 3) * kRecWords + 2 * (q & 7);
-          const u64 wk = __ldcg(r), wi = __ldcg(r + 1);
-          ok = ok && tag_ok(wk, tag) && tag_ok(wi, tag);
-          const uint32_t key = (uint32_t)wk, iw = (uint32_t)wi;
-          lflags |= iw & (kListNaN | kListPartial | kListTimeout);
-          cand[i] = key ? key64(key, (uint32_t)((q >> 3) * G::EA) + (iw & kListIdx)) : 0ull;
-        }
-      }
-    } while (poll_again(A, ok, spins, &timed_out));
-  }
-  TLP(u, 1);
-  const uint32_t allf = __reduce_or_sync(kSettleFull, lflags);
-  if ((allf & kListTimeout) || timed_out) {
-    commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
-    return;
-  }
-  // q at every listed entry, in flight while the list is settled
-  float qc[CR];
-#pragma unroll
-  for (int i = 0; i < CR; ++i) {
-    const uint32_t v = key64_idx(cand[i]);
-    qc[i] = (has_q && cand[i] && v < (uint32_t)A.V) ? __ldcg(A.q + qrow + v) : 0.f;
-  }
-  u64 top = 0ull;
-#pragma unroll
-  for (int i = 0; i < CR; ++i) top = cand[i] > top ? cand[i] : top;
-  top = warp_max_u64(top);
-  const float m = from_okey((uint32_t)(top >> 32));
-  if ((allf & kListNaN) || top == 0ull || !(m > -INFINITY) || !(m < INFINITY)) {
-    commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
-    return;
-  }
-  const int am = (int)key64_idx(top);
-
-  // 2. kappa; tiles that may hold more
-  const u64 kappa = kth_listed<kBF16, CR>(cand, nrd, (uint32_t)K, (uint32_t)A.V);
-  TLP(u, 2);
-  bool unsafe = (allf & kListPartial) != 0;
-  if ((lane & 7) == 7) {
-#pragma unroll
-    for (int i = 0; i < CR; ++i) unsafe |= cand[i] != 0ull && cand[i] > kappa;
-  }
-  unsafe = __any_sync(kSettleFull, unsafe);
-  int n_k = 0;
-  const u64* lk;
-  const float* lq;
-  if (!unsafe) {
-    // the kept entries (exactly min(K, listed)): compact, then each goes to
-    // its rank (the number of kept entries above it)
-    uint32_t n = 0;
-#pragma unroll
-    for (int i = 0; i < CR; ++i) {
-      if (i < nrd) {
-        const bool in = cand[i] != 0ull && cand[i] >= kappa;
-        const unsigned ball = __ballot_sync(kSettleFull, in);
-        const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
-        if (in) {
-          S.sel[p] = cand[i];
-          S.qsel[p] = qc[i];
-        }
-        n += __popc(ball);
-      }
-    }
-    __syncwarp();
-    n_k = (int)n;
-    u64 e[kListRounds];
-    float eq[kListRounds];
-    uint32_t rk[kListRounds];
-#pragma unroll
-    for (int r = 0; r < kListRounds; ++r) {
-      const int i = 32 * r + lane;
-      e[r] = i < n_k ? S.sel[i] : 0ull;
-      eq[r] = i < n_k ? S.qsel[i] : 0.f;
-      rk[r] = 0u;
-    }
-#pragma unroll 4
-    for (int j = 0; j < n_k; ++j) {
-      const u64 kj = S.sel[j];
-#pragma unroll
-      for (int r = 0; r < kListRounds; ++r) rk[r] += kj > e[r] ? 1u : 0u;
-    }
-    u64* sk = S.cand;
-    float* sq = reinterpret_cast<float*>(S.hist);
-#pragma unroll
-    for (int r = 0; r < kListRounds; ++r)
-      if (32 * r + lane < n_k) {
-        sk[rk[r]] = e[r];
-        sq[rk[r]] = eq[r];
-      }
-    __syncwarp();
-    lk = sk;
-    lq = sq;
-  } else {
-    n_k = topk_rescan<kBF16, CR>(A, S, cand, R, nrd, NT, NL, kappa, K, lrow, qrow, has_q);
-    lk = S.sel;
-    lq = S.qsel;
-  }
-  TLP(u, 3);
-
-  // 3. the list, entry 32 r + lane in round r
-  uint32_t idx[kListRounds];
-  float val[kListRounds], ev[kListRounds], qv[kListRounds], cum[kListRounds];
+  // the list in shared memory (in the candidate area, no longer needed):
+  // entry i holds index, logit, e = exp2((l - m) c), q, prefix sum of e
+  // (entries 32 r + lane in rounds r: rolled loops keep the code small)
+  uint32_t* Li = reinterpret_cast<uint32_t*>(S.cand);
+  float* Lv = reinterpret_cast<float*>(Li + kTopkSmall);
+  float* Le = Lv + kTopkSmall;
+  float* Lq = Le + kTopkSmall;
+  float* Lc = Lq + kTopkSmall;
+  float* Lw = Lc + kTopkSmall;   // race weights
+  float* Lu = Lw + kTopkSmall;   // their margin weights
+  static_assert(7 * kTopkSmall * 4 <= sizeof(u64) * kMaxListCand, "list arrays exceed the candidate area");
+  const int nr = (n_k + 31) >> 5;
   float run = 0.f;
-#pragma unroll
-  for (int r = 0; r < kListRounds; ++r) {
+#pragma unroll 1
+  for (int r = 0; r < nr; ++r) {
     const int i = 32 * r + lane;
     const bool in = i < n_k;
     const u64 key = in ? lk[i] : 0ull;
-    idx[r] = in ? key64_idx(key) : 0xffffffffu;
-    val[r] = in ? from_okey((uint32_t)(key >> 32)) : 0.f;
-    ev[r] = in ? ex2((val[r] - m) * c) : 0.f;
-    qv[r] = in ? lq[i] : 0.f;
+    const float v = in ? from_okey((uint32_t)(key >> 32)) : 0.f;
+    const float e = in ? ex2((v - m) * c) : 0.f;
     // inclusive prefix sums in the total order (fixed order)
-    float inc = ev[r];
+    float inc = e;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(kSettleFull, inc, o);
       if (lane >= o) inc += y;
     }
-    cum[r] = run + inc;
+    if (in) {
+      Li[i] = key64_idx(key);
+      Lv[i] = v;
+      Le[i] = e;
+      Lq[i] = lq[i];
+      Lc[i] = run + inc;
+    }
     run += __shfl_sync(kSettleFull, inc, 31);
   }
   __syncwarp();
   TLP(u, 4);
-  const float Zk = list_get(cum, n_k - 1);
+  const float Zk = Lc[n_k - 1];
   uint32_t flags = cfg.bad_param ? SPEC_F_BAD_PARAM : 0u;
   int n_s = n_k;
   if (cfg.P < 1.0f) {
     const float target = cfg.P * Zk;
-#pragma unroll
-    for (int r = 0; r < kListRounds; ++r) {
-      const unsigned ball = __ballot_sync(kSettleFull, 32 * r + lane < n_k && cum[r] >= target);
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+      const int i = 32 * r + lane;
+      const unsigned ball = __ballot_sync(kSettleFull, i < n_k && Lc[i] >= target);
       if (ball) {
-        n_s = min(n_s, 32 * r + __ffs(ball));
+        n_s = 32 * r + __ffs(ball);
+        break;
       }
     }
-    const float at = list_get(cum, n_s - 1) / Zk;
-    const float bef = n_s >= 2 ? list_get(cum, n_s - 2) / Zk : 0.f;
+    const float at = Lc[n_s - 1] / Zk;
+    const float bef = n_s >= 2 ? Lc[n_s - 2] / Zk : 0.f;
     if (fabsf(at - cfg.P) < kMargin || fabsf(cfg.P - bef) < kMargin) flags |= SPEC_F_MARGIN_TOPP;
   }
-  const float Zs = list_get(cum, n_s - 1);
+  const float Zs = Lc[n_s - 1];
   const float invZ = 1.0f / Zs;
   const float lnZ = logf(Zs);
+  const int sr = (n_s + 31) >> 5;
   float alpha_v = 0.f;
   AcceptInfo ai;
   ai.valid = true;
@@ -1092,11 +899,12 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   bool need_race = !has_q;
   if (has_q) {
     float a = 0.f, ex = -1.f;
-#pragma unroll
-    for (int r = 0; r < kListRounds; ++r) {
-      if (32 * r + lane < n_s) {
-        a += fminf(ev[r] * invZ, qv[r]);
-        if (idx[r] == (uint32_t)pr.x) ex = ev[r];
+#pragma unroll 1
+    for (int r = 0; r < sr; ++r) {
+      const int i = 32 * r + lane;
+      if (i < n_s) {
+        a += fminf(Le[i] * invZ, Lq[i]);
+        if (Li[i] == (uint32_t)pr.x) ex = Le[i];
       }
     }
     alpha_v = warp_sum(a);
@@ -1114,63 +922,46 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     need_race = !ai.accept;
   }
   TLP(u, 5);
-  // 4. the draw: the two-level race over the kept entries (blocks by index)
+  // the draw: the two-level race over the kept entries (blocks by index)
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
   if (need_race) {
-    float* Lw = reinterpret_cast<float*>(S.sel);
-    float* Lu = Lw + kTopkSmall;
-    uint32_t* Lb = reinterpret_cast<uint32_t*>(Lu + kTopkSmall);
 #pragma unroll 1
     for (int attempt = 0; attempt < 2; ++attempt) {
       const bool resid = has_q && attempt == 0;   // attempt 1: an empty residual, draw from p
-      float w[kListRounds], wu[kListRounds];
-      uint32_t bl[kListRounds];
-      __syncwarp();
-#pragma unroll
-      for (int r = 0; r < kListRounds; ++r) {
+#pragma unroll 1
+      for (int r = 0; r < sr; ++r) {
         const int i = 32 * r + lane;
-        const bool in = i < n_s;
-        const float p = ev[r] * invZ;
-        w[r] = in ? (resid ? fmaxf(p - qv[r], 0.f) : p) : 0.f;
-        wu[r] = w[r] + ((in && resid) ? 2.0f * qv[r] : 0.f);
-        bl[r] = idx[r] / kRaceBlock;
-        if (i < kTopkSmall) {
-          Lw[i] = w[r];
-          Lu[i] = wu[r];
-          Lb[i] = bl[r];
+        if (i < n_s) {
+          const float p = Le[i] * invZ;
+          const float w = resid ? fmaxf(p - Lq[i], 0.f) : p;
+          Lw[i] = w;
+          Lu[i] = w + (resid ? 2.0f * Lq[i] : 0.f);
         }
       }
       __syncwarp();
       // level 1: a block's weights summed in list order; the block's first
       // entry with weight races for it
-      float W[kListRounds], WU[kListRounds];
-      bool owner[kListRounds];
-#pragma unroll
-      for (int r = 0; r < kListRounds; ++r) {
-        W[r] = 0.f;
-        WU[r] = 0.f;
-        owner[r] = w[r] > 0.f;
-      }
-#pragma unroll 2
-      for (int j = 0; j < n_s; ++j) {
-        const float wj = Lw[j], uj = Lu[j];
-        const uint32_t bj = Lb[j];
-        if (wj > 0.f) {
-#pragma unroll
-          for (int r = 0; r < kListRounds; ++r)
-            if (bj == bl[r]) {
-              W[r] += wj;
-              WU[r] += uj;
-              if (j < 32 * r + lane) owner[r] = false;
-            }
-        }
-      }
       Race r1;
       race_init(r1);
-#pragma unroll
-      for (int r = 0; r < kListRounds; ++r)
-        if (owner[r]) race_consider(r1, W[r], WU[r] - W[r], bl[r], block_word(A, row, pos, bl[r]));
+#pragma unroll 1
+      for (int r = 0; r < sr; ++r) {
+        const int i = 32 * r + lane;
+        const bool mine = i < n_s && Lw[i] > 0.f;
+        const uint32_t bl = mine ? Li[i] / kRaceBlock : 0xffffffffu;
+        float W = 0.f, WU = 0.f;
+        bool owner = mine;
+#pragma unroll 1
+        for (int j = 0; j < n_s; ++j) {
+          const float wj = Lw[j];
+          if (wj > 0.f && Li[j] / kRaceBlock == bl) {
+            W += wj;
+            WU += Lu[j];
+            owner = owner && j >= i;
+          }
+        }
+        if (owner) race_consider(r1, W, WU - W, bl, block_word(A, row, pos, bl));
+      }
       warp_race_merge(r1);
       if (r1.s1 < 0.f) {
         draw_flags |= SPEC_F_RESIDUAL_EMPTY;
@@ -1179,9 +970,12 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       // level 2: the entries of the winning block
       Race r2;
       race_init(r2);
-#pragma unroll
-      for (int r = 0; r < kListRounds; ++r)
-        if (w[r] > 0.f && bl[r] == r1.v1) race_consider(r2, w[r], wu[r] - w[r], idx[r], race_word(A, row, pos, idx[r]));
+#pragma unroll 1
+      for (int r = 0; r < sr; ++r) {
+        const int i = 32 * r + lane;
+        if (i < n_s && Lw[i] > 0.f && Li[i] / kRaceBlock == r1.v1)
+          race_consider(r2, Lw[i], Lu[i] - Lw[i], Li[i], race_word(A, row, pos, Li[i]));
+      }
       warp_race_merge(r2);
       y = r2.v1;
       if (draw_margin(r1) || draw_margin(r2)) draw_flags |= SPEC_F_MARGIN_DRAW;
@@ -1194,12 +988,14 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   {
     float vv = 0.f;
     bool own = false;
-#pragma unroll
-    for (int r = 0; r < kListRounds; ++r)
-      if (32 * r + lane < n_k && idx[r] == y) {
-        vv = val[r];
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+      const int i = 32 * r + lane;
+      if (i < n_k && Li[i] == y) {
+        vv = Lv[i];
         own = true;
       }
+    }
     const unsigned ob = __ballot_sync(kSettleFull, own);
     if (ob) vy = __shfl_sync(kSettleFull, vv, __ffs(ob) - 1);
   }
@@ -1221,6 +1017,176 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   }
   TLP(u, 7);
   commit_record(A, tag, u, row, rec);
+}
+
+// Settle a small top-k unit with the whole CTA (every thread calls it).
+//   1. The tiles' lists into shared memory (candidate q: tile q / 8, slot
+//      q mod 8), with q at every listed entry.
+//   2. The listed entries at or above tau, a value that ceil(K / 8) full
+//      lists end at or above (so at or below the K-th listed entry); each
+//      one's rank among them by counting; the K first go to their places,
+//      which sorts them.  kappa is the K-th.  A tile whose list is full and ends above kappa,
+//      or is marked partial, may hold more top-K entries: then warp 0 re-reads
+//      such tiles (topk_rescan).
+//   3. Warp 0: top-p, alpha, the accept test and the draw (topk_tail).
+template <bool kBF16>
+__device__ __noinline__ void topk_settle_cta(const Args& A, uint32_t tag, TopkCtaShm& C, int u, int row, int pos,
+                                             RowCfg cfg) {
+  using G = Geo<kBF16>;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nth = kCtaWarps * 32;
+  TopkScratch& S = C.ts;
+  const bool has_q = pos < A.k;
+  const int NT = ceil_div(A.V, G::EA);
+  const int NL = NT * kList;
+  const u64* R = A.rec + (size_t)u * A.NTA * kRecWords;
+  const size_t lrow = (size_t)u * A.V;
+  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
+  const int K = cfg.K;
+  Pre pr;
+  if (w == 0) pr = load_pre<kBF16>(A, u, row, pos);   // in flight meanwhile
+
+  // 1. the lists
+  uint32_t allf = 0;
+  bool timed_out = false;
+  {
+    long long spins = 0;
+    while (true) {
+      bool ok = true;
+      uint32_t fl = 0;
+      for (int q = tid; q < NL; q += nth) {
+        const u64* r = R + (size_t)(q >> 3) * kRecWords + 2 * (q & 7);
+        const u64 wk = __ldcg(r), wi = __ldcg(r + 1);
+        ok = ok && tag_ok(wk, tag) && tag_ok(wi, tag);
+        const uint32_t key = (uint32_t)wk, iw = (uint32_t)wi;
+        fl |= iw & (kListNaN | kListPartial | kListTimeout);
+        S.cand[q] = key ? key64(key, (uint32_t)((q >> 3) * G::EA) + (iw & kListIdx)) : 0ull;
+        if ((q & 7) == 0) S.cflag[q >> 3] = (uint8_t)((iw & kListPartial) ? 2u : 0u);
+      }
+      const int all_ok = __syncthreads_and(ok ? 1 : 0);
+      allf = (uint32_t)__syncthreads_or((int)fl);
+      if (all_ok) break;
+      if (++spins > kSpinLimit) {
+        if (tid == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+        timed_out = true;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  TLP(u, 1);
+  if ((allf & kListTimeout) || timed_out) {
+    if (w == 0) commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    return;
+  }
+  // the maximum and the count of listed entries; tau (warp 0): the
+  // ceil(K / 8)-th largest value key among the last entries of full lists --
+  // that many lists hold 8 entries at or above it, so the K-th listed entry
+  // is at or above it
+  u64 top = 0ull;
+  uint32_t cnt = 0;
+  for (int q = tid; q < NL; q += nth) {
+    const u64 k = S.cand[q];
+    top = k > top ? k : top;
+    cnt += k ? 1u : 0u;
+  }
+  top = warp_max_u64(top);
+  cnt = __reduce_add_sync(kSettleFull, cnt);
+  if (lane == 0) {
+    C.wmax[w] = top;
+    C.wcnt[w] = cnt;
+  }
+  if (w == 0) {
+    uint32_t v[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int ch = lane + 32 * i;
+      v[i] = ch < NT ? (uint32_t)(S.cand[ch * kList + kList - 1] >> 32) : 0u;
+    }
+    static_assert(kMaxListCand / kList <= 96, "three list ends per lane");
+    uint32_t tau = 0u;
+    const int need = (K + kList - 1) / kList;
+#pragma unroll 1
+    for (int i = 0; i < need; ++i) {
+      const uint32_t lm = max(v[0], max(v[1], v[2]));
+      const uint32_t M = __reduce_max_sync(kSettleFull, lm);
+      tau = M;
+      if (M == 0u) break;
+      // one occurrence leaves: the first lane holding it, its first slot
+      const int src = __ffs(__ballot_sync(kSettleFull, lm == M)) - 1;
+      if (lane == src) {
+        if (v[0] == M) v[0] = 0u;
+        else if (v[1] == M) v[1] = 0u;
+        else v[2] = 0u;
+      }
+    }
+    if (lane == 0) {
+      C.tau = tau;
+      C.nf = 0u;
+    }
+  }
+  __syncthreads();
+  top = 0ull;
+  cnt = 0;
+  for (int i = 0; i < kCtaWarps; ++i) {
+    top = C.wmax[i] > top ? C.wmax[i] : top;
+    cnt += C.wcnt[i];
+  }
+  const float m = from_okey((uint32_t)(top >> 32));
+  if ((allf & kListNaN) || top == 0ull || !(m > -INFINITY) || !(m < INFINITY)) {
+    if (w == 0) commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
+    return;
+  }
+  const int am = (int)key64_idx(top);
+
+  // 2. the listed entries at or above tau (a few more than K), with their q
+  // (loads in flight during the ranking); each one's rank among them by
+  // counting; the K first go to their places
+  const uint32_t tau = C.tau;
+  u64 mk[kCandPerThread];
+  float mq[kCandPerThread];
+#pragma unroll
+  for (int i = 0; i < kCandPerThread; ++i) {
+    const int q = tid + nth * i;
+    mk[i] = 0ull;
+    mq[i] = 0.f;
+    if (q < NL) {
+      const u64 k = S.cand[q];
+      if (k != 0ull && (uint32_t)(k >> 32) >= tau) {
+        mk[i] = k;
+        C.fk[atomicAdd(&C.nf, 1u)] = k;
+        const uint32_t v = key64_idx(k);
+        if (has_q && v < (uint32_t)A.V) mq[i] = __ldcg(A.q + qrow + v);
+      }
+    }
+  }
+  __syncthreads();
+  const int nf = (int)C.nf;
+#pragma unroll
+  for (int i = 0; i < kCandPerThread; ++i) {
+    if (mk[i] == 0ull) continue;
+    uint32_t rk = 0;
+#pragma unroll 4
+    for (int j = 0; j < nf; ++j) rk += C.fk[j] > mk[i] ? 1u : 0u;
+    if (rk < (uint32_t)K) {
+      S.sel[rk] = mk[i];
+      S.qsel[rk] = mq[i];
+    }
+  }
+  __syncthreads();
+  const int n_k = (int)min(cnt, (uint32_t)K);
+  const u64 kappa = cnt >= (uint32_t)K ? S.sel[K - 1] : 0ull;
+  bool unsafe = false;
+  for (int ch = tid; ch < NT; ch += nth) {
+    const u64 last = S.cand[ch * kList + kList - 1];
+    unsafe |= (S.cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa);
+  }
+  unsafe = __syncthreads_or(unsafe ? 1 : 0) != 0;
+  TLP(u, 2);
+  if (w != 0) return;
+  int nk = n_k;
+  if (unsafe) nk = topk_rescan<kBF16>(A, S, NT, NL, kappa, K, lrow, qrow, has_q);
+  topk_tail<kBF16>(A, tag, S, u, row, pos, cfg, pr, S.sel, S.qsel, nk, m, am);
 }
 
 }  // namespace specv

@@ -113,12 +113,13 @@ extern "C" int spec_verify_commit(const void* logits, int logits_dtype, const fl
                                   const int32_t* cache_slot, float* cache_rec, uint16_t* cache_conv, int L, int H,
                                   int Dk, int Dv, int W, int C, int slots, void* cuda_stream) {
   using namespace specv;
-  int rc = verify_check(logits, logits_dtype, draft_probs, draft_tokens, params, B, k, V, tokens, accept_len,
-                        logprobs, alpha, flags, true, workspace, workspace_bytes);
+  // the commit's argument checks, then the verify's (which end with the device query)
+  if (B < 0 || k < 0 || k > SPEC_MAX_K) return SPEC_E_DIM;
+  int rc = commit_check(verify_rec, verify_conv, accept_len, cache_slot, nullptr, nullptr, cache_rec, cache_conv, L, B,
+                        k + 1, H, Dk, Dv, W, C, slots, flags);
   if (rc != SPEC_OK) return rc;
-  const int S = k + 1;
-  rc = commit_check(verify_rec, verify_conv, accept_len, cache_slot, nullptr, nullptr, cache_rec, cache_conv, L, B, S,
-                    H, Dk, Dv, W, C, slots, flags);
+  rc = verify_check(logits, logits_dtype, draft_probs, draft_tokens, params, B, k, V, tokens, accept_len, logprobs,
+                    alpha, flags, true, workspace, workspace_bytes);
   if (rc != SPEC_OK || B == 0) return rc;
   FusedCommit F;
   memset(&F, 0, sizeof(F));

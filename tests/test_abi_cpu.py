@@ -55,7 +55,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.spec_version() == 2
+    assert lib.spec_version() == 3
     for code in range(0, -8, -1):
         s = lib.spec_status_string(code).decode()
         assert s and s != "unknown status code"
@@ -152,3 +152,42 @@ def test_philox_argument_errors(lib):
     assert lib.spec_philox4x32_10(None, 0, P, 4, None) == -1
     assert lib.spec_philox4x32_10(P + 4, 0, P, 4, None) == -4
     assert lib.spec_philox4x32_10(P, 0, P, 4, None) in (-6, -7)
+
+
+def _fused(lib, **kw):
+    vp, i32, u32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t
+    lib.spec_verify_commit.argtypes = ([vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz]
+                                       + [vp] * 5 + [i32] * 7 + [vp])
+    lib.spec_verify_commit.restype = i32
+    a = dict(logits=P, dt=1, q=P, x=P, params=P, seed=0, row_base=0, B=4, k=2, V=1000, tok=P, acc=P,
+             lp=P, alpha=P, flags=P, ws=P, wsb=1 << 20, vr=P, vc=P, slot=P, cr=P, cc=P, L=2, H=2, Dk=4,
+             Dv=4, W=2, C=8, slots=4, stream=None)
+    a.update(kw)
+    return lib.spec_verify_commit(a["logits"], a["dt"], a["q"], a["x"], a["params"], a["seed"], a["row_base"],
+                                  a["B"], a["k"], a["V"], a["tok"], a["acc"], a["lp"], a["alpha"], a["flags"],
+                                  a["ws"], a["wsb"], a["vr"], a["vc"], a["slot"], a["cr"], a["cc"], a["L"],
+                                  a["H"], a["Dk"], a["Dv"], a["W"], a["C"], a["slots"], a["stream"])
+
+
+def test_fused_verify_commit_checks_every_argument_before_touching_cuda(lib):
+    # the verify's checks
+    assert _fused(lib, B=-1) == -2
+    assert _fused(lib, k=17) == -2
+    assert _fused(lib, V=0) == -2
+    assert _fused(lib, dt=7) == -3
+    assert _fused(lib, logits=None) == -1
+    assert _fused(lib, flags=None) == -1
+    assert _fused(lib, wsb=16) == -5
+    assert _fused(lib, ws=None) == -1
+    # the commit's checks
+    assert _fused(lib, H=0) == -2
+    assert _fused(lib, L=-1) == -2
+    assert _fused(lib, cr=None) == -1
+    assert _fused(lib, vr=None, vc=None) == -1
+    assert _fused(lib, slot=None, slots=2) == -2      # identity slots need slots >= B
+    assert _fused(lib, vr=P + 2) == -4
+    assert _fused(lib, slot=P + 2) == -4
+    # nothing to do, or nothing to commit: the verify alone
+    assert _fused(lib, B=0) == 0
+    assert _fused(lib, L=0) in (-6, -7)
+    assert _fused(lib) in (-6, -7)
