@@ -109,7 +109,7 @@ enum {
  *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
  *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
  *                 settle or finalize wait for records, 8 the row-order wait
- *                 of batches above 256 rows, 16 a grid barrier); 0 when
+ *                 of batches above 256 rows; 16 is unused); 0 when
  *                 every wait ended normally.                                */
 size_t spec_verify_workspace_size(int B, int k, int V);
 

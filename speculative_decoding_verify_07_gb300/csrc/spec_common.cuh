@@ -57,7 +57,7 @@ enum {
   ERR_COPY_WAIT = 2,       // a tile's bulk copy did not complete
   ERR_RECORD_WAIT = 4,     // a settle or finalize gave up waiting for records
   ERR_ORDER_WAIT = 8,      // a CTA gave up waiting for the row order
-  ERR_BARRIER = 16         // a grid barrier wait gave up
+  ERR_QUEUE = 16           // unused
 };
 
 struct WsHeader {
@@ -72,9 +72,7 @@ struct WsHeader {
   uint32_t n_class[4];    // rows per class (large batches)
   uint32_t commit_next;   // fused commit: next copy job
   uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
-  uint32_t bar;           // grid barrier arrivals of the running call
-  uint32_t settle_next;   // next warp-settled unit of the settle pass
-  uint32_t pad[43];
+  uint32_t pad[45];
   uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
   uint32_t pad1[4];
 };
@@ -216,6 +214,8 @@ struct Args {
   int B, k, V, U;
   int NTA, NTB;           // record strides per unit: A tiles, B tiles
   int n_ctas;             // CTAs of the kernel
+  int n_settle;           // settle CTAs: blocks 0, stride, 2 stride, ... (n_settle of them)
+  int settle_stride;
   int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;

@@ -27,6 +27,34 @@ struct alignas(16) GenShm {
   int bci[16];
 };
 
+// One pass over a unit's row by the group: fn(g, v) for every group g of 8
+// entries (thread t takes groups t, t + kThreads, ...), kGenBatch groups of
+// a thread loaded before any is used, so that the pass is bound by
+// bandwidth rather than by one load's latency per group.  Groups past the
+// row hold -inf (the callers check g * 8 + i < V as well).
+constexpr int kGenBatch = 4;
+template <bool kBF16, typename F>
+__device__ __forceinline__ void gsweep(const Args& A, size_t lrow, int G, F fn) {
+  for (int g0 = ctid(); g0 < G; g0 += kThreads * kGenBatch) {
+    float v[kGenBatch][8];
+#pragma unroll
+    for (int b = 0; b < kGenBatch; ++b) {
+      const int g = g0 + b * kThreads;
+      if (g < G) {
+        load_group<kBF16>(A, lrow, g, true, v[b]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[b][i] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kGenBatch; ++b) {
+      const int g = g0 + b * kThreads;
+      if (g < G) fn(g, v[b]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Block reductions (fixed combination order, so results are reproducible).
 // Each returns its result in every thread.
@@ -295,23 +323,39 @@ __device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, floa
   const int lane = ctid() & 31, wp = ctid() >> 5;
   Race r;
   race_init(r);
-  for (int base = 0; base < G; base += kThreads) {
-    const int g = base + ctid();
-    float w8 = 0.f, u8 = 0.f;
-    if (g < G) {
-      float w[8], tq[8];
-      race_weights<kBF16>(A, lrow, qrow, g, m, c, invZ, mode, th, w, tq);
+  constexpr int QB = kGenBatch / 2;   // groups in flight: logits and q
+  for (int base0 = 0; base0 < G; base0 += kThreads * QB) {
+    float v[QB][8], qv[QB][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (w[j] > 0.f) {
-          w8 += w[j];
-          u8 += w[j] + tq[j];
-        }
+    for (int b = 0; b < QB; ++b) {
+      const int g = base0 + b * kThreads + ctid();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) qv[b][j] = 0.f;
+      if (g < G) {
+        load_group<kBF16>(A, lrow, g, true, v[b]);
+        if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv[b]);
+      }
     }
-    const float W = warp_sum(w8), U = warp_sum(u8);
-    if (lane == 0 && W > 0.f) {
-      const uint32_t b = (uint32_t)(base / (kRaceBlock / 8) + wp);
-      race_consider(r, W, U - W, b, block_word(A, row, pos, b));
+#pragma unroll
+    for (int b = 0; b < QB; ++b) {
+      const int base = base0 + b * kThreads;
+      const int g = base + ctid();
+      float w8 = 0.f, u8 = 0.f;
+      if (g < G) {
+        float w[8], tq[8];
+        group_weights(A, g, v[b], qv[b], m, c, invZ, mode, th, w, tq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (w[j] > 0.f) {
+            w8 += w[j];
+            u8 += w[j] + tq[j];
+          }
+      }
+      const float W = warp_sum(w8), U = warp_sum(u8);
+      if (lane == 0 && W > 0.f) {
+        const uint32_t bk = (uint32_t)(base / (kRaceBlock / 8) + wp);
+        race_consider(r, W, U - W, bk, block_word(A, row, pos, bk));
+      }
     }
   }
   return block_race(S, r);
@@ -353,46 +397,41 @@ __device__ uint32_t draw_row(const Args& A, GenShm& S, int row, int pos, float m
 template <bool kBF16>
 __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_t tkey, unsigned long long n) {
   const int G = (A.V + 7) / 8;
+  constexpr int NB = kGenBatch;   // a thread takes NB consecutive groups a round
   unsigned long long need = n;
   uint32_t found = 0xffffffffu;
-  for (int base = 0; base < G; base += kThreads) {
-    const int g = base + ctid();
+  for (int base = 0; base < G; base += kThreads * NB) {
+    const int g0 = base + ctid() * NB;
+    float v[NB][8];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      if (g0 + b < G) load_group<kBF16>(A, lrow, g0 + b, true, v[b]);
     int c = 0;
-    float v[8];
-    if (g < G) {
-      load_group<kBF16>(A, lrow, g, true, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (g * 8 + i < A.V && okey(v[i]) == tkey) ++c;
-    }
-    int inc = c;
-    const int lane = ctid() & 31, w = ctid() >> 5;
+    for (int b = 0; b < NB; ++b)
+      if (g0 + b < G) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += y;
-    }
-    int* wsum = reinterpret_cast<int*>(S.wred);
-    if (lane == 31) wsum[w] = inc;
-    csync();
-    int woff = 0, rowtot = 0;
-    for (int i = 0; i < kWarps; ++i) {
-      if (i < w) woff += wsum[i];
-      rowtot += wsum[i];
-    }
-    const int exc = woff + inc - c;
+        for (int i = 0; i < 8; ++i)
+          if ((g0 + b) * 8 + i < A.V && okey(v[b][i]) == tkey) ++c;
+      }
+    int rowtot = 0;
+    const int exc = block_exclusive_scan(S, c, &rowtot);
     if (c > 0 && need > (unsigned long long)exc && need <= (unsigned long long)(exc + c)) {
       int want = (int)(need - exc);
-      for (int i = 0; i < 8; ++i) {
-        if (g * 8 + i < A.V && okey(v[i]) == tkey && --want == 0) {
-          S.bci[3] = g * 8 + i;
-          break;
+      for (int b = 0; b < NB && want > 0; ++b) {
+        const int g = g0 + b;
+        if (g >= G) break;
+        for (int i = 0; i < 8; ++i) {
+          if (g * 8 + i < A.V && okey(v[b][i]) == tkey && --want == 0) {
+            S.bci[10] = g * 8 + i;
+            break;
+          }
         }
       }
     }
     csync();
     if (need <= (unsigned long long)rowtot) {
-      found = (uint32_t)S.bci[3];
+      found = (uint32_t)S.bci[10];
       csync();
       break;
     }
@@ -412,9 +451,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   // pass 1: max, argmax, NaN
   unsigned long long best = 0;
   bool nan_seen = false;
-  for (int g = ctid(); g < G; g += kThreads) {
-    float v[8];
-    load_group<kBF16>(A, lrow, g, true, v);
+  gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
     const float gm = group_max(v);
     if (gm != gm) {
       nan_seen = true;
@@ -425,9 +462,10 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
         if (v[i] == gm) first = i;
       best = key64(okey(gm), (uint32_t)(g * 8 + first));
     }
-  }
+  });
   if (nan_seen) best = ~0ull;
   best = block_max_u64(S, best);
+  if (ctid() < 32) TLP(u, 1);
   const float m = from_okey((uint32_t)(best >> 32));
   const int am = (int)key64_idx(best);
   if (best == 0 || !(m > -INFINITY) || !(m < INFINITY)) {
@@ -446,13 +484,11 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   if (cfg.K > 0) {
     unsigned long long need = (unsigned long long)cfg.K;
     auto each = [&](auto fn) {
-      for (int g = ctid(); g < G; g += kThreads) {
-        float v[8];
-        load_group<kBF16>(A, lrow, g, true, v);
+      gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (g * 8 + i < A.V) fn(km - kf<kBF16>(v[i]));
-      }
+      });
     };
     const uint32_t d = kth_distance(S, each, need, kBF16 ? 0 : 16, kBF16 ? 16 : 32);
     th.tkey = full_key<kBF16>(km - d);
@@ -468,9 +504,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   csync();
   unsigned long long tail = 0;
   float z0 = 0.f, z1 = 0.f;
-  for (int g = ctid(); g < G; g += kThreads) {
-    float v[8];
-    load_group<kBF16>(A, lrow, g, true, v);
+  gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float x = (v[i] - m) * c;
@@ -484,8 +518,9 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
         else tail += fx;
       }
     }
-  }
+  });
   float Zs;
+  if (ctid() < 32) TLP(u, 2);
   if (topp) {
     csync();
     tail = block_sum_u64(S, tail);
@@ -503,9 +538,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
     select_from_bin0(S, target, &b, &above);
     // key range of bin b
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int g = ctid(); g < G; g += kThreads) {
-      float v[8];
-      load_group<kBF16>(A, lrow, g, true, v);
+    gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (g * 8 + i >= A.V) continue;
@@ -518,8 +551,9 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
           kmax = max(kmax, key);
         }
       }
-    }
+    });
     const uint2 mm = block_minmax_u32(S, kmin, kmax);
+    if (ctid() < 32) TLP(u, 3);
     uint32_t lo = mm.x, hi = mm.y;
     unsigned long long rem = target - above;
     int hs = 1;
@@ -531,9 +565,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
       S.mlo[slot][ctid()] = 0;
       S.mhi[slot][ctid()] = 0;
       csync();
-      for (int g = ctid(); g < G; g += kThreads) {
-        float v[8];
-        load_group<kBF16>(A, lrow, g, true, v);
+      gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (g * 8 + i >= A.V) continue;
@@ -543,7 +575,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
           const uint32_t bin = (hi - key) >> shift;
           mass_add(&S.mlo[slot][bin], &S.mhi[slot][bin], mass_fixed(ex2((v[i] - m) * c)));
         }
-      }
+      });
       csync();
       S.total[ctid()] = ((unsigned long long)S.mhi[slot][ctid()] << 32) + S.mlo[slot][ctid()];
       csync();
@@ -560,6 +592,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
       if (shift == 0) lo = hi;
     }
     const uint32_t tkey = hi;
+    if (ctid() < 32) TLP(u, 4);
     const float et = ex2((from_okey(tkey) - m) * c);
     const unsigned long long efx = mass_fixed(et);
     unsigned long long n_need = efx ? (rem + efx - 1) / efx : 1ull;
@@ -568,6 +601,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
     // prefix of the ties in index order, so the rank carries over
     th.tidx = nth_tie_index<kBF16>(A, S, lrow, tkey, n_need);
     th.tkey = tkey;
+    if (ctid() < 32) TLP(u, 5);
     const unsigned long long zs_fx = above + n_need * efx;
     Zs = (float)((double)zs_fx * (1.0 / 1099511627776.0));
     const double at = (double)zs_fx / (double)zk;
@@ -593,19 +627,32 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   // alpha pass
   float al0 = 0.f, al1 = 0.f;
   if (has_q) {
-    for (int g = ctid(); g < G; g += kThreads) {
-      float v[8], qv[8];
-      load_group<kBF16>(A, lrow, g, true, v);
-      load_q8(A, qrow, g * 8, qv);
+    constexpr int QB = kGenBatch / 2;   // groups in flight: logits and q
+    for (int g0 = ctid(); g0 < G; g0 += kThreads * QB) {
+      float v[QB][8], qv[QB][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const bool in = (g * 8 + i < A.V) && kept(th, okey(v[i]), (uint32_t)(g * 8 + i));
-        const float p = in ? ex2((v[i] - m) * c) * invZ : 0.f;
-        if (i & 1) al1 += fminf(p, qv[i]); else al0 += fminf(p, qv[i]);
+      for (int b = 0; b < QB; ++b) {
+        const int g = g0 + b * kThreads;
+        if (g < G) {
+          load_group<kBF16>(A, lrow, g, true, v[b]);
+          load_q8(A, qrow, g * 8, qv[b]);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < QB; ++b) {
+        const int g = g0 + b * kThreads;
+        if (g >= G) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool in = (g * 8 + i < A.V) && kept(th, okey(v[b][i]), (uint32_t)(g * 8 + i));
+          const float p = in ? ex2((v[b][i] - m) * c) * invZ : 0.f;
+          if (i & 1) al1 += fminf(p, qv[b][i]); else al0 += fminf(p, qv[b][i]);
+        }
       }
     }
   }
   const float alpha_v = has_q ? block_sum(S, al0 + al1) : 0.f;
+  if (ctid() < 32) TLP(u, 6);
   // the draw: residual after a rejection, p at the bonus position
   uint32_t draw_flags = 0;
   uint32_t y = 0xffffffffu;
@@ -618,6 +665,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
     }
     if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
   }
+  if (ctid() < 32) TLP(u, 7);
   UnitRecord rec = empty_record(flags);
   if (ctid() == 0) {
     if (has_q) {

@@ -1,33 +1,40 @@
 // spec_verify: the verify kernel (sm_103a).
 //
 // One persistent CTA of 12 warps per SM, launched cooperatively (every CTA
-// is resident, so CTAs may wait on one another; every such wait is
-// bounded).  The work runs in passes separated by grid barriers, so that
-// each pass runs one kind of code on every SM and the latency-bound settles
-// never queue behind the stream's copies:
-//   1. A pass.  Every warp owns two 8 KB shared-memory buffers and has the
-//      copy engine fill one (cp.async.bulk completed on an mbarrier) while
-//      it reduces the other; the A tiles of all units (4096 bf16 / 2048
-//      fp32 logits) are taken from one counter, class by class (small
-//      top-k, greedy, unfiltered rows last, so that their logits are still
-//      in L2 for the B pass).  A tile yields its max, the softmax sum
-//      relative to it, the first argmax (greedy), the level-1 race of its
-//      256-entry blocks (bonus positions) or its 8 largest entries in the
-//      total order (small top-k), as tagged record words.
-//   2. Settles.  One warp per unit (spec_settle.cuh): greedy and small
-//      top-k units and bonus positions are settled; a drafted unfiltered
-//      unit takes its accept test and publishes its state.  Warps without a
-//      unit bring the q rows of the B pass into L2 meanwhile.
-//   3. B pass (drafted positions of unfiltered rows only).  A B tile (1280
-//      bf16 / 1024 fp32 logits, read again from L2, plus q) computes alpha =
-//      sum min(p, q) and the level-1 race of the residual from the state.
-//   4. Their settles: alpha and the residual draw.
-// The last settled unit of a row resolves its accept chain and writes the
-// row's outputs.  Rows that need a global threshold search
-// (spec_general.cuh) are taken last by the CTAs' first 256 threads, and the
-// fused commit (spec_fused.cuh) follows.  Results pass between warps as
-// 64-bit words tagged with the call's epoch; reductions have a fixed order
-// and no floating-point atomics are used, so results are bit-reproducible.
+// is resident, so warps may wait on one another; every such wait is
+// bounded).  CTAs take one of two roles, so that each SM runs one kind of
+// code and keeps it in its instruction cache:
+//   * Stream CTAs (about 9 in 10).  Each of their 12 warps owns two 8 KB
+//     shared-memory buffers and has the copy engine fill one (cp.async.bulk
+//     completed on an mbarrier) while it reduces the other.  The tiles of
+//     all units form one sequence of segments: A tiles of small top-k rows
+//     (their settles are the longest, so they come first); unfiltered rows
+//     in waves (each wave's drafted positions, then its bonus positions),
+//     the B tiles of a wave placed a fixed number of items after its A
+//     tiles; A tiles of greedy rows.  Item t belongs to stream CTA t mod
+//     (stream CTAs), whose warps take its items in order from a
+//     shared-memory counter; a unit's tiles are taken in a rotated order.
+//     An A tile (4096 bf16 / 2048 fp32 logits of one unit) yields the tile
+//     max, the softmax sum relative to it, the first argmax (greedy), the
+//     level-1 race of its 256-entry blocks (bonus positions) or the 8
+//     largest entries in the total order (small top-k).  A B tile (1280 /
+//     1024 logits, read again from L2, plus q) computes alpha = sum min(p, q)
+//     and the level-1 race of the residual from the unit's published state.
+//     After a tile's record the warp adds one to the unit's tile count (a
+//     reduction nobody waits for).
+//   * Settle CTAs (about 1 in 10, every stride-th block).  Their warps take
+//     the settle tasks -- one per unit after its A tiles, one per drafted
+//     unfiltered unit after its B tiles -- in the order of the sequence,
+//     task t to settle warp t mod (warps); a warp waits for its task's tile
+//     count, settles the unit (spec_settle.cuh) and clears the count.  Tasks
+//     come in the order their tiles do, and a B tile only waits for a state
+//     that an earlier task publishes, so every wait ends.  The last settled
+//     unit of a row resolves its accept chain and writes the row's outputs.
+// Rows that need a global threshold search (spec_general.cuh) are taken
+// last by the CTAs' first 256 threads, and the fused commit (spec_fused.cuh)
+// follows.  Results pass between warps as 64-bit words tagged with the
+// call's epoch; reductions have a fixed order and no floating-point atomics
+// are used, so results are bit-reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,13 +48,26 @@
 
 namespace specv {
 
-constexpr int kNW = kCtaWarps;         // warps per CTA
+constexpr int kNW = kCtaWarps;         // warps per CTA (stream warps of a stream CTA, settle warps of a settle CTA)
 constexpr int kAllThreads = kNW * 32;
 constexpr int kOrderSmem = 256;        // batches up to this many rows keep order and configs in shared memory
 constexpr int kStage = 64;             // per-warp staging of a top-k tile's candidates
+constexpr int kMaxWaves = 40;
+constexpr int kMaxSeg = 4 * kMaxWaves + 8;   // segments of the item sequence (2 A and at most 2 more per wave, 2 classes)
+constexpr int kSettleEvery = 9;        // one settle CTA per this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kAllThreads >= kOrderSmem, "one placement round for a shared-memory order");
 static_assert(kAllThreads >= kThreads, "the general phase uses the first kThreads threads");
+
+// A segment of the item sequence: `nrows` rows from index `first` of the
+// class order, each contributing the units at positions pos_lo ..
+// pos_lo + upr - 1, each unit `tiles` tiles of one kind.
+struct Seg {
+  uint32_t start;     // first item of the segment
+  uint32_t first;
+  uint32_t nrows;
+  uint32_t packed;    // tiles | pos_lo << 16 | upr << 21 | kind << 26 (0 A, 1 B)
+};
 
 struct OrderScratch {
   int n_class[4];
@@ -61,17 +81,21 @@ struct alignas(128) VShm {
       unsigned char buf[kNW][2][kSlot];  // stream buffers
       u64 stage[kNW][kStage];            // top-k tile staging
     } s;
-    TopkCtaShm tkc;                      // settle scratch of a small top-k unit
+    TopkScratch tk[kNW];                 // settle scratch (settle CTAs)
     GenShm gen;                          // general-path group, after the roles
   };
-  unsigned long long bar[kNW][2];        // the warps' stream-buffer barriers
-  uint32_t par[kNW][2];                  // their phase parities (carried from the A pass to the B pass)
-  uint32_t broken[kNW];                  // a copy wait of the warp gave up: its buffers are not used again
-  uint32_t ticket[2];                    // the CTA's item counters of the A and B passes
+  unsigned long long bar[kNW][2];
   unsigned long long cbar[kNW][2];       // fused commit: the warps' copy barriers
+  uint32_t broken[kNW];                  // a copy wait of the warp gave up: its buffers are not used again
+  uint32_t ticket;                       // the stream CTA's item counter
+  Seg seg[kMaxSeg];
+  uint32_t tstart[kMaxSeg];              // first settle task of each segment
+  uint32_t bready[kMaxWaves];            // segment building: when each wave's B tiles fall due
   uint32_t order[kOrderSmem];
   RowPack cfg[kOrderSmem];
   OrderScratch ord;
+  int nseg;
+  uint32_t ntasks;
   int gtask;
   uint32_t tag;
 };
@@ -161,13 +185,13 @@ __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, 
 }
 
 // ---------------------------------------------------------------------------
-// Work of the phases.  Units are taken class by class: small top-k rows,
-// greedy rows, then unfiltered rows (whose logits the B pass reads again, so
-// they are the last to enter L2); each row contributes its k + 1 positions.
+// The item sequence.
 // ---------------------------------------------------------------------------
 struct Plan {
-  const uint32_t* order;    // rows by class: [unfiltered][small top-k][general][greedy]
+  const uint32_t* order;
   const RowPack* cfg;       // per-row configs in shared memory (null: classify from the parameters)
+  const Seg* seg;
+  int nseg;
   int nD, nT, nG, nX;       // rows: unfiltered, small top-k, greedy, general
   int NTA, NTB;             // tiles per unit of this call's dtype
 };
@@ -175,9 +199,10 @@ struct Plan {
 // A work item.  kind: 0 none, 1 A tile, 2 B tile.
 struct Item {
   int kind;
-  uint32_t t;               // index in its pass
+  uint32_t t;               // index in the sequence
   int reread;               // the logits are read again later (default L2 policy)
   int row, pos, u, c, n;    // unit, tile, valid entries in the tile
+  int ntiles;               // tiles of this kind in the unit
 };
 
 // Classification from the parameters (batches whose configs are not kept in
@@ -187,48 +212,117 @@ __device__ __forceinline__ RowCfg plan_cfg(const Args& A, Plan P, int row) {
   return P.cfg ? unpack_cfg(P.cfg[row]) : classify_row(A, row);
 }
 
-// Row ri of the A pass order: small top-k, greedy, unfiltered.
-__device__ __forceinline__ int a_row(const Plan& P, int ri) {
-  if (ri < P.nT) return (int)P.order[P.nD + ri];
-  ri -= P.nT;
-  if (ri < P.nG) return (int)P.order[P.nD + P.nT + P.nX + ri];
-  return (int)P.order[ri - P.nG];
+__device__ __forceinline__ Seg make_seg(uint32_t first, uint32_t nrows, int pos_lo, int upr, int tiles, int kind) {
+  Seg s;
+  s.start = 0;
+  s.first = first;
+  s.nrows = nrows;
+  s.packed = (uint32_t)tiles | ((uint32_t)pos_lo << 16) | ((uint32_t)upr << 21) | ((uint32_t)kind << 26);
+  return s;
 }
-__device__ __forceinline__ int a_units(const Args& A, const Plan& P) { return (P.nT + P.nG + P.nD) * (A.k + 1); }
-__device__ __forceinline__ int b_units(const Args& A, const Plan& P) { return P.nD * A.k; }
+__device__ __forceinline__ uint32_t seg_items(const Seg& s) {
+  return s.nrows * ((s.packed >> 21) & 31u) * (s.packed & 0xffffu);
+}
 
-// Item t of a pass: A tiles (pass 1) of every unit in the A pass order, or
-// B tiles (pass 2) of the drafted positions of unfiltered rows.
+// The segment table (thread 0 of every CTA builds the same one).  The A
+// tiles come class by class, the classes with the longest settles first:
+// small top-k rows, unfiltered rows in waves (each wave's drafted positions,
+// then its bonus positions), greedy rows.  The B tiles of a wave wait in
+// a queue until `b_delay` items have been placed after the wave's A tiles
+// (the wave's settles finish meanwhile) and are then inserted at the next
+// row boundary; waves still waiting at the end come last.
+__device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
+                                            int NTB, uint32_t b_delay) {
+  if (threadIdx.x != 0) return;
+  const int k = A.k, k1 = A.k + 1;
+  Seg* sg = S.seg;
+  int n = 0;
+  uint32_t pos = 0;   // items placed so far
+  int nw = 0, Rw = 1;
+  if (nD > 0) {
+    // a wave's A tiles are about b_delay items; waves of equal size
+    const uint32_t row_items = (uint32_t)k1 * (uint32_t)NTA;
+    Rw = (int)max(1u, b_delay / max(1u, row_items));
+    Rw = max(Rw, ceil_div(nD, kMaxWaves));
+    nw = ceil_div(nD, Rw);
+    Rw = ceil_div(nD, nw);
+    nw = ceil_div(nD, Rw);
+  }
+  uint32_t* ready = S.bready;   // waves [bh, bt) wait for their B tiles: the item count they wait for
+  int bh = 0, bt = 0;
+  auto place = [&](Seg sgm) {
+    sgm.start = pos;
+    pos += seg_items(sgm);
+    sg[n++] = sgm;
+  };
+  auto place_b = [&](int w) {
+    place(make_seg((uint32_t)(w * Rw), (uint32_t)min(Rw, nD - w * Rw), 0, k, NTB, 1));
+  };
+  // rows [f, f + nr) of an A class, split where a B wave falls due
+  auto place_rows = [&](uint32_t f, uint32_t nr, int pos_lo, int upr) {
+    const uint32_t per_row = (uint32_t)upr * (uint32_t)NTA;
+    while (nr > 0) {
+      while (bh < bt && pos >= ready[bh]) place_b(bh++);
+      uint32_t take = nr;
+      if (bh < bt) take = min(nr, (ready[bh] - pos + per_row - 1u) / per_row);
+      place(make_seg(f, take, pos_lo, upr, NTA, 0));
+      f += take;
+      nr -= take;
+    }
+  };
+  // small top-k units first: their settles are the longest
+  place_rows((uint32_t)nD, (uint32_t)nT, 0, k1);
+  for (int i = 0; i < nw; ++i) {
+    const uint32_t f = (uint32_t)(i * Rw), nr = (uint32_t)min(Rw, nD - i * Rw);
+    if (k > 0) place_rows(f, nr, 0, k);
+    place_rows(f, nr, k, 1);
+    if (k > 0) ready[bt++] = pos + b_delay;
+  }
+  place_rows((uint32_t)(nD + nT + nX), (uint32_t)nG, 0, k1);
+  while (bh < bt) place_b(bh++);
+  uint32_t tasks = 0;
+  for (int i = 0; i < n; ++i) {
+    S.tstart[i] = tasks;
+    tasks += sg[i].nrows * ((sg[i].packed >> 21) & 31u);
+  }
+  S.nseg = n;
+  S.ntasks = tasks;
+}
+
+// Item t of the sequence.
 template <bool kBF16>
-__device__ __forceinline__ Item map_item(const Args& A, const Plan& P, int pass, uint32_t t, uint32_t n_items) {
+__device__ __noinline__ Item map_item(const Args& A, Plan P, uint32_t t) {
   using G = Geo<kBF16>;
   Item it;
   it.kind = 0;
-  it.t = t;
-  if (t >= n_items) return it;
-  // a unit's tiles are taken in a rotated order (by the unit's index), so
-  // that the CTAs taking items at a fixed stride do not all get the same
-  // tile of every unit (the last tile of a unit is the partial one)
-  if (pass == 1) {
-    const uint32_t j = t / (uint32_t)P.NTA;
-    it.c = (int)((t - j * (uint32_t)P.NTA + j) % (uint32_t)P.NTA);
-    const uint32_t ri = j / (uint32_t)(A.k + 1);
-    it.pos = (int)(j - ri * (uint32_t)(A.k + 1));
-    it.row = a_row(P, (int)ri);
-    it.kind = 1;
-    it.reread = (int)ri >= P.nT + P.nG ? 1 : 0;   // unfiltered: the B tiles or the bonus draw read it again
-    it.n = min(G::EA, A.V - it.c * G::EA);
-  } else {
-    const uint32_t j = t / (uint32_t)P.NTB;
-    it.c = (int)((t - j * (uint32_t)P.NTB + j) % (uint32_t)P.NTB);
-    const uint32_t ri = j / (uint32_t)A.k;
-    it.pos = (int)(j - ri * (uint32_t)A.k);
-    it.row = (int)P.order[ri];
-    it.kind = 2;
-    it.reread = 0;
-    it.n = min(G::EB, A.V - it.c * G::EB);
+  // the last segment whose start is <= t
+  int lo = 0, hi = P.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.seg[mid].start <= t) lo = mid;
+    else hi = mid - 1;
   }
+  const Seg s = P.seg[lo];
+  it.t = t;
+  if (P.nseg == 0 || t < s.start || t - s.start >= seg_items(s)) return it;
+  const uint32_t tiles = s.packed & 0xffffu, pos_lo = (s.packed >> 16) & 31u, upr = (s.packed >> 21) & 31u;
+  const int kind = (int)((s.packed >> 26) & 1u);
+  const uint32_t off = t - s.start;
+  const uint32_t j = off / tiles;
+  // a unit's tiles are taken in a rotated order (by the unit's index), so
+  // that CTAs taking items at a fixed stride do not all get the same tile of
+  // every unit (the last tile of a unit is the partial one)
+  it.c = (int)((off - j * tiles + j) % tiles);
+  const uint32_t ri = j / upr;
+  it.row = (int)P.order[s.first + ri];
+  it.pos = (int)(pos_lo + (j - ri * upr));
   it.u = it.row * (A.k + 1) + it.pos;
+  it.kind = kind == 0 ? 1 : 2;
+  it.ntiles = (int)tiles;
+  // logits of an unfiltered unit are read again: by its B tiles (drafted
+  // positions) or by its draw's level-2 race (bonus position)
+  it.reread = (kind == 0 && plan_cfg(A, P, it.row).type == UT_DENSE) ? 1 : 0;
+  it.n = it.kind == 1 ? min(G::EA, A.V - it.c * G::EA) : min(G::EB, A.V - it.c * G::EB);
   return it;
 }
 
@@ -835,64 +929,80 @@ __device__ __noinline__ void b_tile(const Args& A, uint32_t tag, Item it, RowCfg
   __syncwarp();
 }
 
-// A stream warp in one pass (1: A tiles, 2: B tiles).  Item t of the pass
-// belongs to CTA t mod n_ctas; a CTA's warps take its items j = 0, 1, ...
-// (item blockIdx + n_ctas j): the first two by the warp's index, later ones
-// from a shared-memory counter (no global counter for all SMs to contend
-// on).  Of the warp's two buffers one is filled by the copy engine while the
-// other is reduced; the barriers' parities carry over from pass to pass.
+struct Bufs {
+  unsigned char* a;
+  unsigned char* b;
+  unsigned long long* ba;
+  unsigned long long* bb;
+  uint32_t pa, pb;
+  __device__ __forceinline__ void rotate() {
+    unsigned char* tb = a;
+    a = b;
+    b = tb;
+    unsigned long long* tr = ba;
+    ba = bb;
+    bb = tr;
+    const uint32_t tp = pa;
+    pa = pb;
+    pb = tp;
+  }
+};
+
+// A stream warp: items of the sequence, the first two by its index, later
+// ones from one counter (the next ticket is in flight while a tile is
+// reduced).  After a tile's record, one is added to the unit's tile count.
 template <bool kBF16>
-__device__ __noinline__ void stream_pass(const Args& A, Plan P0, VShm& S, uint32_t tag, int w, uint32_t gw,
-                                         int pass, uint32_t n_items, uint32_t* ticket) {
+__device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32_t tag, int sw, uint32_t srank,
+                                         uint32_t n_stream) {
   const int lane = threadIdx.x & 31;
   const Plan P = P0;
-  unsigned char* bufa = S.s.buf[w][0];
-  unsigned char* bufb = S.s.buf[w][1];
-  unsigned long long* bara = &S.bar[w][0];
-  unsigned long long* barb = &S.bar[w][1];
-  uint32_t pa = S.par[w][0], pb = S.par[w][1];
-  bool swapped = false;
-  bool broken = S.broken[w] != 0u;
-  const uint32_t nc = (uint32_t)A.n_ctas, cb = blockIdx.x;
-  Item ia = map_item<kBF16>(A, P, pass, cb + nc * (uint32_t)w, n_items);
-  Item ib = map_item<kBF16>(A, P, pass, cb + nc * (uint32_t)(kNW + w), n_items);
+  Bufs B;
+  B.a = S.s.buf[sw][0];
+  B.b = S.s.buf[sw][1];
+  B.ba = &S.bar[sw][0];
+  B.bb = &S.bar[sw][1];
+  B.pa = 0u;
+  B.pb = 0u;
+  if (lane == 0) {
+    mbar_init(B.ba, 1);    // issue() orders the inits before the copies (fence.proxy.async)
+    mbar_init(B.bb, 1);
+  }
+  __syncwarp();
+  const uint32_t gs = (uint32_t)sw * n_stream + srank;   // the warp's index over the stream warps
+  Item ia = map_item<kBF16>(A, P, srank + n_stream * (uint32_t)sw);
+  Item ib = map_item<kBF16>(A, P, srank + n_stream * (uint32_t)(kNW + sw));
   // the first buffer alone: the first data arrives behind half the bytes a
   // second copy per warp would put in flight; the second copy is posted as
   // soon as it has (below)
-  if (lane == 0 && !broken) issue<kBF16>(A, ia, bufa, bara);
+  if (lane == 0) issue<kBF16>(A, ia, B.a, B.ba);
+  bool broken = false;
   bool first = true;
   while (ia.kind != 0) {
     uint32_t tn = 0;
     const bool take = ib.kind != 0 && !broken;   // warp-uniform
-    if (lane == 0 && take) tn = cb + nc * (2u * kNW + atomicAdd(ticket, 1u));
+    if (lane == 0 && take) tn = srank + n_stream * (2u * kNW + atomicAdd(&S.ticket, 1u));
     const RowCfg cfg = plan_cfg(A, P, ia.row);
     u64 sw8[kStateWords];
     if (ia.kind == 2) state_load(A, ia.u, sw8);     // in flight during the copy wait
-    const bool ok = !broken && wait_buffer(A, bara, pa);
+    const bool ok = !broken && wait_buffer(A, B.ba, B.pa);
     if (first) {
-      if (lane == 0 && ok && pass == 1) TL(TL_FIRST_DATA, (int)gw, 2048);
-      if (lane == 0 && ok) issue<kBF16>(A, ib, bufb, barb);
+      if (lane == 0 && ok) TL(TL_FIRST_DATA, (int)gs, 2048);
+      if (lane == 0 && ok) issue<kBF16>(A, ib, B.b, B.bb);
       first = false;
     }
-#ifdef SPEC_TIMELINE
-    if (lane == 0 && pass == 1) {
-      TL(TL_ISTART, (int)ia.t, 16384);
-      if (ia.t < 16384u) g_tl[TL_IWARP + ia.t] = gw + 1u;
-    }
-#endif
     if (!ok) {
       // the buffer's copy never completed: mark this tile and stop taking new ones
       broken = true;
       timeout_record(A, tag, ia, cfg.type == UT_TOPK);
     } else {
-      pa ^= 1u;
+      B.pa ^= 1u;
       if (!A.vec_logits || (ia.kind == 2 && !A.vec_q) || ia.n != (ia.kind == 1 ? Geo<kBF16>::EA : Geo<kBF16>::EB))
-        fill_tail<kBF16>(A, ia, bufa);
+        fill_tail<kBF16>(A, ia, B.a);
       if (ia.kind == 1) {
-        if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, bufa, S.s.stage[w]);
-        else a_stats<kBF16>(A, tag, ia, cfg, bufa);
+        if (cfg.type == UT_TOPK) a_list<kBF16>(A, tag, ia, B.a, S.s.stage[sw]);
+        else a_stats<kBF16>(A, tag, ia, cfg, B.a);
       } else {
-        // the unit state, published before this pass (bounded wait all the same)
+        // the unit state (bounded wait: a settle warp publishes it)
         long long spins = 0;
         bool st_ok = true;
         while (!__all_sync(kFull, state_ok(sw8, tag))) {
@@ -908,116 +1018,107 @@ __device__ __noinline__ void stream_pass(const Args& A, Plan P0, VShm& S, uint32
           timeout_record(A, tag, ia, false);
         } else {
           const UnitState st = state_of(sw8);
-          if (!st.invalid) b_tile<kBF16>(A, tag, ia, cfg, st, bufa);
+          if (!st.invalid) b_tile<kBF16>(A, tag, ia, cfg, st, B.a);
         }
       }
     }
     __syncwarp();
-    if (lane == 0 && pass == 1) TL(TL_ITEM, (int)ia.t, 16384);
+    if (lane == 0) {
+      TL(TL_ITEM, (int)ia.t, 16384);
+      atomicAdd(&A.ucnt[(ia.kind == 2 ? A.U : 0) + ia.u], 1u);   // result unused: a reduction
+    }
     tn = __shfl_sync(kFull, tn, 0);
     Item in;
     in.kind = 0;
-    if (take) in = map_item<kBF16>(A, P, pass, tn, n_items);   // after a failed copy: mapped, marked, not copied
-    if (lane == 0 && !broken) issue<kBF16>(A, in, bufa, bara);
+    if (take) in = map_item<kBF16>(A, P, tn);   // after a failed copy: mapped, marked, not copied
+    if (lane == 0 && !broken) issue<kBF16>(A, in, B.a, B.ba);
     ia = ib;
     ib = in;
-    unsigned char* tb = bufa;
-    bufa = bufb;
-    bufb = tb;
-    unsigned long long* tr = bara;
-    bara = barb;
-    barb = tr;
-    const uint32_t tp = pa;
-    pa = pb;
-    pb = tp;
-    swapped = !swapped;
+    B.rotate();
   }
   if (lane == 0) {
-    S.par[w][0] = swapped ? pb : pa;
-    S.par[w][1] = swapped ? pa : pb;
-    S.broken[w] = broken ? 1u : 0u;
-    if (pass == 1) TL(TL_STREAM_END, (int)gw, 2048);
+    TL(TL_STREAM_END, (int)gs, 2048);
+    S.broken[sw] = broken ? 1u : 0u;
   }
   __syncwarp();
 }
 
-// The settle pass after the A pass: small top-k units by whole CTAs (unit
-// i by CTA i mod n_ctas), the other units by single warps from a counter.
-template <bool kBF16>
-__device__ __noinline__ void settle_pass_a(const Args& A, Plan P, VShm& S, uint32_t tag) {
-  const int lane = threadIdx.x & 31;
-  const int k1 = A.k + 1;
-  const int nTU = P.nT * k1;
-  for (int i = (int)blockIdx.x; i < nTU; i += A.n_ctas) {
-    __syncthreads();   // warp 0 has finished the CTA's previous unit
-    const int ri = i / k1, pos = i - (i / k1) * k1;
-    const int row = a_row(P, ri);
-    const int u = row * k1 + pos;
-    const RowCfg cfg = plan_cfg(A, P, row);
-    if (threadIdx.x == 0) TL(TL_SA_START, u, 2048);
-    topk_settle_cta<kBF16>(A, tag, S.tkc, u, row, pos, cfg);
-    if (threadIdx.x == 0) TL(TL_SA_END, u, 2048);
+// Settle task t: the unit and kind (settle-A after its A tiles, settle-B
+// after its B tiles) and the tile count to wait for.
+struct Task {
+  int u, row, pos, ntiles, kind;   // kind 1: A, 2: B
+};
+__device__ __forceinline__ Task map_task(const Args& A, Plan P, const VShm& S, uint32_t t) {
+  int lo = 0, hi = P.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (S.tstart[mid] <= t) lo = mid;
+    else hi = mid - 1;
   }
-  const uint32_t nu = (uint32_t)a_units(A, P);
-  while (true) {
-    uint32_t j = 0;
-    if (lane == 0) j = atomicAdd(&A.ws->settle_next, 1u);
-    j = __shfl_sync(kFull, j, 0) + (uint32_t)nTU;
-    if (j >= nu) break;
-    const uint32_t ri = j / (uint32_t)k1;
-    const int pos = (int)(j - ri * (uint32_t)k1);
-    const int row = a_row(P, (int)ri);
-    const int u = row * k1 + pos;
-    const RowCfg cfg = plan_cfg(A, P, row);
-    if (lane == 0) TL(TL_SA_START, u, 2048);
-    const Pre pr = load_pre<kBF16>(A, u, row, pos);
-    fin_stats<kBF16>(A, tag, u, row, pos, cfg, pr);
-    if (lane == 0) TL(TL_SA_END, u, 2048);
-    __syncwarp();
-  }
+  const Seg s = P.seg[lo];
+  const uint32_t upr = (s.packed >> 21) & 31u, pos_lo = (s.packed >> 16) & 31u;
+  const uint32_t j = t - S.tstart[lo];
+  const uint32_t ri = j / upr;
+  Task k;
+  k.row = (int)P.order[s.first + ri];
+  k.pos = (int)(pos_lo + (j - ri * upr));
+  k.u = k.row * (A.k + 1) + k.pos;
+  k.ntiles = (int)(s.packed & 0xffffu);
+  k.kind = ((s.packed >> 26) & 1u) ? 2 : 1;
+  return k;
 }
 
-// The settle pass after the B pass: one warp per drafted unfiltered unit.
+// A settle warp: tasks g, g + nst, ... in sequence order; each waits for its
+// unit's tile count, settles the unit and clears the count.
 template <bool kBF16>
-__device__ __noinline__ void settle_pass_b(const Args& A, Plan P, uint32_t tag, uint32_t gw, uint32_t nwarps) {
+__device__ __noinline__ void settle_loop(const Args& A, Plan P, VShm& S, uint32_t tag, int w, uint32_t g,
+                                         uint32_t nst) {
   const int lane = threadIdx.x & 31;
-  const uint32_t nu = (uint32_t)b_units(A, P);
-  for (uint32_t j = gw; j < nu; j += nwarps) {
-    const uint32_t ri = j / (uint32_t)A.k;
-    const int pos = (int)(j - ri * (uint32_t)A.k);
-    const int row = (int)P.order[ri];
-    const int u = row * (A.k + 1) + pos;
-    const RowCfg cfg = plan_cfg(A, P, row);
-    if (lane == 0) TL(TL_SB_START, u, 2048);
+  TopkScratch& TS = S.tk[w];
+  for (uint32_t t = g; t < S.ntasks; t += nst) {
+    const Task k = map_task(A, P, S, t);
+    uint32_t* cnt = &A.ucnt[(k.kind == 2 ? A.U : 0) + k.u];
+    // what the settle needs besides the records is loaded while the tiles
+    // are still being reduced: the draft and its logit and q (settle-A), or
+    // the unit's published state (settle-B)
+    Pre pr;
     StateWords sw8;
-    state_load(A, u, sw8.w);
-    fin_b<kBF16>(A, tag, u, row, pos, cfg, sw8);
-    if (lane == 0) TL(TL_SB_END, u, 2048);
+    if (k.kind == 2) {
+      state_load(A, k.u, sw8.w);
+    } else {
+      pr = load_pre<kBF16>(A, k.u, k.row, k.pos);
+    }
+    bool ready = true;
+    if (lane == 0) {
+      long long spins = 0;
+      while (load_relaxed(cnt) != (uint32_t)k.ntiles) {
+        if (++spins > 16ll * kSpinLimit) {
+          atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+          ready = false;
+          break;
+        }
+        __nanosleep(spins > 64 ? 128 : 32);
+      }
+    }
+    ready = __shfl_sync(kFull, ready ? 1 : 0, 0) != 0;
+    const RowCfg cfg = plan_cfg(A, P, k.row);
+    if (lane == 0) TL(k.kind == 2 ? TL_SB_START : TL_SA_START, k.u, 2048);
+    if (!ready) {
+      commit_record(A, tag, k.u, k.row, empty_record(SPEC_F_TIMEOUT));   // the records' polls would give up too
+    } else if (k.kind == 2) {
+      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg, sw8);
+    } else if (cfg.type == UT_TOPK) {
+      topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg, pr);
+    } else {
+      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg, pr);
+    }
+    if (lane == 0) {
+      TL(k.kind == 2 ? TL_SB_END : TL_SA_END, k.u, 2048);
+      *cnt = 0u;   // leave the workspace clean for the next call
+    }
     __syncwarp();
   }
-}
-
-// Every CTA arrives before any leaves (the launch is cooperative, so all are
-// resident).  The count only grows within a call: barrier i waits for
-// i x n_ctas arrivals.  Bounded: a wait that gives up sets ERR_BARRIER and
-// the CTA goes on (the record polls after it then give up too, and the rows
-// come back with SPEC_F_TIMEOUT).
-__device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&A.ws->bar, 1u);
-    long long spins = 0;
-    while (load_acquire(&A.ws->bar) < target) {
-      if (++spins > 16ll * kSpinLimit) {
-        atomicOr(&A.ws->error, (uint32_t)ERR_BARRIER);
-        break;
-      }
-      __nanosleep(spins > 16 ? 128 : 16);
-    }
-    __threadfence();
-  }
-  __syncthreads();
+  if (lane == 0) TL(TL_SETTLE_END, (int)g, 256);
 }
 
 // General-path units, taken by the CTA's first kThreads threads.
@@ -1033,29 +1134,24 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
     csync();
     if (g >= nGU) break;
     const int row = (int)P.order[gbase + g / k1], pos = g % k1;
+    if (ctid() == 0) TL(TL_SA_START, row * k1 + pos, 2048);
     unit_general<kBF16>(A, S.gen, tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
+    if (ctid() == 0) TL(TL_SA_END, row * k1 + pos, 2048);
   }
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A) {
+__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A, uint32_t b_delay) {
   using G = Geo<kBF16>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     S.tag = next_tag(__ldcg(&A.ws->epoch));
     S.gtask = 0;
-    S.ticket[0] = 0u;
-    S.ticket[1] = 0u;
+    S.ticket = 0u;
   }
-  if (lane == 0) {
-    mbar_init(&S.bar[w][0], 1);    // issue() orders the inits before the copies (fence.proxy.async)
-    mbar_init(&S.bar[w][1], 1);
-    S.par[w][0] = 0u;
-    S.par[w][1] = 0u;
-    S.broken[w] = 0u;
-  }
+  if ((threadIdx.x & 31) == 0) S.broken[threadIdx.x >> 5] = 0u;
   Plan P;
   bool order_ok = true;
   if (!A.global_order) {
@@ -1092,23 +1188,23 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   const uint32_t tag = S.tag;
   P.NTA = ceil_div(A.V, G::EA);
   P.NTB = ceil_div(A.V, G::EB);
+  build_segments(A, S, P.nD, P.nT, P.nX, P.nG, P.NTA, P.NTB, b_delay);
   __syncthreads();
+  P.seg = S.seg;
+  P.nseg = S.nseg;
   if (threadIdx.x == 0) TL(TL_CTA_START, (int)blockIdx.x, 160);
-  // warp gw of nwarps: consecutive indices on different SMs
-  const uint32_t nwarps = (uint32_t)A.n_ctas * kNW;
-  const uint32_t gw = (uint32_t)w * (uint32_t)A.n_ctas + blockIdx.x;
-  const uint32_t nb = (uint32_t)b_units(A, P) * (uint32_t)P.NTB;
   if (order_ok) {
-    // A pass, then every unit's settle (the B pass's q into L2 meanwhile)
-    stream_pass<kBF16>(A, P, S, tag, w, gw, 1, (uint32_t)a_units(A, P) * (uint32_t)P.NTA, &S.ticket[0]);
-    grid_barrier(A, (uint32_t)A.n_ctas);
-    settle_pass_a<kBF16>(A, P, S, tag);
-    if (nb > 0) {
-      // B pass over the drafted unfiltered units, then their settles
-      grid_barrier(A, 2u * (uint32_t)A.n_ctas);
-      stream_pass<kBF16>(A, P, S, tag, w, gw, 2, nb, &S.ticket[1]);
-      grid_barrier(A, 3u * (uint32_t)A.n_ctas);
-      settle_pass_b<kBF16>(A, P, tag, gw, nwarps);
+    const int bx = (int)blockIdx.x;
+    const bool settle_cta = (bx % A.settle_stride) == 0 && bx / A.settle_stride < A.n_settle;
+    if (settle_cta) {
+      const uint32_t nst = (uint32_t)A.n_settle * kNW;
+      settle_loop<kBF16>(A, P, S, tag, w, (uint32_t)(bx / A.settle_stride) * kNW + (uint32_t)w, nst);
+    } else {
+      // stream CTA rank: blocks before this one, minus the settle CTAs among them
+      const int srank = bx - min(A.n_settle, bx / A.settle_stride + 1);
+      const int n_stream = A.n_ctas - A.n_settle;
+      // item t belongs to stream CTA t mod n_stream (consecutive items on different SMs)
+      stream_loop<kBF16>(A, P, S, tag, w, (uint32_t)srank, (uint32_t)n_stream);
     }
   }
   if (P.nX > 0 && order_ok) {
@@ -1119,7 +1215,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   if (A.fc.on && order_ok) {
     // the fused commit: every warp copies rows as they are finalized (not
     // after a copy wait that gave up: that copy may still land in a buffer)
-    const bool copy_failed = (__shfl_sync(kFull, __ldcg(&A.ws->error), 0) & (uint32_t)ERR_COPY_WAIT) != 0u;
+    const bool copy_failed = (__shfl_sync(kFull, __ldcg(&A.ws->error), 0) & (uint32_t)ERR_COPY_WAIT) != 0u ||
+                             S.broken[w] != 0u;
     if (!copy_failed) commit_phase(A, tag, S.s.buf[w][0], S.s.buf[w][1], S.cbar[w]);
     __syncthreads();
   }
@@ -1130,8 +1227,6 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     if (d == (uint32_t)A.n_ctas - 1u) {
       __threadfence();
       A.ws->gnext = 0u;
-      A.ws->bar = 0u;
-      A.ws->settle_next = 0u;
       A.ws->commit_next = 0u;
       A.ws->done_count = 0u;
       A.ws->ctas_done = 0u;
@@ -1146,6 +1241,10 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
+// Items of A tiles between the end of an unfiltered wave's A tiles and its
+// B tiles: the wave's settles (a few microseconds) finish meanwhile.
+constexpr uint32_t kBDelayItems = 1600;
+
 template <bool kBF16>
 int launch_verify(const Args& A0, cudaStream_t stream) {
   static std::mutex mu;
@@ -1174,7 +1273,10 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   }
   Args A = A0;
   A.n_ctas = n;
+  A.n_settle = n >= 2 * kSettleEvery ? n / kSettleEvery : 1;
+  A.settle_stride = n / A.n_settle;
   A.global_order = A.B > kOrderSmem ? 1 : 0;
+  uint32_t b_delay = kBDelayItems;
   // cooperative launch: every CTA is resident, so every wait between warps ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -1187,7 +1289,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, A) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, A, b_delay) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_E_CUDA;
   }

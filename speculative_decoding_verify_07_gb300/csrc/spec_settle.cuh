@@ -623,7 +623,7 @@ static __device__ __noinline__ void warp_sort_desc(u64* s, int n) {
 // ---------------------------------------------------------------------------
 // Small top-k, one warp.
 // ---------------------------------------------------------------------------
-constexpr int kSel = 256;                  // candidates held for the sort
+constexpr int kSel = 128;                  // candidates held for the sort (>= kTopkSmall)
 
 // Scratch of one settle warp.
 struct TopkScratch {
@@ -742,16 +742,9 @@ __device__ __noinline__ int select_k_row(const Args& A, TopkScratch& S, size_t l
 
 static_assert(kList == 8, "list slot q mod 8 of tile q / 8");
 
-// CTA scratch of a small top-k settle.
-struct TopkCtaShm {
-  TopkScratch ts;                  // the lists (tile-major), the selection, its q
-  u64 fk[kMaxListCand];            // the listed entries at or above tau
-  u64 wmax[kCtaWarps];             // per-warp reductions
-  uint32_t wcnt[kCtaWarps];
-  uint32_t tau;                    // a value key at or below the K-th listed entry
-  uint32_t nf;                     // entries in fk
-};
-constexpr int kCandPerThread = (kMaxListCand + kCtaWarps * 32 - 1) / (kCtaWarps * 32);
+static_assert(kSel >= kTopkSmall, "the selection holds the K largest");
+static_assert(sizeof(TopkScratch) <= kSlot, "top-k settle scratch exceeds a stream buffer");
+static_assert(kTopkSmall * 8 <= 256 * 4, "the sorted keys fit the histogram area");
 
 // The exact top-K of a small top-k unit when a tile may hold more top-K
 // entries than it listed (a full list ending above kappa, or one marked
@@ -1019,23 +1012,91 @@ __device__ __noinline__ void topk_tail(const Args& A, uint32_t tag, TopkScratch&
   commit_record(A, tag, u, row, rec);
 }
 
-// Settle a small top-k unit with the whole CTA (every thread calls it).
-//   1. The tiles' lists into shared memory (candidate q: tile q / 8, slot
-//      q mod 8), with q at every listed entry.
-//   2. The listed entries at or above tau, a value that ceil(K / 8) full
-//      lists end at or above (so at or below the K-th listed entry); each
-//      one's rank among them by counting; the K first go to their places,
-//      which sorts them.  kappa is the K-th.  A tile whose list is full and ends above kappa,
-//      or is marked partial, may hold more top-K entries: then warp 0 re-reads
-//      such tiles (topk_rescan).
-//   3. Warp 0: top-p, alpha, the accept test and the draw (topk_tail).
+// The value keys of the listed entries, CR per lane (candidate 32 r + lane
+// in round r; 0 for an empty slot), held in registers for the bisection.
+template <int CR>
+struct KeyRounds {
+  uint32_t k[CR];
+};
+template <int CR>
+__device__ __forceinline__ uint32_t count_key_ge(const KeyRounds<CR>& K, uint32_t t) {
+  uint32_t n = 0;
+#pragma unroll
+  for (int r = 0; r < CR; ++r) n += K.k[r] >= t ? 1u : 0u;
+  return __reduce_add_sync(kSettleFull, n);
+}
+
+// The K-th largest listed entry in the total order (0 when fewer than K are
+// listed), by bisection on the value key within [lo, hi] (lo at or below it,
+// hi the largest), then on the index among the entries at that key.
+template <bool kBF16, int CR>
+__device__ __noinline__ u64 kth_listed(const u64* cand, int NL, uint32_t K, uint32_t lo, uint32_t hi) {
+  const int lane = threadIdx.x & 31;
+  KeyRounds<CR> R;
+#pragma unroll
+  for (int r = 0; r < CR; ++r) {
+    const int q = 32 * r + lane;
+    R.k[r] = q < NL ? (uint32_t)(cand[q] >> 32) : 0u;
+  }
+  if (count_key_ge(R, 1u) < K) return 0ull;
+  uint32_t tkey;
+  if (kBF16) {
+    // bf16 keys are fixed by their top 16 bits
+    uint32_t l = lo >> 16, h = hi >> 16;
+    while (l < h) {
+      const uint32_t mid = l + ((h - l + 1u) >> 1);
+      if (count_key_ge(R, max(mid << 16, 1u)) >= K) l = mid;
+      else h = mid - 1u;
+    }
+    tkey = full_key<true>(l);
+  } else {
+    uint32_t l = max(lo, 1u), h = hi;
+    while (l < h) {
+      const uint32_t mid = l + (uint32_t)(((u64)h - l + 1ull) >> 1);
+      if (count_key_ge(R, mid) >= K) l = mid;
+      else h = mid - 1u;
+    }
+    tkey = l;
+  }
+  const uint32_t n_gt = tkey == 0xffffffffu ? 0u : count_key_ge(R, tkey + 1u);
+  const uint32_t need = K - n_gt;   // entries at the key, smallest indices first
+  const uint32_t n_eq = count_key_ge(R, tkey) - n_gt;
+  uint32_t low = 0xffffffffu;
+  for (int q = lane; q < NL; q += 32)
+    if ((uint32_t)(cand[q] >> 32) == tkey) low = min(low, (uint32_t)cand[q]);
+  low = __reduce_min_sync(kSettleFull, low);
+  if (n_eq == need) return ((u64)tkey << 32) | low;   // every entry at the key is kept
+  // the need-th largest low word (0xffffffff - index) among the entries at tkey
+  uint32_t l = low, h = 0xffffffffu;
+  while (l < h) {
+    const uint32_t mid = l + (uint32_t)(((u64)h - l + 1ull) >> 1);
+    uint32_t n = 0;
+    for (int q = lane; q < NL; q += 32)
+      n += ((uint32_t)(cand[q] >> 32) == tkey && (uint32_t)cand[q] >= mid) ? 1u : 0u;
+    if (__reduce_add_sync(kSettleFull, n) >= need) l = mid;
+    else h = mid - 1u;
+  }
+  return ((u64)tkey << 32) | l;
+}
+
+// Settle a small top-k unit with one warp; S is scratch in shared memory
+// (one of the warp's stream buffers).
+//   1. The tiles' lists into S.cand (candidate q: tile q / 8, slot q mod 8),
+//      loaded 8 candidates a lane at a time.
+//   2. tau: the ceil(K / 8)-th largest value key among the last entries of
+//      full lists -- that many lists hold 8 entries at or above it, so the
+//      K-th listed entry is at or above it.  The listed entries at or above
+//      tau (a few more than K) are gathered with their q, each one's rank
+//      among them is counted, and the K first go to their places, which
+//      sorts them; kappa is the K-th.  A tile whose list is full and ends
+//      above kappa, or is marked partial, may hold more top-K entries: then
+//      such tiles are re-read (topk_rescan).
+//   3. Top-p, alpha, the accept test and the draw (topk_tail).
 template <bool kBF16>
-__device__ __noinline__ void topk_settle_cta(const Args& A, uint32_t tag, TopkCtaShm& C, int u, int row, int pos,
-                                             RowCfg cfg) {
+__device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratch& S, int u, int row, int pos,
+                                         RowCfg cfg, Pre pr) {
   using G = Geo<kBF16>;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int nth = kCtaWarps * 32;
-  TopkScratch& S = C.ts;
+  const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
   const int NT = ceil_div(A.V, G::EA);
   const int NL = NT * kList;
@@ -1043,60 +1104,72 @@ __device__ __noinline__ void topk_settle_cta(const Args& A, uint32_t tag, TopkCt
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const int K = cfg.K;
-  Pre pr;
-  if (w == 0) pr = load_pre<kBF16>(A, u, row, pos);   // in flight meanwhile
 
   // 1. the lists
   uint32_t allf = 0;
   bool timed_out = false;
   {
     long long spins = 0;
-    while (true) {
-      bool ok = true;
+    bool ok;
+    do {
+      ok = true;
       uint32_t fl = 0;
-      for (int q = tid; q < NL; q += nth) {
-        const u64* r = R + (size_t)(q >> 3) * kRecWords + 2 * (q & 7);
-        const u64 wk = __ldcg(r), wi = __ldcg(r + 1);
-        ok = ok && tag_ok(wk, tag) && tag_ok(wi, tag);
-        const uint32_t key = (uint32_t)wk, iw = (uint32_t)wi;
-        fl |= iw & (kListNaN | kListPartial | kListTimeout);
-        S.cand[q] = key ? key64(key, (uint32_t)((q >> 3) * G::EA) + (iw & kListIdx)) : 0ull;
-        if ((q & 7) == 0) S.cflag[q >> 3] = (uint8_t)((iw & kListPartial) ? 2u : 0u);
+#pragma unroll 1
+      for (int q0 = 0; q0 < NL; q0 += 32 * 8) {
+        u64 wk[8], wi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = q0 + 32 * i + lane;
+          wk[i] = 0ull;
+          wi[i] = 0ull;
+          if (q < NL) {
+            const u64* r = R + (size_t)(q >> 3) * kRecWords + 2 * (q & 7);
+            wk[i] = __ldcg(r);
+            wi[i] = __ldcg(r + 1);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = q0 + 32 * i + lane;
+          if (q < NL) {
+            ok = ok && tag_ok(wk[i], tag) && tag_ok(wi[i], tag);
+            const uint32_t key = (uint32_t)wk[i], iw = (uint32_t)wi[i];
+            fl |= iw & (kListNaN | kListPartial | kListTimeout);
+            S.cand[q] = key ? key64(key, (uint32_t)((q >> 3) * G::EA) + (iw & kListIdx)) : 0ull;
+            if ((q & 7) == 0) S.cflag[q >> 3] = (uint8_t)((iw & kListPartial) ? 2u : 0u);
+          }
+        }
       }
-      const int all_ok = __syncthreads_and(ok ? 1 : 0);
-      allf = (uint32_t)__syncthreads_or((int)fl);
-      if (all_ok) break;
-      if (++spins > kSpinLimit) {
-        if (tid == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
-        timed_out = true;
-        break;
-      }
-      __nanosleep(64);
-    }
+      allf = __reduce_or_sync(kSettleFull, fl);
+    } while (poll_again(A, ok, spins, &timed_out));
   }
+  __syncwarp();
   TLP(u, 1);
   if ((allf & kListTimeout) || timed_out) {
-    if (w == 0) commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
     return;
   }
-  // the maximum and the count of listed entries; tau (warp 0): the
-  // ceil(K / 8)-th largest value key among the last entries of full lists --
-  // that many lists hold 8 entries at or above it, so the K-th listed entry
-  // is at or above it
+  // the maximum and the count of listed entries
   u64 top = 0ull;
   uint32_t cnt = 0;
-  for (int q = tid; q < NL; q += nth) {
+  for (int q = lane; q < NL; q += 32) {
     const u64 k = S.cand[q];
     top = k > top ? k : top;
     cnt += k ? 1u : 0u;
   }
   top = warp_max_u64(top);
   cnt = __reduce_add_sync(kSettleFull, cnt);
-  if (lane == 0) {
-    C.wmax[w] = top;
-    C.wcnt[w] = cnt;
+  const float m = from_okey((uint32_t)(top >> 32));
+  if ((allf & kListNaN) || top == 0ull || !(m > -INFINITY) || !(m < INFINITY)) {
+    commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
+    return;
   }
-  if (w == 0) {
+  const int am = (int)key64_idx(top);
+
+  // 2. tau (a lower bound of the K-th listed value key), kappa by bisection
+  // above it, the K entries at or above kappa (in S.sel) with their q, ranked
+  uint32_t tau = 1u;
+  {
     uint32_t v[3];
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -1104,13 +1177,12 @@ __device__ __noinline__ void topk_settle_cta(const Args& A, uint32_t tag, TopkCt
       v[i] = ch < NT ? (uint32_t)(S.cand[ch * kList + kList - 1] >> 32) : 0u;
     }
     static_assert(kMaxListCand / kList <= 96, "three list ends per lane");
-    uint32_t tau = 0u;
     const int need = (K + kList - 1) / kList;
 #pragma unroll 1
     for (int i = 0; i < need; ++i) {
       const uint32_t lm = max(v[0], max(v[1], v[2]));
       const uint32_t M = __reduce_max_sync(kSettleFull, lm);
-      tau = M;
+      tau = max(M, 1u);
       if (M == 0u) break;
       // one occurrence leaves: the first lane holding it, its first slot
       const int src = __ffs(__ballot_sync(kSettleFull, lm == M)) - 1;
@@ -1120,73 +1192,67 @@ __device__ __noinline__ void topk_settle_cta(const Args& A, uint32_t tag, TopkCt
         else v[2] = 0u;
       }
     }
-    if (lane == 0) {
-      C.tau = tau;
-      C.nf = 0u;
-    }
   }
-  __syncthreads();
-  top = 0ull;
-  cnt = 0;
-  for (int i = 0; i < kCtaWarps; ++i) {
-    top = C.wmax[i] > top ? C.wmax[i] : top;
-    cnt += C.wcnt[i];
-  }
-  const float m = from_okey((uint32_t)(top >> 32));
-  if ((allf & kListNaN) || top == 0ull || !(m > -INFINITY) || !(m < INFINITY)) {
-    if (w == 0) commit_record(A, tag, u, row, empty_record(SPEC_F_NAN));
-    return;
-  }
-  const int am = (int)key64_idx(top);
-
-  // 2. the listed entries at or above tau (a few more than K), with their q
-  // (loads in flight during the ranking); each one's rank among them by
-  // counting; the K first go to their places
-  const uint32_t tau = C.tau;
-  u64 mk[kCandPerThread];
-  float mq[kCandPerThread];
-#pragma unroll
-  for (int i = 0; i < kCandPerThread; ++i) {
-    const int q = tid + nth * i;
-    mk[i] = 0ull;
-    mq[i] = 0.f;
-    if (q < NL) {
-      const u64 k = S.cand[q];
-      if (k != 0ull && (uint32_t)(k >> 32) >= tau) {
-        mk[i] = k;
-        C.fk[atomicAdd(&C.nf, 1u)] = k;
-        const uint32_t v = key64_idx(k);
-        if (has_q && v < (uint32_t)A.V) mq[i] = __ldcg(A.q + qrow + v);
-      }
-    }
-  }
-  __syncthreads();
-  const int nf = (int)C.nf;
-#pragma unroll
-  for (int i = 0; i < kCandPerThread; ++i) {
-    if (mk[i] == 0ull) continue;
-    uint32_t rk = 0;
-#pragma unroll 4
-    for (int j = 0; j < nf; ++j) rk += C.fk[j] > mk[i] ? 1u : 0u;
-    if (rk < (uint32_t)K) {
-      S.sel[rk] = mk[i];
-      S.qsel[rk] = mq[i];
-    }
-  }
-  __syncthreads();
+  // candidates a lane holds: a small top-k unit has at most kMaxListCand / kList
+  // tiles of fp32 logits, half as many of bf16
+  constexpr int CR = (kBF16 ? kMaxListCand / 2 : kMaxListCand) / 32;
+  static_assert(Geo<true>::EA == 2 * Geo<false>::EA, "bf16 tiles hold twice the entries");
+  const u64 kappa = kth_listed<kBF16, CR>(S.cand, NL, (uint32_t)K, tau, (uint32_t)(top >> 32));
   const int n_k = (int)min(cnt, (uint32_t)K);
-  const u64 kappa = cnt >= (uint32_t)K ? S.sel[K - 1] : 0ull;
+  {
+    uint32_t n = 0;
+    for (int q0 = 0; q0 < NL; q0 += 32) {
+      const int q = q0 + lane;
+      const u64 k = q < NL ? S.cand[q] : 0ull;
+      const bool in = k != 0ull && k >= kappa;
+      const unsigned ball = __ballot_sync(kSettleFull, in);
+      const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
+      if (in && p < (uint32_t)kSel) S.sel[p] = k;
+      n += __popc(ball);
+    }
+  }
+  __syncwarp();
+  u64* sorted = reinterpret_cast<u64*>(S.hist);
+  {
+    // q of the gathered entries (in flight while they are ranked)
+    u64 mk[kSel / 32];
+    float mq[kSel / 32];
+    uint32_t rk[kSel / 32];
+#pragma unroll
+    for (int r = 0; r < kSel / 32; ++r) {
+      const int i = 32 * r + lane;
+      mk[r] = i < n_k ? S.sel[i] : 0ull;
+      const uint32_t v = key64_idx(mk[r]);
+      mq[r] = (has_q && mk[r] && v < (uint32_t)A.V) ? __ldcg(A.q + qrow + v) : 0.f;
+      rk[r] = 0u;
+    }
+#pragma unroll 2
+    for (int j = 0; j < n_k; ++j) {
+      const u64 kj = S.sel[j];
+#pragma unroll
+      for (int r = 0; r < kSel / 32; ++r) rk[r] += kj > mk[r] ? 1u : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kSel / 32; ++r)
+      if (mk[r]) {
+        sorted[rk[r]] = mk[r];
+        S.qsel[rk[r]] = mq[r];
+      }
+  }
+  __syncwarp();
   bool unsafe = false;
-  for (int ch = tid; ch < NT; ch += nth) {
+  for (int ch = lane; ch < NT; ch += 32) {
     const u64 last = S.cand[ch * kList + kList - 1];
     unsafe |= (S.cflag[ch] & 2u) != 0 || (last != 0ull && last > kappa);
   }
-  unsafe = __syncthreads_or(unsafe ? 1 : 0) != 0;
+  unsafe = __any_sync(kSettleFull, unsafe);
   TLP(u, 2);
-  if (w != 0) return;
-  int nk = n_k;
-  if (unsafe) nk = topk_rescan<kBF16>(A, S, NT, NL, kappa, K, lrow, qrow, has_q);
-  topk_tail<kBF16>(A, tag, S, u, row, pos, cfg, pr, S.sel, S.qsel, nk, m, am);
+  if (unsafe) {
+    const int nr = topk_rescan<kBF16>(A, S, NT, NL, kappa, K, lrow, qrow, has_q);
+    topk_tail<kBF16>(A, tag, S, u, row, pos, cfg, pr, S.sel, S.qsel, nr, m, am);
+  } else {
+    topk_tail<kBF16>(A, tag, S, u, row, pos, cfg, pr, sorted, S.qsel, n_k, m, am);
+  }
 }
 
 }  // namespace specv
