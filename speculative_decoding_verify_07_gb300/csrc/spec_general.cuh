@@ -25,6 +25,7 @@ struct alignas(16) GenShm {
   float wred[kWarps * 8];
   float bcf[8];
   int bci[16];
+  int ring_fail;
 };
 
 // One pass over a unit's row by the group: fn(g, v) for every group g of 8
@@ -52,6 +53,124 @@ __device__ __forceinline__ void gsweep(const Args& A, size_t lrow, int G, F fn) 
       const int g = g0 + b * kThreads;
       if (g < G) fn(g, v[b]);
     }
+  }
+}
+
+// The group's ring of shared-memory chunks: a pass over a row streams it
+// through kGRing slots of kGSlot bytes by bulk copies (several chunks in
+// flight), so that a pass is bound by the SM's bandwidth rather than by one
+// load's latency per group.
+constexpr int kGRing = 5;
+constexpr int kGSlot = 32768;
+struct GenRing {
+  unsigned char* buf;          // kGRing slots of kGSlot bytes
+  unsigned long long* bar;     // one mbarrier per slot
+  int* fail;                   // shared: set when a thread's chunk wait gave up
+  uint32_t seq;                // chunks taken so far (every thread keeps the same count)
+  bool ok;                     // false once a chunk's wait gave up (the same in every thread)
+};
+
+// Entries of a chunk: logits only, or logits and q (a multiple of 256, so
+// that a warp's 32 groups of a round are one race block).
+template <bool kBF16>
+__device__ __forceinline__ int chunk_entries(bool with_q) {
+  return with_q ? (kGSlot / ((kBF16 ? 2 : 4) + 4)) / kRaceBlock * kRaceBlock : kGSlot / (kBF16 ? 2 : 4);
+}
+
+// One pass over a unit's row (and its q row with with_q), through the ring:
+// fn(g, v, qv) for every group g of 8 entries, in rounds in which thread t
+// takes group t of each 256 (every thread calls fn in every round, so fn may
+// use warp collectives; groups past the row get -inf logits and zero q, and
+// the callers check g * 8 + i < V per entry).  Needs 16-byte aligned rows
+// (vec_logits, and vec_q with q).
+template <bool kBF16, typename F>
+__device__ __forceinline__ void csweep(const Args& A, GenRing& R, size_t lrow, size_t qrow, bool with_q, F fn) {
+  constexpr int es = kBF16 ? 2 : 4;
+  const int EC = chunk_entries<kBF16>(with_q);
+  const int nch = (A.V + EC - 1) / EC;
+  const uint32_t base = R.seq;
+  const unsigned char* lg = reinterpret_cast<const unsigned char*>(A.logits);
+  auto issue = [&](int c) {
+    const uint32_t sq = base + (uint32_t)c;
+    const int slot = (int)(sq % kGRing);
+    const int e0 = c * EC, n = min(EC, A.V - e0);
+    const uint32_t bl = (uint32_t)(n * es), bq = with_q ? (uint32_t)(n * 4) : 0u;
+    unsigned char* dst = R.buf + (size_t)slot * kGSlot;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&R.bar[slot], bl + bq);
+    bulk_g2s(dst, lg + (lrow + (size_t)e0) * es, bl, &R.bar[slot]);
+    if (bq) bulk_g2s(dst + (size_t)EC * es, A.q + qrow + e0, bq, &R.bar[slot]);
+  };
+  if (ctid() == 0)
+    for (int c = 0; c < min(nch, kGRing); ++c) issue(c);
+  const int GC = EC / 8;   // groups per chunk
+  for (int c = 0; c < nch; ++c) {
+    const uint32_t sq = base + (uint32_t)c;
+    const int slot = (int)(sq % kGRing);
+    const uint32_t par = (sq / kGRing) & 1u;
+    long long spins = 0;
+    bool got = R.ok;
+    while (got && !mbar_try_wait(&R.bar[slot], par)) {
+      if (++spins > kSpinLimit) {
+        atomicOr(&A.ws->error, (uint32_t)ERR_COPY_WAIT);
+        *R.fail = 1;
+        got = false;
+      }
+      if (spins > 64) __nanosleep(32);
+    }
+    const unsigned char* src = R.buf + (size_t)slot * kGSlot;
+    const float* qsrc = reinterpret_cast<const float*>(src + (size_t)EC * es);
+    const int n = min(EC, A.V - c * EC);
+    const int ng = (n + 7) / 8;
+    for (int r0 = 0; r0 < ng; r0 += kThreads) {
+      const int lgi = r0 + ctid();
+      const int g = lgi < ng ? c * GC + lgi : (1 << 27);   // past the row: g * 8 >= V
+      float v[8], qv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = -INFINITY;
+        qv[i] = 0.f;
+      }
+      if (lgi < ng && got) {
+        if (kBF16) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + (size_t)lgi * 16);
+          v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+          v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+        } else {
+          const float4 a = *reinterpret_cast<const float4*>(src + (size_t)lgi * 32);
+          const float4 b = *reinterpret_cast<const float4*>(src + (size_t)lgi * 32 + 16);
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+        if (with_q) {
+          const float4 a = *reinterpret_cast<const float4*>(qsrc + (size_t)lgi * 8);
+          const float4 b = *reinterpret_cast<const float4*>(qsrc + (size_t)lgi * 8 + 4);
+          qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w; qv[4] = b.x; qv[5] = b.y; qv[6] = b.z; qv[7] = b.w;
+        }
+        // entries past the row in its last group
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (g * 8 + i >= A.V) {
+            v[i] = -INFINITY;
+            qv[i] = 0.f;
+          }
+      }
+      fn(g, v, qv);
+    }
+    csync();   // every thread is done with the slot (and sees a failed wait)
+    R.ok = R.ok && *R.fail == 0;
+    if (ctid() == 0 && c + kGRing < nch && R.ok) issue(c + kGRing);
+  }
+  R.seq = base + (uint32_t)nch;
+}
+
+// A pass over the row: through the ring when the rows allow bulk copies,
+// else with batched plain loads.
+template <bool kBF16, typename F>
+__device__ __forceinline__ void row_pass(const Args& A, GenRing& R, size_t lrow, F fn) {
+  if (A.vec_logits && R.ok) {
+    csweep<kBF16>(A, R, lrow, 0, false, [&](int g, const float* v, const float*) { fn(g, v); });
+  } else {
+    gsweep<kBF16>(A, lrow, (A.V + 7) / 8, fn);
   }
 }
 
@@ -315,14 +434,38 @@ __device__ __forceinline__ unsigned long long mass_fixed(float e) {
 // Level 1 over a whole row, one settle group: every warp-row of 32 groups is one race
 // block.  Returns the winning block's race state (v1 = block) in every thread.
 template <bool kBF16>
-__device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
-                                const Thresh* th) {
+__device__ Race race_blocks_row(const Args& A, GenShm& S, GenRing& R, int row, int pos, float m, float c, float invZ,
+                                int mode, const Thresh* th) {
   const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const int G = (A.V + 7) / 8;
   const int lane = ctid() & 31, wp = ctid() >> 5;
   Race r;
   race_init(r);
+  const bool with_q = mode == RW_RESIDUAL;
+  if (A.vec_logits && (!with_q || A.vec_q) && R.ok) {
+    // a warp's 32 groups of a round are one race block
+    csweep<kBF16>(A, R, lrow, qrow, with_q, [&](int g, const float* v, const float* qv) {
+      float w8 = 0.f, u8 = 0.f;
+      if (g * 8 < A.V) {
+        float w[8], tq[8];
+        group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (w[j] > 0.f) {
+            w8 += w[j];
+            u8 += w[j] + tq[j];
+          }
+      }
+      const float W = warp_sum(w8), U = warp_sum(u8);
+      const int g0 = __shfl_sync(0xffffffffu, g, 0);
+      if (lane == 0 && W > 0.f) {
+        const uint32_t bk = (uint32_t)(g0 / (kRaceBlock / 8));
+        race_consider(r, W, U - W, bk, block_word(A, row, pos, bk));
+      }
+    });
+    return block_race(S, r);
+  }
   constexpr int QB = kGenBatch / 2;   // groups in flight: logits and q
   for (int base0 = 0; base0 < G; base0 += kThreads * QB) {
     float v[QB][8], qv[QB][8];
@@ -364,9 +507,9 @@ __device__ Race race_blocks_row(const Args& A, GenShm& S, int row, int pos, floa
 // The full two-level draw over a row by one settle group; returns the drawn entry
 // (or 0xffffffff when every weight is 0) and sets *margin.
 template <bool kBF16>
-__device__ uint32_t draw_row(const Args& A, GenShm& S, int row, int pos, float m, float c, float invZ, int mode,
-                             const Thresh* th, bool* margin) {
-  const Race l1 = race_blocks_row<kBF16>(A, S, row, pos, m, c, invZ, mode, th);
+__device__ uint32_t draw_row(const Args& A, GenShm& S, GenRing& R, int row, int pos, float m, float c, float invZ,
+                             int mode, const Thresh* th, bool* margin) {
+  const Race l1 = race_blocks_row<kBF16>(A, S, R, row, pos, m, c, invZ, mode, th);
   if (l1.s1 < 0.f) {
     *margin = false;
     return 0xffffffffu;
@@ -442,8 +585,8 @@ __device__ uint32_t nth_tie_index(const Args& A, GenShm& S, size_t lrow, uint32_
 }
 
 template <bool kBF16>
-__device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag, int u, int row, int pos,
-                                          RowCfg cfg) {
+__device__ __noinline__ void unit_general(const Args& A, GenShm& S, GenRing& R, uint32_t tag, int u, int row,
+                                          int pos, RowCfg cfg) {
   const size_t lrow = (size_t)u * A.V;
   const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   const bool has_q = pos < A.k;
@@ -451,7 +594,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   // pass 1: max, argmax, NaN
   unsigned long long best = 0;
   bool nan_seen = false;
-  gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
+  row_pass<kBF16>(A, R, lrow, [&](int g, const float* v) {
     const float gm = group_max(v);
     if (gm != gm) {
       nan_seen = true;
@@ -484,7 +627,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   if (cfg.K > 0) {
     unsigned long long need = (unsigned long long)cfg.K;
     auto each = [&](auto fn) {
-      gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
+      row_pass<kBF16>(A, R, lrow, [&](int g, const float* v) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (g * 8 + i < A.V) fn(km - kf<kBF16>(v[i]));
@@ -504,7 +647,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   csync();
   unsigned long long tail = 0;
   float z0 = 0.f, z1 = 0.f;
-  gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
+  row_pass<kBF16>(A, R, lrow, [&](int g, const float* v) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float x = (v[i] - m) * c;
@@ -538,7 +681,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
     select_from_bin0(S, target, &b, &above);
     // key range of bin b
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
+    row_pass<kBF16>(A, R, lrow, [&](int g, const float* v) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (g * 8 + i >= A.V) continue;
@@ -565,7 +708,7 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
       S.mlo[slot][ctid()] = 0;
       S.mhi[slot][ctid()] = 0;
       csync();
-      gsweep<kBF16>(A, lrow, G, [&](int g, const float* v) {
+      row_pass<kBF16>(A, R, lrow, [&](int g, const float* v) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (g * 8 + i >= A.V) continue;
@@ -627,27 +770,22 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   // alpha pass
   float al0 = 0.f, al1 = 0.f;
   if (has_q) {
-    constexpr int QB = kGenBatch / 2;   // groups in flight: logits and q
-    for (int g0 = ctid(); g0 < G; g0 += kThreads * QB) {
-      float v[QB][8], qv[QB][8];
+    auto acc = [&](int g, const float* v, const float* qv) {
 #pragma unroll
-      for (int b = 0; b < QB; ++b) {
-        const int g = g0 + b * kThreads;
-        if (g < G) {
-          load_group<kBF16>(A, lrow, g, true, v[b]);
-          load_q8(A, qrow, g * 8, qv[b]);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const bool in = (g * 8 + i < A.V) && kept(th, okey(v[i]), (uint32_t)(g * 8 + i));
+        const float p = in ? ex2((v[i] - m) * c) * invZ : 0.f;
+        if (i & 1) al1 += fminf(p, qv[i]); else al0 += fminf(p, qv[i]);
       }
-#pragma unroll
-      for (int b = 0; b < QB; ++b) {
-        const int g = g0 + b * kThreads;
-        if (g >= G) continue;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const bool in = (g * 8 + i < A.V) && kept(th, okey(v[b][i]), (uint32_t)(g * 8 + i));
-          const float p = in ? ex2((v[b][i] - m) * c) * invZ : 0.f;
-          if (i & 1) al1 += fminf(p, qv[b][i]); else al0 += fminf(p, qv[b][i]);
-        }
+    };
+    if (A.vec_logits && A.vec_q && R.ok) {
+      csweep<kBF16>(A, R, lrow, qrow, true, acc);
+    } else {
+      for (int g = ctid(); g < G; g += kThreads) {
+        float v[8], qv[8];
+        load_group<kBF16>(A, lrow, g, true, v);
+        load_q8(A, qrow, g * 8, qv);
+        acc(g, v, qv);
       }
     }
   }
@@ -658,14 +796,20 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, uint32_t tag
   uint32_t y = 0xffffffffu;
   if (need_race) {
     bool mg = false;
-    y = draw_row<kBF16>(A, S, row, pos, m, c, invZ, has_q ? RW_RESIDUAL : RW_BONUS, &th, &mg);
+    y = draw_row<kBF16>(A, S, R, row, pos, m, c, invZ, has_q ? RW_RESIDUAL : RW_BONUS, &th, &mg);
     if (y == 0xffffffffu) {
       draw_flags |= SPEC_F_RESIDUAL_EMPTY;
-      y = draw_row<kBF16>(A, S, row, pos, m, c, invZ, RW_P, &th, &mg);
+      y = draw_row<kBF16>(A, S, R, row, pos, m, c, invZ, RW_P, &th, &mg);
     }
     if (mg) draw_flags |= SPEC_F_MARGIN_DRAW;
   }
   if (ctid() < 32) TLP(u, 7);
+  if (!R.ok) {
+    // a chunk's copy gave up: the unit's results are not trusted
+    if (ctid() < 32) commit_record(A, tag, u, row, empty_record(SPEC_F_TIMEOUT));
+    csync();
+    return;
+  }
   UnitRecord rec = empty_record(flags);
   if (ctid() == 0) {
     if (has_q) {

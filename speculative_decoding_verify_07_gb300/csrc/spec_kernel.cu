@@ -82,7 +82,11 @@ struct alignas(128) VShm {
       u64 stage[kNW][kStage];            // top-k tile staging
     } s;
     TopkScratch tk[kNW];                 // settle scratch (settle CTAs)
-    GenShm gen;                          // general-path group, after the roles
+    struct {
+      GenShm gen;                        // general-path group, after the roles
+      alignas(128) unsigned char ring[kGRing][kGSlot];   // its row chunks
+      unsigned long long bar[kGRing];
+    } g;
   };
   unsigned long long bar[kNW][2];
   unsigned long long cbar[kNW][2];       // fused commit: the warps' copy barriers
@@ -1127,6 +1131,17 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
   const int k1 = A.k + 1;
   const int nGU = P.nX * k1;
   const int gbase = P.nD + P.nT;
+  GenRing R;
+  R.buf = &S.g.ring[0][0];
+  R.bar = S.g.bar;
+  R.fail = &S.g.gen.ring_fail;
+  R.seq = 0u;
+  R.ok = true;
+  if (ctid() == 0) {
+    for (int i = 0; i < kGRing; ++i) mbar_init(&R.bar[i], 1);   // the first copy's fence orders the inits
+    S.g.gen.ring_fail = 0;
+  }
+  csync();
   while (true) {
     if (ctid() == 0) S.gtask = (int)atomicAdd(&A.ws->gnext, 1u);
     csync();
@@ -1135,7 +1150,7 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
     if (g >= nGU) break;
     const int row = (int)P.order[gbase + g / k1], pos = g % k1;
     if (ctid() == 0) TL(TL_SA_START, row * k1 + pos, 2048);
-    unit_general<kBF16>(A, S.gen, tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
+    unit_general<kBF16>(A, S.g.gen, R, tag, row * k1 + pos, row, pos, plan_cfg(A, P, row));
     if (ctid() == 0) TL(TL_SA_END, row * k1 + pos, 2048);
   }
 }
