@@ -288,13 +288,13 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_oracle_baseline(n_rows_all=None, n_rows_1t=4, workers=None):
+def cpu_oracle_baseline(n_rows_all=None, n_rows_1t=16, workers=None):
     """The oracle as it stands, timed on the host cores on bounded samples of
     the mixed workload: one process per core over n_rows_all rows, and one
     thread over n_rows_1t rows.  Input generation happens before the clocks."""
     import multiprocessing as mp
     workers = workers or host_cores()
-    n_rows_all = n_rows_all or max(2 * workers, 16)
+    n_rows_all = n_rows_all or 16 * workers   # about 10 s of CPU work at 16 cores
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers, initializer=_pool_init, initargs=("mixed", {})) as pool:
         # every worker builds its copy of the inputs before the timed map
