@@ -232,7 +232,8 @@ enum {
   TL_CTA_START = 0, TL_CTA_END = 160, TL_FIRST_DATA = 320, TL_STREAM_END = 2368, TL_SETTLE_END = 4416,
   TL_ATICK = 4672, TL_SA_START = 6720, TL_SA_END = 8768, TL_BTICK = 10816, TL_SB_START = 12864,
   TL_SB_END = 14912, TL_FINAL = 16960, TL_ITEM = 17984, TL_PHASE = 34368, TL_ISTART = 34368 + 2048 * 8,
-  TL_IWARP = TL_ISTART + 16384, TL_SIZE = TL_IWARP + 16384
+  TL_IWARP = TL_ISTART + 16384, TL_ISTATE = TL_IWARP + 16384, TL_SUB = TL_ISTATE + 16384,
+  TL_SIZE = TL_SUB + 2048 * 8
 };
 #ifdef SPEC_TIMELINE
 static __device__ unsigned long long g_tl[TL_SIZE];
@@ -246,9 +247,11 @@ __device__ __forceinline__ void tl_stamp(int slot, int i, int lim) {
 #define TL(slot, i, lim) tl_stamp((slot), (i), (lim))
 // phase p (0..7) of the settle of unit u
 #define TLP(u, p) do { if ((threadIdx.x & 31) == 0 && (u) < 2048) tl_stamp(TL_PHASE + (u) * 8 + (p), 0, 1); } while (0)
+#define TLS(u, p) do { if ((threadIdx.x & 31) == 0 && (u) < 2048) tl_stamp(TL_SUB + (u) * 8 + (p), 0, 1); } while (0)
 #else
 #define TL(slot, i, lim) ((void)0)
 #define TLP(u, p) ((void)0)
+#define TLS(u, p) ((void)0)
 #endif
 
 // The row index the random streams are keyed by.

@@ -25,7 +25,7 @@
 //   * Settle CTAs (about 1 in 10, every stride-th block).  Their warps take
 //     the settle tasks -- one per unit after its A tiles, one per drafted
 //     unfiltered unit after its B tiles -- in the order of the sequence,
-//     task t to settle warp t mod (warps); a warp waits for its task's tile
+//     task t to settle CTA t mod (settle CTAs); a warp waits for its task's tile
 //     count, settles the unit (spec_settle.cuh) and clears the count.  Tasks
 //     come in the order their tiles do, and a B tile only waits for a state
 //     that an earlier task publishes, so every wait ends.  The last settled
@@ -54,7 +54,7 @@ constexpr int kOrderSmem = 256;        // batches up to this many rows keep orde
 constexpr int kStage = 64;             // per-warp staging of a top-k tile's candidates
 constexpr int kMaxWaves = 40;
 constexpr int kMaxSeg = 4 * kMaxWaves + 8;   // segments of the item sequence (2 A and at most 2 more per wave, 2 classes)
-constexpr int kSettleEvery = 9;        // one settle CTA per this many CTAs
+constexpr int kSettleEvery = 6;        // one settle CTA per this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
 static_assert(kAllThreads >= kOrderSmem, "one placement round for a shared-memory order");
 static_assert(kAllThreads >= kThreads, "the general phase uses the first kThreads threads");
@@ -994,6 +994,12 @@ __device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32
       if (lane == 0 && ok) issue<kBF16>(A, ib, B.b, B.bb);
       first = false;
     }
+#ifdef SPEC_TIMELINE
+    if (lane == 0 && ia.t < 16384u) {
+      TL(TL_ISTART, (int)ia.t, 16384);
+      g_tl[TL_IWARP + ia.t] = gs + 1u + (ia.kind == 2 ? 0x10000u : 0u);
+    }
+#endif
     if (!ok) {
       // the buffer's copy never completed: mark this tile and stop taking new ones
       broken = true;
@@ -1018,6 +1024,7 @@ __device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32
           __nanosleep(128);
           state_load(A, ia.u, sw8);
         }
+        if (lane == 0 && ia.t < 16384u) TL(TL_ISTATE, (int)ia.t, 16384);
         if (!st_ok) {
           timeout_record(A, tag, ia, false);
         } else {
@@ -1213,7 +1220,9 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     const bool settle_cta = (bx % A.settle_stride) == 0 && bx / A.settle_stride < A.n_settle;
     if (settle_cta) {
       const uint32_t nst = (uint32_t)A.n_settle * kNW;
-      settle_loop<kBF16>(A, P, S, tag, w, (uint32_t)(bx / A.settle_stride) * kNW + (uint32_t)w, nst);
+      // task t to settle CTA t mod n_settle: consecutive tasks (one class,
+      // neighbouring rows) go to different SMs
+      settle_loop<kBF16>(A, P, S, tag, w, (uint32_t)w * (uint32_t)A.n_settle + (uint32_t)(bx / A.settle_stride), nst);
     } else {
       // stream CTA rank: blocks before this one, minus the settle CTAs among them
       const int srank = bx - min(A.n_settle, bx / A.settle_stride + 1);
@@ -1258,7 +1267,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
 // ---------------------------------------------------------------------------
 // Items of A tiles between the end of an unfiltered wave's A tiles and its
 // B tiles: the wave's settles (a few microseconds) finish meanwhile.
-constexpr uint32_t kBDelayItems = 1600;
+constexpr uint32_t kBDelayItems = 2800;
 
 template <bool kBF16>
 int launch_verify(const Args& A0, cudaStream_t stream) {

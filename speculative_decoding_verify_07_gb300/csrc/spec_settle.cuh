@@ -1030,7 +1030,8 @@ __device__ __forceinline__ uint32_t count_key_ge(const KeyRounds<CR>& K, uint32_
 // listed), by bisection on the value key within [lo, hi] (lo at or below it,
 // hi the largest), then on the index among the entries at that key.
 template <bool kBF16, int CR>
-__device__ __noinline__ u64 kth_listed(const u64* cand, int NL, uint32_t K, uint32_t lo, uint32_t hi) {
+__device__ __noinline__ u64 kth_listed(const u64* cand, int NL, uint32_t K, uint32_t lo, uint32_t hi,
+                                       uint32_t* tmp) {
   const int lane = threadIdx.x & 31;
   KeyRounds<CR> R;
 #pragma unroll
@@ -1066,6 +1067,28 @@ __device__ __noinline__ u64 kth_listed(const u64* cand, int NL, uint32_t K, uint
     if ((uint32_t)(cand[q] >> 32) == tkey) low = min(low, (uint32_t)cand[q]);
   low = __reduce_min_sync(kSettleFull, low);
   if (n_eq == need) return ((u64)tkey << 32) | low;   // every entry at the key is kept
+  if (n_eq <= 32u) {
+    // bf16 values tie often: gather the entries at the key (tmp, 32 words)
+    // and take the one with need - 1 larger low words (0xffffffff - index)
+    uint32_t n = 0;
+    for (int q0 = 0; q0 < NL; q0 += 32) {
+      const int q = q0 + lane;
+      const u64 k = q < NL ? cand[q] : 0ull;
+      const bool in = (uint32_t)(k >> 32) == tkey;
+      const unsigned ball = __ballot_sync(kSettleFull, in);
+      const uint32_t p = n + __popc(ball & ((1u << lane) - 1u));
+      if (in && p < 32u) tmp[p] = (uint32_t)k;
+      n += __popc(ball);
+    }
+    __syncwarp();
+    const uint32_t my = (uint32_t)lane < n_eq ? tmp[lane] : 0u;
+    uint32_t rk = 0;
+    for (uint32_t j = 0; j < n_eq; ++j) rk += tmp[j] > my ? 1u : 0u;
+    const unsigned win = __ballot_sync(kSettleFull, (uint32_t)lane < n_eq && rk == need - 1u);
+    const uint32_t lw = __shfl_sync(kSettleFull, my, __ffs(win) - 1);
+    __syncwarp();
+    return ((u64)tkey << 32) | lw;
+  }
   // the need-th largest low word (0xffffffff - index) among the entries at tkey
   uint32_t l = low, h = 0xffffffffu;
   while (l < h) {
@@ -1114,11 +1137,12 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     do {
       ok = true;
       uint32_t fl = 0;
+      constexpr int kB = 8;
 #pragma unroll 1
-      for (int q0 = 0; q0 < NL; q0 += 32 * 8) {
-        u64 wk[8], wi[8];
+      for (int q0 = 0; q0 < NL; q0 += 32 * kB) {
+        u64 wk[kB], wi[kB];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kB; ++i) {
           const int q = q0 + 32 * i + lane;
           wk[i] = 0ull;
           wi[i] = 0ull;
@@ -1129,7 +1153,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
           }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kB; ++i) {
           const int q = q0 + 32 * i + lane;
           if (q < NL) {
             ok = ok && tag_ok(wk[i], tag) && tag_ok(wi[i], tag);
@@ -1165,6 +1189,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     return;
   }
   const int am = (int)key64_idx(top);
+  TLS(u, 0);
 
   // 2. tau (a lower bound of the K-th listed value key), kappa by bisection
   // above it, the K entries at or above kappa (in S.sel) with their q, ranked
@@ -1197,7 +1222,10 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
   // tiles of fp32 logits, half as many of bf16
   constexpr int CR = (kBF16 ? kMaxListCand / 2 : kMaxListCand) / 32;
   static_assert(Geo<true>::EA == 2 * Geo<false>::EA, "bf16 tiles hold twice the entries");
-  const u64 kappa = kth_listed<kBF16, CR>(S.cand, NL, (uint32_t)K, tau, (uint32_t)(top >> 32));
+  TLS(u, 1);
+  const u64 kappa = kth_listed<kBF16, CR>(S.cand, NL, (uint32_t)K, tau, (uint32_t)(top >> 32),
+                                          reinterpret_cast<uint32_t*>(S.qsel));
+  TLS(u, 2);
   const int n_k = (int)min(cnt, (uint32_t)K);
   {
     uint32_t n = 0;
@@ -1212,6 +1240,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     }
   }
   __syncwarp();
+  TLS(u, 3);
   u64* sorted = reinterpret_cast<u64*>(S.hist);
   {
     // q of the gathered entries (in flight while they are ranked)
@@ -1240,6 +1269,7 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
       }
   }
   __syncwarp();
+  TLS(u, 4);
   bool unsafe = false;
   for (int ch = lane; ch < NT; ch += 32) {
     const u64 last = S.cand[ch * kList + kList - 1];
