@@ -109,8 +109,8 @@ enum {
  *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
  *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
  *                 settle or finalize wait for records, 8 the row-order wait
- *                 of batches above 256 rows; 16 is unused); 0 when
- *                 every wait ended normally.                                */
+ *                 of batches above 256 rows, 16 a grid barrier of the
+ *                 top-p passes); 0 when every wait ended normally.          */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.
@@ -233,10 +233,10 @@ int spec_commit_swap(const float* verify_rec, const uint16_t* verify_conv, const
  * library (a file-scope device array, held on every GPU that loads the
  * library until the process exits).  The call allocates nothing.
  *   - Limit: spec_verify_workspace_size(B, k, V) must not exceed
- *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 170 bytes
- *     per (row, position) unit per 1024 vocabulary entries, so at V = 151936
- *     about 325 units fit, e.g. 108 rows at k = 2); a larger batch returns
- *     SPEC_E_WORKSPACE and enqueues nothing.
+ *     SPEC_NOALLOC_MAX_WORKSPACE (8 MiB; the workspace takes about 10.5 KB
+ *     per (row, position) unit plus 126 bytes per unit per 1024 vocabulary
+ *     entries, so at V = 151936 about 282 units fit, e.g. 94 rows at k = 2);
+ *     a larger batch returns SPEC_E_WORKSPACE and enqueues nothing.
  *   - Arguments are checked exactly as spec_verify checks them, before
  *     anything is enqueued: a refused call enqueues nothing.
  *   - The first call on each device looks up the array's device address

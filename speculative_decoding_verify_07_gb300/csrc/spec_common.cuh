@@ -48,7 +48,10 @@ struct Geo {
   static_assert((EB * es) % 16 == 0, "q part of a B tile must start 16-byte aligned");
 };
 
-enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3 };
+// Row classes: greedy, small top-k (candidate lists), unfiltered, a top-k
+// above the list limit (general path), top-p alone (grid-wide passes).
+enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3, UT_TOPP = 4 };
+constexpr int kClasses = 5;
 
 // Error bits of WsHeader::error (OR-ed during a call; moved to last_error by
 // the call's last CTA).
@@ -57,7 +60,7 @@ enum {
   ERR_COPY_WAIT = 2,       // a tile's bulk copy did not complete
   ERR_RECORD_WAIT = 4,     // a settle or finalize gave up waiting for records
   ERR_ORDER_WAIT = 8,      // a CTA gave up waiting for the row order
-  ERR_QUEUE = 16           // unused
+  ERR_BARRIER = 16         // a CTA gave up waiting at a grid barrier of the top-p passes
 };
 
 struct WsHeader {
@@ -69,10 +72,12 @@ struct WsHeader {
   uint32_t inject;        // test hook: nonzero makes the finalize of row 0 wait for a tag nothing writes
   uint32_t last_error;    // ERR_* bits of the last completed call
   uint32_t pad0;
-  uint32_t n_class[4];    // rows per class (large batches)
+  uint32_t n_class[kClasses];   // rows per class (large batches)
   uint32_t commit_next;   // fused commit: next copy job
   uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
-  uint32_t pad[45];
+  uint32_t bar;           // top-p passes: arrivals at the grid barriers of this call
+  uint32_t tp_more;       // top-p passes: bit L set when refinement level L is needed
+  uint32_t pad[42];
   uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
   uint32_t pad1[4];
 };
@@ -155,8 +160,17 @@ __host__ __device__ inline int max_nta(int V) { return ceil_div(V, Geo<false>::E
 __host__ __device__ inline int max_ntb(int V) { return ceil_div(V, Geo<false>::EB); }
 
 struct Layout {
-  size_t row_ticket, ucnt, rec, brec, ust, urec, order, done, total;
+  size_t row_ticket, ucnt, rec, brec, ust, urec, order, done, tp, total;
 };
+
+// Scratch of the top-p passes, per top-p unit (u64 words, zeroed by every
+// call that has top-p rows): 32 unit words (summary and threshold states),
+// the mass histogram of 256 bins, then kTpLevels refinement histograms.
+constexpr int kTpBins = 256;
+constexpr int kTpLevels = 4;             // 8 key bits a level: two for bf16 keys, four for fp32
+constexpr int kTpUnitWords = 32;
+constexpr int kTpStride = kTpUnitWords + kTpBins * (1 + kTpLevels);
+static_assert(kTpStride % 2 == 0, "the top-p scratch is zeroed in 16-byte stores");
 
 __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   const size_t U = (size_t)B * (k + 1);
@@ -170,6 +184,7 @@ __host__ __device__ inline Layout ws_layout(int B, int k, int V) {
   L.urec = off; off = align_up(off + U * kURecWords * 8, 256);
   L.order = off; off = align_up(off + (size_t)B * 4, 256);
   L.done = off; off = align_up(off + (size_t)B * 8, 256);
+  L.tp = off; off = align_up(off + U * kTpStride * 8, 256);
   L.total = off;
   return L;
 }
@@ -220,6 +235,7 @@ struct Args {
   int vec_logits;
   int vec_q;
   u64* done;              // fused commit: finalized rows in order, tagged (row << 5 | accept_len)
+  u64* tp;                // top-p passes: per-unit scratch (kTpStride words per top-p unit)
   FusedCommit fc;
 };
 
@@ -233,7 +249,7 @@ enum {
   TL_ATICK = 4672, TL_SA_START = 6720, TL_SA_END = 8768, TL_BTICK = 10816, TL_SB_START = 12864,
   TL_SB_END = 14912, TL_FINAL = 16960, TL_ITEM = 17984, TL_PHASE = 34368, TL_ISTART = 34368 + 2048 * 8,
   TL_IWARP = TL_ISTART + 16384, TL_ISTATE = TL_IWARP + 16384, TL_SUB = TL_ISTATE + 16384,
-  TL_SIZE = TL_SUB + 2048 * 8
+  TL_TP = TL_SUB + 2048 * 8, TL_TP_WARP = TL_TP + 16, TL_SIZE = TL_TP_WARP + 8 * 2048
 };
 #ifdef SPEC_TIMELINE
 static __device__ unsigned long long g_tl[TL_SIZE];
@@ -284,6 +300,7 @@ __device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
   if (greedy) r.type = UT_GREEDY;
   else if (r.K > 0 && r.K <= kTopkSmall && max_nta(V) * kList <= kMaxListCand) r.type = UT_TOPK;
   else if (r.K == 0 && r.P >= 1.0f) r.type = UT_DENSE;
+  else if (r.K == 0) r.type = UT_TOPP;
   else r.type = UT_GENERAL;
   return r;
 }
@@ -291,14 +308,14 @@ __device__ __forceinline__ RowCfg classify(const spec_params_t& prm, int V) {
 // Row configuration packed in 16 bytes (kept in shared memory per row).
 struct RowPack {
   float c, invT, P;
-  uint32_t tk;            // type | bad_param << 2 | K << 8
+  uint32_t tk;            // type | bad_param << 3 | K << 8
 };
 __device__ __forceinline__ RowPack pack_cfg(const RowCfg& r) {
   RowPack p;
   p.c = r.c;
   p.invT = r.invT;
   p.P = r.P;
-  p.tk = (uint32_t)r.type | (r.bad_param ? 4u : 0u) | ((uint32_t)r.K << 8);
+  p.tk = (uint32_t)r.type | (r.bad_param ? 8u : 0u) | ((uint32_t)r.K << 8);
   return p;
 }
 __device__ __forceinline__ RowCfg unpack_cfg(const RowPack& p) {
@@ -306,8 +323,8 @@ __device__ __forceinline__ RowCfg unpack_cfg(const RowPack& p) {
   r.c = p.c;
   r.invT = p.invT;
   r.P = p.P;
-  r.type = (int)(p.tk & 3u);
-  r.bad_param = (p.tk & 4u) != 0;
+  r.type = (int)(p.tk & 7u);
+  r.bad_param = (p.tk & 8u) != 0;
   r.K = (int)(p.tk >> 8);
   return r;
 }

@@ -278,6 +278,11 @@ struct Race {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// Start bringing `bytes` (a multiple of 16, from a 16-byte aligned address)
+// into L2 with the copy engine.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void race_init(Race& r) {
   r.s1 = -1.0f;

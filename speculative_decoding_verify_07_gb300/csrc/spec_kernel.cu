@@ -45,6 +45,7 @@
 #include "spec_general.cuh"
 #include "spec_host.h"
 #include "spec_settle.cuh"
+#include "spec_topp.cuh"
 
 namespace specv {
 
@@ -70,9 +71,9 @@ struct Seg {
 };
 
 struct OrderScratch {
-  int n_class[4];
-  int run[4];
-  int scan[kNW][4];
+  int n_class[kClasses];
+  int run[kClasses];
+  int scan[kNW][kClasses];
 };
 
 struct alignas(128) VShm {
@@ -108,15 +109,16 @@ static_assert(sizeof(VShm) <= 232448, "shared memory of a CTA exceeds 227 KB");
 
 // ---------------------------------------------------------------------------
 // Row order: rows of each class, stably, as [unfiltered][small top-k]
-// [general][greedy].
+// [general][top-p][greedy].
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int class_rank(int cl) {
-  return cl == UT_DENSE ? 0 : (cl == UT_TOPK ? 1 : (cl == UT_GENERAL ? 2 : 3));
-}
 __device__ __forceinline__ int class_base(const OrderScratch& O, int cl) {
-  const int nD = O.n_class[UT_DENSE], nT = O.n_class[UT_TOPK], nX = O.n_class[UT_GENERAL];
-  const int r = class_rank(cl);
-  return r == 0 ? 0 : (r == 1 ? nD : (r == 2 ? nD + nT : nD + nT + nX));
+  const int nD = O.n_class[UT_DENSE], nT = O.n_class[UT_TOPK], nX = O.n_class[UT_GENERAL],
+            nP = O.n_class[UT_TOPP];
+  return cl == UT_DENSE ? 0
+       : cl == UT_TOPK ? nD
+       : cl == UT_GENERAL ? nD + nT
+       : cl == UT_TOPP ? nD + nT + nX
+                       : nD + nT + nX + nP;
 }
 
 // Stable placement of one round of kAllThreads rows (cl < 0: no row).
@@ -124,7 +126,7 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   unsigned mine = 0;
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
+  for (int t = 0; t < kClasses; ++t) {
     const unsigned b = __ballot_sync(kFull, cl == t);
     if (lane == 0) O.scan[w][t] = __popc(b);
     if (cl == t) mine = b;
@@ -137,7 +139,7 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
     order[off] = (uint32_t)r;
   }
   __syncthreads();
-  if (tid < 4) {
+  if (tid < kClasses) {
     int s = 0;
     for (int ww = 0; ww < kNW; ++ww) s += O.scan[ww][tid];
     O.run[tid] += s;
@@ -149,7 +151,7 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
 // shared memory (one parameter load per row).
 __device__ __noinline__ void build_order_smem(const Args& A, uint32_t* order, RowPack* cfgs, OrderScratch& O) {
   const int tid = threadIdx.x;
-  if (tid < 4) {
+  if (tid < kClasses) {
     O.n_class[tid] = 0;
     O.run[tid] = 0;
   }
@@ -169,7 +171,7 @@ __device__ __noinline__ void build_order_smem(const Args& A, uint32_t* order, Ro
 // workspace and publishes them with the call's tag; the other CTAs wait for it.
 __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, uint32_t tag) {
   const int tid = threadIdx.x;
-  if (tid < 4) {
+  if (tid < kClasses) {
     O.n_class[tid] = 0;
     O.run[tid] = 0;
   }
@@ -180,7 +182,7 @@ __device__ __noinline__ void build_order_global(const Args& A, OrderScratch& O, 
     const int r = base + tid;
     place_round(A.order, O, r, r < A.B ? classify(A.params[r], A.V).type : -1);
   }
-  if (tid < 4) A.ws->n_class[tid] = (uint32_t)O.n_class[tid];
+  if (tid < kClasses) A.ws->n_class[tid] = (uint32_t)O.n_class[tid];
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -196,7 +198,7 @@ struct Plan {
   const RowPack* cfg;       // per-row configs in shared memory (null: classify from the parameters)
   const Seg* seg;
   int nseg;
-  int nD, nT, nG, nX;       // rows: unfiltered, small top-k, greedy, general
+  int nD, nT, nG, nX, nP;   // rows: unfiltered, small top-k, greedy, general, top-p
   int NTA, NTB;             // tiles per unit of this call's dtype
 };
 
@@ -1184,6 +1186,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     P.nT = S.ord.n_class[UT_TOPK];
     P.nG = S.ord.n_class[UT_GREEDY];
     P.nX = S.ord.n_class[UT_GENERAL];
+    P.nP = S.ord.n_class[UT_TOPP];
   } else {
     __syncthreads();
     if (blockIdx.x == 0) build_order_global(A, S.ord, S.tag);
@@ -1206,11 +1209,20 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     P.nT = (int)__ldcg(&A.ws->n_class[UT_TOPK]);
     P.nG = (int)__ldcg(&A.ws->n_class[UT_GREEDY]);
     P.nX = (int)__ldcg(&A.ws->n_class[UT_GENERAL]);
+    P.nP = (int)__ldcg(&A.ws->n_class[UT_TOPP]);
   }
   const uint32_t tag = S.tag;
   P.NTA = ceil_div(A.V, G::EA);
   P.NTB = ceil_div(A.V, G::EB);
-  build_segments(A, S, P.nD, P.nT, P.nX, P.nG, P.NTA, P.NTB, b_delay);
+  // (general and top-p rows have no stream tiles; greedy rows follow them)
+  build_segments(A, S, P.nD, P.nT, P.nX + P.nP, P.nG, P.NTA, P.NTB, b_delay);
+  if (P.nP > 0 && order_ok) {
+    // the top-p passes' scratch, zero before their first barrier
+    const size_t n16 = (size_t)P.nP * (size_t)(A.k + 1) * (kTpStride / 2);
+    uint4* z = reinterpret_cast<uint4*>(A.tp);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+      z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   __syncthreads();
   P.seg = S.seg;
   P.nseg = S.nseg;
@@ -1230,6 +1242,17 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
       // item t belongs to stream CTA t mod n_stream (consecutive items on different SMs)
       stream_loop<kBF16>(A, P, S, tag, w, (uint32_t)srank, (uint32_t)n_stream);
     }
+  }
+  if (P.nP > 0 && order_ok) {
+    // top-p rows: grid-wide passes (every thread of every CTA)
+    __syncthreads();
+    TpPlan T;
+    T.order = P.order;
+    T.cfg = P.cfg;
+    T.base = P.nD + P.nT + P.nX;
+    T.nU = P.nP * (A.k + 1);
+    T.nlev = 0;
+    topp_passes<kBF16>(A, T, tag, S.s.buf[w][0], S.broken[w] == 0u);
   }
   if (P.nX > 0 && order_ok) {
     __syncthreads();
@@ -1253,6 +1276,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
       A.ws->gnext = 0u;
       A.ws->commit_next = 0u;
       A.ws->done_count = 0u;
+      A.ws->bar = 0u;
+      A.ws->tp_more = 0u;
       A.ws->ctas_done = 0u;
       A.ws->last_error = __ldcg(&A.ws->error);
       A.ws->error = 0u;

@@ -1105,7 +1105,7 @@ __device__ __noinline__ u64 kth_listed(const u64* cand, int NL, uint32_t K, uint
 // Settle a small top-k unit with one warp; S is scratch in shared memory
 // (one of the warp's stream buffers).
 //   1. The tiles' lists into S.cand (candidate q: tile q / 8, slot q mod 8),
-//      loaded 8 candidates a lane at a time.
+//      loaded 10 candidates a lane at a time.
 //   2. tau: the ceil(K / 8)-th largest value key among the last entries of
 //      full lists -- that many lists hold 8 entries at or above it, so the
 //      K-th listed entry is at or above it.  The listed entries at or above
@@ -1137,7 +1137,9 @@ __device__ __noinline__ void topk_settle(const Args& A, uint32_t tag, TopkScratc
     do {
       ok = true;
       uint32_t fl = 0;
-      constexpr int kB = 8;
+      // ten candidates a lane at a time: one round trip for a bf16 row of
+      // V <= 163840 (40 tiles)
+      constexpr int kB = 10;
 #pragma unroll 1
       for (int q0 = 0; q0 < NL; q0 += 32 * kB) {
         u64 wk[kB], wi[kB];

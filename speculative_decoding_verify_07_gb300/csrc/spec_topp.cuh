@@ -1,0 +1,1022 @@
+// spec_verify, rows with top-p and no top-k: the threshold search as
+// grid-wide passes (sm_103a).
+//
+// Such a row keeps the shortest prefix of the total order whose mass reaches
+// P, the crossing entry included (inclusionAI/AReno PR #550, "What does this
+// PR do?" Phase 2: the sampler-equivalent target distribution).  Where that
+// prefix ends depends on the mass of the whole row above every candidate
+// threshold, so these units run after the stream and settle roles, in passes
+// over tiles of 2048 logits.  Every warp of the grid takes a contiguous share
+// of all tiles of all top-p units, and a grid barrier separates the passes:
+//   1. max: each tile's maximum (or that it holds a NaN or +inf) goes into
+//      the tile's record; the tile's draft probabilities are prefetched into
+//      L2 for pass 5.  Later passes take the unit's max from its tiles';
+//   2. mass: every entry's fixed-point weight e * 2^40, e = exp2((l - m) c),
+//      goes into one of 256 bins of 1/8 in log2 of the weight, summed in the
+//      warp's shared memory and then added to the unit's histogram in global
+//      memory (fixed point makes every sum exact and independent of order);
+//   3. refinement: each warp reads the unit's histograms, finds the bin where
+//      the mass from the top reaches ceil(P Z) and the bin's range of order
+//      keys, and histograms the mass of the entries in that range by key, 8
+//      key bits a level, until one key, the crossing key, is left (one level
+//      for most bf16 rows; at most two for bf16 and four for fp32);
+//   4. ties: the entries at the crossing key in each tile.  The first n of
+//      them by index are kept, where n comes from the mass still missing;
+//   5. tiles: with the kept set known, alpha = sum min(p, q) and the level-1
+//      races over the tile's 256-entry blocks, of the residual max(p - q, 0)
+//      and of p;
+//   6. settle: one warp per unit merges the tiles' alphas and races, runs the
+//      accept test and the level-2 race in the winning block, and writes the
+//      unit's record (the row's last unit finalizes the row).
+// After each barrier every warp derives its unit's threshold state from the
+// histograms itself (a few loads and warp scans), so no pass waits for a
+// settle step.  Each barrier wait is bounded: one that gives up sets
+// ERR_BARRIER, and the units come back with SPEC_F_TIMEOUT.
+#pragma once
+
+#include "spec_common.cuh"
+#include "spec_general.cuh"
+
+namespace specv {
+
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kTpET = 2048;                  // entries per tile (8 race blocks)
+constexpr int kTpNR = kTpET / kRaceBlock;    // blocks per tile; a lane holds one group of 8 entries of each
+constexpr int kTpHalf = kTpNR / 2;           // pass 5 takes a tile in two halves of 4 blocks
+static_assert(kTpET == Geo<false>::EA, "top-p tiles use the A-record slots of their unit, one per tile");
+
+// The top-p rows of the call: their place in the row order and the levels run.
+struct TpPlan {
+  const uint32_t* order;
+  const RowPack* cfg;     // per-row configs in shared memory (null: classify from the parameters)
+  int base;               // index of the first top-p row in the order
+  int nU;                 // top-p units
+  int nlev;               // refinement levels run
+};
+
+struct TpUnit {
+  int row, pos, uid;
+  bool has_q;
+  RowCfg cfg;
+  size_t lrow, qrow;
+};
+__device__ __noinline__ TpUnit tp_unit(const Args& A, const TpPlan& T, int j) {
+  TpUnit U;
+  const int k1 = A.k + 1;
+  U.row = (int)T.order[T.base + j / k1];
+  U.pos = j % k1;
+  U.uid = U.row * k1 + U.pos;
+  U.has_q = U.pos < A.k;
+  U.cfg = T.cfg ? unpack_cfg(T.cfg[U.row]) : classify(A.params[U.row], A.V);
+  U.lrow = (size_t)U.uid * A.V;
+  U.qrow = ((size_t)U.row * A.k + U.pos) * (size_t)A.V;
+  return U;
+}
+
+__device__ __forceinline__ u64* tp_hist(const Args& A, int j, int lvl) {
+  return A.tp + (size_t)j * kTpStride + kTpUnitWords + lvl * kTpBins;
+}
+// A unit's summary, tagged words at the start of its scratch: [0] the
+// crossing key, [1] n_need, [2] Z_S, [3] its SPEC_F_MARGIN_TOPP flag
+// (written in pass 4), [4] the index of the last kept entry at the crossing
+// key (pass 5), [5] the unit's max key (pass 2).  Then, plain words, the
+// threshold state after each level (5 words a level).
+constexpr int kTpStateWords = 5;
+constexpr int kTpStateBase = 8;
+static_assert(kTpStateBase + kTpLevels * kTpStateWords <= kTpUnitWords, "unit words");
+__device__ __forceinline__ u64* tp_summary(const Args& A, int j) { return A.tp + (size_t)j * kTpStride; }
+__device__ __forceinline__ u64* tp_state_at(const Args& A, int j, int L) {
+  return A.tp + (size_t)j * kTpStride + kTpStateBase + L * kTpStateWords;
+}
+// A tile's record: tagged words in the unit's A-record slot of that tile
+// (top-p units have no stream tiles).  [0] ties at the crossing key,
+// [1] alpha, [2..6] residual race (s1, t1, s2, t2, v1), [7..11] race of p,
+// [12] the tile max's order key (0: no finite entry, kTpBadKey: a NaN or
+// +inf).
+constexpr uint32_t kTpBadKey = 0xffffffffu;
+constexpr uint32_t kTpMissKey = 0xfffffffeu;   // summary only: a tile's max did not arrive (no finite key is this large)
+constexpr int kTpMaxWord = 12;
+__device__ __forceinline__ u64* tp_rec(const Args& A, int uid, int t) {
+  return A.rec + ((size_t)uid * A.NTA + t) * kRecWords;
+}
+
+// Group of 8 logits starting at entry e0 of a row, as raw words (entries
+// past V read as -inf).
+template <bool kBF16>
+__device__ __forceinline__ void tp_group(const Args& A, size_t lrow, int e0, uint32_t (&w)[kBF16 ? 4 : 8]) {
+  if constexpr (kBF16) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(A.logits) + lrow;
+    if (A.vec_logits && e0 + 8 <= A.V) {
+      const uint4 x = __ldcg(reinterpret_cast<const uint4*>(p + e0));
+      w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = e0 + 2 * i < A.V ? (uint32_t)p[e0 + 2 * i] : 0xff80u;
+        const uint32_t hi = e0 + 2 * i + 1 < A.V ? (uint32_t)p[e0 + 2 * i + 1] : 0xff80u;
+        w[i] = lo | (hi << 16);
+      }
+    }
+  } else {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(A.logits) + lrow;
+    if (A.vec_logits && e0 + 8 <= A.V) {
+      const uint4 a = __ldcg(reinterpret_cast<const uint4*>(p + e0));
+      const uint4 b = __ldcg(reinterpret_cast<const uint4*>(p + e0 + 4));
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = e0 + i < A.V ? p[e0 + i] : 0xff800000u;
+    }
+  }
+}
+template <bool kBF16>
+__device__ __forceinline__ float tp_v(const uint32_t* w, int j) {
+  if constexpr (kBF16) return __uint_as_float((j & 1) ? (w[j >> 1] & 0xffff0000u) : (w[j >> 1] << 16));
+  else return __uint_as_float(w[j]);
+}
+// The lane's groups of tile t: group r holds entries t*kTpET + (32 r + lane)*8 ...
+template <bool kBF16>
+__device__ __forceinline__ void tp_tile(const Args& A, size_t lrow, int t, uint32_t (&w)[kTpNR][kBF16 ? 4 : 8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < kTpNR; ++r) tp_group<kBF16>(A, lrow, t * kTpET + (r * 32 + lane) * 8, w[r]);
+}
+
+// The mass bin of x = (l - m) c <= 0: 1/8 in log2 of the weight a bin, the
+// tail (weights below 2^-31.875) in bin 255.  floor(t) for t in [0, 255] by
+// rounding on the float adder (t + 2^23 is t rounded to an integer, exactly)
+// and stepping down when that rounded up: no conversion instruction.
+__device__ __forceinline__ int tp_bin(float x) {
+  const float t = fminf(-x * 8.0f, 255.0f);
+  const float r = t + 8388608.0f;
+  const int k = (int)(__float_as_uint(r) - 0x4b000000u);
+  return k - ((r - 8388608.0f > t) ? 1 : 0);
+}
+template <bool kBF16>
+__device__ __forceinline__ float tp_key_val(uint32_t key) { return from_okey(full_key<kBF16>(key)); }
+
+__device__ __forceinline__ u64 shfl_u64(u64 v, int src) {
+  const uint32_t lo = __shfl_sync(kAll, (uint32_t)v, src), hi = __shfl_sync(kAll, (uint32_t)(v >> 32), src);
+  return ((u64)hi << 32) | lo;
+}
+__device__ __forceinline__ u64 warp_incl_scan_u64(u64 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t lo = __shfl_up_sync(kAll, (uint32_t)v, o), hi = __shfl_up_sync(kAll, (uint32_t)(v >> 32), o);
+    if (lane >= o) v += ((u64)hi << 32) | lo;
+  }
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_excl_scan_u32(uint32_t v, uint32_t* total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kAll, inc, o);
+    if (lane >= o) inc += y;
+  }
+  *total = __shfl_sync(kAll, inc, 31);
+  return inc - v;
+}
+
+// In a 256-bin histogram held 8 bins a lane (lane l: bins 8l .. 8l + 7), the
+// first bin at which the sum from bin 0 reaches `need`, and the sum of the
+// bins before it (bin 255 if the histogram holds less).
+__device__ __noinline__ void tp_select(const u64 (&h)[8], u64 need, int* bin, u64* before) {
+  const int lane = threadIdx.x & 31;
+  u64 tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += h[i];
+  const u64 inc = warp_incl_scan_u64(tot);
+  const unsigned b = __ballot_sync(kAll, inc >= need);
+  const int f = b ? __ffs(b) - 1 : 31;
+  int bi = -1;
+  u64 cum = inc - tot, bef = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (bi < 0 && cum + h[i] >= need) {
+      bi = i;
+      bef = cum;
+    }
+    cum += h[i];
+  }
+  if (bi < 0) {
+    bi = 7;
+    bef = cum - h[7];
+  }
+  *bin = __shfl_sync(kAll, lane * 8 + bi, f);
+  *before = shfl_u64(bef, f);
+}
+
+// The smallest key in [lo, hi] at which pred holds (pred is false, then
+// true, along the keys), or hi + 1 when it holds nowhere; 32 keys probed a
+// round, one per lane.
+template <typename Pred>
+__device__ __forceinline__ uint32_t tp_first_true(uint32_t lo, uint32_t hi, Pred pred) {
+  const int lane = threadIdx.x & 31;
+  u64 L = lo, H = (u64)hi + 1u;   // the answer lies in [L, H]
+  while (L < H) {
+    const u64 step = (H - L + 31u) / 32u;
+    const u64 key = L + step * (u64)lane;
+    const bool p = key >= H || pred((uint32_t)key);
+    const unsigned b = __ballot_sync(kAll, p);
+    if (b == 0u) {
+      L += 31u * step + 1u;
+      continue;
+    }
+    const int f = __ffs(b) - 1;
+    if (f == 0) break;
+    const u64 nL = L + (u64)(f - 1) * step + 1u;
+    H = min(L + (u64)f * step, H);
+    L = nL;
+  }
+  return (uint32_t)L;
+}
+
+// Threshold state of a unit: the mass bin b0 where the sum from the top
+// reaches target = ceil(P zk), the key range [lo, hi] still holding the
+// crossing key, the shift of the next level's bins ((hi - key) >> s), the
+// mass above the range and the mass still missing within it (rem).
+// lo == hi: the crossing key is found.
+struct TpState {
+  u64 zk, above, rem;
+  uint32_t lo, hi;
+  int s, b0;
+};
+__device__ __forceinline__ int tp_shift(uint32_t lo, uint32_t hi) {
+  const int nb = 32 - __clz((int)(hi - lo));
+  return nb > 8 ? nb - 8 : 0;
+}
+// The state before any refinement, from the mass histogram.
+template <bool kBF16>
+__device__ __noinline__ TpState tp_state0(const Args& A, int j, float m, float c, float P) {
+  const int lane = threadIdx.x & 31;
+  TpState st;
+  u64 h[8];
+  const u64* H0 = tp_hist(A, j, 0) + lane * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __ldcg(H0 + i);
+  u64 tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += h[i];
+  st.zk = warp_sum_u64(tot);
+  const u64 target = (u64)ceil((double)P * (double)st.zk);
+  u64 bef;
+  tp_select(h, target, &st.b0, &bef);
+  st.above = bef;
+  st.rem = target - bef;
+  // the keys of bin b0: the bin falls as the key rises
+  const int b0 = st.b0;
+  const uint32_t kmin = kf<kBF16>(-INFINITY), kmax = kf<kBF16>(m);
+  st.lo = tp_first_true(kmin, kmax, [&](uint32_t key) { return tp_bin((tp_key_val<kBF16>(key) - m) * c) <= b0; });
+  st.hi = b0 == 0 ? kmax
+                  : tp_first_true(kmin, kmax,
+                                  [&](uint32_t key) { return tp_bin((tp_key_val<kBF16>(key) - m) * c) <= b0 - 1; }) -
+                        1u;
+  st.s = tp_shift(st.lo, st.hi);
+  return st;
+}
+// The state after one more level: the level's histogram h (8 bins a lane).
+__device__ __noinline__ TpState tp_state_step(TpState st, const u64 (&h)[8]) {
+  if (st.lo >= st.hi) return st;
+  int sb;
+  u64 ab;
+  tp_select(h, st.rem, &sb, &ab);
+  st.rem -= ab;
+  st.above += ab;
+  const uint32_t nhi = st.hi - ((uint32_t)sb << st.s);
+  const uint32_t wdt = (1u << st.s) - 1u;
+  st.lo = (nhi - st.lo >= wdt) ? nhi - wdt : st.lo;
+  st.hi = nhi;
+  st.s = tp_shift(st.lo, st.hi);
+  return st;
+}
+// The state a level pass starts from is kept in the unit's words (by the
+// warp holding the unit's first tile), so that later passes read it back
+// instead of walking every level again.
+__device__ __forceinline__ void tp_state_store(const Args& A, int j, int L, const TpState& st) {
+  const int lane = threadIdx.x & 31;
+  const u64 v = lane == 0 ? ((u64)st.hi << 32 | st.lo)
+              : lane == 1 ? ((u64)(uint32_t)st.b0 << 32 | (uint32_t)st.s)
+              : lane == 2 ? st.above
+              : lane == 3 ? st.rem
+                          : st.zk;
+  if (lane < kTpStateWords) __stcg(tp_state_at(A, j, L) + lane, v);
+}
+// The state after level L (L >= 0): the stored state of level L and that
+// level's histogram, read in one round trip.
+__device__ __noinline__ TpState tp_state_after(const Args& A, int j, int L) {
+  const int lane = threadIdx.x & 31;
+  const u64 sw = lane < kTpStateWords ? __ldcg(tp_state_at(A, j, L) + lane) : 0ull;
+  u64 h[8];
+  const u64* HL = tp_hist(A, j, 1 + L) + lane * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __ldcg(HL + i);
+  TpState st;
+  const u64 w0 = shfl_u64(sw, 0), w1 = shfl_u64(sw, 1);
+  st.lo = (uint32_t)w0;
+  st.hi = (uint32_t)(w0 >> 32);
+  st.s = (int)(uint32_t)w1;
+  st.b0 = (int)(uint32_t)(w1 >> 32);
+  st.above = shfl_u64(sw, 2);
+  st.rem = shfl_u64(sw, 3);
+  st.zk = shfl_u64(sw, 4);
+  return tp_state_step(st, h);
+}
+
+// The unit's max and validity from its tiles' records (a NaN or +inf, or no
+// finite entry: invalid; a record of another call: a pass gave up).
+struct TpMax {
+  float m;
+  uint32_t key;   // the max's order key, kTpBadKey, 0 (no finite entry) or kTpMissKey
+  bool live;      // valid, and every tile's max arrived
+  bool invalid;   // a NaN or +inf, or no finite entry
+  bool missing;   // a tile's record is not this call's
+};
+__device__ __forceinline__ TpMax tp_max_decode(uint32_t mk) {
+  TpMax r;
+  r.key = mk;
+  r.missing = mk == kTpMissKey;
+  r.invalid = !r.missing && (mk == kTpBadKey || mk == 0u);
+  r.live = !r.missing && !r.invalid;
+  r.m = r.live ? from_okey(mk) : 0.f;
+  return r;
+}
+__device__ __noinline__ TpMax tp_max_of(const Args& A, int uid, uint32_t tag) {
+  uint32_t mk = 0u;
+  bool ok = true;
+  for (int t = (int)(threadIdx.x & 31); t < A.NTA; t += 32) {
+    const u64 w = __ldcg(tp_rec(A, uid, t) + kTpMaxWord);
+    ok = ok && tag_ok(w, tag);
+    mk = max(mk, wu(w));
+  }
+  mk = __reduce_max_sync(kAll, mk);
+  return tp_max_decode(__all_sync(kAll, ok) ? mk : kTpMissKey);
+}
+// The same from the unit's summary word (after pass 2).
+__device__ __forceinline__ TpMax tp_max_from(u64 w, uint32_t tag) {
+  return tp_max_decode(tag_ok(w, tag) ? wu(w) : kTpMissKey);
+}
+
+// The warp's share of the call's top-p tiles: a contiguous range, so that
+// consecutive tiles of a warp mostly belong to one unit.
+__device__ __forceinline__ void tp_share(const Args& A, const TpPlan& T, uint32_t gw, uint32_t nwg, u64* t0, u64* t1) {
+  const u64 tiles = (u64)T.nU * (u64)A.NTA;
+  *t0 = tiles * gw / nwg;
+  *t1 = tiles * (gw + 1u) / nwg;
+}
+
+// Tile t of a logit row into the warp's shared memory at sb: the lane's
+// group r (8 entries) at sb + (32 r + lane) * G bytes, G = 16 (bf16) or 32
+// (fp32), copied by cp.async where the row is 16-byte aligned, else loaded
+// and stored (entries past V hold -inf).  Each lane reads back only its own
+// groups, so the copies need no warp-wide ordering.
+template <bool kBF16>
+__device__ __forceinline__ void tp_stage(const Args& A, size_t lrow, int t, unsigned char* sb) {
+  constexpr int G = kBF16 ? 16 : 32;
+  constexpr int es = kBF16 ? 2 : 4;
+  const int lane = threadIdx.x & 31;
+  const unsigned char* row = reinterpret_cast<const unsigned char*>(A.logits) + lrow * es;
+#pragma unroll
+  for (int r = 0; r < kTpNR; ++r) {
+    const int e0 = t * kTpET + (r * 32 + lane) * 8;
+    unsigned char* d = sb + (r * 32 + lane) * G;
+    if (A.vec_logits && e0 + 8 <= A.V) {
+      cp_async16(d, row + (size_t)e0 * es);
+      if constexpr (!kBF16) cp_async16(d + 16, row + (size_t)e0 * es + 16);
+    } else {
+      uint32_t w[kBF16 ? 4 : 8];
+      tp_group<kBF16>(A, lrow, e0, w);
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      if constexpr (!kBF16) d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+}
+// The matching draft probabilities (8 floats a group, 32 bytes) at sq.
+__device__ __forceinline__ void tp_stage_q(const Args& A, size_t qrow, int t, unsigned char* sq) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < kTpNR; ++r) {
+    const int e0 = t * kTpET + (r * 32 + lane) * 8;
+    unsigned char* d = sq + (r * 32 + lane) * 32;
+    if (A.vec_q && e0 + 8 <= A.V) {
+      cp_async16(d, A.q + qrow + e0);
+      cp_async16(d + 16, A.q + qrow + e0 + 4);
+    } else {
+      float qv[8];
+      load_q8(A, qrow, e0, qv);
+      float4* d4 = reinterpret_cast<float4*>(d);
+      d4[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      d4[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+}
+template <bool kBF16>
+__device__ __forceinline__ void tp_row(const unsigned char* sb, int r, uint32_t (&w)[kBF16 ? 4 : 8]) {
+  constexpr int G = kBF16 ? 16 : 32;
+  const uint4* s = reinterpret_cast<const uint4*>(sb + (r * 32 + (int)(threadIdx.x & 31)) * G);
+  const uint4 a = s[0];
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  if constexpr (!kBF16) {
+    const uint4 b = s[1];
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+}
+
+// Pass 1: tile maxima.
+template <bool kBF16>
+__device__ __noinline__ void tp_max_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg) {
+  const int lane = threadIdx.x & 31;
+  u64 t0, t1;
+  tp_share(A, T, gw, nwg, &t0, &t1);
+  int cj = -1;
+  TpUnit U;
+  for (u64 tt = t0; tt < t1; ++tt) {
+    const int j = (int)(tt / (u64)A.NTA), t = (int)(tt % (u64)A.NTA);
+    if (j != cj) {
+      cj = j;
+      U = tp_unit(A, T, j);
+    }
+    uint32_t w[kTpNR][kBF16 ? 4 : 8];
+    tp_tile<kBF16>(A, U.lrow, t, w);
+    float mx;
+    if constexpr (kBF16) {
+      uint32_t acc = w[0][0];
+#pragma unroll
+      for (int r = 0; r < kTpNR; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = max_nan_bf16x2(acc, w[r][i]);
+      mx = max_nan(bf16_lo(acc), bf16_hi(acc));
+    } else {
+      mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kTpNR; ++r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx = max_nan(mx, __uint_as_float(w[r][i]));
+    }
+    mx = warp_max_nan(mx);
+    if (lane == 0) {
+      const uint32_t key = (mx != mx || mx == INFINITY) ? kTpBadKey : (mx > -INFINITY ? okey(mx) : 0u);
+      __stcg(tp_rec(A, U.uid, t) + kTpMaxWord, tagw(tag, key));
+      if (U.has_q && A.vec_q) {
+        // the tile's draft probabilities, read by pass 5
+        const int e0 = t * kTpET;
+        const uint32_t bytes = (uint32_t)(min(kTpET, A.V - e0) * 4) & ~15u;
+        if (bytes) bulk_prefetch_l2(A.q + U.qrow + e0, bytes);
+      }
+    }
+  }
+}
+
+// floor(e * 2^40) for a normal e in (0, 1], as hi = bits 20 and up and
+// lo = bits 0..19, from the float's fields in 32-bit integer arithmetic:
+// e = m24 * 2^(E - 23), so floor(e * 2^40) = m24 * 2^(E + 17), a shift of
+// the 24-bit significand (left by at most 17, or right, truncating).
+__device__ __forceinline__ void tp_fixed(float e, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b = __float_as_uint(e);
+  const uint32_t m24 = (b & 0x7fffffu) | 0x800000u;
+  const int sh = (int)(b >> 23) - 127 + 17;
+  if (sh >= 0) {
+    hi = m24 >> (20 - sh);
+    lo = (m24 << sh) & 0xfffffu;
+  } else {
+    const uint32_t f = sh > -32 ? m24 >> (-sh) : 0u;
+    hi = f >> 20;
+    lo = f & 0xfffffu;
+  }
+}
+// A weight (hi, lo) into bin b of the warp's shared histogram (lo words at
+// hl[0..255], hi words at hl[256..511]).  Within one tile (2048 entries, each
+// word < 2^20 + 1) no word overflows, so the additions need no carry and
+// no returned value.
+__device__ __forceinline__ void tp_add(uint32_t* hl, int b, uint32_t hi, uint32_t lo) {
+  if (lo) atomicAdd(&hl[b], lo);
+  if (hi) atomicAdd(&hl[256 + b], hi);
+}
+// The warp's shared histogram added into a global one and cleared; `tail`
+// goes into bin 255.
+__device__ __forceinline__ void tp_flush(uint32_t* hl, u64* H, u64 tail) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int bin = lane * 8 + i;
+    u64 v = ((u64)hl[256 + bin] << 20) + hl[bin];
+    if (bin == 255) v += tail;
+    if (v) atomicAdd(H + bin, v);   // a reduction: the result is not used
+    hl[bin] = 0u;
+    hl[256 + bin] = 0u;
+  }
+  __syncwarp();
+}
+
+// Pass 2: the mass histogram.
+template <bool kBF16>
+__device__ __noinline__ void tp_mass_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
+                                          uint32_t* hl, unsigned char* sb) {
+  u64 t0, t1;
+  tp_share(A, T, gw, nwg, &t0, &t1);
+  int cj = -1;
+  TpUnit U;
+  TpMax M;
+  M.live = false;
+  M.m = 0.f;
+  for (u64 tt = t0; tt < t1; ++tt) {
+    const int j = (int)(tt / (u64)A.NTA), t = (int)(tt % (u64)A.NTA);
+    if (j != cj) {
+      cj = j;
+      U = tp_unit(A, T, j);
+      M = tp_max_of(A, U.uid, tag);
+      if (t == 0 && (threadIdx.x & 31) == 0) __stcg(tp_summary(A, j) + 5, tagw(tag, M.key));
+    }
+    if (!M.live) continue;
+    const float m = M.m, c = U.cfg.c;
+    tp_stage<kBF16>(A, U.lrow, t, sb);
+    u64 tail = 0;
+#pragma unroll 1
+    for (int r = 0; r < kTpNR; ++r) {
+      uint32_t w[kBF16 ? 4 : 8];
+      tp_row<kBF16>(sb, r, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float x = (tp_v<kBF16>(w, i) - m) * c;
+        const float e = ex2(x);
+        if (e > 0.f) {
+          uint32_t hi, lo;
+          tp_fixed(e, hi, lo);
+          const int b = tp_bin(x);
+          if (b < 255) tp_add(hl, b, hi, lo);
+          else tail += ((u64)hi << 20) | lo;
+        }
+      }
+    }
+    tp_flush(hl, tp_hist(A, j, 0), warp_sum_u64(tail));
+  }
+}
+
+// Pass 3, level L: the mass of the entries in the unit's key range, by key.
+template <bool kBF16>
+__device__ __noinline__ void tp_level_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
+                                           uint32_t* hl, unsigned char* sb, int L) {
+  const int lane = threadIdx.x & 31;
+  u64 t0, t1;
+  tp_share(A, T, gw, nwg, &t0, &t1);
+  int cj = -1;
+  TpUnit U;
+  TpMax M;
+  TpState st;
+  bool run = false;
+  for (u64 tt = t0; tt < t1; ++tt) {
+    const int j = (int)(tt / (u64)A.NTA), t = (int)(tt % (u64)A.NTA);
+    if (j != cj) {
+      cj = j;
+      U = tp_unit(A, T, j);
+      const u64 mw = __ldcg(tp_summary(A, j) + 5);
+      if (L > 0) st = tp_state_after(A, j, L - 1);
+      M = tp_max_from(mw, tag);
+      run = false;
+      if (M.live) {
+        if (L == 0) st = tp_state0<kBF16>(A, j, M.m, U.cfg.c, U.cfg.P);
+        if (t == 0) tp_state_store(A, j, L, st);
+        run = st.lo < st.hi;
+        // the sub-bins hold several keys: the next level is needed (said
+        // once, by the warp holding the unit's first tile)
+        if (run && st.s > 0 && t == 0 && lane == 0) atomicOr(&A.ws->tp_more, 1u << (L + 1));
+      }
+    }
+    if (!run) continue;
+    const float m = M.m, c = U.cfg.c;
+    const uint32_t span = st.hi - st.lo;
+    tp_stage<kBF16>(A, U.lrow, t, sb);
+#pragma unroll 1
+    for (int r = 0; r < kTpNR; ++r) {
+      uint32_t w[kBF16 ? 4 : 8];
+      tp_row<kBF16>(sb, r, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float v = tp_v<kBF16>(w, i);
+        const uint32_t key = kf<kBF16>(v);
+        if (key - st.lo <= span) {
+          const float x = (v - m) * c;
+          const float e = ex2(x);
+          if (e > 0.f && tp_bin(x) == st.b0) {
+            uint32_t hi, lo;
+            tp_fixed(e, hi, lo);
+            tp_add(hl, (int)((st.hi - key) >> st.s), hi, lo);
+          }
+        }
+      }
+    }
+    tp_flush(hl, tp_hist(A, j, 1 + L), 0ull);
+  }
+}
+
+// Pass 4: entries at the crossing key, per tile.  The warp holding a unit's
+// first tile also writes the unit's summary: the crossing key, how many
+// entries at it are kept (n_need: enough of them to cover the mass still
+// missing), Z_S over the kept set and whether P lies within the margin of
+// the mass before or at the crossing entry.
+template <bool kBF16>
+__device__ __noinline__ void tp_ties_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
+                                          unsigned char* sb) {
+  const int lane = threadIdx.x & 31;
+  u64 t0, t1;
+  tp_share(A, T, gw, nwg, &t0, &t1);
+  int cj = -1;
+  TpUnit U;
+  TpMax M;
+  uint32_t tkey = 0u;
+  for (u64 tt = t0; tt < t1; ++tt) {
+    const int j = (int)(tt / (u64)A.NTA), t = (int)(tt % (u64)A.NTA);
+    if (j != cj) {
+      cj = j;
+      U = tp_unit(A, T, j);
+      const u64 mw = __ldcg(tp_summary(A, j) + 5);
+      const TpState st = tp_state_after(A, j, T.nlev - 1);
+      M = tp_max_from(mw, tag);
+      tkey = st.hi;
+      if (M.live && t == 0) {
+        const float et = ex2((tp_key_val<kBF16>(tkey) - M.m) * U.cfg.c);
+        const u64 efx = mass_fixed(et);
+        u64 n = efx ? (st.rem + efx - 1u) / efx : 1u;
+        if (n == 0) n = 1;
+        const u64 zs_fx = st.above + n * efx;
+        const float Zs = (float)((double)zs_fx * (1.0 / 1099511627776.0));
+        const double P = (double)U.cfg.P;
+        const double at = (double)zs_fx / (double)st.zk, bef = (double)(zs_fx - efx) / (double)st.zk;
+        const uint32_t mf = (fabs(at - P) < 1e-6 || fabs(P - bef) < 1e-6) ? (uint32_t)SPEC_F_MARGIN_TOPP : 0u;
+        const uint32_t v = lane == 0 ? tkey : lane == 1 ? (uint32_t)n : lane == 2 ? __float_as_uint(Zs) : mf;
+        if (lane < 4) __stcg(tp_summary(A, j) + lane, tagw(tag, v));
+      }
+    }
+    if (!M.live) continue;
+    tp_stage<kBF16>(A, U.lrow, t, sb);
+    uint32_t n = 0;
+#pragma unroll 1
+    for (int r = 0; r < kTpNR; ++r) {
+      uint32_t w[kBF16 ? 4 : 8];
+      tp_row<kBF16>(sb, r, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) n += kf<kBF16>(tp_v<kBF16>(w, i)) == tkey ? 1u : 0u;
+    }
+    n = __reduce_add_sync(kAll, n);
+    if (lane == 0) __stcg(tp_rec(A, U.uid, t), tagw(tag, n));
+  }
+}
+
+// Ties at the crossing key in tiles [0, t) of a unit (tile records of pass 4).
+__device__ __forceinline__ u64 tp_ties_before(const Args& A, int uid, int t, uint32_t tag, bool* ok) {
+  const int lane = threadIdx.x & 31;
+  u64 s = 0;
+  bool good = true;
+  for (int i = lane; i < t; i += 32) {
+    const u64 wd = __ldcg(tp_rec(A, uid, i));
+    good = good && tag_ok(wd, tag);
+    s += wu(wd);
+  }
+  *ok = __all_sync(kAll, good);
+  return warp_sum_u64(s);
+}
+
+// Pass 5: alpha and the level-1 races of each tile over the kept set.
+template <bool kBF16>
+__device__ __noinline__ void tp_tiles_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
+                                           unsigned char* sb, unsigned char* sq) {
+  const int lane = threadIdx.x & 31;
+  u64 t0, t1;
+  tp_share(A, T, gw, nwg, &t0, &t1);
+  int cj = -1;
+  TpUnit U;
+  TpMax M;
+  uint32_t tkey = 0u;
+  u64 n_need = 0;
+  float invZ = 0.f;
+  for (u64 tt = t0; tt < t1; ++tt) {
+    const int j = (int)(tt / (u64)A.NTA), t = (int)(tt % (u64)A.NTA);
+    TLS((int)gw, 0);
+    if (j != cj) {
+      cj = j;
+      U = tp_unit(A, T, j);
+      // the unit's summary: crossing key, n_need, Z_S (pass 4) and max (pass 2)
+      const u64 sw = lane < 6 ? __ldcg(tp_summary(A, j) + lane) : 0ull;
+      const bool sok = __all_sync(kAll, lane > 3 || tag_ok(sw, tag));
+      M = tp_max_from(shfl_u64(sw, 5), tag);
+      if (!sok) M.live = false;   // the settle finds the summary missing too
+      tkey = __shfl_sync(kAll, wu(sw), 0);
+      n_need = __shfl_sync(kAll, wu(sw), 1);
+      invZ = 1.0f / __uint_as_float(__shfl_sync(kAll, wu(sw), 2));
+      TLS((int)gw, 2);
+    }
+    if (!M.live) continue;
+    const float m = M.m, c = U.cfg.c;
+    bool ok;
+    const u64 pre = tp_ties_before(A, U.uid, t, tag, &ok);
+    const u64 own = __ldcg(tp_rec(A, U.uid, t));
+    const u64 cnt = wu(own);
+    // the tile's ties are all kept, none, or its first n_need - pre; the
+    // tile holding the n_need-th tie ranks its ties and names that one
+    const bool all_ties = pre + cnt <= n_need;
+    const bool boundary = pre < n_need && n_need <= pre + cnt;
+    TLS((int)gw, 3);
+    tp_stage<kBF16>(A, U.lrow, t, sb);
+    if (U.has_q) tp_stage_q(A, U.qrow, t, sq);
+    TLS((int)gw, 4);
+    uint32_t run = (uint32_t)pre;   // ties before the current group row
+    uint32_t last_kept = 0xffffffffu;
+    float a0 = 0.f, a1 = 0.f;
+    float myW = 0.f, myU = 0.f, myP = 0.f;   // lane r: the sums of block r of the tile
+#pragma unroll 1
+    for (int r = 0; r < kTpNR; ++r) {
+      uint32_t w[kBF16 ? 4 : 8];
+      tp_row<kBF16>(sb, r, w);
+      float q[8];
+      if (U.has_q) {
+        const float4* s4 = reinterpret_cast<const float4*>(sq + (r * 32 + lane) * 32);
+        const float4 qa = s4[0], qb = s4[1];
+        q[0] = qa.x; q[1] = qa.y; q[2] = qa.z; q[3] = qa.w;
+        q[4] = qb.x; q[5] = qb.y; q[6] = qb.z; q[7] = qb.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0.f;
+      }
+      uint32_t rank = 0u;
+      if (boundary) {
+        uint32_t cr = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cr += kf<kBF16>(tp_v<kBF16>(w, i)) == tkey ? 1u : 0u;
+        uint32_t tot;
+        rank = run + warp_excl_scan_u32(cr, &tot);
+        run += tot;
+      }
+      float ws = 0.f, us = 0.f, ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float v = tp_v<kBF16>(w, i);
+        const uint32_t key = kf<kBF16>(v);
+        bool in = key > tkey;
+        if (key == tkey) {
+          if (boundary) {
+            in = (u64)rank < n_need;
+            if ((u64)rank + 1u == n_need) last_kept = (uint32_t)(t * kTpET + (r * 32 + lane) * 8 + i);
+            ++rank;
+          } else {
+            in = all_ties;
+          }
+        }
+        const float e = in ? ex2((v - m) * c) : 0.f;
+        if (U.has_q) {
+          const float p = e * invZ;
+          if (i & 1) a1 += fminf(p, q[i]);
+          else a0 += fminf(p, q[i]);
+          const float wv = fmaxf(p - q[i], 0.f);
+          if (wv > 0.f) {
+            ws += wv;
+            us += wv + 2.0f * q[i];
+          }
+        }
+        if (e > 0.f) ps += e;
+      }
+      const float W = U.has_q ? warp_sum(ws) : 0.f;
+      const float Uq = U.has_q ? warp_sum(us) : 0.f;
+      const float WP = warp_sum(ps);
+      if (lane == r) {
+        myW = W;
+        myU = Uq;
+        myP = WP;
+      }
+    }
+    // one step of each level-1 race per block: lane r for block t * 8 + r
+    Race rr, rp;
+    race_init(rr);
+    race_init(rp);
+    if (lane < kTpNR && (myW > 0.f || myP > 0.f)) {
+      const uint32_t blk = (uint32_t)(t * kTpNR + lane);
+      const uint32_t word = block_word(A, U.row, U.pos, blk);
+      if (myW > 0.f) race_consider(rr, myW, myU - myW, blk, word);
+      if (myP > 0.f) race_consider(rp, myP, 0.f, blk, word);
+    }
+    if (U.has_q) warp_race_merge(rr);
+    warp_race_merge(rp);
+    TLS((int)gw, 5);
+    if (boundary) {
+      last_kept = __reduce_min_sync(kAll, last_kept);
+      if (lane == 0) __stcg(tp_summary(A, j) + 4, tagw(tag, last_kept));
+    }
+    const float alpha = U.has_q ? warp_sum(a0 + a1) : 0.f;
+    // a tile whose tie counts were not all there writes no record: the
+    // settle then finds an old tag and gives the unit up
+    const uint32_t v = lane == 1 ? __float_as_uint(alpha)
+                     : lane == 2 ? __float_as_uint(rr.s1)
+                     : lane == 3 ? __float_as_uint(rr.t1)
+                     : lane == 4 ? __float_as_uint(rr.s2)
+                     : lane == 5 ? __float_as_uint(rr.t2)
+                     : lane == 6 ? rr.v1
+                     : lane == 7 ? __float_as_uint(rp.s1)
+                     : lane == 8 ? __float_as_uint(rp.t1)
+                     : lane == 9 ? __float_as_uint(rp.s2)
+                     : lane == 10 ? __float_as_uint(rp.t2)
+                                  : rp.v1;
+    if (ok && tag_ok(own, tag) && lane >= 1 && lane <= 11) __stcg(tp_rec(A, U.uid, t) + lane, tagw(tag, v));
+    TLS((int)gw, 6);
+  }
+}
+
+__device__ __forceinline__ Race tp_race_of(const u64* R, bool* ok, uint32_t tag) {
+  Race r;
+  const u64 w0 = __ldcg(R), w1 = __ldcg(R + 1), w2 = __ldcg(R + 2), w3 = __ldcg(R + 3), w4 = __ldcg(R + 4);
+  *ok = *ok && tag_ok(w0, tag) && tag_ok(w1, tag) && tag_ok(w2, tag) && tag_ok(w3, tag) && tag_ok(w4, tag);
+  r.s1 = wf(w0);
+  r.t1 = wf(w1);
+  r.s2 = wf(w2);
+  r.t2 = wf(w3);
+  r.v1 = wu(w4);
+  r.s1lo = r.s1 * 0.99999905f;
+  return r;
+}
+
+// Pass 6: one warp settles a unit.
+template <bool kBF16>
+__device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
+                                            bool failed) {
+  const int lane = threadIdx.x & 31;
+  for (int j = (int)gw; j < T.nU; j += (int)nwg) {
+    const TpUnit U = tp_unit(A, T, j);
+    if (failed) {
+      commit_record(A, tag, U.uid, U.row, empty_record(SPEC_F_TIMEOUT));
+      continue;
+    }
+    // the summary and the tiles' alphas and races, in one round trip
+    const u64 sw = lane < 6 ? __ldcg(tp_summary(A, j) + lane) : 0ull;
+    bool ok = lane > 4 || tag_ok(sw, tag);
+    float asum = 0.f;
+    Race rr, rp;
+    race_init(rr);
+    race_init(rp);
+    for (int t = lane; t < A.NTA; t += 32) {
+      const u64* R = tp_rec(A, U.uid, t);
+      const u64 wa = __ldcg(R + 1);
+      ok = ok && tag_ok(wa, tag);
+      asum += wf(wa);
+      if (U.has_q) race_merge(rr, tp_race_of(R + 2, &ok, tag));
+      race_merge(rp, tp_race_of(R + 7, &ok, tag));
+    }
+    const TpMax M = tp_max_from(shfl_u64(sw, 5), tag);
+    if (!M.live) {
+      commit_record(A, tag, U.uid, U.row, empty_record(M.missing ? SPEC_F_TIMEOUT : SPEC_F_NAN));
+      continue;
+    }
+    if (!__all_sync(kAll, ok)) {
+      // a record of this unit is missing (a pass gave up)
+      commit_record(A, tag, U.uid, U.row, empty_record(SPEC_F_TIMEOUT));
+      continue;
+    }
+    const RowCfg& cfg = U.cfg;
+    const float m = M.m, c = cfg.c;
+    const uint32_t tkey = __shfl_sync(kAll, wu(sw), 0);
+    const float Zs = __uint_as_float(__shfl_sync(kAll, wu(sw), 2));
+    const uint32_t flags = __shfl_sync(kAll, wu(sw), 3);
+    Thresh th;
+    th.tkey = full_key<kBF16>(tkey);
+    th.tidx = __shfl_sync(kAll, wu(sw), 4);
+    const float alpha_v = U.has_q ? warp_sum(asum) : 0.f;
+    if (U.has_q) warp_race_merge(rr);
+    warp_race_merge(rp);
+    const float invZ = 1.0f / Zs, lnZ = logf(Zs);
+    AcceptInfo ai;
+    ai.accept = false;
+    ai.valid = true;
+    ai.margin = false;
+    ai.lx = 0.f;
+    bool need_race = !U.has_q;
+    if (U.has_q) {
+      ai = accept_test(A, U.row, U.pos, kBF16, false, 0, m, c, Zs, &th);
+      need_race = !ai.accept;
+    }
+    uint32_t draw_flags = 0u;
+    uint32_t y = 0xffffffffu;
+    float ly = 0.f;
+    if (need_race) {
+      Race l1 = rp;
+      int mode = U.has_q ? RW_P : RW_BONUS;
+      if (U.has_q) {
+        if (rr.s1 >= 0.f) {
+          l1 = rr;
+          mode = RW_RESIDUAL;
+        } else {
+          draw_flags |= SPEC_F_RESIDUAL_EMPTY;
+        }
+      }
+      if (l1.s1 >= 0.f) {
+        const Race l2 = race_in_block<kBF16>(A, U.row, U.pos, l1.v1, m, c, invZ, mode, &th, &ly);
+        if (l2.s1 >= 0.f) y = l2.v1;
+        if (draw_margin(l1) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
+      }
+    }
+    UnitRecord rec = empty_record(flags);
+    if (lane == 0) {
+      if (U.has_q) {
+        if (!ai.valid) rec.flags |= SPEC_F_BAD_TOKEN;
+        if (ai.margin) rec.flags |= SPEC_F_MARGIN_ACCEPT;
+        rec.accept = ai.accept ? 1 : 0;
+        rec.lp_x = ai.valid ? (ai.lx - m) * cfg.invT - lnZ : 0.f;
+        rec.alpha = alpha_v;
+      }
+      if (need_race) {
+        if (y < (uint32_t)A.V) {
+          rec.y = (int32_t)y;
+          rec.lp_y = (ly - m) * cfg.invT - lnZ;
+        } else {
+          // no entry won (not reachable: the kept set holds the max)
+          rec.flags |= SPEC_F_TIMEOUT;
+        }
+        rec.draw_flags = draw_flags;
+      }
+    }
+    commit_record(A, tag, U.uid, U.row, rec);
+  }
+}
+
+// Every CTA arrives before any leaves (the launch is cooperative, so all are
+// resident).  The count only grows within a call: barrier i waits for
+// i x n_ctas arrivals.  Bounded: a wait that gives up sets ERR_BARRIER.
+__device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&A.ws->bar, 1u);
+    long long spins = 0;
+    while (load_acquire(&A.ws->bar) < target) {
+      if (++spins > 16ll * kSpinLimit) {
+        atomicOr(&A.ws->error, (uint32_t)ERR_BARRIER);
+        break;
+      }
+      __nanosleep(spins > 16 ? 128 : 16);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// The passes, run by every thread of every CTA.  `buf` is the warp's 16 KB
+// of shared memory (histogram, then staged tiles); `usable` is false for a
+// warp whose buffers may still receive a copy that gave up (it then takes no
+// tiles, and the units come back with SPEC_F_TIMEOUT).
+template <bool kBF16>
+__device__ __noinline__ void topp_passes(const Args& A, TpPlan T, uint32_t tag, unsigned char* buf, bool usable) {
+  const uint32_t w = threadIdx.x >> 5;
+  const uint32_t nwg = (uint32_t)A.n_ctas * (uint32_t)(blockDim.x >> 5);
+  const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + w;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(buf);   // 2 KB
+  unsigned char* sb = buf + 8192;                      // the staged tile (4 KB bf16, 8 KB fp32)
+  unsigned char* sl = buf;                             // pass 5: logits here, q in the second half
+  uint32_t nb = 0;
+  const uint32_t n = (uint32_t)A.n_ctas;
+  // timeline stamps (instrumented builds): barrier exits of CTA 0, pass ends per warp
+  auto stamp_bar = [&]() { if (threadIdx.x == 0 && blockIdx.x == 0) TL(TL_TP, (int)nb, 16); };
+  auto stamp_pass = [&](int p) { if ((threadIdx.x & 31) == 0) TL(TL_TP_WARP + p * 2048, (int)gw, 2048); };
+  for (int i = (int)(threadIdx.x & 31); i < 2 * kTpBins / 4; i += 32)
+    reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncwarp();
+  stamp_bar();
+  grid_barrier(A, ++nb * n);   // the roles are done and the scratch is zero everywhere
+  stamp_bar();
+  if (usable) tp_max_pass<kBF16>(A, T, tag, gw, nwg);
+  stamp_pass(0);
+  grid_barrier(A, ++nb * n);
+  stamp_bar();
+  if (usable) tp_mass_pass<kBF16>(A, T, tag, gw, nwg, hist, sb);
+  stamp_pass(1);
+  grid_barrier(A, ++nb * n);
+  stamp_bar();
+  int L = 0;
+  for (; L < kTpLevels; ++L) {
+    if (L > 0 && (__ldcg(&A.ws->tp_more) & (1u << L)) == 0u) break;
+    if (usable) tp_level_pass<kBF16>(A, T, tag, gw, nwg, hist, sb, L);
+    stamp_pass(2 + L);
+    grid_barrier(A, ++nb * n);
+    stamp_bar();
+  }
+  T.nlev = L;
+  if (usable) tp_ties_pass<kBF16>(A, T, tag, gw, nwg, sb);
+  stamp_pass(6);
+  grid_barrier(A, ++nb * n);
+  stamp_bar();
+  if (usable) tp_tiles_pass<kBF16>(A, T, tag, gw, nwg, sl, buf + 8192);
+  stamp_pass(7);
+  grid_barrier(A, ++nb * n);
+  stamp_bar();
+  const bool failed = (__ldcg(&A.ws->error) & (uint32_t)(ERR_BARRIER | ERR_COPY_WAIT)) != 0u;
+  tp_settle_pass<kBF16>(A, T, tag, gw, nwg, failed);
+  stamp_pass(5);
+}
+
+}  // namespace specv

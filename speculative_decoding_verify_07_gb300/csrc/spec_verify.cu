@@ -75,6 +75,7 @@ int verify_launch(const void* logits, int logits_dtype, const float* draft_probs
   A.urec = reinterpret_cast<u64*>(ws + L.urec);
   A.order = reinterpret_cast<uint32_t*>(ws + L.order);
   A.done = reinterpret_cast<u64*>(ws + L.done);
+  A.tp = reinterpret_cast<u64*>(ws + L.tp);
   if (fc) A.fc = *fc;
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);

@@ -168,6 +168,30 @@ def test_parity_large_topk_and_topp_only():
         compare(run_gpu(case), run_oracle(case), mode)
 
 
+def test_parity_topp_fp32_refinement_levels():
+    # fp32 keys are dense: the crossing bin spans many keys and takes
+    # several refinement levels; coarse rows put exact ties at the crossing
+    rng = np.random.default_rng(321)
+    for V in (40000, 2048 * 3 + 5):
+        case = _random_case(rng, B=8, k=2, V=V, dtype="f32", param_mode="topp")
+        compare(run_gpu(case), run_oracle(case), f"top-p fp32 V={V}")
+
+
+def test_parity_topp_rows_above_the_shared_order_limit():
+    # 300 rows (the row order then lives in the workspace), every class, and
+    # top-p rows holding NaN, +inf and all -inf positions
+    rng = np.random.default_rng(77)
+    case = _random_case(rng, B=300, k=2, V=3000, dtype="bf16", param_mode="mix")
+    topp = [b for b in range(300) if b % 8 == 3]
+    case.logits[topp[0], 1, 17] = np.nan
+    case.logits[topp[1], 0, 9] = np.inf
+    case.logits[topp[2], 2, :] = -np.inf
+    gpu = run_gpu(case)
+    compare(gpu, run_oracle(case), "300 rows")
+    for r in topp[:3]:
+        assert gpu["flags"][r] & ov.F_NAN and gpu["accept_len"][r] == 0
+
+
 def test_invalid_inputs_set_flags():
     rng = np.random.default_rng(9)
     case = _random_case(rng, B=8, k=2, V=513, dtype="f32", param_mode="temp")
