@@ -556,19 +556,11 @@ __device__ __forceinline__ float accept_uniform(const Args& A, int row, int pos)
 // sign of u*q - p taken exactly by one fma.  p(x) = exp((l_x - m) / T) / Z
 // when x is kept (kept_th == nullptr keeps everything); greedy: p(x) = 1 if
 // x is the argmax, else 0.
-static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, int pos, bool bf16, bool greedy, int am,
-                                                      float m, float c, float Zs, const Thresh* kept_th) {
-  AcceptInfo ai;
-  ai.x = A.drafts[(size_t)row * A.k + pos];
-  ai.valid = ai.x >= 0 && ai.x < A.V;
-  ai.lx = 0.f;
+// The decision itself, for a draft whose x, validity, l_x and q(x) are in ai.
+static __device__ __noinline__ AcceptInfo accept_decide(const Args& A, int row, int pos, AcceptInfo ai, bool greedy,
+                                                        int am, float m, float c, float Zs, const Thresh* kept_th) {
   ai.px = 0.f;
-  ai.qx = 0.f;
-  const size_t lrow = ((size_t)row * (A.k + 1) + pos) * (size_t)A.V;
-  const size_t qrow = ((size_t)row * A.k + pos) * (size_t)A.V;
   if (ai.valid) {
-    ai.lx = load_logit(A, bf16, lrow + ai.x);
-    ai.qx = A.q[qrow + ai.x];
     if (greedy) {
       ai.px = (ai.x == am) ? 1.0f : 0.0f;
     } else {
@@ -581,6 +573,27 @@ static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, in
   ai.accept = d < 0.0f;
   ai.margin = (ai.px > 0.0f && ai.px < 1.0f && fabsf(d) < kMargin);
   return ai;
+}
+// x, l_x and q(x) of the draft at (row, pos) (ai.valid: x in [0, V)).
+__device__ __forceinline__ AcceptInfo accept_load(const Args& A, int row, int pos, bool bf16, int x) {
+  AcceptInfo ai;
+  ai.x = x;
+  ai.valid = x >= 0 && x < A.V;
+  ai.lx = 0.f;
+  ai.qx = 0.f;
+  ai.px = 0.f;
+  ai.accept = false;
+  ai.margin = false;
+  if (ai.valid) {
+    ai.lx = load_logit(A, bf16, ((size_t)row * (A.k + 1) + pos) * (size_t)A.V + x);
+    ai.qx = A.q[((size_t)row * A.k + pos) * (size_t)A.V + x];
+  }
+  return ai;
+}
+static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, int pos, bool bf16, bool greedy, int am,
+                                                      float m, float c, float Zs, const Thresh* kept_th) {
+  const AcceptInfo ai = accept_load(A, row, pos, bf16, A.drafts[(size_t)row * A.k + pos]);
+  return accept_decide(A, row, pos, ai, greedy, am, m, c, Zs, kept_th);
 }
 
 // Race uniform words.  Entry v at position pos: counter (v >> 2, pos, row,

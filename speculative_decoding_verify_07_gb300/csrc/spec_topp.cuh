@@ -697,7 +697,7 @@ struct TpSum {
   float Zs;
 };
 template <bool kBF16>
-__device__ __forceinline__ TpSum tp_sum_of(const TpState& st, float m, const RowCfg& cfg) {
+__device__ __forceinline__ TpSum tp_sum_of(const TpState& st, float m, const RowCfg& cfg, bool with_margin) {
   TpSum r;
   r.tkey = st.hi;
   const u64 efx = mass_fixed(ex2((tp_key_val<kBF16>(st.hi) - m) * cfg.c));
@@ -706,9 +706,12 @@ __device__ __forceinline__ TpSum tp_sum_of(const TpState& st, float m, const Row
   r.n_need = (uint32_t)n;
   const u64 zs_fx = st.above + n * efx;
   r.Zs = (float)((double)zs_fx * (1.0 / 1099511627776.0));
-  const double P = (double)cfg.P;
-  const double at = (double)zs_fx / (double)st.zk, bef = (double)(zs_fx - efx) / (double)st.zk;
-  r.mf = (fabs(at - P) < 1e-6 || fabs(P - bef) < 1e-6) ? (uint32_t)SPEC_F_MARGIN_TOPP : 0u;
+  r.mf = 0u;
+  if (with_margin) {
+    const double P = (double)cfg.P;
+    const double at = (double)zs_fx / (double)st.zk, bef = (double)(zs_fx - efx) / (double)st.zk;
+    if (fabs(at - P) < 1e-6 || fabs(P - bef) < 1e-6) r.mf = SPEC_F_MARGIN_TOPP;
+  }
   return r;
 }
 __device__ __forceinline__ void tp_sum_store(const Args& A, int j, uint32_t tag, const TpSum& r) {
@@ -739,7 +742,7 @@ __device__ __noinline__ void tp_ties_pass(const Args& A, const TpPlan& T, uint32
       const TpState st = tp_state_after(A, j, T.nlev - 1);
       M = tp_max_from(mw, tag);
       tkey = st.hi;
-      if (M.live && t == 0) tp_sum_store(A, j, tag, tp_sum_of<kBF16>(st, M.m, U.cfg));
+      if (M.live && t == 0) tp_sum_store(A, j, tag, tp_sum_of<kBF16>(st, M.m, U.cfg, true));
     }
     if (!M.live) continue;
     const float tval = tp_key_val<kBF16>(tkey);   // the entries at the crossing key hold this value
@@ -825,7 +828,7 @@ __device__ __noinline__ void tp_tiles_pass(const Args& A, const TpPlan& T, uint3
         const TpState st = tp_state_after(A, j, T.nlev - 1);
         M = tp_max_from(mw, tag);
         if (M.live) {
-          const TpSum sm = tp_sum_of<kBF16>(st, M.m, U.cfg);
+          const TpSum sm = tp_sum_of<kBF16>(st, M.m, U.cfg, t == 0);
           if (t == 0) tp_sum_store(A, j, tag, sm);
           tkey = sm.tkey;
           n_need = sm.n_need;
@@ -967,7 +970,8 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
       commit_record(A, tag, U.uid, U.row, empty_record(SPEC_F_TIMEOUT));
       continue;
     }
-    // the summary and the tiles' alphas and races, in one round trip
+    // the summary, the draft and the tiles' alphas and races, in one round trip
+    const int xd = U.has_q ? A.drafts[(size_t)U.row * A.k + U.pos] : -1;
     const u64 sw = lane < 6 ? __ldcg(tp_summary(A, j) + lane) : 0ull;
     bool ok = lane > 4 || tag_ok(sw, tag);
     float asum = 0.f;
@@ -994,6 +998,7 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
     }
     const RowCfg& cfg = U.cfg;
     const float m = M.m, c = cfg.c;
+    AcceptInfo ai = accept_load(A, U.row, U.pos, kBF16, xd);   // in flight during the merges
     const uint32_t tkey = __shfl_sync(kAll, wu(sw), 0);
     const float Zs = __uint_as_float(__shfl_sync(kAll, wu(sw), 2));
     const uint32_t flags = __shfl_sync(kAll, wu(sw), 3);
@@ -1004,14 +1009,9 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
     if (U.has_q) warp_race_merge(rr);
     warp_race_merge(rp);
     const float invZ = 1.0f / Zs, lnZ = logf(Zs);
-    AcceptInfo ai;
-    ai.accept = false;
-    ai.valid = true;
-    ai.margin = false;
-    ai.lx = 0.f;
     bool need_race = !U.has_q;
     if (U.has_q) {
-      ai = accept_test(A, U.row, U.pos, kBF16, false, 0, m, c, Zs, &th);
+      ai = accept_decide(A, U.row, U.pos, ai, false, 0, m, c, Zs, &th);
       need_race = !ai.accept;
     }
     uint32_t draw_flags = 0u;
