@@ -309,8 +309,9 @@ def cpu_oracle_baseline(n_rows_all=None, n_rows_1t=16, workers=None):
     t1 = _ORACLE_INPUT.rows(list(range(n_rows_1t)))
     return {
         "value": n_done / wall, "unit": "rows/s", "cores": workers, "kind": "oracle",
-        "sample": f"oracle verify (NumPy float64) on {n_done} of the 64 mixed rows, one process per host "
-                  f"core ({workers} cores from sched_getaffinity), {wall:.2f} s wall",
+        "sample": f"oracle verify (NumPy float64) on {n_done} rows cycling over the 64 mixed rows, one process "
+                  f"per host core ({workers} cores from sched_getaffinity), {wall:.2f} s wall "
+                  f"({wall * workers:.1f} core-seconds)",
         "single_thread": {"value": n_rows_1t / t1, "unit": "rows/s", "cores": 1,
                           "sample": f"{n_rows_1t} rows in one process, {t1 * 1e3 / n_rows_1t:.1f} ms/row"},
     }
