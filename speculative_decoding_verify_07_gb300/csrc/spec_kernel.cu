@@ -4,7 +4,7 @@
 // is resident, so warps may wait on one another; every such wait is
 // bounded).  CTAs take one of two roles, so that each SM runs one kind of
 // code and keeps it in its instruction cache:
-//   * Stream CTAs (about 9 in 10).  Each of their 12 warps owns two 8 KB
+//   * Stream CTAs (5 in 6).  Each of their 12 warps owns two 8 KB
 //     shared-memory buffers and has the copy engine fill one (cp.async.bulk
 //     completed on an mbarrier) while it reduces the other.  The tiles of
 //     all units form one sequence of segments: A tiles of small top-k rows
@@ -22,7 +22,7 @@
 //     and the level-1 race of the residual from the unit's published state.
 //     After a tile's record the warp adds one to the unit's tile count (a
 //     reduction nobody waits for).
-//   * Settle CTAs (about 1 in 10, every stride-th block).  Their warps take
+//   * Settle CTAs (1 in 6, every stride-th block).  Their warps take
 //     the settle tasks -- one per unit after its A tiles, one per drafted
 //     unfiltered unit after its B tiles -- in the order of the sequence,
 //     task t to settle CTA t mod (settle CTAs); a warp waits for its task's tile
@@ -30,9 +30,11 @@
 //     come in the order their tiles do, and a B tile only waits for a state
 //     that an earlier task publishes, so every wait ends.  The last settled
 //     unit of a row resolves its accept chain and writes the row's outputs.
-// Rows that need a global threshold search (spec_general.cuh) are taken
-// last by the CTAs' first 256 threads, and the fused commit (spec_fused.cuh)
-// follows.  Results pass between warps as 64-bit words tagged with the
+// Rows with top-p and no top-k then run the grid-wide top-p passes
+// (spec_topp.cuh, every warp of every CTA, grid barriers between passes);
+// rows with a top-k above the candidate-list limit are taken next by the
+// CTAs' first 256 threads (spec_general.cuh), and the fused commit
+// (spec_fused.cuh) follows.  Results pass between warps as 64-bit words tagged with the
 // call's epoch; reductions have a fixed order and no floating-point atomics
 // are used, so results are bit-reproducible.
 #include <cuda_runtime.h>
