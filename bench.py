@@ -34,8 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "spec-verify rows/s at V=151936,k=2; achieved HBM GB/s vs GB300 peak"
 # spec_verify launches one cooperative kernel; its sources
-VERIFY_SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_settle.cuh", "spec_general.cuh",
-                  "spec_common.cuh", "spec_device.cuh"]
+VERIFY_SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_settle.cuh", "spec_general.cuh", "spec_topp.cuh",
+                  "spec_fused.cuh", "spec_common.cuh", "spec_device.cuh"]
 VERIFY_LAUNCHES = 1
 B, K, V = 64, 2, 151936
 N_SETS = 4   # rotating verify input sets (each ~136 MB, together > L2)
@@ -406,6 +406,44 @@ def _component(sets, inps, n_steps, warmup, dev, peak, peak_kind, name, src_hash
             "mean_accept_len": float(out.accept_len.float().mean().item())}
 
 
+def draft_component(dev, peak, peak_kind, n_sets=8, n_steps=20, warmup=5):
+    """spec_draft_sample on one position of the mixed workload: 64 rows x
+    151936 bf16 draft logits with the mixed sampler settings, q written in
+    full (8 input sets of 19.4 MB rotate: more than L2 holds).  Algorithmic
+    bytes per call: the logits read once and q written once (6 bytes an
+    entry) plus the small per-row I/O."""
+    import torch
+
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    from speculative_decoding_verify_07_gb300 import synth
+    sets = []
+    for i in range(n_sets):
+        inp = synth.make_mixed(seed_offset=100 * i)
+        sets.append((torch.from_numpy(np.ascontiguousarray(inp.logits[:, 0, :])).to(torch.bfloat16).to(dev),
+                     sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev), inp.seed + i))
+    B_, V_ = sets[0][0].shape
+    ws = sv.new_draft_workspace(B_, V_, dev)
+    out = sv.DraftOutputs(B_, V_, dev)
+    res = {}
+    for with_q in (True, False):
+        o = out if with_q else sv.DraftOutputs(B_, V_, dev, with_q=False)
+        fn = lambda i: sv.spec_draft_sample(sets[i % n_sets][0], sets[i % n_sets][1], sets[i % n_sets][2], 1,
+                                            out=o, workspace=ws, with_q=with_q)
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        t = _time_calls(fn, n_steps, torch.cuda.current_stream())
+        res[with_q] = t
+    nbytes = B_ * V_ * (2 + 4) + B_ * (16 + 12)
+    us = statistics.mean(res[True])
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"workload": "spec_draft_sample 64 rows x 151936 bf16, mixed sampler settings, q written",
+            "us": round(us, 2), "us_p50": round(statistics.median(res[True]), 2),
+            "us_tokens_only": round(statistics.mean(res[False]), 2), "rows_per_s": round(B_ / (us * 1e-6), 1),
+            "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1), "frac": round(ach / peak, 4), "peak": peak,
+            "peak_source": peak_kind, "launches": 2}
+
+
 def run_ours(args):
     import torch
 
@@ -517,6 +555,7 @@ def run_ours(args):
                                                                 "spec_verify_adversarial", v_hash)
         del ad_sets
         components["spec_commit"] = commit_component(dev, peak, peak_kind, acc)
+        components["draft_sample_64x151936"] = draft_component(dev, peak, peak_kind)
     value = job_rows_per_s(B * n, world, elapsed_ms * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,

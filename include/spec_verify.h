@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define SPEC_ABI_VERSION 3
+#define SPEC_ABI_VERSION 4
 
 /* Largest vocabulary and draft length accepted by spec_verify. */
 #define SPEC_MAX_V 524288
@@ -296,6 +296,50 @@ int spec_verify_commit(const void* logits, int logits_dtype, const float* draft_
                        size_t workspace_bytes, const float* verify_rec, const uint16_t* verify_conv,
                        const int32_t* cache_slot, float* cache_rec, uint16_t* cache_conv, int L, int H,
                        int Dk, int Dv, int W, int C, int slots, void* cuda_stream);
+
+/* spec_draft_workspace_size - bytes of device workspace spec_draft_sample
+ * needs for B rows over V entries (0 when B < 0 or V < 1); zero-filled
+ * before first use, left reusable by every call, as spec_verify's. */
+size_t spec_draft_workspace_size(int B, int V);
+
+/* spec_draft_sample - one draft step: sample x_j ~ q_j for B rows and write
+ * q_j, the distribution the verify later reads as draft_probs.
+ *
+ * Source: inclusionAI/AReno PR #550, "What does this PR do?" Phase 2 (the
+ * MTP layer drafts EAGLE-style, one position at a time, with the sampler
+ * settings of the target); areal-project/AReaL PR #1659 (EAGLE top-k draft
+ * tokens passed through to the verify).
+ *
+ * q_j is the sampler-equivalent distribution of the draft logits: the
+ * temperature, top-k, top-p filter and renormalisation of spec_verify's p,
+ * with the same total order, parameter rules and invalid-input rules.  x_j
+ * is drawn from q_j by spec_verify's two-level exponential race, on Philox
+ * streams of their own: the race uniform of entry v from counter
+ * (v >> 2, pos, R, 3), word v & 3, and of block b from counter
+ * (b >> 2, pos, R, 4), word b & 3, R = row_base + r.  So draft draws and the
+ * verify's accept and draw uniforms are independent, and a draft step is
+ * reproducible from (seed, row, pos).
+ * Inputs (device):
+ *   logits        [B, V] of logits_dtype: the draft logits at position pos.
+ *   params        [B] spec_params_t (the draft sampler's settings).
+ *   seed, row_base: as spec_verify; pos: the draft position (counter word 1).
+ * Outputs (device):
+ *   q             [B, V] float32: q_j (0 outside the kept set; one-hot at the
+ *                 argmax under greedy decoding; all 0 for an invalid row).
+ *                 May be NULL: the tokens alone (no second kernel).
+ *   tokens        [B] int32: x_j (-1 for an invalid row).
+ *   logprobs      [B] float32: ln q_j(x_j) as spec_verify reports a drawn
+ *                 token's logprob (the raw log-softmax under greedy decoding).
+ *   flags         [B] uint32: SPEC_F_* (NAN, BAD_PARAM, MARGIN_TOPP,
+ *                 MARGIN_DRAW, TIMEOUT).
+ * workspace / workspace_bytes: at least spec_draft_workspace_size(B, V).
+ * Errors: SPEC_E_NULL, SPEC_E_DIM, SPEC_E_DTYPE, SPEC_E_ALIGN,
+ *   SPEC_E_WORKSPACE, SPEC_E_ARCH, SPEC_E_CUDA; every argument is checked
+ *   before anything is enqueued.  B == 0 returns SPEC_OK. */
+int spec_draft_sample(const void* logits, int logits_dtype, const spec_params_t* params, uint64_t seed,
+                      uint32_t row_base, uint32_t pos, int B, int V, float* q, int32_t* tokens,
+                      float* logprobs, uint32_t* flags, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream);
 
 /* SPEC_ABI_VERSION of the loaded library. */
 int spec_version(void);

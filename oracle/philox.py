@@ -37,6 +37,8 @@ _MASK32 = np.uint64(0xFFFFFFFF)
 STREAM_ACCEPT = 0  # u_j for the accept test of draft j:   ctr = (0, j, row, 0), word 0
 STREAM_RACE = 1    # U_v for the race inside a block:      ctr = (v >> 2, pos, row, 1), word v & 3
 STREAM_BLOCK = 2   # U_b for the race among blocks:        ctr = (b >> 2, pos, row, 2), word b & 3
+STREAM_DRAFT_RACE = 3    # the draft sampler's entry race:    ctr = (v >> 2, pos, row, 3), word v & 3
+STREAM_DRAFT_BLOCK = 4   # the draft sampler's block race:    ctr = (b >> 2, pos, row, 4), word b & 3
 
 
 def seed_key(seed: int) -> tuple[int, int]:

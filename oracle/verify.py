@@ -167,7 +167,8 @@ def _best_two(s: np.ndarray):
     return i1, int(np.argmax(rest))
 
 
-def exponential_race(r: np.ndarray, seed: int, row: int, pos: int, unc: np.ndarray):
+def exponential_race(r: np.ndarray, seed: int, row: int, pos: int, unc: np.ndarray,
+                     streams=(philox.STREAM_RACE, philox.STREAM_BLOCK)):
     """Gumbel-max draw from the unnormalised weights r [AReno, "Per-step optimizations"].
 
     An exponential race: each competitor with weight w > 0 draws E = -ln U
@@ -183,6 +184,7 @@ def exponential_race(r: np.ndarray, seed: int, row: int, pos: int, unc: np.ndarr
 
     unc[v] is the magnitude whose relative error of 1e-6 bounds the error of
     r_v (p + q for a residual, p for a bonus draw); it sets the margin.
+    streams: the Philox stream words of the entry and the block uniforms.
     Returns (winner, margin_flag).
     """
     support = np.nonzero(r > 0)[0]
@@ -190,14 +192,14 @@ def exponential_race(r: np.ndarray, seed: int, row: int, pos: int, unc: np.ndarr
     ub, inv = np.unique(blocks, return_inverse=True)
     W = np.bincount(inv, weights=r[support])
     Wu = np.bincount(inv, weights=unc[support])
-    Eb = philox.race_exponentials(seed, row, pos, ub, stream=philox.STREAM_BLOCK)
+    Eb = philox.race_exponentials(seed, row, pos, ub, stream=streams[1])
     sb = W / Eb
     b1, b2 = _best_two(sb)
     margin = False
     if b2 >= 0 and sb[b1] - sb[b2] < MARGIN * (Wu[b1] / Eb[b1] + Wu[b2] / Eb[b2]):
         margin = True
     inb = support[blocks == ub[b1]]
-    E = philox.race_exponentials(seed, row, pos, inb)
+    E = philox.race_exponentials(seed, row, pos, inb, stream=streams[0])
     s = r[inb] / E
     i1, i2 = _best_two(s)
     if i2 >= 0 and s[i1] - s[i2] < MARGIN * (unc[inb[i1]] / E[i1] + unc[inb[i2]] / E[i2]):

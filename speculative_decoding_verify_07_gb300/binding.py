@@ -68,6 +68,10 @@ def _load():
     lib.spec_verify_commit.restype = i32
     lib.spec_verify_noalloc.argtypes = [vp, i32, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_noalloc.restype = i32
+    lib.spec_draft_workspace_size.argtypes = [i32, i32]
+    lib.spec_draft_workspace_size.restype = sz
+    lib.spec_draft_sample.argtypes = [vp, i32, vp, u64, u32, u32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_draft_sample.restype = i32
     lib.spec_philox4x32_10.argtypes = [vp, u64, vp, ctypes.c_int64, vp]
     lib.spec_philox4x32_10.restype = i32
     lib.spec_status_string.argtypes = [i32]
@@ -385,6 +389,57 @@ def spec_commit_swap(verify_rec, verify_conv, accept_len, slot_of_row, scratch_s
                               slots, _ptr(flags), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_commit_swap")
+
+
+class DraftOutputs:
+    def __init__(self, B: int, V: int, device, with_q: bool = True):
+        self.q = torch.empty((B, V), dtype=torch.float32, device=device) if with_q else None
+        self.tokens = torch.empty((B,), dtype=torch.int32, device=device)
+        self.logprobs = torch.empty((B,), dtype=torch.float32, device=device)
+        self.flags = torch.empty((B,), dtype=torch.int32, device=device)   # uint32 bit pattern
+
+
+def draft_workspace_size(B: int, V: int) -> int:
+    return int(LIB.spec_draft_workspace_size(int(B), int(V)))
+
+
+def new_draft_workspace(B: int, V: int, device) -> torch.Tensor:
+    """A zero-filled workspace for spec_draft_sample."""
+    return torch.zeros(max(draft_workspace_size(B, V), 16), dtype=torch.uint8, device=device)
+
+
+def spec_draft_sample(logits: torch.Tensor, params: torch.Tensor, seed: int, pos: int,
+                      out: DraftOutputs | None = None, workspace: torch.Tensor | None = None,
+                      stream=None, row_base: int = 0, with_q: bool = True) -> DraftOutputs:
+    """One draft step (see spec_draft_sample in spec_verify.h): logits [B, V]
+    float32 or bfloat16, params [B, 4] int32 from make_params(); draws x ~ q
+    and writes q (unless with_q is False)."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [B, V]")
+    B, V = logits.shape
+    dev = logits.device
+    if logits.dtype == torch.float32:
+        dt = SPEC_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = SPEC_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    _check(params, "params", torch.int32, (B, 4), dev)
+    if out is None:
+        out = DraftOutputs(B, V, dev, with_q)
+    if out.q is not None:
+        _check(out.q, "q", torch.float32, (B, V), dev)
+    if workspace is None:
+        workspace = new_draft_workspace(B, V, dev)
+    rc = LIB.spec_draft_sample(_ptr(logits), dt, _ptr(params), ctypes.c_uint64(int(seed) & (2 ** 64 - 1)),
+                               ctypes.c_uint32(int(row_base) & 0xFFFFFFFF), ctypes.c_uint32(int(pos) & 0xFFFFFFFF),
+                               B, V, _ptr(out.q), _ptr(out.tokens), _ptr(out.logprobs), _ptr(out.flags),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_draft_sample")
+    return out
 
 
 def philox4x32_10(ctr: torch.Tensor, seed: int, stream=None) -> torch.Tensor:

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
-SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_commit.cu", "spec_api.cu", "spec_noalloc.cu"]
+SOURCES = ["spec_verify.cu", "spec_kernel.cu", "spec_commit.cu", "spec_api.cu", "spec_noalloc.cu", "spec_draft.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -236,6 +236,9 @@ struct Args {
   int vec_q;
   u64* done;              // fused commit: finalized rows in order, tagged (row << 5 | accept_len)
   u64* tp;                // top-p passes: per-unit scratch (kTpStride words per top-p unit)
+  u64* desc;              // draft sampling: per-unit kept-set descriptors (null: not written)
+  uint32_t race_stream;   // Philox stream word of the entries' race uniforms (blocks: the next one)
+  uint32_t pos_base;      // added to a unit's position in the Philox counters
   FusedCommit fc;
 };
 
@@ -516,6 +519,24 @@ static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, i
   __syncwarp();
 }
 
+// Draft sampling (spec_draft_sample): the settled unit's kept set and
+// normaliser, for the kernel that writes q afterwards.  Tagged words:
+// [0] mode, [1] m, [2] 1 / Z_S, [3] threshold order key (full 32-bit key),
+// [4] threshold index (the last kept entry at that key) or the argmax.
+enum { DESC_ALL = 1, DESC_THRESH = 2, DESC_GREEDY = 3 };
+constexpr int kDescWords = 8;
+__device__ __forceinline__ void publish_desc(const Args& A, uint32_t tag, int u, uint32_t mode, float m, float invZ,
+                                             uint32_t tkey, uint32_t tidx) {
+  if (A.desc == nullptr) return;
+  const int lane = threadIdx.x & 31;
+  const uint32_t v = lane == 0 ? mode
+                   : lane == 1 ? __float_as_uint(m)
+                   : lane == 2 ? __float_as_uint(invZ)
+                   : lane == 3 ? tkey
+                               : tidx;
+  if (lane < 5) __stcg(A.desc + (size_t)u * kDescWords + lane, tagw(tag, v));
+}
+
 __device__ __forceinline__ UnitRecord empty_record(uint32_t flags) {
   UnitRecord r;
   r.flags = flags;
@@ -548,7 +569,7 @@ __device__ __forceinline__ bool kept(const Thresh& t, uint32_t key, uint32_t v) 
 // The accept uniform u_j of draft `pos` in row `row`: Philox counter
 // (0, pos, row, 0), word 0.
 __device__ __forceinline__ float accept_uniform(const Args& A, int row, int pos) {
-  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos, srow(A, row), 0u), A.key0, A.key1);
+  const uint4 w = philox4x32_10(make_uint4(0u, (uint32_t)pos + A.pos_base, srow(A, row), 0u), A.key0, A.key1);
   return uniform_of(w.x);
 }
 
@@ -599,7 +620,8 @@ static __device__ __noinline__ AcceptInfo accept_test(const Args& A, int row, in
 // Race uniform words.  Entry v at position pos: counter (v >> 2, pos, row,
 // 1), word v & 3.  Block b (level 1): counter (b >> 2, pos, row, 2), word b & 3.
 __device__ __forceinline__ uint32_t race_word(const Args& A, int row, int pos, uint32_t v) {
-  const uint4 w = philox4x32_10(make_uint4(v >> 2, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
+  const uint4 w = philox4x32_10(make_uint4(v >> 2, (uint32_t)pos + A.pos_base, srow(A, row), A.race_stream),
+                                A.key0, A.key1);
   return word_of(w, v & 3);
 }
 
@@ -614,7 +636,8 @@ __device__ __forceinline__ bool draw_margin(const Race& r) {
 // it with r_v / W_b, so v is drawn with probability r_v / sum r exactly,
 // while only one block needs a random number per entry.
 __device__ __forceinline__ uint32_t block_word(const Args& A, int row, int pos, uint32_t b) {
-  const uint4 w = philox4x32_10(make_uint4(b >> 2, (uint32_t)pos, srow(A, row), 2u), A.key0, A.key1);
+  const uint4 w = philox4x32_10(make_uint4(b >> 2, (uint32_t)pos + A.pos_base, srow(A, row), A.race_stream + 1u),
+                                A.key0, A.key1);
   return word_of(w, b & 3);
 }
 
@@ -683,8 +706,9 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
     if (mode == RW_RESIDUAL) load_q8(A, qrow, g * 8, qv);
     // the Philox blocks of entries 8g..8g+3 and 8g+4..8g+7
     const uint32_t blk = (uint32_t)g * 2u;
-    const uint4 p0 = philox4x32_10(make_uint4(blk, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
-    const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, (uint32_t)pos, srow(A, row), 1u), A.key0, A.key1);
+    const uint32_t cp = (uint32_t)pos + A.pos_base;
+    const uint4 p0 = philox4x32_10(make_uint4(blk, cp, srow(A, row), A.race_stream), A.key0, A.key1);
+    const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, cp, srow(A, row), A.race_stream), A.key0, A.key1);
     float w[8], tq[8];
     group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
     // one race step per entry, in a rolled loop (small code)

@@ -826,7 +826,10 @@ __device__ __noinline__ void unit_general(const Args& A, GenShm& S, GenRing& R, 
       rec.draw_flags = draw_flags;
     }
   }
-  if (ctid() < 32) commit_record(A, tag, u, row, rec);
+  if (ctid() < 32) {
+    publish_desc(A, tag, u, DESC_THRESH, m, invZ, th.tkey, th.tidx);
+    commit_record(A, tag, u, row, rec);
+  }
   csync();
 }
 

@@ -10,6 +10,16 @@ namespace specv {
 
 struct FusedCommit;
 
+// Draft sampling options of a verify launch (spec_draft_sample): where the
+// settled units' kept-set descriptors go, the Philox stream word of the
+// entries' race uniforms (blocks use the next one) and the position added to
+// every Philox counter.
+struct DraftOpts {
+  unsigned long long* desc;
+  uint32_t race_stream;
+  uint32_t pos_base;
+};
+
 // SPEC_OK when the current device is an sm_103 GPU, SPEC_E_ARCH otherwise,
 // SPEC_E_CUDA when the device cannot be queried.  Cached per device.
 int check_arch();
@@ -24,11 +34,12 @@ int verify_check(const void* logits, int logits_dtype, const float* draft_probs,
 
 // The launch of spec_verify on arguments verify_check accepted (B > 0),
 // with a workspace of at least spec_verify_workspace_size(B, k, V) bytes.
-// fc (or null): the commit to fuse into the launch (spec_verify_commit).
+// fc (or null): the commit to fuse into the launch (spec_verify_commit);
+// dr (or null): draft sampling options (spec_draft_sample).
 int verify_launch(const void* logits, int logits_dtype, const float* draft_probs, const int32_t* draft_tokens,
                   const spec_params_t* params, uint64_t seed, uint32_t row_base, int B, int k, int V,
                   int32_t* tokens, int32_t* accept_len, float* logprobs, float* alpha, uint32_t* flags,
-                  void* workspace, void* cuda_stream, const FusedCommit* fc);
+                  void* workspace, void* cuda_stream, const FusedCommit* fc, const DraftOpts* dr = nullptr);
 
 // The argument checks of spec_commit (swap_slot non-null: spec_commit_swap).
 // Enqueues nothing; SPEC_OK for L == 0 or B == 0 after the dimension checks.

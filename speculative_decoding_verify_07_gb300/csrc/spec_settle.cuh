@@ -286,6 +286,7 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
       }
     }
     TLP(u, 3);
+    publish_desc(A, tag, u, DESC_GREEDY, m, 0.f, 0u, (uint32_t)am);
     commit_record(A, tag, u, row, rec);
     return;
   }
@@ -344,6 +345,7 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
       if (draw_margin(a) || draw_margin(l2)) rec.draw_flags |= SPEC_F_MARGIN_DRAW;
     }
     TLP(u, 4);
+    publish_desc(A, tag, u, DESC_ALL, m, 1.0f / Z, 0u, 0u);
     commit_record(A, tag, u, row, rec);
     return;
   }
@@ -1009,6 +1011,7 @@ __device__ __noinline__ void topk_tail(const Args& A, uint32_t tag, TopkScratch&
     }
   }
   TLP(u, 7);
+  publish_desc(A, tag, u, DESC_THRESH, m, invZ, (uint32_t)(lk[n_s - 1] >> 32), Li[n_s - 1]);
   commit_record(A, tag, u, row, rec);
 }
 

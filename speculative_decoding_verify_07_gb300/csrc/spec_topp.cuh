@@ -1054,6 +1054,7 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
         rec.draw_flags = draw_flags;
       }
     }
+    publish_desc(A, tag, U.uid, DESC_THRESH, m, invZ, th.tkey, th.tidx);
     commit_record(A, tag, U.uid, U.row, rec);
   }
 }

@@ -51,7 +51,7 @@ int verify_check(const void* logits, int logits_dtype, const float* draft_probs,
 int verify_launch(const void* logits, int logits_dtype, const float* draft_probs, const int32_t* draft_tokens,
                   const spec_params_t* params, uint64_t seed, uint32_t row_base, int B, int k, int V,
                   int32_t* tokens, int32_t* accept_len, float* logprobs, float* alpha, uint32_t* flags,
-                  void* workspace, void* cuda_stream, const FusedCommit* fc) {
+                  void* workspace, void* cuda_stream, const FusedCommit* fc, const DraftOpts* dr) {
   const size_t es = logits_dtype == SPEC_BF16 ? 2 : 4;
   const Layout L = ws_layout(B, k, V);
   Args A;
@@ -77,6 +77,12 @@ int verify_launch(const void* logits, int logits_dtype, const float* draft_probs
   A.done = reinterpret_cast<u64*>(ws + L.done);
   A.tp = reinterpret_cast<u64*>(ws + L.tp);
   if (fc) A.fc = *fc;
+  A.race_stream = 1u;   // entries on Philox stream 1, blocks on stream 2
+  if (dr) {
+    A.desc = dr->desc;
+    A.race_stream = dr->race_stream;
+    A.pos_base = dr->pos_base;
+  }
   A.key0 = (uint32_t)(seed & 0xffffffffull);
   A.key1 = (uint32_t)(seed >> 32);
   A.row_base = row_base;

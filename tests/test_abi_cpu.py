@@ -55,7 +55,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.spec_version() == 3
+    assert lib.spec_version() == 4
     for code in range(0, -8, -1):
         s = lib.spec_status_string(code).decode()
         assert s and s != "unknown status code"
@@ -191,3 +191,37 @@ def test_fused_verify_commit_checks_every_argument_before_touching_cuda(lib):
     assert _fused(lib, B=0) == 0
     assert _fused(lib, L=0) in (-6, -7)
     assert _fused(lib) in (-6, -7)
+
+
+def _draft(lib, **kw):
+    vp, i32, u32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t
+    lib.spec_draft_sample.argtypes = [vp, i32, vp, u64, u32, u32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_draft_sample.restype = i32
+    lib.spec_draft_workspace_size.argtypes = [i32, i32]
+    lib.spec_draft_workspace_size.restype = sz
+    a = dict(logits=P, dt=1, params=P, seed=0, row_base=0, pos=0, B=4, V=1000, q=P, tok=P, lp=P, flags=P,
+             ws=P, wsb=1 << 22, stream=None)
+    a.update(kw)
+    return lib.spec_draft_sample(a["logits"], a["dt"], a["params"], a["seed"], a["row_base"], a["pos"], a["B"],
+                                 a["V"], a["q"], a["tok"], a["lp"], a["flags"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_draft_sample_checks_arguments_before_touching_cuda(lib):
+    assert lib.spec_draft_workspace_size(4, 1000) >= lib.spec_verify_workspace_size(4, 0, 1000)
+    assert lib.spec_draft_workspace_size(-1, 10) == 0
+    assert _draft(lib, B=-1) == -2
+    assert _draft(lib, V=0) == -2
+    assert _draft(lib, V=524289) == -2
+    assert _draft(lib, dt=5) == -3
+    assert _draft(lib, B=0) == 0
+    assert _draft(lib, logits=None) == -1
+    assert _draft(lib, tok=None) == -1
+    assert _draft(lib, lp=None) == -1
+    assert _draft(lib, ws=None) == -1
+    assert _draft(lib, q=P + 2) == -4
+    assert _draft(lib, ws=P + 8) == -4
+    assert _draft(lib, wsb=64) == -5
+    assert _draft(lib, logits=P + 1) == -4
+    # valid arguments reach the CUDA runtime (q may be NULL: tokens only)
+    assert _draft(lib) in (-6, -7)
+    assert _draft(lib, q=None) in (-6, -7)
