@@ -102,10 +102,14 @@ enum {
  * comes round again); two calls that may run concurrently need two
  * workspaces.
  * Two words of the 256-byte header are for diagnosis and testing:
- *   bytes 20..23  must stay 0.  A nonzero value makes the finalize of row 0
- *                 wait for records that never arrive, so that the row comes
- *                 back with SPEC_F_TIMEOUT after the wait's bound (a few
- *                 hundred milliseconds); it exists to test that path.
+ *   bytes 20..23  must stay 0.  They exist to test the waits that give up:
+ *                 bit 0 makes the finalize of row 0 wait for records that
+ *                 never arrive (the row comes back with SPEC_F_TIMEOUT after
+ *                 the wait's bound, a few hundred milliseconds); bit 1 makes
+ *                 one CTA reach the first grid barrier of the top-p passes
+ *                 1.5 s late, so that the others' wait gives up after about
+ *                 a second and every top-p row comes back with
+ *                 SPEC_F_TIMEOUT.
  *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
  *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
  *                 settle or finalize wait for records, 8 the row-order wait

@@ -69,7 +69,9 @@ struct WsHeader {
   uint32_t error;         // ERR_* bits of the running call
   uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
   uint32_t pad_item;
-  uint32_t inject;        // test hook: nonzero makes the finalize of row 0 wait for a tag nothing writes
+  uint32_t inject;        // test hooks: bit 0 makes the finalize of row 0 wait for a tag nothing
+                          // writes; bit 1 makes CTA 0 reach the first grid barrier of the top-p
+                          // passes 1.5 s late, after the others' wait has given up
   uint32_t last_error;    // ERR_* bits of the last completed call
   uint32_t pad0;
   uint32_t n_class[kClasses];   // rows per class (large batches)
@@ -425,7 +427,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
   const int k = A.k;
   const u64* R = A.urec + ((size_t)row * (k + 1) + lane) * kURecWords;
   // test hook: row 0 waits for a tag that no record carries
-  const uint32_t want = (row == 0 && __ldcg(&A.ws->inject) != 0u) ? (tag ^ 0x80000000u) : tag;
+  const uint32_t want = (row == 0 && (__ldcg(&A.ws->inject) & 1u) != 0u) ? (tag ^ 0x80000000u) : tag;
   u64 w[7];
 #pragma unroll
   for (int i = 0; i < 7; ++i) w[i] = 0ull;

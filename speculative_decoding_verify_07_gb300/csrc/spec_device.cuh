@@ -278,6 +278,13 @@ struct Race {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// The GPU's global timer, in nanoseconds.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Start bringing `bytes` (a multiple of 16, from a 16-byte aligned address)
 // into L2 with the copy engine.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {

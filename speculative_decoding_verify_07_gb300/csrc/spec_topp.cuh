@@ -1061,15 +1061,18 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
 
 // Every CTA arrives before any leaves (the launch is cooperative, so all are
 // resident).  The count only grows within a call: barrier i waits for
-// i x n_ctas arrivals.  Bounded: a wait that gives up sets ERR_BARRIER.
+// i x n_ctas arrivals.  Bounded by the global timer: a wait that lasts a
+// second gives up and sets ERR_BARRIER.
+constexpr unsigned long long kBarrierNs = 1000000000ull;
 __device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(&A.ws->bar, 1u);
+    const unsigned long long t0 = global_ns();
     long long spins = 0;
     while (load_acquire(&A.ws->bar) < target) {
-      if (++spins > 16ll * kSpinLimit) {
+      if ((++spins & 63) == 0 && global_ns() - t0 > kBarrierNs) {
         atomicOr(&A.ws->error, (uint32_t)ERR_BARRIER);
         break;
       }
@@ -1109,6 +1112,12 @@ __device__ __noinline__ void topp_passes(const Args& A, TpPlan T, uint32_t tag, 
   for (int i = (int)(threadIdx.x & 31); i < 3 * kTpBins / 4; i += 32)
     reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncwarp();
+  // test hook: CTA 0 reaches the first barrier 1.5 s late, after the
+  // others' wait has given up (a bounded sleep)
+  if (threadIdx.x == 0 && blockIdx.x == 0 && (__ldcg(&A.ws->inject) & 2u) != 0u) {
+    const unsigned long long t0 = global_ns();
+    for (int i = 0; i < 4000 && global_ns() - t0 < kBarrierNs + kBarrierNs / 2; ++i) __nanosleep(1000000);
+  }
   stamp_bar();
   grid_barrier(A, ++nb * n);   // the roles are done and the scratch is zero everywhere
   stamp_bar();

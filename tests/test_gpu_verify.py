@@ -307,6 +307,29 @@ def test_timed_out_wait_flags_the_row_and_leaves_the_context_usable():
     assert int(ws[24:28].view(torch.int32).item()) == 0
 
 
+def test_grid_barrier_that_gives_up_flags_the_top_p_rows():
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    case = _random_case(np.random.default_rng(32), B=8, k=2, V=5000, dtype="bf16", param_mode="mix")
+    logits, q, x, params = to_device(case)
+    ws = sv.new_workspace(8, 2, 5000, "cuda")
+    ws[20:24].view(torch.int32).fill_(2)        # test hook: one CTA misses a top-p grid barrier
+    out = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
+    torch.cuda.synchronize()
+    topp = [3]                                  # the mix gives row 3 top-p without top-k
+    for r in topp:
+        assert out["flags"][r] & sv.F_TIMEOUT and out["accept_len"][r] == 0
+        assert np.all(out["tokens"][r] == -1)
+    assert int(ws[24:28].view(torch.int32).item()) & 16       # the barrier bit of the last call
+    others = [r for r in range(8) if r not in topp]
+    compare(out, run_oracle(case, rows=others), "rows outside the top-p passes")
+    # hook cleared: every row comes back normally and no wait gave up
+    ws[20:24].view(torch.int32).fill_(0)
+    again = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
+    torch.cuda.synchronize()
+    compare(again, run_oracle(case), "after the barrier timeout")
+    assert int(ws[24:28].view(torch.int32).item()) == 0
+
+
 def test_gpu_distribution_preserved_40k_rows():
     """The page's criterion run on the GPU path: 40k rows, drafts drawn from q."""
     from scipy import stats
