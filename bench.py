@@ -441,7 +441,8 @@ def draft_component(dev, peak, peak_kind, n_sets=8, n_steps=20, warmup=5):
             "us": round(us, 2), "us_p50": round(statistics.median(res[True]), 2),
             "us_tokens_only": round(statistics.mean(res[False]), 2), "rows_per_s": round(B_ / (us * 1e-6), 1),
             "algorithmic_bytes": int(nbytes), "gbs": round(ach, 1), "frac": round(ach / peak, 4), "peak": peak,
-            "peak_source": peak_kind, "launches": 2}
+            "peak_source": peak_kind, "launches": 2,
+            "traffic_q_kernel": traffic_record("draft_q_kernel", kernel_source_hash(["spec_draft.cu"]))}
 
 
 def run_ours(args):
@@ -688,6 +689,21 @@ def run_only(args):
         ws = sv.new_workspace(B, K, V, dev)
         out = sv.VerifyOutputs(B, K, dev)
         fn = lambda i: sv.spec_verify(*sets[i % N_SETS][:4], sets[i % N_SETS][4], out=out, workspace=ws)
+    elif args.only == "topp":
+        sets, _ = _verify_sets(synth.make_topp, N_SETS, dev)
+        Bt, k1, Vt = sets[0][0].shape
+        ws = sv.new_workspace(Bt, k1 - 1, Vt, dev)
+        out = sv.VerifyOutputs(Bt, k1 - 1, dev)
+        fn = lambda i: sv.spec_verify(*sets[i % N_SETS][:4], sets[i % N_SETS][4], out=out, workspace=ws)
+    elif args.only == "draft":
+        dsets = []
+        for i in range(8):
+            inp = synth.make_mixed(seed_offset=100 * i)
+            dsets.append((torch.from_numpy(np.ascontiguousarray(inp.logits[:, 0, :])).to(torch.bfloat16).to(dev),
+                          sv.make_params(inp.temperature, inp.top_k, inp.top_p, dev), inp.seed + i))
+        ws = sv.new_draft_workspace(B, V, dev)
+        dout = sv.DraftOutputs(B, V, dev)
+        fn = lambda i: sv.spec_draft_sample(*dsets[i % 8], 1, out=dout, workspace=ws)
     else:
         sh = synth.CommitShape(L=args.layers)
         vrec = torch.zeros((sh.L, sh.B, sh.S, sh.H, sh.Dk, sh.Dv), dtype=torch.float32, device=dev)
@@ -719,7 +735,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-components", action="store_true")
-    ap.add_argument("--only", choices=["verify", "commit"], default=None,
+    ap.add_argument("--only", choices=["verify", "topp", "draft", "commit"], default=None,
                     help="profiling aid: launch only one kernel per step, print its mean time")
     ap.add_argument("--layers", type=int, default=24, help="profiling aid for --only commit")
     args = ap.parse_args()
