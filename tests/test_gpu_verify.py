@@ -177,6 +177,24 @@ def test_parity_topp_fp32_refinement_levels():
         compare(run_gpu(case), run_oracle(case), f"top-p fp32 V={V}")
 
 
+def test_parity_topp_dense_keys_extreme_p_and_full_vocabulary():
+    rng = np.random.default_rng(404)
+    # bf16 logits packed near zero: a crossing bin holds hundreds of keys, two
+    # refinement levels, tiles with more keys than their lists hold (the ties
+    # pass runs)
+    case = _random_case(rng, B=6, k=2, V=30000, dtype="bf16", param_mode="topp")
+    case.logits[:] = synth.round_to_bf16(rng.normal(0, 0.02, size=case.logits.shape).astype(np.float32))
+    case.top_p[:] = np.array([0.8, 0.5, 0.95, 0.3, 0.99, 0.7], np.float32)
+    compare(run_gpu(case), run_oracle(case), "top-p dense keys")
+    # extreme P: the crossing at the maximum, and nearly the whole row
+    case = _random_case(rng, B=4, k=2, V=20000, dtype="bf16", param_mode="topp")
+    case.top_p[:] = np.array([1e-4, 0.02, 0.9999, 0.99999], np.float32)
+    compare(run_gpu(case), run_oracle(case), "top-p extreme P")
+    # fp32 at the bench vocabulary: four refinement levels and the ties pass
+    case = _random_case(rng, B=4, k=2, V=151936, dtype="f32", param_mode="topp")
+    compare(run_gpu(case), run_oracle(case), "top-p fp32 V=151936")
+
+
 def test_parity_topp_rows_above_the_shared_order_limit():
     # 300 rows (the row order then lives in the workspace), every class, and
     # top-p rows holding NaN, +inf and all -inf positions
