@@ -88,6 +88,13 @@ def test_fused_unaligned_conv_blob_takes_the_plain_copy():
     _both(inp, L=2, H=2, Dk=4, Dv=4, W=3, C=5, slots=10, slot_map=None)
 
 
+def test_fused_with_top_p_rows():
+    # rows that take the grid-wide top-p passes finalize last; their states
+    # are committed after them in the same launch
+    inp = synth.make_topp(B=8, V=20000, seed_offset=9)
+    _both(inp, L=2, H=2, Dk=16, Dv=32, W=4, C=64, slots=8, slot_map=None)
+
+
 def test_fused_conv_only_and_identity_slots():
     inp = synth.make_mixed(B=6, k=2, V=9000, seed_offset=8)
     _both(inp, L=4, H=0, Dk=0, Dv=0, W=4, C=256, slots=6, slot_map=None)
