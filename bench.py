@@ -689,12 +689,13 @@ def run_only(args):
         ws = sv.new_workspace(B, K, V, dev)
         out = sv.VerifyOutputs(B, K, dev)
         fn = lambda i: sv.spec_verify(*sets[i % N_SETS][:4], sets[i % N_SETS][4], out=out, workspace=ws)
-    elif args.only == "topp":
-        sets, _ = _verify_sets(synth.make_topp, N_SETS, dev)
+    elif args.only in ("topp", "adversarial"):
+        sets, _ = _verify_sets(synth.make_topp if args.only == "topp" else synth.make_adversarial,
+                               N_SETS if args.only == "topp" else 1, dev)
         Bt, k1, Vt = sets[0][0].shape
         ws = sv.new_workspace(Bt, k1 - 1, Vt, dev)
         out = sv.VerifyOutputs(Bt, k1 - 1, dev)
-        fn = lambda i: sv.spec_verify(*sets[i % N_SETS][:4], sets[i % N_SETS][4], out=out, workspace=ws)
+        fn = lambda i: sv.spec_verify(*sets[i % len(sets)][:4], sets[i % len(sets)][4], out=out, workspace=ws)
     elif args.only == "draft":
         dsets = []
         for i in range(8):
@@ -735,7 +736,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-components", action="store_true")
-    ap.add_argument("--only", choices=["verify", "topp", "draft", "commit"], default=None,
+    ap.add_argument("--only", choices=["verify", "topp", "adversarial", "draft", "commit"], default=None,
                     help="profiling aid: launch only one kernel per step, print its mean time")
     ap.add_argument("--layers", type=int, default=24, help="profiling aid for --only commit")
     args = ap.parse_args()
