@@ -21,9 +21,12 @@
 //      the mass from the top reaches ceil(P Z) and the bin's range of order
 //      keys, and histograms the mass of the entries in that range by key, 8
 //      key bits a level, until one key, the crossing key, is left (one level
-//      for most bf16 rows; at most two for bf16 and four for fp32);
-//   4. ties: the entries at the crossing key in each tile.  The first n of
-//      them by index are kept, where n comes from the mass still missing;
+//      for most bf16 rows; at most two for bf16 and four for fp32).  The
+//      level whose bins are single keys also lists each tile's keys with
+//      their counts (bf16);
+//   4. ties (fp32 rows, or a tile whose list overflowed): the entries at the
+//      crossing key in each tile.  The first n of them by index are kept,
+//      where n comes from the mass still missing;
 //   5. tiles: with the kept set known, alpha = sum min(p, q) and the level-1
 //      races over the tile's 256-entry blocks, of the residual max(p - q, 0)
 //      and of p;
@@ -31,9 +34,10 @@
 //      accept test and the level-2 race in the winning block, and writes the
 //      unit's record (the row's last unit finalizes the row).
 // After each barrier every warp derives its unit's threshold state from the
-// histograms itself (a few loads and warp scans), so no pass waits for a
-// settle step.  Each barrier wait is bounded: one that gives up sets
-// ERR_BARRIER, and the units come back with SPEC_F_TIMEOUT.
+// state the previous pass stored and the newest histogram (one round trip and
+// a warp scan), so no pass waits for a settle step.  Each barrier wait is
+// bounded (a second): one that gives up sets ERR_BARRIER, and the units come
+// back with SPEC_F_TIMEOUT.
 #pragma once
 
 #include "spec_common.cuh"
