@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define SPEC_ABI_VERSION 4
+#define SPEC_ABI_VERSION 5
 
 /* Largest vocabulary and draft length accepted by spec_verify. */
 #define SPEC_MAX_V 524288
@@ -92,16 +92,18 @@ enum {
 
 /* Bytes of workspace spec_verify needs for a batch of B rows with k drafts.
  * The workspace must be zero-filled before its first use (for example with
- * cudaMemsetAsync).  Every completed spec_verify call returns the words that
- * must start at zero (the counters at the start of the 256-byte header, one
- * ticket per row and two tile counters per (row, position)) to zero and
- * advances an epoch word in the header; every record behind them carries
- * the tag of the call that wrote it (never 0), so stale or foreign contents
- * are never read as this call's.  One workspace serves any number of later
- * calls on one stream (re-zero it once every 2^32 - 1 calls, when the tag
- * comes round again); two calls that may run concurrently need two
- * workspaces.
- * Two words of the 256-byte header are for diagnosis and testing:
+ * cudaMemsetAsync).  Each call numbers itself from a count of the CTAs that
+ * entered earlier calls (so every call on one workspace launches the same
+ * grid: one workspace belongs to one device), counts in one of two sets of
+ * counters in the 256-byte header by the parity of its number, and zeroes
+ * the other set for the call after it.  The settles return the per-row
+ * tickets and per-(row, position) tile counters to zero as they finish.
+ * Every record behind them carries the tag of the call that wrote it (its
+ * number + 1, never 0), so stale or foreign contents are never read as this
+ * call's.  One workspace serves any number of later calls on one stream
+ * (re-zero it once every 2^32 - 1 calls, when the tag comes round again);
+ * two calls that may run concurrently need two workspaces.
+ * Words of the 256-byte header for diagnosis and testing:
  *   bytes 20..23  must stay 0.  They exist to test the waits that give up:
  *                 bit 0 makes the finalize of row 0 wait for records that
  *                 never arrive (the row comes back with SPEC_F_TIMEOUT after
@@ -110,11 +112,14 @@ enum {
  *                 1.5 s late, so that the others' wait gives up after about
  *                 a second and every top-p row comes back with
  *                 SPEC_F_TIMEOUT.
- *   bytes 24..27  after a call: bits of the waits that gave up in it (1 a
- *                 tile's wait for its unit's state, 2 a tile's copy, 4 a
- *                 settle or finalize wait for records, 8 the row-order wait
- *                 of batches above 256 rows, 16 a grid barrier of the
- *                 top-p passes); 0 when every wait ended normally.          */
+ *   bytes 24..27  the counter set (0 or 1) of the last call.
+ *   bytes 52..55 (set 0) and 84..87 (set 1)  after a call: bits of the waits
+ *                 that gave up in it (1 a tile's wait for its unit's state,
+ *                 2 a tile's copy, 4 a settle or finalize wait for records,
+ *                 8 the row-order wait of batches above 256 rows, 16 a grid
+ *                 barrier of the top-p passes); 0 when every wait ended
+ *                 normally.
+ *   bytes 236..239  the tag of the last call.                              */
 size_t spec_verify_workspace_size(int B, int k, int V);
 
 /* spec_verify - one verify step for B rows of k drafts over a V-entry vocabulary.

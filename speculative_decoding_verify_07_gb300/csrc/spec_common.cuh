@@ -53,8 +53,8 @@ struct Geo {
 enum { UT_GREEDY = 0, UT_TOPK = 1, UT_DENSE = 2, UT_GENERAL = 3, UT_TOPP = 4 };
 constexpr int kClasses = 5;
 
-// Error bits of WsHeader::error (OR-ed during a call; moved to last_error by
-// the call's last CTA).
+// Error bits of CallWords::error (OR-ed during a call, kept until the call
+// after next starts).
 enum {
   ERR_STATE_WAIT = 1,      // a B tile gave up waiting for its unit's state
   ERR_COPY_WAIT = 2,       // a tile's bulk copy did not complete
@@ -63,35 +63,44 @@ enum {
   ERR_BARRIER = 16         // a CTA gave up waiting at a grid barrier of the top-p passes
 };
 
-struct WsHeader {
+// The counters of one call.  Calls alternate between two sets: call n
+// counts in set n & 1 and zeroes set (n + 1) & 1 for the call after it, so
+// no call has to wait at its end for the last CTA to reset anything.
+struct CallWords {
   uint32_t gnext;         // next general-path unit
-  uint32_t ctas_done;     // CTAs that left the kernel
-  uint32_t error;         // ERR_* bits of the running call
+  uint32_t commit_next;   // fused commit: next copy job
+  uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
+  uint32_t bar;           // top-p passes: arrivals at the grid barriers
+  uint32_t tp_more;       // top-p passes: bit L set when refinement level L is needed
+  uint32_t error;         // ERR_* bits of the waits that gave up
+  uint32_t pad[2];
+};
+static_assert(sizeof(CallWords) == 32, "call words");
+
+struct WsHeader {
+  unsigned long long arrivals;  // CTAs that have entered a call on this workspace, over all calls
   uint32_t order_tag;     // the row order in the workspace is this call's (large batches)
-  uint32_t pad_item;
+  uint32_t pad_a[2];
   uint32_t inject;        // test hooks: bit 0 makes the finalize of row 0 wait for a tag nothing
                           // writes; bit 1 makes CTA 0 reach the first grid barrier of the top-p
                           // passes 1.5 s late, after the others' wait has given up
-  uint32_t last_error;    // ERR_* bits of the last completed call
-  uint32_t pad0;
+  uint32_t last_set;      // the counter set of the last call to start (written by its CTA 0)
+  uint32_t pad_b;
+  CallWords call[2];      // by the parity of the call's number
   uint32_t n_class[kClasses];   // rows per class (large batches)
-  uint32_t commit_next;   // fused commit: next copy job
-  uint32_t done_count;    // fused commit: rows finalized so far (entries of the done queue)
-  uint32_t bar;           // top-p passes: arrivals at the grid barriers of this call
-  uint32_t tp_more;       // top-p passes: bit L set when refinement level L is needed
-  uint32_t pad[42];
-  uint32_t epoch;         // tag of the last completed call (records of this call carry the next tag)
+  uint32_t pad[30];
+  uint32_t epoch;         // tag of the last call to start (written by its CTA 0)
   uint32_t pad1[4];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header");
+static_assert(offsetof(WsHeader, inject) == 20, "test hook word");
+static_assert(offsetof(WsHeader, last_set) == 24, "last call's counter set");
+static_assert(offsetof(WsHeader, call) == 32, "call words");
 static_assert(offsetof(WsHeader, epoch) == 236, "epoch word");
 
-// The tag of the call after the one tagged `epoch` (0 is never a tag, so a
-// zero-filled workspace holds no tagged word).
-__device__ __forceinline__ uint32_t next_tag(uint32_t epoch) {
-  const uint32_t t = epoch + 1u;
-  return t == 0u ? 1u : t;
-}
+// The parity of the running call's number, set by each CTA as it enters the
+// verify kernel; selects the call's counter set.
+static __shared__ uint32_t s_call_parity;
 
 // General-path group: the CTA's first kThreads (256) threads run the
 // group-wide code on a named barrier of their own.
@@ -243,6 +252,10 @@ struct Args {
   uint32_t pos_base;      // added to a unit's position in the Philox counters
   FusedCommit fc;
 };
+
+// The running call's counters (in the verify kernel, after its prologue).
+__device__ __forceinline__ CallWords& cur(const Args& A) { return A.ws->call[s_call_parity]; }
+
 
 // Timeline stamps (global timer, ns) of an instrumented build compiled with
 // SPEC_TIMELINE; empty otherwise.  Slots: per CTA start and end, per stream
@@ -416,7 +429,7 @@ __device__ __forceinline__ float group_max(const float v[8]) {
 __device__ __forceinline__ void enqueue_done(const Args& A, int row, int acc_len, uint32_t tag) {
   if ((threadIdx.x & 31) == 0) {
     __threadfence();
-    const uint32_t i = atomicAdd(&A.ws->done_count, 1u);
+    const uint32_t i = atomicAdd(&cur(A).done_count, 1u);
     __stcg(A.done + i, tagw(tag, ((uint32_t)row << 5) | (uint32_t)acc_len));
   }
 }
@@ -444,7 +457,7 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
     }
     if (__all_sync(full, ok)) break;
     if (++spins > kSpinLimit) {
-      if (lane == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+      if (lane == 0) atomicOr(&cur(A).error, (uint32_t)ERR_RECORD_WAIT);
       timed_out = true;
       break;
     }

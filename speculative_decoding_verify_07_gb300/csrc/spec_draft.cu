@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kQThreads) draft_q_kernel(const void* logits, 
   __shared__ int ok;
   const int row = blockIdx.y;
   if (threadIdx.x < 32) {
-    // the verify launch before this one ended with its tag as the epoch
+    // the verify launch before this one wrote its tag as the epoch
     const uint32_t tag = __ldcg(&ws->epoch);
     const int lane = threadIdx.x;
     const u64 w = lane < 5 ? __ldcg(desc + (size_t)row * kDescWords + lane) : 0ull;

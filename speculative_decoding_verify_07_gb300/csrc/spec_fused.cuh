@@ -46,7 +46,7 @@ __device__ __forceinline__ bool bulk_job(const Args& A, unsigned char* dst, cons
     long long spins = 0;
     while (!mbar_try_wait(&bar[b], par[b])) {
       if (++spins > kSpinLimit) {
-        atomicOr(&A.ws->error, (uint32_t)ERR_COPY_WAIT);
+        atomicOr(&cur(A).error, (uint32_t)ERR_COPY_WAIT);
         return false;
       }
       if (spins > 64) __nanosleep(32);
@@ -86,7 +86,7 @@ __device__ __noinline__ void commit_phase(const Args& A, uint32_t tag, unsigned 
   bool bad = true, broken = false;
   while (!broken) {
     uint32_t jt = 0;
-    if (lane == 0) jt = atomicAdd(&A.ws->commit_next, 1u);
+    if (lane == 0) jt = atomicAdd(&cur(A).commit_next, 1u);
     const long long j = (long long)__shfl_sync(0xffffffffu, jt, 0);
     if (j >= total) break;
     const long long q = j / jpr;
@@ -106,7 +106,7 @@ __device__ __noinline__ void commit_phase(const Args& A, uint32_t tag, unsigned 
             break;
           }
           if (++spins > 16ll * kSpinLimit) {
-            atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+            atomicOr(&cur(A).error, (uint32_t)ERR_RECORD_WAIT);
             break;
           }
           __nanosleep(spins > 64 ? 256 : 32);

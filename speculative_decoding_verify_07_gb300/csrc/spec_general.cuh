@@ -112,7 +112,7 @@ __device__ __forceinline__ void csweep(const Args& A, GenRing& R, size_t lrow, s
     bool got = R.ok;
     while (got && !mbar_try_wait(&R.bar[slot], par)) {
       if (++spins > kSpinLimit) {
-        atomicOr(&A.ws->error, (uint32_t)ERR_COPY_WAIT);
+        atomicOr(&cur(A).error, (uint32_t)ERR_COPY_WAIT);
         *R.fail = 1;
         got = false;
       }

@@ -72,10 +72,14 @@ struct Seg {
   uint32_t packed;    // tiles | pos_lo << 16 | upr << 21 | kind << 26 (0 A, 1 B)
 };
 
+constexpr int kOrderWarps = kOrderSmem / 32;   // warps that hold a row of a shared-memory order
+static_assert(kOrderWarps == 8, "class counts are read as two uint4 per class");
+
 struct OrderScratch {
   int n_class[kClasses];
   int run[kClasses];
   int scan[kNW][kClasses];
+  alignas(16) uint32_t cnt[kClasses][kOrderWarps];   // shared-memory order: rows per class and warp
 };
 
 struct alignas(128) VShm {
@@ -150,23 +154,62 @@ __device__ __forceinline__ void place_round(uint32_t* order, OrderScratch& O, in
 }
 
 // Batches of up to kOrderSmem rows: every CTA classifies the rows into
-// shared memory (one parameter load per row).
-__device__ __noinline__ void build_order_smem(const Args& A, uint32_t* order, RowPack* cfgs, OrderScratch& O) {
-  const int tid = threadIdx.x;
-  if (tid < kClasses) {
-    O.n_class[tid] = 0;
-    O.run[tid] = 0;
-  }
-  __syncthreads();
-  int cl = -1;
+// shared memory (thread r loads row r's parameters) and places them by
+// class with warp ballots; the warps' class counts meet behind one barrier.
+// Returns with the counts of this thread's row class set up for placement;
+// the caller places the row after the barrier (order_place_smem).
+struct SmemPlace {
+  int cl;          // the thread's row class (-1: no row)
+  unsigned mine;   // the lanes of the thread's warp in that class
+};
+__device__ __forceinline__ SmemPlace order_classify_smem(const Args& A, RowPack* cfgs, OrderScratch& O) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  SmemPlace sp;
+  sp.cl = -1;
+  sp.mine = 0u;
   if (tid < A.B) {
     const RowCfg c = classify(A.params[tid], A.V);
     cfgs[tid] = pack_cfg(c);
-    cl = c.type;
-    atomicAdd(&O.n_class[cl], 1);
+    sp.cl = c.type;
   }
-  __syncthreads();
-  place_round(order, O, tid, cl);
+  if (w < kOrderWarps) {
+#pragma unroll
+    for (int t = 0; t < kClasses; ++t) {
+      const unsigned b = __ballot_sync(kFull, sp.cl == t);
+      if (lane == 0) O.cnt[t][w] = __popc(b);
+      if (sp.cl == t) sp.mine = b;
+    }
+  }
+  return sp;
+}
+
+// After the barrier: every thread with a row writes it into the order
+// ([unfiltered][small top-k][general][top-p][greedy], stable), and thread 0
+// also fills in the class totals.
+__device__ __forceinline__ void order_place_smem(uint32_t* order, OrderScratch& O, const SmemPlace& sp) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (sp.cl < 0 && tid != 0) return;
+  int n[kClasses];
+#pragma unroll
+  for (int t = 0; t < kClasses; ++t) {
+    const uint4 a = *reinterpret_cast<const uint4*>(&O.cnt[t][0]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&O.cnt[t][4]);
+    n[t] = (int)(a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w);
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int t = 0; t < kClasses; ++t) O.n_class[t] = n[t];
+  }
+  if (sp.cl < 0) return;
+  const int cl = sp.cl;
+  int off = cl == UT_DENSE ? 0
+          : cl == UT_TOPK ? n[UT_DENSE]
+          : cl == UT_GENERAL ? n[UT_DENSE] + n[UT_TOPK]
+          : cl == UT_TOPP ? n[UT_DENSE] + n[UT_TOPK] + n[UT_GENERAL]
+                          : n[UT_DENSE] + n[UT_TOPK] + n[UT_GENERAL] + n[UT_TOPP];
+  for (int ww = 0; ww < w; ++ww) off += (int)O.cnt[cl][ww];
+  off += __popc(sp.mine & ((1u << lane) - 1u));
+  order[off] = (uint32_t)tid;
 }
 
 // Larger batches: CTA 0 writes the order and the class counts into the
@@ -368,7 +411,7 @@ __device__ __forceinline__ bool wait_buffer(const Args& A, unsigned long long* b
   long long spins = 0;
   while (!mbar_try_wait(bar, parity)) {
     if (++spins > kSpinLimit) {
-      if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, (uint32_t)ERR_COPY_WAIT);
+      if ((threadIdx.x & 31) == 0) atomicOr(&cur(A).error, (uint32_t)ERR_COPY_WAIT);
       return false;
     }
     if (spins > 64) __nanosleep(32);
@@ -1021,7 +1064,7 @@ __device__ __noinline__ void stream_loop(const Args& A, Plan P0, VShm& S, uint32
         bool st_ok = true;
         while (!__all_sync(kFull, state_ok(sw8, tag))) {
           if (++spins > kSpinLimit) {
-            if (lane == 0) atomicOr(&A.ws->error, (uint32_t)ERR_STATE_WAIT);
+            if (lane == 0) atomicOr(&cur(A).error, (uint32_t)ERR_STATE_WAIT);
             st_ok = false;
             break;
           }
@@ -1108,7 +1151,7 @@ __device__ __noinline__ void settle_loop(const Args& A, Plan P, VShm& S, uint32_
       long long spins = 0;
       while (load_relaxed(cnt) != (uint32_t)k.ntiles) {
         if (++spins > 16ll * kSpinLimit) {
-          atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+          atomicOr(&cur(A).error, (uint32_t)ERR_RECORD_WAIT);
           ready = false;
           break;
         }
@@ -1154,7 +1197,7 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
   }
   csync();
   while (true) {
-    if (ctid() == 0) S.gtask = (int)atomicAdd(&A.ws->gnext, 1u);
+    if (ctid() == 0) S.gtask = (int)atomicAdd(&cur(A).gnext, 1u);
     csync();
     const int g = S.gtask;
     csync();
@@ -1172,8 +1215,26 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
   const int w = threadIdx.x >> 5;
+  if (threadIdx.x == kAllThreads - 32) {
+    // The call's number: the CTAs that entered earlier calls over the grid
+    // size (calls on one workspace never overlap, and each launches the
+    // same grid).  Its tag is that number plus one, wrapping past 0.
+    const unsigned long long call = atomicAdd(&A.ws->arrivals, 1ull) / (unsigned long long)A.n_ctas;
+    const uint32_t tag = (uint32_t)(call % 0xFFFFFFFFull) + 1u;
+    const uint32_t par = (uint32_t)(call & 1ull);
+    S.tag = tag;
+    s_call_parity = par;
+    if (blockIdx.x == 0) {
+      // the next call's counters start at zero (the call before this one
+      // used them, and it has ended)
+      A.ws->epoch = tag;
+      A.ws->last_set = par;
+      uint4* nx = reinterpret_cast<uint4*>(&A.ws->call[par ^ 1u]);
+      nx[0] = make_uint4(0u, 0u, 0u, 0u);
+      nx[1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   if (threadIdx.x == 0) {
-    S.tag = next_tag(__ldcg(&A.ws->epoch));
     S.gtask = 0;
     S.ticket = 0u;
   }
@@ -1181,7 +1242,14 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   Plan P;
   bool order_ok = true;
   if (!A.global_order) {
-    build_order_smem(A, S.order, S.cfg, S.ord);     // synchronises the CTA
+    const SmemPlace sp = order_classify_smem(A, S.cfg, S.ord);
+    __syncthreads();
+    order_place_smem(S.order, S.ord, sp);
+    if (threadIdx.x == 0)
+      build_segments(A, S, S.ord.n_class[UT_DENSE], S.ord.n_class[UT_TOPK],
+                     S.ord.n_class[UT_GENERAL] + S.ord.n_class[UT_TOPP], S.ord.n_class[UT_GREEDY],
+                     ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay);
+    __syncthreads();
     P.order = S.order;
     P.cfg = S.cfg;
     P.nD = S.ord.n_class[UT_DENSE];
@@ -1196,7 +1264,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
       long long spins = 0;
       while (load_acquire(&A.ws->order_tag) != S.tag) {
         if (++spins > kSpinLimit) {
-          atomicOr(&A.ws->error, (uint32_t)ERR_ORDER_WAIT);
+          atomicOr(&cur(A).error, (uint32_t)ERR_ORDER_WAIT);
           S.gtask = -1;
           break;
         }
@@ -1212,12 +1280,13 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     P.nG = (int)__ldcg(&A.ws->n_class[UT_GREEDY]);
     P.nX = (int)__ldcg(&A.ws->n_class[UT_GENERAL]);
     P.nP = (int)__ldcg(&A.ws->n_class[UT_TOPP]);
+    // (general and top-p rows have no stream tiles; greedy rows follow them)
+    build_segments(A, S, P.nD, P.nT, P.nX + P.nP, P.nG, ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay);
+    __syncthreads();
   }
   const uint32_t tag = S.tag;
   P.NTA = ceil_div(A.V, G::EA);
   P.NTB = ceil_div(A.V, G::EB);
-  // (general and top-p rows have no stream tiles; greedy rows follow them)
-  build_segments(A, S, P.nD, P.nT, P.nX + P.nP, P.nG, P.NTA, P.NTB, b_delay);
   if (P.nP > 0 && order_ok) {
     // the top-p passes' scratch, zero before their first barrier
     const size_t n16 = (size_t)P.nP * (size_t)(A.k + 1) * (kTpStride / 2);
@@ -1225,7 +1294,6 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
       z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
   P.seg = S.seg;
   P.nseg = S.nseg;
   if (threadIdx.x == 0) TL(TL_CTA_START, (int)blockIdx.x, 160);
@@ -1264,29 +1332,12 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   if (A.fc.on && order_ok) {
     // the fused commit: every warp copies rows as they are finalized (not
     // after a copy wait that gave up: that copy may still land in a buffer)
-    const bool copy_failed = (__shfl_sync(kFull, __ldcg(&A.ws->error), 0) & (uint32_t)ERR_COPY_WAIT) != 0u ||
+    const bool copy_failed = (__shfl_sync(kFull, __ldcg(&cur(A).error), 0) & (uint32_t)ERR_COPY_WAIT) != 0u ||
                              S.broken[w] != 0u;
     if (!copy_failed) commit_phase(A, tag, S.s.buf[w][0], S.s.buf[w][1], S.cbar[w]);
     __syncthreads();
   }
   if (threadIdx.x == 0) TL(TL_CTA_END, (int)blockIdx.x, 160);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t d = atomicAdd(&A.ws->ctas_done, 1u);
-    if (d == (uint32_t)A.n_ctas - 1u) {
-      __threadfence();
-      A.ws->gnext = 0u;
-      A.ws->commit_next = 0u;
-      A.ws->done_count = 0u;
-      A.ws->bar = 0u;
-      A.ws->tp_more = 0u;
-      A.ws->ctas_done = 0u;
-      A.ws->last_error = __ldcg(&A.ws->error);
-      A.ws->error = 0u;
-      A.ws->epoch = tag;
-      __threadfence();
-    }
-  }
 }
 
 // ---------------------------------------------------------------------------

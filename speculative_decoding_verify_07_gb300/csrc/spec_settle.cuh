@@ -49,7 +49,7 @@ __device__ __forceinline__ void publish_state(const Args& A, uint32_t tag, int u
 __device__ __forceinline__ bool poll_again(const Args& A, bool ok, long long& spins, bool* timed_out) {
   if (__all_sync(kSettleFull, ok)) return false;
   if (++spins > kSpinLimit) {
-    if ((threadIdx.x & 31) == 0) atomicOr(&A.ws->error, (uint32_t)ERR_RECORD_WAIT);
+    if ((threadIdx.x & 31) == 0) atomicOr(&cur(A).error, (uint32_t)ERR_RECORD_WAIT);
     *timed_out = true;
     return false;
   }

@@ -632,7 +632,7 @@ __device__ __noinline__ void tp_level_pass(const Args& A, const TpPlan& T, uint3
         run = L == 0 || st.lo < st.hi || st.s_prev > 0;
         // the sub-bins hold several keys: the next level is needed (said
         // once, by the warp holding the unit's first tile)
-        if (run && st.s > 0 && t == 0 && lane == 0) atomicOr(&A.ws->tp_more, 1u << (L + 1));
+        if (run && st.s > 0 && t == 0 && lane == 0) atomicOr(&cur(A).tp_more, 1u << (L + 1));
       }
     }
     if (!run) continue;
@@ -685,7 +685,7 @@ __device__ __noinline__ void tp_level_pass(const Args& A, const TpPlan& T, uint3
         if ((uint32_t)lane >= total && lane < kTpListLen) __stcg(tp_list(A, U.uid, t, lane), tagw(tag, 0u));
       } else if (lane == 0) {
         __stcg(tp_list(A, U.uid, t, 0), tagw(tag, kTpTieOverflow));
-        atomicOr(&A.ws->tp_more, kTpNeedTies);
+        atomicOr(&cur(A).tp_more, kTpNeedTies);
       }
       __syncwarp();
     }
@@ -1072,12 +1072,12 @@ __device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(&A.ws->bar, 1u);
+    atomicAdd(&cur(A).bar, 1u);
     const unsigned long long t0 = global_ns();
     long long spins = 0;
-    while (load_acquire(&A.ws->bar) < target) {
+    while (load_acquire(&cur(A).bar) < target) {
       if ((++spins & 63) == 0 && global_ns() - t0 > kBarrierNs) {
-        atomicOr(&A.ws->error, (uint32_t)ERR_BARRIER);
+        atomicOr(&cur(A).error, (uint32_t)ERR_BARRIER);
         break;
       }
       __nanosleep(spins > 16 ? 128 : 16);
@@ -1135,14 +1135,14 @@ __device__ __noinline__ void topp_passes(const Args& A, TpPlan T, uint32_t tag, 
   stamp_bar();
   int L = 0;
   for (; L < kTpLevels; ++L) {
-    if (L > 0 && (__ldcg(&A.ws->tp_more) & (1u << L)) == 0u) break;
+    if (L > 0 && (__ldcg(&cur(A).tp_more) & (1u << L)) == 0u) break;
     if (usable) tp_level_pass<kBF16>(A, T, tag, gw, nwg, hist, c0, c1, L);
     stamp_pass(2 + L);
     grid_barrier(A, ++nb * n);
     stamp_bar();
   }
   T.nlev = L;
-  T.ties = !kBF16 || (__ldcg(&A.ws->tp_more) & kTpNeedTies) != 0u;
+  T.ties = !kBF16 || (__ldcg(&cur(A).tp_more) & kTpNeedTies) != 0u;
   if (T.ties) {
     if (usable) tp_ties_pass<kBF16>(A, T, tag, gw, nwg, c0, c1);
     stamp_pass(6);
@@ -1153,7 +1153,7 @@ __device__ __noinline__ void topp_passes(const Args& A, TpPlan T, uint32_t tag, 
   stamp_pass(7);
   grid_barrier(A, ++nb * n);
   stamp_bar();
-  const bool failed = (__ldcg(&A.ws->error) & (uint32_t)(ERR_BARRIER | ERR_COPY_WAIT)) != 0u;
+  const bool failed = (__ldcg(&cur(A).error) & (uint32_t)(ERR_BARRIER | ERR_COPY_WAIT)) != 0u;
   tp_settle_pass<kBF16>(A, T, tag, gw, nwg, failed);
   stamp_pass(5);
 }

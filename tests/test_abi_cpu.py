@@ -55,7 +55,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.spec_version() == 4
+    assert lib.spec_version() == 5
     for code in range(0, -8, -1):
         s = lib.spec_status_string(code).decode()
         assert s and s != "unknown status code"

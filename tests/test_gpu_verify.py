@@ -235,17 +235,19 @@ def test_empty_batch_and_workspace_left_clean():
     for _ in range(3):
         sv.spec_verify(logits, q, x, params, 7, workspace=ws)
     torch.cuda.synchronize()
-    # the header's counters (unit counter, exit counter, error bits, item
-    # counter), the per-row tickets (padded to 256 bytes) and the two tile
-    # counters per (row, position) (padded to 256 bytes) are back at zero;
-    # the epoch word at the end of the header counts the calls
+    # three calls, numbered 0, 1, 2 (tags 1, 2, 3): the last counted in set
+    # 0, and set 1, the next call's, is zero, as are the per-row tickets
+    # (padded to 256 bytes) and the two tile counters per (row, position)
+    # (padded to 256 bytes); the epoch word holds the last call's tag
     B, U = 5, 5 * 4
     tickets = 256
     counters = tickets + 256 * ((B * 4 + 255) // 256)
     records = counters + 256 * ((U * 8 + 255) // 256)
-    assert int(ws[:12].count_nonzero()) == 0 and int(ws[16:20].count_nonzero()) == 0
+    assert int(ws[24:28].view(torch.int32).item()) == 0
+    assert int(ws[64:96].count_nonzero()) == 0
     assert int(ws[tickets:records].count_nonzero()) == 0
     assert int(ws[236:240].view(torch.int32).item()) == 3
+    assert int(ws[0:8].view(torch.int64).item()) == 3 * torch.cuda.get_device_properties(0).multi_processor_count
     # dirty records behind them do not matter: every record word carries the
     # call's tag, so results stay identical
     ref = sv.spec_verify(logits, q, x, params, 7, workspace=ws)
@@ -304,6 +306,15 @@ def test_row_base_split_equals_whole_batch():
     compare(whole, run_oracle(inp, seed=19), "whole")
 
 
+def _last_call_errors(ws):
+    """The error bits of the last call: its counter set (bytes 24..27) picks
+    the word (bytes 52..55 for set 0, 84..87 for set 1)."""
+    cs = int(ws[24:28].view(torch.int32).item())
+    assert cs in (0, 1)
+    off = 52 + 32 * cs
+    return int(ws[off:off + 4].view(torch.int32).item())
+
+
 def test_timed_out_wait_flags_the_row_and_leaves_the_context_usable():
     from speculative_decoding_verify_07_gb300 import binding as sv
     case = _random_case(np.random.default_rng(31), B=4, k=2, V=4096, dtype="bf16", param_mode="mix")
@@ -314,7 +325,7 @@ def test_timed_out_wait_flags_the_row_and_leaves_the_context_usable():
     torch.cuda.synchronize()
     assert out["flags"][0] & sv.F_TIMEOUT and out["accept_len"][0] == 0
     assert np.all(out["tokens"][0] == -1)
-    assert int(ws[24:28].view(torch.int32).item()) & 4       # the record-wait bit of the last call
+    assert _last_call_errors(ws) & 4       # the record-wait bit of the last call
     orc = run_oracle(case, rows=[1, 2, 3])
     compare(out, orc, "rows after the timeout")
     # the same workspace, hook cleared: every row comes back normally
@@ -322,7 +333,7 @@ def test_timed_out_wait_flags_the_row_and_leaves_the_context_usable():
     again = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
     torch.cuda.synchronize()
     compare(again, run_oracle(case), "after the timeout")
-    assert int(ws[24:28].view(torch.int32).item()) == 0
+    assert _last_call_errors(ws) == 0
 
 
 def test_grid_barrier_that_gives_up_flags_the_top_p_rows():
@@ -337,7 +348,7 @@ def test_grid_barrier_that_gives_up_flags_the_top_p_rows():
     for r in topp:
         assert out["flags"][r] & sv.F_TIMEOUT and out["accept_len"][r] == 0
         assert np.all(out["tokens"][r] == -1)
-    assert int(ws[24:28].view(torch.int32).item()) & 16       # the barrier bit of the last call
+    assert _last_call_errors(ws) & 16       # the barrier bit of the last call
     others = [r for r in range(8) if r not in topp]
     compare(out, run_oracle(case, rows=others), "rows outside the top-p passes")
     # hook cleared: every row comes back normally and no wait gave up
@@ -345,7 +356,7 @@ def test_grid_barrier_that_gives_up_flags_the_top_p_rows():
     again = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
     torch.cuda.synchronize()
     compare(again, run_oracle(case), "after the barrier timeout")
-    assert int(ws[24:28].view(torch.int32).item()) == 0
+    assert _last_call_errors(ws) == 0
 
 
 def test_gpu_distribution_preserved_40k_rows():
