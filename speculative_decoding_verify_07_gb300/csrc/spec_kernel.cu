@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "spec_common.cuh"
@@ -282,19 +283,18 @@ __device__ __forceinline__ uint32_t seg_items(const Seg& s) {
 // a queue until `b_delay` items have been placed after the wave's A tiles
 // (the wave's settles finish meanwhile) and are then inserted at the next
 // row boundary; waves still waiting at the end come last.
-__device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
-                                            int NTB, uint32_t b_delay) {
-  if (threadIdx.x != 0) return;
+// `rw0` = max(1, b_delay / (items of one row's A tiles)), from the host.
+__device__ __forceinline__ void build_segments(const Args& A, VShm& S, int nD, int nT, int nX, int nG, int NTA,
+                                               int NTB, uint32_t b_delay, int rw0) {
   const int k = A.k, k1 = A.k + 1;
   Seg* sg = S.seg;
   int n = 0;
-  uint32_t pos = 0;   // items placed so far
+  uint32_t pos = 0;     // items placed so far
+  uint32_t tasks = 0;   // settle tasks placed so far
   int nw = 0, Rw = 1;
   if (nD > 0) {
     // a wave's A tiles are about b_delay items; waves of equal size
-    const uint32_t row_items = (uint32_t)k1 * (uint32_t)NTA;
-    Rw = (int)max(1u, b_delay / max(1u, row_items));
-    Rw = max(Rw, ceil_div(nD, kMaxWaves));
+    Rw = max(rw0, ceil_div(nD, kMaxWaves));
     nw = ceil_div(nD, Rw);
     Rw = ceil_div(nD, nw);
     nw = ceil_div(nD, Rw);
@@ -304,6 +304,8 @@ __device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int 
   auto place = [&](Seg sgm) {
     sgm.start = pos;
     pos += seg_items(sgm);
+    S.tstart[n] = tasks;
+    tasks += sgm.nrows * ((sgm.packed >> 21) & 31u);
     sg[n++] = sgm;
   };
   auto place_b = [&](int w) {
@@ -331,11 +333,6 @@ __device__ __noinline__ void build_segments(const Args& A, VShm& S, int nD, int 
   }
   place_rows((uint32_t)(nD + nT + nX), (uint32_t)nG, 0, k1);
   while (bh < bt) place_b(bh++);
-  uint32_t tasks = 0;
-  for (int i = 0; i < n; ++i) {
-    S.tstart[i] = tasks;
-    tasks += sg[i].nrows * ((sg[i].packed >> 21) & 31u);
-  }
   S.nseg = n;
   S.ntasks = tasks;
 }
@@ -1210,7 +1207,8 @@ __device__ __noinline__ void general_phase(const Args& A, Plan P, VShm& S, uint3
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A, uint32_t b_delay) {
+__global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_constant__ Args A, uint32_t b_delay,
+                                                                int rw0) {
   using G = Geo<kBF16>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
@@ -1248,7 +1246,7 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     if (threadIdx.x == 0)
       build_segments(A, S, S.ord.n_class[UT_DENSE], S.ord.n_class[UT_TOPK],
                      S.ord.n_class[UT_GENERAL] + S.ord.n_class[UT_TOPP], S.ord.n_class[UT_GREEDY],
-                     ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay);
+                     ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay, rw0);
     __syncthreads();
     P.order = S.order;
     P.cfg = S.cfg;
@@ -1281,7 +1279,8 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
     P.nX = (int)__ldcg(&A.ws->n_class[UT_GENERAL]);
     P.nP = (int)__ldcg(&A.ws->n_class[UT_TOPP]);
     // (general and top-p rows have no stream tiles; greedy rows follow them)
-    build_segments(A, S, P.nD, P.nT, P.nX + P.nP, P.nG, ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay);
+    if (threadIdx.x == 0)
+      build_segments(A, S, P.nD, P.nT, P.nX + P.nP, P.nG, ceil_div(A.V, G::EA), ceil_div(A.V, G::EB), b_delay, rw0);
     __syncthreads();
   }
   const uint32_t tag = S.tag;
@@ -1379,6 +1378,9 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   A.settle_stride = n / A.n_settle;
   A.global_order = A.B > kOrderSmem ? 1 : 0;
   uint32_t b_delay = kBDelayItems;
+  // rows of unfiltered units per wave, before the bound on the wave count
+  const uint32_t row_items = (uint32_t)(A.k + 1) * (uint32_t)ceil_div(A.V, Geo<kBF16>::EA);
+  const int rw0 = (int)std::max(1u, b_delay / std::max(1u, row_items));
   // cooperative launch: every CTA is resident, so every wait between warps ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -1391,7 +1393,7 @@ int launch_verify(const Args& A0, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, A, b_delay) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, A, b_delay, rw0) != cudaSuccess) {
     cudaGetLastError();
     return SPEC_E_CUDA;
   }
