@@ -434,7 +434,9 @@ __device__ __forceinline__ void enqueue_done(const Args& A, int row, int acc_len
   }
 }
 
-static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_t tag) {
+// w[] holds words 0..6 of unit `lane` of the row as loaded before the
+// row's ticket was taken; they are used if they all carry the tag already.
+static __device__ __forceinline__ void finalize_row(const Args& A, int row, uint32_t tag, const u64 (&w0)[7]) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int k = A.k;
@@ -443,15 +445,15 @@ static __device__ __noinline__ void finalize_row(const Args& A, int row, uint32_
   const uint32_t want = (row == 0 && (__ldcg(&A.ws->inject) & 1u) != 0u) ? (tag ^ 0x80000000u) : tag;
   u64 w[7];
 #pragma unroll
-  for (int i = 0; i < 7; ++i) w[i] = 0ull;
+  for (int i = 0; i < 7; ++i) w[i] = w0[i];
   long long spins = 0;
   bool timed_out = false;
-  while (true) {
+  for (bool first = true;; first = false) {
     bool ok = true;
     if (lane <= k) {
 #pragma unroll
       for (int i = 0; i < 7; ++i) {
-        w[i] = __ldcg(R + i);
+        if (!first) w[i] = __ldcg(R + i);
         ok = ok && tag_ok(w[i], want);
       }
     }
@@ -523,11 +525,17 @@ static __device__ __noinline__ void commit_record(const Args& A, uint32_t tag, i
                                 __shfl_sync(full, __float_as_uint(rec.lp_y), 0), __shfl_sync(full, rec.draw_flags, 0),
                                 0u);
   if (lane < kURecWords) __stcg(A.urec + (size_t)u * kURecWords + lane, tagw(tag, v));
+  // the row's records, in flight with the ticket: the last unit usually
+  // finds the others' already written and finalizes without another load
+  u64 w[7];
+  const int ul = row * (A.k + 1) + (lane <= A.k ? lane : 0);
+#pragma unroll
+  for (int i = 0; i < 7; ++i) w[i] = __ldcg(A.urec + (size_t)ul * kURecWords + i);
   uint32_t old = 0u;
   if (lane == 0) old = atomicAdd(&A.row_ticket[row], 1u);
   old = __shfl_sync(full, old, 0);
   if (old == (uint32_t)A.k) {
-    finalize_row(A, row, tag);
+    finalize_row(A, row, tag, w);
     if (lane == 0) TL(TL_FINAL, row, 1024);
     if (lane == 0) A.row_ticket[row] = 0;   // leave the workspace clean for the next call
   }
