@@ -968,7 +968,12 @@ template <bool kBF16>
 __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint32_t tag, uint32_t gw, uint32_t nwg,
                                             bool failed) {
   const int lane = threadIdx.x & 31;
-  for (int j = (int)gw; j < T.nU; j += (int)nwg) {
+  // unit j on CTA j mod n_ctas, warp j / n_ctas: consecutive units on
+  // different SMs, so that the settles (one warp's latency-bound code each)
+  // do not share an SM's schedulers while others sit idle
+  const uint32_t wpc = blockDim.x >> 5;
+  const uint32_t jfirst = (gw % wpc) * (uint32_t)A.n_ctas + gw / wpc;
+  for (int j = (int)jfirst; j < T.nU; j += (int)nwg) {
     const TpUnit U = tp_unit(A, T, j);
     if (failed) {
       commit_record(A, tag, U.uid, U.row, empty_record(SPEC_F_TIMEOUT));
