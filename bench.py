@@ -505,24 +505,44 @@ def run_ours(args):
     e2e_steps = max(3, min(n, 10))
     h2d = sum(t.numel() * t.element_size() for t in h_sets[0][:4])
     d2h = sum(t.numel() * t.element_size() for t in d_out.values())
-    dl, dq, dx, dp = (torch.empty_like(t) for t in sets[0][:4])
+    # two device input sets: step i+1's inputs cross on a copy stream while
+    # step i is verified (the host-to-device link, about 200 GB/s on this
+    # machine, is the bound; the verify hides behind it)
+    dev_in = [tuple(torch.empty_like(t) for t in sets[0][:4]) for _ in range(2)]
+    cstream = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
-        hl, hq, hx, hp, seed = h_sets[i % N_SETS]
-        dl.copy_(hl, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
-        dx.copy_(hx, non_blocking=True)
-        dp.copy_(hp, non_blocking=True)
-        sv.spec_verify(dl, dq, dx, dp, seed, out=out, workspace=ws, row_base=row_lo)
-        for k_, t in d_out.items():
-            t.copy_(getattr(out, k_), non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    def e2e_h2d(i):
+        hl, hq, hx, hp, _ = h_sets[i % N_SETS]
+        b = i % 2
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(free[b])
+            for dst, src in zip(dev_in[b], (hl, hq, hx, hp)):
+                dst.copy_(src, non_blocking=True)
+            ready[b].record(cstream)
 
-    e2e_step(0)
+    def e2e_run(steps):
+        cur = torch.cuda.current_stream()
+        for b in range(2):
+            free[b].record(cur)
+        e2e_h2d(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                e2e_h2d(i + 1)
+            b = i % 2
+            cur.wait_event(ready[b])
+            dl, dq, dx, dp = dev_in[b]
+            sv.spec_verify(dl, dq, dx, dp, h_sets[i % N_SETS][4], out=out, workspace=ws, row_base=row_lo)
+            free[b].record(cur)
+            for k_, t in d_out.items():
+                t.copy_(getattr(out, k_), non_blocking=True)
+            cur.synchronize()   # the step's results are on the host
+
+    e2e_run(2)
     barrier(world)
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
+    e2e_run(e2e_steps)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
 
     if rank != 0:
