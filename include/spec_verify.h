@@ -100,9 +100,10 @@ enum {
  * tickets and per-(row, position) tile counters to zero as they finish.
  * Every record behind them carries the tag of the call that wrote it (its
  * number + 1, never 0), so stale or foreign contents are never read as this
- * call's.  One workspace serves any number of later calls on one stream
- * (re-zero it once every 2^32 - 1 calls, when the tag comes round again);
- * two calls that may run concurrently need two workspaces.
+ * call's.  One workspace serves any number of later calls of the same B, k
+ * and V on one stream (re-zero it once every 2^32 - 1 calls, when the tag
+ * comes round again, and before a call of another shape, whose counters lie
+ * elsewhere); two calls that may run concurrently need two workspaces.
  * Words of the 256-byte header for diagnosis and testing:
  *   bytes 20..23  must stay 0.  They exist to test the waits that give up:
  *                 bit 0 makes the finalize of row 0 wait for records that

@@ -262,6 +262,30 @@ def test_empty_batch_and_workspace_left_clean():
     assert out.tokens.shape == (0, 3)
 
 
+def test_one_workspace_through_calls_of_every_row_class():
+    # consecutive calls on one workspace alternate between the two sets of
+    # call counters: every call, whatever rows it holds (the top-p passes use
+    # the grid barrier count and refinement flags, large top-k rows the
+    # general-path counter), starts from a zeroed set and leaves the next
+    # one zeroed
+    from speculative_decoding_verify_07_gb300 import binding as sv
+    rng = np.random.default_rng(2024)
+    B, k, V = 24, 2, 20000
+    ws = sv.new_workspace(B, k, V, "cuda")
+    for i, mode in enumerate(["mix", "topp", "greedy", "bigk", "mix", "topp", "both"]):
+        case = _random_case(rng, B=B, k=k, V=V, dtype="bf16", param_mode=mode)
+        logits, q, x, params = to_device(case)
+        out = host_outputs(sv.spec_verify(logits, q, x, params, case.seed, workspace=ws))
+        torch.cuda.synchronize()
+        compare(out, run_oracle(case), f"call {i} ({mode})")
+        assert _last_call_errors(ws) == 0
+        assert int(ws[236:240].view(torch.int32).item()) == i + 1
+        cs = int(ws[24:28].view(torch.int32).item())
+        assert cs == i % 2
+        nxt = 32 + 32 * (1 - cs)
+        assert int(ws[nxt:nxt + 32].count_nonzero()) == 0
+
+
 def test_deterministic_and_graph_replay_bit_identical():
     from speculative_decoding_verify_07_gb300 import binding as sv
     inp = synth.make_mixed(B=16, V=32768)
