@@ -34,9 +34,12 @@
 // (spec_topp.cuh, every warp of every CTA, grid barriers between passes);
 // rows with a top-k above the candidate-list limit are taken next by the
 // CTAs' first 256 threads (spec_general.cuh), and the fused commit
-// (spec_fused.cuh) follows.  Results pass between warps as 64-bit words tagged with the
-// call's epoch; reductions have a fixed order and no floating-point atomics
-// are used, so results are bit-reproducible.
+// (spec_fused.cuh) follows.  Each CTA numbers the call from a count of the
+// CTAs that entered earlier calls; results pass between warps as 64-bit
+// words tagged with the call's number, and the call counts in one of two
+// counter sets by its parity (zeroing the other for the next call), so no
+// CTA waits at the end to reset anything.  Reductions have a fixed order and
+// no floating-point atomics are used, so results are bit-reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
