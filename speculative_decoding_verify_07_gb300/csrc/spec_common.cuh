@@ -245,6 +245,7 @@ struct Args {
   int global_order;       // the row order lives in the workspace
   int vec_logits;
   int vec_q;
+  int l2_stage;           // the logits fit L2 with room to spare: top-p rows are staged there at entry
   u64* done;              // fused commit: finalized rows in order, tagged (row << 5 | accept_len)
   u64* tp;                // top-p passes: per-unit scratch (kTpStride words per top-p unit)
   u64* desc;              // draft sampling: per-unit kept-set descriptors (null: not written)

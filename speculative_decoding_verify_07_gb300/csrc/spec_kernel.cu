@@ -1216,6 +1216,28 @@ __global__ void __launch_bounds__(kAllThreads, 1) verify_kernel(const __grid_con
   extern __shared__ __align__(128) unsigned char smem_raw[];
   VShm& S = *reinterpret_cast<VShm*>(smem_raw);
   const int w = threadIdx.x >> 5;
+  if (threadIdx.x == kAllThreads - 64 && A.l2_stage) {
+    // Rows with top-p alone are read by every top-p pass, the first of which
+    // starts only after the roles and a grid barrier: their logits go into
+    // L2 now, in bulk prefetches of 64 KB, while the prologue and the roles
+    // run.  A CTA classifies one row (a few when rows outnumber CTAs), so
+    // the prologue does not wait on this thread; with more CTAs than rows, a
+    // row's pieces are split over gridDim.x / B CTAs.
+    const size_t row_bytes = (size_t)(A.k + 1) * (size_t)A.V * (size_t)G::es;
+    const unsigned char* lg = reinterpret_cast<const unsigned char*>(A.logits);
+    const int grid = (int)gridDim.x, cta = (int)blockIdx.x;
+    const int per = grid >= A.B ? grid / A.B : 1;   // CTAs per row
+    const int r0 = grid >= A.B ? (cta < per * A.B ? cta % A.B : A.B) : cta;
+    const int rstep = grid >= A.B ? A.B : grid;
+    const size_t o0 = grid >= A.B ? (size_t)(cta / A.B) * 65536 : 0;
+    for (int r = r0; r < A.B; r += rstep) {
+      if (classify(A.params[r], A.V).type != UT_TOPP) continue;
+      for (size_t o = o0; o < row_bytes; o += (size_t)per * 65536) {
+        const uint32_t n = (uint32_t)min((size_t)65536, row_bytes - o) & ~15u;
+        if (n) bulk_prefetch_l2(lg + (size_t)r * row_bytes + o, n);
+      }
+    }
+  }
   if (threadIdx.x == kAllThreads - 32) {
     // The call's number: the CTAs that entered earlier calls over the grid
     // size (calls on one workspace never overlap, and each launches the

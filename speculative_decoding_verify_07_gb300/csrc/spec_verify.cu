@@ -93,6 +93,7 @@ int verify_launch(const void* logits, int logits_dtype, const float* draft_probs
   A.NTA = max_nta(V);
   A.NTB = max_ntb(V);
   A.vec_logits = aligned(logits, 16) && ((size_t)V * es) % 16 == 0;
+  A.l2_stage = A.vec_logits && (size_t)B * (size_t)(k + 1) * (size_t)V * es <= ((size_t)64 << 20);
   A.vec_q = k > 0 && aligned(draft_probs, 16) && (V % 4) == 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
   return logits_dtype == SPEC_BF16 ? launch_verify<true>(A, st) : launch_verify<false>(A, st);
