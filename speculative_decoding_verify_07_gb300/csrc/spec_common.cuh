@@ -707,8 +707,12 @@ __device__ __forceinline__ void race_weights(const Args& A, size_t lrow, size_t 
 // Level 2: the race among the entries of block b, run by one warp (the
 // result is in every lane).  The group's two Philox blocks are computed
 // while its loads are in flight.  *ly (if given) receives the logit of the
-// winning entry.
-template <bool kBF16>
+// winning entry.  kInline runs race_consider's steps unrolled and inline:
+// the same race, without the latency of an out-of-line update per entry,
+// for a warp that runs it alone (the top-p settles, one unit an SM); where
+// settles share SMs and are throughput-bound, the rolled loop's smaller
+// code and out-of-line updates are faster.
+template <bool kBF16, bool kInline = false>
 __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint32_t b, float m, float c, float invZ,
                                            int mode, const Thresh* th, float* ly = nullptr) {
   const int lane = threadIdx.x & 31;
@@ -735,19 +739,32 @@ __device__ __noinline__ Race race_in_block(const Args& A, int row, int pos, uint
     const uint4 p1 = philox4x32_10(make_uint4(blk + 1u, cp, srow(A, row), A.race_stream), A.key0, A.key1);
     float w[8], tq[8];
     group_weights(A, g, v, qv, m, c, invZ, mode, th, w, tq);
-    // one race step per entry, in a rolled loop (small code)
-#pragma unroll 1
-    for (int j = 0; j < 8; ++j) {
-      float wj = w[0], tj = tq[0];
-      uint32_t pj = p0.x;
+    if constexpr (kInline) {
+      // zero weights skip the score (its division would take the slow path)
 #pragma unroll
-      for (int t = 1; t < 8; ++t)
-        if (j == t) {
-          wj = w[t];
-          tj = tq[t];
-          pj = t < 4 ? word_of(p0, t) : word_of(p1, t - 4);
+      for (int j = 0; j < 8; ++j) {
+        const float om = one_minus_uniform_of(j < 4 ? word_of(p0, j) : word_of(p1, j - 4));
+        if (w[j] > 0.f && w[j] >= r.s1lo * om) {
+          float sj, uj;
+          race_score(w[j], tq[j], om, sj, uj);
+          race_apply(r, sj, uj, (uint32_t)(g * 8 + j));
         }
-      if (wj > 0.f) race_consider(r, wj, tj, (uint32_t)(g * 8 + j), pj);
+      }
+    } else {
+      // one race step per entry, in a rolled loop (small code)
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j) {
+        float wj = w[0], tj = tq[0];
+        uint32_t pj = p0.x;
+#pragma unroll
+        for (int t = 1; t < 8; ++t)
+          if (j == t) {
+            wj = w[t];
+            tj = tq[t];
+            pj = t < 4 ? word_of(p0, t) : word_of(p1, t - 4);
+          }
+        if (wj > 0.f) race_consider(r, wj, tj, (uint32_t)(g * 8 + j), pj);
+      }
     }
   }
   warp_race_merge(r);

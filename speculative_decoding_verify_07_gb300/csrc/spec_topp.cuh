@@ -1038,7 +1038,7 @@ __device__ __noinline__ void tp_settle_pass(const Args& A, const TpPlan& T, uint
         }
       }
       if (l1.s1 >= 0.f) {
-        const Race l2 = race_in_block<kBF16>(A, U.row, U.pos, l1.v1, m, c, invZ, mode, &th, &ly);
+        const Race l2 = race_in_block<kBF16, true>(A, U.row, U.pos, l1.v1, m, c, invZ, mode, &th, &ly);
         if (l2.s1 >= 0.f) y = l2.v1;
         if (draw_margin(l1) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
       }
