@@ -1160,15 +1160,18 @@ __device__ __noinline__ void settle_loop(const Args& A, Plan P, VShm& S, uint32_
     }
     ready = __shfl_sync(kFull, ready ? 1 : 0, 0) != 0;
     const RowCfg cfg = plan_cfg(A, P, k.row);
+    // the warp's last task: no settle follows it on this warp, and the SMs
+    // are emptying, so its draw takes the inline race (lower latency alone)
+    const bool late = t + nst >= S.ntasks;
     if (lane == 0) TL(k.kind == 2 ? TL_SB_START : TL_SA_START, k.u, 2048);
     if (!ready) {
       commit_record(A, tag, k.u, k.row, empty_record(SPEC_F_TIMEOUT));   // the records' polls would give up too
     } else if (k.kind == 2) {
-      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg, sw8);
+      fin_b<kBF16>(A, tag, k.u, k.row, k.pos, cfg, sw8, late);
     } else if (cfg.type == UT_TOPK) {
       topk_settle<kBF16>(A, tag, TS, k.u, k.row, k.pos, cfg, pr);
     } else {
-      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg, pr);
+      fin_stats<kBF16>(A, tag, k.u, k.row, k.pos, cfg, pr, late);
     }
     if (lane == 0) {
       TL(k.kind == 2 ? TL_SB_END : TL_SA_END, k.u, 2048);

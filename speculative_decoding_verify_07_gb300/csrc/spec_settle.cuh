@@ -160,7 +160,7 @@ __device__ __noinline__ uint32_t warp_draw_p(const Args& A, int row, int pos, fl
 // later (fin_b).
 template <bool kBF16>
 __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int row, int pos, RowCfg cfg,
-                                       Pre pr) {
+                                       Pre pr, bool late) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   const bool has_q = pos < A.k;
@@ -333,7 +333,8 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
     warp_race_merge(a);
     TLP(u, 2);
     float ly = 0.f;
-    const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
+    const Race l2 = late ? race_in_block<kBF16, true>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly)
+                         : race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
     TLP(u, 3);
     uint32_t y = l2.v1;
     const bool drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
@@ -401,7 +402,7 @@ __device__ __forceinline__ UnitState state_of(const u64 (&w)[kStateWords]) {
 // read without a wait.
 template <bool kBF16>
 __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, int pos, RowCfg cfg,
-                                   StateWords sw0) {
+                                   StateWords sw0, bool late) {
   using G = Geo<kBF16>;
   const int lane = threadIdx.x & 31;
   u64 sw[kStateWords];
@@ -486,7 +487,8 @@ __device__ __noinline__ void fin_b(const Args& A, uint32_t tag, int u, int row, 
   if (need_race) {
     warp_race_merge(a);
     if (a.s1 >= 0.f) {
-      const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr, &ly);
+      const Race l2 = late ? race_in_block<kBF16, true>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr, &ly)
+                           : race_in_block<kBF16>(A, row, pos, a.v1, st.m, cfg.c, st.invZ, RW_RESIDUAL, nullptr, &ly);
       y = l2.v1;
       drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
       if (draw_margin(a) || draw_margin(l2)) draw_flags |= SPEC_F_MARGIN_DRAW;
