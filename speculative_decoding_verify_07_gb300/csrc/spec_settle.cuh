@@ -333,8 +333,9 @@ __device__ __noinline__ void fin_stats(const Args& A, uint32_t tag, int u, int r
     warp_race_merge(a);
     TLP(u, 2);
     float ly = 0.f;
-    const Race l2 = late ? race_in_block<kBF16, true>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly)
-                         : race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
+    // (every entry of the block weighs: the rolled loop's out-of-line
+    // updates beat the inline steps here even for a warp's last task)
+    const Race l2 = race_in_block<kBF16>(A, row, pos, a.v1, m, cfg.c, 1.f, RW_BONUS, nullptr, &ly);
     TLP(u, 3);
     uint32_t y = l2.v1;
     const bool drawn = l2.s1 >= 0.f && y < (uint32_t)A.V;
