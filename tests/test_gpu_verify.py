@@ -262,6 +262,17 @@ def test_empty_batch_and_workspace_left_clean():
     assert out.tokens.shape == (0, 3)
 
 
+def test_parity_many_units_several_settle_rounds():
+    # 96 rows at k = 4: more settle tasks than settle warps, so warps take
+    # several tasks (the earlier ones draw with the rolled race, the last
+    # with the inline one) and the unfiltered rows come in several waves
+    rng = np.random.default_rng(8080)
+    case = _random_case(rng, B=96, k=4, V=12289, dtype="bf16", param_mode="mix")
+    compare(run_gpu(case), run_oracle(case), "96 rows k=4")
+    case = _random_case(rng, B=96, k=4, V=12289, dtype="bf16", param_mode="temp")
+    compare(run_gpu(case), run_oracle(case), "96 unfiltered rows k=4")
+
+
 def test_one_workspace_through_calls_of_every_row_class():
     # consecutive calls on one workspace alternate between the two sets of
     # call counters: every call, whatever rows it holds (the top-p passes use
