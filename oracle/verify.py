@@ -323,10 +323,10 @@ def verify(logits: np.ndarray, q: np.ndarray, drafts: np.ndarray,
     arrays are indexed like `rows`.
 
     Row r of this batch draws its random numbers as row `row_base + r` of the
-    stream keyed by (seed, row, position).  READING: the benchmark spec keys the
-    stream by the row; a batch split into blocks of rows (one block per GPU)
-    reproduces the whole batch's draws when every block passes the index of
-    its first row as row_base.  The stream row is a 32-bit counter word, so
+    stream keyed by (seed, row, position).  READING: the random stream is
+    keyed by the row's index in the whole batch, so a batch split into
+    blocks of rows (one block per GPU) reproduces the whole batch's draws
+    when every block passes the index of its first row as row_base.  The stream row is a 32-bit counter word, so
     row_base + r wraps modulo 2^32.
 
     Besides the outputs, the result holds each row's margin record: the
