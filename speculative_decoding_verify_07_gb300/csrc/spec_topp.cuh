@@ -1076,8 +1076,11 @@ constexpr unsigned long long kBarrierNs = 1000000000ull;
 __device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&cur(A).bar, 1u);
+    // a release add (ordering the CTA's writes, which the block barrier
+    // made this thread's to release, before the arrival) and acquire loads
+    // (ordering everything after the wait, which the block barrier below
+    // passes on to the CTA's other threads)
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&cur(A).bar) : "memory");
     const unsigned long long t0 = global_ns();
     long long spins = 0;
     while (load_acquire(&cur(A).bar) < target) {
@@ -1087,7 +1090,6 @@ __device__ __noinline__ void grid_barrier(const Args& A, uint32_t target) {
       }
       __nanosleep(spins > 16 ? 128 : 16);
     }
-    __threadfence();
   }
   __syncthreads();
 }
